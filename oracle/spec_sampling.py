@@ -1,0 +1,253 @@
+"""fp64 CPU oracle of the speculative-sampling verification step.
+
+TEST INFRASTRUCTURE ONLY. The test suite, the smoke check and the benchmark's
+CPU-baseline leg are the only callers; the CUDA library neither imports nor
+calls anything here, and this module shares no code with it.
+
+What it computes, step by step, in the order and notation of
+"Accelerating Large Language Model Decoding with Speculative Sampling"
+(Chen et al., DeepMind), as summarised by its wikillm.com paper card:
+
+* q(.|...) and p(.|...) are the target and draft distributions. The decoding
+  transform (temperature) is applied to both before anything else
+  (card, §4.2 "Decoding transforms"; Pitfalls, "Use the same transformed
+  distributions everywhere").
+* Draft token x~_t is accepted while r_t < min(1, q(x~_t)/p(x~_t)), left to
+  right, the ratio evaluated at the drafted token (card, §4.2 "Modified
+  rejection sampling"; Algorithm 2 step 3; Pitfalls, "Indexing in alg. 2").
+* At the first rejection a replacement is drawn from the normalised residual
+  (q - p)_+ = max(0, q - p) / sum max(0, q - p), and the loop stops
+  (card, §4.2).
+* If all K drafts are accepted, one bonus token is drawn from the (K+1)-th
+  target distribution (card, Algorithm 2 step 4; Pitfalls, "Bonus-token typo").
+* Each loop therefore emits between 1 and K+1 tokens (card, §4.2).
+
+Readings taken where the pages leave a step open (each also listed in the
+design notes):
+
+* U1 uniform slots: u[:, t] (t < K) drives the acceptance test of x~_t,
+  u[:, K] drives the residual draw, u[:, K+1] the bonus draw.
+* U2 the acceptance test is strict, `u < min(1, q/p)`, as printed.
+* U3 a categorical draw from weights w with uniform u is the inverse CDF over
+  ascending token id: the smallest i with C_i > u * S, C_i = w_0 + ... + w_i
+  summed in that order, S = C_{V-1}. If rounding (or u = 1) leaves no such i,
+  the largest i with w_i > 0 is taken.
+* U4 p(x~) = 0 with q(x~) > 0 accepts (the limit of min(1, q/p)); q(x~) = 0
+  rejects.
+* U5 zero residual (sum max(0, q - p) == 0): fall back to q itself, drawn with
+  u[:, K] (the card's Pitfalls suggest the fallback; the paper is silent).
+* U6 temperature: q = softmax(l / T) with T > 0 finite; T is given in fp32 and
+  widened exactly.
+* U8 n_accepted counts accepted drafts (0..K); out_tokens holds them, then the
+  sampled token, then -1 padding (U9).
+* U12 -inf logits are masked entries (probability 0). A sequence any of whose
+  2K+1 rows holds NaN or +inf, or is entirely -inf, any of whose draft tokens
+  lies outside [0, V), or any of whose K+2 uniforms is NaN or outside [0, 1],
+  fails: all its outputs are -1 and its status word says why.
+
+Inputs are widened exactly to fp64 (bf16 and fp32 both embed exactly). Every
+decision also reports its margin, the distance of the uniform from the fp64
+threshold it was compared with, so a caller can tell a genuine disagreement
+from a decision that sits on a rounding boundary.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+STATUS_OK = 0
+STATUS_TOKEN_RANGE = 16
+STATUS_NONFINITE = 32
+STATUS_EMPTY_ROW = 64
+STATUS_UNIFORM_RANGE = 128
+
+
+@dataclass
+class OracleResult:
+    out_tokens: np.ndarray       # [B, K+1] int64, -1 padded
+    n_accepted: np.ndarray       # [B] int64, -1 for failed sequences
+    status: np.ndarray           # [B] int64 status bits (0 = ok)
+    thresholds: np.ndarray       # [B, K] fp64 min(1, q/p) at the drafted tokens
+    accept_margin: np.ndarray    # [B, K] |u_t - thr_t| for decisions taken, NaN after
+    sample_margin: np.ndarray    # [B] distance of u from the chosen CDF interval's ends
+    sample_prob: np.ndarray      # [B] normalised weight of the sampled token
+    residual_fallback: np.ndarray  # [B] bool, zero-residual fallback to q was used
+    lse: np.ndarray              # [B, 2K+1] log-sum-exp of l/T: target rows 0..K, then draft rows 0..K-1
+
+    def decisions(self) -> int:
+        """Number of decisions taken (acceptance tests plus one draw per ok sequence)."""
+        ok = self.status == 0
+        return int(np.sum(np.isfinite(self.accept_margin[ok])) + np.sum(ok))
+
+
+def temperature_softmax(logits: np.ndarray, temperature: float):
+    """softmax(l / T) over the last axis, in fp64.
+
+    The temperature transform of the card's §4.2 "Decoding transforms",
+    applied identically to target and draft rows. Returns (probs, lse, status)
+    with lse = log sum_i exp(l_i / T) and per-row status bits (NaN / +inf
+    entries, or a row with every entry -inf).
+    """
+    z = logits / np.float64(temperature)
+    nonfinite = np.isnan(z).any(axis=-1) | np.isposinf(z).any(axis=-1)
+    with np.errstate(invalid="ignore"):
+        m = np.max(z, axis=-1)
+    empty = ~nonfinite & np.isneginf(m)
+    bad = nonfinite | empty
+    m_safe = np.where(bad, 0.0, m)
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        e = np.exp(z - m_safe[..., None])
+        e = np.where(bad[..., None], 0.0, e)
+        s = np.sum(e, axis=-1)
+        s_safe = np.where(bad, 1.0, s)
+        probs = e / s_safe[..., None]
+        lse = np.where(bad, np.nan, m_safe + np.log(s_safe))
+    status = np.where(nonfinite, STATUS_NONFINITE, 0) | np.where(empty, STATUS_EMPTY_ROW, 0)
+    return probs, lse, status.astype(np.int64)
+
+
+def acceptance_thresholds(q_at: np.ndarray, p_at: np.ndarray) -> np.ndarray:
+    """min(1, q(x~)/p(x~)) at the drafted tokens (card, §4.2), with U4's limits."""
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = q_at / np.where(p_at > 0, p_at, 1.0)
+    return np.where(p_at > 0, np.minimum(1.0, ratio), np.where(q_at > 0, 1.0, 0.0))
+
+
+def first_rejection(u_acc: np.ndarray, thr: np.ndarray) -> np.ndarray:
+    """Index of the first draft whose test `u < thr` fails, or K if none fails.
+
+    Algorithm 2 step 3 scans t = 1..K left to right and stops at the first
+    rejection; a separate count keeps the accepted length (card, Pitfalls).
+    """
+    accept = u_acc < thr
+    K = accept.shape[1]
+    return np.where(accept.all(axis=1), K, np.argmin(accept, axis=1)).astype(np.int64)
+
+
+def residual_weights(q_row: np.ndarray, p_row: np.ndarray):
+    """max(0, q - p) per token (card, §4.2); rows whose residual sums to zero
+    fall back to q (U5). Returns (weights, fallback flags)."""
+    w = np.maximum(0.0, q_row - p_row)
+    fallback = ~(w > 0).any(axis=-1)
+    w = np.where(fallback[..., None], q_row, w)
+    return w, fallback
+
+
+def inverse_cdf(w: np.ndarray, u: np.ndarray):
+    """Draw one index per row from weights w (unnormalised) with uniform u (U3).
+
+    Returns (index, margin, normalised weight of the index). The margin is
+    the distance of u from the nearer end of the chosen index's interval
+    [C_{i-1}/S, C_i/S) of the normalised CDF (0 when the fallback was taken).
+    """
+    B, V = w.shape
+    C = np.cumsum(w, axis=-1)
+    S = C[:, -1]
+    target = u * S
+    above = C > target[:, None]
+    found = above.any(axis=-1)
+    first = np.argmax(above, axis=-1)
+    last_pos = V - 1 - np.argmax((w > 0)[:, ::-1], axis=-1)
+    idx = np.where(found, first, last_pos)
+    rows = np.arange(B)
+    with np.errstate(invalid="ignore", divide="ignore"):   # S == 0 only on failed rows
+        lo = np.where(idx > 0, C[rows, np.maximum(idx - 1, 0)], 0.0) / S
+        hi = C[rows, idx] / S
+        margin = np.where(found, np.minimum(u - lo, hi - u), 0.0)
+        prob = w[rows, idx] / S
+    return idx.astype(np.int64), margin, prob
+
+
+def verify(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
+           uniforms: np.ndarray, temperature: float) -> OracleResult:
+    """One verification step for a batch: target [B,K+1,V], draft [B,K,V]
+    (fp64, widened exactly from the input dtype), tokens [B,K] ints,
+    uniforms [B,K+2], temperature > 0."""
+    target = np.asarray(target, dtype=np.float64)
+    draft = np.asarray(draft, dtype=np.float64)
+    tokens = np.asarray(tokens).astype(np.int64)
+    uniforms = np.asarray(uniforms, dtype=np.float64)
+    B, K1, V = target.shape
+    K = K1 - 1
+    if K < 1 or draft.shape != (B, K, V) or tokens.shape != (B, K) or uniforms.shape != (B, K + 2):
+        raise ValueError("shape mismatch")
+    T = float(np.float64(temperature))
+    if not (np.isfinite(T) and T > 0):
+        raise ValueError("temperature must be finite and > 0")
+
+    # Temperature transform of both distributions, every row.
+    q, lse_q, st_q = temperature_softmax(target, T)      # [B, K+1, V]
+    p, lse_p, st_p = temperature_softmax(draft, T)       # [B, K, V]
+    status = np.bitwise_or.reduce(st_q, axis=1) | np.bitwise_or.reduce(st_p, axis=1)
+    tok_ok = ((tokens >= 0) & (tokens < V)).all(axis=1)
+    status |= np.where(tok_ok, 0, STATUS_TOKEN_RANGE)
+    u_ok = ((uniforms >= 0) & (uniforms <= 1)).all(axis=1)   # NaN compares false
+    status |= np.where(u_ok, 0, STATUS_UNIFORM_RANGE)
+
+    # Acceptance thresholds at the drafted tokens, and the left-to-right scan.
+    tok = np.where((tokens >= 0) & (tokens < V), tokens, 0)
+    q_at = np.take_along_axis(q[:, :K, :], tok[..., None], axis=-1)[..., 0]
+    p_at = np.take_along_axis(p, tok[..., None], axis=-1)[..., 0]
+    thr = acceptance_thresholds(q_at, p_at)
+    u_acc = uniforms[:, :K]
+    j = first_rejection(u_acc, thr)
+    taken = np.arange(K)[None, :] <= j[:, None]
+    accept_margin = np.where(taken, np.abs(u_acc - thr), np.nan)
+
+    # The one draw per sequence: residual at row j, or bonus from target row K.
+    rows = np.arange(B)
+    residual = j < K
+    q_row = q[rows, j]
+    p_row = p[rows, np.minimum(j, K - 1)]
+    w_res, fallback = residual_weights(q_row, p_row)
+    w = np.where(residual[:, None], w_res, q_row)
+    u_draw = np.where(residual, uniforms[:, K], uniforms[:, K + 1])
+    idx, sample_margin, sample_prob = inverse_cdf(w, u_draw)
+
+    out = np.full((B, K + 1), -1, dtype=np.int64)
+    for b in range(B):
+        out[b, : j[b]] = tokens[b, : j[b]]
+        out[b, j[b]] = idx[b]
+    n_acc = j.copy()
+
+    failed = status != 0
+    out[failed] = -1
+    n_acc[failed] = -1
+    thr = np.where(failed[:, None], np.nan, thr)
+    accept_margin = np.where(failed[:, None], np.nan, accept_margin)
+    sample_margin = np.where(failed, np.nan, sample_margin)
+    sample_prob = np.where(failed, np.nan, sample_prob)
+    fallback = residual & fallback & ~failed
+    lse = np.concatenate([lse_q, lse_p], axis=1)
+    return OracleResult(out, n_acc, status, thr, accept_margin, sample_margin, sample_prob,
+                        fallback, lse)
+
+
+def _widen(x) -> np.ndarray:
+    """Exact widening of a torch tensor (bf16 / fp32 / int) or array to numpy fp64."""
+    if hasattr(x, "detach"):
+        import torch  # local: the oracle itself needs only numpy
+
+        x = x.detach().cpu()
+        if x.dtype in (torch.bfloat16, torch.float16, torch.float32, torch.float64):
+            return x.to(torch.float64).numpy()
+        return x.numpy()
+    return np.asarray(x)
+
+
+def verify_inputs(inputs: dict, chunk: int = 8) -> OracleResult:
+    """`verify` over an input dict from the synthetic generator, `chunk`
+    sequences at a time to bound memory; results are concatenated."""
+    B = inputs["target"].shape[0]
+    parts = []
+    for s in range(0, B, chunk):
+        e = min(B, s + chunk)
+        parts.append(verify(_widen(inputs["target"][s:e]), _widen(inputs["draft"][s:e]),
+                            _widen(inputs["tokens"][s:e]), _widen(inputs["uniforms"][s:e]),
+                            inputs["temperature"]))
+    if len(parts) == 1:
+        return parts[0]
+    return OracleResult(*[np.concatenate([getattr(p, f) for p in parts], axis=0)
+                          for f in OracleResult.__dataclass_fields__])

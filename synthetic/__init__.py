@@ -1,0 +1,22 @@
+"""Seeded synthetic inputs for the speculative-sampling verification step.
+
+This package only draws random numbers in the shapes and distributions of the
+workloads; it holds none of the verification arithmetic (no normalisation, no
+acceptance ratio, no residual). Both the fp64 oracle and the CUDA library are
+fed from here, and neither imports the other.
+"""
+
+from .configs import WORKLOADS, SWEEP_K, SWEEP_NOISE, Workload, sweep_workload, get_workload
+from .generate import make_inputs, make_sequence, DTYPES
+
+__all__ = [
+    "WORKLOADS",
+    "SWEEP_K",
+    "SWEEP_NOISE",
+    "Workload",
+    "sweep_workload",
+    "get_workload",
+    "make_inputs",
+    "make_sequence",
+    "DTYPES",
+]

@@ -1,0 +1,102 @@
+"""Seeded generator of verification inputs (CPU, torch).
+
+Recipe per sequence b of step s (each sequence has its own seeds, so any subset
+of a batch can be regenerated on its own):
+
+* target logits: fp32 normals N(0, target_std^2) for the K+1 target rows; when
+  the workload asks for peaks, `peaks` distinct random ids per target row get
+  `+peak_boost`;
+* draft logits: draft row t = target row t (peaks included) + N(0, noise^2),
+  t < K (the draft row conditions on the same prefix as target row t);
+* both are then rounded to the workload dtype (bf16 rounds to nearest even);
+* draft tokens: x_t = argmax_i(dl[t,i]/T + G_i), G_i standard Gumbel noise in
+  fp64 drawn from a second stream (the Gumbel-max trick, an exact draw from
+  softmax(dl[t]/T) that evaluates no softmax); this follows the pages'
+  requirement that drafts come from the transformed p;
+* uniforms: K+2 fp32 draws in [0, 1) from a third stream.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from .configs import Workload
+
+DTYPES = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+_MASK64 = (1 << 64) - 1
+
+
+def _mix(*parts: int) -> int:
+    """Deterministic 63-bit seed from integers (splitmix64 finaliser over a sum)."""
+    x = 0x243F6A8885A308D3
+    for p in parts:
+        x = (x + (p & _MASK64) * 0x9E3779B97F4A7C15 + 0x632BE59BD9B4E019) & _MASK64
+        x ^= x >> 30
+        x = (x * 0xBF58476D1CE4E5B9) & _MASK64
+        x ^= x >> 27
+        x = (x * 0x94D049BB133111EB) & _MASK64
+        x ^= x >> 31
+    return x & ((1 << 63) - 1)
+
+
+def _gen(w: Workload, step: int, b: int, stream: int) -> torch.Generator:
+    return torch.Generator().manual_seed(_mix(w.seed, step, b, stream))
+
+
+def gumbel_max_draw(rows: torch.Tensor, temperature: float, g: torch.Generator) -> torch.Tensor:
+    """One index per row of `rows` [n, V], distributed as softmax(rows / T):
+    argmax_i(rows_i / T + G_i) with G_i = -log(-log U_i), U_i uniform (fp64)."""
+    u = torch.rand(rows.shape, dtype=torch.float64, generator=g)
+    gumbel = -torch.log(-torch.log(u))
+    return torch.argmax(rows.to(torch.float64) / float(temperature) + gumbel, dim=-1).to(torch.int32)
+
+
+def make_sequence(w: Workload, step: int, b: int):
+    """One sequence: (target [K+1,V], draft [K,V], tokens [K] int32, uniforms [K+2] f32)."""
+    dtype = DTYPES[w.dtype]
+    g = _gen(w, step, b, 0)
+    tl = torch.randn(w.K + 1, w.V, generator=g) * w.target_std
+    if w.peaks:
+        for r in range(w.K + 1):
+            ids = torch.randperm(w.V, generator=g)[: w.peaks]
+            tl[r, ids] += w.peak_boost
+    dl = tl[: w.K] + torch.randn(w.K, w.V, generator=g) * w.draft_noise_std
+    tl = tl.to(dtype)
+    dl = dl.to(dtype)
+
+    tokens = gumbel_max_draw(dl, w.temperature, _gen(w, step, b, 1))
+
+    g3 = _gen(w, step, b, 2)
+    uniforms = torch.rand(w.K + 2, generator=g3, dtype=torch.float32)
+    return tl, dl, tokens, uniforms
+
+
+def make_inputs(w: Workload, step: int = 0, seqs=None, pin_memory: bool = False):
+    """A batch of inputs for workload `w` at verify step `step`.
+
+    `seqs` (optional iterable of sequence indices) generates only those
+    sequences, in that order; by default all B. Returns a dict of CPU tensors:
+    target [n,K+1,V], draft [n,K,V], tokens [n,K] int32, uniforms [n,K+2] f32,
+    and the temperature as a Python float.
+    """
+    idx = list(range(w.B)) if seqs is None else list(seqs)
+    n = len(idx)
+    dtype = DTYPES[w.dtype]
+    target = torch.empty(n, w.K + 1, w.V, dtype=dtype, pin_memory=pin_memory)
+    draft = torch.empty(n, w.K, w.V, dtype=dtype, pin_memory=pin_memory)
+    tokens = torch.empty(n, w.K, dtype=torch.int32, pin_memory=pin_memory)
+    uniforms = torch.empty(n, w.K + 2, dtype=torch.float32, pin_memory=pin_memory)
+    for i, b in enumerate(idx):
+        tl, dl, tk, un = make_sequence(w, step, b)
+        target[i] = tl
+        draft[i] = dl
+        tokens[i] = tk
+        uniforms[i] = un
+    return {
+        "target": target,
+        "draft": draft,
+        "tokens": tokens,
+        "uniforms": uniforms,
+        "temperature": float(w.temperature),
+    }

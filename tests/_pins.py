@@ -1,0 +1,346 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each pin takes the oracle module as an argument so that the same checks can be
+run against deliberately broken copies of it (tests/test_oracle_mutations.py):
+a plausible mistake anywhere in the oracle must make at least one pin fail.
+
+None of these checks re-types the oracle's own formulas. They use
+* the hand-worked cases in tests/golden/hand_cases.json;
+* Theorem 1 of "Accelerating Large Language Model Decoding with Speculative
+  Sampling" (Supplementary Materials, Proofs; card §4.2): the emitted token of
+  one step is distributed exactly as q. The oracle is treated as a black box
+  whose output is piecewise constant in each uniform; the breakpoints are
+  located by bisection and the law is integrated exactly;
+* the acceptance probability sum_x min(p(x), q(x)) from the same proof;
+* library routines (scipy softmax / logsumexp, numpy searchsorted) for the
+  special cases that reduce to them;
+* invariants (1..K+1 emitted tokens, accepted prefix equals the drafts,
+  exact temperature rescaling).
+"""
+
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+from scipy.special import logsumexp, softmax
+from scipy.stats import chi2
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "hand_cases.json")
+
+
+# ---------------------------------------------------------------- helpers
+
+def probs_to_logits(probs) -> np.ndarray:
+    """ln(prob) rounded to fp32 (zero probability -> -inf), widened back to fp64."""
+    p = np.asarray(probs, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        return np.log(p).astype(np.float32).astype(np.float64)
+
+
+def load_golden():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+def run_fixed_rows(O, tl, dl, tokens, uniforms, T):
+    """Run the oracle on n sequences that share the rows tl [K+1,V], dl [K,V]."""
+    n = len(tokens)
+    tl_b = np.broadcast_to(tl, (n,) + tl.shape)
+    dl_b = np.broadcast_to(dl, (n,) + dl.shape)
+    return O.verify(tl_b, dl_b, np.asarray(tokens), np.asarray(uniforms, dtype=np.float64), T)
+
+
+def sup_true(pred, n, iters=64):
+    """For n monotone predicates (true on [0, a), false on [a, 1]) return each a.
+    A predicate already true at 1 gives 1; one false at 0 gives 0."""
+    lo = np.zeros(n)
+    hi = np.ones(n)
+    t_hi = pred(hi.copy())
+    t_lo = pred(lo.copy())
+    for _ in range(iters):
+        mid = 0.5 * (lo + hi)
+        t = pred(mid)
+        lo = np.where(t, mid, lo)
+        hi = np.where(t, hi, mid)
+    return np.where(t_hi, 1.0, np.where(t_lo, hi, 0.0))
+
+
+def accept_measure(O, tl, dl, pos, prefix, T):
+    """Lebesgue measure of {u_pos : draft x at position `pos` is accepted}, for
+    every candidate x, with the drafts before `pos` fixed to `prefix` and
+    accepted (their uniforms are 0). Returns an array over x."""
+    K = dl.shape[0]
+    V = tl.shape[1]
+    xs = np.arange(V)
+
+    def pred(u):
+        toks = np.zeros((V, K), dtype=np.int64)
+        toks[:, :pos] = prefix
+        toks[:, pos] = xs
+        uni = np.zeros((V, K + 2))
+        uni[:, pos] = u
+        uni[:, pos + 1:K] = 1.0   # later drafts, if any, are rejected; irrelevant here
+        r = run_fixed_rows(O, tl, dl, toks, uni, T)
+        return r.n_accepted > pos
+
+    return sup_true(pred, V)
+
+
+def draw_measure(O, tl, dl, pos, prefix, T, slot, rejected_token=None):
+    """Measure of {u_slot : emitted token at `pos` == y} for every y.
+
+    With `rejected_token` set, draft x = rejected_token sits at `pos` and its
+    test is forced to fail (u_pos = 1.0, rejecting whenever the threshold is
+    at most 1), so the residual draw is measured; without it, all K drafts
+    are the prefix and accepted, so the bonus draw is measured."""
+    K = dl.shape[0]
+    V = tl.shape[1]
+    ys = np.arange(V)
+
+    def pred(u):
+        toks = np.zeros((V, K), dtype=np.int64)
+        uni = np.zeros((V, K + 2))
+        toks[:, :pos] = prefix
+        if rejected_token is not None:
+            toks[:, pos] = rejected_token
+            uni[:, pos] = 1.0
+        uni[:, slot] = u
+        r = run_fixed_rows(O, tl, dl, toks, uni, T)
+        return r.out_tokens[:, pos] <= ys
+
+    F = sup_true(pred, V)
+    return np.diff(np.concatenate([[0.0], F]))
+
+
+def step_law(O, tl, dl, pos, prefix, T):
+    """Exact law of the token emitted at position `pos`, given that the drafts
+    in `prefix` were accepted: sum_x p(x) [a(x) 1{y=x} + (1-a(x)) m_x(y)]."""
+    K = dl.shape[0]
+    V = tl.shape[1]
+    p = softmax(dl[pos] / T)
+    a = accept_measure(O, tl, dl, pos, prefix, T)
+    law = p * a
+    for x in range(V):
+        if p[x] == 0.0 or a[x] == 1.0:
+            continue
+        m = draw_measure(O, tl, dl, pos, prefix, T, slot=K, rejected_token=x)
+        law = law + p[x] * (1.0 - a[x]) * m
+    return law, a, p
+
+
+# ---------------------------------------------------------------- pins
+
+def pin_golden(O):
+    """Hand-worked cases (tests/golden/hand_cases.json)."""
+    for c in load_golden():
+        tl = probs_to_logits(c["target_probs"])[None]
+        dl = probs_to_logits(c["draft_probs"])[None]
+        tok = np.array([c["tokens"]])
+        uni = np.array([c["uniforms"]], dtype=np.float32).astype(np.float64)
+        r = O.verify(tl, dl, tok, uni, 1.0)
+        name = c["name"]
+        assert r.status[0] == 0, name
+        assert list(r.out_tokens[0]) == c["expected_out"], (name, r.out_tokens[0])
+        assert r.n_accepted[0] == c["expected_n_accepted"], name
+        assert bool(r.residual_fallback[0]) == c["expected_fallback"], name
+        np.testing.assert_allclose(r.thresholds[0], c["expected_thresholds"], atol=1e-6,
+                                   err_msg=name)
+        exp_m = np.array([np.nan if v is None else v for v in c["expected_accept_margins"]])
+        np.testing.assert_allclose(r.accept_margin[0], exp_m, atol=1e-6, err_msg=name)
+        np.testing.assert_allclose(r.sample_margin[0], c["expected_sample_margin"], atol=1e-6,
+                                   err_msg=name)
+        np.testing.assert_allclose(r.sample_prob[0], c["expected_sample_prob"], atol=1e-6,
+                                   err_msg=name)
+
+
+def theorem1_cases():
+    rng = np.random.default_rng(7)
+    V = 8
+    base_t = rng.normal(0, 2.0, (2, V))
+    base_d = base_t[:1] + rng.normal(0, 1.5, (1, V))
+    masked_t = base_t.copy()
+    masked_t[0, 3] = -np.inf           # q(3) = 0
+    masked_d = base_d.copy()
+    masked_d[0, 5] = -np.inf           # p(5) = 0: never drafted
+    far_d = rng.normal(0, 3.0, (1, V))
+    return [
+        ("random", base_t, base_d, 1.0),
+        ("temperature-0.7", base_t, base_d, 0.7),
+        ("temperature-1.9", base_t, base_d, 1.9),
+        ("masked", masked_t, masked_d, 1.0),
+        ("q-equals-p", base_t, base_t[:1].copy(), 1.0),
+        ("far-draft", base_t, far_d, 1.0),
+    ]
+
+
+def pin_theorem1(O):
+    """Theorem 1: one step emits x with probability exactly q(x) (to 1e-12),
+    and the acceptance probability is sum_x min(p(x), q(x))."""
+    for name, tl, dl, T in theorem1_cases():
+        law, a, p = step_law(O, tl, dl, 0, np.zeros(0, dtype=np.int64), T)
+        q = softmax(tl[0] / T)
+        np.testing.assert_allclose(law, q, rtol=0, atol=1e-12, err_msg=name)
+        assert abs(np.sum(p * a) - np.sum(np.minimum(p, q))) < 1e-12, name
+
+
+def pin_sequential(O):
+    """Applying the rule position after position recovers the target
+    distribution at each position (card, §4.2): K=2, V=4, exact."""
+    rng = np.random.default_rng(11)
+    V, K, T = 4, 2, 1.0
+    tl = rng.normal(0, 1.5, (K + 1, V))
+    dl = tl[:K] + rng.normal(0, 1.0, (K, V))
+    q = softmax(tl / T, axis=-1)
+    law0, _, _ = step_law(O, tl, dl, 0, np.zeros(0, dtype=np.int64), T)
+    np.testing.assert_allclose(law0, q[0], atol=1e-12)
+    for x0 in range(V):
+        law1, _, _ = step_law(O, tl, dl, 1, np.array([x0]), T)
+        np.testing.assert_allclose(law1, q[1], atol=1e-12, err_msg=f"x0={x0}")
+    # both drafts accepted: the bonus draw at position K follows q_K
+    for prefix in ([0, 1], [3, 2]):
+        m = draw_measure(O, tl, dl, K, np.array(prefix), T, slot=K + 1)
+        np.testing.assert_allclose(m, q[K], atol=1e-12, err_msg=f"bonus {prefix}")
+
+
+def pin_chi_square(O, trials=1_000_000, V=8, seed=3, chunk=200_000):
+    """Seeded trials of one step (K=1): the first emitted token against q, and
+    the bonus token (when the draft is accepted) against q_1; Pearson chi^2
+    p-values above 1e-3. Drafts are drawn by Gumbel-max, so no softmax of
+    the oracle's is used to make them."""
+    rng = np.random.default_rng(seed)
+    tl = rng.normal(0, 2.0, (2, V))
+    dl = tl[:1] + rng.normal(0, 1.0, (1, V))
+    T = 1.0
+    counts0 = np.zeros(V)
+    counts1 = np.zeros(V)
+    n_acc = 0
+    for s in range(0, trials, chunk):
+        n = min(chunk, trials - s)
+        g = rng.gumbel(size=(n, V))
+        toks = np.argmax(dl[0] / T + g, axis=1)[:, None]
+        uni = rng.random((n, 3)).astype(np.float32).astype(np.float64)
+        r = run_fixed_rows(O, tl, dl, toks, uni, T)
+        counts0 += np.bincount(r.out_tokens[:, 0], minlength=V)
+        acc = r.n_accepted == 1
+        counts1 += np.bincount(r.out_tokens[acc, 1], minlength=V)
+        n_acc += int(acc.sum())
+    q = softmax(tl / T, axis=-1)
+    p = softmax(dl / T, axis=-1)
+    for counts, qq, n in ((counts0, q[0], trials), (counts1, q[1], n_acc)):
+        exp = n * qq
+        stat = np.sum((counts - exp) ** 2 / exp)
+        pval = chi2.sf(stat, V - 1)
+        assert pval > 1e-3, (stat, pval)
+    # acceptance rate against sum min(p, q) (binomial, 5 sigma)
+    beta = np.sum(np.minimum(p[0], q[0]))
+    sd = np.sqrt(beta * (1 - beta) / trials)
+    assert abs(n_acc / trials - beta) < 5 * sd, (n_acc / trials, beta)
+
+
+def pin_expected_length(O, n=200_000, seed=5):
+    """Mean accepted count over independent positions: E[n] = sum_k prod_{t<k} beta_t,
+    beta_t = sum_x min(p_t, q_t); Monte Carlo within 5 standard errors."""
+    rng = np.random.default_rng(seed)
+    V, K, T = 16, 4, 1.0
+    tl = rng.normal(0, 2.0, (K + 1, V))
+    dl = tl[:K] + rng.normal(0, 0.8, (K, V))
+    q = softmax(tl / T, axis=-1)
+    p = softmax(dl / T, axis=-1)
+    beta = np.sum(np.minimum(p, q[:K]), axis=-1)
+    expect = sum(np.prod(beta[:k]) for k in range(1, K + 1))
+    g = rng.gumbel(size=(n, K, V))
+    toks = np.argmax(dl[None] / T + g, axis=-1)
+    uni = rng.random((n, K + 2))
+    r = run_fixed_rows(O, tl, dl, toks, uni, T)
+    mean = r.n_accepted.mean()
+    se = r.n_accepted.std() / np.sqrt(n)
+    assert abs(mean - expect) < 5 * se, (mean, expect, se)
+
+
+def pin_library_special_cases(O):
+    """(i) the log-sum-exp of every row against scipy's logsumexp in fp64;
+    (ii) p == q: every draft is accepted and the bonus token equals
+    numpy.searchsorted over the CDF of q_K (side='right')."""
+    rng = np.random.default_rng(13)
+    B, K, V, T = 5, 3, 257, 0.9
+    tl = rng.normal(0, 3.0, (B, K + 1, V))
+    tl[0, 1, :100] = -np.inf
+    dl = tl[:, :K] + rng.normal(0, 0.5, (B, K, V))
+    toks = rng.integers(0, V, (B, K))
+    uni = rng.random((B, K + 2))
+    r = O.verify(tl, dl, toks, uni, T)
+    ref = np.concatenate([logsumexp(tl / T, axis=-1), logsumexp(dl / T, axis=-1)], axis=1)
+    np.testing.assert_allclose(r.lse, ref, rtol=1e-12)
+
+    same = tl[:, :K].copy()
+    toks2 = np.argmax(same / T + rng.gumbel(size=same.shape), axis=-1)
+    uni2 = rng.random((B, K + 2)) * 0.999
+    r2 = O.verify(tl, same, toks2, uni2, T)
+    assert (r2.n_accepted == K).all()
+    for b in range(B):
+        qk = softmax(tl[b, K] / T)
+        cdf = np.cumsum(qk)
+        want = int(np.searchsorted(cdf, uni2[b, K + 1] * cdf[-1], side="right"))
+        assert r2.out_tokens[b, K] == want
+        assert list(r2.out_tokens[b, :K]) == list(toks2[b])
+
+
+def pin_invariants(O):
+    """Emission count in [1, K+1], accepted prefix equals the drafts, the
+    sampled token has positive weight in the distribution it came from, -1
+    padding, and exact invariance under (l, T) -> (2l, 2T)."""
+    rng = np.random.default_rng(17)
+    for K, V, noise in ((1, 50, 0.3), (4, 300, 1.0), (7, 33, 2.5)):
+        B, T = 64, 1.0
+        tl = rng.normal(0, 2.0, (B, K + 1, V))
+        dl = tl[:, :K] + rng.normal(0, noise, (B, K, V))
+        toks = np.argmax(dl / T + rng.gumbel(size=dl.shape), axis=-1)
+        uni = rng.random((B, K + 2))
+        r = O.verify(tl, dl, toks, uni, T)
+        q = softmax(tl / T, axis=-1)
+        p = softmax(dl / T, axis=-1)
+        assert (r.status == 0).all()
+        n = r.n_accepted
+        assert ((n >= 0) & (n <= K)).all()
+        for b in range(B):
+            j = n[b]
+            assert list(r.out_tokens[b, :j]) == list(toks[b, :j])
+            assert (r.out_tokens[b, j + 1:] == -1).all()
+            y = r.out_tokens[b, j]
+            if j < K and not r.residual_fallback[b]:
+                assert q[b, j, y] > p[b, j, y]
+            else:
+                assert q[b, j, y] > 0
+        r2 = O.verify(2.0 * tl, 2.0 * dl, toks, uni, 2.0 * T)
+        assert (r2.out_tokens == r.out_tokens).all()
+        assert (r2.n_accepted == r.n_accepted).all()
+
+
+def pin_failures(O):
+    """Failed sequences: -1 outputs with the right status bit; others untouched."""
+    rng = np.random.default_rng(19)
+    B, K, V = 6, 2, 20
+    tl = rng.normal(0, 1.0, (B, K + 1, V))
+    dl = tl[:, :K] + rng.normal(0, 0.5, (B, K, V))
+    toks = rng.integers(0, V, (B, K))
+    uni = rng.random((B, K + 2))
+    tl[1, 2, 4] = np.nan
+    dl[2, 0, :] = -np.inf
+    toks[3, 1] = V
+    uni[4, 3] = 1.5
+    tl[5, 0, 0] = np.inf
+    r = O.verify(tl, dl, toks, uni, 1.0)
+    assert r.status[0] == 0 and r.n_accepted[0] >= 0
+    assert r.status[1] == O.STATUS_NONFINITE
+    assert r.status[2] == O.STATUS_EMPTY_ROW
+    assert r.status[3] == O.STATUS_TOKEN_RANGE
+    assert r.status[4] == O.STATUS_UNIFORM_RANGE
+    assert r.status[5] == O.STATUS_NONFINITE
+    for b in range(1, B):
+        assert (r.out_tokens[b] == -1).all() and r.n_accepted[b] == -1
+
+
+FAST_PINS = (pin_golden, pin_theorem1, pin_sequential, pin_library_special_cases,
+             pin_invariants, pin_failures)

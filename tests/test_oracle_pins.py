@@ -1,0 +1,70 @@
+"""The fp64 oracle against its pins (CPU only)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import _pins
+
+
+def test_golden_hand_cases():
+    _pins.pin_golden(oracle)
+
+
+def test_theorem1_exact_law_equals_q():
+    _pins.pin_theorem1(oracle)
+
+
+def test_sequential_application_recovers_q_at_each_position():
+    _pins.pin_sequential(oracle)
+
+
+def test_chi_square_million_trials_v8():
+    _pins.pin_chi_square(oracle, trials=1_000_000, V=8)
+
+
+def test_chi_square_million_trials_v64():
+    _pins.pin_chi_square(oracle, trials=1_000_000, V=64, seed=4, chunk=100_000)
+
+
+def test_expected_accepted_length():
+    _pins.pin_expected_length(oracle)
+
+
+def test_library_special_cases():
+    _pins.pin_library_special_cases(oracle)
+
+
+def test_invariants():
+    _pins.pin_invariants(oracle)
+
+
+def test_failure_statuses():
+    _pins.pin_failures(oracle)
+
+
+def test_bf16_inputs_widen_exactly():
+    torch = pytest.importorskip("torch")
+    from synthetic import make_inputs
+    from synthetic.configs import shrink, WORKLOADS
+
+    w = shrink(WORKLOADS["c3"], B=2, V=4096)
+    inp = make_inputs(w)
+    r = oracle.verify_inputs(inp)
+    t64 = inp["target"].to(torch.float64).numpy()
+    # every bf16 value round-trips through fp64 unchanged
+    assert np.array_equal(torch.from_numpy(t64).to(torch.bfloat16).view(torch.int16).numpy(),
+                          inp["target"].view(torch.int16).numpy())
+    assert (r.status == 0).all()
+    assert ((r.n_accepted >= 0) & (r.n_accepted <= w.K)).all()
+
+
+def test_rejects_bad_temperature_and_shapes():
+    tl = np.zeros((1, 2, 4))
+    dl = np.zeros((1, 1, 4))
+    with pytest.raises(ValueError):
+        oracle.verify(tl, dl, np.zeros((1, 1)), np.zeros((1, 3)), 0.0)
+    with pytest.raises(ValueError):
+        oracle.verify(tl, dl, np.zeros((1, 1)), np.zeros((1, 3)), float("nan"))
+    with pytest.raises(ValueError):
+        oracle.verify(tl, dl, np.zeros((1, 2)), np.zeros((1, 3)), 1.0)
