@@ -1,0 +1,381 @@
+"""Benchmark of the speculative-sampling verification step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config c2]
+
+A step is one verification call over one batch of the workload (default: B=8
+sequences, K=4 drafts, V=32000, bf16 logits, T=1; the workload defined over
+1000 repeated verify steps). Inputs are seeded synthetic logits resident in
+HBM before timing starts; steps rotate through a pool of input sets larger
+than twice the L2 cache, so every step streams its logits from HBM. The K
+timed steps are captured in one CUDA graph and timed with CUDA events on the
+launching stream; the streaming kernel of every step is bracketed by its own
+events for the roofline figure.
+
+Rank 0 prints one JSON line. `value` is verified draft positions per second
+over all ranks (B*K per step); `e2e` is the same metric through the
+host-buffer entry point (host->device copy of each step's inputs from pinned
+memory, device->host copy of its outputs, inside the timed region).
+`--impl reference` times the fp64 CPU oracle on the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synthetic import get_workload, make_inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "verified draft positions/sec (and achieved HBM GB/s, % of GB300 peak)"
+UNIT = "draft_positions/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c2", help="c1..c4 or sweep-k{K}-n{noise}")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity at world size 1)."""
+    if world <= 1:
+        return float(x)
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: int, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: units every rank processed over the slowest rank's time."""
+    return world * units_per_rank / seconds_max
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def load_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
+    summary was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+        ent = data[f"{kernel}@{workload}"]
+    except Exception:
+        return None
+    import hashlib
+
+    src = os.path.join(ROOT, "speculative_sampling_verification_gb300", "csrc", "sv_kernels.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return ent["dram_bytes_per_launch"] if ent.get("source_sha") == h else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [p for (t, p) in self.samples if t0 - 0.1 <= t <= t1 + 0.1] or \
+               [p for (_, p) in self.samples]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][1]), "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_rate(w, seconds: float = 12.0, max_steps: int = 400, warmup: int = 0):
+    """Draft positions per second of the fp64 oracle on whole steps of `w`."""
+    import oracle
+
+    sets = [make_inputs(w, step=10_000 + i) for i in range(min(8, max_steps))]
+    for i in range(warmup):
+        oracle.verify_inputs(sets[i % len(sets)], chunk=w.B)
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_steps:
+        oracle.verify_inputs(sets[n % len(sets)], chunk=w.B)
+        n += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return n * w.B * w.K / dt, n, dt
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    steps = max(1, args.steps)
+    import oracle
+
+    sets = [make_inputs(w, step=20_000 + i) for i in range(min(8, steps))]
+    for i in range(args.warmup):
+        oracle.verify_inputs(sets[i % len(sets)], chunk=w.B)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        oracle.verify_inputs(sets[i % len(sets)], chunk=w.B)
+    dt = time.perf_counter() - t0
+    value = steps * w.B * w.K / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "detail": w.describe()},
+        "cpu_baseline": {"value": value, "unit": "draft_positions/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{steps} whole steps of {w.name} (fp64 numpy oracle, 1 thread)"},
+        "e2e": {"value": value, "unit": "draft_positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, world, rank, local):
+    import speculative_sampling_verification_gb300 as sv
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sv.load_library(build=True)
+    dt_code = sv.SV_BF16 if w.dtype == "bf16" else sv.SV_F32
+    B, K, V, es = w.B, w.K, w.V, w.elem_bytes
+    set_bytes = B * (2 * K + 1) * V * es
+    n_sets = max(2, min(64, -(-2 * L2_BYTES // set_bytes) + 1))
+    if set_bytes * n_sets > 40e9:
+        n_sets = 1
+    step_base = 1000 * rank
+    host_sets = [make_inputs(w, step=step_base + i, pin_memory=True) for i in range(n_sets)]
+    sets = []
+    for h in host_sets:
+        sets.append({k: (v.to(dev, non_blocking=True) if torch.is_tensor(v) else v)
+                     for k, v in h.items()})
+    outs = [(torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+             torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
+    ws = sv.new_workspace(B, K, V, dt_code, dev)
+    T = w.temperature
+    stream = torch.cuda.Stream(dev)
+
+    def call(i, evs=None):
+        s = sets[i % n_sets]
+        o, n = outs[i % n_sets]
+        if evs is None:
+            rc = sv.spec_verify(s["target"], s["draft"], s["tokens"], s["uniforms"], T, o, n, ws)
+        else:
+            rc = sv.spec_verify_profiled(s["target"], s["draft"], s["tokens"], s["uniforms"], T,
+                                         o, n, ws, *evs)
+        if rc != 0:
+            raise RuntimeError(f"spec_verify failed: {sv.sv_status_string(rc)}")
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        call(0)  # first call on the device: kernel set-up, before any capture
+    torch.cuda.synchronize()
+
+    steps, warmup = args.steps, max(3, args.warmup)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=stream):
+        for i in range(warmup):
+            call(i)
+    with torch.cuda.graph(g_timed, stream=stream):
+        for i in range(steps):
+            call(warmup + i, evs[i])
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    g_warm.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        g_timed.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    time.sleep(0.3)
+    clocks.stop()
+
+    status = sv.sv_read_device_status(ws, stream)
+    nacc_all = torch.stack([n for _, n in outs]).cpu().numpy()
+    if status != 0 or (nacc_all < 0).any() or (nacc_all > K).any():
+        raise RuntimeError(f"bad device status {status} or n_accepted out of range")
+
+    stats_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in evs]))
+    tail_ms = float(np.mean([b.elapsed_time(c) for _, b, c in evs]))
+
+    elapsed_ms = reduce_max(elapsed_ms, world, dev)
+
+    # End to end through the host-buffer entry point.
+    e2e_steps = args.e2e_steps or min(steps, 200)
+    staging = torch.empty(sv.sv_staging_size(B, K, V, dt_code), dtype=torch.uint8, device=dev)
+    h_out = torch.empty(B, K + 1, dtype=torch.int32).pin_memory()
+    h_nacc = torch.empty(B, dtype=torch.int32).pin_memory()
+
+    def host_call(i):
+        h = host_sets[i % n_sets]
+        rc = sv.spec_verify_host(h["target"], h["draft"], h["tokens"], h["uniforms"], T, h_out,
+                                 h_nacc, staging, ws, stream=stream)
+        if rc != 0:
+            raise RuntimeError(f"spec_verify_host: {rc}")
+
+    for i in range(3):
+        host_call(i)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        host_call(i)
+    e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
+
+    if rank != 0:
+        return
+    per_step_s = elapsed_ms / 1e3 / steps
+    value = aggregate(B * K, world, per_step_s)
+    ideal = w.ideal_bytes_per_step()
+    peak, peak_kind = load_peaks()
+    stats_bytes = B * (2 * K + 1) * V * es
+    achieved = stats_bytes / (stats_ms * 1e-3) / 1e9
+    h2d = B * (K + 1) * V * es + B * K * V * es + B * K * 4 + B * (K + 2) * 4
+    d2h = B * (K + 1) * 4 + B * 4 + 4
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, n, dt = cpu_oracle_rate(w)
+        cpu = {"value": rate, "unit": "draft_positions/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} whole steps of {w.name} in {dt:.1f} s (fp64 numpy oracle, 1 thread)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": per_step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "detail": w.describe(), "input_dtype": w.dtype,
+                   "l2": f"inputs rotate over {n_sets} resident sets of {set_bytes / 1e6:.1f} MB "
+                         f"(> 2x L2 per cycle)" if n_sets > 1 else "one set larger than L2",
+                   "timing": "K steps in one CUDA graph, CUDA events on the launching stream"},
+        "sequences_per_s": world * B / per_step_s,
+        "hbm_gbs_ideal_bytes": ideal / per_step_s / 1e9 * world,
+        "frac_of_peak_ideal_bytes": ideal / per_step_s / 1e9 / peak,
+        "mean_accepted": float(nacc_all.mean()),
+        "roofline": {"bound": "hbm", "kernel": "stats (streaming row statistics)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": load_traffic("stats", w.name),
+                     "bytes_per_launch": stats_bytes, "ms_per_launch": stats_ms,
+                     "rest_of_step_ms": tail_ms},
+        "e2e": {"value": aggregate(B * K * e2e_steps, world, e2e_s), "unit": "draft_positions/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": steps * sv.sv_kernels_per_call(),
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = get_workload(args.config)
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, world, rank)
+        else:
+            run_ours(args, w, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) verification step of speculative sampling.
+ *
+ * The operation is the target-side modified rejection sampling of
+ * "Accelerating Large Language Model Decoding with Speculative Sampling"
+ * (Chen et al., DeepMind), as summarised by the wikillm.com paper card:
+ *   - §4.2 "Decoding transforms": the temperature transform softmax(l / T) is
+ *     applied to both the target rows q and the draft rows p before anything else;
+ *   - §4.2 "Modified rejection sampling" and Algorithm 2 step 3: draft token
+ *     x~_t is accepted, left to right, while u_t < min(1, q(x~_t) / p(x~_t));
+ *     at the first rejection one token is drawn from the normalised residual
+ *     (q - p)_+ = max(0, q - p) / sum max(0, q - p), and the scan stops;
+ *   - Algorithm 2 step 4 and the card's Pitfalls ("Bonus-token typo"): if all K
+ *     drafts are accepted, one bonus token is drawn from the (K+1)-th target row;
+ *   - the card's Pitfalls ("The residual distribution needs care"): a residual
+ *     that sums to zero falls back to q itself.
+ * Each sequence therefore emits between 1 and K+1 tokens (§4.2).
+ *
+ * Conventions the pages leave open, fixed here:
+ *   - uniforms[b, t], t < K, drives the test of draft t; uniforms[b, K] drives
+ *     the residual draw; uniforms[b, K+1] drives the bonus draw;
+ *   - the test is strict (u < min(1, q/p)); p(x~) = 0 with q(x~) > 0 accepts,
+ *     q(x~) = 0 rejects;
+ *   - a draw from weights w with uniform u is the inverse CDF over ascending
+ *     token id: the smallest i with w_0 + ... + w_i > u * sum(w); when no
+ *     such i exists (u = 1) the largest i with w_i > 0 is taken;
+ *   - -inf logits are masked entries (probability 0).
+ *
+ * All entry points are plain C. Pointers marked "device" must point to memory
+ * of the current CUDA device; the library never allocates, frees or keeps
+ * pointers between calls. Work is enqueued on `stream` (a cudaStream_t passed
+ * as void*; NULL means the legacy default stream) and runs asynchronously.
+ *
+ * The first call on a device sets kernel attributes for that device; make it
+ * before capturing the stream into a CUDA graph.
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Logit element types. */
+enum {
+  SV_BF16 = 0, /* bfloat16 */
+  SV_F32 = 1   /* IEEE fp32 */
+};
+
+/* Host-side return codes (no work is enqueued when one of these is returned). */
+enum {
+  SV_OK = 0,
+  SV_ERR_NULL = 1,        /* a required pointer is NULL */
+  SV_ERR_SHAPE = 2,       /* B < 0, K outside [1, 64], V outside [1, 2^31 - 1], or sizes overflow */
+  SV_ERR_TEMPERATURE = 3, /* temperature not finite or not > 0 */
+  SV_ERR_DTYPE = 4,       /* dtype is neither SV_BF16 nor SV_F32 */
+  SV_ERR_ALIGN = 5,       /* a pointer is not aligned to its element (workspace: 256 bytes) */
+  SV_ERR_WORKSPACE = 6,   /* workspace_bytes below sv_workspace_size(), or staging too small */
+  SV_ERR_CUDA = 7         /* a CUDA runtime call failed */
+};
+
+/* Device-side status bits, OR-ed into the status word of the workspace. A
+ * sequence that raises one of the first four gets out_tokens[b, :] = -1 and
+ * n_accepted[b] = -1; other sequences are unaffected. */
+enum {
+  SV_DEV_TOKEN_RANGE = 16,   /* a draft token outside [0, V) */
+  SV_DEV_NONFINITE = 32,     /* a logit row holds NaN or +inf */
+  SV_DEV_EMPTY_ROW = 64,     /* a logit row is entirely -inf */
+  SV_DEV_UNIFORM_RANGE = 128,/* a uniform is NaN or outside [0, 1] */
+  SV_DEV_TIMEOUT = 256       /* a bounded wait inside a kernel ran out (results invalid) */
+};
+
+/* Bytes of device workspace spec_verify needs for this problem size; 0 for an
+ * invalid size. The workspace is scratch owned by the caller; it must be
+ * 256-byte aligned and must not be shared by calls in flight at the same time.
+ * Pure host function: it touches no device. */
+size_t sv_workspace_size(int B, int K, int V, int dtype);
+
+/* One verification step for a batch of B independent sequences.
+ *
+ *   target_logits  device, [B, K+1, V] row-major, dtype; row t of sequence b is
+ *                  q(. | prefix, x~_1..x~_t), t = 0..K (the target's K+1 outputs)
+ *   draft_logits   device, [B, K, V] row-major, dtype; row t is p(. | prefix, x~_1..x~_t)
+ *   draft_tokens   device, [B, K] int32, the drafted tokens x~ (expected in [0, V))
+ *   uniforms       device, [B, K+2] fp32, expected in [0, 1)
+ *   B, K, V        batch, lookahead (1..64), vocabulary (1..2^31-1)
+ *   dtype          SV_BF16 or SV_F32
+ *   temperature    T > 0, applied to both p and q (softmax(l / T))
+ *   out_tokens     device, [B, K+1] int32 (written): accepted drafts, then the
+ *                  drawn token, then -1 padding
+ *   n_accepted     device, [B] int32 (written): accepted drafts per sequence, 0..K
+ *   workspace      device, sv_workspace_size(B, K, V, dtype) bytes, 256-byte aligned
+ *
+ * Inputs are read only. Base pointers of the logits need only element
+ * alignment; 16-byte aligned bases with V * sizeof(dtype) a multiple of 16
+ * take the bulk-copy (TMA) path. Returns SV_OK once the work is enqueued, or
+ * a host-side error code with nothing enqueued. B == 0 returns SV_OK at once.
+ * Device-side problems are reported through sv_read_device_status(). */
+int spec_verify(const void* target_logits, const void* draft_logits,
+                const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* spec_verify plus intermediate values for inspection (each pointer may be NULL):
+ *   row_lse      device, [B, 2K+1] fp64: log sum_i exp(l_i / T) per row, target
+ *                rows 0..K first, then draft rows 0..K-1 (from the streaming pass)
+ *   thresholds   device, [B, K] fp64: min(1, q(x~_t)/p(x~_t)) for every t
+ *   sample_prob  device, [B] fp64: normalised weight of the drawn token in the
+ *                distribution it was drawn from (residual, fallback q, or bonus q) */
+int spec_verify_debug(const void* target_logits, const void* draft_logits,
+                      const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                      int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
+                      void* workspace, size_t workspace_bytes, void* stream, double* row_lse,
+                      double* thresholds, double* sample_prob);
+
+/* spec_verify that also records three caller-owned CUDA events (cudaEvent_t
+ * passed as void*, created with timing enabled) on `stream`: `ev_start` before
+ * the first kernel, `ev_stats_done` after the streaming row-statistics
+ * kernel, `ev_end` after the last kernel. Elapsed times between them time the
+ * streaming pass and the rest of the step. Any event may be NULL. */
+int spec_verify_profiled(const void* target_logits, const void* draft_logits,
+                         const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                         int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
+                         void* workspace, size_t workspace_bytes, void* stream, void* ev_start,
+                         void* ev_stats_done, void* ev_end);
+
+/* Bytes of device staging memory spec_verify_host needs (inputs and outputs). */
+size_t sv_staging_size(int B, int K, int V, int dtype);
+
+/* spec_verify on HOST buffers: copies the four inputs host -> device into
+ * `staging` (device, sv_staging_size() bytes, 256-byte aligned), runs the step,
+ * copies out_tokens / n_accepted back to the host buffers and synchronises
+ * `stream`. Pinned host memory gives the fastest copies. Returns a host-side
+ * error code, or else the device status bits of this call (0 = all ok). */
+int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
+                     const int32_t* h_draft_tokens, const float* h_uniforms, int B, int K,
+                     int V, int dtype, float temperature, int32_t* h_out_tokens,
+                     int32_t* h_n_accepted, void* staging, size_t staging_bytes,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Reads the device status word of the last call that used `workspace`: waits
+ * for `stream`, then stores the OR of the SV_DEV_* bits in *status. */
+int sv_read_device_status(const void* workspace, void* stream, int* status);
+
+/* Static description of a return code or device status bit set. */
+const char* sv_status_string(int status);
+
+/* Kernels one spec_verify call launches (for launch accounting). */
+int sv_kernels_per_call(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H_ */

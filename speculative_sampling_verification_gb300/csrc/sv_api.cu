@@ -1,0 +1,228 @@
+// C-ABI entry points (declared in include/spec_verify.h): argument checks,
+// workspace layout and the launch of the verification kernels.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/spec_verify.h"
+#include "sv_internal.h"
+
+namespace {
+
+bool misaligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+// Checks that need no device. Returns SV_OK or a host error code.
+int validate(const void* target, const void* draft, const void* tokens, const void* uniforms,
+             int B, int K, int V, int dtype, float temperature, const void* out,
+             const void* n_acc, const void* workspace, size_t workspace_bytes, sv::Layout* L) {
+  if (dtype != SV_BF16 && dtype != SV_F32) return SV_ERR_DTYPE;
+  if (!sv::make_layout(B, K, V, dtype, L)) return SV_ERR_SHAPE;
+  if (!std::isfinite(temperature) || !(temperature > 0.0f)) return SV_ERR_TEMPERATURE;
+  if (B == 0) return SV_OK;
+  if (!target || !draft || !tokens || !uniforms || !out || !n_acc || !workspace) return SV_ERR_NULL;
+  const size_t es = dtype == SV_BF16 ? 2 : 4;
+  if (misaligned(target, es) || misaligned(draft, es) || misaligned(tokens, 4) ||
+      misaligned(uniforms, 4) || misaligned(out, 4) || misaligned(n_acc, 4) ||
+      misaligned(workspace, 256))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < L->total) return SV_ERR_WORKSPACE;
+  return SV_OK;
+}
+
+int run(const void* target, const void* draft, const int32_t* tokens, const float* uniforms,
+        int B, int K, int V, int dtype, float temperature, int32_t* out, int32_t* n_acc,
+        void* workspace, size_t workspace_bytes, void* stream, double* dbg_lse, double* dbg_thr,
+        double* dbg_prob, const sv::Events& ev = sv::Events()) {
+  sv::Layout L;
+  int rc = validate(target, draft, tokens, uniforms, B, K, V, dtype, temperature, out, n_acc,
+                    workspace, workspace_bytes, &L);
+  if (rc != SV_OK || B == 0) return rc;
+
+  sv::Params P{};
+  P.target = target;
+  P.draft = draft;
+  P.tokens = tokens;
+  P.uniforms = uniforms;
+  P.B = B;
+  P.K = K;
+  P.V = V;
+  P.dtype = dtype;
+  P.es = L.es;
+  const double T = (double)temperature;
+  const double inv = 1.0 / T;
+  P.c2 = (float)(1.4426950408889634074 / T);
+  P.ih = (float)inv;
+  P.il = (float)(inv - (double)P.ih);
+  P.unit_t = temperature == 1.0f ? 1 : 0;
+  P.inv_t = inv;
+  P.rows_per_seq = L.rows_per_seq;
+  P.nseg = L.nseg;
+  P.seg_elems = L.seg_elems;
+  P.n_units = L.n_units;
+  P.nchunk = L.nchunk;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  P.status = reinterpret_cast<unsigned*>(ws + L.off_status);
+  P.seg_part = reinterpret_cast<float2*>(ws + L.off_seg);
+  P.plans = reinterpret_cast<sv::Plan*>(ws + L.off_plan);
+  P.sub_part = reinterpret_cast<float2*>(ws + L.off_sub);
+  P.out_tokens = out;
+  P.n_acc = n_acc;
+  P.dbg_lse = dbg_lse;
+  P.dbg_thr = dbg_thr;
+  P.dbg_prob = dbg_prob;
+  const bool aligned = !misaligned(target, 16) && !misaligned(draft, 16) &&
+                       ((size_t)V * L.es) % 16 == 0;
+  cudaError_t e = sv::launch_all(P, aligned, static_cast<cudaStream_t>(stream), ev);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+struct Staging {
+  size_t target, draft, tokens, uniforms, out, nacc, total;
+};
+
+bool staging_layout(int B, int K, int V, int dtype, Staging* S) {
+  sv::Layout L;
+  if (!sv::make_layout(B, K, V, dtype, &L)) return false;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = sv::align_up(off + bytes, 256);
+    return at;
+  };
+  S->target = take((size_t)B * (K + 1) * V * L.es);
+  S->draft = take((size_t)B * K * V * L.es);
+  S->tokens = take((size_t)B * K * 4);
+  S->uniforms = take((size_t)B * (K + 2) * 4);
+  S->out = take((size_t)B * (K + 1) * 4);
+  S->nacc = take((size_t)B * 4);
+  S->total = off;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sv_workspace_size(int B, int K, int V, int dtype) {
+  sv::Layout L;
+  if (!sv::make_layout(B, K, V, dtype, &L)) return 0;
+  return L.total;
+}
+
+int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                const float* uniforms, int B, int K, int V, int dtype, float temperature,
+                int32_t* out_tokens, int32_t* n_accepted, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  return run(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype, temperature,
+             out_tokens, n_accepted, workspace, workspace_bytes, stream, nullptr, nullptr, nullptr);
+}
+
+int spec_verify_debug(const void* target_logits, const void* draft_logits,
+                      const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                      int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
+                      void* workspace, size_t workspace_bytes, void* stream, double* row_lse,
+                      double* thresholds, double* sample_prob) {
+  return run(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype, temperature,
+             out_tokens, n_accepted, workspace, workspace_bytes, stream, row_lse, thresholds,
+             sample_prob);
+}
+
+int spec_verify_profiled(const void* target_logits, const void* draft_logits,
+                         const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                         int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
+                         void* workspace, size_t workspace_bytes, void* stream, void* ev_start,
+                         void* ev_stats_done, void* ev_end) {
+  sv::Events ev;
+  ev.start = static_cast<cudaEvent_t>(ev_start);
+  ev.stats_done = static_cast<cudaEvent_t>(ev_stats_done);
+  ev.end = static_cast<cudaEvent_t>(ev_end);
+  return run(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype, temperature,
+             out_tokens, n_accepted, workspace, workspace_bytes, stream, nullptr, nullptr, nullptr,
+             ev);
+}
+
+size_t sv_staging_size(int B, int K, int V, int dtype) {
+  Staging S;
+  if (!staging_layout(B, K, V, dtype, &S)) return 0;
+  return S.total;
+}
+
+int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
+                     const int32_t* h_draft_tokens, const float* h_uniforms, int B, int K, int V,
+                     int dtype, float temperature, int32_t* h_out_tokens, int32_t* h_n_accepted,
+                     void* staging, size_t staging_bytes, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  sv::Layout L;
+  int rc = validate(h_target_logits, h_draft_logits, h_draft_tokens, h_uniforms, B, K, V, dtype,
+                    temperature, h_out_tokens, h_n_accepted, workspace, workspace_bytes, &L);
+  if (rc != SV_OK || B == 0) return rc;
+  Staging S;
+  if (!staging_layout(B, K, V, dtype, &S)) return SV_ERR_SHAPE;
+  if (!staging) return SV_ERR_NULL;
+  if (misaligned(staging, 256)) return SV_ERR_ALIGN;
+  if (staging_bytes < S.total) return SV_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned char* d = static_cast<unsigned char*>(staging);
+  const size_t es = L.es;
+  const size_t nt = (size_t)B * (K + 1) * V * es, nd = (size_t)B * K * V * es;
+  if (cudaMemcpyAsync(d + S.target, h_target_logits, nt, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(d + S.draft, h_draft_logits, nd, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(d + S.tokens, h_draft_tokens, (size_t)B * K * 4, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess ||
+      cudaMemcpyAsync(d + S.uniforms, h_uniforms, (size_t)B * (K + 2) * 4, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  rc = spec_verify(d + S.target, d + S.draft, reinterpret_cast<const int32_t*>(d + S.tokens),
+                   reinterpret_cast<const float*>(d + S.uniforms), B, K, V, dtype, temperature,
+                   reinterpret_cast<int32_t*>(d + S.out), reinterpret_cast<int32_t*>(d + S.nacc),
+                   workspace, workspace_bytes, stream);
+  if (rc != SV_OK) return rc;
+  unsigned status = 0;
+  if (cudaMemcpyAsync(h_out_tokens, d + S.out, (size_t)B * (K + 1) * 4, cudaMemcpyDeviceToHost,
+                      st) != cudaSuccess ||
+      cudaMemcpyAsync(h_n_accepted, d + S.nacc, (size_t)B * 4, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(&status, static_cast<unsigned char*>(workspace) + L.off_status,
+                      sizeof(status), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
+  return (int)status;
+}
+
+int sv_read_device_status(const void* workspace, void* stream, int* status) {
+  if (!workspace || !status) return SV_ERR_NULL;
+  if (misaligned(workspace, 256)) return SV_ERR_ALIGN;
+  unsigned v = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
+  *status = (int)v;
+  return SV_OK;
+}
+
+const char* sv_status_string(int status) {
+  switch (status) {
+    case SV_OK: return "ok";
+    case SV_ERR_NULL: return "a required pointer is NULL";
+    case SV_ERR_SHAPE: return "invalid shape (B < 0, K outside [1,64], V < 1, or too large)";
+    case SV_ERR_TEMPERATURE: return "temperature must be finite and > 0";
+    case SV_ERR_DTYPE: return "dtype must be SV_BF16 or SV_F32";
+    case SV_ERR_ALIGN: return "pointer misaligned (elements, or 256 bytes for workspace/staging)";
+    case SV_ERR_WORKSPACE: return "workspace or staging buffer too small";
+    case SV_ERR_CUDA: return "a CUDA runtime call failed";
+    default: break;
+  }
+  if (status & SV_DEV_TIMEOUT) return "device: a bounded wait ran out (results invalid)";
+  if (status & SV_DEV_NONFINITE) return "device: a logit row holds NaN or +inf";
+  if (status & SV_DEV_EMPTY_ROW) return "device: a logit row is entirely -inf";
+  if (status & SV_DEV_TOKEN_RANGE) return "device: a draft token lies outside [0, V)";
+  if (status & SV_DEV_UNIFORM_RANGE) return "device: a uniform is NaN or outside [0, 1]";
+  return "unknown status";
+}
+
+int sv_kernels_per_call(void) { return sv::kernels_per_call(); }
+
+}  // extern "C"

@@ -1,0 +1,214 @@
+// Device helpers of the verification kernels: inline PTX for the mbarrier /
+// bulk-copy (TMA) pipeline, float-float arithmetic, and a float-float
+// exponential accurate to about 1e-12 relative.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "sv_exp_table.h"
+
+#define SV_DEVINL __device__ __forceinline__
+
+namespace sv {
+
+SV_DEVINL float neg_inf() { return __int_as_float(0xff800000u); }
+
+// ---------------------------------------------------------------- PTX: shared memory, mbarrier, bulk copy
+
+SV_DEVINL uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+SV_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes barrier initialisation visible to the async (bulk-copy) proxy.
+SV_DEVINL void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+SV_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+SV_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+SV_DEVINL uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase: gives up after 200 ms of wall time and
+// returns false (the caller records an error status and winds down).
+constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
+SV_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// dst, src and bytes must all be multiples of 16.
+SV_DEVINL void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+SV_DEVINL uint4 ld_shared_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+// Streaming 16-byte global load that skips L1.
+SV_DEVINL uint4 ld_global_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------------- bf16 and fast fp32 helpers
+
+SV_DEVINL float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+SV_DEVINL float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Packed max of two bf16 pairs (a NaN operand yields the other operand).
+SV_DEVINL uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Hardware 2^x (MUFU), flushes subnormal results to zero; 2^-inf = 0.
+SV_DEVINL float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------- float-float arithmetic
+// A float-float value is hi + lo with |lo| small against |hi|. The error-free
+// transformations below use the _rn intrinsics so that the compiler neither
+// contracts nor reassociates them.
+
+struct ff {
+  float hi, lo;
+};
+
+// s + e == a + b exactly (Knuth's TwoSum).
+SV_DEVINL ff two_sum(float a, float b) {
+  float s = __fadd_rn(a, b);
+  float bb = __fsub_rn(s, a);
+  float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+// s + e == a + b exactly, given |a| >= |b| (Dekker's FastTwoSum).
+SV_DEVINL ff fast_two_sum(float a, float b) {
+  float s = __fadd_rn(a, b);
+  float e = __fsub_rn(b, __fsub_rn(s, a));
+  return {s, e};
+}
+
+// p + e == a * b exactly (FMA-based).
+SV_DEVINL ff two_prod(float a, float b) {
+  float p = __fmul_rn(a, b);
+  float e = __fmaf_rn(a, b, -p);
+  return {p, e};
+}
+
+// acc += x, keeping the sum's low part unnormalised (normalise once at the end).
+SV_DEVINL void ff_accumulate(ff& acc, ff x) {
+  ff s = two_sum(acc.hi, x.hi);
+  acc.hi = s.hi;
+  acc.lo = __fadd_rn(acc.lo, __fadd_rn(s.lo, x.lo));
+}
+
+SV_DEVINL ff ff_normalize(ff a) { return fast_two_sum(a.hi, a.lo); }
+
+SV_DEVINL ff ff_add(ff a, ff b) {
+  ff s = two_sum(a.hi, b.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+SV_DEVINL double ff_to_double(ff a) { return (double)a.hi + (double)a.lo; }
+
+SV_DEVINL ff ff_shfl_xor(ff a, int lane_mask) {
+  return {__shfl_xor_sync(0xffffffffu, a.hi, lane_mask),
+          __shfl_xor_sync(0xffffffffu, a.lo, lane_mask)};
+}
+
+SV_DEVINL ff ff_warp_sum(ff a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = ff_add(a, ff_shfl_xor(a, o));
+  return a;
+}
+
+// ---------------------------------------------------------------- float-float exponential
+//
+// exp(xh + xl) for xh <= ~0 (|xl| at most an ulp of xh), after Tang's
+// table-driven method: k = rint(x * 256/ln2), r = x - k*ln2/256 (two-constant
+// reduction; the head product is exact because head(ln2/256) has its last bit
+// at 2^-32 and |r| < 2^-9), exp(r) - 1 by its Taylor series to r^4 (|r| <=
+// ln2/512, so the next term is below 4e-17), and 2^((k & 255)/256) from a
+// head+tail table. Relative error about 1e-12 for x >= -30; exp(x) for x <
+// -87 (below 2^-125) returns 0. `tab` points at the 256-entry table in
+// shared memory.
+SV_DEVINL ff exp_ff(float xh, float xl, const float2* tab) {
+  const float kf = rintf(__fmul_rn(xh, SV_EXP_INV_LN2_256));
+  const float t = __fmaf_rn(-kf, SV_EXP_LN2_256_HI, xh);     // exact
+  const float c = __fmaf_rn(-kf, SV_EXP_LN2_256_LO, xl);     // small correction, |c| < 1e-5
+  const float t2 = __fmul_rn(t, t);
+  const float poly = __fmaf_rn(__fmaf_rn(t, 1.0f / 24.0f, 1.0f / 6.0f), t, 0.5f);
+  const float cc = __fmaf_rn(__fmul_rn(0.5f, c), c, c);       // c + c^2/2
+  const float rest = __fmaf_rn(t2, poly, __fmaf_rn(cc, t, cc));  // expm1(t + c) - t
+  const int k = __float2int_rn(kf);
+  const float2 T = tab[k & 255];
+  const ff pr = two_prod(T.x, t);
+  const ff s = fast_two_sum(T.x, pr.hi);
+  const float lo =
+      __fadd_rn(__fmaf_rn(T.x, rest, __fmaf_rn(T.y, t, T.y)), __fadd_rn(s.lo, pr.lo));
+  const int q = k >> 8;  // floor(k / 256)
+  const float scale = __int_as_float((q + 127) << 23);
+  const bool under = xh < -87.0f;
+  return {under ? 0.0f : __fmul_rn(s.hi, scale), under ? 0.0f : __fmul_rn(lo, scale)};
+}
+
+// d = l - m as a float-float (exact), then x = d / T via the float-float
+// reciprocal (ih + il) of T. With `unit_t` the scaling is skipped (T == 1).
+SV_DEVINL ff scaled_diff(float l, float m, float ih, float il, bool unit_t) {
+  const ff d = two_sum(l, -m);
+  if (unit_t) return d;
+  const ff p = two_prod(d.hi, ih);
+  const float lo = __fmaf_rn(d.hi, il, __fmaf_rn(d.lo, ih, p.lo));
+  return {p.hi, lo};
+}
+
+}  // namespace sv

@@ -1,0 +1,122 @@
+// Internal definitions shared by the host entry points and the kernels:
+// workspace layout, per-sequence plan, and the launch parameter block.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace sv {
+
+// Streaming pass (row statistics): a row is cut into `nseg` segments of
+// `seg_elems` elements; one (row, segment) pair is a unit of work.
+constexpr long long kTargetUnits = 1216;  // aim for at least this many units per call
+constexpr long long kSegMinBytes = 4096;
+constexpr long long kSegMaxBytes = 65536;
+
+// Sampling pass: rows are cut into chunks of 4096 elements (one CTA of 256
+// threads), each chunk into 8 sub-chunks of 512 elements (one warp).
+constexpr int kChunkElems = 4096;
+constexpr int kSubElems = 512;
+constexpr int kSubPerChunk = kChunkElems / kSubElems;
+
+constexpr int kMaxK = 64;
+
+enum : int { kModeResidual = 0, kModeBonus = 1, kModeFailed = -1 };
+
+// What the scan decided for one sequence; read by the sampling kernels.
+struct Plan {
+  int j;        // accepted drafts (index of the first rejection, or K)
+  int mode;     // kModeResidual, kModeBonus or kModeFailed
+  long long row_q;  // target row to draw from (global row index into target_logits)
+  long long row_p;  // draft row of the residual (global row index into draft_logits)
+  float m_q, m_p;   // maxima of those rows (raw logits)
+  float s_q, s_p;   // streaming-pass sums of exp((l - m) / T) of those rows
+  float u;          // uniform of the draw
+  int pad;
+};
+
+struct Layout {
+  int es;                // element bytes
+  int rows_per_seq;      // 2K+1
+  long long rows_total;  // B (2K+1)
+  int nseg;              // segments per row
+  int seg_elems;         // elements per segment (multiple of 8)
+  long long n_units;     // rows_total * nseg
+  int nchunk;            // sampling chunks per row
+  size_t off_status, off_seg, off_plan, off_sub, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Pure host computation of the workspace layout; false for invalid sizes.
+inline bool make_layout(int B, int K, int V, int dtype, Layout* L) {
+  if (B < 0 || K < 1 || K > kMaxK || V < 1) return false;
+  if (dtype != 0 && dtype != 1) return false;
+  L->es = dtype == 0 ? 2 : 4;
+  L->rows_per_seq = 2 * K + 1;
+  L->rows_total = (long long)B * L->rows_per_seq;
+  const long long row_bytes = (long long)V * L->es;
+  const long long total_bytes = L->rows_total * row_bytes;
+  if (total_bytes > (1LL << 46)) return false;
+  long long target = L->rows_total > kTargetUnits ? L->rows_total : kTargetUnits;
+  long long seg_bytes = target > 0 ? total_bytes / target : kSegMaxBytes;
+  if (seg_bytes < kSegMinBytes) seg_bytes = kSegMinBytes;
+  if (seg_bytes > kSegMaxBytes) seg_bytes = kSegMaxBytes;
+  long long nseg = (row_bytes + seg_bytes - 1) / seg_bytes;
+  if (nseg < 1) nseg = 1;
+  long long seg_elems = ((V + nseg - 1) / nseg + 7) / 8 * 8;
+  nseg = (V + seg_elems - 1) / seg_elems;
+  L->nseg = (int)nseg;
+  L->seg_elems = (int)seg_elems;
+  L->n_units = L->rows_total * nseg;
+  L->nchunk = (int)(((long long)V + kChunkElems - 1) / kChunkElems);
+  size_t off = 0;
+  L->off_status = off;
+  off = align_up(off + 16, 256);
+  L->off_seg = off;
+  off = align_up(off + (size_t)L->n_units * sizeof(float2), 256);
+  L->off_plan = off;
+  off = align_up(off + (size_t)B * sizeof(Plan), 256);
+  L->off_sub = off;
+  off = align_up(off + (size_t)B * L->nchunk * kSubPerChunk * 4 * sizeof(float2), 256);
+  L->total = off;
+  return true;
+}
+
+struct Params {
+  const void* target;
+  const void* draft;
+  const int32_t* tokens;
+  const float* uniforms;
+  int B, K, V, dtype, es;
+  float c2;        // log2(e) / T in fp32 (streaming pass)
+  float ih, il;    // 1/T as a float-float (sampling pass)
+  int unit_t;      // T == 1 exactly
+  double inv_t;    // 1/T in fp64 (scan)
+  int rows_per_seq;
+  int nseg, seg_elems;
+  long long n_units;
+  int nchunk;
+  float2* seg_part;
+  Plan* plans;
+  float2* sub_part;
+  unsigned* status;
+  int32_t* out_tokens;
+  int32_t* n_acc;
+  double* dbg_lse;
+  double* dbg_thr;
+  double* dbg_prob;
+};
+
+// Launchers (sv_kernels.cu). `aligned`: 16-byte aligned rows (bulk-copy path).
+cudaError_t prepare_device(int device);
+// Optional events recorded around the streaming kernel (any may be null).
+struct Events {
+  cudaEvent_t start = nullptr, stats_done = nullptr, end = nullptr;
+};
+cudaError_t launch_all(const Params& P, bool aligned, cudaStream_t stream, const Events& ev);
+int kernels_per_call();
+
+}  // namespace sv

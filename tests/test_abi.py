@@ -1,0 +1,88 @@
+"""The C-ABI library: it builds, loads, exports every declared symbol, and its
+pure host logic (sizes, argument checks, status strings) behaves; nothing
+here launches GPU work."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_sampling_verification_gb300 as sv
+from speculative_sampling_verification_gb300._build import build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return sv.load_library(build_library())
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    keywords = {"if", "sizeof", "defined"}
+    return sorted({n for n in names if n not in keywords})
+
+
+def test_header_declares_the_binding_names():
+    assert set(declared_functions()) == set(sv.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_workspace_size_is_pure_and_monotone(lib):
+    s1 = lib.sv_workspace_size(8, 4, 32000, sv.SV_BF16)
+    s2 = lib.sv_workspace_size(64, 8, 128256, sv.SV_BF16)
+    s3 = lib.sv_workspace_size(256, 4, 256000, sv.SV_F32)
+    assert 0 < s1 < s2 < s3
+    assert s1 % 256 == 0 and s2 % 256 == 0
+    assert lib.sv_workspace_size(0, 4, 1000, sv.SV_F32) > 0
+    for bad in ((-1, 4, 10, 0), (1, 0, 10, 0), (1, 65, 10, 0), (1, 4, 0, 0), (1, 4, 10, 7)):
+        assert lib.sv_workspace_size(*bad) == 0
+    assert lib.sv_staging_size(8, 4, 32000, sv.SV_BF16) >= 8 * 9 * 32000 * 2
+
+
+def _call(lib, **kw):
+    a = dict(t=1 << 20, d=1 << 20, tok=1 << 20, u=1 << 20, B=2, K=3, V=100, dtype=sv.SV_F32,
+             T=1.0, out=1 << 20, nacc=1 << 20, ws=1 << 20, wsb=1 << 30)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.spec_verify(vp(a["t"]), vp(a["d"]), vp(a["tok"]), vp(a["u"]), a["B"], a["K"], a["V"],
+                           a["dtype"], ctypes.c_float(a["T"]), vp(a["out"]), vp(a["nacc"]),
+                           vp(a["ws"]), a["wsb"], None)
+
+
+def test_host_validation_codes(lib):
+    # Every case fails validation before any CUDA call is made.
+    assert _call(lib, dtype=3) == 4
+    assert _call(lib, K=0) == 2
+    assert _call(lib, K=65) == 2
+    assert _call(lib, V=0) == 2
+    assert _call(lib, B=-1) == 2
+    assert _call(lib, T=0.0) == 3
+    assert _call(lib, T=-1.0) == 3
+    assert _call(lib, T=float("nan")) == 3
+    assert _call(lib, T=float("inf")) == 3
+    assert _call(lib, t=0) == 1
+    assert _call(lib, ws=0) == 1
+    assert _call(lib, nacc=0) == 1
+    assert _call(lib, t=(1 << 20) + 2) == 5          # fp32 logits need 4-byte alignment
+    assert _call(lib, ws=(1 << 20) + 16) == 5        # workspace needs 256-byte alignment
+    assert _call(lib, wsb=16) == 6
+    # B == 0 is a no-op that succeeds (nothing is launched).
+    assert _call(lib, B=0, t=0, d=0) == 0
+
+
+def test_status_strings(lib):
+    for code in (0, 1, 2, 3, 4, 5, 6, 7, 16, 32, 64, 128, 256):
+        s = sv.sv_status_string(code)
+        assert s and s != "unknown status"
+    assert lib.sv_kernels_per_call() >= 1
