@@ -173,7 +173,9 @@ def verify(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
     K = K1 - 1
     if K < 1 or draft.shape != (B, K, V) or tokens.shape != (B, K) or uniforms.shape != (B, K + 2):
         raise ValueError("shape mismatch")
-    T = float(np.float64(temperature))
+    # U6: the temperature is an fp32 argument; its fp32 value is widened exactly.
+    with np.errstate(over="ignore"):
+        T = float(np.float32(temperature))
     if not (np.isfinite(T) and T > 0):
         raise ValueError("temperature must be finite and > 0")
 

@@ -167,8 +167,8 @@ def theorem1_cases():
     far_d = rng.normal(0, 3.0, (1, V))
     return [
         ("random", base_t, base_d, 1.0),
-        ("temperature-0.7", base_t, base_d, 0.7),
-        ("temperature-1.9", base_t, base_d, 1.9),
+        ("temperature-0.6875", base_t, base_d, 0.6875),
+        ("temperature-1.875", base_t, base_d, 1.875),
         ("masked", masked_t, masked_d, 1.0),
         ("q-equals-p", base_t, base_t[:1].copy(), 1.0),
         ("far-draft", base_t, far_d, 1.0),
@@ -264,7 +264,7 @@ def pin_library_special_cases(O):
     (ii) p == q: every draft is accepted and the bonus token equals
     numpy.searchsorted over the CDF of q_K (side='right')."""
     rng = np.random.default_rng(13)
-    B, K, V, T = 5, 3, 257, 0.9
+    B, K, V, T = 5, 3, 257, 0.9375
     tl = rng.normal(0, 3.0, (B, K + 1, V))
     tl[0, 1, :100] = -np.inf
     dl = tl[:, :K] + rng.normal(0, 0.5, (B, K, V))

@@ -59,6 +59,21 @@ def test_bf16_inputs_widen_exactly():
     assert ((r.n_accepted >= 0) & (r.n_accepted <= w.K)).all()
 
 
+def test_temperature_is_widened_from_fp32():
+    """The step takes T as fp32 (U6): 0.6 means fp32(0.6) = 0.60000002384..."""
+    rng = np.random.default_rng(2)
+    tl = rng.normal(0, 2.0, (1, 2, 9))
+    dl = tl[:, :1] + rng.normal(0, 1.0, (1, 1, 9))
+    tok = np.array([[3]])
+    uni = np.array([[0.99, 0.5, 0.5]])
+    r = oracle.verify(tl, dl, tok, uni, 0.6)
+    from scipy.special import logsumexp
+
+    T32 = float(np.float32(0.6))
+    np.testing.assert_allclose(r.lse[0, 0], logsumexp(tl[0, 0] / T32), rtol=1e-14)
+    assert abs(r.lse[0, 0] - logsumexp(tl[0, 0] / 0.6)) > 1e-9
+
+
 def test_rejects_bad_temperature_and_shapes():
     tl = np.zeros((1, 2, 4))
     dl = np.zeros((1, 1, 4))
