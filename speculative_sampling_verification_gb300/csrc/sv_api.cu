@@ -62,8 +62,17 @@ int run(const void* target, const void* draft, const int32_t* tokens, const floa
   P.seg_elems = L.seg_elems;
   P.n_units = L.n_units;
   P.nchunk = L.nchunk;
+  P.ns = (long long)L.rows_per_seq * L.nseg;
+  P.np = L.nchunk;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  P.status = reinterpret_cast<unsigned*>(ws + L.off_status);
+  // Control block: status (4 B), pad, ticket (8 B), then done_s, done_p, ready [B] each.
+  P.ctrl = ws + L.off_ctrl;
+  P.ctrl_bytes = L.ctrl_bytes;
+  P.status = reinterpret_cast<unsigned*>(ws + L.off_ctrl);
+  P.ticket = reinterpret_cast<unsigned long long*>(ws + L.off_ctrl + 8);
+  P.done_s = reinterpret_cast<unsigned*>(ws + L.off_ctrl + 16);
+  P.done_p = P.done_s + B;
+  P.ready = P.done_p + B;
   P.seg_part = reinterpret_cast<float2*>(ws + L.off_seg);
   P.plans = reinterpret_cast<sv::Plan*>(ws + L.off_plan);
   P.sub_part = reinterpret_cast<float2*>(ws + L.off_sub);

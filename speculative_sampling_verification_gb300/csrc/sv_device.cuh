@@ -160,6 +160,30 @@ SV_DEVINL ff ff_add(ff a, ff b) {
 
 SV_DEVINL double ff_to_double(ff a) { return (double)a.hi + (double)a.lo; }
 
+SV_DEVINL ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
+
+SV_DEVINL ff ff_sub(ff a, ff b) { return ff_add(a, ff_neg(b)); }
+
+// a * b for float-float operands (relative error about 2^-44).
+SV_DEVINL ff ff_mul(ff a, ff b) {
+  const ff p = two_prod(a.hi, b.hi);
+  const float lo = __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, p.lo));
+  return fast_two_sum(p.hi, lo);
+}
+
+// a * b for a float-float and a float.
+SV_DEVINL ff ff_mul_f(ff a, float b) {
+  const ff p = two_prod(a.hi, b);
+  return fast_two_sum(p.hi, __fmaf_rn(a.lo, b, p.lo));
+}
+
+// a > b for normalised float-float values.
+SV_DEVINL bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+
+SV_DEVINL ff ff_shfl_up(ff a, int delta) {
+  return {__shfl_up_sync(0xffffffffu, a.hi, delta), __shfl_up_sync(0xffffffffu, a.lo, delta)};
+}
+
 SV_DEVINL ff ff_shfl_xor(ff a, int lane_mask) {
   return {__shfl_xor_sync(0xffffffffu, a.hi, lane_mask),
           __shfl_xor_sync(0xffffffffu, a.lo, lane_mask)};

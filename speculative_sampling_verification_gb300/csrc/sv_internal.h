@@ -13,7 +13,7 @@ namespace sv {
 // `seg_elems` elements; one (row, segment) pair is a unit of work.
 constexpr long long kTargetUnits = 1216;  // aim for at least this many units per call
 constexpr long long kSegMinBytes = 4096;
-constexpr long long kSegMaxBytes = 65536;
+constexpr long long kSegMaxBytes = 32768;  // two 16 KB ring stages, so the next segment can be in flight
 
 // Sampling pass: rows are cut into chunks of 4096 elements (one CTA of 256
 // threads), each chunk into 8 sub-chunks of 512 elements (one warp).
@@ -45,7 +45,7 @@ struct Layout {
   int seg_elems;         // elements per segment (multiple of 8)
   long long n_units;     // rows_total * nseg
   int nchunk;            // sampling chunks per row
-  size_t off_status, off_seg, off_plan, off_sub, total;
+  size_t off_status, off_ctrl, ctrl_bytes, off_seg, off_plan, off_sub, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -73,8 +73,10 @@ inline bool make_layout(int B, int K, int V, int dtype, Layout* L) {
   L->n_units = L->rows_total * nseg;
   L->nchunk = (int)(((long long)V + kChunkElems - 1) / kChunkElems);
   size_t off = 0;
-  L->off_status = off;
-  off = align_up(off + 16, 256);
+  L->off_status = off;  // status word (read by the host), then the control block
+  L->off_ctrl = off;
+  L->ctrl_bytes = align_up(16 + (size_t)B * 12, 16);
+  off = align_up(off + L->ctrl_bytes, 256);
   L->off_seg = off;
   off = align_up(off + (size_t)L->n_units * sizeof(float2), 256);
   L->off_plan = off;
@@ -99,6 +101,15 @@ struct Params {
   int nseg, seg_elems;
   long long n_units;
   int nchunk;
+  long long ns;    // stats tickets per sequence ((2K+1) * nseg)
+  long long np;    // draw tickets per sequence (nchunk)
+  int lag;         // sequences between a sequence's stats and draw tickets
+  void* ctrl;      // control block, zeroed before every launch
+  size_t ctrl_bytes;
+  unsigned long long* ticket;
+  unsigned* done_s;  // [B] finished stats tickets
+  unsigned* done_p;  // [B] finished draw tickets
+  unsigned* ready;   // [B] plan published
   float2* seg_part;
   Plan* plans;
   float2* sub_part;
@@ -116,7 +127,7 @@ cudaError_t prepare_device(int device);
 struct Events {
   cudaEvent_t start = nullptr, stats_done = nullptr, end = nullptr;
 };
-cudaError_t launch_all(const Params& P, bool aligned, cudaStream_t stream, const Events& ev);
+cudaError_t launch_all(Params P, bool aligned, cudaStream_t stream, const Events& ev);
 int kernels_per_call();
 
 }  // namespace sv

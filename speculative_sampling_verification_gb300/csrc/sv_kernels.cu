@@ -1,17 +1,32 @@
-// Kernels of the verification step of speculative sampling (modified
-// rejection sampling: §4.2 and Algorithm 2 of "Accelerating Large Language
-// Model Decoding with Speculative Sampling", wikillm.com paper card).
+// Kernel of the verification step of speculative sampling (modified rejection
+// sampling: §4.2 and Algorithm 2 of "Accelerating Large Language Model
+// Decoding with Speculative Sampling", wikillm.com paper card).
 //
-// One call runs four kernels on the caller's stream:
-//   1. stats      one streaming pass over all B(2K+1) logit rows: per (row,
-//                 segment) the maximum m and sum_i 2^((l_i - m) log2(e)/T), the
-//                 temperature transform of §4.2 "Decoding transforms";
-//   2. scan       per sequence: combine the segments, gather the logits at the
-//                 drafted tokens, thresholds min(1, q/p), first rejection j;
-//   3. partials   per (sequence, 4096-element chunk) of the one row pair that
-//                 the draw needs: float-float sums of exp((l - m)/T) (and of
-//                 the residual's positive part), per 512-element sub-chunk;
-//   4. finish     per sequence: exact inverse-CDF search for the drawn token.
+// One persistent kernel per call. CTAs take tickets from a counter; a ticket
+// is one of two kinds of work item, dispensed in sequence-major order:
+//
+//   stats(b, u)   one segment of one of the 2K+1 logit rows of sequence b,
+//                 streamed HBM -> shared memory by 1-D bulk copies
+//                 (cp.async.bulk, mbarrier completion): per segment the
+//                 maximum m and sum_i 2^((l_i - m) log2(e)/T), the
+//                 temperature transform of §4.2 "Decoding transforms".
+//                 The CTA that completes the last segment of b runs the scan
+//                 of b: combine segments, gather the logits at the drafted
+//                 tokens, thresholds min(1, q/p) in fp64, first rejection j
+//                 (Algorithm 2 step 3), and publishes the plan of b.
+//   draw(b, c)    one 4096-element chunk of the row pair the draw of b needs
+//                 (target and draft row j for the residual (q - p)_+, or
+//                 target row K for the bonus token, Algorithm 2 step 4):
+//                 float-float sums of exp((l - m)/T) and of the residual's
+//                 positive part per 512-element sub-chunk. The CTA that
+//                 completes the last chunk of b runs the exact inverse-CDF
+//                 search and writes the drawn token.
+//
+// draw(b, .) tickets come `lag` sequences after stats(b, .) tickets, so the
+// plan of b is normally ready when they are taken and the two rows they
+// re-read are still in L2; their float-float arithmetic overlaps the HBM
+// streaming of later sequences. A draw ticket never waits on a ticket handed
+// out after it, so the schedule cannot deadlock; every wait is bounded.
 #include <cfloat>
 #include <climits>
 #include <cstdint>
@@ -25,6 +40,14 @@ namespace sv {
 constexpr unsigned kDevTokenRange = 16, kDevNonfinite = 32, kDevEmptyRow = 64,
                    kDevUniformRange = 128, kDevTimeout = 256;
 constexpr float kLn2 = 0.693147180559945309f;
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kStageBytes = 16384;
+constexpr int kStages = 4;
+constexpr int kVecPerThread = kStageBytes / 16 / kThreads;  // 4
+constexpr int kCtasPerSm = 3;
+static_assert(kSegMaxBytes <= (long long)kStages * kStageBytes, "a segment must fit the ring");
 
 // ---------------------------------------------------------------- addressing and loads
 
@@ -47,6 +70,46 @@ SV_DEVINL float load_elem(const unsigned char* row, long long i) {
   }
 }
 
+SV_DEVINL uint32_t ld_acquire(const unsigned* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+SV_DEVINL void st_release(unsigned* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait for a flag another CTA sets (200 ms of wall time at most).
+SV_DEVINL bool wait_flag(const unsigned* p) {
+  if (ld_acquire(p)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    __nanosleep(100);
+    if (ld_acquire(p)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---------------------------------------------------------------- per-CTA shared state
+
+struct CtaShared {
+  float2 tab[256];  // 2^(j/256), head + tail
+  uint64_t full[kStages];
+  float red_m[kWarps], red_s[kWarps];
+  float s_m[2 * kMaxK + 1], s_s[2 * kMaxK + 1];
+  double s_lse[2 * kMaxK + 1];
+  double s_thr[kMaxK];
+  float s_u[kMaxK + 2];
+  int s_tok[kMaxK];
+  ff red_f[kWarps];
+  ff s_pref;
+  Plan plan;
+  unsigned long long ticket, next;
+  unsigned bits;
+  int j, g, flag;
+};
+
 // ---------------------------------------------------------------- (max, sum) pairs
 // A pair (m, s) stands for the sum s * 2^(m c2) of 2^(l_i c2) terms; s is
 // NaN when a NaN (or +inf) entry was seen; m = -inf with s = 0 means "no
@@ -64,8 +127,8 @@ SV_DEVINL void ms_combine(float& m, float& s, float m2, float s2, float c2) {
   m = M;
 }
 
-// Block-wide combine; blockDim.x a multiple of 32, at most 1024. Result in thread 0.
-SV_DEVINL void block_combine(float& m, float& s, float c2, float* red_m, float* red_s) {
+// Block-wide combine (kThreads threads). Result in thread 0.
+SV_DEVINL void block_combine(float& m, float& s, float c2, CtaShared& sh) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -74,14 +137,13 @@ SV_DEVINL void block_combine(float& m, float& s, float c2, float* red_m, float* 
   }
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0) {
-    red_m[w] = m;
-    red_s[w] = s;
+    sh.red_m[w] = m;
+    sh.red_s[w] = s;
   }
   __syncthreads();
   if (w == 0) {
-    const int nw = blockDim.x >> 5;
-    m = l < nw ? red_m[l] : neg_inf();
-    s = l < nw ? red_s[l] : 0.0f;
+    m = l < kWarps ? sh.red_m[l] : neg_inf();
+    s = l < kWarps ? sh.red_s[l] : 0.0f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -92,21 +154,12 @@ SV_DEVINL void block_combine(float& m, float& s, float c2, float* red_m, float* 
   __syncthreads();
 }
 
-// ---------------------------------------------------------------- 1. stats, bulk-copy path
+// ---------------------------------------------------------------- stats: one segment
 //
-// Persistent CTAs, each owning a contiguous range of units (row segments) in
-// sequence-major order. Thread 0 streams the range through a ring of kStages
-// 16 KB shared-memory stages with 1-D bulk copies (cp.async.bulk, completion
-// on an mbarrier); all 256 threads consume each stage with 16-byte shared
-// loads. Per thread: the stage's local max (packed bf16x2 max for bf16), a
-// rescale of the four running sums only when the max grows, then one FFMA and
-// one MUFU ex2 per element against H = fl(m * c2). The rounding residual of H
-// is folded back in once per unit.
-
-constexpr int kStatsThreads = 256;
-constexpr int kStageBytes = 16384;
-constexpr int kStages = 4;
-constexpr int kVecPerThread = kStageBytes / 16 / kStatsThreads;  // 4
+// Per thread: the stage's local max (packed bf16x2 max for bf16), a rescale
+// of the four running sums only when the max grows, then one FFMA and one
+// MUFU ex2 per element against H = fl(m * c2); the rounding residual of H is
+// folded back in once per segment.
 
 template <int DT>
 SV_DEVINL bool any_nan(const uint4 (&v)[kVecPerThread]) {
@@ -171,7 +224,7 @@ SV_DEVINL void stats_consume(const uint4 (&v)[kVecPerThread], float& m_run, floa
   }
 }
 
-// Per-thread (m, s) of a finished unit, with H's rounding residual folded in.
+// Per-thread sum of a finished segment, with H's rounding residual folded in.
 SV_DEVINL float thread_sum(float m_run, float H, const float (&acc)[4], bool nan_seen, float c2) {
   if (m_run == neg_inf()) return nan_seen ? __int_as_float(0x7fc00000) : 0.0f;
   float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
@@ -180,285 +233,239 @@ SV_DEVINL float thread_sum(float m_run, float H, const float (&acc)[4], bool nan
   return nan_seen ? __int_as_float(0x7fc00000) : s;
 }
 
+SV_DEVINL int unit_len(const Params& P, long long u) {
+  const int seg = (int)(u % P.nseg);
+  return seg == P.nseg - 1 ? P.V - seg * P.seg_elems : P.seg_elems;
+}
+
+SV_DEVINL const unsigned char* unit_row(const Params& P, long long u) {
+  const long long row = u / P.nseg;
+  return row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
+}
+
+// Bulk-copy path, producer side (thread 0): issue the segment's 16 KB pieces
+// (at most two: segments are at most 32 KB) into the next ring stages.
+// `issued` counts pieces issued over the CTA's life.
 template <int DT>
-__global__ void __launch_bounds__(kStatsThreads) stats_tma_kernel(Params P) {
-  extern __shared__ __align__(128) unsigned char sbuf[];
-  __shared__ __align__(8) uint64_t full[kStages];
-  __shared__ float red_m[kStatsThreads / 32], red_s[kStatsThreads / 32];
+SV_DEVINL void stats_issue(const Params& P, long long u, unsigned char* ring, CtaShared& sh,
+                           uint32_t& issued) {
+  constexpr int kEs = DT == 0 ? 2 : 4;
+  constexpr int kStageElems = kStageBytes / kEs;
+  const int len = unit_len(P, u);
+  const int npieces = (len + kStageElems - 1) / kStageElems;
+  const unsigned char* src = unit_row(P, u) + (size_t)(u % P.nseg) * P.seg_elems * kEs;
+  for (int i = 0; i < npieces; ++i) {
+    const int st = (int)((issued + i) % kStages);
+    const int n = min(kStageElems, len - i * kStageElems);
+    const uint32_t bytes = (uint32_t)n * kEs;
+    mbar_arrive_expect_tx(&sh.full[st], bytes);
+    bulk_copy_g2s(ring + st * kStageBytes, src + (size_t)i * kStageBytes, bytes, &sh.full[st]);
+  }
+  issued += npieces;
+}
+
+// Bulk-copy path, consumer side (all threads): the segment's pieces are the
+// next ones in ring order. `piece` counts consumed pieces (mbarrier phases).
+// Returns false, with every thread agreeing, if a wait ran out.
+template <int DT>
+SV_DEVINL bool stats_consume_unit(const Params& P, long long u, const unsigned char* ring,
+                                  CtaShared& sh, uint32_t& piece) {
   constexpr int kEs = DT == 0 ? 2 : 4;
   constexpr int kStageElems = kStageBytes / kEs;
   const int tid = threadIdx.x;
-  const long long u0 = (long long)blockIdx.x * P.n_units / gridDim.x;
-  const long long u1 = (long long)(blockIdx.x + 1) * P.n_units / gridDim.x;
-  if (u0 >= u1) return;
-
-  auto unit_len = [&](long long u) -> int {
-    const int seg = (int)(u % P.nseg);
-    return seg == P.nseg - 1 ? P.V - seg * P.seg_elems : P.seg_elems;
-  };
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  // Producer cursor (thread 0): next piece = unit pu, element offset poff.
-  long long pu = u0;
-  int poff = 0;
-  uint32_t issued = 0;
-  auto issue = [&](int stage) {
-    if (pu >= u1) return;
-    ++issued;
-    const int len = unit_len(pu);
-    const int n = min(kStageElems, len - poff);
-    const long long row = pu / P.nseg;
-    const int seg = (int)(pu % P.nseg);
-    const unsigned char* src = row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq)) +
-                               ((size_t)seg * P.seg_elems + poff) * kEs;
-    const uint32_t bytes = (uint32_t)n * kEs;
-    mbar_arrive_expect_tx(&full[stage], bytes);
-    bulk_copy_g2s(sbuf + stage * kStageBytes, src, bytes, &full[stage]);
-    poff += n;
-    if (poff >= len) {
-      ++pu;
-      poff = 0;
-    }
-  };
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) issue(s);
-  }
-
+  const int len = unit_len(P, u);
+  const int npieces = (len + kStageElems - 1) / kStageElems;
   const float c2 = P.c2;
-  long long cu = u0;
-  int coff = 0;
-  uint32_t piece = 0;
   float m_run = neg_inf(), H = neg_inf();
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   bool nan_seen = false, timed_out = false;
   const uint32_t fill = DT == 0 ? 0xff80ff80u : 0xff800000u;  // -inf
-
-  while (cu < u1) {
-    const int stage = (int)(piece % kStages);
-    const uint32_t parity = (piece / kStages) & 1u;
-    const int len = unit_len(cu);
-    const int n = min(kStageElems, len - coff);
-    if (!mbar_wait(&full[stage], parity)) timed_out = true;
-    const unsigned char* buf = sbuf + stage * kStageBytes;
-    const int nvec = n * kEs / 16;
+  for (int i = 0; i < npieces; ++i) {
+    const uint32_t p = piece + i;
+    const int st = (int)(p % kStages);
+    if (!mbar_wait(&sh.full[st], (p / kStages) & 1u)) timed_out = true;
+    const unsigned char* buf = ring + st * kStageBytes;
+    const int nvec = min(kStageElems, len - i * kStageElems) * kEs / 16;
     uint4 v[kVecPerThread];
 #pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) {
-      const int idx = tid + i * kStatsThreads;
-      v[i] = idx < nvec ? ld_shared_v4(buf + idx * 16) : make_uint4(fill, fill, fill, fill);
+    for (int k = 0; k < kVecPerThread; ++k) {
+      const int idx = tid + k * kThreads;
+      v[k] = idx < nvec ? ld_shared_v4(buf + idx * 16) : make_uint4(fill, fill, fill, fill);
     }
     stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
-    coff += n;
-    if (coff >= len) {
-      float s = thread_sum(m_run, H, acc, nan_seen, c2);
-      float m = m_run;
-      block_combine(m, s, c2, red_m, red_s);
-      if (tid == 0) P.seg_part[cu] = make_float2(m, s);
-      m_run = neg_inf();
-      H = neg_inf();
-      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-      nan_seen = false;
-      ++cu;
-      coff = 0;
-    }
-    // Every thread is done with this stage; a timed-out wait anywhere aborts the CTA.
-    if (__syncthreads_or(timed_out)) {
-      if (tid == 0) {
-        atomicOr(P.status, kDevTimeout);
-        // Give the copies still in flight a bounded chance to land before exiting.
-        for (uint32_t p = piece; p < issued; ++p)
-          (void)mbar_wait(&full[p % kStages], (p / kStages) & 1u);
-      }
-      return;
-    }
-    if (tid == 0) issue(stage);
-    ++piece;
   }
+  piece += npieces;
+  float s = thread_sum(m_run, H, acc, nan_seen, c2);
+  float m = m_run;
+  block_combine(m, s, c2, sh);  // its barriers also free the segment's stages
+  if (tid == 0) P.seg_part[u] = make_float2(m, s);
+  return !__syncthreads_or(timed_out);
 }
 
-// ---------------------------------------------------------------- 1'. stats, plain-load path
-// For rows that are not 16-byte aligned: one CTA per unit at a time, two
-// passes over the unit with element loads (max, then sum).
-
+// Plain-load path for rows that are not 16-byte aligned: two passes (max, sum).
 template <int DT>
-__global__ void __launch_bounds__(kStatsThreads) stats_plain_kernel(Params P) {
-  __shared__ float red_m[kStatsThreads / 32], red_s[kStatsThreads / 32];
+SV_DEVINL void stats_unit_plain(const Params& P, long long u, CtaShared& sh) {
   const float c2 = P.c2;
-  for (long long u = blockIdx.x; u < P.n_units; u += gridDim.x) {
-    const long long row = u / P.nseg;
-    const int seg = (int)(u % P.nseg);
-    const int len = seg == P.nseg - 1 ? P.V - seg * P.seg_elems : P.seg_elems;
-    const unsigned char* rb = row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
-    const long long e0 = (long long)seg * P.seg_elems;
-    float m = neg_inf();
-    bool nan_seen = false;
-    for (int i = threadIdx.x; i < len; i += blockDim.x) {
-      const float l = load_elem<DT>(rb, e0 + i);
-      nan_seen |= (l != l);
-      m = fmaxf(m, l);
-    }
-    float s = 0.f;
-    if (m != neg_inf()) {
-      for (int i = threadIdx.x; i < len; i += blockDim.x)
-        s += ex2_fast((load_elem<DT>(rb, e0 + i) - m) * c2);
-    }
-    if (nan_seen) s = __int_as_float(0x7fc00000);
-    block_combine(m, s, c2, red_m, red_s);
-    if (threadIdx.x == 0) P.seg_part[u] = make_float2(m, s);
+  const int len = unit_len(P, u);
+  const unsigned char* rb = unit_row(P, u);
+  const long long e0 = (long long)(u % P.nseg) * P.seg_elems;
+  float m = neg_inf();
+  bool nan_seen = false;
+  for (int i = threadIdx.x; i < len; i += kThreads) {
+    const float l = load_elem<DT>(rb, e0 + i);
+    nan_seen |= (l != l);
+    m = fmaxf(m, l);
   }
+  float s = 0.f;
+  if (m != neg_inf()) {
+    for (int i = threadIdx.x; i < len; i += kThreads)
+      s += ex2_fast((load_elem<DT>(rb, e0 + i) - m) * c2);
+  }
+  if (nan_seen) s = __int_as_float(0x7fc00000);
+  block_combine(m, s, c2, sh);
+  if (threadIdx.x == 0) P.seg_part[u] = make_float2(m, s);
 }
 
-// ---------------------------------------------------------------- 2. scan
+// ---------------------------------------------------------------- scan of one sequence
 
-constexpr int kScanThreads = 128;
-
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(Params P) {
-  __shared__ float s_m[2 * kMaxK + 1];
-  __shared__ float s_s[2 * kMaxK + 1];
-  __shared__ double s_lse[2 * kMaxK + 1];
-  __shared__ double s_thr[kMaxK];
-  __shared__ unsigned s_bits;
-  __shared__ int s_j;
-  const long long b = blockIdx.x;
+SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
   const int tid = threadIdx.x, K = P.K, R = P.rows_per_seq;
-  if (tid == 0) s_bits = 0;
+  if (tid == 0) sh.bits = 0;
+  // Stage the drafted tokens and uniforms of the sequence.
+  for (int t = tid; t < K + 2; t += kThreads) {
+    if (t < K) sh.s_tok[t] = P.tokens[b * K + t];
+    sh.s_u[t] = P.uniforms[b * (K + 2) + t];
+  }
   __syncthreads();
 
-  // Row statistics: m = max over segments, S = sum of rescaled segment sums.
-  for (int r = tid; r < R; r += blockDim.x) {
+  // Row statistics: m = max over segments, S = sum of rescaled segment sums
+  // (one pass, rescaling the running sum when the maximum grows).
+  for (int r = tid; r < R; r += kThreads) {
     const float2* part = P.seg_part + ((long long)b * R + r) * P.nseg;
     float m = neg_inf();
+    double S = 0.0;
     bool nan_seen = false;
     for (int g = 0; g < P.nseg; ++g) {
-      const float2 ps = part[g];
-      m = fmaxf(m, ps.x);
+      const float2 ps = __ldcg(part + g);
       nan_seen |= (ps.y != ps.y);
+      if (ps.x == neg_inf()) continue;
+      if (ps.x > m) {
+        if (m != neg_inf()) S *= (double)exp2f((m - ps.x) * P.c2);
+        m = ps.x;
+      }
+      S += (double)ps.y * (double)exp2f((ps.x - m) * P.c2);
     }
-    double S = 0.0;
     unsigned bits = 0;
     if (nan_seen) {
       bits = kDevNonfinite;
     } else if (m == neg_inf()) {
       bits = kDevEmptyRow;
-    } else {
-      for (int g = 0; g < P.nseg; ++g) {
-        const float2 ps = part[g];
-        if (ps.x != neg_inf()) S += (double)ps.y * (double)exp2f((ps.x - m) * P.c2);
-      }
     }
-    if (bits) atomicOr(&s_bits, bits);
-    s_m[r] = m;
-    s_s[r] = (float)S;
-    s_lse[r] = bits ? __longlong_as_double(0x7ff8000000000000LL) : (double)m * P.inv_t + log(S);
+    if (bits) atomicOr(&sh.bits, bits);
+    sh.s_m[r] = m;
+    sh.s_s[r] = (float)S;
+    sh.s_lse[r] = bits ? __longlong_as_double(0x7ff8000000000000LL) : (double)m * P.inv_t + log(S);
   }
-  for (int t = tid; t < K; t += blockDim.x) {
-    const int x = P.tokens[b * K + t];
-    if (x < 0 || x >= P.V) atomicOr(&s_bits, kDevTokenRange);
+  for (int t = tid; t < K; t += kThreads) {
+    const int x = sh.s_tok[t];
+    if (x < 0 || x >= P.V) atomicOr(&sh.bits, kDevTokenRange);
   }
-  for (int t = tid; t < K + 2; t += blockDim.x) {
-    const float u = P.uniforms[b * (K + 2) + t];
-    if (!(u >= 0.0f && u <= 1.0f)) atomicOr(&s_bits, kDevUniformRange);
+  for (int t = tid; t < K + 2; t += kThreads) {
+    const float u = sh.s_u[t];
+    if (!(u >= 0.0f && u <= 1.0f)) atomicOr(&sh.bits, kDevUniformRange);
   }
   __syncthreads();
-  const unsigned bits = s_bits;
+  const unsigned bits = sh.bits;
   if (P.dbg_lse)
-    for (int r = tid; r < R; r += blockDim.x) P.dbg_lse[b * R + r] = s_lse[r];
-  if (bits) {
-    for (int t = tid; t <= K; t += blockDim.x) P.out_tokens[b * (K + 1) + t] = -1;
-    if (P.dbg_thr)
-      for (int t = tid; t < K; t += blockDim.x)
-        P.dbg_thr[b * K + t] = __longlong_as_double(0x7ff8000000000000LL);
-    if (tid == 0) {
+    for (int r = tid; r < R; r += kThreads) P.dbg_lse[b * R + r] = sh.s_lse[r];
+
+  if (!bits) {
+    // Thresholds min(1, q(x~)/p(x~)) at the drafted tokens (§4.2), in fp64:
+    // log q(x) - log p(x) = (lq - lp)/T - (lse_q - lse_p).
+    for (int t = tid; t < K; t += kThreads) {
+      const int x = sh.s_tok[t];
+      float lq, lp;
+      if (P.dtype == 0) {
+        lq = load_elem<0>(row_base(P, b, t), x);
+        lp = load_elem<0>(row_base(P, b, K + 1 + t), x);
+      } else {
+        lq = load_elem<1>(row_base(P, b, t), x);
+        lp = load_elem<1>(row_base(P, b, K + 1 + t), x);
+      }
+      double thr;
+      if (lq == neg_inf()) {
+        thr = 0.0;  // q(x~) = 0 rejects
+      } else if (lp == neg_inf()) {
+        thr = 1.0;  // p(x~) = 0 < q(x~) accepts
+      } else {
+        const double lr =
+            ((double)lq - (double)lp) * P.inv_t - (sh.s_lse[t] - sh.s_lse[K + 1 + t]);
+        thr = lr >= 0.0 ? 1.0 : exp(lr);
+      }
+      sh.s_thr[t] = thr;
+      if (P.dbg_thr) P.dbg_thr[b * K + t] = thr;
+    }
+  }
+  __syncthreads();
+
+  if (tid == 0) {
+    Plan pl{};
+    if (bits) {
       atomicOr(P.status, bits);
-      Plan pl{};
       pl.j = -1;
       pl.mode = kModeFailed;
-      P.plans[b] = pl;
       P.n_acc[b] = -1;
       if (P.dbg_prob) P.dbg_prob[b] = __longlong_as_double(0x7ff8000000000000LL);
-    }
-    return;
-  }
-
-  // Thresholds min(1, q(x~)/p(x~)) at the drafted tokens (§4.2), in fp64:
-  // log q(x) - log p(x) = (lq - lp)/T - (lse_q - lse_p).
-  for (int t = tid; t < K; t += blockDim.x) {
-    const int x = P.tokens[b * K + t];
-    float lq, lp;
-    if (P.dtype == 0) {
-      lq = load_elem<0>(row_base(P, b, t), x);
-      lp = load_elem<0>(row_base(P, b, K + 1 + t), x);
     } else {
-      lq = load_elem<1>(row_base(P, b, t), x);
-      lp = load_elem<1>(row_base(P, b, K + 1 + t), x);
-    }
-    double thr;
-    if (lq == neg_inf()) {
-      thr = 0.0;  // q(x~) = 0 rejects
-    } else if (lp == neg_inf()) {
-      thr = 1.0;  // p(x~) = 0 < q(x~) accepts
-    } else {
-      const double lr = ((double)lq - (double)lp) * P.inv_t - (s_lse[t] - s_lse[K + 1 + t]);
-      thr = lr >= 0.0 ? 1.0 : exp(lr);
-    }
-    s_thr[t] = thr;
-    if (P.dbg_thr) P.dbg_thr[b * K + t] = thr;
-  }
-  __syncthreads();
-
-  // Left-to-right scan: accept while u_t < thr_t (Algorithm 2 step 3).
-  if (tid == 0) {
-    const float* u = P.uniforms + b * (K + 2);
-    int j = K;
-    for (int t = 0; t < K; ++t) {
-      if (!((double)u[t] < s_thr[t])) {
-        j = t;
-        break;
+      // Left-to-right scan: accept while u_t < thr_t (Algorithm 2 step 3).
+      int j = K;
+      for (int t = 0; t < K; ++t) {
+        if (!((double)sh.s_u[t] < sh.s_thr[t])) {
+          j = t;
+          break;
+        }
       }
-    }
-    Plan pl{};
-    pl.j = j;
-    if (j < K) {
-      pl.mode = kModeResidual;
-      pl.row_q = b * (K + 1) + j;
-      pl.row_p = b * K + j;
-      pl.m_q = s_m[j];
-      pl.s_q = s_s[j];
-      pl.m_p = s_m[K + 1 + j];
-      pl.s_p = s_s[K + 1 + j];
-      pl.u = u[K];
-    } else {
-      pl.mode = kModeBonus;
-      pl.row_q = b * (K + 1) + K;
-      pl.row_p = -1;
-      pl.m_q = s_m[K];
-      pl.s_q = s_s[K];
-      pl.m_p = 0.f;
-      pl.s_p = 0.f;
-      pl.u = u[K + 1];
+      pl.j = j;
+      if (j < K) {
+        pl.mode = kModeResidual;
+        pl.row_q = b * (K + 1) + j;
+        pl.row_p = b * K + j;
+        pl.m_q = sh.s_m[j];
+        pl.s_q = sh.s_s[j];
+        pl.m_p = sh.s_m[K + 1 + j];
+        pl.s_p = sh.s_s[K + 1 + j];
+        pl.u = sh.s_u[K];
+      } else {
+        pl.mode = kModeBonus;
+        pl.row_q = b * (K + 1) + K;
+        pl.row_p = -1;
+        pl.m_q = sh.s_m[K];
+        pl.s_q = sh.s_s[K];
+        pl.u = sh.s_u[K + 1];
+      }
+      P.n_acc[b] = j;
     }
     P.plans[b] = pl;
-    P.n_acc[b] = j;
-    s_j = j;
+    sh.j = pl.j;
   }
   __syncthreads();
-  const int j = s_j;
-  for (int t = tid; t <= K; t += blockDim.x) {
-    if (t < j)
-      P.out_tokens[b * (K + 1) + t] = P.tokens[b * K + t];
-    else if (t > j)
+  const int j = sh.j;
+  for (int t = tid; t <= K; t += kThreads) {
+    if (j < 0 || t > j)
       P.out_tokens[b * (K + 1) + t] = -1;
+    else if (t < j)
+      P.out_tokens[b * (K + 1) + t] = sh.s_tok[t];
   }
+  if (P.dbg_thr && bits)
+    for (int t = tid; t < K; t += kThreads)
+      P.dbg_thr[b * K + t] = __longlong_as_double(0x7ff8000000000000LL);
+  // Publish the plan: every thread's writes first, then the flag (release).
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) st_release(P.ready + b, 1u);
 }
 
-// ---------------------------------------------------------------- 3./4. draw: shared element code
-
-constexpr int kSampleThreads = 256;
+// ---------------------------------------------------------------- draw: shared element code
 
 // Element weights of the draw, in float-float. For the residual,
 // w = e_q * S_p - e_p * S_q on the positive set (q > p judged with the
@@ -472,7 +479,23 @@ struct DrawRow {
   bool unit_t;
 };
 
-template <int DT, bool RESID>
+SV_DEVINL DrawRow draw_row(const Params& P, const Plan& pl) {
+  DrawRow d;
+  d.rq = static_cast<const unsigned char*>(P.target) + (size_t)pl.row_q * P.V * P.es;
+  d.rp = pl.mode == kModeResidual
+             ? static_cast<const unsigned char*>(P.draft) + (size_t)pl.row_p * P.V * P.es
+             : nullptr;
+  d.mq = pl.m_q;
+  d.mp = pl.m_p;
+  d.sq = pl.s_q;
+  d.sp = pl.s_p;
+  d.ih = P.ih;
+  d.il = P.il;
+  d.unit_t = P.unit_t != 0;
+  return d;
+}
+
+template <bool RESID>
 SV_DEVINL void element_exps(const DrawRow& d, float lq, float lp, const float2* tab, ff& eq,
                             ff& ep, bool& in_pos) {
   const ff xq = scaled_diff(lq, d.mq, d.ih, d.il, d.unit_t);
@@ -510,26 +533,15 @@ SV_DEVINL void load_run(const unsigned char* row, long long e, int V, bool vec_o
   }
 }
 
-// ---------------------------------------------------------------- 3. partials
+// ---------------------------------------------------------------- draw: one chunk
 
 template <int DT, bool RESID>
-SV_DEVINL void partial_body(const Params& P, const Plan& pl, const float2* tab, bool aligned,
+SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab, bool aligned,
                             long long b, int c) {
   constexpr int kVec = 16 / (DT == 0 ? 2 : 4);
   constexpr int kRuns = kSubElems / (32 * kVec);
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long e0 = ((long long)c * kSubPerChunk + w) * kSubElems;
-  DrawRow d;
-  d.rq = static_cast<const unsigned char*>(P.target) + (size_t)pl.row_q * P.V * P.es;
-  d.rp = RESID ? static_cast<const unsigned char*>(P.draft) + (size_t)pl.row_p * P.V * P.es
-               : nullptr;
-  d.mq = pl.m_q;
-  d.mp = pl.m_p;
-  d.sq = pl.s_q;
-  d.sp = pl.s_p;
-  d.ih = P.ih;
-  d.il = P.il;
-  d.unit_t = P.unit_t != 0;
   ff Sq{0.f, 0.f}, Sp{0.f, 0.f}, A{0.f, 0.f}, Bs{0.f, 0.f};
   if (e0 < P.V) {
 #pragma unroll
@@ -542,7 +554,7 @@ SV_DEVINL void partial_body(const Params& P, const Plan& pl, const float2* tab, 
       for (int k = 0; k < kVec; ++k) {
         ff eq, ep;
         bool pos;
-        element_exps<DT, RESID>(d, xq[k], RESID ? xp[k] : 0.f, tab, eq, ep, pos);
+        element_exps<RESID>(d, xq[k], xp[k], tab, eq, ep, pos);
         ff_accumulate(Sq, eq);
         if constexpr (RESID) {
           ff_accumulate(Sp, ep);
@@ -561,241 +573,331 @@ SV_DEVINL void partial_body(const Params& P, const Plan& pl, const float2* tab, 
     Bs = ff_warp_sum(ff_normalize(Bs));
   }
   if (lane == 0) {
-    float2* out = P.sub_part + (((size_t)b * P.nchunk + c) * kSubPerChunk + w) * 4;
-    out[0] = make_float2(Sq.hi, Sq.lo);
-    out[1] = make_float2(Sp.hi, Sp.lo);
-    out[2] = make_float2(A.hi, A.lo);
-    out[3] = make_float2(Bs.hi, Bs.lo);
+    float4* out = reinterpret_cast<float4*>(
+        P.sub_part + (((size_t)b * P.nchunk + c) * kSubPerChunk + w) * 4);
+    out[0] = make_float4(Sq.hi, Sq.lo, Sp.hi, Sp.lo);
+    out[1] = make_float4(A.hi, A.lo, Bs.hi, Bs.lo);
   }
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kSampleThreads) partials_kernel(Params P, int aligned) {
-  __shared__ float2 tab[256];
-  const long long b = blockIdx.x / P.nchunk;
-  const int c = (int)(blockIdx.x % P.nchunk);
-  const Plan pl = P.plans[b];
-  if (pl.mode == kModeFailed) return;
-  tab[threadIdx.x] = kSvExp2Table[threadIdx.x];
-  __syncthreads();
-  if (pl.mode == kModeResidual)
-    partial_body<DT, true>(P, pl, tab, aligned != 0, b, c);
-  else
-    partial_body<DT, false>(P, pl, tab, aligned != 0, b, c);
-}
+// ---------------------------------------------------------------- draw: finish of one sequence
+// All arithmetic here is float-float (fp32 pairs): fp64 throughput is low on
+// this part, and a block-wide fp64 operation costs as much as hundreds of
+// fp32 ones.
 
-// ---------------------------------------------------------------- 4. finish
+SV_DEVINL ff ff_of(float x, float y) { return {x, y}; }
 
-SV_DEVINL double ffd(float2 v) { return (double)v.x + (double)v.y; }
-
-SV_DEVINL double warp_sum_d(double x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
-// Block sum of doubles (256 threads); result in every thread.
-SV_DEVINL double block_sum_d(double x, double* red) {
-  x = warp_sum_d(x);
+// Block sum of float-float values; result in every thread.
+SV_DEVINL ff block_sum_ff(ff x, CtaShared& sh) {
+  x = ff_warp_sum(x);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
-  if (l == 0) red[w] = x;
+  if (l == 0) sh.red_f[w] = x;
   __syncthreads();
-  double t = 0.0;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
+  ff t{0.f, 0.f};
+  for (int i = 0; i < kWarps; ++i) t = ff_add(t, sh.red_f[i]);
   return t;
 }
 
-// Block exclusive prefix of doubles in thread order (256 threads).
-SV_DEVINL double block_exclusive_d(double x, double* red, double* total) {
+// Block exclusive prefix of float-float values in thread order.
+SV_DEVINL ff block_exclusive_ff(ff x, CtaShared& sh, ff* total) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  double inc = x;
+  ff inc = x;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (l >= o) inc += y;
+    const ff y = ff_shfl_up(inc, o);
+    if (l >= o) inc = ff_add(inc, y);
   }
+  ff exc = ff_shfl_up(inc, 1);
+  if (l == 0) exc = {0.f, 0.f};
   __syncthreads();
-  if (l == 31) red[w] = inc;
+  if (l == 31) sh.red_f[w] = inc;
   __syncthreads();
-  double base = 0.0, all = 0.0;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
-    if (i < w) base += red[i];
-    all += red[i];
+  ff base{0.f, 0.f}, all{0.f, 0.f};
+  for (int i = 0; i < kWarps; ++i) {
+    if (i < w) base = ff_add(base, sh.red_f[i]);
+    all = ff_add(all, sh.red_f[i]);
   }
   *total = all;
-  return base + inc - x;
+  return ff_add(base, exc);
+}
+
+// Weight of element e in the draw (0 outside the row or the positive set).
+template <int DT>
+SV_DEVINL ff draw_weight(const DrawRow& d, bool use_res, ff Sq, ff Sp, long long e, int V,
+                         const float2* tab) {
+  if (e >= V) return {0.f, 0.f};
+  const float lq = load_elem<DT>(d.rq, e);
+  ff eq, ep;
+  bool pos;
+  if (use_res) {
+    const float lp = load_elem<DT>(d.rp, e);
+    element_exps<true>(d, lq, lp, tab, eq, ep, pos);
+    return pos ? ff_sub(ff_mul(ff_normalize(eq), Sp), ff_mul(ff_normalize(ep), Sq))
+               : ff{0.f, 0.f};
+  }
+  element_exps<false>(d, lq, 0.f, tab, eq, ep, pos);
+  return ff_normalize(eq);
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kSampleThreads) finish_kernel(Params P, int aligned) {
-  __shared__ float2 tab[256];
-  __shared__ double red[kSampleThreads / 32];
-  __shared__ int s_g;
-  __shared__ double s_pref;
-  const long long b = blockIdx.x;
-  const Plan pl = P.plans[b];
-  if (pl.mode == kModeFailed) return;
+SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShared& sh) {
   const int tid = threadIdx.x;
-  tab[tid] = kSvExp2Table[tid];
-  if (tid == 0) s_g = INT_MAX;
-  __syncthreads();
-
   const int nsub = P.nchunk * kSubPerChunk;
-  const float2* part = P.sub_part + (size_t)b * nsub * 4;
+  const float4* part = reinterpret_cast<const float4*>(P.sub_part + (size_t)b * nsub * 4);
   const bool resid = pl.mode == kModeResidual;
-  const int run = (nsub + kSampleThreads - 1) / kSampleThreads;
+  const int run = (nsub + kThreads - 1) / kThreads;
   const int g0 = min(nsub, tid * run), g1 = min(nsub, g0 + run);
 
   // Totals over the row(s): S_q, S_p and the positive-set sums A, B.
-  double tq = 0, tp = 0, ta = 0, tb = 0;
+  ff tq{0.f, 0.f}, tp{0.f, 0.f}, ta{0.f, 0.f}, tb{0.f, 0.f};
   for (int g = g0; g < g1; ++g) {
-    tq += ffd(part[g * 4 + 0]);
+    const float4 x = __ldcg(part + 2 * g);
+    tq = ff_add(tq, ff_of(x.x, x.y));
     if (resid) {
-      tp += ffd(part[g * 4 + 1]);
-      ta += ffd(part[g * 4 + 2]);
-      tb += ffd(part[g * 4 + 3]);
+      const float4 y = __ldcg(part + 2 * g + 1);
+      tp = ff_add(tp, ff_of(x.z, x.w));
+      ta = ff_add(ta, ff_of(y.x, y.y));
+      tb = ff_add(tb, ff_of(y.z, y.w));
     }
   }
-  const double Sq = block_sum_d(tq, red);
-  double Sp = 0, A = 0, Bt = 0;
+  const ff Sq = block_sum_ff(tq, sh);
+  ff Sp{0.f, 0.f}, A{0.f, 0.f}, Bt{0.f, 0.f};
   if (resid) {
-    Sp = block_sum_d(tp, red);
-    A = block_sum_d(ta, red);
-    Bt = block_sum_d(tb, red);
+    Sp = block_sum_ff(tp, sh);
+    A = block_sum_ff(ta, sh);
+    Bt = block_sum_ff(tb, sh);
   }
   // Residual mass sum max(0, q - p), scaled by S_q S_p; zero -> fall back to q.
-  const bool use_res = resid && (Sp * A - Sq * Bt > 0.0);
-  auto mass = [&](int g) -> double {
-    return use_res ? Sp * ffd(part[g * 4 + 2]) - Sq * ffd(part[g * 4 + 3]) : ffd(part[g * 4 + 0]);
+  const bool use_res = resid && ff_sub(ff_mul(Sp, A), ff_mul(Sq, Bt)).hi > 0.f;
+  auto mass = [&](int g) -> ff {
+    if (use_res) {
+      const float4 y = __ldcg(part + 2 * g + 1);
+      return ff_sub(ff_mul(Sp, ff_of(y.x, y.y)), ff_mul(Sq, ff_of(y.z, y.w)));
+    }
+    const float4 x = __ldcg(part + 2 * g);
+    return ff_of(x.x, x.y);
   };
-  double run_sum = 0.0;
-  for (int g = g0; g < g1; ++g) run_sum += mass(g);
-  double total;
-  const double run_pref = block_exclusive_d(run_sum, red, &total);
-  const double tau = (double)pl.u * total;
+  ff run_sum{0.f, 0.f};
+  for (int g = g0; g < g1; ++g) run_sum = ff_add(run_sum, mass(g));
+  ff total;
+  const ff run_pref = block_exclusive_ff(run_sum, sh, &total);
+  const ff tau = ff_mul_f(total, pl.u);
 
   // First sub-chunk whose cumulative mass passes tau.
+  if (tid == 0) sh.g = INT_MAX;
+  __syncthreads();
   {
-    double cum = run_pref;
+    ff cum = run_pref;
     for (int g = g0; g < g1; ++g) {
-      const double mg = mass(g);
-      if (mg > 0.0 && cum + mg > tau) {
-        atomicMin(&s_g, g);
+      const ff mg = mass(g);
+      const ff next = ff_add(cum, mg);
+      if (mg.hi > 0.f && ff_gt(next, tau)) {
+        atomicMin(&sh.g, g);
         break;
       }
-      cum += mg;
+      cum = next;
     }
   }
   __syncthreads();
-  int gs = s_g;
-  bool last_mode = gs == INT_MAX;
+  int gs = sh.g;
+  const bool last_mode = gs == INT_MAX;
+  __syncthreads();
   if (last_mode) {
     // u * total reached the end (u = 1): the last sub-chunk with positive mass.
-    __syncthreads();
-    if (tid == 0) s_g = -1;
+    if (tid == 0) sh.g = -1;
     __syncthreads();
     for (int g = g1 - 1; g >= g0; --g) {
-      if (mass(g) > 0.0) {
-        atomicMax(&s_g, g);
+      if (mass(g).hi > 0.f) {
+        atomicMax(&sh.g, g);
         break;
       }
     }
     __syncthreads();
-    gs = s_g;
+    gs = sh.g;
   } else {
-    double cum = run_pref;
+    ff cum = run_pref;
     for (int g = g0; g < g1; ++g) {
-      if (g == gs) s_pref = cum;
-      cum += mass(g);
+      if (g == gs) sh.s_pref = cum;
+      cum = ff_add(cum, mass(g));
+    }
+    __syncthreads();
+  }
+  if (tid < 32 && gs >= 0) {
+    // Warp 0: exact search inside sub-chunk gs, 16 consecutive elements per lane.
+    const int lane = tid;
+    const DrawRow d = draw_row(P, pl);
+    const long long eb = (long long)gs * kSubElems + lane * 16;
+    ff lsum{0.f, 0.f};
+    for (int k = 0; k < 16; ++k)
+      lsum = ff_add(lsum, draw_weight<DT>(d, use_res, Sq, Sp, eb + k, P.V, sh.tab));
+    ff inc = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const ff y = ff_shfl_up(inc, o);
+      if (lane >= o) inc = ff_add(inc, y);
+    }
+    ff lpre = ff_shfl_up(inc, 1);
+    if (lane == 0) lpre = {0.f, 0.f};
+    int found = -1, lastk = -1;
+    ff wfound{0.f, 0.f}, wlast{0.f, 0.f};
+    ff cum = ff_add(sh.s_pref, lpre);
+    for (int k = 0; k < 16; ++k) {
+      const ff wk = draw_weight<DT>(d, use_res, Sq, Sp, eb + k, P.V, sh.tab);
+      cum = ff_add(cum, wk);
+      if (wk.hi > 0.f) {
+        lastk = k;
+        wlast = wk;
+        if (!last_mode && found < 0 && ff_gt(cum, tau)) {
+          found = k;
+          wfound = wk;
+        }
+      }
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
+    int token;
+    ff wt;
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      token = (int)((long long)gs * kSubElems + src * 16 + __shfl_sync(0xffffffffu, found, src));
+      wt = {__shfl_sync(0xffffffffu, wfound.hi, src), __shfl_sync(0xffffffffu, wfound.lo, src)};
+    } else {
+      // Last positive element of the sub-chunk (u = 1, or rounding at its end).
+      const unsigned any = __ballot_sync(0xffffffffu, lastk >= 0);
+      const int src = any ? 31 - __clz(any) : 0;
+      const int kk = __shfl_sync(0xffffffffu, lastk, src);
+      wt = {__shfl_sync(0xffffffffu, wlast.hi, src), __shfl_sync(0xffffffffu, wlast.lo, src)};
+      token = (int)((long long)gs * kSubElems + src * 16 + (kk < 0 ? 0 : kk));
+    }
+    if (lane == 0) {
+      P.out_tokens[b * (P.K + 1) + pl.j] = token;
+      if (P.dbg_prob) P.dbg_prob[b] = ff_to_double(wt) / ff_to_double(total);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- the persistent kernel
+
+struct Item {
+  bool stats;
+  long long b;
+  long long idx;
+};
+
+// Ticket -> work item: stats tickets of sequence s, then (after `lag`
+// sequences) the draw tickets of sequence s - lag.
+SV_DEVINL Item decode(const Params& P, unsigned long long t) {
+  const long long NS = P.ns, NP = P.np, L = P.lag, B = P.B;
+  const unsigned long long ph1 = (unsigned long long)(L * NS);
+  if (t < ph1) return {true, (long long)(t / NS), (long long)(t % NS)};
+  t -= ph1;
+  const unsigned long long ph2 = (unsigned long long)((B - L) * (NS + NP));
+  if (t < ph2) {
+    const long long s = L + (long long)(t / (NS + NP));
+    const long long o = (long long)(t % (NS + NP));
+    if (o < NS) return {true, s, o};
+    return {false, s - L, o - NS};
+  }
+  t -= ph2;
+  return {false, (B - L) + (long long)(t / NP), (long long)(t % NP)};
+}
+
+SV_DEVINL unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) verify_kernel(Params P) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ CtaShared sh;
+  const int tid = threadIdx.x;
+  sh.tab[tid] = kSvExp2Table[tid];
+  const unsigned long long total = (unsigned long long)P.B * (P.ns + P.np);
+  uint32_t piece = 0, issued = 0;  // consumed / issued ring pieces (thread 0 issues)
+  if (tid == 0) {
+    if (ALIGNED) {
+      for (int s = 0; s < kStages; ++s) mbar_init(&sh.full[s], 1);
+      fence_barrier_init();
+    }
+    // One ticket of lookahead: the next streaming unit's bytes are in flight
+    // while the current item is processed.
+    sh.next = atomicAdd(P.ticket, 1ull);
+    if (ALIGNED && sh.next < total) {
+      const Item it = decode(P, sh.next);
+      if (it.stats) stats_issue<DT>(P, it.b * P.ns + it.idx, ring, sh, issued);
     }
   }
   __syncthreads();
-  if (tid >= 32 || gs < 0) return;
-
-  // Warp 0: exact search inside sub-chunk gs, 16 consecutive elements per lane.
-  const int lane = tid;
-  DrawRow d;
-  d.rq = static_cast<const unsigned char*>(P.target) + (size_t)pl.row_q * P.V * P.es;
-  d.rp = resid ? static_cast<const unsigned char*>(P.draft) + (size_t)pl.row_p * P.V * P.es
-               : nullptr;
-  d.mq = pl.m_q;
-  d.mp = pl.m_p;
-  d.sq = pl.s_q;
-  d.sp = pl.s_p;
-  d.ih = P.ih;
-  d.il = P.il;
-  d.unit_t = P.unit_t != 0;
-  const long long eb = (long long)gs * kSubElems + lane * 16;
-  double wv[16];
-  double lsum = 0.0;
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const long long e = eb + k;
-    double wk = 0.0;
-    if (e < P.V) {
-      const float lq = load_elem<DT>(d.rq, e);
-      ff eq, ep;
-      bool pos;
-      if (use_res) {
-        const float lp = load_elem<DT>(d.rp, e);
-        element_exps<DT, true>(d, lq, lp, tab, eq, ep, pos);
-        if (pos) wk = ff_to_double(eq) * Sp - ff_to_double(ep) * Sq;
+  for (;;) {
+    const unsigned long long t = sh.next;
+    if (t >= total) break;
+    __syncthreads();  // everyone has read sh.next
+    if (tid == 0) {
+      const unsigned long long n = atomicAdd(P.ticket, 1ull);
+      sh.next = n;
+      if (ALIGNED && n < total) {
+        const Item nt = decode(P, n);
+        if (nt.stats) stats_issue<DT>(P, nt.b * P.ns + nt.idx, ring, sh, issued);
+      }
+    }
+    const Item it = decode(P, t);
+    const long long b = it.b;
+    if (it.stats) {
+      const long long u = b * P.ns + it.idx;
+      if constexpr (ALIGNED) {
+        if (!stats_consume_unit<DT>(P, u, ring, sh, piece)) {
+          if (tid == 0) {
+            atomicOr(P.status, kDevTimeout);
+            // The current segment's pieces and the prefetched ones may still be
+            // in flight: give them a bounded chance to land before exiting.
+            for (uint32_t q = piece >= 2 ? piece - 2 : 0; q < issued; ++q)
+              (void)mbar_wait(&sh.full[q % kStages], (q / kStages) & 1u);
+          }
+          return;
+        }
       } else {
-        element_exps<DT, false>(d, lq, 0.f, tab, eq, ep, pos);
-        wk = ff_to_double(eq);
+        stats_unit_plain<DT>(P, u, sh);
       }
-    }
-    wv[k] = wk;
-    lsum += wk;
-  }
-  double lpre = lsum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, lpre, o);
-    if (lane >= o) lpre += y;
-  }
-  lpre -= lsum;  // exclusive
-
-  int found = -1;
-  double wfound = 0.0;
-  if (!last_mode) {
-    double cum = s_pref + lpre;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      cum += wv[k];
-      if (found < 0 && wv[k] > 0.0 && cum > tau) {
-        found = k;
-        wfound = wv[k];
+      if (tid == 0) sh.flag = atomic_add_acq_rel(P.done_s + b, 1u) == (unsigned)(P.ns - 1);
+      __syncthreads();
+      if (sh.flag) scan_seq(P, b, sh);
+    } else {
+      if (tid == 0) {
+        if (wait_flag(P.ready + b)) {
+          const Plan* src = P.plans + b;
+          Plan pl;
+          pl.j = __ldcg(&src->j);
+          pl.mode = __ldcg(&src->mode);
+          pl.row_q = __ldcg(&src->row_q);
+          pl.row_p = __ldcg(&src->row_p);
+          pl.m_q = __ldcg(&src->m_q);
+          pl.m_p = __ldcg(&src->m_p);
+          pl.s_q = __ldcg(&src->s_q);
+          pl.s_p = __ldcg(&src->s_p);
+          pl.u = __ldcg(&src->u);
+          sh.plan = pl;
+        } else {
+          atomicOr(P.status, kDevTimeout);
+          sh.plan.mode = kModeFailed;
+        }
       }
+      __syncthreads();
+      const Plan pl = sh.plan;
+      if (pl.mode != kModeFailed) {
+        const DrawRow d = draw_row(P, pl);
+        if (pl.mode == kModeResidual)
+          partial_body<DT, true>(P, d, sh.tab, ALIGNED, b, (int)it.idx);
+        else
+          partial_body<DT, false>(P, d, sh.tab, ALIGNED, b, (int)it.idx);
+      }
+      __syncthreads();  // all partial writes of this CTA precede the release below
+      if (tid == 0) sh.flag = atomic_add_acq_rel(P.done_p + b, 1u) == (unsigned)(P.np - 1);
+      __syncthreads();
+      if (sh.flag && pl.mode != kModeFailed) finish_seq<DT>(P, b, pl, sh);
     }
-  }
-  unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
-  int token;
-  double wt;
-  if (hit) {
-    const int src = __ffs(hit) - 1;
-    token = (int)((long long)gs * kSubElems + src * 16 + __shfl_sync(0xffffffffu, found, src));
-    wt = __shfl_sync(0xffffffffu, wfound, src);
-  } else {
-    // Last positive element of the sub-chunk (u = 1, or rounding at its end).
-    int lastk = -1;
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-      if (wv[k] > 0.0) lastk = k;
-    const unsigned any = __ballot_sync(0xffffffffu, lastk >= 0);
-    const int src = any ? 31 - __clz(any) : 0;
-    const int kk = __shfl_sync(0xffffffffu, lastk, src);
-    double wl = 0.0;
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-      if (k == lastk) wl = wv[k];
-    wt = __shfl_sync(0xffffffffu, wl, src);
-    token = (int)((long long)gs * kSubElems + src * 16 + (kk < 0 ? 0 : kk));
-  }
-  if (lane == 0) {
-    P.out_tokens[b * (P.K + 1) + pl.j] = token;
-    if (P.dbg_prob) P.dbg_prob[b] = wt / total;
+    __syncthreads();
   }
 }
 
@@ -804,11 +906,22 @@ __global__ void __launch_bounds__(kSampleThreads) finish_kernel(Params P, int al
 namespace {
 struct DeviceInfo {
   int sms = 0;
-  int stats_blocks_per_sm = 0;
+  int blocks_per_sm[4] = {0, 0, 0, 0};
   bool ready = false;
 };
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
+
+template <int DT, bool AL>
+cudaError_t setup_kernel(int* occ) {
+  const int smem = AL ? kStages * kStageBytes : 0;
+  cudaError_t e = cudaFuncSetAttribute(verify_kernel<DT, AL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, verify_kernel<DT, AL>, kThreads, smem);
+  if (e == cudaSuccess && *occ < 1) *occ = 1;
+  return e;
+}
 }  // namespace
 
 cudaError_t prepare_device(int device) {
@@ -817,58 +930,57 @@ cudaError_t prepare_device(int device) {
   DeviceInfo& di = g_dev[device];
   if (di.ready) return cudaSuccess;
   cudaError_t e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, device);
+  if (e == cudaSuccess) e = setup_kernel<0, true>(&di.blocks_per_sm[0]);
+  if (e == cudaSuccess) e = setup_kernel<0, false>(&di.blocks_per_sm[1]);
+  if (e == cudaSuccess) e = setup_kernel<1, true>(&di.blocks_per_sm[2]);
+  if (e == cudaSuccess) e = setup_kernel<1, false>(&di.blocks_per_sm[3]);
   if (e != cudaSuccess) return e;
-  const int smem = kStages * kStageBytes;
-  e = cudaFuncSetAttribute(stats_tma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(stats_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, stats_tma_kernel<0>, kStatsThreads, smem);
-  if (e != cudaSuccess) return e;
-  di.stats_blocks_per_sm = occ > 0 ? occ : 1;
   di.ready = true;
   return cudaSuccess;
 }
 
-int kernels_per_call() { return 4; }
+int kernels_per_call() { return 1; }
 
-template <int DT>
-static cudaError_t launch_typed(const Params& P, bool aligned, cudaStream_t st, const DeviceInfo& di,
-                                const Events& ev) {
-  if (aligned) {
-    long long grid = (long long)di.sms * di.stats_blocks_per_sm;
-    if (grid > P.n_units) grid = P.n_units;
-    stats_tma_kernel<DT><<<(unsigned)grid, kStatsThreads, kStages * kStageBytes, st>>>(P);
-  } else {
-    long long grid = (long long)di.sms * 4;
-    if (grid > P.n_units) grid = P.n_units;
-    stats_plain_kernel<DT><<<(unsigned)grid, kStatsThreads, 0, st>>>(P);
-  }
-  if (ev.stats_done && cudaEventRecord(ev.stats_done, st) != cudaSuccess) return cudaGetLastError();
-  scan_kernel<<<(unsigned)P.B, kScanThreads, 0, st>>>(P);
-  partials_kernel<DT><<<(unsigned)((long long)P.B * P.nchunk), kSampleThreads, 0, st>>>(P, aligned ? 1 : 0);
-  finish_kernel<DT><<<(unsigned)P.B, kSampleThreads, 0, st>>>(P, aligned ? 1 : 0);
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess && ev.end) e = cudaEventRecord(ev.end, st);
-  return e;
-}
-
-cudaError_t launch_all(const Params& P, bool aligned, cudaStream_t st, const Events& ev) {
+cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev) {
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   e = prepare_device(device);
   if (e != cudaSuccess) return e;
+  const DeviceInfo& di = g_dev[device];
+  const int variant = (P.dtype == 0 ? 0 : 2) + (aligned ? 0 : 1);
+  long long grid = (long long)di.sms * di.blocks_per_sm[variant];
+  const long long tickets = (long long)P.B * (P.ns + P.np);
+  if (grid > tickets) grid = tickets;
+  // Draw tickets of sequence b follow its stats tickets by about one wave of
+  // the grid, so that its plan is normally ready when they are taken.
+  long long lag = (grid + P.ns - 1) / P.ns + 1;
+  P.lag = lag < P.B ? (int)lag : P.B;
+  e = cudaMemsetAsync(P.ctrl, 0, P.ctrl_bytes, st);
+  if (e != cudaSuccess) return e;
+  // External records, so that the events become timing nodes when the stream
+  // is being captured into a graph.
   if (ev.start) {
-    e = cudaEventRecord(ev.start, st);
+    e = cudaEventRecordWithFlags(ev.start, st, cudaEventRecordExternal);
     if (e != cudaSuccess) return e;
   }
-  e = cudaMemsetAsync(P.status, 0, sizeof(unsigned), st);
+  const int smem = aligned ? kStages * kStageBytes : 0;
+  if (P.dtype == 0) {
+    if (aligned)
+      verify_kernel<0, true><<<(unsigned)grid, kThreads, smem, st>>>(P);
+    else
+      verify_kernel<0, false><<<(unsigned)grid, kThreads, smem, st>>>(P);
+  } else {
+    if (aligned)
+      verify_kernel<1, true><<<(unsigned)grid, kThreads, smem, st>>>(P);
+    else
+      verify_kernel<1, false><<<(unsigned)grid, kThreads, smem, st>>>(P);
+  }
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const DeviceInfo& di = g_dev[device];
-  return P.dtype == 0 ? launch_typed<0>(P, aligned, st, di, ev)
-                      : launch_typed<1>(P, aligned, st, di, ev);
+  if (ev.stats_done) e = cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
+  if (e == cudaSuccess && ev.end) e = cudaEventRecordWithFlags(ev.end, st, cudaEventRecordExternal);
+  return e;
 }
 
 }  // namespace sv
