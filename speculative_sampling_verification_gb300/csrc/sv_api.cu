@@ -65,10 +65,12 @@ int run(const void* target, const void* draft, const int32_t* tokens, const floa
   P.ns = (long long)L.rows_per_seq * L.nseg;
   P.np = L.nchunk;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  // Control block: status (4 B), pad, ticket (8 B), then done_s, done_p, ready [B] each.
+  // Control block: status (4 B), abort (4 B), ticket (8 B), then done_s,
+  // done_p, ready [B] each; zeroed before every launch.
   P.ctrl = ws + L.off_ctrl;
   P.ctrl_bytes = L.ctrl_bytes;
   P.status = reinterpret_cast<unsigned*>(ws + L.off_ctrl);
+  P.abort = reinterpret_cast<unsigned*>(ws + L.off_ctrl + 4);
   P.ticket = reinterpret_cast<unsigned long long*>(ws + L.off_ctrl + 8);
   P.done_s = reinterpret_cast<unsigned*>(ws + L.off_ctrl + 16);
   P.done_p = P.done_s + B;

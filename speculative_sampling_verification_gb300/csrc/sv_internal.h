@@ -101,14 +101,14 @@ struct Params {
   int nseg, seg_elems;
   long long n_units;
   int nchunk;
-  long long ns;    // stats tickets per sequence ((2K+1) * nseg)
-  long long np;    // draw tickets per sequence (nchunk)
-  int lag;         // sequences between a sequence's stats and draw tickets
+  long long ns;    // streaming units per sequence ((2K+1) * nseg)
+  long long np;    // draw chunks per sequence (nchunk)
   void* ctrl;      // control block, zeroed before every launch
   size_t ctrl_bytes;
-  unsigned long long* ticket;
-  unsigned* done_s;  // [B] finished stats tickets
-  unsigned* done_p;  // [B] finished draw tickets
+  unsigned* abort;             // set by the first timed-out wait
+  unsigned long long* ticket;  // worker ticket counter
+  unsigned* done_s;  // [B] streamed units counted per sequence
+  unsigned* done_p;  // [B] draw chunks counted per sequence
   unsigned* ready;   // [B] plan published
   float2* seg_part;
   Plan* plans;

@@ -2,31 +2,35 @@
 // sampling: §4.2 and Algorithm 2 of "Accelerating Large Language Model
 // Decoding with Speculative Sampling", wikillm.com paper card).
 //
-// One persistent kernel per call. CTAs take tickets from a counter; a ticket
-// is one of two kinds of work item, dispensed in sequence-major order:
+// One cooperative persistent kernel per call, three CTAs per SM in two roles:
 //
-//   stats(b, u)   one segment of one of the 2K+1 logit rows of sequence b,
-//                 streamed HBM -> shared memory by 1-D bulk copies
-//                 (cp.async.bulk, mbarrier completion): per segment the
-//                 maximum m and sum_i 2^((l_i - m) log2(e)/T), the
-//                 temperature transform of §4.2 "Decoding transforms".
-//                 The CTA that completes the last segment of b runs the scan
-//                 of b: combine segments, gather the logits at the drafted
-//                 tokens, thresholds min(1, q/p) in fp64, first rejection j
-//                 (Algorithm 2 step 3), and publishes the plan of b.
-//   draw(b, c)    one 4096-element chunk of the row pair the draw of b needs
-//                 (target and draft row j for the residual (q - p)_+, or
-//                 target row K for the bonus token, Algorithm 2 step 4):
-//                 float-float sums of exp((l - m)/T) and of the residual's
-//                 positive part per 512-element sub-chunk. The CTA that
-//                 completes the last chunk of b runs the exact inverse-CDF
-//                 search and writes the drawn token.
+//   streamers (2 per SM)  walk a static, interleaved list of row segments
+//       (segment u goes to streamer u mod Gs, in sequence-major order, so
+//       sequences complete one after another). Thread 0 keeps a 4-stage ring
+//       of 16 KB shared-memory stages full with 1-D bulk copies
+//       (cp.async.bulk, mbarrier completion), across segment boundaries; all
+//       threads reduce each segment to its maximum m and
+//       sum_i 2^((l_i - m) log2(e)/T), the temperature transform of §4.2
+//       "Decoding transforms", then release-add one to the sequence's count.
+//       Streamers never wait on anything but their own copies.
+//   workers (1 per SM)    take tickets in sequence order, NP + 2 per sequence:
+//       scan(b)     once every segment of b is counted: combine segments,
+//                   gather the logits at the drafted tokens, thresholds
+//                   min(1, q/p) in fp64, first rejection j (Algorithm 2
+//                   step 3), publish the plan of b;
+//       draw(b, c)  one 4096-element chunk of the row pair the draw needs
+//                   (target and draft row j for the residual (q - p)_+, or
+//                   target row K for the bonus token, Algorithm 2 step 4):
+//                   float-float sums of exp((l - m)/T) and of the residual's
+//                   positive part per 512-element sub-chunk; the rows are
+//                   re-read while still in L2;
+//       finish(b)   once every chunk of b is counted: the exact inverse-CDF
+//                   search, in float-float, for the drawn token.
 //
-// draw(b, .) tickets come `lag` sequences after stats(b, .) tickets, so the
-// plan of b is normally ready when they are taken and the two rows they
-// re-read are still in L2; their float-float arithmetic overlaps the HBM
-// streaming of later sequences. A draw ticket never waits on a ticket handed
-// out after it, so the schedule cannot deadlock; every wait is bounded.
+// A worker waits only on streamers or on tickets handed out before its own,
+// and the cooperative launch keeps every CTA resident, so the kernel cannot
+// deadlock; every wait is bounded (200 ms of wall time) and reports a status
+// bit instead of hanging.
 #include <cfloat>
 #include <climits>
 #include <cstdint>
@@ -80,15 +84,11 @@ SV_DEVINL void st_release(unsigned* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Bounded wait for a flag another CTA sets (200 ms of wall time at most).
-SV_DEVINL bool wait_flag(const unsigned* p) {
-  if (ld_acquire(p)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    __nanosleep(100);
-    if (ld_acquire(p)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
+// Records a timed-out wait: the status bit, and the abort flag that makes
+// every later wait of this launch give up at once.
+SV_DEVINL void note_timeout(const Params& P) {
+  atomicOr(P.status, kDevTimeout);
+  atomicExch(P.abort, 1u);
 }
 
 // ---------------------------------------------------------------- per-CTA shared state
@@ -114,6 +114,19 @@ struct CtaShared {
 // A pair (m, s) stands for the sum s * 2^(m c2) of 2^(l_i c2) terms; s is
 // NaN when a NaN (or +inf) entry was seen; m = -inf with s = 0 means "no
 // finite entry yet".
+
+// Same with the accurate exp2f, for the few pairs the scan combines.
+SV_DEVINL void ms_combine_acc(float& m, float& s, float m2, float s2, float c2) {
+  const float M = fmaxf(m, m2);
+  if (M == neg_inf()) {
+    s = s + s2;
+    return;
+  }
+  const float a = (m == neg_inf()) ? 0.0f : exp2f((m - M) * c2);
+  const float b = (m2 == neg_inf()) ? 0.0f : exp2f((m2 - M) * c2);
+  s = s * a + s2 * b;
+  m = M;
+}
 
 SV_DEVINL void ms_combine(float& m, float& s, float m2, float s2, float c2) {
   const float M = fmaxf(m, m2);
@@ -243,66 +256,101 @@ SV_DEVINL const unsigned char* unit_row(const Params& P, long long u) {
   return row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
 }
 
-// Bulk-copy path, producer side (thread 0): issue the segment's 16 KB pieces
-// (at most two: segments are at most 32 KB) into the next ring stages.
-// `issued` counts pieces issued over the CTA's life.
-template <int DT>
-SV_DEVINL void stats_issue(const Params& P, long long u, unsigned char* ring, CtaShared& sh,
-                           uint32_t& issued) {
-  constexpr int kEs = DT == 0 ? 2 : 4;
-  constexpr int kStageElems = kStageBytes / kEs;
-  const int len = unit_len(P, u);
-  const int npieces = (len + kStageElems - 1) / kStageElems;
-  const unsigned char* src = unit_row(P, u) + (size_t)(u % P.nseg) * P.seg_elems * kEs;
-  for (int i = 0; i < npieces; ++i) {
-    const int st = (int)((issued + i) % kStages);
-    const int n = min(kStageElems, len - i * kStageElems);
-    const uint32_t bytes = (uint32_t)n * kEs;
-    mbar_arrive_expect_tx(&sh.full[st], bytes);
-    bulk_copy_g2s(ring + st * kStageBytes, src + (size_t)i * kStageBytes, bytes, &sh.full[st]);
-  }
-  issued += npieces;
+SV_DEVINL void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Bulk-copy path, consumer side (all threads): the segment's pieces are the
-// next ones in ring order. `piece` counts consumed pieces (mbarrier phases).
-// Returns false, with every thread agreeing, if a wait ran out.
+// Streamer, bulk-copy path. Streamer s of Gs owns units s, s+Gs, s+2Gs, ...
+// (sequence-major order, so sequences complete one after another). Thread 0
+// keeps the 4-stage ring full across unit boundaries; all threads consume
+// the pieces in order. After each unit thread 0 writes its (max, sum) pair
+// and adds 1 to the unit's sequence counter with release semantics.
 template <int DT>
-SV_DEVINL bool stats_consume_unit(const Params& P, long long u, const unsigned char* ring,
-                                  CtaShared& sh, uint32_t& piece) {
+SV_DEVINL void streamer_tma(const Params& P, long long s, long long Gs, unsigned char* ring,
+                            CtaShared& sh) {
   constexpr int kEs = DT == 0 ? 2 : 4;
   constexpr int kStageElems = kStageBytes / kEs;
   const int tid = threadIdx.x;
-  const int len = unit_len(P, u);
-  const int npieces = (len + kStageElems - 1) / kStageElems;
-  const float c2 = P.c2;
-  float m_run = neg_inf(), H = neg_inf();
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  bool nan_seen = false, timed_out = false;
-  const uint32_t fill = DT == 0 ? 0xff80ff80u : 0xff800000u;  // -inf
-  for (int i = 0; i < npieces; ++i) {
-    const uint32_t p = piece + i;
-    const int st = (int)(p % kStages);
-    if (!mbar_wait(&sh.full[st], (p / kStages) & 1u)) timed_out = true;
-    const unsigned char* buf = ring + st * kStageBytes;
-    const int nvec = min(kStageElems, len - i * kStageElems) * kEs / 16;
-    uint4 v[kVecPerThread];
-#pragma unroll
-    for (int k = 0; k < kVecPerThread; ++k) {
-      const int idx = tid + k * kThreads;
-      v[k] = idx < nvec ? ld_shared_v4(buf + idx * 16) : make_uint4(fill, fill, fill, fill);
+  const long long n_units = P.n_units;
+  if (s >= n_units) return;
+  // Producer cursor (thread 0): next piece = unit pu, element offset poff.
+  long long pu = s;
+  int poff = 0;
+  uint32_t issued = 0;
+  auto issue = [&]() {
+    if (pu >= n_units) return;
+    const int len = unit_len(P, pu);
+    const int n = min(kStageElems, len - poff);
+    const int st = (int)(issued % kStages);
+    const unsigned char* src =
+        unit_row(P, pu) + ((size_t)(pu % P.nseg) * P.seg_elems + poff) * kEs;
+    const uint32_t bytes = (uint32_t)n * kEs;
+    mbar_arrive_expect_tx(&sh.full[st], bytes);
+    bulk_copy_g2s(ring + st * kStageBytes, src, bytes, &sh.full[st]);
+    ++issued;
+    poff += n;
+    if (poff >= len) {
+      pu += Gs;
+      poff = 0;
     }
-    stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
+  };
+  if (tid == 0)
+    for (int i = 0; i < kStages; ++i) issue();
+
+  const float c2 = P.c2;
+  const uint32_t fill = DT == 0 ? 0xff80ff80u : 0xff800000u;  // -inf
+  uint32_t piece = 0;
+  for (long long u = s; u < n_units; u += Gs) {
+    const int len = unit_len(P, u);
+    float m_run = neg_inf(), H = neg_inf();
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    bool nan_seen = false, timed_out = false;
+    for (int off = 0; off < len; off += kStageElems) {
+      const int st = (int)(piece % kStages);
+      if (!mbar_wait(&sh.full[st], (piece / kStages) & 1u)) timed_out = true;
+      const unsigned char* buf = ring + st * kStageBytes;
+      const int nvec = min(kStageElems, len - off) * kEs / 16;
+      uint4 v[kVecPerThread];
+#pragma unroll
+      for (int k = 0; k < kVecPerThread; ++k) {
+        const int idx = tid + k * kThreads;
+        v[k] = idx < nvec ? ld_shared_v4(buf + idx * 16) : make_uint4(fill, fill, fill, fill);
+      }
+      stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
+      ++piece;
+      // Everyone is done with this stage; a timed-out wait anywhere aborts.
+      if (__syncthreads_or(timed_out)) {
+        if (tid == 0) {
+          note_timeout(P);
+          for (uint32_t q = piece - 1; q < issued; ++q)  // let copies in flight land
+            (void)mbar_wait(&sh.full[q % kStages], (q / kStages) & 1u);
+        }
+        return;
+      }
+      if (tid == 0) issue();
+    }
+    float sum = thread_sum(m_run, H, acc, nan_seen, c2);
+    float m = m_run;
+    block_combine(m, sum, c2, sh);
+    if (tid == 0) {
+      P.seg_part[u] = make_float2(m, sum);
+      red_release_add(P.done_s + u / P.ns, 1u);
+    }
   }
-  piece += npieces;
-  float s = thread_sum(m_run, H, acc, nan_seen, c2);
-  float m = m_run;
-  block_combine(m, s, c2, sh);  // its barriers also free the segment's stages
-  if (tid == 0) P.seg_part[u] = make_float2(m, s);
-  return !__syncthreads_or(timed_out);
 }
 
 // Plain-load path for rows that are not 16-byte aligned: two passes (max, sum).
+template <int DT>
+SV_DEVINL void stats_unit_plain(const Params& P, long long u, CtaShared& sh);
+
+template <int DT>
+SV_DEVINL void streamer_plain(const Params& P, long long s, long long Gs, CtaShared& sh) {
+  for (long long u = s; u < P.n_units; u += Gs) {
+    stats_unit_plain<DT>(P, u, sh);
+    if (threadIdx.x == 0) red_release_add(P.done_s + u / P.ns, 1u);
+  }
+}
+
 template <int DT>
 SV_DEVINL void stats_unit_plain(const Params& P, long long u, CtaShared& sh) {
   const float c2 = P.c2;
@@ -338,33 +386,41 @@ SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
   }
   __syncthreads();
 
-  // Row statistics: m = max over segments, S = sum of rescaled segment sums
-  // (one pass, rescaling the running sum when the maximum grows).
-  for (int r = tid; r < R; r += kThreads) {
-    const float2* part = P.seg_part + ((long long)b * R + r) * P.nseg;
-    float m = neg_inf();
-    double S = 0.0;
-    bool nan_seen = false;
-    for (int g = 0; g < P.nseg; ++g) {
-      const float2 ps = __ldcg(part + g);
-      nan_seen |= (ps.y != ps.y);
-      if (ps.x == neg_inf()) continue;
-      if (ps.x > m) {
-        if (m != neg_inf()) S *= (double)exp2f((m - ps.x) * P.c2);
-        m = ps.x;
+  // Row statistics, one warp per row: lanes load the row's segment pairs in
+  // parallel, combine them as (max, sum) pairs, and lane 0 forms
+  // lse = m/T + ln S in fp64.
+  {
+    const int w = tid >> 5, lane = tid & 31;
+    for (int r = w; r < R; r += kWarps) {
+      const float2* part = P.seg_part + ((long long)b * R + r) * P.nseg;
+      float m = neg_inf(), sum = 0.f;
+      bool nan_seen = false;
+      for (int g = lane; g < P.nseg; g += 32) {
+        const float2 ps = __ldcg(part + g);
+        nan_seen |= (ps.y != ps.y);
+        ms_combine_acc(m, sum, ps.x, ps.y, P.c2);
       }
-      S += (double)ps.y * (double)exp2f((ps.x - m) * P.c2);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+        ms_combine_acc(m, sum, m2, s2, P.c2);
+      }
+      nan_seen = __any_sync(0xffffffffu, nan_seen);
+      if (lane == 0) {
+        unsigned bits = 0;
+        if (nan_seen || sum != sum) {
+          bits = kDevNonfinite;
+        } else if (m == neg_inf()) {
+          bits = kDevEmptyRow;
+        }
+        if (bits) atomicOr(&sh.bits, bits);
+        sh.s_m[r] = m;
+        sh.s_s[r] = sum;
+        sh.s_lse[r] =
+            bits ? __longlong_as_double(0x7ff8000000000000LL) : (double)m * P.inv_t + log((double)sum);
+      }
     }
-    unsigned bits = 0;
-    if (nan_seen) {
-      bits = kDevNonfinite;
-    } else if (m == neg_inf()) {
-      bits = kDevEmptyRow;
-    }
-    if (bits) atomicOr(&sh.bits, bits);
-    sh.s_m[r] = m;
-    sh.s_s[r] = (float)S;
-    sh.s_lse[r] = bits ? __longlong_as_double(0x7ff8000000000000LL) : (double)m * P.inv_t + log(S);
   }
   for (int t = tid; t < K; t += kThreads) {
     const int x = sh.s_tok[t];
@@ -622,26 +678,9 @@ SV_DEVINL ff block_exclusive_ff(ff x, CtaShared& sh, ff* total) {
   return ff_add(base, exc);
 }
 
-// Weight of element e in the draw (0 outside the row or the positive set).
 template <int DT>
-SV_DEVINL ff draw_weight(const DrawRow& d, bool use_res, ff Sq, ff Sp, long long e, int V,
-                         const float2* tab) {
-  if (e >= V) return {0.f, 0.f};
-  const float lq = load_elem<DT>(d.rq, e);
-  ff eq, ep;
-  bool pos;
-  if (use_res) {
-    const float lp = load_elem<DT>(d.rp, e);
-    element_exps<true>(d, lq, lp, tab, eq, ep, pos);
-    return pos ? ff_sub(ff_mul(ff_normalize(eq), Sp), ff_mul(ff_normalize(ep), Sq))
-               : ff{0.f, 0.f};
-  }
-  element_exps<false>(d, lq, 0.f, tab, eq, ep, pos);
-  return ff_normalize(eq);
-}
-
-template <int DT>
-SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShared& sh) {
+SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShared& sh,
+                          bool aligned) {
   const int tid = threadIdx.x;
   const int nsub = P.nchunk * kSubPerChunk;
   const float4* part = reinterpret_cast<const float4*>(P.sub_part + (size_t)b * nsub * 4);
@@ -678,8 +717,31 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
     const float4 x = __ldcg(part + 2 * g);
     return ff_of(x.x, x.y);
   };
+  // Masses of this thread's sub-chunks, kept in registers when there are few
+  // (V up to 2^19); otherwise re-read from L2 on each pass.
+  constexpr int kCache = 4;
+  ff mcache[kCache];
+  const bool cached = run <= kCache;
   ff run_sum{0.f, 0.f};
-  for (int g = g0; g < g1; ++g) run_sum = ff_add(run_sum, mass(g));
+  for (int g = g0; g < g1; ++g) {
+    const ff mg = mass(g);
+    if (cached) {
+#pragma unroll
+      for (int i = 0; i < kCache; ++i)
+        if (g - g0 == i) mcache[i] = mg;
+    }
+    run_sum = ff_add(run_sum, mg);
+  }
+  auto mass_c = [&](int g) -> ff {
+    if (cached) {
+      ff v{0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < kCache; ++i)
+        if (g - g0 == i) v = mcache[i];
+      return v;
+    }
+    return mass(g);
+  };
   ff total;
   const ff run_pref = block_exclusive_ff(run_sum, sh, &total);
   const ff tau = ff_mul_f(total, pl.u);
@@ -690,7 +752,7 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
   {
     ff cum = run_pref;
     for (int g = g0; g < g1; ++g) {
-      const ff mg = mass(g);
+      const ff mg = mass_c(g);
       const ff next = ff_add(cum, mg);
       if (mg.hi > 0.f && ff_gt(next, tau)) {
         atomicMin(&sh.g, g);
@@ -708,7 +770,7 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
     if (tid == 0) sh.g = -1;
     __syncthreads();
     for (int g = g1 - 1; g >= g0; --g) {
-      if (mass(g).hi > 0.f) {
+      if (mass_c(g).hi > 0.f) {
         atomicMax(&sh.g, g);
         break;
       }
@@ -719,167 +781,130 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
     ff cum = run_pref;
     for (int g = g0; g < g1; ++g) {
       if (g == gs) sh.s_pref = cum;
-      cum = ff_add(cum, mass(g));
+      cum = ff_add(cum, mass_c(g));
     }
     __syncthreads();
   }
-  if (tid < 32 && gs >= 0) {
-    // Warp 0: exact search inside sub-chunk gs, 16 consecutive elements per lane.
-    const int lane = tid;
-    const DrawRow d = draw_row(P, pl);
-    const long long eb = (long long)gs * kSubElems + lane * 16;
-    ff lsum{0.f, 0.f};
-    for (int k = 0; k < 16; ++k)
-      lsum = ff_add(lsum, draw_weight<DT>(d, use_res, Sq, Sp, eb + k, P.V, sh.tab));
-    ff inc = lsum;
+  if (gs < 0) return;
+  // Exact search inside sub-chunk gs: two consecutive elements per thread.
+  const DrawRow d = draw_row(P, pl);
+  const long long e0 = (long long)gs * kSubElems + 2 * tid;
+  ff w[2];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const ff y = ff_shfl_up(inc, o);
-      if (lane >= o) inc = ff_add(inc, y);
-    }
-    ff lpre = ff_shfl_up(inc, 1);
-    if (lane == 0) lpre = {0.f, 0.f};
-    int found = -1, lastk = -1;
-    ff wfound{0.f, 0.f}, wlast{0.f, 0.f};
-    ff cum = ff_add(sh.s_pref, lpre);
-    for (int k = 0; k < 16; ++k) {
-      const ff wk = draw_weight<DT>(d, use_res, Sq, Sp, eb + k, P.V, sh.tab);
-      cum = ff_add(cum, wk);
-      if (wk.hi > 0.f) {
-        lastk = k;
-        wlast = wk;
-        if (!last_mode && found < 0 && ff_gt(cum, tau)) {
-          found = k;
-          wfound = wk;
-        }
+  for (int k = 0; k < 2; ++k) {
+    const long long e = e0 + k;
+    w[k] = {0.f, 0.f};
+    if (e < P.V) {
+      const float lq = load_elem<DT>(d.rq, e);
+      ff eq, ep;
+      bool pos;
+      if (use_res) {
+        const float lp = load_elem<DT>(d.rp, e);
+        element_exps<true>(d, lq, lp, sh.tab, eq, ep, pos);
+        if (pos) w[k] = ff_sub(ff_mul(ff_normalize(eq), Sp), ff_mul(ff_normalize(ep), Sq));
+      } else {
+        element_exps<false>(d, lq, 0.f, sh.tab, eq, ep, pos);
+        w[k] = ff_normalize(eq);
       }
     }
-    const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
-    int token;
-    ff wt;
-    if (hit) {
-      const int src = __ffs(hit) - 1;
-      token = (int)((long long)gs * kSubElems + src * 16 + __shfl_sync(0xffffffffu, found, src));
-      wt = {__shfl_sync(0xffffffffu, wfound.hi, src), __shfl_sync(0xffffffffu, wfound.lo, src)};
-    } else {
-      // Last positive element of the sub-chunk (u = 1, or rounding at its end).
-      const unsigned any = __ballot_sync(0xffffffffu, lastk >= 0);
-      const int src = any ? 31 - __clz(any) : 0;
-      const int kk = __shfl_sync(0xffffffffu, lastk, src);
-      wt = {__shfl_sync(0xffffffffu, wlast.hi, src), __shfl_sync(0xffffffffu, wlast.lo, src)};
-      token = (int)((long long)gs * kSubElems + src * 16 + (kk < 0 ? 0 : kk));
-    }
-    if (lane == 0) {
-      P.out_tokens[b * (P.K + 1) + pl.j] = token;
-      if (P.dbg_prob) P.dbg_prob[b] = ff_to_double(wt) / ff_to_double(total);
-    }
+  }
+  ff unused;
+  const ff tpre = block_exclusive_ff(ff_add(w[0], w[1]), sh, &unused);
+  if (tid == 0) {
+    sh.g = INT_MAX;
+    sh.j = -1;
+  }
+  __syncthreads();
+  ff cum = ff_add(sh.s_pref, tpre);
+  int found = -1;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    cum = ff_add(cum, w[k]);
+    if (!last_mode && found < 0 && w[k].hi > 0.f && ff_gt(cum, tau)) found = k;
+  }
+  if (found >= 0) atomicMin(&sh.g, 2 * tid + found);
+  const int lastk = w[1].hi > 0.f ? 1 : (w[0].hi > 0.f ? 0 : -1);
+  if (lastk >= 0) atomicMax(&sh.j, 2 * tid + lastk);
+  __syncthreads();
+  // The first element whose cumulative weight passes tau; else (u = 1, or
+  // rounding at the sub-chunk's end) the last positive element.
+  const int pick = sh.g != INT_MAX ? sh.g : sh.j;
+  if (pick >= 0 && pick / 2 == tid) {
+    const ff wt = w[pick & 1];
+    P.out_tokens[b * (P.K + 1) + pl.j] = (int)((long long)gs * kSubElems + pick);
+    if (P.dbg_prob) P.dbg_prob[b] = ff_to_double(wt) / ff_to_double(total);
   }
 }
 
 // ---------------------------------------------------------------- the persistent kernel
 
-struct Item {
-  bool stats;
-  long long b;
-  long long idx;
-};
-
-// Ticket -> work item: stats tickets of sequence s, then (after `lag`
-// sequences) the draw tickets of sequence s - lag.
-SV_DEVINL Item decode(const Params& P, unsigned long long t) {
-  const long long NS = P.ns, NP = P.np, L = P.lag, B = P.B;
-  const unsigned long long ph1 = (unsigned long long)(L * NS);
-  if (t < ph1) return {true, (long long)(t / NS), (long long)(t % NS)};
-  t -= ph1;
-  const unsigned long long ph2 = (unsigned long long)((B - L) * (NS + NP));
-  if (t < ph2) {
-    const long long s = L + (long long)(t / (NS + NP));
-    const long long o = (long long)(t % (NS + NP));
-    if (o < NS) return {true, s, o};
-    return {false, s - L, o - NS};
-  }
-  t -= ph2;
-  return {false, (B - L) + (long long)(t / NP), (long long)(t % NP)};
-}
-
-SV_DEVINL unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-template <int DT, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) verify_kernel(Params P) {
-  extern __shared__ __align__(128) unsigned char ring[];
-  __shared__ CtaShared sh;
-  const int tid = threadIdx.x;
-  sh.tab[tid] = kSvExp2Table[tid];
-  const unsigned long long total = (unsigned long long)P.B * (P.ns + P.np);
-  uint32_t piece = 0, issued = 0;  // consumed / issued ring pieces (thread 0 issues)
-  if (tid == 0) {
-    if (ALIGNED) {
-      for (int s = 0; s < kStages; ++s) mbar_init(&sh.full[s], 1);
-      fence_barrier_init();
-    }
-    // One ticket of lookahead: the next streaming unit's bytes are in flight
-    // while the current item is processed.
-    sh.next = atomicAdd(P.ticket, 1ull);
-    if (ALIGNED && sh.next < total) {
-      const Item it = decode(P, sh.next);
-      if (it.stats) stats_issue<DT>(P, it.b * P.ns + it.idx, ring, sh, issued);
-    }
-  }
-  __syncthreads();
+// Bounded wait until a counter another CTA increments reaches `target`.
+// Gives up after 200 ms of wall time, or at once once the launch is aborting.
+SV_DEVINL bool wait_count(const Params& P, const unsigned* p, unsigned target) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = global_ns();
   for (;;) {
-    const unsigned long long t = sh.next;
-    if (t >= total) break;
-    __syncthreads();  // everyone has read sh.next
-    if (tid == 0) {
-      const unsigned long long n = atomicAdd(P.ticket, 1ull);
-      sh.next = n;
-      if (ALIGNED && n < total) {
-        const Item nt = decode(P, n);
-        if (nt.stats) stats_issue<DT>(P, nt.b * P.ns + nt.idx, ring, sh, issued);
-      }
+    __nanosleep(64);
+    if (ld_acquire(p) >= target) return true;
+    if (ld_acquire(P.abort) != 0u) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      note_timeout(P);
+      return false;
     }
-    const Item it = decode(P, t);
-    const long long b = it.b;
-    if (it.stats) {
-      const long long u = b * P.ns + it.idx;
-      if constexpr (ALIGNED) {
-        if (!stats_consume_unit<DT>(P, u, ring, sh, piece)) {
-          if (tid == 0) {
-            atomicOr(P.status, kDevTimeout);
-            // The current segment's pieces and the prefetched ones may still be
-            // in flight: give them a bounded chance to land before exiting.
-            for (uint32_t q = piece >= 2 ? piece - 2 : 0; q < issued; ++q)
-              (void)mbar_wait(&sh.full[q % kStages], (q / kStages) & 1u);
-          }
-          return;
-        }
-      } else {
-        stats_unit_plain<DT>(P, u, sh);
-      }
-      if (tid == 0) sh.flag = atomic_add_acq_rel(P.done_s + b, 1u) == (unsigned)(P.ns - 1);
+  }
+}
+
+SV_DEVINL Plan load_plan(const Plan* src) {
+  Plan pl;
+  pl.j = __ldcg(&src->j);
+  pl.mode = __ldcg(&src->mode);
+  pl.row_q = __ldcg(&src->row_q);
+  pl.row_p = __ldcg(&src->row_p);
+  pl.m_q = __ldcg(&src->m_q);
+  pl.m_p = __ldcg(&src->m_p);
+  pl.s_q = __ldcg(&src->s_q);
+  pl.s_p = __ldcg(&src->s_p);
+  pl.u = __ldcg(&src->u);
+  return pl;
+}
+
+// Worker: tickets in sequence order, (NP + 2) per sequence b:
+//   scan(b)      waits until all streaming units of b are counted, then scans;
+//   draw(b, c)   waits for the plan of b, then sums one chunk of the draw row(s);
+//   finish(b)    waits until all draw chunks of b are counted, then searches.
+// Each wait is on streamers (which never wait) or on an earlier ticket.
+template <int DT, bool ALIGNED>
+SV_DEVINL void worker(const Params& P, CtaShared& sh) {
+  const int tid = threadIdx.x;
+  const long long per = P.np + 2;
+  const unsigned long long total = (unsigned long long)P.B * per;
+  for (;;) {
+    if (tid == 0) sh.ticket = atomicAdd(P.ticket, 1ull);
+    __syncthreads();
+    const unsigned long long t = sh.ticket;
+    __syncthreads();
+    if (t >= total) return;
+    const long long b = (long long)(t / per);
+    const long long k = (long long)(t % per);
+    if (k == 0) {
+      if (tid == 0) sh.flag = wait_count(P, P.done_s + b, (unsigned)P.ns);
       __syncthreads();
-      if (sh.flag) scan_seq(P, b, sh);
-    } else {
+      if (sh.flag) {
+        __threadfence();
+        scan_seq(P, b, sh);
+      } else if (tid == 0) {
+        Plan pl{};
+        pl.j = -1;
+        pl.mode = kModeFailed;
+        P.plans[b] = pl;
+        __threadfence();
+        st_release(P.ready + b, 1u);
+      }
+    } else if (k <= P.np) {
       if (tid == 0) {
-        if (wait_flag(P.ready + b)) {
-          const Plan* src = P.plans + b;
-          Plan pl;
-          pl.j = __ldcg(&src->j);
-          pl.mode = __ldcg(&src->mode);
-          pl.row_q = __ldcg(&src->row_q);
-          pl.row_p = __ldcg(&src->row_p);
-          pl.m_q = __ldcg(&src->m_q);
-          pl.m_p = __ldcg(&src->m_p);
-          pl.s_q = __ldcg(&src->s_q);
-          pl.s_p = __ldcg(&src->s_p);
-          pl.u = __ldcg(&src->u);
-          sh.plan = pl;
+        if (wait_count(P, P.ready + b, 1u)) {
+          sh.plan = load_plan(P.plans + b);
         } else {
-          atomicOr(P.status, kDevTimeout);
           sh.plan.mode = kModeFailed;
         }
       }
@@ -888,16 +913,57 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) verify_kernel(Params P) 
       if (pl.mode != kModeFailed) {
         const DrawRow d = draw_row(P, pl);
         if (pl.mode == kModeResidual)
-          partial_body<DT, true>(P, d, sh.tab, ALIGNED, b, (int)it.idx);
+          partial_body<DT, true>(P, d, sh.tab, ALIGNED, b, (int)(k - 1));
         else
-          partial_body<DT, false>(P, d, sh.tab, ALIGNED, b, (int)it.idx);
+          partial_body<DT, false>(P, d, sh.tab, ALIGNED, b, (int)(k - 1));
       }
       __syncthreads();  // all partial writes of this CTA precede the release below
-      if (tid == 0) sh.flag = atomic_add_acq_rel(P.done_p + b, 1u) == (unsigned)(P.np - 1);
+      if (tid == 0) red_release_add(P.done_p + b, 1u);
+    } else {
+      if (tid == 0) {
+        if (wait_count(P, P.done_p + b, (unsigned)P.np) && wait_count(P, P.ready + b, 1u)) {
+          sh.plan = load_plan(P.plans + b);
+        } else {
+          sh.plan.mode = kModeFailed;
+        }
+      }
       __syncthreads();
-      if (sh.flag && pl.mode != kModeFailed) finish_seq<DT>(P, b, pl, sh);
+      const Plan pl = sh.plan;
+      if (pl.mode != kModeFailed) {
+        __threadfence();
+        finish_seq<DT>(P, b, pl, sh, ALIGNED);
+      }
     }
     __syncthreads();
+  }
+}
+
+// Every third CTA (blockIdx % 3 == 2) is a worker, the others stream; with
+// three CTAs per SM this places one worker on each SM whether consecutive
+// blocks share an SM or are spread round-robin.
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) verify_kernel(Params P) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ CtaShared sh;
+  const int tid = threadIdx.x;
+  sh.tab[tid] = kSvExp2Table[tid];
+  if (ALIGNED && tid == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(&sh.full[st], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const long long bid = blockIdx.x;
+  const bool is_worker = (bid % 3) == 2;
+  if (is_worker) {
+    worker<DT, ALIGNED>(P, sh);
+  } else {
+    const long long s = (bid / 3) * 2 + (bid % 3);
+    const long long G = gridDim.x;
+    const long long Gs = (G / 3) * 2 + min(G % 3, 2LL);
+    if constexpr (ALIGNED)
+      streamer_tma<DT>(P, s, Gs, ring, sh);
+    else
+      streamer_plain<DT>(P, s, Gs, sh);
   }
 }
 
@@ -949,13 +1015,10 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
   if (e != cudaSuccess) return e;
   const DeviceInfo& di = g_dev[device];
   const int variant = (P.dtype == 0 ? 0 : 2) + (aligned ? 0 : 1);
-  long long grid = (long long)di.sms * di.blocks_per_sm[variant];
-  const long long tickets = (long long)P.B * (P.ns + P.np);
-  if (grid > tickets) grid = tickets;
-  // Draw tickets of sequence b follow its stats tickets by about one wave of
-  // the grid, so that its plan is normally ready when they are taken.
-  long long lag = (grid + P.ns - 1) / P.ns + 1;
-  P.lag = lag < P.B ? (int)lag : P.B;
+  // All CTAs must be resident at once (workers wait on streamers), so the
+  // grid is exactly what fits and the launch is cooperative.
+  const int grid = di.sms * di.blocks_per_sm[variant];
+  if (grid < 3) return cudaErrorInvalidConfiguration;
   e = cudaMemsetAsync(P.ctrl, 0, P.ctrl_bytes, st);
   if (e != cudaSuccess) return e;
   // External records, so that the events become timing nodes when the stream
@@ -964,19 +1027,22 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
     e = cudaEventRecordWithFlags(ev.start, st, cudaEventRecordExternal);
     if (e != cudaSuccess) return e;
   }
-  const int smem = aligned ? kStages * kStageBytes : 0;
-  if (P.dtype == 0) {
-    if (aligned)
-      verify_kernel<0, true><<<(unsigned)grid, kThreads, smem, st>>>(P);
-    else
-      verify_kernel<0, false><<<(unsigned)grid, kThreads, smem, st>>>(P);
-  } else {
-    if (aligned)
-      verify_kernel<1, true><<<(unsigned)grid, kThreads, smem, st>>>(P);
-    else
-      verify_kernel<1, false><<<(unsigned)grid, kThreads, smem, st>>>(P);
-  }
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = aligned ? kStages * kStageBytes : 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (P.dtype == 0)
+    e = aligned ? cudaLaunchKernelEx(&cfg, verify_kernel<0, true>, P)
+                : cudaLaunchKernelEx(&cfg, verify_kernel<0, false>, P);
+  else
+    e = aligned ? cudaLaunchKernelEx(&cfg, verify_kernel<1, true>, P)
+                : cudaLaunchKernelEx(&cfg, verify_kernel<1, false>, P);
   if (e != cudaSuccess) return e;
   if (ev.stats_done) e = cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
   if (e == cudaSuccess && ev.end) e = cudaEventRecordWithFlags(ev.end, st, cudaEventRecordExternal);
