@@ -59,8 +59,12 @@ enum {
   SV_ERR_DTYPE = 4,       /* dtype is neither SV_BF16 nor SV_F32 */
   SV_ERR_ALIGN = 5,       /* a pointer is not aligned to its element (workspace: 256 bytes) */
   SV_ERR_WORKSPACE = 6,   /* workspace_bytes below sv_workspace_size(), or staging too small */
-  SV_ERR_CUDA = 7         /* a CUDA runtime call failed */
+  SV_ERR_CUDA = 7,        /* a CUDA runtime call failed */
+  SV_ERR_SCRATCH_LIMIT = 8 /* spec_verify_static: the problem needs more than its fixed scratch */
 };
+
+/* Size of the fixed device scratch array behind spec_verify_static. */
+#define SV_STATIC_SCRATCH_BYTES (8u << 20)
 
 /* Device-side status bits, OR-ed into the status word of the workspace. A
  * sequence that raises one of the first four gets out_tokens[b, :] = -1 and
@@ -140,6 +144,32 @@ int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
                      int V, int dtype, float temperature, int32_t* h_out_tokens,
                      int32_t* h_n_accepted, void* staging, size_t staging_bytes,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* spec_verify for callers that cannot allocate device memory (the paper has no
+ * counterpart to this; it is a property of this library only). Some callers
+ * cannot provide a workspace: code running during stream capture in the global
+ * or thread-local mode (where cudaMalloc is not allowed), plugins whose device
+ * memory must all come from a host framework's pool, and latency-critical loops
+ * where cudaMalloc may stall the device. This entry point allocates nothing and
+ * takes no workspace: its scratch is one fixed array of SV_STATIC_SCRATCH_BYTES
+ * (8 MiB) of device memory inside the library, which every GPU that loads the
+ * library holds until the process exits.
+ *
+ * Arguments, layouts and results are those of spec_verify. Problems whose
+ * sv_workspace_size exceeds SV_STATIC_SCRATCH_BYTES are rejected with
+ * SV_ERR_SCRATCH_LIMIT and nothing is enqueued. Every call on a device shares
+ * that device's array, which keeps the previous call's contents; each call
+ * clears what must start at zero itself. Calls that overlap on the GPU (on
+ * different streams, or from different threads) race on the array and must
+ * be serialised by the caller. The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current) and
+ * sets kernel attributes; make it before any stream capture. Device status
+ * bits are not readable for these calls (there is no workspace to read them
+ * from); failed sequences still show as -1 outputs and n_accepted = -1. */
+int spec_verify_static(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                       int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
+                       void* stream);
 
 /* Reads the device status word of the last call that used `workspace`: waits
  * for `stream`, then stores the OR of the SV_DEV_* bits in *status. */

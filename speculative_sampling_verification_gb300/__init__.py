@@ -24,7 +24,8 @@ __all__ = [
     "SV_BF16", "SV_F32", "StatusError", "load_library", "sv_workspace_size", "sv_staging_size",
     "spec_verify", "spec_verify_debug", "spec_verify_profiled", "spec_verify_host",
     "sv_read_device_status",
-    "sv_status_string", "sv_kernels_per_call", "verify", "EXPORTED_SYMBOLS",
+    "sv_status_string", "sv_kernels_per_call", "spec_verify_static", "verify",
+    "EXPORTED_SYMBOLS",
 ]
 
 SV_BF16 = 0
@@ -37,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "sv_workspace_size", "spec_verify", "spec_verify_debug", "spec_verify_profiled",
     "sv_staging_size",
     "spec_verify_host", "sv_read_device_status", "sv_status_string", "sv_kernels_per_call",
+    "spec_verify_static",
 )
 
 _lib = None
@@ -79,6 +81,8 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.sv_read_device_status.restype = i32
     lib.sv_status_string.argtypes = [i32]
     lib.sv_status_string.restype = ctypes.c_char_p
+    lib.spec_verify_static.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp, vp]
+    lib.spec_verify_static.restype = i32
     lib.sv_kernels_per_call.argtypes = []
     lib.sv_kernels_per_call.restype = i32
     if path is None:
@@ -196,6 +200,17 @@ def spec_verify_host(h_target, h_draft, h_tokens, h_uniforms, temperature, h_out
         ctypes.c_float(temperature), _ptr(h_out_tokens), _ptr(h_n_accepted), _ptr(staging),
         staging.numel() * staging.element_size(), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(staging.device, stream)))
+
+
+def spec_verify_static(target, draft, tokens, uniforms, temperature, out_tokens, n_accepted,
+                       stream=None) -> int:
+    """The step with the library's fixed scratch array instead of a workspace,
+    for callers that cannot allocate device memory; returns the host status."""
+    B, K, V, dt = _check(target, draft, tokens, uniforms)
+    return int(load_library().spec_verify_static(
+        _ptr(target), _ptr(draft), _ptr(tokens), _ptr(uniforms), B, K, V, dt,
+        ctypes.c_float(temperature), _ptr(out_tokens), _ptr(n_accepted),
+        _stream(target.device, stream)))
 
 
 def sv_read_device_status(workspace, stream=None) -> int:

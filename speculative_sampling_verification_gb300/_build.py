@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libspecverify.so")
-SOURCES = ["sv_kernels.cu", "sv_api.cu"]
+SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_static_scratch.cu"]
 HEADERS = ["sv_device.cuh", "sv_internal.h", "sv_exp_table.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -224,6 +224,7 @@ const char* sv_status_string(int status) {
     case SV_ERR_ALIGN: return "pointer misaligned (elements, or 256 bytes for workspace/staging)";
     case SV_ERR_WORKSPACE: return "workspace or staging buffer too small";
     case SV_ERR_CUDA: return "a CUDA runtime call failed";
+    case SV_ERR_SCRATCH_LIMIT: return "problem needs more scratch than spec_verify_static holds";
     default: break;
   }
   if (status & SV_DEV_TIMEOUT) return "device: a bounded wait ran out (results invalid)";
