@@ -74,7 +74,7 @@ enum {
   SV_DEV_NONFINITE = 32,     /* a logit row holds NaN or +inf */
   SV_DEV_EMPTY_ROW = 64,     /* a logit row is entirely -inf */
   SV_DEV_UNIFORM_RANGE = 128,/* a uniform is NaN or outside [0, 1] */
-  SV_DEV_TIMEOUT = 256       /* a bounded wait inside a kernel ran out (results invalid) */
+  SV_DEV_TIMEOUT = 256       /* reserved; never set (the kernels contain no waits) */
 };
 
 /* Bytes of device workspace spec_verify needs for this problem size; 0 for an

@@ -65,16 +65,13 @@ int run(const void* target, const void* draft, const int32_t* tokens, const floa
   P.ns = (long long)L.rows_per_seq * L.nseg;
   P.np = L.nchunk;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  // Control block: status (4 B), abort (4 B), ticket (8 B), then done_s,
-  // done_p, ready [B] each; zeroed before every launch.
+  // Control block: status word (4 B), 12 B reserved, then done_s and done_p
+  // [B] each; zeroed before every launch.
   P.ctrl = ws + L.off_ctrl;
   P.ctrl_bytes = L.ctrl_bytes;
   P.status = reinterpret_cast<unsigned*>(ws + L.off_ctrl);
-  P.abort = reinterpret_cast<unsigned*>(ws + L.off_ctrl + 4);
-  P.ticket = reinterpret_cast<unsigned long long*>(ws + L.off_ctrl + 8);
   P.done_s = reinterpret_cast<unsigned*>(ws + L.off_ctrl + 16);
   P.done_p = P.done_s + B;
-  P.ready = P.done_p + B;
   P.seg_part = reinterpret_cast<float2*>(ws + L.off_seg);
   P.plans = reinterpret_cast<sv::Plan*>(ws + L.off_plan);
   P.sub_part = reinterpret_cast<float2*>(ws + L.off_sub);
@@ -227,7 +224,7 @@ const char* sv_status_string(int status) {
     case SV_ERR_SCRATCH_LIMIT: return "problem needs more scratch than spec_verify_static holds";
     default: break;
   }
-  if (status & SV_DEV_TIMEOUT) return "device: a bounded wait ran out (results invalid)";
+  if (status & SV_DEV_TIMEOUT) return "device: reserved status bit";
   if (status & SV_DEV_NONFINITE) return "device: a logit row holds NaN or +inf";
   if (status & SV_DEV_EMPTY_ROW) return "device: a logit row is entirely -inf";
   if (status & SV_DEV_TOKEN_RANGE) return "device: a draft token lies outside [0, V)";

@@ -1,6 +1,6 @@
-// Device helpers of the verification kernels: inline PTX for the mbarrier /
-// bulk-copy (TMA) pipeline, float-float arithmetic, and a float-float
-// exponential accurate to about 1e-12 relative.
+// Device helpers of the verification kernels: streaming loads, bf16
+// unpacking, float-float arithmetic, and a float-float exponential accurate
+// to about 1e-12 relative.
 #pragma once
 
 #include <cstdint>
@@ -15,75 +15,7 @@ namespace sv {
 
 SV_DEVINL float neg_inf() { return __int_as_float(0xff800000u); }
 
-// ---------------------------------------------------------------- PTX: shared memory, mbarrier, bulk copy
-
-SV_DEVINL uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-SV_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-               : "memory");
-}
-
-// Makes barrier initialisation visible to the async (bulk-copy) proxy.
-SV_DEVINL void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-SV_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-SV_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-SV_DEVINL uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait on an mbarrier phase: gives up after 200 ms of wall time and
-// returns false (the caller records an error status and winds down).
-constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
-SV_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
-// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
-// dst, src and bytes must all be multiples of 16.
-SV_DEVINL void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
-SV_DEVINL uint4 ld_shared_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(smem_addr(p)));
-  return v;
-}
+// ---------------------------------------------------------------- loads
 
 // Streaming 16-byte global load that skips L1.
 SV_DEVINL uint4 ld_global_nc_v4(const void* p) {
@@ -152,6 +84,20 @@ SV_DEVINL void ff_accumulate(ff& acc, ff x) {
 }
 
 SV_DEVINL ff ff_normalize(ff a) { return fast_two_sum(a.hi, a.lo); }
+
+// Accumulator for sums of terms in [0, 1]: it starts at 1 (ff_bias_start) so
+// that its head is never smaller than a term, which makes Dekker's
+// FastTwoSum exact for every addition; ff_bias_end removes the 1 exactly.
+SV_DEVINL ff ff_bias_start() { return {1.0f, 0.0f}; }
+
+SV_DEVINL void ff_accumulate_biased(ff& acc, ff x) {
+  const float s = __fadd_rn(acc.hi, x.hi);
+  const float e = __fsub_rn(x.hi, __fsub_rn(s, acc.hi));
+  acc.hi = s;
+  acc.lo = __fadd_rn(acc.lo, __fadd_rn(e, x.lo));
+}
+
+SV_DEVINL ff ff_bias_end(ff acc) { return fast_two_sum(__fsub_rn(acc.hi, 1.0f), acc.lo); }
 
 SV_DEVINL ff ff_add(ff a, ff b) {
   ff s = two_sum(a.hi, b.hi);

@@ -105,11 +105,8 @@ struct Params {
   long long np;    // draw chunks per sequence (nchunk)
   void* ctrl;      // control block, zeroed before every launch
   size_t ctrl_bytes;
-  unsigned* abort;             // set by the first timed-out wait
-  unsigned long long* ticket;  // worker ticket counter
-  unsigned* done_s;  // [B] streamed units counted per sequence
+  unsigned* done_s;  // [B] streamed segments counted per sequence
   unsigned* done_p;  // [B] draw chunks counted per sequence
-  unsigned* ready;   // [B] plan published
   float2* seg_part;
   Plan* plans;
   float2* sub_part;

@@ -1,36 +1,26 @@
-// Kernel of the verification step of speculative sampling (modified rejection
-// sampling: §4.2 and Algorithm 2 of "Accelerating Large Language Model
-// Decoding with Speculative Sampling", wikillm.com paper card).
+// Kernels of the verification step of speculative sampling (modified
+// rejection sampling: §4.2 and Algorithm 2 of "Accelerating Large Language
+// Model Decoding with Speculative Sampling", wikillm.com paper card).
 //
-// One cooperative persistent kernel per call, three CTAs per SM in two roles:
+// Two kernels per call, neither of which ever waits on another CTA:
 //
-//   streamers (2 per SM)  walk a static, interleaved list of row segments
-//       (segment u goes to streamer u mod Gs, in sequence-major order, so
-//       sequences complete one after another). Thread 0 keeps a 4-stage ring
-//       of 16 KB shared-memory stages full with 1-D bulk copies
-//       (cp.async.bulk, mbarrier completion), across segment boundaries; all
-//       threads reduce each segment to its maximum m and
+//   stats_kernel   one CTA per row segment (at most 32 KB; sequence-major, so
+//       sequences complete one after another). 16-byte vector loads, four per
+//       thread in flight, reduce the segment to its maximum m and
 //       sum_i 2^((l_i - m) log2(e)/T), the temperature transform of §4.2
-//       "Decoding transforms", then release-add one to the sequence's count.
-//       Streamers never wait on anything but their own copies.
-//   workers (1 per SM)    take tickets in sequence order, NP + 2 per sequence:
-//       scan(b)     once every segment of b is counted: combine segments,
-//                   gather the logits at the drafted tokens, thresholds
-//                   min(1, q/p) in fp64, first rejection j (Algorithm 2
-//                   step 3), publish the plan of b;
-//       draw(b, c)  one 4096-element chunk of the row pair the draw needs
-//                   (target and draft row j for the residual (q - p)_+, or
-//                   target row K for the bonus token, Algorithm 2 step 4):
-//                   float-float sums of exp((l - m)/T) and of the residual's
-//                   positive part per 512-element sub-chunk; the rows are
-//                   re-read while still in L2;
-//       finish(b)   once every chunk of b is counted: the exact inverse-CDF
-//                   search, in float-float, for the drawn token.
+//       "Decoding transforms". The CTA that counts the last segment of a
+//       sequence runs its scan: combine segments, gather the logits at the
+//       drafted tokens, thresholds min(1, q/p) in fp64, first rejection j
+//       (Algorithm 2 step 3), and the plan of the draw.
+//   draw_kernel    one CTA per 4096-element chunk of the row pair the draw
+//       needs (target and draft row j for the residual (q - p)_+, or target
+//       row K for the bonus token, Algorithm 2 step 4): float-float sums of
+//       exp((l - m)/T) and of the residual's positive part per 512-element
+//       sub-chunk. The CTA that counts the last chunk of a sequence runs the
+//       exact inverse-CDF search, in float-float, for the drawn token.
 //
-// A worker waits only on streamers or on tickets handed out before its own,
-// and the cooperative launch keeps every CTA resident, so the kernel cannot
-// deadlock; every wait is bounded (200 ms of wall time) and reports a status
-// bit instead of hanging.
+// Completion counting uses acquire-release atomics ("last CTA to arrive does
+// the follow-up"), so no CTA spins and no co-residency is assumed.
 #include <cfloat>
 #include <climits>
 #include <cstdint>
@@ -42,16 +32,12 @@
 namespace sv {
 
 constexpr unsigned kDevTokenRange = 16, kDevNonfinite = 32, kDevEmptyRow = 64,
-                   kDevUniformRange = 128, kDevTimeout = 256;
+                   kDevUniformRange = 128;
 constexpr float kLn2 = 0.693147180559945309f;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStageBytes = 16384;
-constexpr int kStages = 4;
-constexpr int kVecPerThread = kStageBytes / 16 / kThreads;  // 4
-constexpr int kCtasPerSm = 3;
-static_assert(kSegMaxBytes <= (long long)kStages * kStageBytes, "a segment must fit the ring");
+constexpr int kVecPerThread = 4;  // 16-byte vectors in flight per thread
 
 // ---------------------------------------------------------------- addressing and loads
 
@@ -74,38 +60,19 @@ SV_DEVINL float load_elem(const unsigned char* row, long long i) {
   }
 }
 
-SV_DEVINL uint32_t ld_acquire(const unsigned* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-SV_DEVINL void st_release(unsigned* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Records a timed-out wait: the status bit, and the abort flag that makes
-// every later wait of this launch give up at once.
-SV_DEVINL void note_timeout(const Params& P) {
-  atomicOr(P.status, kDevTimeout);
-  atomicExch(P.abort, 1u);
-}
-
 // ---------------------------------------------------------------- per-CTA shared state
 
 struct CtaShared {
   float2 tab[256];  // 2^(j/256), head + tail
-  uint64_t full[kStages];
   float red_m[kWarps], red_s[kWarps];
   float s_m[2 * kMaxK + 1], s_s[2 * kMaxK + 1];
-  double s_lse[2 * kMaxK + 1];
   double s_thr[kMaxK];
   float s_u[kMaxK + 2];
   int s_tok[kMaxK];
   ff red_f[kWarps];
+  ff red4[kWarps][4];
   ff s_pref;
   Plan plan;
-  unsigned long long ticket, next;
   unsigned bits;
   int j, g, flag;
 };
@@ -256,101 +223,36 @@ SV_DEVINL const unsigned char* unit_row(const Params& P, long long u) {
   return row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
 }
 
-SV_DEVINL void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Streamer, bulk-copy path. Streamer s of Gs owns units s, s+Gs, s+2Gs, ...
-// (sequence-major order, so sequences complete one after another). Thread 0
-// keeps the 4-stage ring full across unit boundaries; all threads consume
-// the pieces in order. After each unit thread 0 writes its (max, sum) pair
-// and adds 1 to the unit's sequence counter with release semantics.
+// Vector-load path (16-byte aligned rows): the segment's 16-byte vectors,
+// four per thread in flight at a time, streamed past L1.
 template <int DT>
-SV_DEVINL void streamer_tma(const Params& P, long long s, long long Gs, unsigned char* ring,
-                            CtaShared& sh) {
+SV_DEVINL void stats_unit_vec(const Params& P, long long u, CtaShared& sh) {
   constexpr int kEs = DT == 0 ? 2 : 4;
-  constexpr int kStageElems = kStageBytes / kEs;
   const int tid = threadIdx.x;
-  const long long n_units = P.n_units;
-  if (s >= n_units) return;
-  // Producer cursor (thread 0): next piece = unit pu, element offset poff.
-  long long pu = s;
-  int poff = 0;
-  uint32_t issued = 0;
-  auto issue = [&]() {
-    if (pu >= n_units) return;
-    const int len = unit_len(P, pu);
-    const int n = min(kStageElems, len - poff);
-    const int st = (int)(issued % kStages);
-    const unsigned char* src =
-        unit_row(P, pu) + ((size_t)(pu % P.nseg) * P.seg_elems + poff) * kEs;
-    const uint32_t bytes = (uint32_t)n * kEs;
-    mbar_arrive_expect_tx(&sh.full[st], bytes);
-    bulk_copy_g2s(ring + st * kStageBytes, src, bytes, &sh.full[st]);
-    ++issued;
-    poff += n;
-    if (poff >= len) {
-      pu += Gs;
-      poff = 0;
-    }
-  };
-  if (tid == 0)
-    for (int i = 0; i < kStages; ++i) issue();
-
+  const int len = unit_len(P, u);
+  const unsigned char* base = unit_row(P, u) + (size_t)(u % P.nseg) * P.seg_elems * kEs;
+  const int nvec = len * kEs / 16;
   const float c2 = P.c2;
   const uint32_t fill = DT == 0 ? 0xff80ff80u : 0xff800000u;  // -inf
-  uint32_t piece = 0;
-  for (long long u = s; u < n_units; u += Gs) {
-    const int len = unit_len(P, u);
-    float m_run = neg_inf(), H = neg_inf();
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    bool nan_seen = false, timed_out = false;
-    for (int off = 0; off < len; off += kStageElems) {
-      const int st = (int)(piece % kStages);
-      if (!mbar_wait(&sh.full[st], (piece / kStages) & 1u)) timed_out = true;
-      const unsigned char* buf = ring + st * kStageBytes;
-      const int nvec = min(kStageElems, len - off) * kEs / 16;
-      uint4 v[kVecPerThread];
+  float m_run = neg_inf(), H = neg_inf();
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  bool nan_seen = false;
+  for (int i0 = 0; i0 < nvec; i0 += kVecPerThread * kThreads) {
+    uint4 v[kVecPerThread];
 #pragma unroll
-      for (int k = 0; k < kVecPerThread; ++k) {
-        const int idx = tid + k * kThreads;
-        v[k] = idx < nvec ? ld_shared_v4(buf + idx * 16) : make_uint4(fill, fill, fill, fill);
-      }
-      stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
-      ++piece;
-      // Everyone is done with this stage; a timed-out wait anywhere aborts.
-      if (__syncthreads_or(timed_out)) {
-        if (tid == 0) {
-          note_timeout(P);
-          for (uint32_t q = piece - 1; q < issued; ++q)  // let copies in flight land
-            (void)mbar_wait(&sh.full[q % kStages], (q / kStages) & 1u);
-        }
-        return;
-      }
-      if (tid == 0) issue();
+    for (int k = 0; k < kVecPerThread; ++k) {
+      const int idx = i0 + k * kThreads + tid;
+      v[k] = idx < nvec ? ld_global_nc_v4(base + (size_t)idx * 16) : make_uint4(fill, fill, fill, fill);
     }
-    float sum = thread_sum(m_run, H, acc, nan_seen, c2);
-    float m = m_run;
-    block_combine(m, sum, c2, sh);
-    if (tid == 0) {
-      P.seg_part[u] = make_float2(m, sum);
-      red_release_add(P.done_s + u / P.ns, 1u);
-    }
+    stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
   }
+  float s = thread_sum(m_run, H, acc, nan_seen, c2);
+  float m = m_run;
+  block_combine(m, s, c2, sh);
+  if (tid == 0) P.seg_part[u] = make_float2(m, s);
 }
 
 // Plain-load path for rows that are not 16-byte aligned: two passes (max, sum).
-template <int DT>
-SV_DEVINL void stats_unit_plain(const Params& P, long long u, CtaShared& sh);
-
-template <int DT>
-SV_DEVINL void streamer_plain(const Params& P, long long s, long long Gs, CtaShared& sh) {
-  for (long long u = s; u < P.n_units; u += Gs) {
-    stats_unit_plain<DT>(P, u, sh);
-    if (threadIdx.x == 0) red_release_add(P.done_s + u / P.ns, 1u);
-  }
-}
-
 template <int DT>
 SV_DEVINL void stats_unit_plain(const Params& P, long long u, CtaShared& sh) {
   const float c2 = P.c2;
@@ -379,6 +281,7 @@ SV_DEVINL void stats_unit_plain(const Params& P, long long u, CtaShared& sh) {
 SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
   const int tid = threadIdx.x, K = P.K, R = P.rows_per_seq;
   if (tid == 0) sh.bits = 0;
+  sh.tab[tid] = kSvExp2Table[tid];
   // Stage the drafted tokens and uniforms of the sequence.
   for (int t = tid; t < K + 2; t += kThreads) {
     if (t < K) sh.s_tok[t] = P.tokens[b * K + t];
@@ -417,8 +320,9 @@ SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
         if (bits) atomicOr(&sh.bits, bits);
         sh.s_m[r] = m;
         sh.s_s[r] = sum;
-        sh.s_lse[r] =
-            bits ? __longlong_as_double(0x7ff8000000000000LL) : (double)m * P.inv_t + log((double)sum);
+        if (P.dbg_lse)  // lse = m/T + ln S, only for the debug export
+          P.dbg_lse[b * R + r] = bits ? __longlong_as_double(0x7ff8000000000000LL)
+                                      : (double)m * P.inv_t + log((double)sum);
       }
     }
   }
@@ -432,12 +336,12 @@ SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
   }
   __syncthreads();
   const unsigned bits = sh.bits;
-  if (P.dbg_lse)
-    for (int r = tid; r < R; r += kThreads) P.dbg_lse[b * R + r] = sh.s_lse[r];
 
   if (!bits) {
-    // Thresholds min(1, q(x~)/p(x~)) at the drafted tokens (§4.2), in fp64:
-    // log q(x) - log p(x) = (lq - lp)/T - (lse_q - lse_p).
+    // Thresholds min(1, q(x~)/p(x~)) at the drafted tokens (§4.2):
+    // q(x)/p(x) = e_q(x) S_p / (e_p(x) S_q), e(x) = exp((l(x) - m)/T) <= 1 in
+    // float-float against each row's own maximum, S the streaming sums. When
+    // an e(x) underflows fp32, the log-space form is used in fp64 instead.
     for (int t = tid; t < K; t += kThreads) {
       const int x = sh.s_tok[t];
       float lq, lp;
@@ -448,15 +352,27 @@ SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
         lq = load_elem<1>(row_base(P, b, t), x);
         lp = load_elem<1>(row_base(P, b, K + 1 + t), x);
       }
+      const float mq = sh.s_m[t], mp = sh.s_m[K + 1 + t];
+      const float sq = sh.s_s[t], sp = sh.s_s[K + 1 + t];
       double thr;
       if (lq == neg_inf()) {
         thr = 0.0;  // q(x~) = 0 rejects
       } else if (lp == neg_inf()) {
         thr = 1.0;  // p(x~) = 0 < q(x~) accepts
       } else {
-        const double lr =
-            ((double)lq - (double)lp) * P.inv_t - (sh.s_lse[t] - sh.s_lse[K + 1 + t]);
-        thr = lr >= 0.0 ? 1.0 : exp(lr);
+        const bool unit_t = P.unit_t != 0;
+        const ff xq = scaled_diff(lq, mq, P.ih, P.il, unit_t);
+        const ff xp = scaled_diff(lp, mp, P.ih, P.il, unit_t);
+        const ff eq = exp_ff(xq.hi, xq.lo, sh.tab);
+        const ff ep = exp_ff(xp.hi, xp.lo, sh.tab);
+        if (eq.hi > 1e-30f && ep.hi > 1e-30f) {
+          const double r = (ff_to_double(eq) * (double)sp) / (ff_to_double(ep) * (double)sq);
+          thr = r >= 1.0 ? 1.0 : r;
+        } else {
+          const double lr = ((double)lq - (double)lp) * P.inv_t -
+                            (((double)mq - (double)mp) * P.inv_t + log((double)sq / (double)sp));
+          thr = lr >= 0.0 ? 1.0 : exp(lr);
+        }
       }
       sh.s_thr[t] = thr;
       if (P.dbg_thr) P.dbg_thr[b * K + t] = thr;
@@ -515,10 +431,6 @@ SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
   if (P.dbg_thr && bits)
     for (int t = tid; t < K; t += kThreads)
       P.dbg_thr[b * K + t] = __longlong_as_double(0x7ff8000000000000LL);
-  // Publish the plan: every thread's writes first, then the flag (release).
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) st_release(P.ready + b, 1u);
 }
 
 // ---------------------------------------------------------------- draw: shared element code
@@ -598,7 +510,7 @@ SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab
   constexpr int kRuns = kSubElems / (32 * kVec);
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long e0 = ((long long)c * kSubPerChunk + w) * kSubElems;
-  ff Sq{0.f, 0.f}, Sp{0.f, 0.f}, A{0.f, 0.f}, Bs{0.f, 0.f};
+  ff Sq = ff_bias_start(), Sp = ff_bias_start(), A = ff_bias_start(), Bs = ff_bias_start();
   if (e0 < P.V) {
 #pragma unroll
     for (int r = 0; r < kRuns; ++r) {
@@ -611,22 +523,22 @@ SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab
         ff eq, ep;
         bool pos;
         element_exps<RESID>(d, xq[k], xp[k], tab, eq, ep, pos);
-        ff_accumulate(Sq, eq);
+        ff_accumulate_biased(Sq, eq);
         if constexpr (RESID) {
-          ff_accumulate(Sp, ep);
+          ff_accumulate_biased(Sp, ep);
           if (pos) {
-            ff_accumulate(A, eq);
-            ff_accumulate(Bs, ep);
+            ff_accumulate_biased(A, eq);
+            ff_accumulate_biased(Bs, ep);
           }
         }
       }
     }
   }
-  Sq = ff_warp_sum(ff_normalize(Sq));
+  Sq = ff_warp_sum(ff_bias_end(Sq));
   if constexpr (RESID) {
-    Sp = ff_warp_sum(ff_normalize(Sp));
-    A = ff_warp_sum(ff_normalize(A));
-    Bs = ff_warp_sum(ff_normalize(Bs));
+    Sp = ff_warp_sum(ff_bias_end(Sp));
+    A = ff_warp_sum(ff_bias_end(A));
+    Bs = ff_warp_sum(ff_bias_end(Bs));
   }
   if (lane == 0) {
     float4* out = reinterpret_cast<float4*>(
@@ -643,16 +555,29 @@ SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab
 
 SV_DEVINL ff ff_of(float x, float y) { return {x, y}; }
 
-// Block sum of float-float values; result in every thread.
-SV_DEVINL ff block_sum_ff(ff x, CtaShared& sh) {
-  x = ff_warp_sum(x);
+// Block sums of four float-float values at once; results in every thread.
+SV_DEVINL void block_sum4_ff(ff a, ff b, ff c, ff d, CtaShared& sh, ff& ra, ff& rb, ff& rc,
+                             ff& rd) {
+  a = ff_warp_sum(a);
+  b = ff_warp_sum(b);
+  c = ff_warp_sum(c);
+  d = ff_warp_sum(d);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
-  if (l == 0) sh.red_f[w] = x;
+  if (l == 0) {
+    sh.red4[w][0] = a;
+    sh.red4[w][1] = b;
+    sh.red4[w][2] = c;
+    sh.red4[w][3] = d;
+  }
   __syncthreads();
-  ff t{0.f, 0.f};
-  for (int i = 0; i < kWarps; ++i) t = ff_add(t, sh.red_f[i]);
-  return t;
+  ra = rb = rc = rd = {0.f, 0.f};
+  for (int i = 0; i < kWarps; ++i) {
+    ra = ff_add(ra, sh.red4[i][0]);
+    rb = ff_add(rb, sh.red4[i][1]);
+    rc = ff_add(rc, sh.red4[i][2]);
+    rd = ff_add(rd, sh.red4[i][3]);
+  }
 }
 
 // Block exclusive prefix of float-float values in thread order.
@@ -700,13 +625,8 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
       tb = ff_add(tb, ff_of(y.z, y.w));
     }
   }
-  const ff Sq = block_sum_ff(tq, sh);
-  ff Sp{0.f, 0.f}, A{0.f, 0.f}, Bt{0.f, 0.f};
-  if (resid) {
-    Sp = block_sum_ff(tp, sh);
-    A = block_sum_ff(ta, sh);
-    Bt = block_sum_ff(tb, sh);
-  }
+  ff Sq, Sp, A, Bt;
+  block_sum4_ff(tq, tp, ta, tb, sh, Sq, Sp, A, Bt);
   // Residual mass sum max(0, q - p), scaled by S_q S_p; zero -> fall back to q.
   const bool use_res = resid && ff_sub(ff_mul(Sp, A), ff_mul(Sq, Bt)).hi > 0.f;
   auto mass = [&](int g) -> ff {
@@ -836,134 +756,61 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
   }
 }
 
-// ---------------------------------------------------------------- the persistent kernel
+// ---------------------------------------------------------------- the two kernels
 
-// Bounded wait until a counter another CTA increments reaches `target`.
-// Gives up after 200 ms of wall time, or at once once the launch is aborting.
-SV_DEVINL bool wait_count(const Params& P, const unsigned* p, unsigned target) {
-  if (ld_acquire(p) >= target) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    __nanosleep(64);
-    if (ld_acquire(p) >= target) return true;
-    if (ld_acquire(P.abort) != 0u) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
-      note_timeout(P);
-      return false;
-    }
+SV_DEVINL unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+constexpr int kStatsCtasPerSm = 5;
+
+// One CTA per row segment u; the CTA that counts the last segment of a
+// sequence scans it.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kThreads, kStatsCtasPerSm) stats_kernel(Params P) {
+  __shared__ CtaShared sh;
+  const long long u = blockIdx.x;
+  const long long b = u / P.ns;
+  if constexpr (VEC)
+    stats_unit_vec<DT>(P, u, sh);
+  else
+    stats_unit_plain<DT>(P, u, sh);
+  // Thread 0 wrote the segment's pair; release it and count the segment.
+  if (threadIdx.x == 0) sh.flag = atomic_add_acq_rel(P.done_s + b, 1u) == (unsigned)(P.ns - 1);
+  __syncthreads();
+  if (sh.flag) {
+    __threadfence();
+    scan_seq(P, b, sh);
   }
 }
 
-SV_DEVINL Plan load_plan(const Plan* src) {
-  Plan pl;
-  pl.j = __ldcg(&src->j);
-  pl.mode = __ldcg(&src->mode);
-  pl.row_q = __ldcg(&src->row_q);
-  pl.row_p = __ldcg(&src->row_p);
-  pl.m_q = __ldcg(&src->m_q);
-  pl.m_p = __ldcg(&src->m_p);
-  pl.s_q = __ldcg(&src->s_q);
-  pl.s_p = __ldcg(&src->s_p);
-  pl.u = __ldcg(&src->u);
-  return pl;
-}
-
-// Worker: tickets in sequence order, (NP + 2) per sequence b:
-//   scan(b)      waits until all streaming units of b are counted, then scans;
-//   draw(b, c)   waits for the plan of b, then sums one chunk of the draw row(s);
-//   finish(b)    waits until all draw chunks of b are counted, then searches.
-// Each wait is on streamers (which never wait) or on an earlier ticket.
-template <int DT, bool ALIGNED>
-SV_DEVINL void worker(const Params& P, CtaShared& sh) {
-  const int tid = threadIdx.x;
-  const long long per = P.np + 2;
-  const unsigned long long total = (unsigned long long)P.B * per;
-  for (;;) {
-    if (tid == 0) sh.ticket = atomicAdd(P.ticket, 1ull);
-    __syncthreads();
-    const unsigned long long t = sh.ticket;
-    __syncthreads();
-    if (t >= total) return;
-    const long long b = (long long)(t / per);
-    const long long k = (long long)(t % per);
-    if (k == 0) {
-      if (tid == 0) sh.flag = wait_count(P, P.done_s + b, (unsigned)P.ns);
-      __syncthreads();
-      if (sh.flag) {
-        __threadfence();
-        scan_seq(P, b, sh);
-      } else if (tid == 0) {
-        Plan pl{};
-        pl.j = -1;
-        pl.mode = kModeFailed;
-        P.plans[b] = pl;
-        __threadfence();
-        st_release(P.ready + b, 1u);
-      }
-    } else if (k <= P.np) {
-      if (tid == 0) {
-        if (wait_count(P, P.ready + b, 1u)) {
-          sh.plan = load_plan(P.plans + b);
-        } else {
-          sh.plan.mode = kModeFailed;
-        }
-      }
-      __syncthreads();
-      const Plan pl = sh.plan;
-      if (pl.mode != kModeFailed) {
-        const DrawRow d = draw_row(P, pl);
-        if (pl.mode == kModeResidual)
-          partial_body<DT, true>(P, d, sh.tab, ALIGNED, b, (int)(k - 1));
-        else
-          partial_body<DT, false>(P, d, sh.tab, ALIGNED, b, (int)(k - 1));
-      }
-      __syncthreads();  // all partial writes of this CTA precede the release below
-      if (tid == 0) red_release_add(P.done_p + b, 1u);
-    } else {
-      if (tid == 0) {
-        if (wait_count(P, P.done_p + b, (unsigned)P.np) && wait_count(P, P.ready + b, 1u)) {
-          sh.plan = load_plan(P.plans + b);
-        } else {
-          sh.plan.mode = kModeFailed;
-        }
-      }
-      __syncthreads();
-      const Plan pl = sh.plan;
-      if (pl.mode != kModeFailed) {
-        __threadfence();
-        finish_seq<DT>(P, b, pl, sh, ALIGNED);
-      }
-    }
-    __syncthreads();
-  }
-}
-
-// Every third CTA (blockIdx % 3 == 2) is a worker, the others stream; with
-// three CTAs per SM this places one worker on each SM whether consecutive
-// blocks share an SM or are spread round-robin.
-template <int DT, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) verify_kernel(Params P) {
-  extern __shared__ __align__(128) unsigned char ring[];
+// One CTA per draw chunk c of sequence b (the plans are complete: the stats
+// kernel ran before this one on the stream); the CTA that counts the last
+// chunk of a sequence runs its inverse-CDF search.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kThreads) draw_kernel(Params P) {
   __shared__ CtaShared sh;
   const int tid = threadIdx.x;
   sh.tab[tid] = kSvExp2Table[tid];
-  if (ALIGNED && tid == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&sh.full[st], 1);
-    fence_barrier_init();
-  }
+  const long long b = blockIdx.x / P.np;
+  const int c = (int)(blockIdx.x % P.np);
+  if (tid == 0) sh.plan = P.plans[b];
   __syncthreads();
-  const long long bid = blockIdx.x;
-  const bool is_worker = (bid % 3) == 2;
-  if (is_worker) {
-    worker<DT, ALIGNED>(P, sh);
-  } else {
-    const long long s = (bid / 3) * 2 + (bid % 3);
-    const long long G = gridDim.x;
-    const long long Gs = (G / 3) * 2 + min(G % 3, 2LL);
-    if constexpr (ALIGNED)
-      streamer_tma<DT>(P, s, Gs, ring, sh);
-    else
-      streamer_plain<DT>(P, s, Gs, sh);
+  const Plan pl = sh.plan;
+  if (pl.mode == kModeFailed) return;  // outputs already written by the scan
+  const DrawRow d = draw_row(P, pl);
+  if (pl.mode == kModeResidual)
+    partial_body<DT, true>(P, d, sh.tab, VEC, b, c);
+  else
+    partial_body<DT, false>(P, d, sh.tab, VEC, b, c);
+  __syncthreads();  // all sub-chunk writes of this CTA precede the release below
+  if (tid == 0) sh.flag = atomic_add_acq_rel(P.done_p + b, 1u) == (unsigned)(P.np - 1);
+  __syncthreads();
+  if (sh.flag) {
+    __threadfence();
+    finish_seq<DT>(P, b, pl, sh, VEC);
   }
 }
 
@@ -971,41 +818,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) verify_kernel(Params P) 
 
 namespace {
 struct DeviceInfo {
-  int sms = 0;
-  int blocks_per_sm[4] = {0, 0, 0, 0};
   bool ready = false;
 };
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
-
-template <int DT, bool AL>
-cudaError_t setup_kernel(int* occ) {
-  const int smem = AL ? kStages * kStageBytes : 0;
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel<DT, AL>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, verify_kernel<DT, AL>, kThreads, smem);
-  if (e == cudaSuccess && *occ < 1) *occ = 1;
-  return e;
-}
 }  // namespace
 
 cudaError_t prepare_device(int device) {
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_dev_mu);
-  DeviceInfo& di = g_dev[device];
-  if (di.ready) return cudaSuccess;
-  cudaError_t e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, device);
-  if (e == cudaSuccess) e = setup_kernel<0, true>(&di.blocks_per_sm[0]);
-  if (e == cudaSuccess) e = setup_kernel<0, false>(&di.blocks_per_sm[1]);
-  if (e == cudaSuccess) e = setup_kernel<1, true>(&di.blocks_per_sm[2]);
-  if (e == cudaSuccess) e = setup_kernel<1, false>(&di.blocks_per_sm[3]);
-  if (e != cudaSuccess) return e;
-  di.ready = true;
+  g_dev[device].ready = true;
   return cudaSuccess;
 }
 
-int kernels_per_call() { return 1; }
+int kernels_per_call() { return 2; }
 
 cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev) {
   int device = 0;
@@ -1013,12 +839,6 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
   if (e != cudaSuccess) return e;
   e = prepare_device(device);
   if (e != cudaSuccess) return e;
-  const DeviceInfo& di = g_dev[device];
-  const int variant = (P.dtype == 0 ? 0 : 2) + (aligned ? 0 : 1);
-  // All CTAs must be resident at once (workers wait on streamers), so the
-  // grid is exactly what fits and the launch is cooperative.
-  const int grid = di.sms * di.blocks_per_sm[variant];
-  if (grid < 3) return cudaErrorInvalidConfiguration;
   e = cudaMemsetAsync(P.ctrl, 0, P.ctrl_bytes, st);
   if (e != cudaSuccess) return e;
   // External records, so that the events become timing nodes when the stream
@@ -1027,24 +847,28 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
     e = cudaEventRecordWithFlags(ev.start, st, cudaEventRecordExternal);
     if (e != cudaSuccess) return e;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = aligned ? kStages * kStageBytes : 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (P.dtype == 0)
-    e = aligned ? cudaLaunchKernelEx(&cfg, verify_kernel<0, true>, P)
-                : cudaLaunchKernelEx(&cfg, verify_kernel<0, false>, P);
-  else
-    e = aligned ? cudaLaunchKernelEx(&cfg, verify_kernel<1, true>, P)
-                : cudaLaunchKernelEx(&cfg, verify_kernel<1, false>, P);
-  if (e != cudaSuccess) return e;
-  if (ev.stats_done) e = cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
+  if (P.dtype == 0) {
+    if (aligned) {
+      stats_kernel<0, true><<<(unsigned)P.n_units, kThreads, 0, st>>>(P);
+      if (ev.stats_done) cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
+      draw_kernel<0, true><<<(unsigned)((long long)P.B * P.np), kThreads, 0, st>>>(P);
+    } else {
+      stats_kernel<0, false><<<(unsigned)P.n_units, kThreads, 0, st>>>(P);
+      if (ev.stats_done) cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
+      draw_kernel<0, false><<<(unsigned)((long long)P.B * P.np), kThreads, 0, st>>>(P);
+    }
+  } else {
+    if (aligned) {
+      stats_kernel<1, true><<<(unsigned)P.n_units, kThreads, 0, st>>>(P);
+      if (ev.stats_done) cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
+      draw_kernel<1, true><<<(unsigned)((long long)P.B * P.np), kThreads, 0, st>>>(P);
+    } else {
+      stats_kernel<1, false><<<(unsigned)P.n_units, kThreads, 0, st>>>(P);
+      if (ev.stats_done) cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
+      draw_kernel<1, false><<<(unsigned)((long long)P.B * P.np), kThreads, 0, st>>>(P);
+    }
+  }
+  e = cudaGetLastError();
   if (e == cudaSuccess && ev.end) e = cudaEventRecordWithFlags(ev.end, st, cudaEventRecordExternal);
   return e;
 }
