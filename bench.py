@@ -168,7 +168,7 @@ class ClockSampler:
                 "sm_max_mhz": num(rows[0][1]), "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_oracle_rate(w, seconds: float = 12.0, max_steps: int = 400, warmup: int = 0):
+def cpu_oracle_rate(w, seconds: float = 12.0, max_steps: int = 5000, warmup: int = 0):
     """Draft positions per second of the fp64 oracle on whole steps of `w`."""
     import oracle
 

@@ -13,7 +13,7 @@ namespace sv {
 // `seg_elems` elements; one (row, segment) pair is a unit of work.
 constexpr long long kTargetUnits = 1216;  // aim for at least this many units per call
 constexpr long long kSegMinBytes = 4096;
-constexpr long long kSegMaxBytes = 32768;  // two 16 KB ring stages, so the next segment can be in flight
+constexpr long long kSegMaxBytes = 32768;  // two rounds of four 16-byte loads per thread
 
 // Sampling pass: rows are cut into chunks of 4096 elements (one CTA of 256
 // threads), each chunk into 8 sub-chunks of 512 elements (one warp).
@@ -118,7 +118,7 @@ struct Params {
   double* dbg_prob;
 };
 
-// Launchers (sv_kernels.cu). `aligned`: 16-byte aligned rows (bulk-copy path).
+// Launchers (sv_kernels.cu). `aligned`: 16-byte aligned rows (vector-load path).
 cudaError_t prepare_device(int device);
 // Optional events recorded around the streaming kernel (any may be null).
 struct Events {
