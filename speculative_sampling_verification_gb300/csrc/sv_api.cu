@@ -66,13 +66,15 @@ int run(const void* target, const void* draft, const int32_t* tokens, const floa
   P.np = L.nchunk;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   // Control block: status word (4 B), 12 B reserved, then done_s and done_p
-  // [B] each; zeroed before every launch.
+  // [B] each and done_r [B (2K+1)]; zeroed before every launch.
   P.ctrl = ws + L.off_ctrl;
   P.ctrl_bytes = L.ctrl_bytes;
   P.status = reinterpret_cast<unsigned*>(ws + L.off_ctrl);
   P.done_s = reinterpret_cast<unsigned*>(ws + L.off_ctrl + 16);
   P.done_p = P.done_s + B;
+  P.done_r = P.done_p + B;
   P.seg_part = reinterpret_cast<float2*>(ws + L.off_seg);
+  P.row_stat = reinterpret_cast<float2*>(ws + L.off_row);
   P.plans = reinterpret_cast<sv::Plan*>(ws + L.off_plan);
   P.sub_part = reinterpret_cast<float2*>(ws + L.off_sub);
   P.out_tokens = out;

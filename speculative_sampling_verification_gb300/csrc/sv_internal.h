@@ -10,10 +10,10 @@
 namespace sv {
 
 // Streaming pass (row statistics): a row is cut into `nseg` segments of
-// `seg_elems` elements; one (row, segment) pair is a unit of work.
-constexpr long long kTargetUnits = 1216;  // aim for at least this many units per call
-constexpr long long kSegMinBytes = 4096;
-constexpr long long kSegMaxBytes = 32768;  // two rounds of four 16-byte loads per thread
+// `seg_elems` elements; one (row, segment) pair is a unit of work for one warp.
+constexpr long long kTargetUnits = 16384;  // aim for at least this many units per call
+constexpr long long kSegMinBytes = 2048;   // four 16-byte vectors per lane
+constexpr long long kSegMaxBytes = 32768;  // eight rounds of eight 16-byte vectors per lane
 
 // Sampling pass: rows are cut into chunks of 4096 elements (one CTA of 256
 // threads), each chunk into 8 sub-chunks of 512 elements (one warp).
@@ -45,7 +45,7 @@ struct Layout {
   int seg_elems;         // elements per segment (multiple of 8)
   long long n_units;     // rows_total * nseg
   int nchunk;            // sampling chunks per row
-  size_t off_status, off_ctrl, ctrl_bytes, off_seg, off_plan, off_sub, total;
+  size_t off_status, off_ctrl, ctrl_bytes, off_seg, off_row, off_plan, off_sub, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -75,10 +75,13 @@ inline bool make_layout(int B, int K, int V, int dtype, Layout* L) {
   size_t off = 0;
   L->off_status = off;  // status word (read by the host), then the control block
   L->off_ctrl = off;
-  L->ctrl_bytes = align_up(16 + (size_t)B * 12, 16);
+  // status (16 B), then done_s [B], done_p [B] and done_r [B (2K+1)]
+  L->ctrl_bytes = align_up(16 + (size_t)B * 8 + (size_t)L->rows_total * 4, 16);
   off = align_up(off + L->ctrl_bytes, 256);
   L->off_seg = off;
   off = align_up(off + (size_t)L->n_units * sizeof(float2), 256);
+  L->off_row = off;
+  off = align_up(off + (size_t)L->rows_total * sizeof(float2), 256);
   L->off_plan = off;
   off = align_up(off + (size_t)B * sizeof(Plan), 256);
   L->off_sub = off;
@@ -105,9 +108,11 @@ struct Params {
   long long np;    // draw chunks per sequence (nchunk)
   void* ctrl;      // control block, zeroed before every launch
   size_t ctrl_bytes;
-  unsigned* done_s;  // [B] streamed segments counted per sequence
+  unsigned* done_s;  // [B] rows whose statistics are complete, per sequence
   unsigned* done_p;  // [B] draw chunks counted per sequence
-  float2* seg_part;
+  unsigned* done_r;  // [B (2K+1)] streamed segments counted per row
+  float2* seg_part;  // [n_units] (max, sum) per segment
+  float2* row_stat;  // [B (2K+1)] (max, sum) per row
   Plan* plans;
   float2* sub_part;
   unsigned* status;

@@ -37,7 +37,6 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kVecPerThread = 4;  // 16-byte vectors in flight per thread
 
 // ---------------------------------------------------------------- addressing and loads
 
@@ -60,15 +59,10 @@ SV_DEVINL float load_elem(const unsigned char* row, long long i) {
   }
 }
 
-// ---------------------------------------------------------------- per-CTA shared state
+// ---------------------------------------------------------------- per-CTA shared state of the draw
 
 struct CtaShared {
   float2 tab[256];  // 2^(j/256), head + tail
-  float red_m[kWarps], red_s[kWarps];
-  float s_m[2 * kMaxK + 1], s_s[2 * kMaxK + 1];
-  double s_thr[kMaxK];
-  float s_u[kMaxK + 2];
-  int s_tok[kMaxK];
   ff red_f[kWarps];
   ff red4[kWarps][4];
   ff s_pref;
@@ -82,70 +76,39 @@ struct CtaShared {
 // NaN when a NaN (or +inf) entry was seen; m = -inf with s = 0 means "no
 // finite entry yet".
 
-// Same with the accurate exp2f, for the few pairs the scan combines.
-SV_DEVINL void ms_combine_acc(float& m, float& s, float m2, float s2, float c2) {
-  const float M = fmaxf(m, m2);
-  if (M == neg_inf()) {
-    s = s + s2;
-    return;
-  }
-  const float a = (m == neg_inf()) ? 0.0f : exp2f((m - M) * c2);
-  const float b = (m2 == neg_inf()) ? 0.0f : exp2f((m2 - M) * c2);
-  s = s * a + s2 * b;
-  m = M;
-}
-
-SV_DEVINL void ms_combine(float& m, float& s, float m2, float s2, float c2) {
-  const float M = fmaxf(m, m2);
-  if (M == neg_inf()) {
-    s = s + s2;
-    return;
-  }
-  const float a = (m == neg_inf()) ? 0.0f : ex2_fast((m - M) * c2);
-  const float b = (m2 == neg_inf()) ? 0.0f : ex2_fast((m2 - M) * c2);
-  s = s * a + s2 * b;
-  m = M;
-}
-
-// Block-wide combine (kThreads threads). Result in thread 0.
-SV_DEVINL void block_combine(float& m, float& s, float c2, CtaShared& sh) {
+// Warp-wide combine of one pair per lane with the accurate exp2f: the
+// maximum first, then every lane's sum rescaled to it. All lanes get the
+// result.
+SV_DEVINL float2 warp_combine_pairs(float m, float s, float c2) {
+  float M = m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    ms_combine(m, s, m2, s2, c2);
-  }
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) {
-    sh.red_m[w] = m;
-    sh.red_s[w] = s;
-  }
-  __syncthreads();
-  if (w == 0) {
-    m = l < kWarps ? sh.red_m[l] : neg_inf();
-    s = l < kWarps ? sh.red_s[l] : 0.0f;
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (M != neg_inf() && M != m) s = (m == neg_inf()) ? s * 0.0f : s * exp2f((m - M) * c2);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      ms_combine(m, s, m2, s2, c2);
-    }
-  }
-  __syncthreads();
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return make_float2(M, s);
 }
 
-// ---------------------------------------------------------------- stats: one segment
+// ---------------------------------------------------------------- stats: one warp, one segment
 //
-// Per thread: the stage's local max (packed bf16x2 max for bf16), a rescale
-// of the four running sums only when the max grows, then one FFMA and one
-// MUFU ex2 per element against H = fl(m * c2); the rounding residual of H is
-// folded back in once per segment.
+// A unit is one segment (at most 32 KB) of one row, reduced by one warp with
+// no shared memory and no barrier. Per round each lane holds eight 16-byte
+// vectors. It takes their max (packed bf16x2 max for bf16), rescales its
+// four running sums when the max grows, then spends one FFMA and one MUFU
+// ex2 per element against H = fl(m * c2). The lanes are then combined: the
+// warp maximum M first, then every lane's sum scaled by 2^(H - M c2), which
+// also folds the rounding residual of H back in.
+
+constexpr int kStatsThreads = 128;
+constexpr int kStatsWarps = kStatsThreads / 32;
+constexpr int kStatsCtasPerSm = 8;
+constexpr int kStatsVec = 8;  // 16-byte vectors per lane per round
 
 template <int DT>
-SV_DEVINL bool any_nan(const uint4 (&v)[kVecPerThread]) {
+SV_DEVINL bool any_nan(const uint4 (&v)[kStatsVec]) {
   bool bad = false;
 #pragma unroll
-  for (int i = 0; i < kVecPerThread; ++i) {
+  for (int i = 0; i < kStatsVec; ++i) {
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -160,19 +123,19 @@ SV_DEVINL bool any_nan(const uint4 (&v)[kVecPerThread]) {
 }
 
 template <int DT>
-SV_DEVINL void stats_consume(const uint4 (&v)[kVecPerThread], float& m_run, float& H,
+SV_DEVINL void stats_consume(const uint4 (&v)[kStatsVec], float& m_run, float& H,
                              float (&acc)[4], bool& nan_seen, float c2) {
   float lm;
   if constexpr (DT == 0) {
     uint32_t mx = bf16x2_max(bf16x2_max(v[0].x, v[0].y), bf16x2_max(v[0].z, v[0].w));
 #pragma unroll
-    for (int i = 1; i < kVecPerThread; ++i)
+    for (int i = 1; i < kStatsVec; ++i)
       mx = bf16x2_max(mx, bf16x2_max(bf16x2_max(v[i].x, v[i].y), bf16x2_max(v[i].z, v[i].w)));
     lm = fmaxf(bf16_lo(mx), bf16_hi(mx));
   } else {
     lm = neg_inf();
 #pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i)
+    for (int i = 0; i < kStatsVec; ++i)
       lm = fmaxf(lm, fmaxf(fmaxf(__uint_as_float(v[i].x), __uint_as_float(v[i].y)),
                            fmaxf(__uint_as_float(v[i].z), __uint_as_float(v[i].w))));
   }
@@ -189,7 +152,7 @@ SV_DEVINL void stats_consume(const uint4 (&v)[kVecPerThread], float& m_run, floa
     return;
   }
 #pragma unroll
-  for (int i = 0; i < kVecPerThread; ++i) {
+  for (int i = 0; i < kStatsVec; ++i) {
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     if constexpr (DT == 0) {
 #pragma unroll
@@ -204,13 +167,23 @@ SV_DEVINL void stats_consume(const uint4 (&v)[kVecPerThread], float& m_run, floa
   }
 }
 
-// Per-thread sum of a finished segment, with H's rounding residual folded in.
-SV_DEVINL float thread_sum(float m_run, float H, const float (&acc)[4], bool nan_seen, float c2) {
-  if (m_run == neg_inf()) return nan_seen ? __int_as_float(0x7fc00000) : 0.0f;
-  float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-  const float L = __fmaf_rn(m_run, c2, -H);  // m*c2 - H exactly (to fp32)
-  s *= __fmaf_rn(-L, kLn2, 1.0f);            // 2^-L to first order (|L| < 1e-5)
-  return nan_seen ? __int_as_float(0x7fc00000) : s;
+// Warp-wide (max, sum) of the lanes' running statistics; all lanes get it.
+SV_DEVINL float2 warp_stats(float m_run, float H, const float (&acc)[4], bool nan_seen, float c2) {
+  float M = m_run;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float s = 0.0f;
+  if (m_run != neg_inf()) {
+    s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    // 2^(H - M c2): to first order when m_run is the maximum (|H - M c2| is
+    // below an ulp of H), else by the hardware exp2.
+    const float E = __fmaf_rn(-M, c2, H);
+    s *= (m_run == M) ? __fmaf_rn(E, kLn2, 1.0f) : ex2_fast(E);
+  }
+  if (nan_seen) s = __int_as_float(0x7fc00000);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return make_float2(M, s);
 }
 
 SV_DEVINL int unit_len(const Params& P, long long u) {
@@ -224,11 +197,10 @@ SV_DEVINL const unsigned char* unit_row(const Params& P, long long u) {
 }
 
 // Vector-load path (16-byte aligned rows): the segment's 16-byte vectors,
-// four per thread in flight at a time, streamed past L1.
+// eight per lane in flight at a time, streamed past L1.
 template <int DT>
-SV_DEVINL void stats_unit_vec(const Params& P, long long u, CtaShared& sh) {
+SV_DEVINL float2 stats_warp_vec(const Params& P, long long u, int lane) {
   constexpr int kEs = DT == 0 ? 2 : 4;
-  const int tid = threadIdx.x;
   const int len = unit_len(P, u);
   const unsigned char* base = unit_row(P, u) + (size_t)(u % P.nseg) * P.seg_elems * kEs;
   const int nvec = len * kEs / 16;
@@ -237,113 +209,131 @@ SV_DEVINL void stats_unit_vec(const Params& P, long long u, CtaShared& sh) {
   float m_run = neg_inf(), H = neg_inf();
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   bool nan_seen = false;
-  for (int i0 = 0; i0 < nvec; i0 += kVecPerThread * kThreads) {
-    uint4 v[kVecPerThread];
+  for (int i0 = 0; i0 < nvec; i0 += kStatsVec * 32) {
+    uint4 v[kStatsVec];
 #pragma unroll
-    for (int k = 0; k < kVecPerThread; ++k) {
-      const int idx = i0 + k * kThreads + tid;
+    for (int k = 0; k < kStatsVec; ++k) {
+      const int idx = i0 + k * 32 + lane;
       v[k] = idx < nvec ? ld_global_nc_v4(base + (size_t)idx * 16) : make_uint4(fill, fill, fill, fill);
     }
     stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
   }
-  float s = thread_sum(m_run, H, acc, nan_seen, c2);
-  float m = m_run;
-  block_combine(m, s, c2, sh);
-  if (tid == 0) P.seg_part[u] = make_float2(m, s);
+  return warp_stats(m_run, H, acc, nan_seen, c2);
 }
 
-// Plain-load path for rows that are not 16-byte aligned: two passes (max, sum).
+// Plain-load path for rows that are not 16-byte aligned: two passes (the
+// warp maximum, then the sum against it).
 template <int DT>
-SV_DEVINL void stats_unit_plain(const Params& P, long long u, CtaShared& sh) {
+SV_DEVINL float2 stats_warp_plain(const Params& P, long long u, int lane) {
   const float c2 = P.c2;
   const int len = unit_len(P, u);
   const unsigned char* rb = unit_row(P, u);
   const long long e0 = (long long)(u % P.nseg) * P.seg_elems;
   float m = neg_inf();
   bool nan_seen = false;
-  for (int i = threadIdx.x; i < len; i += kThreads) {
+  for (int i = lane; i < len; i += 32) {
     const float l = load_elem<DT>(rb, e0 + i);
     nan_seen |= (l != l);
     m = fmaxf(m, l);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float s = 0.f;
   if (m != neg_inf()) {
-    for (int i = threadIdx.x; i < len; i += kThreads)
-      s += ex2_fast((load_elem<DT>(rb, e0 + i) - m) * c2);
+    for (int i = lane; i < len; i += 32) s += ex2_fast((load_elem<DT>(rb, e0 + i) - m) * c2);
   }
   if (nan_seen) s = __int_as_float(0x7fc00000);
-  block_combine(m, s, c2, sh);
-  if (threadIdx.x == 0) P.seg_part[u] = make_float2(m, s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return make_float2(m, s);
 }
 
-// ---------------------------------------------------------------- scan of one sequence
-
-SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
-  const int tid = threadIdx.x, K = P.K, R = P.rows_per_seq;
-  if (tid == 0) sh.bits = 0;
-  sh.tab[tid] = kSvExp2Table[tid];
-  // Stage the drafted tokens and uniforms of the sequence.
-  for (int t = tid; t < K + 2; t += kThreads) {
-    if (t < K) sh.s_tok[t] = P.tokens[b * K + t];
-    sh.s_u[t] = P.uniforms[b * (K + 2) + t];
+// (max, sum) of a whole row from its segments' pairs, one warp; all lanes
+// get it.
+SV_DEVINL float2 row_combine(const Params& P, long long row, int lane) {
+  const float2* part = P.seg_part + row * P.nseg;
+  float m = neg_inf(), s = 0.0f;
+  if (P.nseg <= 32) {
+    if (lane < P.nseg) {
+      const float2 ps = __ldcg(part + lane);
+      m = ps.x;
+      s = ps.y;
+    }
+    return warp_combine_pairs(m, s, P.c2);
   }
-  __syncthreads();
-
-  // Row statistics, one warp per row: lanes load the row's segment pairs in
-  // parallel, combine them as (max, sum) pairs, and lane 0 forms
-  // lse = m/T + ln S in fp64.
-  {
-    const int w = tid >> 5, lane = tid & 31;
-    for (int r = w; r < R; r += kWarps) {
-      const float2* part = P.seg_part + ((long long)b * R + r) * P.nseg;
-      float m = neg_inf(), sum = 0.f;
-      bool nan_seen = false;
-      for (int g = lane; g < P.nseg; g += 32) {
-        const float2 ps = __ldcg(part + g);
-        nan_seen |= (ps.y != ps.y);
-        ms_combine_acc(m, sum, ps.x, ps.y, P.c2);
-      }
+  // More segments than lanes: each lane first combines its own.
+  float2 ps[4];
+  for (int g0 = 0; g0 < P.nseg; g0 += 4 * 32) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-        ms_combine_acc(m, sum, m2, s2, P.c2);
-      }
-      nan_seen = __any_sync(0xffffffffu, nan_seen);
-      if (lane == 0) {
-        unsigned bits = 0;
-        if (nan_seen || sum != sum) {
-          bits = kDevNonfinite;
-        } else if (m == neg_inf()) {
-          bits = kDevEmptyRow;
-        }
-        if (bits) atomicOr(&sh.bits, bits);
-        sh.s_m[r] = m;
-        sh.s_s[r] = sum;
-        if (P.dbg_lse)  // lse = m/T + ln S, only for the debug export
-          P.dbg_lse[b * R + r] = bits ? __longlong_as_double(0x7ff8000000000000LL)
-                                      : (double)m * P.inv_t + log((double)sum);
+    for (int k = 0; k < 4; ++k) {
+      const int g = g0 + k * 32 + lane;
+      ps[k] = g < P.nseg ? __ldcg(part + g) : make_float2(neg_inf(), 0.0f);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float M = fmaxf(m, ps[k].x);
+      if (M != neg_inf()) {
+        const float a = (m == neg_inf()) ? 0.0f : exp2f((m - M) * P.c2);
+        const float c = (ps[k].x == neg_inf()) ? 0.0f : exp2f((ps[k].x - M) * P.c2);
+        s = s * a + ps[k].y * c;
+        m = M;
+      } else {
+        s += ps[k].y;
       }
     }
   }
-  for (int t = tid; t < K; t += kThreads) {
-    const int x = sh.s_tok[t];
-    if (x < 0 || x >= P.V) atomicOr(&sh.bits, kDevTokenRange);
+  return warp_combine_pairs(m, s, P.c2);
+}
+
+// ---------------------------------------------------------------- scan of one sequence, one warp
+
+struct WarpScan {
+  float m[2 * kMaxK + 1], s[2 * kMaxK + 1];
+  double thr[kMaxK];
+  float u[kMaxK + 2];
+  int tok[kMaxK];
+};
+
+SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
+  const int K = P.K, R = P.rows_per_seq;
+  unsigned bits = 0;
+  // The drafted tokens, the uniforms and the row statistics, one lane per
+  // entry.
+  for (int t = lane; t < K + 2; t += 32) {
+    if (t < K) {
+      const int x = P.tokens[b * K + t];
+      ws.tok[t] = x;
+      if (x < 0 || x >= P.V) bits |= kDevTokenRange;
+    }
+    const float u = P.uniforms[b * (K + 2) + t];
+    ws.u[t] = u;
+    if (!(u >= 0.0f && u <= 1.0f)) bits |= kDevUniformRange;
   }
-  for (int t = tid; t < K + 2; t += kThreads) {
-    const float u = sh.s_u[t];
-    if (!(u >= 0.0f && u <= 1.0f)) atomicOr(&sh.bits, kDevUniformRange);
+  for (int r = lane; r < R; r += 32) {
+    const float2 st = __ldcg(P.row_stat + b * R + r);
+    unsigned rb = 0;
+    if (st.y != st.y) {
+      rb = kDevNonfinite;
+    } else if (st.x == neg_inf()) {
+      rb = kDevEmptyRow;
+    }
+    bits |= rb;
+    ws.m[r] = st.x;
+    ws.s[r] = st.y;
+    if (P.dbg_lse)  // lse = m/T + ln S, only for the debug export
+      P.dbg_lse[b * R + r] = rb ? __longlong_as_double(0x7ff8000000000000LL)
+                                : (double)st.x * P.inv_t + log((double)st.y);
   }
-  __syncthreads();
-  const unsigned bits = sh.bits;
+  bits = __reduce_or_sync(0xffffffffu, bits);
+  __syncwarp();
 
   if (!bits) {
     // Thresholds min(1, q(x~)/p(x~)) at the drafted tokens (§4.2):
     // q(x)/p(x) = e_q(x) S_p / (e_p(x) S_q), e(x) = exp((l(x) - m)/T) <= 1 in
     // float-float against each row's own maximum, S the streaming sums. When
     // an e(x) underflows fp32, the log-space form is used in fp64 instead.
-    for (int t = tid; t < K; t += kThreads) {
-      const int x = sh.s_tok[t];
+    for (int t = lane; t < K; t += 32) {
+      const int x = ws.tok[t];
       float lq, lp;
       if (P.dtype == 0) {
         lq = load_elem<0>(row_base(P, b, t), x);
@@ -352,8 +342,8 @@ SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
         lq = load_elem<1>(row_base(P, b, t), x);
         lp = load_elem<1>(row_base(P, b, K + 1 + t), x);
       }
-      const float mq = sh.s_m[t], mp = sh.s_m[K + 1 + t];
-      const float sq = sh.s_s[t], sp = sh.s_s[K + 1 + t];
+      const float mq = ws.m[t], mp = ws.m[K + 1 + t];
+      const float sq = ws.s[t], sp = ws.s[K + 1 + t];
       double thr;
       if (lq == neg_inf()) {
         thr = 0.0;  // q(x~) = 0 rejects
@@ -363,8 +353,8 @@ SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
         const bool unit_t = P.unit_t != 0;
         const ff xq = scaled_diff(lq, mq, P.ih, P.il, unit_t);
         const ff xp = scaled_diff(lp, mp, P.ih, P.il, unit_t);
-        const ff eq = exp_ff(xq.hi, xq.lo, sh.tab);
-        const ff ep = exp_ff(xp.hi, xp.lo, sh.tab);
+        const ff eq = exp_ff(xq.hi, xq.lo, kSvExp2Table);
+        const ff ep = exp_ff(xp.hi, xp.lo, kSvExp2Table);
         if (eq.hi > 1e-30f && ep.hi > 1e-30f) {
           const double r = (ff_to_double(eq) * (double)sp) / (ff_to_double(ep) * (double)sq);
           thr = r >= 1.0 ? 1.0 : r;
@@ -374,13 +364,27 @@ SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
           thr = lr >= 0.0 ? 1.0 : exp(lr);
         }
       }
-      sh.s_thr[t] = thr;
+      ws.thr[t] = thr;
       if (P.dbg_thr) P.dbg_thr[b * K + t] = thr;
     }
   }
-  __syncthreads();
+  __syncwarp();
 
-  if (tid == 0) {
+  // Left-to-right scan: accept while u_t < thr_t (Algorithm 2 step 3); the
+  // first rejection is the lowest lane (of each group of 32) that rejects.
+  int j = bits ? -1 : K;
+  if (!bits) {
+    for (int t0 = 0; t0 < K; t0 += 32) {
+      const int t = t0 + lane;
+      const bool rej = t < K && !((double)ws.u[t] < ws.thr[t]);
+      const unsigned mask = __ballot_sync(0xffffffffu, rej);
+      if (mask) {
+        j = t0 + __ffs(mask) - 1;
+        break;
+      }
+    }
+  }
+  if (lane == 0) {
     Plan pl{};
     if (bits) {
       atomicOr(P.status, bits);
@@ -389,48 +393,36 @@ SV_DEVINL void scan_seq(const Params& P, long long b, CtaShared& sh) {
       P.n_acc[b] = -1;
       if (P.dbg_prob) P.dbg_prob[b] = __longlong_as_double(0x7ff8000000000000LL);
     } else {
-      // Left-to-right scan: accept while u_t < thr_t (Algorithm 2 step 3).
-      int j = K;
-      for (int t = 0; t < K; ++t) {
-        if (!((double)sh.s_u[t] < sh.s_thr[t])) {
-          j = t;
-          break;
-        }
-      }
       pl.j = j;
       if (j < K) {
         pl.mode = kModeResidual;
         pl.row_q = b * (K + 1) + j;
         pl.row_p = b * K + j;
-        pl.m_q = sh.s_m[j];
-        pl.s_q = sh.s_s[j];
-        pl.m_p = sh.s_m[K + 1 + j];
-        pl.s_p = sh.s_s[K + 1 + j];
-        pl.u = sh.s_u[K];
+        pl.m_q = ws.m[j];
+        pl.s_q = ws.s[j];
+        pl.m_p = ws.m[K + 1 + j];
+        pl.s_p = ws.s[K + 1 + j];
+        pl.u = ws.u[K];
       } else {
         pl.mode = kModeBonus;
         pl.row_q = b * (K + 1) + K;
         pl.row_p = -1;
-        pl.m_q = sh.s_m[K];
-        pl.s_q = sh.s_s[K];
-        pl.u = sh.s_u[K + 1];
+        pl.m_q = ws.m[K];
+        pl.s_q = ws.s[K];
+        pl.u = ws.u[K + 1];
       }
       P.n_acc[b] = j;
     }
     P.plans[b] = pl;
-    sh.j = pl.j;
   }
-  __syncthreads();
-  const int j = sh.j;
-  for (int t = tid; t <= K; t += kThreads) {
+  for (int t = lane; t <= K; t += 32) {
     if (j < 0 || t > j)
       P.out_tokens[b * (K + 1) + t] = -1;
     else if (t < j)
-      P.out_tokens[b * (K + 1) + t] = sh.s_tok[t];
+      P.out_tokens[b * (K + 1) + t] = ws.tok[t];
   }
   if (P.dbg_thr && bits)
-    for (int t = tid; t < K; t += kThreads)
-      P.dbg_thr[b * K + t] = __longlong_as_double(0x7ff8000000000000LL);
+    for (int t = lane; t < K; t += 32) P.dbg_thr[b * K + t] = __longlong_as_double(0x7ff8000000000000LL);
 }
 
 // ---------------------------------------------------------------- draw: shared element code
@@ -764,26 +756,47 @@ SV_DEVINL unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
   return old;
 }
 
-constexpr int kStatsCtasPerSm = 5;
+SV_DEVINL uint32_t ld_acquire(const unsigned* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
-// One CTA per row segment u; the CTA that counts the last segment of a
-// sequence scans it.
+// One warp per row segment u. The warp that counts the last segment of a row
+// combines the row; the warp that completes the last row of a sequence scans
+// it. The counters are acquire-release atomics, and a warp that goes on to
+// read what other warps published first acquires the counter in every lane.
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads, kStatsCtasPerSm) stats_kernel(Params P) {
-  __shared__ CtaShared sh;
-  const long long u = blockIdx.x;
-  const long long b = u / P.ns;
+__global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(Params P) {
+  __shared__ WarpScan scan_sh[kStatsWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long u = (long long)blockIdx.x * kStatsWarps + warp;
+  if (u >= P.n_units) return;
+  const long long row = u / P.nseg;
+  const long long b = row / P.rows_per_seq;
+  float2 st;
   if constexpr (VEC)
-    stats_unit_vec<DT>(P, u, sh);
+    st = stats_warp_vec<DT>(P, u, lane);
   else
-    stats_unit_plain<DT>(P, u, sh);
-  // Thread 0 wrote the segment's pair; release it and count the segment.
-  if (threadIdx.x == 0) sh.flag = atomic_add_acq_rel(P.done_s + b, 1u) == (unsigned)(P.ns - 1);
-  __syncthreads();
-  if (sh.flag) {
-    __threadfence();
-    scan_seq(P, b, sh);
+    st = stats_warp_plain<DT>(P, u, lane);
+  if (P.nseg > 1) {
+    unsigned last = 0;
+    if (lane == 0) {
+      P.seg_part[u] = st;
+      last = atomic_add_acq_rel(P.done_r + row, 1u) == (unsigned)(P.nseg - 1);
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    (void)ld_acquire(P.done_r + row);
+    st = row_combine(P, row, lane);
   }
+  unsigned last = 0;
+  if (lane == 0) {
+    P.row_stat[row] = st;
+    last = atomic_add_acq_rel(P.done_s + b, 1u) == (unsigned)(P.rows_per_seq - 1);
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  (void)ld_acquire(P.done_s + b);
+  scan_warp(P, b, lane, scan_sh[warp]);
 }
 
 // One CTA per draw chunk c of sequence b (the plans are complete: the stats
@@ -847,23 +860,24 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
     e = cudaEventRecordWithFlags(ev.start, st, cudaEventRecordExternal);
     if (e != cudaSuccess) return e;
   }
+  const unsigned stats_grid = (unsigned)((P.n_units + kStatsWarps - 1) / kStatsWarps);
   if (P.dtype == 0) {
     if (aligned) {
-      stats_kernel<0, true><<<(unsigned)P.n_units, kThreads, 0, st>>>(P);
+      stats_kernel<0, true><<<stats_grid, kStatsThreads, 0, st>>>(P);
       if (ev.stats_done) cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
       draw_kernel<0, true><<<(unsigned)((long long)P.B * P.np), kThreads, 0, st>>>(P);
     } else {
-      stats_kernel<0, false><<<(unsigned)P.n_units, kThreads, 0, st>>>(P);
+      stats_kernel<0, false><<<stats_grid, kStatsThreads, 0, st>>>(P);
       if (ev.stats_done) cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
       draw_kernel<0, false><<<(unsigned)((long long)P.B * P.np), kThreads, 0, st>>>(P);
     }
   } else {
     if (aligned) {
-      stats_kernel<1, true><<<(unsigned)P.n_units, kThreads, 0, st>>>(P);
+      stats_kernel<1, true><<<stats_grid, kStatsThreads, 0, st>>>(P);
       if (ev.stats_done) cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
       draw_kernel<1, true><<<(unsigned)((long long)P.B * P.np), kThreads, 0, st>>>(P);
     } else {
-      stats_kernel<1, false><<<(unsigned)P.n_units, kThreads, 0, st>>>(P);
+      stats_kernel<1, false><<<stats_grid, kStatsThreads, 0, st>>>(P);
       if (ev.stats_done) cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
       draw_kernel<1, false><<<(unsigned)((long long)P.B * P.np), kThreads, 0, st>>>(P);
     }
