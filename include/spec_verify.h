@@ -31,8 +31,11 @@
  * pointers between calls. Work is enqueued on `stream` (a cudaStream_t passed
  * as void*; NULL means the legacy default stream) and runs asynchronously.
  *
- * The first call on a device sets kernel attributes for that device; make it
- * before capturing the stream into a CUDA graph.
+ * A call enqueues a memset of the workspace's control block and two kernels:
+ * the streaming kernel, then the draw kernel as its programmatic dependent
+ * (launched while the streaming grid drains, and waiting on the device for it
+ * to complete). Make the first call on a device before capturing a stream
+ * into a CUDA graph.
  */
 #ifndef SPEC_VERIFY_H_
 #define SPEC_VERIFY_H_
@@ -100,7 +103,7 @@ size_t sv_workspace_size(int B, int K, int V, int dtype);
  *
  * Inputs are read only. Base pointers of the logits need only element
  * alignment; 16-byte aligned bases with V * sizeof(dtype) a multiple of 16
- * take the bulk-copy (TMA) path. Returns SV_OK once the work is enqueued, or
+ * take the 16-byte vector-load path. Returns SV_OK once the work is enqueued, or
  * a host-side error code with nothing enqueued. B == 0 returns SV_OK at once.
  * Device-side problems are reported through sv_read_device_status(). */
 int spec_verify(const void* target_logits, const void* draft_logits,
@@ -122,9 +125,11 @@ int spec_verify_debug(const void* target_logits, const void* draft_logits,
 
 /* spec_verify that also records three caller-owned CUDA events (cudaEvent_t
  * passed as void*, created with timing enabled) on `stream`: `ev_start` before
- * the first kernel, `ev_stats_done` after the streaming row-statistics
- * kernel, `ev_end` after the last kernel. Elapsed times between them time the
- * streaming pass and the rest of the step. Any event may be NULL. */
+ * the first kernel, `ev_stats_done` between the streaming row-statistics
+ * kernel and the draw kernel, `ev_end` after the draw kernel. Elapsed times
+ * between them time the streaming pass and the draw. With `ev_stats_done` set
+ * the draw kernel is an ordinary launch rather than a programmatic dependent,
+ * so the pair runs back to back without overlap. Any event may be NULL. */
 int spec_verify_profiled(const void* target_logits, const void* draft_logits,
                          const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
                          int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
@@ -178,8 +183,10 @@ int sv_read_device_status(const void* workspace, void* stream, int* status);
 /* Static description of a return code or device status bit set. */
 const char* sv_status_string(int status);
 
-/* Kernels one spec_verify call launches (for launch accounting). */
-int sv_kernels_per_call(void);
+/* Kernels one spec_verify call over these sizes launches (for launch
+ * accounting): 2, the streaming and the draw kernel; 0 for invalid sizes or
+ * B == 0. */
+int sv_kernels_per_call(int B, int K, int V, int dtype);
 
 #ifdef __cplusplus
 }

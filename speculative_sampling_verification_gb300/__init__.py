@@ -83,7 +83,7 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.spec_verify_static.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp, vp]
     lib.spec_verify_static.restype = i32
-    lib.sv_kernels_per_call.argtypes = []
+    lib.sv_kernels_per_call.argtypes = [i32, i32, i32, i32]
     lib.sv_kernels_per_call.restype = i32
     if path is None:
         _lib = lib
@@ -119,8 +119,8 @@ def sv_status_string(code: int) -> str:
     return load_library().sv_status_string(int(code)).decode()
 
 
-def sv_kernels_per_call() -> int:
-    return int(load_library().sv_kernels_per_call())
+def sv_kernels_per_call(B: int, K: int, V: int, dtype: int) -> int:
+    return int(load_library().sv_kernels_per_call(B, K, V, dtype))
 
 
 def _check(target, draft, tokens, uniforms):

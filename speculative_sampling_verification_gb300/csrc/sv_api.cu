@@ -226,7 +226,7 @@ const char* sv_status_string(int status) {
     case SV_ERR_SCRATCH_LIMIT: return "problem needs more scratch than spec_verify_static holds";
     default: break;
   }
-  if (status & SV_DEV_TIMEOUT) return "device: reserved status bit";
+  if (status & SV_DEV_TIMEOUT) return "device: reserved status bit (never set)";
   if (status & SV_DEV_NONFINITE) return "device: a logit row holds NaN or +inf";
   if (status & SV_DEV_EMPTY_ROW) return "device: a logit row is entirely -inf";
   if (status & SV_DEV_TOKEN_RANGE) return "device: a draft token lies outside [0, V)";
@@ -234,6 +234,10 @@ const char* sv_status_string(int status) {
   return "unknown status";
 }
 
-int sv_kernels_per_call(void) { return sv::kernels_per_call(); }
+int sv_kernels_per_call(int B, int K, int V, int dtype) {
+  sv::Layout L;
+  if (!sv::make_layout(B, K, V, dtype, &L) || B == 0) return 0;
+  return sv::kernels_per_call();
+}
 
 }  // extern "C"

@@ -141,6 +141,69 @@ SV_DEVINL ff ff_warp_sum(ff a) {
   return a;
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs
+// f32x2 instructions: two independent fp32 operations per instruction, each
+// lane rounded to nearest exactly as the scalar _rn operation would be, so a
+// packed routine below gives bit for bit the results of its scalar
+// counterpart on each lane.
+
+SV_DEVINL float2 f2_add(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+SV_DEVINL float2 f2_sub(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+SV_DEVINL float2 f2_mul(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+SV_DEVINL float2 f2_fma(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+SV_DEVINL float2 f2(float v) { return make_float2(v, v); }
+
+// Two float-float values side by side: lane x is (hi.x, lo.x), lane y is
+// (hi.y, lo.y).
+struct ff2 {
+  float2 hi, lo;
+};
+
+// two_sum on each lane.
+SV_DEVINL ff2 two_sum2(float2 a, float2 b) {
+  const float2 s = f2_add(a, b);
+  const float2 bb = f2_sub(s, a);
+  const float2 e = f2_add(f2_sub(a, f2_sub(s, bb)), f2_sub(b, bb));
+  return {s, e};
+}
+
+// ff_accumulate_biased on each lane.
+SV_DEVINL void ff_accumulate_biased2(ff2& acc, const ff2& x) {
+  const float2 s = f2_add(acc.hi, x.hi);
+  const float2 e = f2_sub(x.hi, f2_sub(s, acc.hi));
+  acc.hi = s;
+  acc.lo = f2_add(acc.lo, f2_add(e, x.lo));
+}
+
 // ---------------------------------------------------------------- float-float exponential
 //
 // exp(xh + xl) for xh <= ~0 (|xl| at most an ulp of xh), after Tang's
@@ -179,6 +242,44 @@ SV_DEVINL ff scaled_diff(float l, float m, float ih, float il, bool unit_t) {
   const ff p = two_prod(d.hi, ih);
   const float lo = __fmaf_rn(d.hi, il, __fmaf_rn(d.lo, ih, p.lo));
   return {p.hi, lo};
+}
+
+// exp_ff on each lane of a pair: the same operations in the same order, with
+// the rounding of -k (rint of x * (-256/ln2), which is -rint(x * 256/ln2)
+// exactly) taken in place of negating k.
+SV_DEVINL ff2 exp_ff2(float2 xh, float2 xl, const float2* tab) {
+  const float2 nkf = make_float2(rintf(__fmul_rn(xh.x, -SV_EXP_INV_LN2_256)),
+                                 rintf(__fmul_rn(xh.y, -SV_EXP_INV_LN2_256)));
+  const float2 t = f2_fma(nkf, f2(SV_EXP_LN2_256_HI), xh);  // exact
+  const float2 c = f2_fma(nkf, f2(SV_EXP_LN2_256_LO), xl);
+  const float2 t2 = f2_mul(t, t);
+  const float2 poly = f2_fma(f2_fma(t, f2(1.0f / 24.0f), f2(1.0f / 6.0f)), t, f2(0.5f));
+  const float2 cc = f2_fma(f2_mul(f2(0.5f), c), c, c);
+  const float2 rest = f2_fma(t2, poly, f2_fma(cc, t, cc));
+  const int kx = -__float2int_rn(nkf.x), ky = -__float2int_rn(nkf.y);
+  const float2 Tx = tab[kx & 255], Ty = tab[ky & 255];
+  const float2 Th = make_float2(Tx.x, Ty.x), Tl = make_float2(Tx.y, Ty.y);
+  const float2 ph = f2_mul(Th, t);
+  const float2 pe = f2_fma(Th, t, f2_mul(ph, f2(-1.0f)));
+  const float2 sh = f2_add(Th, ph);
+  const float2 se = f2_sub(ph, f2_sub(sh, Th));
+  const float2 lo = f2_add(f2_fma(Th, rest, f2_fma(Tl, t, Tl)), f2_add(se, pe));
+  const float2 scale = make_float2(__int_as_float(((kx >> 8) + 127) << 23),
+                                   __int_as_float(((ky >> 8) + 127) << 23));
+  const float2 rh = f2_mul(sh, scale), rl = f2_mul(lo, scale);
+  const bool ux = xh.x < -87.0f, uy = xh.y < -87.0f;
+  return {make_float2(ux ? 0.0f : rh.x, uy ? 0.0f : rh.y),
+          make_float2(ux ? 0.0f : rl.x, uy ? 0.0f : rl.y)};
+}
+
+// scaled_diff on each lane; `nm` holds -m of each lane.
+SV_DEVINL ff2 scaled_diff2(float2 l, float2 nm, float ih, float il, bool unit_t) {
+  const ff2 d = two_sum2(l, nm);
+  if (unit_t) return d;
+  const float2 ph = f2_mul(d.hi, f2(ih));
+  const float2 pe = f2_fma(d.hi, f2(ih), f2_mul(ph, f2(-1.0f)));
+  const float2 lo = f2_fma(d.hi, f2(il), f2_fma(d.lo, f2(ih), pe));
+  return {ph, lo};
 }
 
 }  // namespace sv

@@ -125,7 +125,9 @@ struct Params {
 
 // Launchers (sv_kernels.cu). `aligned`: 16-byte aligned rows (vector-load path).
 cudaError_t prepare_device(int device);
-// Optional events recorded around the streaming kernel (any may be null).
+// Optional events recorded around the step (any may be null): `start` before
+// the streaming kernel, `stats_done` between it and the draw kernel, `end`
+// after the draw kernel.
 struct Events {
   cudaEvent_t start = nullptr, stats_done = nullptr, end = nullptr;
 };

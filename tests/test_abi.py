@@ -85,4 +85,11 @@ def test_status_strings(lib):
     for code in (0, 1, 2, 3, 4, 5, 6, 7, 16, 32, 64, 128, 256):
         s = sv.sv_status_string(code)
         assert s and s != "unknown status"
-    assert lib.sv_kernels_per_call() >= 1
+
+
+def test_kernels_per_call(lib):
+    # The streaming and the draw kernel; nothing for invalid sizes or B == 0.
+    assert sv.sv_kernels_per_call(8, 4, 32000, sv.SV_BF16) == 2
+    assert sv.sv_kernels_per_call(256, 4, 256000, sv.SV_F32) == 2
+    assert sv.sv_kernels_per_call(0, 4, 1000, sv.SV_F32) == 0
+    assert sv.sv_kernels_per_call(1, 0, 1000, sv.SV_F32) == 0

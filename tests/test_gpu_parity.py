@@ -267,8 +267,11 @@ def test_host_entry_point_matches_device_entry_point():
     assert np.array_equal(h_out.numpy(), out_d) and np.array_equal(h_nacc.numpy(), nacc_d)
 
 
-def test_graph_capture_replay_and_determinism():
-    w = shrink(WORKLOADS["c3"], B=16, V=50000)
+@pytest.mark.parametrize("B,V", [(16, 50000), (24, 128256)])
+def test_graph_capture_replay_and_determinism(B, V):
+    # 27 MB of logits is one sequence group; 105 MB is three, whose draws run
+    # on the library's second stream, forked and joined inside the capture.
+    w = shrink(WORKLOADS["c3"], B=B, V=V)
     inp = make_inputs(w, step=2)
     args = [to_dev(inp[k]) for k in ("target", "draft", "tokens", "uniforms")]
     B, K = w.B, w.K
@@ -280,6 +283,9 @@ def test_graph_capture_replay_and_determinism():
         assert sv.spec_verify(*args, inp["temperature"], out, nacc, ws) == 0  # first call: set-up
     torch.cuda.synchronize()
     ref_out, ref_nacc = out.clone(), nacc.clone()
+    ref = oracle.verify_inputs(inp)
+    _parity.compare(ref_out.cpu().numpy(), ref_nacc.cpu().numpy(), ref,
+                    inp["tokens"].numpy()).assert_ok()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         sv.spec_verify(*args, inp["temperature"], out, nacc, ws)
