@@ -11,7 +11,11 @@ namespace sv {
 
 // Streaming pass (row statistics): a row is cut into `nseg` segments of
 // `seg_elems` elements; one (row, segment) pair is a unit of work for one warp.
-constexpr long long kTargetUnits = 16384;  // aim for at least this many units per call
+// A call small enough to be one unit per resident warp (152 SMs x 8 CTAs x 4
+// warps) is cut that way, so that it streams in a single wave; larger calls
+// aim for at least kTargetUnits units, for balance across waves.
+constexpr long long kWarpsPerWave = 152 * 8 * 4;
+constexpr long long kTargetUnits = 16384;
 constexpr long long kSegMinBytes = 2048;   // four 16-byte vectors per lane
 constexpr long long kSegMaxBytes = 32768;  // eight rounds of eight 16-byte vectors per lane
 
@@ -60,7 +64,8 @@ inline bool make_layout(int B, int K, int V, int dtype, Layout* L) {
   const long long row_bytes = (long long)V * L->es;
   const long long total_bytes = L->rows_total * row_bytes;
   if (total_bytes > (1LL << 46)) return false;
-  long long target = L->rows_total > kTargetUnits ? L->rows_total : kTargetUnits;
+  long long target = total_bytes <= kWarpsPerWave * kSegMaxBytes ? kWarpsPerWave : kTargetUnits;
+  if (L->rows_total > target) target = L->rows_total;
   long long seg_bytes = target > 0 ? total_bytes / target : kSegMaxBytes;
   if (seg_bytes < kSegMinBytes) seg_bytes = kSegMinBytes;
   if (seg_bytes > kSegMaxBytes) seg_bytes = kSegMaxBytes;
