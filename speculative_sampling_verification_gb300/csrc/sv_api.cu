@@ -62,6 +62,7 @@ int run(const void* target, const void* draft, const int32_t* tokens, const floa
   P.seg_elems = L.seg_elems;
   P.n_units = L.n_units;
   P.nchunk = L.nchunk;
+  P.sub_elems = L.sub_elems;
   P.ns = (long long)L.rows_per_seq * L.nseg;
   P.np = L.nchunk;
   unsigned char* ws = static_cast<unsigned char*>(workspace);

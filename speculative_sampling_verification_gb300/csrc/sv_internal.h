@@ -19,11 +19,11 @@ constexpr long long kTargetUnits = 16384;
 constexpr long long kSegMinBytes = 2048;   // four 16-byte vectors per lane
 constexpr long long kSegMaxBytes = 32768;  // eight rounds of eight 16-byte vectors per lane
 
-// Sampling pass: rows are cut into chunks of 4096 elements (one CTA of 256
-// threads), each chunk into 8 sub-chunks of 512 elements (one warp).
-constexpr int kChunkElems = 4096;
-constexpr int kSubElems = 512;
-constexpr int kSubPerChunk = kChunkElems / kSubElems;
+// Sampling pass: rows are cut into chunks (one CTA of 256 threads), each
+// chunk into 8 sub-chunks (one warp each) of 512 elements, or of 256 when
+// 4096-element chunks would give fewer than two CTAs per SM (152 SMs).
+constexpr int kSubPerChunk = 8;
+constexpr long long kMinDrawCtas = 2 * 152;
 
 constexpr int kMaxK = 64;
 
@@ -49,6 +49,7 @@ struct Layout {
   int seg_elems;         // elements per segment (multiple of 8)
   long long n_units;     // rows_total * nseg
   int nchunk;            // sampling chunks per row
+  int sub_elems;         // elements per sub-chunk (512 or 256)
   size_t off_status, off_ctrl, ctrl_bytes, off_seg, off_row, off_plan, off_sub, total;
 };
 
@@ -76,7 +77,9 @@ inline bool make_layout(int B, int K, int V, int dtype, Layout* L) {
   L->nseg = (int)nseg;
   L->seg_elems = (int)seg_elems;
   L->n_units = L->rows_total * nseg;
-  L->nchunk = (int)(((long long)V + kChunkElems - 1) / kChunkElems);
+  L->sub_elems = (long long)B * ((V + 4095) / 4096) < kMinDrawCtas ? 256 : 512;
+  const long long chunk = (long long)kSubPerChunk * L->sub_elems;
+  L->nchunk = (int)(((long long)V + chunk - 1) / chunk);
   size_t off = 0;
   L->off_status = off;  // status word (read by the host), then the control block
   L->off_ctrl = off;
@@ -109,6 +112,7 @@ struct Params {
   int nseg, seg_elems;
   long long n_units;
   int nchunk;
+  int sub_elems;   // elements per sub-chunk of the draw (512 or 256)
   long long ns;    // streaming units per sequence ((2K+1) * nseg)
   long long np;    // draw chunks per sequence (nchunk)
   void* ctrl;      // control block, zeroed before every launch

@@ -360,7 +360,12 @@ SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
         const ff eq = exp_ff(xq.hi, xq.lo, kSvExp2Table);
         const ff ep = exp_ff(xp.hi, xp.lo, kSvExp2Table);
         if (eq.hi > 1e-30f && ep.hi > 1e-30f) {
-          const double r = (ff_to_double(eq) * (double)sp) / (ff_to_double(ep) * (double)sq);
+          // q/p = (e_q S_p) / (e_p S_q) in float-float: the fp32 quotient and
+          // one correction from the float-float remainder.
+          const ff num = ff_mul_f(eq, sp), den = ff_mul_f(ep, sq);
+          const float q1 = __fdiv_rn(num.hi, den.hi);
+          const ff rem = ff_sub(num, ff_mul_f(den, q1));
+          const double r = ff_to_double(fast_two_sum(q1, __fdiv_rn(rem.hi, den.hi)));
           thr = r >= 1.0 ? 1.0 : r;
         } else {
           const double lr = ((double)lq - (double)lp) * P.inv_t -
@@ -499,13 +504,14 @@ SV_DEVINL void load_run(const unsigned char* row, long long e, int V, bool vec_o
 
 // ---------------------------------------------------------------- draw: one chunk
 
-template <int DT, bool RESID>
+template <int DT, bool RESID, int SUB>
 SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab, bool aligned,
                             long long b, int c) {
   constexpr int kVec = 16 / (DT == 0 ? 2 : 4);
-  constexpr int kRuns = kSubElems / (32 * kVec);
+  constexpr int kRuns = SUB / (32 * kVec);
+  static_assert(kRuns >= 1 && kRuns * 32 * kVec == SUB, "sub-chunk must be whole runs");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long e0 = ((long long)c * kSubPerChunk + w) * kSubElems;
+  const long long e0 = ((long long)c * kSubPerChunk + w) * SUB;
   ff Sq = ff_bias_start(), Sp = ff_bias_start(), A = ff_bias_start(), Bs = ff_bias_start();
   if (e0 < P.V) {
     if constexpr (RESID) {
@@ -628,9 +634,11 @@ SV_DEVINL ff block_exclusive_ff(ff x, CtaShared& sh) {
 // weight before sub-chunk g is S_p * (A[0] + .. + A[g-1]) - S_q * (B[0] + ..
 // + B[g-1]) with S_p, S_q the row totals (at the end: R = S_p A - S_q B), for
 // the bonus draw (or the zero-residual fallback) it is S_q[0] + .. + S_q[g-1].
-template <int DT>
+template <int DT, int SUB>
 SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShared& sh,
                           bool aligned) {
+  constexpr int kPer = SUB / kThreads;  // elements per thread in the exact search
+  static_assert(kPer * kThreads == SUB, "sub-chunk must split evenly over the CTA");
   const int tid = threadIdx.x;
   const int nsub = P.nchunk * kSubPerChunk;
   const float4* part = reinterpret_cast<const float4*>(P.sub_part + (size_t)b * nsub * 4);
@@ -741,12 +749,13 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
     }
     sh.s_pref = weight_before(pa, pb);
   }
-  // Exact search inside sub-chunk gs: two consecutive elements per thread.
+  // Exact search inside sub-chunk gs: kPer consecutive elements per thread.
   const DrawRow d = draw_row(P, pl);
-  const long long e0 = (long long)gs * kSubElems + 2 * tid;
-  ff w[2];
+  const long long e0 = (long long)gs * SUB + kPer * tid;
+  ff w[kPer];
+  ff wsum{0.f, 0.f};
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < kPer; ++k) {
     const long long e = e0 + k;
     w[k] = {0.f, 0.f};
     if (e < P.V) {
@@ -762,31 +771,32 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
         w[k] = ff_normalize(eq);
       }
     }
+    wsum = ff_add(wsum, w[k]);
   }
   // block_exclusive_ff's barriers also publish s_pref.
-  const ff tpre = block_exclusive_ff(ff_add(w[0], w[1]), sh);
+  const ff tpre = block_exclusive_ff(wsum, sh);
   if (tid == 0) {
     sh.g = INT_MAX;
     sh.j = -1;
   }
   __syncthreads();
   ff cum = ff_add(sh.s_pref, tpre);
-  int found = -1;
+  int found = -1, lastk = -1;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < kPer; ++k) {
     cum = ff_add(cum, w[k]);
     if (!last_mode && found < 0 && w[k].hi > 0.f && ff_gt(cum, tau)) found = k;
+    if (w[k].hi > 0.f) lastk = k;
   }
-  if (found >= 0) atomicMin(&sh.g, 2 * tid + found);
-  const int lastk = w[1].hi > 0.f ? 1 : (w[0].hi > 0.f ? 0 : -1);
-  if (lastk >= 0) atomicMax(&sh.j, 2 * tid + lastk);
+  if (found >= 0) atomicMin(&sh.g, kPer * tid + found);
+  if (lastk >= 0) atomicMax(&sh.j, kPer * tid + lastk);
   __syncthreads();
   // The first element whose cumulative weight passes tau; else (u = 1, or
   // rounding at the sub-chunk's end) the last positive element.
   const int pick = sh.g != INT_MAX ? sh.g : sh.j;
-  if (pick >= 0 && pick / 2 == tid) {
-    const ff wt = w[pick & 1];
-    P.out_tokens[b * (P.K + 1) + pl.j] = (int)((long long)gs * kSubElems + pick);
+  if (pick >= 0 && pick / kPer == tid) {
+    const ff wt = w[pick % kPer];
+    P.out_tokens[b * (P.K + 1) + pl.j] = (int)((long long)gs * SUB + pick);
     if (P.dbg_prob) P.dbg_prob[b] = ff_to_double(wt) / ff_to_double(total);
   }
 }
@@ -799,16 +809,10 @@ SV_DEVINL unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
   return old;
 }
 
-SV_DEVINL uint32_t ld_acquire(const unsigned* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // One warp per row segment u. The warp that counts the last segment of a row
 // combines the row; the warp that completes the last row of a sequence scans
-// it. The counters are acquire-release atomics, and a warp that goes on to
-// read what other warps published first acquires the counter in every lane.
+// it. The counters are acquire-release atomics taken by lane 0; __syncwarp
+// then orders the other lanes' reads (through L2) after lane 0's acquire.
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(Params P) {
   __shared__ WarpScan scan_sh[kStatsWarps];
@@ -831,7 +835,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(P
       last = atomic_add_acq_rel(P.done_r + row, 1u) == (unsigned)(P.nseg - 1);
     }
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    (void)ld_acquire(P.done_r + row);
+    __syncwarp();
     st = row_combine(P, row, lane);
   }
   unsigned last = 0;
@@ -840,14 +844,14 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(P
     last = atomic_add_acq_rel(P.done_s + b, 1u) == (unsigned)(P.rows_per_seq - 1);
   }
   if (!__shfl_sync(0xffffffffu, last, 0)) return;
-  (void)ld_acquire(P.done_s + b);
+  __syncwarp();
   scan_warp(P, b, lane, scan_sh[warp]);
 }
 
 // One CTA per draw chunk c of sequence b (the plans are complete once the
 // streaming grid is); the CTA that counts the last chunk of a sequence runs
 // its inverse-CDF search.
-template <int DT, bool VEC>
+template <int DT, bool VEC, int SUB>
 __global__ void __launch_bounds__(kThreads) draw_kernel(Params P) {
   __shared__ CtaShared sh;
   const int tid = threadIdx.x;
@@ -863,16 +867,13 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(Params P) {
   if (pl.mode == kModeFailed) return;  // outputs already written by the scan
   const DrawRow d = draw_row(P, pl);
   if (pl.mode == kModeResidual)
-    partial_body<DT, true>(P, d, sh.tab, VEC, b, c);
+    partial_body<DT, true, SUB>(P, d, sh.tab, VEC, b, c);
   else
-    partial_body<DT, false>(P, d, sh.tab, VEC, b, c);
+    partial_body<DT, false, SUB>(P, d, sh.tab, VEC, b, c);
   __syncthreads();  // all sub-chunk writes of this CTA precede the release below
   if (tid == 0) sh.flag = atomic_add_acq_rel(P.done_p + b, 1u) == (unsigned)(P.np - 1);
   __syncthreads();
-  if (sh.flag) {
-    __threadfence();
-    finish_seq<DT>(P, b, pl, sh, VEC);
-  }
+  if (sh.flag) finish_seq<DT, SUB>(P, b, pl, sh, VEC);  // the barrier above orders its reads
 }
 
 // ---------------------------------------------------------------- host-side launch
@@ -885,7 +886,7 @@ DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
 }  // namespace
 
-template <int DT, bool VEC>
+template <int DT, bool VEC, int SUB>
 cudaError_t launch_pair(const Params& P, cudaStream_t st, const Events& ev) {
   const unsigned stats_grid = (unsigned)((P.n_units + kStatsWarps - 1) / kStatsWarps);
   stats_kernel<DT, VEC><<<stats_grid, kStatsThreads, 0, st>>>(P);
@@ -908,7 +909,7 @@ cudaError_t launch_pair(const Params& P, cudaStream_t st, const Events& ev) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = ev.stats_done ? 0 : 1;
-  return cudaLaunchKernelEx(&cfg, draw_kernel<DT, VEC>, P);
+  return cudaLaunchKernelEx(&cfg, draw_kernel<DT, VEC, SUB>, P);
 }
 
 cudaError_t prepare_device(int device) {
@@ -932,10 +933,13 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
     e = cudaEventRecordWithFlags(ev.start, st, cudaEventRecordExternal);
     if (e != cudaSuccess) return e;
   }
+  const bool big = P.sub_elems == 512;
   if (P.dtype == 0)
-    e = aligned ? launch_pair<0, true>(P, st, ev) : launch_pair<0, false>(P, st, ev);
+    e = aligned ? (big ? launch_pair<0, true, 512>(P, st, ev) : launch_pair<0, true, 256>(P, st, ev))
+                : (big ? launch_pair<0, false, 512>(P, st, ev) : launch_pair<0, false, 256>(P, st, ev));
   else
-    e = aligned ? launch_pair<1, true>(P, st, ev) : launch_pair<1, false>(P, st, ev);
+    e = aligned ? (big ? launch_pair<1, true, 512>(P, st, ev) : launch_pair<1, true, 256>(P, st, ev))
+                : (big ? launch_pair<1, false, 512>(P, st, ev) : launch_pair<1, false, 256>(P, st, ev));
   if (e != cudaSuccess) return e;
   if (ev.end) e = cudaEventRecordWithFlags(ev.end, st, cudaEventRecordExternal);
   return e;
