@@ -206,6 +206,11 @@ SV_DEVINL void ff_accumulate_biased2(ff2& acc, const ff2& x) {
 
 // ---------------------------------------------------------------- float-float exponential
 //
+// Adding 1.5 * 2^23 to a float y with |y| <= 2^22 rounds it to an integer
+// (ties to even) in the low mantissa bits: (y + M) - M == rint(y), and the
+// integer is bits(y + M) - bits(M).
+constexpr float kRoundMagic = 12582912.0f;
+
 // exp(xh + xl) for xh <= ~0 (|xl| at most an ulp of xh), after Tang's
 // table-driven method: k = rint(x * 256/ln2), r = x - k*ln2/256 (two-constant
 // reduction; the head product is exact because head(ln2/256) has its last bit
@@ -215,14 +220,16 @@ SV_DEVINL void ff_accumulate_biased2(ff2& acc, const ff2& x) {
 // -87 (below 2^-125) returns 0. `tab` points at the 256-entry table in
 // shared memory.
 SV_DEVINL ff exp_ff(float xh, float xl, const float2* tab) {
-  const float kf = rintf(__fmul_rn(xh, SV_EXP_INV_LN2_256));
+  // |x * 256/ln2| <= 2^22 wherever the result is not flushed to zero below.
+  const float ym = __fadd_rn(__fmul_rn(xh, SV_EXP_INV_LN2_256), kRoundMagic);
+  const float kf = __fsub_rn(ym, kRoundMagic);
   const float t = __fmaf_rn(-kf, SV_EXP_LN2_256_HI, xh);     // exact
   const float c = __fmaf_rn(-kf, SV_EXP_LN2_256_LO, xl);     // small correction, |c| < 1e-5
   const float t2 = __fmul_rn(t, t);
   const float poly = __fmaf_rn(__fmaf_rn(t, 1.0f / 24.0f, 1.0f / 6.0f), t, 0.5f);
   const float cc = __fmaf_rn(__fmul_rn(0.5f, c), c, c);       // c + c^2/2
   const float rest = __fmaf_rn(t2, poly, __fmaf_rn(cc, t, cc));  // expm1(t + c) - t
-  const int k = __float2int_rn(kf);
+  const int k = __float_as_int(ym) - __float_as_int(kRoundMagic);
   const float2 T = tab[k & 255];
   const ff pr = two_prod(T.x, t);
   const ff s = fast_two_sum(T.x, pr.hi);
@@ -245,18 +252,18 @@ SV_DEVINL ff scaled_diff(float l, float m, float ih, float il, bool unit_t) {
 }
 
 // exp_ff on each lane of a pair: the same operations in the same order, with
-// the rounding of -k (rint of x * (-256/ln2), which is -rint(x * 256/ln2)
-// exactly) taken in place of negating k.
+// -k rounded from x * (-256/ln2), which gives exactly -rint(x * 256/ln2).
 SV_DEVINL ff2 exp_ff2(float2 xh, float2 xl, const float2* tab) {
-  const float2 nkf = make_float2(rintf(__fmul_rn(xh.x, -SV_EXP_INV_LN2_256)),
-                                 rintf(__fmul_rn(xh.y, -SV_EXP_INV_LN2_256)));
+  const float2 ym = f2_add(f2_mul(xh, f2(-SV_EXP_INV_LN2_256)), f2(kRoundMagic));
+  const float2 nkf = f2_sub(ym, f2(kRoundMagic));
   const float2 t = f2_fma(nkf, f2(SV_EXP_LN2_256_HI), xh);  // exact
   const float2 c = f2_fma(nkf, f2(SV_EXP_LN2_256_LO), xl);
   const float2 t2 = f2_mul(t, t);
   const float2 poly = f2_fma(f2_fma(t, f2(1.0f / 24.0f), f2(1.0f / 6.0f)), t, f2(0.5f));
   const float2 cc = f2_fma(f2_mul(f2(0.5f), c), c, c);
   const float2 rest = f2_fma(t2, poly, f2_fma(cc, t, cc));
-  const int kx = -__float2int_rn(nkf.x), ky = -__float2int_rn(nkf.y);
+  const int kx = __float_as_int(kRoundMagic) - __float_as_int(ym.x);
+  const int ky = __float_as_int(kRoundMagic) - __float_as_int(ym.y);
   const float2 Tx = tab[kx & 255], Ty = tab[ky & 255];
   const float2 Th = make_float2(Tx.x, Ty.x), Tl = make_float2(Tx.y, Ty.y);
   const float2 ph = f2_mul(Th, t);

@@ -213,11 +213,19 @@ SV_DEVINL float2 stats_warp_vec(const Params& P, long long u, int lane) {
   float m_run = neg_inf(), H = neg_inf();
   float2 acc[2] = {f2(0.0f), f2(0.0f)};
   bool nan_seen = false;
-  for (int i0 = 0; i0 < nvec; i0 += kStatsVec * 32) {
+  constexpr int kRound = kStatsVec * 32;
+  const int nfull = nvec / kRound * kRound;
+  for (int i0 = 0; i0 < nfull; i0 += kRound) {  // whole rounds: no bounds tests
+    uint4 v[kStatsVec];
+#pragma unroll
+    for (int k = 0; k < kStatsVec; ++k) v[k] = ld_global_nc_v4(base + (size_t)(i0 + k * 32 + lane) * 16);
+    stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
+  }
+  if (nfull < nvec) {  // the last, partial round, padded with -inf
     uint4 v[kStatsVec];
 #pragma unroll
     for (int k = 0; k < kStatsVec; ++k) {
-      const int idx = i0 + k * 32 + lane;
+      const int idx = nfull + k * 32 + lane;
       v[k] = idx < nvec ? ld_global_nc_v4(base + (size_t)idx * 16) : make_uint4(fill, fill, fill, fill);
     }
     stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
@@ -852,7 +860,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(P
 // streaming grid is); the CTA that counts the last chunk of a sequence runs
 // its inverse-CDF search.
 template <int DT, bool VEC, int SUB>
-__global__ void __launch_bounds__(kThreads) draw_kernel(Params P) {
+__global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
   __shared__ CtaShared sh;
   const int tid = threadIdx.x;
   sh.tab[tid] = kSvExp2Table[tid];
