@@ -6,12 +6,14 @@ benchmark's CPU-baseline leg, never by the library.
 
 from .spec_sampling import (  # noqa: F401
     OracleResult,
+    SampleResult,
     STATUS_EMPTY_ROW,
     STATUS_NONFINITE,
     STATUS_OK,
     STATUS_TOKEN_RANGE,
     STATUS_UNIFORM_RANGE,
     acceptance_thresholds,
+    draft_sample,
     first_rejection,
     inverse_cdf,
     residual_weights,

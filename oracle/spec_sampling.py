@@ -6,7 +6,8 @@ calls anything here, and this module shares no code with it.
 
 What it computes, step by step, in the order and notation of
 "Accelerating Large Language Model Decoding with Speculative Sampling"
-(Chen et al., DeepMind), as summarised by its wikillm.com paper card:
+(Chen et al., DeepMind), as summarised by its wikillm.com paper card (the
+draft-side sampler of Algorithm 2 step 1, `draft_sample`, follows `verify`):
 
 * q(.|...) and p(.|...) are the target and draft distributions. The decoding
   transform (temperature) is applied to both before anything else
@@ -225,6 +226,46 @@ def verify(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
     lse = np.concatenate([lse_q, lse_p], axis=1)
     return OracleResult(out, n_acc, status, thr, accept_margin, sample_margin, sample_prob,
                         fallback, lse)
+
+
+@dataclass
+class SampleResult:
+    tokens: np.ndarray           # [N] int64, -1 for failed rows
+    status: np.ndarray           # [N] status bits (U12), 0 = ok
+    sample_margin: np.ndarray    # [N] distance of u from the chosen CDF interval's ends
+    sample_prob: np.ndarray      # [N] probability of the drawn token
+    lse: np.ndarray              # [N] log sum_i exp(l_i / T)
+
+
+def draft_sample(logits: np.ndarray, uniforms: np.ndarray, temperature: float) -> SampleResult:
+    """Draft-side sampling: one token per row, x~ ~ softmax(l / T).
+
+    This is step 1 of the card's Algorithm 2 (the K sequential draft samples,
+    one row per call here), drawn from the transformed draft distribution as
+    the card's Pitfalls require ("Use the same transformed distributions
+    everywhere": draft tokens must come from the transformed p). The draw is
+    the inverse CDF of U3 with the row's uniform; rows fail as in U12 (NaN or
+    +inf entries, every entry -inf, or a uniform that is NaN or outside
+    [0, 1]): token -1 and a status word saying why.
+
+    logits [N, V] (widened exactly), uniforms [N], temperature > 0 (an fp32
+    value widened exactly, U6).
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    uniforms = np.asarray(uniforms, dtype=np.float64)
+    if logits.ndim != 2 or uniforms.shape != (logits.shape[0],):
+        raise ValueError("shape mismatch")
+    with np.errstate(over="ignore"):
+        T = float(np.float32(temperature))
+    if not (np.isfinite(T) and T > 0):
+        raise ValueError("temperature must be finite and > 0")
+    p, lse, status = temperature_softmax(logits, T)
+    u_ok = (uniforms >= 0) & (uniforms <= 1)   # NaN compares false
+    status = status | np.where(u_ok, 0, STATUS_UNIFORM_RANGE)
+    idx, margin, prob = inverse_cdf(p, np.where(u_ok, uniforms, 0.0))
+    failed = status != 0
+    return SampleResult(np.where(failed, -1, idx), status, np.where(failed, np.nan, margin),
+                        np.where(failed, np.nan, prob), np.where(failed, np.nan, lse))
 
 
 def _widen(x) -> np.ndarray:

@@ -27,7 +27,8 @@ import numpy as np
 from scipy.special import logsumexp, softmax
 from scipy.stats import chi2
 
-GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "hand_cases.json")
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+GOLDEN = os.path.join(GOLDEN_DIR, "hand_cases.json")
 
 
 # ---------------------------------------------------------------- helpers
@@ -342,5 +343,82 @@ def pin_failures(O):
         assert (r.out_tokens[b] == -1).all() and r.n_accepted[b] == -1
 
 
+# ---------------------------------------------------------------- draft-side sampler pins
+
+def load_draft_golden():
+    with open(os.path.join(GOLDEN_DIR, "draft_sample_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+def _golden_logits(vals):
+    return np.array([[-np.inf if v == "-inf" else float(v) for v in vals]])
+
+
+def pin_draft_golden(O):
+    """Hand-worked draws (tests/golden/draft_sample_cases.json)."""
+    for c in load_draft_golden():
+        r = O.draft_sample(_golden_logits(c["logits"]), np.array([c["u"]]), c["temperature"])
+        name = c["name"]
+        assert r.status[0] == 0, name
+        assert r.tokens[0] == c["token"], (name, r.tokens[0])
+        np.testing.assert_allclose(r.sample_prob[0], c["prob"], atol=1e-12, err_msg=name)
+        np.testing.assert_allclose(r.sample_margin[0], c["margin"], atol=1e-12, err_msg=name)
+
+
+def pin_draft_law(O, n=200_000, V=16, seed=11):
+    """The sampler's law is softmax(l / T): chi-square of seeded draws against
+    scipy's softmax (a different routine from the oracle's)."""
+    from scipy import stats
+
+    rng = np.random.default_rng(seed)
+    logits = rng.normal(0.0, 2.0, size=V)
+    T = 0.7
+    u = rng.random(n)
+    r = O.draft_sample(np.repeat(logits[None], n, axis=0), u, T)
+    assert (r.status == 0).all()
+    counts = np.bincount(r.tokens, minlength=V)
+    expect = softmax(logits / np.float32(T).astype(np.float64)) * n
+    keep = expect > 5
+    obs, exp = counts[keep], expect[keep]
+    if (~keep).any():  # lump the rare tokens into one bin
+        obs, exp = np.append(obs, counts[~keep].sum()), np.append(exp, expect[~keep].sum())
+    assert stats.chisquare(obs, exp * obs.sum() / exp.sum()).pvalue > 1e-4
+
+
+def pin_draft_failures(O):
+    """U12 for the sampler: each bad row fails alone with its status bit."""
+    good = np.zeros(6)
+    rows = np.stack([good, good, good, good, good, good])
+    rows[1, 2] = np.nan
+    rows[2, 4] = np.inf
+    rows[3, :] = -np.inf
+    u = np.array([0.3, 0.3, 0.3, 0.3, np.nan, 1.5])
+    r = O.draft_sample(rows, u, 1.0)
+    assert r.status[0] == 0 and r.tokens[0] == 1   # C_0 = 1/6 <= 0.3 < C_1 = 1/3
+    assert r.status[1] == O.STATUS_NONFINITE and r.tokens[1] == -1
+    assert r.status[2] == O.STATUS_NONFINITE and r.tokens[2] == -1
+    assert r.status[3] == O.STATUS_EMPTY_ROW and r.tokens[3] == -1
+    assert r.status[4] == O.STATUS_UNIFORM_RANGE and r.tokens[4] == -1
+    assert r.status[5] == O.STATUS_UNIFORM_RANGE and r.tokens[5] == -1
+    r = O.draft_sample(np.zeros((1, 3)), np.array([-0.1]), 1.0)
+    assert r.status[0] == O.STATUS_UNIFORM_RANGE
+
+
+def pin_draft_matches_bonus(O):
+    """When every draft is accepted, the verifier's bonus draw (Algorithm 2
+    step 4) is the sampler applied to target row K with uniform u[K+1]."""
+    rng = np.random.default_rng(13)
+    B, K, V = 6, 3, 40
+    tl = rng.normal(0, 1.5, size=(B, K + 1, V))
+    dl = tl[:, :K].copy()                      # p == q on every drafted row: all accept
+    tok = rng.integers(0, V, size=(B, K))
+    uni = rng.random((B, K + 2))
+    r = O.verify(tl, dl, tok, uni, 0.9)
+    assert (r.n_accepted == K).all()
+    s = O.draft_sample(tl[:, K], uni[:, K + 1], 0.9)
+    assert (r.out_tokens[:, K] == s.tokens).all()
+
+
 FAST_PINS = (pin_golden, pin_theorem1, pin_sequential, pin_library_special_cases,
-             pin_invariants, pin_failures)
+             pin_invariants, pin_failures, pin_draft_golden, pin_draft_failures,
+             pin_draft_matches_bonus)

@@ -45,6 +45,12 @@ MUTATIONS = [
      "u_acc = uniforms[:, :K]", "u_acc = uniforms[:, 1:K + 1]"),
     ("q(x)=0 accepts",
      "np.where(q_at > 0, 1.0, 0.0)", "np.where(q_at > 0, 1.0, 1.0)"),
+    ("sampler ignores the temperature",
+     "p, lse, status = temperature_softmax(logits, T)", "p, lse, status = temperature_softmax(logits, 1.0)"),
+    ("sampler accepts bad uniforms",
+     "status = status | np.where(u_ok, 0, STATUS_UNIFORM_RANGE)", "status = status"),
+    ("sampler reports failed rows' draws",
+     "return SampleResult(np.where(failed, -1, idx), status,", "return SampleResult(idx, status,"),
 ]
 
 

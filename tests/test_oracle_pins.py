@@ -83,3 +83,19 @@ def test_rejects_bad_temperature_and_shapes():
         oracle.verify(tl, dl, np.zeros((1, 1)), np.zeros((1, 3)), float("nan"))
     with pytest.raises(ValueError):
         oracle.verify(tl, dl, np.zeros((1, 2)), np.zeros((1, 3)), 1.0)
+
+
+def test_draft_sampler_hand_cases():
+    _pins.pin_draft_golden(oracle)
+
+
+def test_draft_sampler_law_is_softmax():
+    _pins.pin_draft_law(oracle)
+
+
+def test_draft_sampler_failures():
+    _pins.pin_draft_failures(oracle)
+
+
+def test_draft_sampler_is_the_bonus_draw():
+    _pins.pin_draft_matches_bonus(oracle)
