@@ -176,6 +176,39 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
                        int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
                        void* stream);
 
+/* ---------------------------------------------------------------- draft-side sampler
+ *
+ * Step 1 of the card's Algorithm 2: the draft model's tokens x~_t ~ p(.),
+ * drawn from the transformed distribution p = softmax(l / T), which the card's
+ * Pitfalls require ("Use the same transformed distributions everywhere":
+ * draft tokens must be sampled from the transformed p). One token per row, by
+ * the inverse-CDF convention above with the row's uniform; rows are
+ * independent, so a caller samples one draft position for a batch per call
+ * (or several positions at once when their logits are already known). */
+
+/* Bytes of device workspace spec_draft_sample needs for N rows of V elements;
+ * 0 for invalid sizes. Pure host function. */
+size_t sv_sample_workspace_size(int N, int V, int dtype);
+
+/* One token per row:
+ *   logits       device, [N, V] row-major, dtype elements (element-aligned;
+ *                16-byte aligned with V * sizeof(dtype) a multiple of 16 takes
+ *                the 16-byte vector-load path)
+ *   uniforms     device, [N] fp32: the uniform of each row's draw
+ *   temperature  T > 0, finite (fp32)
+ *   out_tokens   device, [N] int32: the drawn token, or -1 for a failed row
+ *   sample_prob  device, [N] fp64, may be NULL: probability of the drawn token
+ *   workspace    device, sv_sample_workspace_size() bytes, 256-byte aligned,
+ *                caller-owned; one call at a time per workspace
+ * A row fails (token -1, status bit) if it holds NaN or +inf, is entirely
+ * -inf, or its uniform is NaN or outside [0, 1]; other rows are unaffected.
+ * Returns SV_OK once the work is enqueued on `stream`, or a host-side error
+ * code with nothing enqueued; N == 0 returns SV_OK at once. Device status bits
+ * are read with sv_read_device_status(). */
+int spec_draft_sample(const void* logits, const float* uniforms, int N, int V, int dtype,
+                      float temperature, int32_t* out_tokens, double* sample_prob,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* Reads the device status word of the last call that used `workspace`: waits
  * for `stream`, then stores the OR of the SV_DEV_* bits in *status. */
 int sv_read_device_status(const void* workspace, void* stream, int* status);

@@ -25,6 +25,7 @@ __all__ = [
     "spec_verify", "spec_verify_debug", "spec_verify_profiled", "spec_verify_host",
     "sv_read_device_status",
     "sv_status_string", "sv_kernels_per_call", "spec_verify_static", "verify",
+    "sv_sample_workspace_size", "spec_draft_sample", "draft_sample",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -38,7 +39,7 @@ EXPORTED_SYMBOLS = (
     "sv_workspace_size", "spec_verify", "spec_verify_debug", "spec_verify_profiled",
     "sv_staging_size",
     "spec_verify_host", "sv_read_device_status", "sv_status_string", "sv_kernels_per_call",
-    "spec_verify_static",
+    "spec_verify_static", "sv_sample_workspace_size", "spec_draft_sample",
 )
 
 _lib = None
@@ -83,6 +84,10 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.spec_verify_static.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp, vp]
     lib.spec_verify_static.restype = i32
+    lib.sv_sample_workspace_size.argtypes = [i32, i32, i32]
+    lib.sv_sample_workspace_size.restype = sz
+    lib.spec_draft_sample.argtypes = [vp, vp, i32, i32, i32, f32, vp, dp, vp, sz, vp]
+    lib.spec_draft_sample.restype = i32
     lib.sv_kernels_per_call.argtypes = [i32, i32, i32, i32]
     lib.sv_kernels_per_call.restype = i32
     if path is None:
@@ -249,3 +254,45 @@ def verify(target, draft, tokens, uniforms, temperature, *, workspace=None, debu
         return out, nacc, {"row_lse": lse, "thresholds": thr, "sample_prob": prob,
                            "workspace": ws}
     return out, nacc
+
+
+def sv_sample_workspace_size(N: int, V: int, dtype: int) -> int:
+    return int(load_library().sv_sample_workspace_size(N, V, dtype))
+
+
+def spec_draft_sample(logits, uniforms, temperature, out_tokens, workspace, sample_prob=None,
+                      stream=None) -> int:
+    """Direct binding of the sampler on torch tensors: logits [N, V] bf16/f32,
+    uniforms [N] f32, out_tokens [N] int32; returns the host status code."""
+    for name, t in (("logits", logits), ("uniforms", uniforms), ("out_tokens", out_tokens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if logits.dim() != 2:
+        raise ValueError("logits must be [N, V]")
+    N, V = logits.shape
+    if tuple(uniforms.shape) != (N,) or uniforms.dtype != torch.float32:
+        raise ValueError("uniforms must be [N] float32")
+    if tuple(out_tokens.shape) != (N,) or out_tokens.dtype != torch.int32:
+        raise ValueError("out_tokens must be [N] int32")
+    return int(load_library().spec_draft_sample(
+        _ptr(logits), _ptr(uniforms), N, V, _dtype_code(logits), ctypes.c_float(temperature),
+        _ptr(out_tokens), _ptr(sample_prob), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(logits.device, stream)))
+
+
+def draft_sample(logits, uniforms, temperature, *, workspace=None, with_prob=False, stream=None):
+    """Allocate the outputs (and a workspace if none is given) with torch and
+    draw one token per row of `logits`; returns tokens [N] int32 (and the
+    drawn tokens' probabilities [N] fp64 when `with_prob`)."""
+    N, V = logits.shape
+    dev = logits.device
+    out = torch.empty(N, dtype=torch.int32, device=dev)
+    prob = torch.empty(N, dtype=torch.float64, device=dev) if with_prob else None
+    ws = workspace
+    if ws is None:
+        n = sv_sample_workspace_size(N, V, _dtype_code(logits))
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    rc = spec_draft_sample(logits, uniforms, temperature, out, ws, prob, stream=stream)
+    if rc != SV_OK:
+        raise StatusError(rc, "spec_draft_sample")
+    return (out, prob) if with_prob else out

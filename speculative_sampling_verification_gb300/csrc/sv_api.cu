@@ -9,6 +9,9 @@
 #include "../../include/spec_verify.h"
 #include "sv_internal.h"
 
+static void fill_params(sv::Params& P, const sv::Layout& L, int B, int K, int V, int dtype,
+                        float temperature, void* workspace);
+
 namespace {
 
 bool misaligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
@@ -41,10 +44,45 @@ int run(const void* target, const void* draft, const int32_t* tokens, const floa
   if (rc != SV_OK || B == 0) return rc;
 
   sv::Params P{};
+  fill_params(P, L, B, K, V, dtype, temperature, workspace);
   P.target = target;
   P.draft = draft;
   P.tokens = tokens;
   P.uniforms = uniforms;
+  P.out_tokens = out;
+  P.n_acc = n_acc;
+  P.dbg_lse = dbg_lse;
+  P.dbg_thr = dbg_thr;
+  P.dbg_prob = dbg_prob;
+  const bool aligned = !misaligned(target, 16) && !misaligned(draft, 16) &&
+                       ((size_t)V * L.es) % 16 == 0;
+  cudaError_t e = sv::launch_all(P, aligned, static_cast<cudaStream_t>(stream), ev);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// Checks of the sampler's arguments that need no device.
+int validate_sample(const void* logits, const void* uniforms, int N, int V, int dtype,
+                    float temperature, const void* out, const void* workspace,
+                    size_t workspace_bytes, sv::Layout* L) {
+  if (dtype != SV_BF16 && dtype != SV_F32) return SV_ERR_DTYPE;
+  if (!sv::make_sample_layout(N, V, dtype, L)) return SV_ERR_SHAPE;
+  if (!std::isfinite(temperature) || !(temperature > 0.0f)) return SV_ERR_TEMPERATURE;
+  if (N == 0) return SV_OK;
+  if (!logits || !uniforms || !out || !workspace) return SV_ERR_NULL;
+  const size_t es = dtype == SV_BF16 ? 2 : 4;
+  if (misaligned(logits, es) || misaligned(uniforms, 4) || misaligned(out, 4) ||
+      misaligned(workspace, 256))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < L->total) return SV_ERR_WORKSPACE;
+  return SV_OK;
+}
+
+}  // namespace
+
+// Parameter fields shared by the verification and the sampler: sizes, the
+// temperature constants, the layout and the workspace's pointers.
+static void fill_params(sv::Params& P, const sv::Layout& L, int B, int K, int V, int dtype,
+                        float temperature, void* workspace) {
   P.B = B;
   P.K = K;
   P.V = V;
@@ -78,16 +116,9 @@ int run(const void* target, const void* draft, const int32_t* tokens, const floa
   P.row_stat = reinterpret_cast<float2*>(ws + L.off_row);
   P.plans = reinterpret_cast<sv::Plan*>(ws + L.off_plan);
   P.sub_part = reinterpret_cast<float2*>(ws + L.off_sub);
-  P.out_tokens = out;
-  P.n_acc = n_acc;
-  P.dbg_lse = dbg_lse;
-  P.dbg_thr = dbg_thr;
-  P.dbg_prob = dbg_prob;
-  const bool aligned = !misaligned(target, 16) && !misaligned(draft, 16) &&
-                       ((size_t)V * L.es) % 16 == 0;
-  cudaError_t e = sv::launch_all(P, aligned, static_cast<cudaStream_t>(stream), ev);
-  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
+
+namespace {
 
 struct Staging {
   size_t target, draft, tokens, uniforms, out, nacc, total;
@@ -200,6 +231,31 @@ int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
     return SV_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
   return (int)status;
+}
+
+size_t sv_sample_workspace_size(int N, int V, int dtype) {
+  sv::Layout L;
+  if (!sv::make_sample_layout(N, V, dtype, &L)) return 0;
+  return L.total;
+}
+
+int spec_draft_sample(const void* logits, const float* uniforms, int N, int V, int dtype,
+                      float temperature, int32_t* out_tokens, double* sample_prob,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  sv::Layout L;
+  const int rc = validate_sample(logits, uniforms, N, V, dtype, temperature, out_tokens,
+                                 workspace, workspace_bytes, &L);
+  if (rc != SV_OK || N == 0) return rc;
+  sv::Params P{};
+  fill_params(P, L, N, 0, V, dtype, temperature, workspace);
+  P.sampler = 1;
+  P.target = logits;
+  P.uniforms = uniforms;
+  P.out_tokens = out_tokens;
+  P.dbg_prob = sample_prob;
+  const bool aligned = !misaligned(logits, 16) && ((size_t)V * L.es) % 16 == 0;
+  const cudaError_t e = sv::launch_all(P, aligned, static_cast<cudaStream_t>(stream), sv::Events());
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 int sv_read_device_status(const void* workspace, void* stream, int* status) {

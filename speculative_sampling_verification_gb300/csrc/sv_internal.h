@@ -55,12 +55,13 @@ struct Layout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Pure host computation of the workspace layout; false for invalid sizes.
-inline bool make_layout(int B, int K, int V, int dtype, Layout* L) {
-  if (B < 0 || K < 1 || K > kMaxK || V < 1) return false;
+// Pure host computation of the workspace layout for B sequences of
+// `rows_per_seq` rows of V elements; false for invalid sizes.
+inline bool make_layout_rows(int B, int rows_per_seq, int V, int dtype, Layout* L) {
+  if (B < 0 || rows_per_seq < 1 || V < 1) return false;
   if (dtype != 0 && dtype != 1) return false;
   L->es = dtype == 0 ? 2 : 4;
-  L->rows_per_seq = 2 * K + 1;
+  L->rows_per_seq = rows_per_seq;
   L->rows_total = (long long)B * L->rows_per_seq;
   const long long row_bytes = (long long)V * L->es;
   const long long total_bytes = L->rows_total * row_bytes;
@@ -98,6 +99,17 @@ inline bool make_layout(int B, int K, int V, int dtype, Layout* L) {
   return true;
 }
 
+// The verification step: B sequences of 2K+1 rows (K+1 target, K draft).
+inline bool make_layout(int B, int K, int V, int dtype, Layout* L) {
+  if (K < 1 || K > kMaxK) return false;
+  return make_layout_rows(B, 2 * K + 1, V, dtype, L);
+}
+
+// The draft-side sampler: N independent rows, each its own "sequence".
+inline bool make_sample_layout(int N, int V, int dtype, Layout* L) {
+  return make_layout_rows(N, 1, V, dtype, L);
+}
+
 struct Params {
   const void* target;
   const void* draft;
@@ -107,6 +119,7 @@ struct Params {
   float c2;        // log2(e) / T in fp32 (streaming pass)
   float ih, il;    // 1/T as a float-float (sampling pass)
   int unit_t;      // T == 1 exactly
+  int sampler;     // 1: draft-side sampler (one row per sequence, K = 0, no scan)
   double inv_t;    // 1/T in fp64 (scan)
   int rows_per_seq;
   int nseg, seg_elems;

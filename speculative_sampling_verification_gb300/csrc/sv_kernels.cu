@@ -817,6 +817,41 @@ SV_DEVINL unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
   return old;
 }
 
+// Draft-side sampler: once row b's statistics are complete, its plan is a
+// bonus-mode draw from the row with the row's uniform (or, for a bad row or
+// uniform, the failure outputs) -- there is no acceptance scan.
+SV_DEVINL void sample_plan(const Params& P, long long b, float2 st, int lane) {
+  if (lane != 0) return;
+  unsigned bits = 0;
+  if (st.y != st.y) {
+    bits = kDevNonfinite;
+  } else if (st.x == neg_inf()) {
+    bits = kDevEmptyRow;
+  }
+  const float u = P.uniforms[b];
+  if (!(u >= 0.0f && u <= 1.0f)) bits |= kDevUniformRange;
+  if (P.dbg_lse)
+    P.dbg_lse[b] = bits ? __longlong_as_double(0x7ff8000000000000LL)
+                        : (double)st.x * P.inv_t + log((double)st.y);
+  Plan pl{};
+  if (bits) {
+    atomicOr(P.status, bits);
+    pl.j = -1;
+    pl.mode = kModeFailed;
+    P.out_tokens[b] = -1;
+    if (P.dbg_prob) P.dbg_prob[b] = __longlong_as_double(0x7ff8000000000000LL);
+  } else {
+    pl.j = 0;
+    pl.mode = kModeBonus;
+    pl.row_q = b;
+    pl.row_p = -1;
+    pl.m_q = st.x;
+    pl.s_q = st.y;
+    pl.u = u;
+  }
+  P.plans[b] = pl;
+}
+
 // One warp per row segment u. The warp that counts the last segment of a row
 // combines the row; the warp that completes the last row of a sequence scans
 // it. The counters are acquire-release atomics taken by lane 0; __syncwarp
@@ -845,6 +880,10 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(P
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __syncwarp();
     st = row_combine(P, row, lane);
+  }
+  if (P.sampler) {
+    sample_plan(P, row, st, lane);
+    return;
   }
   unsigned last = 0;
   if (lane == 0) {

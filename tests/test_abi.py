@@ -93,3 +93,36 @@ def test_kernels_per_call(lib):
     assert sv.sv_kernels_per_call(256, 4, 256000, sv.SV_F32) == 2
     assert sv.sv_kernels_per_call(0, 4, 1000, sv.SV_F32) == 0
     assert sv.sv_kernels_per_call(1, 0, 1000, sv.SV_F32) == 0
+
+
+def _call_sample(lib, **kw):
+    a = dict(l=1 << 20, u=1 << 20, N=3, V=100, dtype=sv.SV_F32, T=1.0, out=1 << 20, prob=0,
+             ws=1 << 20, wsb=1 << 30)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.spec_draft_sample(vp(a["l"]), vp(a["u"]), a["N"], a["V"], a["dtype"],
+                                 ctypes.c_float(a["T"]), vp(a["out"]), vp(a["prob"]) if a["prob"] else None,
+                                 vp(a["ws"]), a["wsb"], None)
+
+
+def test_sampler_workspace_and_validation(lib):
+    s1 = lib.sv_sample_workspace_size(32, 32000, sv.SV_BF16)
+    s2 = lib.sv_sample_workspace_size(512, 128256, sv.SV_BF16)
+    assert 0 < s1 < s2 and s1 % 256 == 0
+    for bad in ((-1, 10, 0), (1, 0, 0), (1, 10, 7)):
+        assert lib.sv_sample_workspace_size(*bad) == 0
+    # Every case fails validation before any CUDA call is made.
+    assert _call_sample(lib, dtype=3) == 4
+    assert _call_sample(lib, V=0) == 2
+    assert _call_sample(lib, N=-1) == 2
+    assert _call_sample(lib, T=0.0) == 3
+    assert _call_sample(lib, T=float("nan")) == 3
+    assert _call_sample(lib, l=0) == 1
+    assert _call_sample(lib, u=0) == 1
+    assert _call_sample(lib, out=0) == 1
+    assert _call_sample(lib, ws=0) == 1
+    assert _call_sample(lib, l=(1 << 20) + 2) == 5
+    assert _call_sample(lib, u=(1 << 20) + 2) == 5
+    assert _call_sample(lib, ws=(1 << 20) + 16) == 5
+    assert _call_sample(lib, wsb=16) == 6
+    assert _call_sample(lib, N=0, l=0, u=0) == 0
