@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--config", default="c2", help="c1..c4 or sweep-k{K}-n{noise}")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["verify", "draft_sample"], default="verify",
+                    help="verify: the verification step (default); draft_sample: the draft-side "
+                         "sampler over every draft row of the workload")
     return ap.parse_args()
 
 
@@ -381,12 +384,193 @@ def run_ours(args, w, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+SAMPLE_METRIC = "draft tokens sampled/sec (and achieved HBM GB/s, % of GB300 peak)"
+SAMPLE_UNIT = "tokens/s"
+
+
+def sample_sets(w, n_sets: int, base: int, pin: bool):
+    """Draft rows [B*K, V] of the workload's steps, with seeded uniforms [B*K]."""
+    out = []
+    for i in range(n_sets):
+        inp = make_inputs(w, step=base + i)
+        g = torch.Generator().manual_seed(base + i)
+        u = torch.rand(w.B * w.K, generator=g, dtype=torch.float32)
+        lg = inp["draft"].reshape(w.B * w.K, w.V)
+        out.append((lg.pin_memory() if pin else lg, u.pin_memory() if pin else u))
+    return out
+
+
+def run_sampler_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    import oracle
+
+    steps = max(1, args.steps)
+    sets = sample_sets(w, min(4, steps), 30_000, pin=False)
+    wide = [(lg.to(torch.float64).numpy(), u.to(torch.float64).numpy()) for lg, u in sets]
+    for i in range(args.warmup):
+        oracle.draft_sample(*wide[i % len(wide)], w.temperature)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        oracle.draft_sample(*wide[i % len(wide)], w.temperature)
+    dt = time.perf_counter() - t0
+    n = w.B * w.K
+    value = steps * n / dt
+    print(json.dumps({
+        "impl": "reference", "op": "draft_sample", "metric": SAMPLE_METRIC, "value": value,
+        "unit": SAMPLE_UNIT, "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name + "-draft-rows", "rows": n, "V": w.V},
+        "cpu_baseline": {"value": value, "unit": SAMPLE_UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{steps} calls over the {n} draft rows of {w.name} "
+                                   f"(fp64 numpy oracle, 1 thread)"},
+        "e2e": {"value": value, "unit": SAMPLE_UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_sampler(args, w, world, rank, local):
+    """A step is one spec_draft_sample call over all B*K draft rows of one
+    step of the workload (both of its kernels)."""
+    import speculative_sampling_verification_gb300 as sv
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sv.load_library(build=True)
+    n, V, es = w.B * w.K, w.V, w.elem_bytes
+    dt_code = sv.SV_BF16 if w.dtype == "bf16" else sv.SV_F32
+    set_bytes = n * V * es
+    n_sets = max(2, min(64, -(-2 * L2_BYTES // set_bytes) + 1))
+    host = sample_sets(w, n_sets, 40_000 + 1000 * rank, pin=True)
+    sets = [(lg.to(dev), u.to(dev)) for lg, u in host]
+    outs = [torch.empty(n, dtype=torch.int32, device=dev) for _ in range(n_sets)]
+    ws = torch.empty(max(256, sv.sv_sample_workspace_size(n, V, dt_code)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.Stream(dev)
+    T = w.temperature
+
+    def call(i):
+        lg, u = sets[i % n_sets]
+        rc = sv.spec_draft_sample(lg, u, T, outs[i % n_sets], ws, stream=stream)
+        if rc != 0:
+            raise RuntimeError(f"spec_draft_sample failed: {sv.sv_status_string(rc)}")
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        call(0)
+    torch.cuda.synchronize()
+    steps, warmup = args.steps, max(3, args.warmup)
+    g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=stream):
+        for i in range(warmup):
+            call(i)
+    with torch.cuda.graph(g_timed, stream=stream):
+        for i in range(steps):
+            call(warmup + i)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    g_warm.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        g_timed.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = reduce_max(start.elapsed_time(end), world, dev)
+    time.sleep(0.3)
+    clocks.stop()
+    status = sv.sv_read_device_status(ws, stream)
+    toks = torch.stack(outs).cpu().numpy()
+    if status != 0 or (toks < 0).any() or (toks >= V).any():
+        raise RuntimeError(f"bad device status {status} or token out of range")
+
+    # End to end: pinned host rows -> device, the call, tokens -> host.
+    e2e_steps = args.e2e_steps or min(steps, 200)
+    h_out = torch.empty(n, dtype=torch.int32).pin_memory()
+    d_lg = torch.empty(n, V, dtype=sets[0][0].dtype, device=dev)
+    d_u = torch.empty(n, dtype=torch.float32, device=dev)
+
+    def host_call(i):
+        lg, u = host[i % n_sets]
+        with torch.cuda.stream(stream):
+            d_lg.copy_(lg, non_blocking=True)
+            d_u.copy_(u, non_blocking=True)
+            rc = sv.spec_draft_sample(d_lg, d_u, T, outs[0], ws, stream=stream)
+            if rc != 0:
+                raise RuntimeError(f"spec_draft_sample: {rc}")
+            h_out.copy_(outs[0], non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        host_call(i)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        host_call(i)
+    e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
+    if rank != 0:
+        return
+    per_step_s = elapsed_ms / 1e3 / steps
+    peak, peak_kind = load_peaks()
+    achieved = set_bytes / per_step_s / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        wide = [(lg.to(torch.float64).numpy(), u.to(torch.float64).numpy()) for lg, u in host[:2]]
+        t0, k = time.perf_counter(), 0
+        while time.perf_counter() - t0 < 12.0 and k < 2000:
+            oracle.draft_sample(*wide[k % len(wide)], T)
+            k += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": k * n / dt, "unit": SAMPLE_UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{k} calls over the {n} draft rows of {w.name} in {dt:.1f} s "
+                         f"(fp64 numpy oracle, 1 thread)"}
+    print(json.dumps({
+        "op": "draft_sample", "metric": SAMPLE_METRIC, "value": aggregate(n, world, per_step_s),
+        "unit": SAMPLE_UNIT, "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": per_step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name + "-draft-rows", "rows": n, "V": V, "input_dtype": w.dtype,
+                   "l2": f"inputs rotate over {n_sets} resident sets of {set_bytes / 1e6:.1f} MB",
+                   "timing": "K calls in one CUDA graph, CUDA events on the launching stream"},
+        "roofline": {"bound": "hbm", "kernel": "stats_kernel + draw_kernel (one sampler call)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                     "bytes_per_launch": set_bytes, "ms_per_launch": per_step_s * 1e3,
+                     "bytes_basis": "N rows of V elements, once (both kernels' time)"},
+        "e2e": {"value": aggregate(n * e2e_steps, world, e2e_s), "unit": SAMPLE_UNIT,
+                "h2d_bytes_per_step": set_bytes + 4 * n, "d2h_bytes_per_step": 4 * n,
+                "steps": e2e_steps},
+        "gpu_launches": steps * 2,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "cpu_baseline": cpu,
+    }), flush=True)
+
+
 def main():
     args = parse()
     w = get_workload(args.config)
     world, rank, local = dist_setup(args)
     try:
-        if args.impl == "reference":
+        if args.op == "draft_sample":
+            if args.impl == "reference":
+                run_sampler_reference(args, w, world, rank)
+            else:
+                run_sampler(args, w, world, rank, local)
+        elif args.impl == "reference":
             run_reference(args, w, world, rank)
         else:
             run_ours(args, w, world, rank, local)
