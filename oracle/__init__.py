@@ -7,6 +7,7 @@ benchmark's CPU-baseline leg, never by the library.
 from .spec_sampling import (  # noqa: F401
     OracleResult,
     SampleResult,
+    GreedyResult,
     STATUS_EMPTY_ROW,
     STATUS_NONFINITE,
     STATUS_OK,
@@ -19,5 +20,6 @@ from .spec_sampling import (  # noqa: F401
     residual_weights,
     temperature_softmax,
     verify,
+    verify_greedy,
     verify_inputs,
 )

@@ -7,7 +7,8 @@ calls anything here, and this module shares no code with it.
 What it computes, step by step, in the order and notation of
 "Accelerating Large Language Model Decoding with Speculative Sampling"
 (Chen et al., DeepMind), as summarised by its wikillm.com paper card (the
-draft-side sampler of Algorithm 2 step 1, `draft_sample`, follows `verify`):
+draft-side sampler of Algorithm 2 step 1, `draft_sample`, and the greedy
+variant, `verify_greedy`, follow `verify`):
 
 * q(.|...) and p(.|...) are the target and draft distributions. The decoding
   transform (temperature) is applied to both before anything else
@@ -266,6 +267,57 @@ def draft_sample(logits: np.ndarray, uniforms: np.ndarray, temperature: float) -
     failed = status != 0
     return SampleResult(np.where(failed, -1, idx), status, np.where(failed, np.nan, margin),
                         np.where(failed, np.nan, prob), np.where(failed, np.nan, lse))
+
+
+@dataclass
+class GreedyResult:
+    out_tokens: np.ndarray       # [B, K+1] int64, -1 padded
+    n_accepted: np.ndarray       # [B] int64, -1 for failed sequences
+    status: np.ndarray           # [B] status bits (U12), 0 = ok
+    argmax: np.ndarray           # [B, K+1] target argmax of every row (-1 where failed)
+
+
+def verify_greedy(target: np.ndarray, tokens: np.ndarray) -> GreedyResult:
+    """Greedy-mode verification (T = 0).
+
+    The paper reports greedy results but does not state the rule; the card's
+    Pitfalls ("Greedy mode is not specified") infer it by applying the
+    general rule to one-hot distributions: accept while the draft's greedy
+    token equals the target's, otherwise emit the target's greedy token. U15:
+    the drafted token x~_t is compared with argmax q_t (the two coincide when
+    the drafts were taken greedily); ties in an argmax go to the smallest
+    token id; at the first mismatch j the target's argmax q_j is emitted, and
+    if all K match, argmax q_K (the bonus token of Algorithm 2 step 4). No
+    uniforms and no draft logits are involved. A sequence fails as in U12
+    (a target row with NaN or +inf, or entirely -inf; a token outside [0, V)).
+
+    target [B, K+1, V] (widened exactly), tokens [B, K] ints.
+    """
+    target = np.asarray(target, dtype=np.float64)
+    tokens = np.asarray(tokens).astype(np.int64)
+    B, K1, V = target.shape
+    K = K1 - 1
+    if K < 1 or tokens.shape != (B, K):
+        raise ValueError("shape mismatch")
+    nonfinite = np.isnan(target).any(axis=-1) | np.isposinf(target).any(axis=-1)
+    empty = ~nonfinite & np.isneginf(target).all(axis=-1)
+    status = (np.bitwise_or.reduce(np.where(nonfinite, STATUS_NONFINITE, 0), axis=1)
+              | np.bitwise_or.reduce(np.where(empty, STATUS_EMPTY_ROW, 0), axis=1))
+    tok_ok = ((tokens >= 0) & (tokens < V)).all(axis=1)
+    status = status | np.where(tok_ok, 0, STATUS_TOKEN_RANGE)
+    with np.errstate(invalid="ignore"):
+        am = np.argmax(np.where(np.isnan(target), -np.inf, target), axis=-1)   # first maximum
+    match = tokens == am[:, :K]
+    j = np.where(match.all(axis=1), K, np.argmin(match, axis=1))
+    out = np.full((B, K + 1), -1, dtype=np.int64)
+    for b in range(B):
+        out[b, : j[b]] = tokens[b, : j[b]]
+        out[b, j[b]] = am[b, j[b]]
+    n_acc = j.astype(np.int64)
+    failed = status != 0
+    out[failed] = -1
+    n_acc[failed] = -1
+    return GreedyResult(out, n_acc, status.astype(np.int64), np.where(failed[:, None], -1, am))
 
 
 def _widen(x) -> np.ndarray:

@@ -419,6 +419,59 @@ def pin_draft_matches_bonus(O):
     assert (r.out_tokens[:, K] == s.tokens).all()
 
 
+# ---------------------------------------------------------------- greedy-mode pins
+
+def pin_greedy_golden(O):
+    """Hand-worked greedy cases (tests/golden/greedy_cases.json)."""
+    with open(os.path.join(GOLDEN_DIR, "greedy_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        tl = np.array([[[-np.inf if v == "-inf" else float(v) for v in row] for row in c["target"]]])
+        r = O.verify_greedy(tl, np.array([c["tokens"]]))
+        assert r.status[0] == 0, c["name"]
+        assert list(r.out_tokens[0]) == c["out"], (c["name"], r.out_tokens[0])
+        assert r.n_accepted[0] == c["n_accepted"], c["name"]
+
+
+def pin_greedy_is_zero_temperature(O, B=64, K=4, V=50, seed=17):
+    """Greedy mode is the general rule on one-hot distributions: with logits
+    spaced at least 1 apart and T = 1e-3, softmax(l/T) is one-hot in fp64, and
+    verify must give exactly verify_greedy's outputs for any drafts."""
+    rng = np.random.default_rng(seed)
+    tl = np.stack([np.stack([rng.permutation(V) for _ in range(K + 1)]) for _ in range(B)]).astype(float)
+    dl = np.stack([np.stack([rng.permutation(V) for _ in range(K)]) for _ in range(B)]).astype(float)
+    am_q = tl.argmax(-1)
+    am_p = dl.argmax(-1)
+    # drafts: mostly the draft argmax, sometimes the target argmax, sometimes random
+    pick = rng.random((B, K))
+    tok = np.where(pick < 0.5, am_p, np.where(pick < 0.8, am_q[:, :K], rng.integers(0, V, (B, K))))
+    uni = rng.random((B, K + 2)) * 0.999
+    r = O.verify(tl, dl, tok, uni, 1e-3)
+    g = O.verify_greedy(tl, tok)
+    assert (r.status == 0).all() and (g.status == 0).all()
+    assert (r.out_tokens == g.out_tokens).all() and (r.n_accepted == g.n_accepted).all()
+    assert (g.n_accepted < K).any() and (g.n_accepted == K).any()
+
+
+def pin_greedy_failures(O):
+    """U12 for greedy mode: each bad sequence fails alone."""
+    rng = np.random.default_rng(19)
+    B, K, V = 5, 2, 16
+    tl = rng.normal(size=(B, K + 1, V))
+    tok = rng.integers(0, V, size=(B, K))
+    tl[1, 2, 3] = np.nan
+    tl[2, 0, 0] = np.inf
+    tl[3, 1, :] = -np.inf
+    tok[4, 1] = V
+    r = O.verify_greedy(tl, tok)
+    assert list(r.status) == [0, O.STATUS_NONFINITE, O.STATUS_NONFINITE, O.STATUS_EMPTY_ROW,
+                              O.STATUS_TOKEN_RANGE]
+    for b in range(1, B):
+        assert (r.out_tokens[b] == -1).all() and r.n_accepted[b] == -1
+    assert 0 <= r.n_accepted[0] <= K and (r.out_tokens[0, : r.n_accepted[0] + 1] >= 0).all()
+
+
 FAST_PINS = (pin_golden, pin_theorem1, pin_sequential, pin_library_special_cases,
              pin_invariants, pin_failures, pin_draft_golden, pin_draft_failures,
-             pin_draft_matches_bonus)
+             pin_draft_matches_bonus, pin_greedy_golden, pin_greedy_is_zero_temperature,
+             pin_greedy_failures)

@@ -51,6 +51,13 @@ MUTATIONS = [
      "status = status | np.where(u_ok, 0, STATUS_UNIFORM_RANGE)", "status = status"),
     ("sampler reports failed rows' draws",
      "return SampleResult(np.where(failed, -1, idx), status,", "return SampleResult(idx, status,"),
+    ("greedy ties go to the largest id",
+     "am = np.argmax(np.where(np.isnan(target), -np.inf, target), axis=-1)",
+     "am = V - 1 - np.argmax(np.where(np.isnan(target), -np.inf, target)[..., ::-1], axis=-1)"),
+    ("greedy emits the draft token at the mismatch",
+     "out[b, j[b]] = am[b, j[b]]", "out[b, j[b]] = tokens[b, min(j[b], K - 1)]"),
+    ("greedy compares with the next row's argmax",
+     "match = tokens == am[:, :K]", "match = tokens == am[:, 1:]"),
 ]
 
 

@@ -99,3 +99,15 @@ def test_draft_sampler_failures():
 
 def test_draft_sampler_is_the_bonus_draw():
     _pins.pin_draft_matches_bonus(oracle)
+
+
+def test_greedy_hand_cases():
+    _pins.pin_greedy_golden(oracle)
+
+
+def test_greedy_is_the_zero_temperature_limit():
+    _pins.pin_greedy_is_zero_temperature(oracle)
+
+
+def test_greedy_failures():
+    _pins.pin_greedy_failures(oracle)
