@@ -209,6 +209,30 @@ int spec_draft_sample(const void* logits, const float* uniforms, int N, int V, i
                       float temperature, int32_t* out_tokens, double* sample_prob,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- greedy mode
+ *
+ * Verification at T = 0. The paper reports greedy results but does not state
+ * the rule; the card's Pitfalls ("Greedy mode is not specified") infer it by
+ * applying the general rule to one-hot distributions: accept while the draft's
+ * greedy token equals the target's, otherwise emit the target's greedy token.
+ * Here: x~_t is accepted while it equals argmax q_t (ties go to the smallest
+ * token id; -inf entries are masked); at the first mismatch j, argmax q_j is
+ * emitted; if all K match, argmax q_K (the bonus token). No uniforms, no
+ * temperature and no draft logits are read; the target rows are read once. */
+
+/* Bytes of device workspace spec_verify_greedy needs; 0 for invalid sizes. */
+size_t sv_greedy_workspace_size(int B, int K, int V, int dtype);
+
+/* Greedy verification: target_logits, draft_tokens, out_tokens, n_accepted,
+ * workspace and stream as for spec_verify (out_tokens holds the accepted
+ * drafts, then the emitted token, then -1 padding). A sequence fails (all -1,
+ * status bit) if a target row holds NaN or +inf or is entirely -inf, or a
+ * draft token lies outside [0, V). Returns SV_OK once enqueued, or a host-side
+ * error code with nothing enqueued; B == 0 returns SV_OK at once. */
+int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int K,
+                       int V, int dtype, int32_t* out_tokens, int32_t* n_accepted,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* Reads the device status word of the last call that used `workspace`: waits
  * for `stream`, then stores the OR of the SV_DEV_* bits in *status. */
 int sv_read_device_status(const void* workspace, void* stream, int* status);

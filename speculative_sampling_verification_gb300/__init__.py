@@ -26,6 +26,7 @@ __all__ = [
     "sv_read_device_status",
     "sv_status_string", "sv_kernels_per_call", "spec_verify_static", "verify",
     "sv_sample_workspace_size", "spec_draft_sample", "draft_sample",
+    "sv_greedy_workspace_size", "spec_verify_greedy", "verify_greedy",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -40,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "sv_staging_size",
     "spec_verify_host", "sv_read_device_status", "sv_status_string", "sv_kernels_per_call",
     "spec_verify_static", "sv_sample_workspace_size", "spec_draft_sample",
+    "sv_greedy_workspace_size", "spec_verify_greedy",
 )
 
 _lib = None
@@ -88,6 +90,10 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.sv_sample_workspace_size.restype = sz
     lib.spec_draft_sample.argtypes = [vp, vp, i32, i32, i32, f32, vp, dp, vp, sz, vp]
     lib.spec_draft_sample.restype = i32
+    lib.sv_greedy_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.sv_greedy_workspace_size.restype = sz
+    lib.spec_verify_greedy.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+    lib.spec_verify_greedy.restype = i32
     lib.sv_kernels_per_call.argtypes = [i32, i32, i32, i32]
     lib.sv_kernels_per_call.restype = i32
     if path is None:
@@ -296,3 +302,45 @@ def draft_sample(logits, uniforms, temperature, *, workspace=None, with_prob=Fal
     if rc != SV_OK:
         raise StatusError(rc, "spec_draft_sample")
     return (out, prob) if with_prob else out
+
+
+def sv_greedy_workspace_size(B: int, K: int, V: int, dtype: int) -> int:
+    return int(load_library().sv_greedy_workspace_size(B, K, V, dtype))
+
+
+def spec_verify_greedy(target, tokens, out_tokens, n_accepted, workspace, stream=None) -> int:
+    """Direct binding of greedy verification on torch tensors: target [B, K+1, V]
+    bf16/f32, tokens [B, K] int32; returns the host status code."""
+    for name, t in (("target", target), ("tokens", tokens), ("out_tokens", out_tokens),
+                    ("n_accepted", n_accepted)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if target.dim() != 3:
+        raise ValueError("target must be [B, K+1, V]")
+    B, K1, V = target.shape
+    K = K1 - 1
+    if tuple(tokens.shape) != (B, K) or tokens.dtype != torch.int32:
+        raise ValueError("tokens must be [B, K] int32")
+    return int(load_library().spec_verify_greedy(
+        _ptr(target), _ptr(tokens), B, K, V, _dtype_code(target), _ptr(out_tokens),
+        _ptr(n_accepted), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(target.device, stream)))
+
+
+def verify_greedy(target, tokens, *, workspace=None, stream=None):
+    """Allocate outputs (and a workspace if none is given) and run greedy
+    verification; returns (out_tokens [B, K+1] int32, n_accepted [B] int32)."""
+    if tokens.dtype == torch.int64:
+        tokens = tokens.to(torch.int32)
+    B, K1, V = target.shape
+    dev = target.device
+    out = torch.empty(B, K1, dtype=torch.int32, device=dev)
+    nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = workspace
+    if ws is None:
+        n = sv_greedy_workspace_size(B, K1 - 1, V, _dtype_code(target))
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    rc = spec_verify_greedy(target, tokens, out, nacc, ws, stream=stream)
+    if rc != SV_OK:
+        raise StatusError(rc, "spec_verify_greedy")
+    return out, nacc

@@ -258,6 +258,36 @@ int spec_draft_sample(const void* logits, const float* uniforms, int N, int V, i
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+size_t sv_greedy_workspace_size(int B, int K, int V, int dtype) {
+  sv::Layout L;
+  if (!sv::make_greedy_layout(B, K, V, dtype, &L)) return 0;
+  return L.total;
+}
+
+int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int K,
+                       int V, int dtype, int32_t* out_tokens, int32_t* n_accepted,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (dtype != SV_BF16 && dtype != SV_F32) return SV_ERR_DTYPE;
+  sv::Layout L;
+  if (!sv::make_greedy_layout(B, K, V, dtype, &L)) return SV_ERR_SHAPE;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !draft_tokens || !out_tokens || !n_accepted || !workspace)
+    return SV_ERR_NULL;
+  if (misaligned(target_logits, L.es) || misaligned(draft_tokens, 4) ||
+      misaligned(out_tokens, 4) || misaligned(n_accepted, 4) || misaligned(workspace, 256))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
+  sv::Params P{};
+  fill_params(P, L, B, K, V, dtype, 1.0f, workspace);
+  P.target = target_logits;
+  P.tokens = draft_tokens;
+  P.out_tokens = out_tokens;
+  P.n_acc = n_accepted;
+  const bool aligned = !misaligned(target_logits, 16) && ((size_t)V * L.es) % 16 == 0;
+  const cudaError_t e = sv::launch_greedy(P, aligned, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 int sv_read_device_status(const void* workspace, void* stream, int* status) {
   if (!workspace || !status) return SV_ERR_NULL;
   if (misaligned(workspace, 256)) return SV_ERR_ALIGN;

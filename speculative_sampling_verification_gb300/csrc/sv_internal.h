@@ -105,6 +105,12 @@ inline bool make_layout(int B, int K, int V, int dtype, Layout* L) {
   return make_layout_rows(B, 2 * K + 1, V, dtype, L);
 }
 
+// Greedy mode: B sequences of the K+1 target rows only.
+inline bool make_greedy_layout(int B, int K, int V, int dtype, Layout* L) {
+  if (K < 1 || K > kMaxK) return false;
+  return make_layout_rows(B, K + 1, V, dtype, L);
+}
+
 // The draft-side sampler: N independent rows, each its own "sequence".
 inline bool make_sample_layout(int N, int V, int dtype, Layout* L) {
   return make_layout_rows(N, 1, V, dtype, L);
@@ -154,6 +160,8 @@ struct Events {
   cudaEvent_t start = nullptr, stats_done = nullptr, end = nullptr;
 };
 cudaError_t launch_all(Params P, bool aligned, cudaStream_t stream, const Events& ev);
+// Greedy mode: one kernel over the K+1 target rows of each sequence.
+cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t stream);
 int kernels_per_call();
 
 }  // namespace sv

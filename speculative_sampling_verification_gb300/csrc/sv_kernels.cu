@@ -923,6 +923,227 @@ __global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
   if (sh.flag) finish_seq<DT, SUB>(P, b, pl, sh, VEC);  // the barrier above orders its reads
 }
 
+// ---------------------------------------------------------------- greedy mode (T = 0)
+//
+// The card's inferred greedy rule (Pitfalls, "Greedy mode is not specified"):
+// accept x~_t while it equals argmax q_t, ties to the smallest token id, else
+// emit argmax q_j; all K accepted emits argmax q_K. Only the K+1 target rows
+// are read, once: one warp per segment finds the segment's maximum and the
+// first index holding it; the warp that counts a row's last segment combines
+// the row; the warp that completes a sequence's last row compares.
+// A pair (v, i) holds the value and the first index of the maximum; v is NaN
+// when a NaN or +inf entry was seen (the sequence fails, U12).
+
+SV_DEVINL uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+SV_DEVINL float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Warp-wide (max, first index of the max) of one pair per lane; NaN wins.
+SV_DEVINL void warp_argmax(float& v, long long& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const long long i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    const bool take = (v2 != v2) ? !(v != v) || i2 < i
+                      : (v != v) ? false
+                                 : (v2 > v || (v2 == v && i2 < i));
+    if (take) {
+      v = v2;
+      i = i2;
+    }
+  }
+}
+
+template <int DT>
+SV_DEVINL float vec_elem(const uint4& q, int e) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  if constexpr (DT == 0)
+    return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+  else
+    return __uint_as_float(w[e]);
+}
+
+// Vector-load path: per round, the round's maximum with a NaN-propagating
+// packed max; only when it beats the lane's best is the round searched (in
+// index order) for the first element equal to it.
+template <int DT>
+SV_DEVINL void greedy_warp_vec(const Params& P, long long u, int lane, float& bv, long long& bi) {
+  constexpr int kEs = DT == 0 ? 2 : 4;
+  constexpr int kPerVec = 16 / kEs;
+  const int len = unit_len(P, u);
+  const long long e_base = (long long)(u % P.nseg) * P.seg_elems;
+  const unsigned char* base = unit_row(P, u) + (size_t)e_base * kEs;
+  const int nvec = len * kEs / 16;
+  const uint32_t fill = DT == 0 ? 0xff80ff80u : 0xff800000u;  // -inf
+  bv = neg_inf();
+  bi = e_base;
+  for (int i0 = 0; i0 < nvec; i0 += kStatsVec * 32) {
+    uint4 v[kStatsVec];
+#pragma unroll
+    for (int k = 0; k < kStatsVec; ++k) {
+      const int idx = i0 + k * 32 + lane;
+      v[k] = idx < nvec ? ld_global_nc_v4(base + (size_t)idx * 16) : make_uint4(fill, fill, fill, fill);
+    }
+    float lm;
+    if constexpr (DT == 0) {
+      uint32_t mx = bf16x2_max_nan(bf16x2_max_nan(v[0].x, v[0].y), bf16x2_max_nan(v[0].z, v[0].w));
+#pragma unroll
+      for (int k = 1; k < kStatsVec; ++k)
+        mx = bf16x2_max_nan(mx, bf16x2_max_nan(bf16x2_max_nan(v[k].x, v[k].y),
+                                               bf16x2_max_nan(v[k].z, v[k].w)));
+      lm = fmax_nan(bf16_lo(mx), bf16_hi(mx));
+    } else {
+      lm = neg_inf();
+#pragma unroll
+      for (int k = 0; k < kStatsVec; ++k)
+        lm = fmax_nan(lm, fmax_nan(fmax_nan(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
+                                   fmax_nan(__uint_as_float(v[k].z), __uint_as_float(v[k].w))));
+    }
+    if (lm != lm) {  // a NaN: the sequence fails, the index no longer matters
+      bv = lm;
+    } else if (bv == bv && lm > bv) {
+      bool found = false;
+#pragma unroll
+      for (int k = 0; k < kStatsVec; ++k) {
+#pragma unroll
+        for (int e = 0; e < kPerVec; ++e) {
+          if (!found && vec_elem<DT>(v[k], e) == lm) {
+            found = true;
+            bi = e_base + (long long)(i0 + k * 32 + lane) * kPerVec + e;
+          }
+        }
+      }
+      bv = lm;
+    }
+  }
+  warp_argmax(bv, bi);
+}
+
+// Plain-load path for rows that are not 16-byte aligned.
+template <int DT>
+SV_DEVINL void greedy_warp_plain(const Params& P, long long u, int lane, float& bv, long long& bi) {
+  const int len = unit_len(P, u);
+  const unsigned char* rb = unit_row(P, u);
+  const long long e0 = (long long)(u % P.nseg) * P.seg_elems;
+  bv = neg_inf();
+  bi = e0;
+  for (int i = lane; i < len; i += 32) {
+    const float l = load_elem<DT>(rb, e0 + i);
+    if (l != l) {
+      bv = l;
+    } else if (bv == bv && l > bv) {
+      bv = l;
+      bi = e0 + i;
+    }
+  }
+  warp_argmax(bv, bi);
+}
+
+// (max, first index) of a whole row from its segments' pairs.
+SV_DEVINL void greedy_row_combine(const Params& P, long long row, int lane, float& bv,
+                                  long long& bi) {
+  const float2* part = P.seg_part + row * P.nseg;
+  bv = neg_inf();
+  bi = LLONG_MAX;
+  for (int g = lane; g < P.nseg; g += 32) {
+    const float2 ps = __ldcg(part + g);
+    const long long i = (long long)__float_as_int(ps.y);
+    const bool take = (ps.x != ps.x) ? true : (bv != bv) ? false : (ps.x > bv || (ps.x == bv && i < bi));
+    if (take && !(bv != bv)) {
+      bv = ps.x;
+      bi = i;
+    }
+  }
+  warp_argmax(bv, bi);
+}
+
+SV_DEVINL void greedy_scan(const Params& P, long long b, int lane) {
+  const int K = P.K, R = P.rows_per_seq;  // R = K + 1
+  unsigned bits = 0;
+  for (int r = lane; r < R; r += 32) {
+    const float2 st = __ldcg(P.row_stat + b * R + r);
+    if (st.x != st.x || st.x == __int_as_float(0x7f800000)) {
+      bits |= kDevNonfinite;
+    } else if (st.x == neg_inf()) {
+      bits |= kDevEmptyRow;
+    }
+  }
+  for (int t = lane; t < K; t += 32) {
+    const int x = P.tokens[b * K + t];
+    if (x < 0 || x >= P.V) bits |= kDevTokenRange;
+  }
+  bits = __reduce_or_sync(0xffffffffu, bits);
+  int j = K;
+  if (!bits) {
+    for (int t0 = 0; t0 < K; t0 += 32) {
+      const int t = t0 + lane;
+      bool mismatch = false;
+      if (t < K) {
+        const int am = __float_as_int(__ldcg(P.row_stat + b * R + t).y);
+        mismatch = P.tokens[b * K + t] != am;
+      }
+      const unsigned mask = __ballot_sync(0xffffffffu, mismatch);
+      if (mask) {
+        j = t0 + __ffs(mask) - 1;
+        break;
+      }
+    }
+  } else {
+    j = -1;
+  }
+  if (lane == 0) {
+    if (bits) atomicOr(P.status, bits);
+    P.n_acc[b] = j;
+  }
+  for (int t = lane; t <= K; t += 32) {
+    int o = -1;
+    if (j >= 0 && t < j) o = P.tokens[b * K + t];
+    if (j >= 0 && t == j) o = __float_as_int(__ldcg(P.row_stat + b * R + j).y);
+    P.out_tokens[b * (K + 1) + t] = o;
+  }
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) greedy_kernel(Params P) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long u = (long long)blockIdx.x * kStatsWarps + warp;
+  if (u >= P.n_units) return;
+  const long long row = u / P.nseg;
+  const long long b = row / P.rows_per_seq;
+  float bv;
+  long long bi;
+  if constexpr (VEC)
+    greedy_warp_vec<DT>(P, u, lane, bv, bi);
+  else
+    greedy_warp_plain<DT>(P, u, lane, bv, bi);
+  if (P.nseg > 1) {
+    unsigned last = 0;
+    if (lane == 0) {
+      P.seg_part[u] = make_float2(bv, __int_as_float((int)bi));
+      last = atomic_add_acq_rel(P.done_r + row, 1u) == (unsigned)(P.nseg - 1);
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __syncwarp();
+    greedy_row_combine(P, row, lane, bv, bi);
+  }
+  unsigned last = 0;
+  if (lane == 0) {
+    P.row_stat[row] = make_float2(bv, __int_as_float((int)bi));
+    last = atomic_add_acq_rel(P.done_s + b, 1u) == (unsigned)(P.rows_per_seq - 1);
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __syncwarp();
+  greedy_scan(P, b, lane);
+}
+
 // ---------------------------------------------------------------- host-side launch
 
 namespace {
@@ -993,5 +1214,28 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
 }
 
 int kernels_per_call() { return 2; }
+
+cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t st) {
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  e = prepare_device(device);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(P.ctrl, 0, P.ctrl_bytes, st);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)((P.n_units + kStatsWarps - 1) / kStatsWarps);
+  if (P.dtype == 0) {
+    if (aligned)
+      greedy_kernel<0, true><<<grid, kStatsThreads, 0, st>>>(P);
+    else
+      greedy_kernel<0, false><<<grid, kStatsThreads, 0, st>>>(P);
+  } else {
+    if (aligned)
+      greedy_kernel<1, true><<<grid, kStatsThreads, 0, st>>>(P);
+    else
+      greedy_kernel<1, false><<<grid, kStatsThreads, 0, st>>>(P);
+  }
+  return cudaGetLastError();
+}
 
 }  // namespace sv

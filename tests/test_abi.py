@@ -126,3 +126,22 @@ def test_sampler_workspace_and_validation(lib):
     assert _call_sample(lib, ws=(1 << 20) + 16) == 5
     assert _call_sample(lib, wsb=16) == 6
     assert _call_sample(lib, N=0, l=0, u=0) == 0
+
+
+def test_greedy_workspace_and_validation(lib):
+    assert 0 < lib.sv_greedy_workspace_size(8, 4, 32000, sv.SV_BF16) < lib.sv_workspace_size(8, 4, 32000, sv.SV_BF16)
+    for bad in ((-1, 4, 10, 0), (1, 0, 10, 0), (1, 65, 10, 0), (1, 4, 0, 0), (1, 4, 10, 7)):
+        assert lib.sv_greedy_workspace_size(*bad) == 0
+    vp = ctypes.c_void_p
+
+    def call(t=1 << 20, tok=1 << 20, B=2, K=3, V=100, dtype=sv.SV_F32, out=1 << 20, nacc=1 << 20,
+             ws=1 << 20, wsb=1 << 30):
+        return lib.spec_verify_greedy(vp(t), vp(tok), B, K, V, dtype, vp(out), vp(nacc), vp(ws),
+                                      wsb, None)
+
+    assert call(dtype=3) == 4
+    assert call(K=0) == 2 and call(K=65) == 2 and call(V=0) == 2 and call(B=-1) == 2
+    assert call(t=0) == 1 and call(tok=0) == 1 and call(nacc=0) == 1 and call(ws=0) == 1
+    assert call(t=(1 << 20) + 2) == 5 and call(ws=(1 << 20) + 16) == 5
+    assert call(wsb=16) == 6
+    assert call(B=0, t=0, tok=0) == 0
