@@ -992,35 +992,39 @@ SV_DEVINL void greedy_warp_vec(const Params& P, long long u, int lane, float& bv
       const int idx = i0 + k * 32 + lane;
       v[k] = idx < nvec ? ld_global_nc_v4(base + (size_t)idx * 16) : make_uint4(fill, fill, fill, fill);
     }
-    float lm;
-    if constexpr (DT == 0) {
-      uint32_t mx = bf16x2_max_nan(bf16x2_max_nan(v[0].x, v[0].y), bf16x2_max_nan(v[0].z, v[0].w));
+    // Each vector's maximum, then the round's.
+    float vmax[kStatsVec];
 #pragma unroll
-      for (int k = 1; k < kStatsVec; ++k)
-        mx = bf16x2_max_nan(mx, bf16x2_max_nan(bf16x2_max_nan(v[k].x, v[k].y),
-                                               bf16x2_max_nan(v[k].z, v[k].w)));
-      lm = fmax_nan(bf16_lo(mx), bf16_hi(mx));
-    } else {
-      lm = neg_inf();
-#pragma unroll
-      for (int k = 0; k < kStatsVec; ++k)
-        lm = fmax_nan(lm, fmax_nan(fmax_nan(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
-                                   fmax_nan(__uint_as_float(v[k].z), __uint_as_float(v[k].w))));
+    for (int k = 0; k < kStatsVec; ++k) {
+      if constexpr (DT == 0) {
+        const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(v[k].x, v[k].y),
+                                           bf16x2_max_nan(v[k].z, v[k].w));
+        vmax[k] = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+      } else {
+        vmax[k] = fmax_nan(fmax_nan(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
+                           fmax_nan(__uint_as_float(v[k].z), __uint_as_float(v[k].w)));
+      }
     }
+    float lm = vmax[0];
+#pragma unroll
+    for (int k = 1; k < kStatsVec; ++k) lm = fmax_nan(lm, vmax[k]);
     if (lm != lm) {  // a NaN: the sequence fails, the index no longer matters
       bv = lm;
     } else if (bv == bv && lm > bv) {
-      bool found = false;
+      // The first vector holding lm, then the first element of it that does.
+      int kk = 0;
 #pragma unroll
-      for (int k = 0; k < kStatsVec; ++k) {
+      for (int k = kStatsVec - 1; k >= 0; --k)
+        if (vmax[k] == lm) kk = k;
+      uint4 q = v[0];
 #pragma unroll
-        for (int e = 0; e < kPerVec; ++e) {
-          if (!found && vec_elem<DT>(v[k], e) == lm) {
-            found = true;
-            bi = e_base + (long long)(i0 + k * 32 + lane) * kPerVec + e;
-          }
-        }
-      }
+      for (int k = 1; k < kStatsVec; ++k)
+        if (k == kk) q = v[k];
+      int ee = 0;
+#pragma unroll
+      for (int e = kPerVec - 1; e >= 0; --e)
+        if (vec_elem<DT>(q, e) == lm) ee = e;
+      bi = e_base + (long long)(i0 + kk * 32 + lane) * kPerVec + ee;
       bv = lm;
     }
   }
