@@ -342,8 +342,10 @@ def run_ours(args, w, world, rank, local):
     value = aggregate(B * K, world, per_step_s)
     ideal = w.ideal_bytes_per_step()
     peak, peak_kind = load_peaks()
-    # Dominant HBM kernel: the streaming row-statistics kernel. Its
+    # Dominant HBM kernel: the streaming row-statistics kernel, or for small
+    # calls the fused kernel (streaming, scan and draw in one launch). Its
     # algorithmic bytes are every one of the B(2K+1) rows once.
+    fused = sv.sv_kernels_per_call(B, K, V, dt_code) == 1
     launch_bytes = B * (2 * K + 1) * V * es
     achieved = launch_bytes / (stats_ms * 1e-3) / 1e9
     # The draw kernel re-reads two rows per residual draw and one per bonus draw.
@@ -369,13 +371,17 @@ def run_ours(args, w, world, rank, local):
         "hbm_gbs_ideal_bytes": ideal / per_step_s / 1e9 * world,
         "frac_of_peak_ideal_bytes": ideal / per_step_s / 1e9 / peak,
         "mean_accepted": float(nacc_all.mean()),
-        "roofline": {"bound": "hbm", "kernel": "stats_kernel (streaming row statistics)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("fused_kernel (streaming, scan and draw)" if fused
+                                else "stats_kernel (streaming row statistics)"),
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "traffic": load_traffic("stats_kernel", w.name),
+                     "traffic": load_traffic("fused_kernel" if fused else "stats_kernel", w.name),
                      "bytes_per_launch": launch_bytes, "ms_per_launch": stats_ms,
                      "bytes_basis": "B(2K+1) rows of V elements, once"},
-        "draw_kernel": {"ms_per_launch": draw_ms, "rows_reread_per_step": draw_rows * B},
+        "draw_kernel": ({"ms_per_launch": None, "note": "inside fused_kernel",
+                         "rows_reread_per_step": draw_rows * B} if fused else
+                        {"ms_per_launch": draw_ms, "rows_reread_per_step": draw_rows * B}),
         "e2e": {"value": aggregate(B * K * e2e_steps, world, e2e_s), "unit": "draft_positions/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": steps * sv.sv_kernels_per_call(B, K, V, dt_code),

@@ -31,11 +31,16 @@
  * pointers between calls. Work is enqueued on `stream` (a cudaStream_t passed
  * as void*; NULL means the legacy default stream) and runs asynchronously.
  *
- * A call enqueues a memset of the workspace's control block and two kernels:
- * the streaming kernel, then the draw kernel as its programmatic dependent
- * (launched while the streaming grid drains, and waiting on the device for it
- * to complete). Make the first call on a device before capturing a stream
- * into a CUDA graph.
+ * A call enqueues a memset of the workspace's control block and then either
+ *   - two kernels: the streaming kernel, then the draw kernel as its
+ *     programmatic dependent (launched while the streaming grid drains, and
+ *     waiting on the device for it to complete); or, for calls streaming
+ *     between 16 MiB and 1 GiB of logits,
+ *   - one fused kernel whose CTAs take tickets: streaming work first, then the
+ *     draw of each sequence, which waits on the device for that sequence's
+ *     plan. The wait is bounded: after 200 ms it sets SV_DEV_TIMEOUT and the
+ *     kernel winds down.
+ * Make the first call on a device before capturing a stream into a CUDA graph.
  */
 #ifndef SPEC_VERIFY_H_
 #define SPEC_VERIFY_H_
@@ -77,7 +82,7 @@ enum {
   SV_DEV_NONFINITE = 32,     /* a logit row holds NaN or +inf */
   SV_DEV_EMPTY_ROW = 64,     /* a logit row is entirely -inf */
   SV_DEV_UNIFORM_RANGE = 128,/* a uniform is NaN or outside [0, 1] */
-  SV_DEV_TIMEOUT = 256       /* reserved; never set (the kernels contain no waits) */
+  SV_DEV_TIMEOUT = 256       /* a bounded wait in the fused kernel ran out (results invalid) */
 };
 
 /* Bytes of device workspace spec_verify needs for this problem size; 0 for an
@@ -126,10 +131,11 @@ int spec_verify_debug(const void* target_logits, const void* draft_logits,
 /* spec_verify that also records three caller-owned CUDA events (cudaEvent_t
  * passed as void*, created with timing enabled) on `stream`: `ev_start` before
  * the first kernel, `ev_stats_done` between the streaming row-statistics
- * kernel and the draw kernel, `ev_end` after the draw kernel. Elapsed times
- * between them time the streaming pass and the draw. With `ev_stats_done` set
- * the draw kernel is an ordinary launch rather than a programmatic dependent,
- * so the pair runs back to back without overlap. Any event may be NULL. */
+ * kernel and the draw kernel (after the fused kernel, when that one runs),
+ * `ev_end` after the last kernel. Elapsed times between them time the
+ * streaming pass and the draw. With `ev_stats_done` set the draw kernel is an
+ * ordinary launch rather than a programmatic dependent, so the pair runs back
+ * to back without overlap. Any event may be NULL. */
 int spec_verify_profiled(const void* target_logits, const void* draft_logits,
                          const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
                          int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
@@ -241,9 +247,15 @@ int sv_read_device_status(const void* workspace, void* stream, int* status);
 const char* sv_status_string(int status);
 
 /* Kernels one spec_verify call over these sizes launches (for launch
- * accounting): 2, the streaming and the draw kernel; 0 for invalid sizes or
+ * accounting): 1 (the fused kernel) for calls streaming between 16 MiB and
+ * 1 GiB, else 2 (the streaming and the draw kernel); 0 for invalid sizes or
  * B == 0. */
 int sv_kernels_per_call(int B, int K, int V, int dtype);
+
+/* Test hook: 0 (the default) chooses the kernels by size, 1 forces the kernel
+ * pair, 2 forces the fused kernel. Process-wide; for tests that compare the
+ * two paths. */
+void sv_force_path(int path);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,7 @@ __all__ = [
     "sv_read_device_status",
     "sv_status_string", "sv_kernels_per_call", "spec_verify_static", "verify",
     "sv_sample_workspace_size", "spec_draft_sample", "draft_sample",
-    "sv_greedy_workspace_size", "spec_verify_greedy", "verify_greedy",
+    "sv_greedy_workspace_size", "spec_verify_greedy", "verify_greedy", "sv_force_path",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "sv_staging_size",
     "spec_verify_host", "sv_read_device_status", "sv_status_string", "sv_kernels_per_call",
     "spec_verify_static", "sv_sample_workspace_size", "spec_draft_sample",
-    "sv_greedy_workspace_size", "spec_verify_greedy",
+    "sv_greedy_workspace_size", "spec_verify_greedy", "sv_force_path",
 )
 
 _lib = None
@@ -96,6 +96,8 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.spec_verify_greedy.restype = i32
     lib.sv_kernels_per_call.argtypes = [i32, i32, i32, i32]
     lib.sv_kernels_per_call.restype = i32
+    lib.sv_force_path.argtypes = [i32]
+    lib.sv_force_path.restype = None
     if path is None:
         _lib = lib
     return lib
@@ -132,6 +134,12 @@ def sv_status_string(code: int) -> str:
 
 def sv_kernels_per_call(B: int, K: int, V: int, dtype: int) -> int:
     return int(load_library().sv_kernels_per_call(B, K, V, dtype))
+
+
+def sv_force_path(path: int) -> None:
+    """Test hook: 0 chooses the kernels by size, 1 forces the kernel pair,
+    2 the fused kernel."""
+    load_library().sv_force_path(int(path))
 
 
 def _check(target, draft, tokens, uniforms):

@@ -104,14 +104,18 @@ static void fill_params(sv::Params& P, const sv::Layout& L, int B, int K, int V,
   P.ns = (long long)L.rows_per_seq * L.nseg;
   P.np = L.nchunk;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  // Control block: status word (4 B), 12 B reserved, then done_s and done_p
-  // [B] each and done_r [B (2K+1)]; zeroed before every launch.
+  // Control block: status, abort, ticket (4 B each, 4 reserved), then done_s,
+  // done_p, ready [B] each and done_r [B rows_per_seq]; zeroed before every
+  // launch.
   P.ctrl = ws + L.off_ctrl;
   P.ctrl_bytes = L.ctrl_bytes;
   P.status = reinterpret_cast<unsigned*>(ws + L.off_ctrl);
+  P.abort = P.status + 1;
+  P.ticket = P.status + 2;
   P.done_s = reinterpret_cast<unsigned*>(ws + L.off_ctrl + 16);
   P.done_p = P.done_s + B;
-  P.done_r = P.done_p + B;
+  P.ready = P.done_p + B;
+  P.done_r = P.ready + B;
   P.seg_part = reinterpret_cast<float2*>(ws + L.off_seg);
   P.row_stat = reinterpret_cast<float2*>(ws + L.off_row);
   P.plans = reinterpret_cast<sv::Plan*>(ws + L.off_plan);
@@ -313,7 +317,7 @@ const char* sv_status_string(int status) {
     case SV_ERR_SCRATCH_LIMIT: return "problem needs more scratch than spec_verify_static holds";
     default: break;
   }
-  if (status & SV_DEV_TIMEOUT) return "device: reserved status bit (never set)";
+  if (status & SV_DEV_TIMEOUT) return "device: a bounded wait ran out (results invalid)";
   if (status & SV_DEV_NONFINITE) return "device: a logit row holds NaN or +inf";
   if (status & SV_DEV_EMPTY_ROW) return "device: a logit row is entirely -inf";
   if (status & SV_DEV_TOKEN_RANGE) return "device: a draft token lies outside [0, V)";
@@ -324,7 +328,9 @@ const char* sv_status_string(int status) {
 int sv_kernels_per_call(int B, int K, int V, int dtype) {
   sv::Layout L;
   if (!sv::make_layout(B, K, V, dtype, &L) || B == 0) return 0;
-  return sv::kernels_per_call();
+  return sv::kernels_per_call(B, L.rows_per_seq, V, L.es);
 }
+
+void sv_force_path(int path) { sv::force_path(path); }
 
 }  // extern "C"

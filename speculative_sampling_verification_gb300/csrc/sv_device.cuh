@@ -26,6 +26,27 @@ SV_DEVINL uint4 ld_global_nc_v4(const void* p) {
   return v;
 }
 
+// ---------------------------------------------------------------- flags and bounded waits
+
+SV_DEVINL uint32_t ld_acquire_u32(const unsigned* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+SV_DEVINL void st_release_u32(unsigned* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+SV_DEVINL uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Every wait in the kernels gives up after this much wall time.
+constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
+
 // ---------------------------------------------------------------- bf16 and fast fp32 helpers
 
 SV_DEVINL float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -84,8 +84,9 @@ inline bool make_layout_rows(int B, int rows_per_seq, int V, int dtype, Layout* 
   size_t off = 0;
   L->off_status = off;  // status word (read by the host), then the control block
   L->off_ctrl = off;
-  // status (16 B), then done_s [B], done_p [B] and done_r [B (2K+1)]
-  L->ctrl_bytes = align_up(16 + (size_t)B * 8 + (size_t)L->rows_total * 4, 16);
+  // status, abort, ticket (12 B, then 4 reserved), then done_s [B], done_p
+  // [B], ready [B] and done_r [B rows_per_seq]
+  L->ctrl_bytes = align_up(16 + (size_t)B * 12 + (size_t)L->rows_total * 4, 16);
   off = align_up(off + L->ctrl_bytes, 256);
   L->off_seg = off;
   off = align_up(off + (size_t)L->n_units * sizeof(float2), 256);
@@ -126,6 +127,7 @@ struct Params {
   float ih, il;    // 1/T as a float-float (sampling pass)
   int unit_t;      // T == 1 exactly
   int sampler;     // 1: draft-side sampler (one row per sequence, K = 0, no scan)
+  int fused;       // 1: the fused kernel runs (plans are published with a release flag)
   double inv_t;    // 1/T in fp64 (scan)
   int rows_per_seq;
   int nseg, seg_elems;
@@ -136,8 +138,11 @@ struct Params {
   long long np;    // draw chunks per sequence (nchunk)
   void* ctrl;      // control block, zeroed before every launch
   size_t ctrl_bytes;
+  unsigned* abort;   // set by the first bounded wait that runs out (fused kernel)
+  unsigned* ticket;  // work items handed out (fused kernel)
   unsigned* done_s;  // [B] rows whose statistics are complete, per sequence
   unsigned* done_p;  // [B] draw chunks counted per sequence
+  unsigned* ready;   // [B] the sequence's plan is published
   unsigned* done_r;  // [B (2K+1)] streamed segments counted per row
   float2* seg_part;  // [n_units] (max, sum) per segment
   float2* row_stat;  // [B (2K+1)] (max, sum) per row
@@ -162,6 +167,11 @@ struct Events {
 cudaError_t launch_all(Params P, bool aligned, cudaStream_t stream, const Events& ev);
 // Greedy mode: one kernel over the K+1 target rows of each sequence.
 cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t stream);
-int kernels_per_call();
+// Kernels one call over B sequences of rows_per_seq rows of V elements of
+// `es` bytes launches: 1 when the fused kernel is taken, else 2.
+int kernels_per_call(long long B, int rows_per_seq, long long V, int es);
+// Test hook: 0 chooses the kernels by size, 1 forces the kernel pair, 2 the
+// fused kernel.
+void force_path(int path);
 
 }  // namespace sv

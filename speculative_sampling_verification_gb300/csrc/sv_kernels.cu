@@ -24,6 +24,7 @@
 #include <cfloat>
 #include <climits>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "sv_device.cuh"
@@ -32,7 +33,7 @@
 namespace sv {
 
 constexpr unsigned kDevTokenRange = 16, kDevNonfinite = 32, kDevEmptyRow = 64,
-                   kDevUniformRange = 128;
+                   kDevUniformRange = 128, kDevTimeout = 256;
 constexpr float kLn2 = 0.693147180559945309f;
 
 constexpr int kThreads = 256;
@@ -431,6 +432,7 @@ SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
       P.n_acc[b] = j;
     }
     P.plans[b] = pl;
+    if (P.fused) st_release_u32(P.ready + b, 1u);  // the plan, for the fused kernel's draw CTAs
   }
   for (int t = lane; t <= K; t += 32) {
     if (j < 0 || t > j)
@@ -850,6 +852,7 @@ SV_DEVINL void sample_plan(const Params& P, long long b, float2 st, int lane) {
     pl.u = u;
   }
   P.plans[b] = pl;
+  if (P.fused) st_release_u32(P.ready + b, 1u);
 }
 
 // One warp per row segment u. The warp that counts the last segment of a row
@@ -857,13 +860,7 @@ SV_DEVINL void sample_plan(const Params& P, long long b, float2 st, int lane) {
 // it. The counters are acquire-release atomics taken by lane 0; __syncwarp
 // then orders the other lanes' reads (through L2) after lane 0's acquire.
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(Params P) {
-  __shared__ WarpScan scan_sh[kStatsWarps];
-  // Let the draw kernel be launched once every CTA of this grid has started.
-  asm volatile("griddepcontrol.launch_dependents;");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long u = (long long)blockIdx.x * kStatsWarps + warp;
-  if (u >= P.n_units) return;
+SV_DEVINL void stats_warp_unit(const Params& P, long long u, int lane, WarpScan& ws) {
   const long long row = u / P.nseg;
   const long long b = row / P.rows_per_seq;
   float2 st;
@@ -892,23 +889,39 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(P
   }
   if (!__shfl_sync(0xffffffffu, last, 0)) return;
   __syncwarp();
-  scan_warp(P, b, lane, scan_sh[warp]);
+  scan_warp(P, b, lane, ws);
 }
 
-// One CTA per draw chunk c of sequence b (the plans are complete once the
-// streaming grid is); the CTA that counts the last chunk of a sequence runs
-// its inverse-CDF search.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(Params P) {
+  __shared__ WarpScan scan_sh[kStatsWarps];
+  // Let the draw kernel be launched once every CTA of this grid has started.
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long u = (long long)blockIdx.x * kStatsWarps + warp;
+  if (u < P.n_units) stats_warp_unit<DT, VEC>(P, u, lane, scan_sh[warp]);
+}
+
+// Chunk c of sequence b's draw, by one CTA whose table is loaded and whose
+// view of the plan is current: the sub-chunk sums, and the finish in the CTA
+// that counts the sequence's last chunk.
 template <int DT, bool VEC, int SUB>
-__global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
-  __shared__ CtaShared sh;
+SV_DEVINL void draw_chunk(const Params& P, long long b, int c, CtaShared& sh) {
   const int tid = threadIdx.x;
-  sh.tab[tid] = kSvExp2Table[tid];
-  const long long b = blockIdx.x / P.np;
-  const int c = (int)(blockIdx.x % P.np);
-  // Wait until the streaming grid has completed and its writes are visible
-  // (immediate when this kernel was launched as an ordinary dependent).
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0) sh.plan = P.plans[b];
+  if (tid == 0) {
+    const Plan* src = P.plans + b;
+    Plan pl;
+    pl.j = __ldcg(&src->j);
+    pl.mode = __ldcg(&src->mode);
+    pl.row_q = __ldcg(&src->row_q);
+    pl.row_p = __ldcg(&src->row_p);
+    pl.m_q = __ldcg(&src->m_q);
+    pl.m_p = __ldcg(&src->m_p);
+    pl.s_q = __ldcg(&src->s_q);
+    pl.s_p = __ldcg(&src->s_p);
+    pl.u = __ldcg(&src->u);
+    sh.plan = pl;
+  }
   __syncthreads();
   const Plan pl = sh.plan;
   if (pl.mode == kModeFailed) return;  // outputs already written by the scan
@@ -921,6 +934,88 @@ __global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
   if (tid == 0) sh.flag = atomic_add_acq_rel(P.done_p + b, 1u) == (unsigned)(P.np - 1);
   __syncthreads();
   if (sh.flag) finish_seq<DT, SUB>(P, b, pl, sh, VEC);  // the barrier above orders its reads
+}
+
+// One CTA per draw chunk c of sequence b (the plans are complete once the
+// streaming grid is); the CTA that counts the last chunk of a sequence runs
+// its inverse-CDF search.
+template <int DT, bool VEC, int SUB>
+__global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
+  __shared__ CtaShared sh;
+  sh.tab[threadIdx.x] = kSvExp2Table[threadIdx.x];
+  // Wait until the streaming grid has completed and its writes are visible
+  // (immediate when this kernel was launched as an ordinary dependent).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  draw_chunk<DT, VEC, SUB>(P, blockIdx.x / P.np, (int)(blockIdx.x % P.np), sh);
+}
+
+// ---------------------------------------------------------------- the fused kernel
+//
+// For mid-sized calls one launch does the whole step. Each CTA takes a ticket when it starts: tickets below
+// ceil(n_units / 8) are streaming items (eight warp-units, as stats_kernel's
+// warps), the rest draw chunks in sequence order (as draw_kernel's CTAs). A
+// draw CTA waits for its sequence's plan, which the sequence's scan releases;
+// every streaming ticket precedes every draw ticket and streaming never
+// waits, so each awaited plan is being computed by a CTA already running. The
+// wait is bounded: after kWaitLimitNs it sets kDevTimeout and the abort flag
+// and the CTA returns. Compared with the kernel pair, a sequence's draw starts
+// as soon as its own scan is done, during the last streaming wave instead of
+// after the grid boundary. Measured on GB300 it wins between a few tens of MB
+// and a GB of logits; below, the ticket's round trip at every CTA's start
+// costs more than it saves, and above, the draw's 4 CTAs per SM (64 registers
+// for the streaming role) lose to the draw kernel's 5.
+
+constexpr long long kFusedMinBytes = 16ll << 20;   // calls streaming from this much ...
+constexpr long long kFusedMaxBytes = 1ll << 30;    // ... up to this take the fused kernel
+
+union FusedShared {
+  WarpScan scan[kWarps];
+  CtaShared draw;
+};
+
+SV_DEVINL void note_timeout(const Params& P) {
+  atomicOr(P.status, kDevTimeout);
+  atomicExch(P.abort, 1u);
+}
+
+// Bounded wait (one thread) for sequence b's plan.
+SV_DEVINL bool wait_ready(const Params& P, long long b) {
+  if (ld_acquire_u32(P.ready + b)) return true;
+  const uint64_t t0 = global_ns();
+  unsigned ns = 64;
+  for (;;) {
+    __nanosleep(ns);
+    if (ns < 1024) ns <<= 1;
+    if (ld_acquire_u32(P.ready + b)) return true;
+    if (ld_acquire_u32(P.abort)) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      note_timeout(P);
+      return false;
+    }
+  }
+}
+
+template <int DT, bool VEC, int SUB>
+__global__ void __launch_bounds__(kThreads, 4) fused_kernel(Params P) {
+  __shared__ FusedShared sh;
+  __shared__ unsigned s_ticket;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) s_ticket = atomicAdd(P.ticket, 1u);
+  __syncthreads();
+  const long long t = s_ticket;
+  const long long n_stream = (P.n_units + kWarps - 1) / kWarps;
+  if (t < n_stream) {
+    const long long u = t * kWarps + warp;
+    if (u < P.n_units) stats_warp_unit<DT, VEC>(P, u, lane, sh.scan[warp]);
+    return;
+  }
+  const long long d = t - n_stream;
+  const long long b = d / P.np;
+  sh.draw.tab[tid] = kSvExp2Table[tid];
+  if (tid == 0) sh.draw.flag = wait_ready(P, b) ? 1 : 0;
+  __syncthreads();
+  if (!sh.draw.flag) return;
+  draw_chunk<DT, VEC, SUB>(P, b, (int)(d % P.np), sh.draw);
 }
 
 // ---------------------------------------------------------------- greedy mode (T = 0)
@@ -1156,7 +1251,33 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
+std::atomic<int> g_force_path{0};
+
+bool take_fused(long long B, int rows_per_seq, long long V, int es, bool sampler = false) {
+  const int path = g_force_path.load();
+  if (path == 1) return false;
+  if (path == 2) return true;
+  // The sampler draws every row, so its draw kernel's occupancy decides: the pair.
+  const long long bytes = B * rows_per_seq * V * es;
+  return !sampler && bytes >= kFusedMinBytes && bytes <= kFusedMaxBytes;
+}
 }  // namespace
+
+void force_path(int path) { g_force_path.store(path); }
+
+int kernels_per_call(long long B, int rows_per_seq, long long V, int es) {
+  return take_fused(B, rows_per_seq, V, es) ? 1 : 2;
+}
+
+template <int DT, bool VEC, int SUB>
+cudaError_t launch_fused(const Params& P, cudaStream_t st, const Events& ev) {
+  const long long n_stream = (P.n_units + kWarps - 1) / kWarps;
+  fused_kernel<DT, VEC, SUB><<<(unsigned)(n_stream + (long long)P.B * P.np), kThreads, 0, st>>>(P);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && ev.stats_done)
+    e = cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
+  return e;
+}
 
 template <int DT, bool VEC, int SUB>
 cudaError_t launch_pair(const Params& P, cudaStream_t st, const Events& ev) {
@@ -1206,18 +1327,25 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
     if (e != cudaSuccess) return e;
   }
   const bool big = P.sub_elems == 512;
-  if (P.dtype == 0)
+  P.fused = take_fused(P.B, P.rows_per_seq, P.V, P.es, P.sampler != 0) ? 1 : 0;
+  if (P.fused) {
+    if (P.dtype == 0)
+      e = aligned ? (big ? launch_fused<0, true, 512>(P, st, ev) : launch_fused<0, true, 256>(P, st, ev))
+                  : (big ? launch_fused<0, false, 512>(P, st, ev) : launch_fused<0, false, 256>(P, st, ev));
+    else
+      e = aligned ? (big ? launch_fused<1, true, 512>(P, st, ev) : launch_fused<1, true, 256>(P, st, ev))
+                  : (big ? launch_fused<1, false, 512>(P, st, ev) : launch_fused<1, false, 256>(P, st, ev));
+  } else if (P.dtype == 0) {
     e = aligned ? (big ? launch_pair<0, true, 512>(P, st, ev) : launch_pair<0, true, 256>(P, st, ev))
                 : (big ? launch_pair<0, false, 512>(P, st, ev) : launch_pair<0, false, 256>(P, st, ev));
-  else
+  } else {
     e = aligned ? (big ? launch_pair<1, true, 512>(P, st, ev) : launch_pair<1, true, 256>(P, st, ev))
                 : (big ? launch_pair<1, false, 512>(P, st, ev) : launch_pair<1, false, 256>(P, st, ev));
+  }
   if (e != cudaSuccess) return e;
   if (ev.end) e = cudaEventRecordWithFlags(ev.end, st, cudaEventRecordExternal);
   return e;
 }
-
-int kernels_per_call() { return 2; }
 
 cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t st) {
   int device = 0;

@@ -17,6 +17,15 @@ from synthetic.configs import shrink
 
 pytestmark = pytest.mark.gpu
 
+
+@pytest.fixture(autouse=True, params=[1, 2], ids=["kernel_pair", "fused"])
+def kernel_path(request):
+    """Every test here runs on both paths: the streaming + draw kernel pair,
+    and the fused kernel that the library takes for small calls."""
+    sv.sv_force_path(request.param)
+    yield request.param
+    sv.sv_force_path(0)
+
 DEV = torch.device("cuda:0")
 MARGIN = 1e-6
 
