@@ -257,6 +257,12 @@ int sv_kernels_per_call(int B, int K, int V, int dtype);
  * two paths. */
 void sv_force_path(int path);
 
+/* Test hook for failure detection: with `on` nonzero, calls never publish
+ * their plans' release flag, so on the fused path every draw CTA's bounded
+ * wait runs out (200 ms) and the call ends with SV_DEV_TIMEOUT; no GPU fault,
+ * and the context stays usable. Process-wide; 0 restores normal calls. */
+void sv_test_withhold_plans(int on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,6 +27,7 @@ __all__ = [
     "sv_status_string", "sv_kernels_per_call", "spec_verify_static", "verify",
     "sv_sample_workspace_size", "spec_draft_sample", "draft_sample",
     "sv_greedy_workspace_size", "spec_verify_greedy", "verify_greedy", "sv_force_path",
+    "sv_test_withhold_plans",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -41,7 +42,7 @@ EXPORTED_SYMBOLS = (
     "sv_staging_size",
     "spec_verify_host", "sv_read_device_status", "sv_status_string", "sv_kernels_per_call",
     "spec_verify_static", "sv_sample_workspace_size", "spec_draft_sample",
-    "sv_greedy_workspace_size", "spec_verify_greedy", "sv_force_path",
+    "sv_greedy_workspace_size", "spec_verify_greedy", "sv_force_path", "sv_test_withhold_plans",
 )
 
 _lib = None
@@ -98,6 +99,8 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.sv_kernels_per_call.restype = i32
     lib.sv_force_path.argtypes = [i32]
     lib.sv_force_path.restype = None
+    lib.sv_test_withhold_plans.argtypes = [i32]
+    lib.sv_test_withhold_plans.restype = None
     if path is None:
         _lib = lib
     return lib
@@ -134,6 +137,12 @@ def sv_status_string(code: int) -> str:
 
 def sv_kernels_per_call(B: int, K: int, V: int, dtype: int) -> int:
     return int(load_library().sv_kernels_per_call(B, K, V, dtype))
+
+
+def sv_test_withhold_plans(on: bool) -> None:
+    """Test hook: withhold the plans' release flag so that the fused kernel's
+    bounded waits run out (SV_DEV_TIMEOUT), without any GPU fault."""
+    load_library().sv_test_withhold_plans(1 if on else 0)
 
 
 def sv_force_path(path: int) -> None:

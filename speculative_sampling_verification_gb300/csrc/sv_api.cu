@@ -333,4 +333,6 @@ int sv_kernels_per_call(int B, int K, int V, int dtype) {
 
 void sv_force_path(int path) { sv::force_path(path); }
 
+void sv_test_withhold_plans(int on) { sv::withhold_plans(on); }
+
 }  // extern "C"

@@ -128,6 +128,7 @@ struct Params {
   int unit_t;      // T == 1 exactly
   int sampler;     // 1: draft-side sampler (one row per sequence, K = 0, no scan)
   int fused;       // 1: the fused kernel runs (plans are published with a release flag)
+  int withhold;    // test hook: 1 = never publish the flag, so the draw's waits run out
   double inv_t;    // 1/T in fp64 (scan)
   int rows_per_seq;
   int nseg, seg_elems;
@@ -173,5 +174,7 @@ int kernels_per_call(long long B, int rows_per_seq, long long V, int es);
 // Test hook: 0 chooses the kernels by size, 1 forces the kernel pair, 2 the
 // fused kernel.
 void force_path(int path);
+// Test hook: withhold the plans' release flag (the fused kernel's waits run out).
+void withhold_plans(int on);
 
 }  // namespace sv

@@ -432,7 +432,7 @@ SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
       P.n_acc[b] = j;
     }
     P.plans[b] = pl;
-    if (P.fused) st_release_u32(P.ready + b, 1u);  // the plan, for the fused kernel's draw CTAs
+    if (P.fused && !P.withhold) st_release_u32(P.ready + b, 1u);  // for the fused kernel's draw CTAs
   }
   for (int t = lane; t <= K; t += 32) {
     if (j < 0 || t > j)
@@ -852,7 +852,7 @@ SV_DEVINL void sample_plan(const Params& P, long long b, float2 st, int lane) {
     pl.u = u;
   }
   P.plans[b] = pl;
-  if (P.fused) st_release_u32(P.ready + b, 1u);
+  if (P.fused && !P.withhold) st_release_u32(P.ready + b, 1u);
 }
 
 // One warp per row segment u. The warp that counts the last segment of a row
@@ -1252,6 +1252,7 @@ struct DeviceInfo {
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
 std::atomic<int> g_force_path{0};
+std::atomic<int> g_withhold{0};
 
 bool take_fused(long long B, int rows_per_seq, long long V, int es, bool sampler = false) {
   const int path = g_force_path.load();
@@ -1264,6 +1265,8 @@ bool take_fused(long long B, int rows_per_seq, long long V, int es, bool sampler
 }  // namespace
 
 void force_path(int path) { g_force_path.store(path); }
+
+void withhold_plans(int on) { g_withhold.store(on ? 1 : 0); }
 
 int kernels_per_call(long long B, int rows_per_seq, long long V, int es) {
   return take_fused(B, rows_per_seq, V, es) ? 1 : 2;
@@ -1328,6 +1331,7 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
   }
   const bool big = P.sub_elems == 512;
   P.fused = take_fused(P.B, P.rows_per_seq, P.V, P.es, P.sampler != 0) ? 1 : 0;
+  P.withhold = g_withhold.load();
   if (P.fused) {
     if (P.dtype == 0)
       e = aligned ? (big ? launch_fused<0, true, 512>(P, st, ev) : launch_fused<0, true, 256>(P, st, ev))
