@@ -129,6 +129,8 @@ struct Params {
   int sampler;     // 1: draft-side sampler (one row per sequence, K = 0, no scan)
   int fused;       // 1: the fused kernel runs (plans are published with a release flag)
   int withhold;    // test hook: 1 = never publish the flag, so the draw's waits run out
+  long long nsi;   // fused kernel: streaming items (of up to 8 units) per sequence
+  long long lag;   // fused kernel: sequences between a sequence's streaming and draw tickets
   double inv_t;    // 1/T in fp64 (scan)
   int rows_per_seq;
   int nseg, seg_elems;

@@ -995,6 +995,30 @@ SV_DEVINL bool wait_ready(const Params& P, long long b) {
   }
 }
 
+// Ticket t -> work item. Sequence s has nsi streaming items (up to eight of
+// its units each) and np draw chunks. The streaming items of sequences
+// 0 .. lag-1 come first; then, for s = lag .. B-1, the streaming items of s
+// followed by the draw chunks of s - lag; then the draw chunks of the last lag
+// sequences. So every streaming ticket of a sequence precedes its draw
+// tickets, whatever the lag (lag = B: all streaming first).
+struct FusedItem {
+  bool stream;
+  long long b, idx;
+};
+
+SV_DEVINL FusedItem fused_item(const Params& P, long long t) {
+  const long long NS = P.nsi, NP = P.np, L = P.lag, B = P.B;
+  if (t < L * NS) return {true, t / NS, t % NS};
+  t -= L * NS;
+  if (t < (B - L) * (NS + NP)) {
+    const long long s = L + t / (NS + NP), o = t % (NS + NP);
+    if (o < NS) return {true, s, o};
+    return {false, s - L, o - NS};
+  }
+  t -= (B - L) * (NS + NP);
+  return {false, (B - L) + t / NP, t % NP};
+}
+
 template <int DT, bool VEC, int SUB>
 __global__ void __launch_bounds__(kThreads, 4) fused_kernel(Params P) {
   __shared__ FusedShared sh;
@@ -1002,20 +1026,18 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(Params P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) s_ticket = atomicAdd(P.ticket, 1u);
   __syncthreads();
-  const long long t = s_ticket;
-  const long long n_stream = (P.n_units + kWarps - 1) / kWarps;
-  if (t < n_stream) {
-    const long long u = t * kWarps + warp;
-    if (u < P.n_units) stats_warp_unit<DT, VEC>(P, u, lane, sh.scan[warp]);
+  const FusedItem it = fused_item(P, (long long)s_ticket);
+  if (it.stream) {
+    const long long k = it.idx * kWarps + warp;  // the sequence's k-th unit
+    if (k < P.ns) stats_warp_unit<DT, VEC>(P, it.b * P.ns + k, lane, sh.scan[warp]);
     return;
   }
-  const long long d = t - n_stream;
-  const long long b = d / P.np;
+  const long long b = it.b;
   sh.draw.tab[tid] = kSvExp2Table[tid];
   if (tid == 0) sh.draw.flag = wait_ready(P, b) ? 1 : 0;
   __syncthreads();
   if (!sh.draw.flag) return;
-  draw_chunk<DT, VEC, SUB>(P, b, (int)(d % P.np), sh.draw);
+  draw_chunk<DT, VEC, SUB>(P, b, (int)it.idx, sh.draw);
 }
 
 // ---------------------------------------------------------------- greedy mode (T = 0)
@@ -1266,6 +1288,10 @@ bool take_fused(long long B, int rows_per_seq, long long V, int es, bool sampler
 
 void force_path(int path) { g_force_path.store(path); }
 
+// Sequences between a sequence's streaming tickets and its draw tickets in
+// the fused kernel (B: every streaming ticket first).
+long long fused_lag(long long B) { return B; }
+
 void withhold_plans(int on) { g_withhold.store(on ? 1 : 0); }
 
 int kernels_per_call(long long B, int rows_per_seq, long long V, int es) {
@@ -1273,9 +1299,10 @@ int kernels_per_call(long long B, int rows_per_seq, long long V, int es) {
 }
 
 template <int DT, bool VEC, int SUB>
-cudaError_t launch_fused(const Params& P, cudaStream_t st, const Events& ev) {
-  const long long n_stream = (P.n_units + kWarps - 1) / kWarps;
-  fused_kernel<DT, VEC, SUB><<<(unsigned)(n_stream + (long long)P.B * P.np), kThreads, 0, st>>>(P);
+cudaError_t launch_fused(Params P, cudaStream_t st, const Events& ev) {
+  P.nsi = (P.ns + kWarps - 1) / kWarps;
+  P.lag = fused_lag(P.B);
+  fused_kernel<DT, VEC, SUB><<<(unsigned)((long long)P.B * (P.nsi + P.np)), kThreads, 0, st>>>(P);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess && ev.stats_done)
     e = cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
