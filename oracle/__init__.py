@@ -21,5 +21,7 @@ from .spec_sampling import (  # noqa: F401
     temperature_softmax,
     verify,
     verify_greedy,
+    verify_topk,
+    topk_mask,
     verify_inputs,
 )

@@ -7,8 +7,9 @@ calls anything here, and this module shares no code with it.
 What it computes, step by step, in the order and notation of
 "Accelerating Large Language Model Decoding with Speculative Sampling"
 (Chen et al., DeepMind), as summarised by its wikillm.com paper card (the
-draft-side sampler of Algorithm 2 step 1, `draft_sample`, and the greedy
-variant, `verify_greedy`, follow `verify`):
+draft-side sampler of Algorithm 2 step 1, `draft_sample`, the greedy
+variant, `verify_greedy`, and verification on top-k filtered distributions,
+`verify_topk`, follow `verify`):
 
 * q(.|...) and p(.|...) are the target and draft distributions. The decoding
   transform (temperature) is applied to both before anything else
@@ -318,6 +319,44 @@ def verify_greedy(target: np.ndarray, tokens: np.ndarray) -> GreedyResult:
     out[failed] = -1
     n_acc[failed] = -1
     return GreedyResult(out, n_acc, status.astype(np.int64), np.where(failed[:, None], -1, am))
+
+
+def topk_mask(logits: np.ndarray, k: int) -> np.ndarray:
+    """The top-k decoding transform on logits (U16): every entry outside the k
+    largest of its row becomes -inf (probability 0 after the softmax), the
+    rest are unchanged. Order: larger logit first, ties to the smaller token
+    id (-0.0 equals +0.0). k >= V keeps every entry. Rows holding NaN are
+    returned unchanged (they fail anyway, U12)."""
+    logits = np.asarray(logits, dtype=np.float64)
+    V = logits.shape[-1]
+    if k >= V:
+        return logits.copy()
+    flat = logits.reshape(-1, V)
+    out = np.full_like(flat, -np.inf)
+    for r in range(flat.shape[0]):
+        row = flat[r]
+        if np.isnan(row).any():
+            out[r] = row
+            continue
+        order = np.argsort(-(row + 0.0), kind="stable")   # descending; stable keeps id order
+        keep = order[:k]
+        out[r, keep] = row[keep]
+    return out.reshape(logits.shape)
+
+
+def verify_topk(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
+                uniforms: np.ndarray, temperature: float, top_k: int) -> OracleResult:
+    """Verification on top-k filtered distributions: the card's §4.2
+    "Decoding transforms" (apply top-k to both p and q first, then run the
+    rejection scheme on the modified distributions) and Pitfalls ("Use the
+    same transformed distributions everywhere"). Each of the 2K+1 rows keeps
+    its top_k largest logits (U16, `topk_mask`); the temperature softmax of
+    the kept entries, the thresholds, the residual and the draws are then
+    exactly those of `verify`."""
+    if top_k < 1:
+        raise ValueError("top_k must be >= 1")
+    return verify(topk_mask(target, top_k), topk_mask(draft, top_k), tokens, uniforms,
+                  temperature)
 
 
 def _widen(x) -> np.ndarray:

@@ -471,7 +471,94 @@ def pin_greedy_failures(O):
     assert 0 <= r.n_accepted[0] <= K and (r.out_tokens[0, : r.n_accepted[0] + 1] >= 0).all()
 
 
+# ---------------------------------------------------------------- top-k pins
+
+def pin_topk_mask_cases(O):
+    """Hand-checked masks (U16): ties to the smaller id, -0 equal to +0,
+    -inf entries last, k >= V keeps the row."""
+    ni = -np.inf
+    cases = [
+        ([3.0, 1.0, 3.0, 2.0, -0.0, 0.0], 3, [3.0, ni, 3.0, 2.0, ni, ni]),
+        ([1.0, 2.0, 2.0, 2.0], 2, [ni, 2.0, 2.0, ni]),
+        ([-0.0, 0.0, -1.0], 1, [-0.0, ni, ni]),
+        ([0.0, -0.0, -1.0], 1, [0.0, ni, ni]),
+        ([ni, 5.0, ni, 4.0], 3, [ni, 5.0, ni, 4.0]),          # a -inf entry fills the third slot
+        ([1.0, 2.0, 3.0], 3, [1.0, 2.0, 3.0]),
+        ([1.0, 2.0, 3.0], 7, [1.0, 2.0, 3.0]),
+    ]
+    for row, k, want in cases:
+        got = O.topk_mask(np.array([row]), k)[0]
+        assert np.array_equal(got, np.array(want)), (row, k, got)
+
+
+def pin_topk_hand_case(O):
+    """Worked by hand: V = 3, K = 1, k = 2, T = 1. Target probabilities
+    .5, .3, .2 keep ids 0, 1 -> q = .625, .375, 0; draft .2, .3, .5 keep ids
+    2, 1 -> p = 0, .375, .625. The draft x~ = 2 has q(2) = 0: rejected. The
+    residual (q - p)_+ = .625, 0, 0 draws id 0 for any uniform (had p not
+    been filtered, (q - p)_+ = .425, .075, 0 would draw id 1 at u = .9)."""
+    tl = np.log(np.array([[[0.5, 0.3, 0.2], [0.4, 0.4, 0.2]]]))
+    dl = np.log(np.array([[[0.2, 0.3, 0.5]]]))
+    r = O.verify_topk(tl, dl, np.array([[2]]), np.array([[0.5, 0.9, 0.5]]), 1.0, 2)
+    assert r.status[0] == 0
+    assert list(r.out_tokens[0]) == [0, -1] and r.n_accepted[0] == 0, r.out_tokens
+    np.testing.assert_allclose(r.thresholds[0], [0.0])
+    np.testing.assert_allclose(r.sample_prob[0], 1.0)
+
+
+def pin_topk_full_is_verify(O):
+    """k >= V is no filter: verify_topk equals verify."""
+    rng = np.random.default_rng(23)
+    B, K, V = 16, 3, 30
+    tl, dl = rng.normal(0, 2, (B, K + 1, V)), rng.normal(0, 2, (B, K, V))
+    tok, uni = rng.integers(0, V, (B, K)), rng.random((B, K + 2))
+    a, b = O.verify(tl, dl, tok, uni, 0.8), O.verify_topk(tl, dl, tok, uni, 0.8, V)
+    assert (a.out_tokens == b.out_tokens).all() and (a.n_accepted == b.n_accepted).all()
+    np.testing.assert_array_equal(a.thresholds, b.thresholds)
+
+
+def pin_topk_one_is_greedy(O):
+    """k = 1 leaves one-hot distributions at each row's first argmax, on which
+    the general rule is the greedy rule (U15), for any drafts and T."""
+    rng = np.random.default_rng(29)
+    B, K, V = 64, 4, 20
+    tl = np.round(rng.normal(0, 1.5, (B, K + 1, V)), 1)    # rounded: ties occur
+    dl = np.round(rng.normal(0, 1.5, (B, K, V)), 1)
+    pick = rng.random((B, K))
+    tok = np.where(pick < 0.5, dl.argmax(-1), np.where(pick < 0.8, tl[:, :K].argmax(-1),
+                                                       rng.integers(0, V, (B, K))))
+    uni = rng.random((B, K + 2)) * 0.999
+    r = O.verify_topk(tl, dl, tok, uni, 1.3, 1)
+    g = O.verify_greedy(tl, tok)
+    assert (r.out_tokens == g.out_tokens).all() and (r.n_accepted == g.n_accepted).all()
+
+
+def pin_topk_law(O, n=200_000, V=12, k=5, seed=31):
+    """Theorem 1 under the transform: the first emitted token is distributed as
+    the top-k filtered q; chi-square against scipy's softmax of the kept
+    logits, with the draft drawn from the filtered p by inverse CDF."""
+    from scipy import stats
+
+    rng = np.random.default_rng(seed)
+    tl = rng.normal(0, 1.0, (1, 2, V))
+    dl = rng.normal(0, 1.0, (1, 1, V))
+    T = 0.9
+    keep_q = np.argsort(-tl[0, 0], kind="stable")[:k]
+    keep_p = np.argsort(-dl[0, 0], kind="stable")[:k]
+    pf = np.zeros(V)
+    pf[keep_p] = softmax(dl[0, 0, keep_p] / T)
+    toks = np.minimum(np.searchsorted(np.cumsum(pf), rng.random(n), side="right"), V - 1)
+    r = O.verify_topk(np.repeat(tl, n, 0), np.repeat(dl, n, 0), toks[:, None],
+                      rng.random((n, 3)), T, k)
+    first = r.out_tokens[:, 0]
+    counts = np.bincount(first, minlength=V)
+    assert counts[np.setdiff1d(np.arange(V), keep_q)].sum() == 0
+    expect = softmax(tl[0, 0, keep_q] / T) * n
+    assert stats.chisquare(counts[keep_q], expect * counts[keep_q].sum() / expect.sum()).pvalue > 1e-4
+
+
 FAST_PINS = (pin_golden, pin_theorem1, pin_sequential, pin_library_special_cases,
              pin_invariants, pin_failures, pin_draft_golden, pin_draft_failures,
              pin_draft_matches_bonus, pin_greedy_golden, pin_greedy_is_zero_temperature,
-             pin_greedy_failures)
+             pin_greedy_failures, pin_topk_mask_cases, pin_topk_hand_case,
+             pin_topk_full_is_verify, pin_topk_one_is_greedy)

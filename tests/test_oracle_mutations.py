@@ -58,6 +58,14 @@ MUTATIONS = [
      "out[b, j[b]] = am[b, j[b]]", "out[b, j[b]] = tokens[b, min(j[b], K - 1)]"),
     ("greedy compares with the next row's argmax",
      "match = tokens == am[:, :K]", "match = tokens == am[:, 1:]"),
+    ("top-k ties go to the larger id",
+     "order = np.argsort(-(row + 0.0), kind=\"stable\")",
+     "order = (V - 1 - np.argsort(-(row[::-1] + 0.0), kind=\"stable\"))"),
+    ("top-k keeps one too many",
+     "keep = order[:k]", "keep = order[:k + 1]"),
+    ("top-k filters the target only",
+     "return verify(topk_mask(target, top_k), topk_mask(draft, top_k), tokens, uniforms,",
+     "return verify(topk_mask(target, top_k), draft, tokens, uniforms,"),
 ]
 
 

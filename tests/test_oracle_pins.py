@@ -111,3 +111,23 @@ def test_greedy_is_the_zero_temperature_limit():
 
 def test_greedy_failures():
     _pins.pin_greedy_failures(oracle)
+
+
+def test_topk_mask_hand_cases():
+    _pins.pin_topk_mask_cases(oracle)
+
+
+def test_topk_with_k_at_least_v_is_verify():
+    _pins.pin_topk_full_is_verify(oracle)
+
+
+def test_topk_with_k_one_is_greedy():
+    _pins.pin_topk_one_is_greedy(oracle)
+
+
+def test_topk_first_token_law_is_filtered_q():
+    _pins.pin_topk_law(oracle)
+
+
+def test_topk_hand_case_filters_the_draft_too():
+    _pins.pin_topk_hand_case(oracle)
