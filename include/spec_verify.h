@@ -239,6 +239,36 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
                        int V, int dtype, int32_t* out_tokens, int32_t* n_accepted,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- top-k filtered verification
+ *
+ * The card's §4.2 "Decoding transforms": top-k is applied to both p and q,
+ * and the rejection scheme then runs on the filtered distributions (the
+ * Pitfalls section: the same transformed distributions are used for the
+ * thresholds, the residual and the bonus draw). Each of the 2K+1 rows keeps
+ * its top_k largest logits; ties go to the smaller token id and -0.0 equals
+ * +0.0; the other entries count as -inf. The kept entries' softmax at
+ * temperature T, the thresholds min(1, q/p), the residual max(0, q - p) and
+ * the inverse-CDF draws are those of spec_verify, on the filtered rows. */
+
+/* Bytes of device workspace spec_verify_topk needs; 0 for invalid sizes.
+ * top_k >= V keeps every entry and needs sv_workspace_size(B, K, V, dtype). */
+size_t sv_topk_workspace_size(int B, int K, int V, int dtype, int top_k);
+
+/* Top-k filtered verification. Arguments as for spec_verify, plus
+ *   top_k  entries kept per row: 1 <= top_k <= 256, or top_k >= V (every
+ *          entry kept: the call is spec_verify's); other values return
+ *          SV_ERR_SHAPE
+ * Rows are reduced to their top_k (token id, logit) pairs by a radix select
+ * (one CTA per row), then the verification runs on those pairs in fp64 (one
+ * warp per sequence): two kernels per call. Failures and status bits as for
+ * spec_verify (a row holding +inf or NaN fails its sequence, a row whose kept
+ * entries are all -inf is an empty row). Returns SV_OK once enqueued, or a
+ * host-side error code with nothing enqueued; B == 0 returns SV_OK at once. */
+int spec_verify_topk(const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                     int dtype, float temperature, int top_k, int32_t* out_tokens,
+                     int32_t* n_accepted, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Reads the device status word of the last call that used `workspace`: waits
  * for `stream`, then stores the OR of the SV_DEV_* bits in *status. */
 int sv_read_device_status(const void* workspace, void* stream, int* status);

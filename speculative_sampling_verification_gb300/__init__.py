@@ -27,7 +27,7 @@ __all__ = [
     "sv_status_string", "sv_kernels_per_call", "spec_verify_static", "verify",
     "sv_sample_workspace_size", "spec_draft_sample", "draft_sample",
     "sv_greedy_workspace_size", "spec_verify_greedy", "verify_greedy", "sv_force_path",
-    "sv_test_withhold_plans",
+    "sv_test_withhold_plans", "sv_topk_workspace_size", "spec_verify_topk", "verify_topk",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -43,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "spec_verify_host", "sv_read_device_status", "sv_status_string", "sv_kernels_per_call",
     "spec_verify_static", "sv_sample_workspace_size", "spec_draft_sample",
     "sv_greedy_workspace_size", "spec_verify_greedy", "sv_force_path", "sv_test_withhold_plans",
+    "sv_topk_workspace_size", "spec_verify_topk",
 )
 
 _lib = None
@@ -95,6 +96,10 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.sv_greedy_workspace_size.restype = sz
     lib.spec_verify_greedy.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
     lib.spec_verify_greedy.restype = i32
+    lib.sv_topk_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.sv_topk_workspace_size.restype = sz
+    lib.spec_verify_topk.argtypes = core[:9] + [i32] + core[9:]
+    lib.spec_verify_topk.restype = i32
     lib.sv_kernels_per_call.argtypes = [i32, i32, i32, i32]
     lib.sv_kernels_per_call.restype = i32
     lib.sv_force_path.argtypes = [i32]
@@ -276,6 +281,42 @@ def verify(target, draft, tokens, uniforms, temperature, *, workspace=None, debu
     if debug:
         return out, nacc, {"row_lse": lse, "thresholds": thr, "sample_prob": prob,
                            "workspace": ws}
+    return out, nacc
+
+
+def sv_topk_workspace_size(B: int, K: int, V: int, dtype: int, top_k: int) -> int:
+    return int(load_library().sv_topk_workspace_size(B, K, V, dtype, top_k))
+
+
+def spec_verify_topk(target, draft, tokens, uniforms, temperature, top_k, out_tokens, n_accepted,
+                     workspace, stream=None) -> int:
+    """Direct binding of top-k filtered verification; returns the host status code."""
+    B, K, V, dt = _check(target, draft, tokens, uniforms)
+    return int(load_library().spec_verify_topk(
+        _ptr(target), _ptr(draft), _ptr(tokens), _ptr(uniforms), B, K, V, dt,
+        ctypes.c_float(temperature), int(top_k), _ptr(out_tokens), _ptr(n_accepted),
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(target.device, stream)))
+
+
+def verify_topk(target, draft, tokens, uniforms, temperature, top_k, *, workspace=None,
+                stream=None):
+    """Allocate outputs (and a workspace if none is given) and run top-k
+    filtered verification; returns (out_tokens [B, K+1] int32, n_accepted [B] int32)."""
+    if tokens.dtype == torch.int64:
+        tokens = tokens.to(torch.int32)
+    B, K, V, dt = _check(target, draft, tokens, uniforms)
+    dev = target.device
+    out = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+    nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = workspace
+    if ws is None:
+        n = sv_topk_workspace_size(B, K, V, dt, int(top_k))
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    rc = spec_verify_topk(target, draft, tokens, uniforms, temperature, top_k, out, nacc, ws,
+                          stream=stream)
+    if rc != SV_OK:
+        raise StatusError(rc, "spec_verify_topk")
     return out, nacc
 
 

@@ -292,6 +292,63 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+size_t sv_topk_workspace_size(int B, int K, int V, int dtype, int top_k) {
+  if (top_k >= V) return sv_workspace_size(B, K, V, dtype);
+  sv::TopKLayout L;
+  if (!sv::make_topk_layout(B, K, V, dtype, top_k, &L)) return 0;
+  return L.total;
+}
+
+int spec_verify_topk(const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                     int dtype, float temperature, int top_k, int32_t* out_tokens,
+                     int32_t* n_accepted, void* workspace, size_t workspace_bytes, void* stream) {
+  if (top_k >= V && V >= 1)  // keeps every entry: the unfiltered verification
+    return run(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype, temperature,
+               out_tokens, n_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
+               nullptr);
+  if (dtype != SV_BF16 && dtype != SV_F32) return SV_ERR_DTYPE;
+  sv::TopKLayout L;
+  if (!sv::make_topk_layout(B, K, V, dtype, top_k, &L)) return SV_ERR_SHAPE;
+  if (!std::isfinite(temperature) || !(temperature > 0.0f)) return SV_ERR_TEMPERATURE;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !draft_tokens || !uniforms || !out_tokens ||
+      !n_accepted || !workspace)
+    return SV_ERR_NULL;
+  if (misaligned(target_logits, L.es) || misaligned(draft_logits, L.es) ||
+      misaligned(draft_tokens, 4) || misaligned(uniforms, 4) || misaligned(out_tokens, 4) ||
+      misaligned(n_accepted, 4) || misaligned(workspace, 256))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
+  sv::Params P{};
+  P.B = B;
+  P.K = K;
+  P.V = V;
+  P.dtype = dtype;
+  P.es = L.es;
+  P.rows_per_seq = L.rows_per_seq;
+  P.top_k = top_k;
+  P.temp_d = (double)temperature;
+  int ib = 1;
+  while (ib < 31 && ((long long)(V - 1) >> ib) != 0) ++ib;
+  P.key_ibits = ib;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  P.ctrl = ws;
+  P.ctrl_bytes = L.ctrl_bytes;
+  P.status = reinterpret_cast<unsigned*>(ws);
+  P.topk_flag = reinterpret_cast<unsigned*>(ws + L.off_flag);
+  P.topk_idx = reinterpret_cast<int*>(ws + L.off_idx);
+  P.topk_val = reinterpret_cast<float*>(ws + L.off_val);
+  P.target = target_logits;
+  P.draft = draft_logits;
+  P.tokens = draft_tokens;
+  P.uniforms = uniforms;
+  P.out_tokens = out_tokens;
+  P.n_acc = n_accepted;
+  const cudaError_t e = sv::launch_topk(P, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 int sv_read_device_status(const void* workspace, void* stream, int* status) {
   if (!workspace || !status) return SV_ERR_NULL;
   if (misaligned(workspace, 256)) return SV_ERR_ALIGN;

@@ -112,6 +112,33 @@ inline bool make_greedy_layout(int B, int K, int V, int dtype, Layout* L) {
   return make_layout_rows(B, K + 1, V, dtype, L);
 }
 
+// Top-k filtered verification: the control block (status), then per row of
+// the B (2K+1) rows a flag word and its k kept (id, logit) pairs.
+constexpr int kTopKMax = 256;
+struct TopKLayout {
+  int es, rows_per_seq;
+  long long rows;
+  size_t ctrl_bytes, off_flag, off_idx, off_val, total;
+};
+inline bool make_topk_layout(int B, int K, int V, int dtype, int top_k, TopKLayout* L) {
+  if (B < 0 || K < 1 || K > kMaxK || V < 1 || top_k < 1 || top_k > kTopKMax) return false;
+  if (dtype != 0 && dtype != 1) return false;
+  L->es = dtype == 0 ? 2 : 4;
+  L->rows_per_seq = 2 * K + 1;
+  L->rows = (long long)B * L->rows_per_seq;
+  size_t off = 0;
+  L->ctrl_bytes = 16;
+  off = align_up(off + L->ctrl_bytes, 256);
+  L->off_flag = off;
+  off = align_up(off + (size_t)L->rows * 4, 256);
+  L->off_idx = off;
+  off = align_up(off + (size_t)L->rows * top_k * 4, 256);
+  L->off_val = off;
+  off = align_up(off + (size_t)L->rows * top_k * 4, 256);
+  L->total = off;
+  return true;
+}
+
 // The draft-side sampler: N independent rows, each its own "sequence".
 inline bool make_sample_layout(int N, int V, int dtype, Layout* L) {
   return make_layout_rows(N, 1, V, dtype, L);
@@ -129,6 +156,12 @@ struct Params {
   int sampler;     // 1: draft-side sampler (one row per sequence, K = 0, no scan)
   int fused;       // 1: the fused kernel runs (plans are published with a release flag)
   int withhold;    // test hook: 1 = never publish the flag, so the draw's waits run out
+  int top_k;       // top-k path: entries kept per row
+  double temp_d;   // top-k path: the temperature, widened to fp64
+  int key_ibits;   // top-k path: bits of the (V-1-id) tie-break below the value key
+  unsigned* topk_flag;  // top-k path: [B (2K+1)] row flags (nonfinite)
+  int* topk_idx;        // top-k path: [B (2K+1), k] kept ids, ascending
+  float* topk_val;      // top-k path: [B (2K+1), k] their logits
   long long nsi;   // fused kernel: streaming items (of up to 8 units) per sequence
   long long lag;   // fused kernel: sequences between a sequence's streaming and draw tickets
   double inv_t;    // 1/T in fp64 (scan)
@@ -170,6 +203,9 @@ struct Events {
 cudaError_t launch_all(Params P, bool aligned, cudaStream_t stream, const Events& ev);
 // Greedy mode: one kernel over the K+1 target rows of each sequence.
 cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t stream);
+// Top-k filtered verification: the row selection kernel, then the sparse
+// verification kernel.
+cudaError_t launch_topk(const Params& P, cudaStream_t stream);
 // Kernels one call over B sequences of rows_per_seq rows of V elements of
 // `es` bytes launches: 1 when the fused kernel is taken, else 2.
 int kernels_per_call(long long B, int rows_per_seq, long long V, int es);

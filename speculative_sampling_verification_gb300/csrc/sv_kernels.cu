@@ -22,6 +22,7 @@
 // Completion counting uses acquire-release atomics ("last CTA to arrive does
 // the follow-up"), so no CTA spins and no co-residency is assumed.
 #include <cfloat>
+#include <math_constants.h>
 #include <climits>
 #include <cstdint>
 #include <atomic>
@@ -1265,6 +1266,325 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) greedy_kernel(
   greedy_scan(P, b, lane);
 }
 
+// ---------------------------------------------------------------- top-k filtered verification
+//
+// The card's §4.2 "Decoding transforms": top-k is applied to both p and q,
+// then the rejection scheme runs on the filtered distributions. Each of the
+// 2K+1 rows keeps its k largest logits (ties to the smaller token id, -0
+// equal to +0). Rows are reduced to their k kept (id, logit) pairs by a radix
+// select (one CTA per row, no sort of the row), and the verification then
+// runs on those k-entry rows, one warp per sequence, in fp64 with the same
+// formulas as the oracle (k is at most 256, so the arithmetic is small).
+
+// Order-preserving key of element idx of a row: the value's bits mapped so
+// that unsigned order is numeric order (-0 folded into +0), above (V-1-idx)
+// in the low `ibits` bits, so that among equal values the smaller id has the
+// larger key; all keys of a row are distinct. Returns true for NaN or +inf.
+template <int DT>
+SV_DEVINL bool topk_key(const unsigned char* row, long long idx, int V, int ibits,
+                        unsigned long long& key, float& val) {
+  uint32_t vk;
+  bool bad;
+  if constexpr (DT == 0) {
+    uint32_t h = __ldg(reinterpret_cast<const unsigned short*>(row) + idx);
+    if (h == 0x8000u) h = 0;
+    bad = ((h & 0x7fffu) > 0x7f80u) || h == 0x7f80u;
+    vk = (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
+    val = __uint_as_float(h << 16);
+  } else {
+    uint32_t f = __float_as_uint(__ldg(reinterpret_cast<const float*>(row) + idx));
+    if (f == 0x80000000u) f = 0;
+    bad = ((f & 0x7fffffffu) > 0x7f800000u) || f == 0x7f800000u;
+    vk = (f & 0x80000000u) ? ~f : (f | 0x80000000u);
+    val = __uint_as_float(f);
+  }
+  key = ((unsigned long long)vk << ibits) | (unsigned long long)(V - 1 - idx);
+  return bad;
+}
+
+static_assert(kThreads == kTopKMax, "the id sort gives one kept entry per thread");
+
+struct TopKShared {
+  unsigned hist[kWarps][256];
+  unsigned wsum[kWarps];
+  unsigned long long prefix;
+  unsigned remaining, in_bucket, next_remaining, found_bin, bad, n_out;
+  int out_idx[kTopKMax];
+  float out_val[kTopKMax];
+};
+
+// One CTA per row: the k largest keys by radix select over 8-bit digits from
+// the top (per-warp shared histograms of the digit among keys that match the
+// bits resolved so far), stopping as soon as the selected bucket is taken
+// whole; then one pass collects exactly k entries, sorted by id (bitonic).
+template <int DT>
+__global__ void __launch_bounds__(kThreads) topk_select_kernel(Params P) {
+  __shared__ TopKShared sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long row = blockIdx.x;
+  const unsigned char* rb = row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
+  const int V = P.V, k = P.top_k, ib = P.key_ibits;
+  const int top = ((DT == 0 ? 16 : 32) + ib + 7) / 8 * 8;
+  if (tid == 0) {
+    sh.prefix = 0;
+    sh.remaining = (unsigned)k;
+    sh.bad = 0;
+    sh.n_out = 0;
+  }
+  int resolved = 0;
+  for (;;) {
+    const int shift = top - resolved - 8;
+    for (int i = tid; i < kWarps * 256; i += kThreads) (&sh.hist[0][0])[i] = 0;
+    __syncthreads();  // also publishes the previous pass's prefix
+    const bool all = shift + 8 >= 64;
+    const unsigned long long pre = all ? 0ull : (sh.prefix >> (shift + 8));
+    unsigned bad = 0;
+    // Every lane runs the same trip count, so the warp is whole at the match.
+    for (long long base = 0; base < V; base += kThreads) {
+      const long long i = base + tid;
+      unsigned bin = 256u;
+      if (i < V) {
+        unsigned long long key;
+        float v;
+        bad |= topk_key<DT>(rb, i, V, ib, key, v) ? 1u : 0u;
+        if (all || (key >> (shift + 8)) == pre) bin = (unsigned)((key >> shift) & 255u);
+      }
+      // Lanes with the same bin add once (the group's leader adds its size).
+      const unsigned grp = __match_any_sync(0xffffffffu, bin);
+      if (bin < 256u && lane == __ffs(grp) - 1) atomicAdd(&sh.hist[warp][bin], __popc(grp));
+    }
+    if (resolved == 0 && __any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(&sh.bad, 1u);
+    __syncthreads();
+    if (sh.bad) break;
+    // Thread t holds bin 255 - t (descending); an inclusive scan over t gives
+    // how many matching keys lie at or above each bin.
+    unsigned tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += sh.hist[w][255 - tid];
+    unsigned inc = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 31) sh.wsum[warp] = inc;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) inc += sh.wsum[w];
+    const unsigned rem = sh.remaining;
+    if (inc >= rem && inc - tot < rem) {
+      sh.found_bin = 255u - (unsigned)tid;
+      sh.in_bucket = tot;
+      sh.next_remaining = rem - (inc - tot);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      sh.prefix |= (unsigned long long)sh.found_bin << shift;
+      sh.remaining = sh.next_remaining;
+    }
+    resolved += 8;
+    __syncthreads();
+    if (sh.in_bucket == sh.remaining || resolved >= top) break;
+  }
+  if (sh.bad) {
+    if (tid == 0) P.topk_flag[row] = kDevNonfinite;
+    return;
+  }
+  // Keep every key whose resolved high bits reach the selected prefix: the
+  // keys above it, and the whole selected bucket.
+  const int lo = top - resolved;
+  const unsigned long long thr = sh.prefix >> lo;
+  for (long long i = tid; i < V; i += kThreads) {
+    unsigned long long key;
+    float v;
+    (void)topk_key<DT>(rb, i, V, ib, key, v);
+    if ((key >> lo) >= thr) {
+      const unsigned slot = atomicAdd(&sh.n_out, 1u);
+      if (slot < (unsigned)kTopKMax) {
+        sh.out_idx[slot] = (int)i;
+        sh.out_val[slot] = v;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid >= (int)sh.n_out) sh.out_idx[tid] = INT_MAX;
+  __syncthreads();
+  for (int size = 2; size <= kTopKMax; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int j = tid ^ stride;
+      if (j > tid) {
+        const bool asc = (tid & size) == 0;
+        if ((sh.out_idx[tid] > sh.out_idx[j]) == asc) {
+          const int ti = sh.out_idx[tid];
+          sh.out_idx[tid] = sh.out_idx[j];
+          sh.out_idx[j] = ti;
+          const float tv = sh.out_val[tid];
+          sh.out_val[tid] = sh.out_val[j];
+          sh.out_val[j] = tv;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (tid < k) {
+    P.topk_idx[row * k + tid] = sh.out_idx[tid];
+    P.topk_val[row * k + tid] = sh.out_val[tid];
+  }
+  if (tid == 0) P.topk_flag[row] = sh.n_out == (unsigned)k ? 0u : kDevNonfinite;
+}
+
+// Position of `x` in a row's ascending kept ids, or -1.
+SV_DEVINL int topk_find(const int* ids, int k, int x) {
+  int lo = 0, hi = k - 1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    const int v = __ldcg(ids + mid);
+    if (v == x) return mid;
+    if (v < x)
+      lo = mid + 1;
+    else
+      hi = mid - 1;
+  }
+  return -1;
+}
+
+SV_DEVINL double warp_max_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+SV_DEVINL double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+struct TopKRows {
+  double m[2 * kMaxK + 1], s[2 * kMaxK + 1];  // max of l/T and sum of exp(l/T - m), per row
+};
+
+// One warp per sequence: the verification of `verify` on the k-entry rows.
+__global__ void __launch_bounds__(128) topk_verify_kernel(Params P) {
+  __shared__ TopKRows rows_sh[4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long b = (long long)blockIdx.x * 4 + warp;
+  if (b >= P.B) return;
+  TopKRows& rs = rows_sh[warp];
+  const int K = P.K, R = P.rows_per_seq, k = P.top_k;
+  const double T = P.temp_d;
+  const long long row0 = b * R;
+  unsigned bits = 0;
+  for (int r = lane; r < R; r += 32) bits |= __ldcg(P.topk_flag + row0 + r);
+  for (int t = lane; t < K; t += 32) {
+    const int x = P.tokens[b * K + t];
+    if (x < 0 || x >= P.V) bits |= kDevTokenRange;
+  }
+  for (int t = lane; t < K + 2; t += 32) {
+    const float u = P.uniforms[b * (K + 2) + t];
+    if (!(u >= 0.0f && u <= 1.0f)) bits |= kDevUniformRange;
+  }
+  // Per row: m = max l/T, S = sum exp(l/T - m) over the kept entries.
+  for (int r = 0; r < R; ++r) {
+    if (__ldcg(P.topk_flag + row0 + r)) continue;  // nonfinite row: its pairs are unset
+    const float* vals = P.topk_val + (row0 + r) * k;
+    double m = -CUDART_INF;
+    for (int e = lane; e < k; e += 32) m = fmax(m, (double)__ldcg(vals + e) / T);
+    m = warp_max_d(m);
+    double s = 0.0;
+    if (m != -CUDART_INF)
+      for (int e = lane; e < k; e += 32) s += exp((double)__ldcg(vals + e) / T - m);
+    s = warp_sum_d(s);
+    if (lane == 0) {
+      rs.m[r] = m;
+      rs.s[r] = s;
+    }
+    if (m == -CUDART_INF) bits |= kDevEmptyRow;
+  }
+  bits = __reduce_or_sync(0xffffffffu, bits);
+  __syncwarp();
+  // q(x) or p(x) of token x in row r.
+  auto prob = [&](int r, int x) -> double {
+    const int pos = topk_find(P.topk_idx + (row0 + r) * k, k, x);
+    if (pos < 0) return 0.0;
+    return exp((double)__ldcg(P.topk_val + (row0 + r) * k + pos) / T - rs.m[r]) / rs.s[r];
+  };
+  int j = bits ? -1 : K;
+  if (!bits) {
+    for (int t0 = 0; t0 < K; t0 += 32) {
+      const int t = t0 + lane;
+      bool rej = false;
+      if (t < K) {
+        const int x = P.tokens[b * K + t];
+        const double q = prob(t, x), p = prob(K + 1 + t, x);
+        const double thr = p > 0.0 ? fmin(1.0, q / p) : (q > 0.0 ? 1.0 : 0.0);
+        rej = !((double)P.uniforms[b * (K + 2) + t] < thr);
+      }
+      const unsigned mask = __ballot_sync(0xffffffffu, rej);
+      if (mask) {
+        j = t0 + __ffs(mask) - 1;
+        break;
+      }
+    }
+  }
+  int token = -1;
+  if (!bits) {
+    const bool resid = j < K;
+    const int qr = resid ? j : K;
+    const int* qids = P.topk_idx + (row0 + qr) * k;
+    const float* qvals = P.topk_val + (row0 + qr) * k;
+    const int per = (k + 31) / 32, e0 = min(k, lane * per), e1 = min(k, e0 + per);
+    auto weight = [&](int e, bool residual) -> double {
+      const double q = exp((double)__ldcg(qvals + e) / T - rs.m[qr]) / rs.s[qr];
+      if (!residual) return q;
+      const double p = prob(K + 1 + j, __ldcg(qids + e));
+      return fmax(0.0, q - p);
+    };
+    bool use_res = resid;
+    double lsum = 0.0;
+    for (int e = e0; e < e1; ++e) lsum += weight(e, use_res);
+    double total = warp_sum_d(lsum);
+    if (use_res && !(total > 0.0)) {  // zero residual: fall back to q (U5)
+      use_res = false;
+      lsum = 0.0;
+      for (int e = e0; e < e1; ++e) lsum += weight(e, false);
+      total = warp_sum_d(lsum);
+    }
+    const double target = (double)P.uniforms[b * (K + 2) + (resid ? K : K + 1)] * total;
+    // Exclusive prefix of the lanes' sums, then the first entry whose
+    // cumulative weight passes the target; else the last positive entry.
+    double inc = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    double c = inc - lsum;
+    int first = INT_MAX, lastpos = -1;
+    for (int e = e0; e < e1; ++e) {
+      const double w = weight(e, use_res);
+      c += w;
+      if (w > 0.0) {
+        lastpos = e;
+        if (first == INT_MAX && c > target) first = e;
+      }
+    }
+    first = __reduce_min_sync(0xffffffffu, first);
+    lastpos = __reduce_max_sync(0xffffffffu, lastpos);
+    const int pick = first != INT_MAX ? first : lastpos;
+    token = pick >= 0 ? __ldcg(qids + pick) : -1;
+  }
+  if (lane == 0) {
+    if (bits) atomicOr(P.status, bits);
+    P.n_acc[b] = j;
+  }
+  for (int t = lane; t <= K; t += 32) {
+    int o = -1;
+    if (j >= 0 && t < j) o = P.tokens[b * K + t];
+    if (j >= 0 && t == j) o = token;
+    P.out_tokens[b * (K + 1) + t] = o;
+  }
+}
+
 // ---------------------------------------------------------------- host-side launch
 
 namespace {
@@ -1376,6 +1696,25 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
   if (e != cudaSuccess) return e;
   if (ev.end) e = cudaEventRecordWithFlags(ev.end, st, cudaEventRecordExternal);
   return e;
+}
+
+cudaError_t launch_topk(const Params& P, cudaStream_t st) {
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  e = prepare_device(device);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(P.ctrl, 0, P.ctrl_bytes, st);
+  if (e != cudaSuccess) return e;
+  const unsigned rows = (unsigned)((long long)P.B * P.rows_per_seq);
+  if (P.dtype == 0)
+    topk_select_kernel<0><<<rows, kThreads, 0, st>>>(P);
+  else
+    topk_select_kernel<1><<<rows, kThreads, 0, st>>>(P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  topk_verify_kernel<<<(unsigned)((P.B + 3) / 4), 128, 0, st>>>(P);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t st) {

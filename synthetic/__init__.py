@@ -7,7 +7,7 @@ fed from here, and neither imports the other.
 """
 
 from .configs import WORKLOADS, SWEEP_K, SWEEP_NOISE, Workload, sweep_workload, get_workload
-from .generate import make_inputs, make_sequence, DTYPES
+from .generate import make_inputs, make_sequence, make_topk_inputs, topk_draft_tokens, DTYPES
 
 __all__ = [
     "WORKLOADS",
@@ -18,5 +18,7 @@ __all__ = [
     "get_workload",
     "make_inputs",
     "make_sequence",
+    "make_topk_inputs",
+    "topk_draft_tokens",
     "DTYPES",
 ]

@@ -100,3 +100,28 @@ def make_inputs(w: Workload, step: int = 0, seqs=None, pin_memory: bool = False)
         "uniforms": uniforms,
         "temperature": float(w.temperature),
     }
+
+
+def topk_draft_tokens(draft: torch.Tensor, top_k: int, temperature: float,
+                      g: torch.Generator) -> torch.Tensor:
+    """Drafts for top-k decoding: x_t drawn (Gumbel-max) from softmax(dl[t]/T)
+    restricted to the top_k largest logits of draft row t (torch.topk's choice
+    among equal logits at the cut; any choice is a valid draft)."""
+    rows = draft.reshape(-1, draft.shape[-1]).to(torch.float64)
+    if top_k < rows.shape[-1]:
+        keep = torch.topk(rows, top_k, dim=-1).indices
+        masked = torch.full_like(rows, float("-inf"))
+        masked.scatter_(-1, keep, rows.gather(-1, keep))
+        rows = masked
+    return gumbel_max_draw(rows, temperature, g).reshape(draft.shape[:-1])
+
+
+def make_topk_inputs(w: Workload, top_k: int, step: int = 0, seqs=None, pin_memory: bool = False):
+    """`make_inputs` with drafts drawn from the top-k filtered draft rows (a
+    fourth per-sequence stream), as a top-k decoding draft model would."""
+    inp = make_inputs(w, step=step, seqs=seqs, pin_memory=pin_memory)
+    idx = list(range(w.B)) if seqs is None else list(seqs)
+    for i, b in enumerate(idx):
+        inp["tokens"][i] = topk_draft_tokens(inp["draft"][i], top_k, w.temperature,
+                                             _gen(w, step, b, 3))
+    return inp

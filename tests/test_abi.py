@@ -147,3 +147,32 @@ def test_greedy_workspace_and_validation(lib):
     assert call(t=(1 << 20) + 2) == 5 and call(ws=(1 << 20) + 16) == 5
     assert call(wsb=16) == 6
     assert call(B=0, t=0, tok=0) == 0
+
+
+def test_topk_workspace_and_validation(lib):
+    full = lib.sv_workspace_size(8, 4, 32000, sv.SV_BF16)
+    small = lib.sv_topk_workspace_size(8, 4, 32000, sv.SV_BF16, 50)
+    assert 0 < small < full
+    # top_k >= V keeps every entry: the unfiltered call and its workspace.
+    assert lib.sv_topk_workspace_size(8, 4, 32000, sv.SV_BF16, 32000) == full
+    assert lib.sv_topk_workspace_size(8, 4, 100, sv.SV_BF16, 1000) == lib.sv_workspace_size(8, 4, 100, sv.SV_BF16)
+    for bad in ((1, 4, 1000, 0, 0), (1, 4, 1000, 0, 257), (1, 4, 1000, 0, -3), (-1, 4, 1000, 0, 8),
+                (1, 0, 1000, 0, 8), (1, 65, 1000, 0, 8), (1, 4, 1000, 7, 8)):
+        assert lib.sv_topk_workspace_size(*bad) == 0
+    vp = ctypes.c_void_p
+
+    def call(t=1 << 20, d=1 << 20, tok=1 << 20, u=1 << 20, B=2, K=3, V=1000, dtype=sv.SV_F32,
+             T=1.0, k=20, out=1 << 20, nacc=1 << 20, ws=1 << 20, wsb=1 << 30):
+        return lib.spec_verify_topk(vp(t), vp(d), vp(tok), vp(u), B, K, V, dtype,
+                                    ctypes.c_float(T), k, vp(out), vp(nacc), vp(ws), wsb, None)
+
+    assert call(dtype=3) == 4
+    assert call(k=0) == 2 and call(k=257) == 2 and call(K=0) == 2 and call(B=-1) == 2
+    assert call(T=0.0) == 3 and call(T=float("nan")) == 3
+    assert call(t=0) == 1 and call(d=0) == 1 and call(u=0) == 1 and call(ws=0) == 1
+    assert call(t=(1 << 20) + 2) == 5 and call(tok=(1 << 20) + 2) == 5
+    assert call(ws=(1 << 20) + 16) == 5
+    assert call(wsb=16) == 6
+    # top_k >= V takes the unfiltered entry point, with its own checks.
+    assert call(k=5000, wsb=16) == 6 and call(k=5000, T=-1.0) == 3
+    assert call(B=0, t=0, d=0, tok=0, u=0) == 0
