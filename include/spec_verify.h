@@ -258,9 +258,11 @@ size_t sv_topk_workspace_size(int B, int K, int V, int dtype, int top_k);
  *   top_k  entries kept per row: 1 <= top_k <= 256, or top_k >= V (every
  *          entry kept: the call is spec_verify's); other values return
  *          SV_ERR_SHAPE
- * Rows are reduced to their top_k (token id, logit) pairs by a radix select
- * (one CTA per row), then the verification runs on those pairs in fp64 (one
- * warp per sequence): two kernels per call. Failures and status bits as for
+ * Each row is reduced to its top_k entries in one pass over it (one CTA per
+ * row: a running threshold and a candidate buffer in shared memory, with an
+ * exact radix select over the row for adversarial orders), their softmax is
+ * taken in fp64, and the verification runs on the kept (token id,
+ * probability) pairs (one CTA per sequence): two kernels per call. Failures and status bits as for
  * spec_verify (a row holding +inf or NaN fails its sequence, a row whose kept
  * entries are all -inf is an empty row). Returns SV_OK once enqueued, or a
  * host-side error code with nothing enqueued; B == 0 returns SV_OK at once. */

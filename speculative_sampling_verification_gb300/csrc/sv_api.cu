@@ -337,15 +337,18 @@ int spec_verify_topk(const void* target_logits, const void* draft_logits,
   P.ctrl_bytes = L.ctrl_bytes;
   P.status = reinterpret_cast<unsigned*>(ws);
   P.topk_flag = reinterpret_cast<unsigned*>(ws + L.off_flag);
+  P.topk_at = reinterpret_cast<double*>(ws + L.off_at);
   P.topk_idx = reinterpret_cast<int*>(ws + L.off_idx);
-  P.topk_val = reinterpret_cast<float*>(ws + L.off_val);
+  P.topk_prob = reinterpret_cast<double*>(ws + L.off_prob);
   P.target = target_logits;
   P.draft = draft_logits;
   P.tokens = draft_tokens;
   P.uniforms = uniforms;
   P.out_tokens = out_tokens;
   P.n_acc = n_accepted;
-  const cudaError_t e = sv::launch_topk(P, static_cast<cudaStream_t>(stream));
+  const bool aligned = !misaligned(target_logits, 16) && !misaligned(draft_logits, 16) &&
+                       ((size_t)V * L.es) % 16 == 0;
+  const cudaError_t e = sv::launch_topk(P, aligned, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

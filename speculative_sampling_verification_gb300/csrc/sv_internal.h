@@ -113,12 +113,13 @@ inline bool make_greedy_layout(int B, int K, int V, int dtype, Layout* L) {
 }
 
 // Top-k filtered verification: the control block (status), then per row of
-// the B (2K+1) rows a flag word and its k kept (id, logit) pairs.
+// the B (2K+1) rows a flag word, the probability of the row's drafted token,
+// and its k kept (id, probability) pairs.
 constexpr int kTopKMax = 256;
 struct TopKLayout {
   int es, rows_per_seq;
   long long rows;
-  size_t ctrl_bytes, off_flag, off_idx, off_val, total;
+  size_t ctrl_bytes, off_flag, off_at, off_idx, off_prob, total;
 };
 inline bool make_topk_layout(int B, int K, int V, int dtype, int top_k, TopKLayout* L) {
   if (B < 0 || K < 1 || K > kMaxK || V < 1 || top_k < 1 || top_k > kTopKMax) return false;
@@ -131,10 +132,12 @@ inline bool make_topk_layout(int B, int K, int V, int dtype, int top_k, TopKLayo
   off = align_up(off + L->ctrl_bytes, 256);
   L->off_flag = off;
   off = align_up(off + (size_t)L->rows * 4, 256);
+  L->off_at = off;
+  off = align_up(off + (size_t)L->rows * 8, 256);
   L->off_idx = off;
   off = align_up(off + (size_t)L->rows * top_k * 4, 256);
-  L->off_val = off;
-  off = align_up(off + (size_t)L->rows * top_k * 4, 256);
+  L->off_prob = off;
+  off = align_up(off + (size_t)L->rows * top_k * 8, 256);
   L->total = off;
   return true;
 }
@@ -159,9 +162,10 @@ struct Params {
   int top_k;       // top-k path: entries kept per row
   double temp_d;   // top-k path: the temperature, widened to fp64
   int key_ibits;   // top-k path: bits of the (V-1-id) tie-break below the value key
-  unsigned* topk_flag;  // top-k path: [B (2K+1)] row flags (nonfinite)
+  unsigned* topk_flag;  // top-k path: [B (2K+1)] row flags (nonfinite, empty row)
+  double* topk_at;      // top-k path: [B (2K+1)] probability of the row's drafted token
   int* topk_idx;        // top-k path: [B (2K+1), k] kept ids, ascending
-  float* topk_val;      // top-k path: [B (2K+1), k] their logits
+  double* topk_prob;    // top-k path: [B (2K+1), k] their probabilities over the kept set
   long long nsi;   // fused kernel: streaming items (of up to 8 units) per sequence
   long long lag;   // fused kernel: sequences between a sequence's streaming and draw tickets
   double inv_t;    // 1/T in fp64 (scan)
@@ -205,7 +209,7 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t stream, const Events
 cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t stream);
 // Top-k filtered verification: the row selection kernel, then the sparse
 // verification kernel.
-cudaError_t launch_topk(const Params& P, cudaStream_t stream);
+cudaError_t launch_topk(const Params& P, bool aligned, cudaStream_t stream);
 // Kernels one call over B sequences of rows_per_seq rows of V elements of
 // `es` bytes launches: 1 when the fused kernel is taken, else 2.
 int kernels_per_call(long long B, int rows_per_seq, long long V, int es);

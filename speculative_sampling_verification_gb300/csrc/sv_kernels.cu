@@ -1271,96 +1271,193 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) greedy_kernel(
 // The card's §4.2 "Decoding transforms": top-k is applied to both p and q,
 // then the rejection scheme runs on the filtered distributions. Each of the
 // 2K+1 rows keeps its k largest logits (ties to the smaller token id, -0
-// equal to +0). Rows are reduced to their k kept (id, logit) pairs by a radix
-// select (one CTA per row, no sort of the row), and the verification then
-// runs on those k-entry rows, one warp per sequence, in fp64 with the same
-// formulas as the oracle (k is at most 256, so the arithmetic is small).
+// equal to +0). A row is reduced to its k kept entries in one streaming pass
+// (one CTA per row): elements are compared against a running threshold, the
+// k-th largest key known so far, and the few that beat it are appended to a
+// candidate buffer in shared memory, which is cut back to its k largest (a
+// radix select over the buffer) once it holds more than a few times k. For
+// rows in random order the threshold rises fast, so nearly every element
+// costs one packed max and one compare, and the row is read from memory
+// once. A row whose candidates overflow the buffer (an adversarial order,
+// such as ascending logits) is selected exactly by a radix select over the
+// row itself instead. The kept entries' softmax is taken in fp64 and stored
+// as (id, q) pairs in ascending id, and the verification runs on those pairs.
 
-// Order-preserving key of element idx of a row: the value's bits mapped so
-// that unsigned order is numeric order (-0 folded into +0), above (V-1-idx)
-// in the low `ibits` bits, so that among equal values the smaller id has the
-// larger key; all keys of a row are distinct. Returns true for NaN or +inf.
+constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelTile = kSelThreads * 8;  // elements per tile: 8 consecutive per thread
+constexpr int kSelCap = 5120;              // candidate buffer entries
+constexpr int kSelTrigger = 1024;          // the buffer is cut back above at most this many
+static_assert(kTopKMax == kSelThreads, "the final stage gives one kept entry per thread");
+
+// Order-preserving map of a bf16 (16-bit) or f32 bit pattern to an unsigned
+// key: unsigned order is numeric order, -0 folded into +0.
 template <int DT>
-SV_DEVINL bool topk_key(const unsigned char* row, long long idx, int V, int ibits,
-                        unsigned long long& key, float& val) {
-  uint32_t vk;
-  bool bad;
+SV_DEVINL uint32_t value_key(uint32_t bits) {
   if constexpr (DT == 0) {
-    uint32_t h = __ldg(reinterpret_cast<const unsigned short*>(row) + idx);
-    if (h == 0x8000u) h = 0;
-    bad = ((h & 0x7fffu) > 0x7f80u) || h == 0x7f80u;
-    vk = (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
-    val = __uint_as_float(h << 16);
+    if (bits == 0x8000u) bits = 0;
+    return (bits & 0x8000u) ? (~bits & 0xffffu) : (bits | 0x8000u);
   } else {
-    uint32_t f = __float_as_uint(__ldg(reinterpret_cast<const float*>(row) + idx));
-    if (f == 0x80000000u) f = 0;
-    bad = ((f & 0x7fffffffu) > 0x7f800000u) || f == 0x7f800000u;
-    vk = (f & 0x80000000u) ? ~f : (f | 0x80000000u);
-    val = __uint_as_float(f);
+    if (bits == 0x80000000u) bits = 0;
+    return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
   }
-  key = ((unsigned long long)vk << ibits) | (unsigned long long)(V - 1 - idx);
-  return bad;
 }
 
-static_assert(kThreads == kTopKMax, "the id sort gives one kept entry per thread");
+// The logit back from a key (value_key above the low `ib` id bits).
+template <int DT>
+SV_DEVINL float key_value(unsigned long long key, int ib) {
+  const uint32_t vk = (uint32_t)(key >> ib);
+  if constexpr (DT == 0) {
+    const uint32_t h = (vk & 0x8000u) ? (vk & 0x7fffu) : (~vk & 0xffffu);
+    return __uint_as_float(h << 16);
+  } else {
+    return __uint_as_float((vk & 0x80000000u) ? (vk & 0x7fffffffu) : ~vk);
+  }
+}
 
-struct TopKShared {
-  unsigned hist[kWarps][256];
-  unsigned wsum[kWarps];
-  unsigned long long prefix;
-  unsigned remaining, in_bucket, next_remaining, found_bin, bad, n_out;
-  int out_idx[kTopKMax];
-  float out_val[kTopKMax];
+template <int DT>
+SV_DEVINL bool nan_or_pos_inf(uint32_t bits) {
+  if constexpr (DT == 0)
+    return ((bits & 0x7fffu) > 0x7f80u) || bits == 0x7f80u;
+  else
+    return ((bits & 0x7fffffffu) > 0x7f800000u) || bits == 0x7f800000u;
+}
+
+// Words per thread per tile: 8 bf16 in 4 words, or 8 f32 in 8.
+template <int DT>
+struct SelWords {
+  static constexpr int n = DT == 0 ? 4 : 8;
 };
 
-// One CTA per row: the k largest keys by radix select over 8-bit digits from
-// the top (per-warp shared histograms of the digit among keys that match the
-// bits resolved so far), stopping as soon as the selected bucket is taken
-// whole; then one pass collects exactly k entries, sorted by id (bitonic).
 template <int DT>
-__global__ void __launch_bounds__(kThreads) topk_select_kernel(Params P) {
-  __shared__ TopKShared sh;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long row = blockIdx.x;
-  const unsigned char* rb = row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
-  const int V = P.V, k = P.top_k, ib = P.key_ibits;
-  const int top = ((DT == 0 ? 16 : 32) + ib + 7) / 8 * 8;
+SV_DEVINL uint32_t elem_bits(const uint32_t (&w)[SelWords<DT>::n], int j) {
+  if constexpr (DT == 0)
+    return (w[j >> 1] >> ((j & 1) * 16)) & 0xffffu;
+  else
+    return w[j];
+}
+
+// This thread's 8 elements of the tile starting at e0 (elements past V read
+// as -inf and are marked invalid by the returned count). VEC: 16-byte loads
+// (the row is 16-byte aligned and V * element size a multiple of 16).
+template <int DT, bool VEC>
+SV_DEVINL int load_sel_tile(const unsigned char* rb, long long e0, int V,
+                            uint32_t (&w)[SelWords<DT>::n]) {
+  const long long left = (long long)V - e0;
+  const int nv = left <= 0 ? 0 : (left >= 8 ? 8 : (int)left);
+  constexpr uint32_t kNegInf = DT == 0 ? 0xff80ff80u : 0xff800000u;
+  if constexpr (VEC) {
+    if constexpr (DT == 0) {
+      uint4 v = make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+      if (nv > 0) v = ld_global_nc_v4(rb + e0 * 2);
+      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else {
+      uint4 a = make_uint4(kNegInf, kNegInf, kNegInf, kNegInf), b = a;
+      if (nv > 0) a = ld_global_nc_v4(rb + e0 * 4);
+      if (nv > 4) b = ld_global_nc_v4(rb + (e0 + 4) * 4);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    }
+  } else {
+    if constexpr (DT == 0) {
+      const unsigned short* r = reinterpret_cast<const unsigned short*>(rb) + e0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = 2 * j < nv ? __ldg(r + 2 * j) : 0xff80u;
+        const uint32_t hi = 2 * j + 1 < nv ? __ldg(r + 2 * j + 1) : 0xff80u;
+        w[j] = lo | (hi << 16);
+      }
+    } else {
+      const uint32_t* r = reinterpret_cast<const uint32_t*>(rb) + e0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = j < nv ? __ldg(r + j) : kNegInf;
+    }
+  }
+  return nv;
+}
+
+SV_DEVINL double warp_max_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+SV_DEVINL double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Bit pattern (bf16: 16 bits) of the NaN-propagating max of one thread's 8
+// values of a tile.
+template <int DT>
+SV_DEVINL uint32_t sel_max_bits(const uint32_t (&w)[SelWords<DT>::n]) {
+  if constexpr (DT == 0) {
+    const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(w[0], w[1]), bf16x2_max_nan(w[2], w[3]));
+    return __float_as_uint(fmax_nan(bf16_lo(m2), bf16_hi(m2))) >> 16;
+  } else {
+    return __float_as_uint(
+        fmax_nan(fmax_nan(fmax_nan(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                          fmax_nan(__uint_as_float(w[2]), __uint_as_float(w[3]))),
+                 fmax_nan(fmax_nan(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                          fmax_nan(__uint_as_float(w[6]), __uint_as_float(w[7])))));
+  }
+}
+
+struct SelShared {
+  unsigned long long buf[kSelCap];    // candidate keys
+  unsigned long long keep[kTopKMax];  // the k largest, while the buffer is cut back
+  unsigned hist[256];
+  unsigned wsum[kSelWarps];
+  unsigned long long prefix, tau, kmax;
+  unsigned count, remaining, in_bucket, next_remaining, found_bin, n_keep, overflow, bad;
+  unsigned cnt[3];
+  double ssum;
+};
+// Within the default dynamic shared memory limit (no opt-in attribute needed).
+static_assert(sizeof(SelShared) <= 48 * 1024, "select kernel shared memory");
+
+// The k largest of n distinct keys key(0..n-1) into buf[0, k): a radix select
+// over 8-bit digits from the top key bit, stopping once the selected bucket
+// is taken whole, then one pass that keeps every key whose resolved digits
+// reach the selected prefix (exactly k of them). Sets count = k and tau = the
+// smallest kept key. `get(i, key)` returns false for NaN / +inf (sh.bad).
+template <typename GetKey>
+SV_DEVINL void sel_radix(SelShared& sh, long long n, int k, int top, GetKey get) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     sh.prefix = 0;
     sh.remaining = (unsigned)k;
-    sh.bad = 0;
-    sh.n_out = 0;
+    sh.n_keep = 0;
+    sh.tau = ~0ull;
   }
   int resolved = 0;
+  unsigned bad = 0;
   for (;;) {
     const int shift = top - resolved - 8;
-    for (int i = tid; i < kWarps * 256; i += kThreads) (&sh.hist[0][0])[i] = 0;
-    __syncthreads();  // also publishes the previous pass's prefix
+    sh.hist[tid] = 0;
+    __syncthreads();
     const bool all = shift + 8 >= 64;
     const unsigned long long pre = all ? 0ull : (sh.prefix >> (shift + 8));
-    unsigned bad = 0;
-    // Every lane runs the same trip count, so the warp is whole at the match.
-    for (long long base = 0; base < V; base += kThreads) {
+    for (long long base = 0; base < n; base += kSelThreads) {
       const long long i = base + tid;
       unsigned bin = 256u;
-      if (i < V) {
+      if (i < n) {
         unsigned long long key;
-        float v;
-        bad |= topk_key<DT>(rb, i, V, ib, key, v) ? 1u : 0u;
+        bad |= get(i, key) ? 0u : 1u;
         if (all || (key >> (shift + 8)) == pre) bin = (unsigned)((key >> shift) & 255u);
       }
-      // Lanes with the same bin add once (the group's leader adds its size).
       const unsigned grp = __match_any_sync(0xffffffffu, bin);
-      if (bin < 256u && lane == __ffs(grp) - 1) atomicAdd(&sh.hist[warp][bin], __popc(grp));
+      if (bin < 256u && lane == __ffs(grp) - 1) atomicAdd(&sh.hist[bin], __popc(grp));
     }
-    if (resolved == 0 && __any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(&sh.bad, 1u);
-    __syncthreads();
-    if (sh.bad) break;
-    // Thread t holds bin 255 - t (descending); an inclusive scan over t gives
-    // how many matching keys lie at or above each bin.
-    unsigned tot = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) tot += sh.hist[w][255 - tid];
+    if (__syncthreads_or(bad)) {
+      if (tid == 0) sh.bad = 1;
+      __syncthreads();
+      return;
+    }
+    // Thread t holds bin 255 - t; the inclusive scan over t counts the
+    // matching keys at or above each bin.
+    const unsigned tot = sh.hist[255 - tid];
     unsigned inc = tot;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1385,59 +1482,240 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(Params P) {
     __syncthreads();
     if (sh.in_bucket == sh.remaining || resolved >= top) break;
   }
-  if (sh.bad) {
+  const int lo = top - resolved;
+  const unsigned long long thr = sh.prefix >> lo;
+  for (long long i = tid; i < n; i += kSelThreads) {
+    unsigned long long key;
+    get(i, key);
+    if ((key >> lo) >= thr) {
+      const unsigned s = atomicAdd(&sh.n_keep, 1u);
+      if (s < (unsigned)kTopKMax) sh.keep[s] = key;
+    }
+  }
+  __syncthreads();
+  if (tid < k) {
+    const unsigned long long key = sh.keep[tid];
+    sh.buf[tid] = key;
+    atomicMin(&sh.tau, key);
+  }
+  if (tid == 0) sh.count = (unsigned)k;
+  __syncthreads();
+}
+
+// One CTA per row of the B (2K+1) rows: the row's k kept entries, as token
+// ids in ascending order with their fp64 probabilities softmax(l / T) over
+// the kept set, and the probability of the row's drafted token; the row's
+// flag is 0, kDevNonfinite (NaN or +inf anywhere in the row) or kDevEmptyRow
+// (every kept entry -inf).
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(Params P) {
+  extern __shared__ __align__(16) unsigned char sel_smem[];
+  SelShared& sh = *reinterpret_cast<SelShared*>(sel_smem);
+  constexpr int W = SelWords<DT>::n;
+  constexpr int U = DT == 0 ? 4 : 2;  // tiles per load group: 64 bytes per thread
+  constexpr int kGroup = U * kSelTile;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const long long row = blockIdx.x;
+  const unsigned char* rb = row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
+  const int V = P.V, k = P.top_k, ib = P.key_ibits;
+  const int top = ((DT == 0 ? 16 : 32) + ib + 7) / 8 * 8;
+  const unsigned long long idmask = (1ull << ib) - 1;
+  const unsigned cut_at = (unsigned)min(kSelTrigger, max(2 * k, k + 128));
+  if (tid == 0) {
+    sh.count = 0;
+    sh.overflow = 0;
+    sh.bad = 0;
+    sh.cnt[0] = sh.cnt[1] = sh.cnt[2] = 0;
+    sh.kmax = 0;
+    sh.ssum = 0.0;
+  }
+  unsigned long long tau = 0;
+  bool bad = false;
+  const long long ngroups = ((long long)V + kGroup - 1) / kGroup;
+  uint32_t cur[U][W], nxt[U][W];
+  int ncur[U], nnxt[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    ncur[u] = load_sel_tile<DT, VEC>(rb, (long long)u * kSelTile + tid * 8, V, cur[u]);
+  __syncthreads();
+  {
+    // A first threshold from the first load group: x = the k-th largest of
+    // its per-thread, per-tile maxima (value keys), found bit by bit with
+    // block-wide counts. At least k elements have a value key >= x, so no
+    // element below x is among the row's k largest.
+    uint32_t mk[U];
+    int has = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t mb = sel_max_bits<DT>(cur[u]);
+      const bool ok = ncur[u] > 0 && !nan_or_pos_inf<DT>(mb);
+      mk[u] = ok ? value_key<DT>(mb) : 0u;
+      has += ok ? 1 : 0;
+    }
+    auto block_count = [&](int c, int it) -> unsigned {
+      c = __reduce_add_sync(0xffffffffu, c);
+      if (lane == 0 && c) atomicAdd(&sh.cnt[it % 3], (unsigned)c);
+      if (tid == 0) sh.cnt[(it + 1) % 3] = 0;
+      __syncthreads();
+      return sh.cnt[it % 3];
+    };
+    if (block_count(has, 0) >= (unsigned)k) {
+      uint32_t x = 0;
+      int it = 1;
+      for (int bit = (DT == 0 ? 15 : 31); bit >= 0; --bit, ++it) {
+        const uint32_t y = x | (1u << bit);
+        int c = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) c += mk[u] >= y ? 1 : 0;
+        if (block_count(c, it) >= (unsigned)k) x = y;
+      }
+      tau = ((unsigned long long)x << ib) - 1;  // x > 0: k maxima are at least x
+    }
+  }
+  for (long long g = 0; g < ngroups; ++g) {
+    if (g + 1 < ngroups) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        nnxt[u] = load_sel_tile<DT, VEC>(rb, ((g + 1) * U + u) * kSelTile + tid * 8, V, nxt[u]);
+    }
+    // key > tau, compared as (value key, id bits) in 32-bit halves
+    const uint32_t tau_vk = (uint32_t)(tau >> ib), tau_lo = (uint32_t)(tau & idmask);
+    bool any = false;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long e0 = (g * U + u) * kSelTile + tid * 8;
+      // NaN-propagating max of the 8 values: one compare for the common case.
+      const uint32_t mbits = sel_max_bits<DT>(cur[u]);
+      const bool nf = nan_or_pos_inf<DT>(mbits);
+      bad |= nf;
+      unsigned cand = 0;
+      if (!nf && value_key<DT>(mbits) >= tau_vk) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t vk = value_key<DT>(elem_bits<DT>(cur[u], j));
+          const uint32_t lo = (uint32_t)(V - 1 - (int)(e0 + j));
+          if (j < ncur[u] && (vk > tau_vk || (vk == tau_vk && lo > tau_lo))) cand |= 1u << j;
+        }
+      }
+      const unsigned c = __popc(cand);
+      const unsigned lanes = __ballot_sync(0xffffffffu, c != 0);
+      if (lanes) {
+        any = true;
+        // Warp prefix of the counts (0..8) from the ballots of their bits.
+        const unsigned b0 = __ballot_sync(0xffffffffu, c & 1u), b1 = __ballot_sync(0xffffffffu, c & 2u),
+                       b2 = __ballot_sync(0xffffffffu, c & 4u), b3 = __ballot_sync(0xffffffffu, c & 8u);
+        const unsigned lt = (1u << lane) - 1u;
+        const unsigned excl = __popc(b0 & lt) + 2u * __popc(b1 & lt) + 4u * __popc(b2 & lt) +
+                              8u * __popc(b3 & lt);
+        const unsigned total = __popc(b0) + 2u * __popc(b1) + 4u * __popc(b2) + 8u * __popc(b3);
+        const int leader = __ffs(lanes) - 1;
+        unsigned base = 0;
+        if (lane == leader) {
+          base = atomicAdd(&sh.count, total);
+          if (base + total > (unsigned)kSelCap) sh.overflow = 1;
+        }
+        base = __shfl_sync(0xffffffffu, base, leader);
+        unsigned pos = base + excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if ((cand & (1u << j)) && pos < (unsigned)kSelCap)
+            sh.buf[pos++] = ((unsigned long long)value_key<DT>(elem_bits<DT>(cur[u], j)) << ib) |
+                            (unsigned long long)(V - 1 - (e0 + j));
+      }
+    }
+    // One barrier per load group: cut the buffer back once it holds more than
+    // cut_at keys (the threshold then rises), or leave for the exact path.
+    if (__syncthreads_or(any)) {
+      if (sh.overflow) break;
+      const unsigned n = sh.count;
+      if (n > cut_at) {
+        sel_radix(sh, n, k, top, [&](long long i, unsigned long long& key) {
+          key = sh.buf[i];
+          return true;
+        });
+        tau = sh.tau;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      ncur[u] = nnxt[u];
+#pragma unroll
+      for (int i = 0; i < W; ++i) cur[u][i] = nxt[u][i];
+    }
+  }
+  if (__syncthreads_or(bad)) {
     if (tid == 0) P.topk_flag[row] = kDevNonfinite;
     return;
   }
-  // Keep every key whose resolved high bits reach the selected prefix: the
-  // keys above it, and the whole selected bucket.
-  const int lo = top - resolved;
-  const unsigned long long thr = sh.prefix >> lo;
-  for (long long i = tid; i < V; i += kThreads) {
-    unsigned long long key;
-    float v;
-    (void)topk_key<DT>(rb, i, V, ib, key, v);
-    if ((key >> lo) >= thr) {
-      const unsigned slot = atomicAdd(&sh.n_out, 1u);
-      if (slot < (unsigned)kTopKMax) {
-        sh.out_idx[slot] = (int)i;
-        sh.out_val[slot] = v;
-      }
+  if (sh.overflow) {
+    // Exact selection over the row itself (NaN / +inf are checked again, as
+    // the streaming pass stopped early).
+    sel_radix(sh, V, k, top, [&](long long i, unsigned long long& key) {
+      uint32_t bits;
+      if constexpr (DT == 0)
+        bits = __ldg(reinterpret_cast<const unsigned short*>(rb) + i);
+      else
+        bits = __ldg(reinterpret_cast<const uint32_t*>(rb) + i);
+      key = ((unsigned long long)value_key<DT>(bits) << ib) | (unsigned long long)(V - 1 - i);
+      return !nan_or_pos_inf<DT>(bits);
+    });
+    if (sh.bad) {
+      if (tid == 0) P.topk_flag[row] = kDevNonfinite;
+      return;
     }
+  } else if (sh.count > (unsigned)k) {
+    sel_radix(sh, sh.count, k, top, [&](long long i, unsigned long long& key) {
+      key = sh.buf[i];
+      return true;
+    });
   }
-  __syncthreads();
-  if (tid >= (int)sh.n_out) sh.out_idx[tid] = INT_MAX;
-  __syncthreads();
-  for (int size = 2; size <= kTopKMax; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const int j = tid ^ stride;
-      if (j > tid) {
-        const bool asc = (tid & size) == 0;
-        if ((sh.out_idx[tid] > sh.out_idx[j]) == asc) {
-          const int ti = sh.out_idx[tid];
-          sh.out_idx[tid] = sh.out_idx[j];
-          sh.out_idx[j] = ti;
-          const float tv = sh.out_val[tid];
-          sh.out_val[tid] = sh.out_val[j];
-          sh.out_val[j] = tv;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  // buf[0, k): the kept keys. Softmax(l / T) over them in fp64: the max is
+  // the largest key's value (division by T > 0 keeps the order).
+  unsigned long long key = 0;
   if (tid < k) {
-    P.topk_idx[row * k + tid] = sh.out_idx[tid];
-    P.topk_val[row * k + tid] = sh.out_val[tid];
+    key = sh.buf[tid];
+    atomicMax(&sh.kmax, key);
   }
-  if (tid == 0) P.topk_flag[row] = sh.n_out == (unsigned)k ? 0u : kDevNonfinite;
+  __syncthreads();
+  const double m = (double)key_value<DT>(sh.kmax, ib) / P.temp_d;
+  if (m == -CUDART_INF) {
+    if (tid == 0) P.topk_flag[row] = kDevEmptyRow;
+    return;
+  }
+  const int id = V - 1 - (int)(key & idmask);
+  const double e = tid < k ? exp((double)key_value<DT>(key, ib) / P.temp_d - m) : 0.0;
+  const double ws = warp_sum_d(e);
+  if (lane == 0) atomicAdd(&sh.ssum, ws);
+  // Position in ascending id: the kept entries with a smaller id, i.e. a
+  // larger low (V-1-id) part.
+  int pos = 0;
+  if (tid < k) {
+    const unsigned long long mine = key & idmask;
+    for (int s = 0; s < k; ++s) pos += (sh.buf[s] & idmask) > mine ? 1 : 0;
+  }
+  __syncthreads();
+  const double q = e / sh.ssum;
+  const int r = (int)(row % P.rows_per_seq), K = P.K;
+  const long long b = row / P.rows_per_seq;
+  // The drafted token this row is tested at: x_t for target row t < K and for
+  // draft row K+1+t; the bonus row K has none.
+  const int x = r == K ? -1 : __ldg(P.tokens + b * K + (r < K ? r : r - K - 1));
+  if (tid < k) {
+    P.topk_idx[row * k + pos] = id;
+    P.topk_prob[row * k + pos] = q;
+    if (id == x) P.topk_at[row] = q;
+  }
+  if (tid == 0) P.topk_flag[row] = 0;
+  // A drafted token outside the kept set has probability 0 in this row.
+  if (!__syncthreads_or(tid < k && id == x) && tid == 0) P.topk_at[row] = 0.0;
 }
 
-// Position of `x` in a row's ascending kept ids, or -1.
-SV_DEVINL int topk_find(const int* ids, int k, int x) {
-  int lo = 0, hi = k - 1;
+// Position of `x` in ascending ids[0, n), or -1.
+SV_DEVINL int sorted_find(const int* ids, int n, int x) {
+  int lo = 0, hi = n - 1;
   while (lo <= hi) {
     const int mid = (lo + hi) >> 1;
-    const int v = __ldcg(ids + mid);
+    const int v = ids[mid];
     if (v == x) return mid;
     if (v < x)
       lo = mid + 1;
@@ -1447,141 +1725,117 @@ SV_DEVINL int topk_find(const int* ids, int k, int x) {
   return -1;
 }
 
-SV_DEVINL double warp_max_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
+constexpr int kTvThreads = kTopKMax;  // one kept entry per thread
 
-SV_DEVINL double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-struct TopKRows {
-  double m[2 * kMaxK + 1], s[2 * kMaxK + 1];  // max of l/T and sum of exp(l/T - m), per row
+struct TopKVerifyShared {
+  int pid[kTopKMax];
+  double pprob[kTopKMax];
+  double wsum[kTvThreads / 32];
+  unsigned bits;
+  int j, first, last;
 };
 
-// One warp per sequence: the verification of `verify` on the k-entry rows.
-__global__ void __launch_bounds__(128) topk_verify_kernel(Params P) {
-  __shared__ TopKRows rows_sh[4];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long b = (long long)blockIdx.x * 4 + warp;
-  if (b >= P.B) return;
-  TopKRows& rs = rows_sh[warp];
+// One CTA per sequence: the verification of `verify` on the kept entries.
+// The thresholds use the per-row probabilities of the drafted tokens; the
+// draw walks the k kept entries of the drawn row in ascending id, one per
+// thread, with the draft row's kept list in shared memory for the residual.
+__global__ void __launch_bounds__(kTvThreads) topk_verify_kernel(Params P) {
+  __shared__ TopKVerifyShared sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long b = blockIdx.x;
   const int K = P.K, R = P.rows_per_seq, k = P.top_k;
-  const double T = P.temp_d;
   const long long row0 = b * R;
+  if (tid == 0) {
+    sh.bits = 0;
+    sh.j = K;
+    sh.first = INT_MAX;
+    sh.last = -1;
+  }
+  __syncthreads();
   unsigned bits = 0;
-  for (int r = lane; r < R; r += 32) bits |= __ldcg(P.topk_flag + row0 + r);
-  for (int t = lane; t < K; t += 32) {
+  for (int r = tid; r < R; r += kTvThreads) bits |= __ldcg(P.topk_flag + row0 + r);
+  for (int t = tid; t < K; t += kTvThreads) {
     const int x = P.tokens[b * K + t];
     if (x < 0 || x >= P.V) bits |= kDevTokenRange;
   }
-  for (int t = lane; t < K + 2; t += 32) {
+  for (int t = tid; t < K + 2; t += kTvThreads) {
     const float u = P.uniforms[b * (K + 2) + t];
     if (!(u >= 0.0f && u <= 1.0f)) bits |= kDevUniformRange;
   }
-  // Per row: m = max l/T, S = sum exp(l/T - m) over the kept entries.
-  for (int r = 0; r < R; ++r) {
-    if (__ldcg(P.topk_flag + row0 + r)) continue;  // nonfinite row: its pairs are unset
-    const float* vals = P.topk_val + (row0 + r) * k;
-    double m = -CUDART_INF;
-    for (int e = lane; e < k; e += 32) m = fmax(m, (double)__ldcg(vals + e) / T);
-    m = warp_max_d(m);
-    double s = 0.0;
-    if (m != -CUDART_INF)
-      for (int e = lane; e < k; e += 32) s += exp((double)__ldcg(vals + e) / T - m);
-    s = warp_sum_d(s);
-    if (lane == 0) {
-      rs.m[r] = m;
-      rs.s[r] = s;
-    }
-    if (m == -CUDART_INF) bits |= kDevEmptyRow;
-  }
   bits = __reduce_or_sync(0xffffffffu, bits);
-  __syncwarp();
-  // q(x) or p(x) of token x in row r.
-  auto prob = [&](int r, int x) -> double {
-    const int pos = topk_find(P.topk_idx + (row0 + r) * k, k, x);
-    if (pos < 0) return 0.0;
-    return exp((double)__ldcg(P.topk_val + (row0 + r) * k + pos) / T - rs.m[r]) / rs.s[r];
-  };
-  int j = bits ? -1 : K;
-  if (!bits) {
-    for (int t0 = 0; t0 < K; t0 += 32) {
-      const int t = t0 + lane;
-      bool rej = false;
-      if (t < K) {
-        const int x = P.tokens[b * K + t];
-        const double q = prob(t, x), p = prob(K + 1 + t, x);
-        const double thr = p > 0.0 ? fmin(1.0, q / p) : (q > 0.0 ? 1.0 : 0.0);
-        rej = !((double)P.uniforms[b * (K + 2) + t] < thr);
-      }
-      const unsigned mask = __ballot_sync(0xffffffffu, rej);
-      if (mask) {
-        j = t0 + __ffs(mask) - 1;
-        break;
-      }
+  if (lane == 0 && bits) atomicOr(&sh.bits, bits);
+  __syncthreads();
+  bits = sh.bits;
+  if (bits) {
+    if (tid == 0) {
+      atomicOr(P.status, bits);
+      P.n_acc[b] = -1;
     }
+    for (int t = tid; t <= K; t += kTvThreads) P.out_tokens[b * (K + 1) + t] = -1;
+    return;
   }
-  int token = -1;
-  if (!bits) {
-    const bool resid = j < K;
-    const int qr = resid ? j : K;
-    const int* qids = P.topk_idx + (row0 + qr) * k;
-    const float* qvals = P.topk_val + (row0 + qr) * k;
-    const int per = (k + 31) / 32, e0 = min(k, lane * per), e1 = min(k, e0 + per);
-    auto weight = [&](int e, bool residual) -> double {
-      const double q = exp((double)__ldcg(qvals + e) / T - rs.m[qr]) / rs.s[qr];
-      if (!residual) return q;
-      const double p = prob(K + 1 + j, __ldcg(qids + e));
-      return fmax(0.0, q - p);
-    };
-    bool use_res = resid;
-    double lsum = 0.0;
-    for (int e = e0; e < e1; ++e) lsum += weight(e, use_res);
-    double total = warp_sum_d(lsum);
-    if (use_res && !(total > 0.0)) {  // zero residual: fall back to q (U5)
-      use_res = false;
-      lsum = 0.0;
-      for (int e = e0; e < e1; ++e) lsum += weight(e, false);
-      total = warp_sum_d(lsum);
-    }
-    const double target = (double)P.uniforms[b * (K + 2) + (resid ? K : K + 1)] * total;
-    // Exclusive prefix of the lanes' sums, then the first entry whose
-    // cumulative weight passes the target; else the last positive entry.
-    double inc = lsum;
+  // Acceptance tests: the first t whose u_t < min(1, q/p) fails.
+  for (int t = tid; t < K; t += kTvThreads) {
+    const double q = __ldcg(P.topk_at + row0 + t), p = __ldcg(P.topk_at + row0 + K + 1 + t);
+    const double thr = p > 0.0 ? fmin(1.0, q / p) : (q > 0.0 ? 1.0 : 0.0);
+    if (!((double)P.uniforms[b * (K + 2) + t] < thr)) atomicMin(&sh.j, t);
+  }
+  __syncthreads();
+  const int j = sh.j;
+  const bool resid = j < K;
+  const long long qrow = row0 + (resid ? j : K), prow = row0 + K + 1 + j;
+  if (resid && tid < k) {
+    sh.pid[tid] = __ldcg(P.topk_idx + prow * k + tid);
+    sh.pprob[tid] = __ldcg(P.topk_prob + prow * k + tid);
+  }
+  const int id = tid < k ? __ldcg(P.topk_idx + qrow * k + tid) : 0;
+  const double q = tid < k ? __ldcg(P.topk_prob + qrow * k + tid) : 0.0;
+  __syncthreads();
+  double w = q;
+  if (resid && tid < k) {
+    const int pos = sorted_find(sh.pid, k, id);
+    w = fmax(0.0, q - (pos >= 0 ? sh.pprob[pos] : 0.0));
+  }
+  // Inclusive scan of the weights in ascending id; the last entry is the total.
+  auto block_scan = [&](double v) -> double {
+    double inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const double y = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += y;
     }
-    double c = inc - lsum;
-    int first = INT_MAX, lastpos = -1;
-    for (int e = e0; e < e1; ++e) {
-      const double w = weight(e, use_res);
-      c += w;
-      if (w > 0.0) {
-        lastpos = e;
-        if (first == INT_MAX && c > target) first = e;
-      }
-    }
-    first = __reduce_min_sync(0xffffffffu, first);
-    lastpos = __reduce_max_sync(0xffffffffu, lastpos);
-    const int pick = first != INT_MAX ? first : lastpos;
-    token = pick >= 0 ? __ldcg(qids + pick) : -1;
+    if (lane == 31) sh.wsum[warp] = inc;
+    __syncthreads();
+    for (int w2 = 0; w2 < warp; ++w2) inc += sh.wsum[w2];
+    return inc;
+  };
+  double c = block_scan(w);
+  double total = 0.0;
+#pragma unroll
+  for (int w2 = 0; w2 < kTvThreads / 32; ++w2) total += sh.wsum[w2];
+  if (resid && !(total > 0.0)) {  // zero residual: fall back to q (U5)
+    __syncthreads();
+    w = q;
+    c = block_scan(w);
+    total = 0.0;
+#pragma unroll
+    for (int w2 = 0; w2 < kTvThreads / 32; ++w2) total += sh.wsum[w2];
   }
-  if (lane == 0) {
-    if (bits) atomicOr(P.status, bits);
+  const double target = (double)P.uniforms[b * (K + 2) + (resid ? K : K + 1)] * total;
+  if (tid < k && w > 0.0) {
+    atomicMax(&sh.last, tid);
+    if (c > target) atomicMin(&sh.first, tid);
+  }
+  __syncthreads();
+  const int pick = sh.first != INT_MAX ? sh.first : sh.last;
+  if (tid == pick) P.out_tokens[b * (K + 1) + j] = id;
+  if (tid == 0) {
     P.n_acc[b] = j;
+    if (pick < 0) P.out_tokens[b * (K + 1) + j] = -1;
   }
-  for (int t = lane; t <= K; t += 32) {
-    int o = -1;
-    if (j >= 0 && t < j) o = P.tokens[b * K + t];
-    if (j >= 0 && t == j) o = token;
-    P.out_tokens[b * (K + 1) + t] = o;
+  for (int t = tid; t <= K; t += kTvThreads) {
+    if (t < j) P.out_tokens[b * (K + 1) + t] = P.tokens[b * K + t];
+    if (t > j) P.out_tokens[b * (K + 1) + t] = -1;
   }
 }
 
@@ -1698,7 +1952,13 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
   return e;
 }
 
-cudaError_t launch_topk(const Params& P, cudaStream_t st) {
+template <int DT, bool VEC>
+cudaError_t launch_select(const Params& P, unsigned rows, size_t smem, cudaStream_t st) {
+  topk_select_kernel<DT, VEC><<<rows, kSelThreads, smem, st>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const Params& P, bool aligned, cudaStream_t st) {
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
@@ -1707,13 +1967,14 @@ cudaError_t launch_topk(const Params& P, cudaStream_t st) {
   e = cudaMemsetAsync(P.ctrl, 0, P.ctrl_bytes, st);
   if (e != cudaSuccess) return e;
   const unsigned rows = (unsigned)((long long)P.B * P.rows_per_seq);
+  const size_t smem = sizeof(SelShared);
   if (P.dtype == 0)
-    topk_select_kernel<0><<<rows, kThreads, 0, st>>>(P);
+    e = aligned ? launch_select<0, true>(P, rows, smem, st) : launch_select<0, false>(P, rows, smem, st);
   else
-    topk_select_kernel<1><<<rows, kThreads, 0, st>>>(P);
-  e = cudaGetLastError();
+    e = aligned ? launch_select<1, true>(P, rows, smem, st) : launch_select<1, false>(P, rows, smem, st);
   if (e != cudaSuccess) return e;
-  topk_verify_kernel<<<(unsigned)((P.B + 3) / 4), 128, 0, st>>>(P);
+  if (e != cudaSuccess) return e;
+  topk_verify_kernel<<<(unsigned)P.B, kTvThreads, 0, st>>>(P);
   return cudaGetLastError();
 }
 

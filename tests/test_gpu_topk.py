@@ -126,6 +126,28 @@ def test_failures_and_masked_rows():
     parity(inp, 20)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_adversarial_orders_and_late_nan(dt):
+    """Ascending rows make every element a new candidate (the buffer overflows
+    and the row is selected exactly from memory); descending rows are decided
+    by the first threshold; a NaN far into an ascending row must still fail
+    its sequence."""
+    B, K, V, k = 6, 2, 30011, 64
+    inp = make_topk_inputs(_w(B, K, V, dt, seed=21), k)
+    g = torch.Generator().manual_seed(5)
+    base = torch.randn(V, generator=g).sort().values * 4
+    for b in range(4):
+        inp["target"][b] = base.to(inp["target"].dtype)
+        inp["draft"][b] = (base + 0.3 * torch.randn(V, generator=g)).sort().values.to(inp["draft"].dtype)
+    inp["target"][1] = inp["target"][1].flip(-1)
+    inp["draft"][1] = inp["draft"][1].flip(-1)
+    inp["target"][2, 1, V - 40] = float("nan")
+    # drafts near the top of the (ascending) draft rows
+    inp["tokens"][:4] = torch.randint(V - 3 * k, V, (4, K), generator=g).to(torch.int32)
+    inp["tokens"][1] = torch.randint(0, 2 * k, (K,), generator=g).to(torch.int32)
+    parity(inp, k)
+
+
 def test_uniform_extremes_and_zero_residual():
     inp = make_topk_inputs(_w(6, 3, 400, "f32", seed=13), 16)
     u = inp["uniforms"]
