@@ -1287,7 +1287,6 @@ constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelTile = kSelThreads * 8;  // elements per tile: 8 consecutive per thread
 constexpr int kSelCap = 5120;              // candidate buffer entries
-constexpr int kSelTrigger = 1024;          // the buffer is cut back above at most this many
 static_assert(kTopKMax == kSelThreads, "the final stage gives one kept entry per thread");
 
 // Order-preserving map of a bf16 (16-bit) or f32 bit pattern to an unsigned
@@ -1376,6 +1375,32 @@ SV_DEVINL int load_sel_tile(const unsigned char* rb, long long e0, int V,
   return nv;
 }
 
+// This thread's 8 elements of a tile that lies wholly inside the row.
+template <int DT, bool VEC>
+SV_DEVINL void load_full_tile(const unsigned char* rb, unsigned e0, uint32_t (&w)[SelWords<DT>::n]) {
+  if constexpr (VEC) {
+    if constexpr (DT == 0) {
+      const uint4 v = ld_global_nc_v4(rb + (size_t)e0 * 2);
+      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else {
+      const uint4 a = ld_global_nc_v4(rb + (size_t)e0 * 4);
+      const uint4 b = ld_global_nc_v4(rb + (size_t)e0 * 4 + 16);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    }
+  } else {
+    if constexpr (DT == 0) {
+      const unsigned short* r = reinterpret_cast<const unsigned short*>(rb) + e0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = (uint32_t)__ldg(r + 2 * j) | ((uint32_t)__ldg(r + 2 * j + 1) << 16);
+    } else {
+      const uint32_t* r = reinterpret_cast<const uint32_t*>(rb) + e0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = __ldg(r + j);
+    }
+  }
+}
+
 SV_DEVINL double warp_max_d(double v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -1417,14 +1442,17 @@ struct SelShared {
 // Within the default dynamic shared memory limit (no opt-in attribute needed).
 static_assert(sizeof(SelShared) <= 48 * 1024, "select kernel shared memory");
 
-// The k largest of n distinct keys key(0..n-1) into buf[0, k): a radix select
-// over 8-bit digits from the top key bit, stopping once the selected bucket
-// is taken whole, then one pass that keeps every key whose resolved digits
-// reach the selected prefix (exactly k of them). Sets count = k and tau = the
-// smallest kept key. `get(i, key)` returns false for NaN / +inf (sh.bad).
+// The k largest of n distinct keys key(0..n-1) of `bits` bits into buf[0, k):
+// a radix select over 8-bit digits from the top key bit (the key is padded
+// with zeros at the bottom to a whole number of digits), stopping once the
+// selected bucket is taken whole, then one pass that keeps every key whose
+// resolved digits reach the selected prefix (exactly k of them). Sets count
+// = k and tau = the smallest kept key. `get(i, key)` returns false for NaN /
+// +inf (sets sh.bad and returns early).
 template <typename GetKey>
-SV_DEVINL void sel_radix(SelShared& sh, long long n, int k, int top, GetKey get) {
+SV_DEVINL void sel_radix(SelShared& sh, long long n, int k, int bits, GetKey get) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int pad = (8 - bits % 8) % 8, top = bits + pad;
   if (tid == 0) {
     sh.prefix = 0;
     sh.remaining = (unsigned)k;
@@ -1445,6 +1473,7 @@ SV_DEVINL void sel_radix(SelShared& sh, long long n, int k, int top, GetKey get)
       if (i < n) {
         unsigned long long key;
         bad |= get(i, key) ? 0u : 1u;
+        key <<= pad;
         if (all || (key >> (shift + 8)) == pre) bin = (unsigned)((key >> shift) & 255u);
       }
       const unsigned grp = __match_any_sync(0xffffffffu, bin);
@@ -1487,7 +1516,7 @@ SV_DEVINL void sel_radix(SelShared& sh, long long n, int k, int top, GetKey get)
   for (long long i = tid; i < n; i += kSelThreads) {
     unsigned long long key;
     get(i, key);
-    if ((key >> lo) >= thr) {
+    if (((key << pad) >> lo) >= thr) {
       const unsigned s = atomicAdd(&sh.n_keep, 1u);
       if (s < (unsigned)kTopKMax) sh.keep[s] = key;
     }
@@ -1502,145 +1531,189 @@ SV_DEVINL void sel_radix(SelShared& sh, long long n, int k, int top, GetKey get)
   __syncthreads();
 }
 
+// The largest 16-bit x such that at least k of the threads' values m[0..3]
+// (those with ok set) are >= x, by a radix select over two 8-bit digits with
+// block-wide histograms; 0 when fewer than k values are given.
+SV_DEVINL uint32_t sel_kth16(SelShared& sh, const uint32_t (&m)[4], const bool (&ok)[4], int k) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0;
+  unsigned rem = (unsigned)k;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 8 : 0;
+    sh.hist[tid] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool in = ok[u] && (pass == 0 || (m[u] >> 8) == prefix);
+      const unsigned bin = in ? ((m[u] >> shift) & 255u) : 256u;
+      const unsigned grp = __match_any_sync(0xffffffffu, bin);
+      if (bin < 256u && lane == __ffs(grp) - 1) atomicAdd(&sh.hist[bin], __popc(grp));
+    }
+    __syncthreads();
+    const unsigned tot = sh.hist[255 - tid];
+    unsigned inc = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 31) sh.wsum[warp] = inc;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) inc += sh.wsum[w];
+    if (pass == 0 && tid == kSelThreads - 1) sh.found_bin = inc;  // all the values
+    if (inc >= rem && inc - tot < rem) {
+      sh.in_bucket = 255u - (unsigned)tid;
+      sh.next_remaining = rem - (inc - tot);
+    }
+    __syncthreads();
+    if (pass == 0 && sh.found_bin < (unsigned)k) return 0;
+    prefix = pass == 0 ? sh.in_bucket : ((prefix << 8) | sh.in_bucket);
+    rem = sh.next_remaining;
+    __syncthreads();
+  }
+  return prefix;
+}
+
+template <int DT>
+struct TileWords {
+  uint32_t v[SelWords<DT>::n];
+};
+
+// The rare path of the collecting pass, for a thread whose tile maximum
+// reached the threshold value (or is NaN): appends its elements (the first
+// nv of 8, from element e0) whose key beats thr to the candidate buffer, and
+// returns whether one of them is NaN or +inf. Out of line, so that the
+// streaming loop stays small.
+template <int DT>
+__device__ __noinline__ bool sel_slow(SelShared& sh, TileWords<DT> t, int nv, unsigned e0, int V,
+                                      int ib, unsigned long long thr) {
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= nv) break;
+    const uint32_t bits = elem_bits<DT>(t.v, j);
+    if (nan_or_pos_inf<DT>(bits)) {
+      bad = true;
+      continue;
+    }
+    const unsigned long long key =
+        ((unsigned long long)value_key<DT>(bits) << ib) | (unsigned long long)(V - 1 - (int)(e0 + j));
+    if (key > thr) {
+      const unsigned pos = atomicAdd(&sh.count, 1u);
+      if (pos < (unsigned)kSelCap)
+        sh.buf[pos] = key;
+      else
+        sh.overflow = 1;
+    }
+  }
+  return bad;
+}
+
+// Float value (NaN-propagating max) of one thread's 8 values of a tile.
+template <int DT>
+SV_DEVINL float sel_max_f(const uint32_t (&w)[SelWords<DT>::n]) {
+  const uint32_t mb = sel_max_bits<DT>(w);
+  return __uint_as_float(DT == 0 ? mb << 16 : mb);
+}
+
 // One CTA per row of the B (2K+1) rows: the row's k kept entries, as token
 // ids in ascending order with their fp64 probabilities softmax(l / T) over
 // the kept set, and the probability of the row's drafted token; the row's
 // flag is 0, kDevNonfinite (NaN or +inf anywhere in the row) or kDevEmptyRow
 // (every kept entry -inf).
+//
+// A first pass over a leading sample of the row (at least kSelSampleTiles
+// tiles, at least an eighth of the row) takes every thread's maxima over its
+// elements of it (4 per thread), and x, the k-th largest of them (to 16 bits
+// of the value key), bounds the candidates from below: at least k elements
+// are at least x, so none below x is among the row's k largest. The second
+// pass reads the whole row (the sample again from L2) and appends the
+// elements at or above x to the buffer; about k times the row/sample ratio
+// of them for rows in random order. Neither pass has a block-wide barrier,
+// so every warp keeps its loads in flight.
+constexpr int kSelSampleTiles = 16;
+
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(Params P) {
   extern __shared__ __align__(16) unsigned char sel_smem[];
   SelShared& sh = *reinterpret_cast<SelShared*>(sel_smem);
   constexpr int W = SelWords<DT>::n;
-  constexpr int U = DT == 0 ? 4 : 2;  // tiles per load group: 64 bytes per thread
-  constexpr int kGroup = U * kSelTile;
+  constexpr int NB = DT == 0 ? 16 : 32;  // value key bits
+  constexpr int S = DT == 0 ? 4 : 2;      // tiles loaded per step: 64 bytes per thread
   const int tid = threadIdx.x, lane = tid & 31;
   const long long row = blockIdx.x;
   const unsigned char* rb = row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
   const int V = P.V, k = P.top_k, ib = P.key_ibits;
-  const int top = ((DT == 0 ? 16 : 32) + ib + 7) / 8 * 8;
+  const int top = NB + ib;  // key bits
   const unsigned long long idmask = (1ull << ib) - 1;
-  const unsigned cut_at = (unsigned)min(kSelTrigger, max(2 * k, k + 128));
   if (tid == 0) {
     sh.count = 0;
     sh.overflow = 0;
     sh.bad = 0;
-    sh.cnt[0] = sh.cnt[1] = sh.cnt[2] = 0;
     sh.kmax = 0;
     sh.ssum = 0.0;
   }
-  unsigned long long tau = 0;
   bool bad = false;
-  const long long ngroups = ((long long)V + kGroup - 1) / kGroup;
-  uint32_t cur[U][W], nxt[U][W];
-  int ncur[U], nnxt[U];
+  const unsigned ntiles = (unsigned)(((long long)V + kSelTile - 1) / kSelTile);
+  const unsigned nfull = (unsigned)V / kSelTile;  // tiles wholly inside the row
+  const unsigned nsample = min(ntiles, max((unsigned)kSelSampleTiles, (ntiles + 7) / 8));
+  // Pass 1 over the sample: NaN-propagating maxima in 4 slots (tile mod 4).
+  float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+  bool ok[4] = {false, false, false, false};
+  const unsigned sfull = min(nsample, nfull) / 4 * 4;
+  for (unsigned t = 0; t < sfull; t += 4) {
+    uint32_t w[4][W];
 #pragma unroll
-  for (int u = 0; u < U; ++u)
-    ncur[u] = load_sel_tile<DT, VEC>(rb, (long long)u * kSelTile + tid * 8, V, cur[u]);
-  __syncthreads();
-  {
-    // A first threshold from the first load group: x = the k-th largest of
-    // its per-thread, per-tile maxima (value keys), found bit by bit with
-    // block-wide counts. At least k elements have a value key >= x, so no
-    // element below x is among the row's k largest.
-    uint32_t mk[U];
-    int has = 0;
+    for (int u = 0; u < 4; ++u) load_full_tile<DT, VEC>(rb, (t + u) * kSelTile + tid * 8, w[u]);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint32_t mb = sel_max_bits<DT>(cur[u]);
-      const bool ok = ncur[u] > 0 && !nan_or_pos_inf<DT>(mb);
-      mk[u] = ok ? value_key<DT>(mb) : 0u;
-      has += ok ? 1 : 0;
-    }
-    auto block_count = [&](int c, int it) -> unsigned {
-      c = __reduce_add_sync(0xffffffffu, c);
-      if (lane == 0 && c) atomicAdd(&sh.cnt[it % 3], (unsigned)c);
-      if (tid == 0) sh.cnt[(it + 1) % 3] = 0;
-      __syncthreads();
-      return sh.cnt[it % 3];
-    };
-    if (block_count(has, 0) >= (unsigned)k) {
-      uint32_t x = 0;
-      int it = 1;
-      for (int bit = (DT == 0 ? 15 : 31); bit >= 0; --bit, ++it) {
-        const uint32_t y = x | (1u << bit);
-        int c = 0;
+    for (int u = 0; u < 4; ++u) mx[u] = fmax_nan(mx[u], sel_max_f<DT>(w[u]));
+  }
+  if (sfull > 0) ok[0] = ok[1] = ok[2] = ok[3] = true;
+  for (unsigned t = sfull; t < nsample; ++t) {
+    uint32_t w[W];
+    const int nv = load_sel_tile<DT, VEC>(rb, (long long)t * kSelTile + tid * 8, V, w);
+    mx[t % 4] = fmax_nan(mx[t % 4], sel_max_f<DT>(w));
+    ok[t % 4] |= nv > 0;
+  }
+  uint32_t m16[4];
 #pragma unroll
-        for (int u = 0; u < U; ++u) c += mk[u] >= y ? 1 : 0;
-        if (block_count(c, it) >= (unsigned)k) x = y;
+  for (int u = 0; u < 4; ++u) {
+    const uint32_t mb = DT == 0 ? (__float_as_uint(mx[u]) >> 16) : __float_as_uint(mx[u]);
+    ok[u] = ok[u] && !nan_or_pos_inf<DT>(mb);  // a failing row is caught by pass 2
+    m16[u] = value_key<DT>(mb) >> (NB - 16);
+  }
+  __syncthreads();  // the shared counters above
+  const uint32_t x16 = sel_kth16(sh, m16, ok, k);
+  // Candidates: value key >= xv = x16 << (NB - 16), i.e. key > thr; a tile is
+  // looked at element by element only when its maximum reaches xv's value.
+  const uint32_t xv = x16 << (NB - 16);
+  const unsigned long long thr = x16 ? ((unsigned long long)xv << ib) - 1 : 0ull;
+  const float tvf = x16 ? key_value<DT>((unsigned long long)xv, 0) : -CUDART_INF_F;
+  // Pass 2 over the row, appending the candidates.
+  const unsigned rfull = nfull / S * S;
+  for (unsigned t = 0; t < rfull; t += S) {
+    uint32_t w[S][W];
+#pragma unroll
+    for (int u = 0; u < S; ++u) load_full_tile<DT, VEC>(rb, (t + u) * kSelTile + tid * 8, w[u]);
+#pragma unroll
+    for (int u = 0; u < S; ++u) {
+      if (!(sel_max_f<DT>(w[u]) < tvf)) {  // at or above the threshold value, or NaN
+        TileWords<DT> tw;
+#pragma unroll
+        for (int i = 0; i < W; ++i) tw.v[i] = w[u][i];
+        bad |= sel_slow<DT>(sh, tw, 8, (t + u) * kSelTile + tid * 8, V, ib, thr);
       }
-      tau = ((unsigned long long)x << ib) - 1;  // x > 0: k maxima are at least x
     }
   }
-  for (long long g = 0; g < ngroups; ++g) {
-    if (g + 1 < ngroups) {
+  for (unsigned t = rfull; t < ntiles; ++t) {
+    uint32_t w[W];
+    const unsigned e0 = t * kSelTile + tid * 8;
+    const int nv = load_sel_tile<DT, VEC>(rb, (long long)e0, V, w);
+    if (nv > 0 && !(sel_max_f<DT>(w) < tvf)) {
+      TileWords<DT> tw;
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        nnxt[u] = load_sel_tile<DT, VEC>(rb, ((g + 1) * U + u) * kSelTile + tid * 8, V, nxt[u]);
-    }
-    // key > tau, compared as (value key, id bits) in 32-bit halves
-    const uint32_t tau_vk = (uint32_t)(tau >> ib), tau_lo = (uint32_t)(tau & idmask);
-    bool any = false;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long e0 = (g * U + u) * kSelTile + tid * 8;
-      // NaN-propagating max of the 8 values: one compare for the common case.
-      const uint32_t mbits = sel_max_bits<DT>(cur[u]);
-      const bool nf = nan_or_pos_inf<DT>(mbits);
-      bad |= nf;
-      unsigned cand = 0;
-      if (!nf && value_key<DT>(mbits) >= tau_vk) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t vk = value_key<DT>(elem_bits<DT>(cur[u], j));
-          const uint32_t lo = (uint32_t)(V - 1 - (int)(e0 + j));
-          if (j < ncur[u] && (vk > tau_vk || (vk == tau_vk && lo > tau_lo))) cand |= 1u << j;
-        }
-      }
-      const unsigned c = __popc(cand);
-      const unsigned lanes = __ballot_sync(0xffffffffu, c != 0);
-      if (lanes) {
-        any = true;
-        // Warp prefix of the counts (0..8) from the ballots of their bits.
-        const unsigned b0 = __ballot_sync(0xffffffffu, c & 1u), b1 = __ballot_sync(0xffffffffu, c & 2u),
-                       b2 = __ballot_sync(0xffffffffu, c & 4u), b3 = __ballot_sync(0xffffffffu, c & 8u);
-        const unsigned lt = (1u << lane) - 1u;
-        const unsigned excl = __popc(b0 & lt) + 2u * __popc(b1 & lt) + 4u * __popc(b2 & lt) +
-                              8u * __popc(b3 & lt);
-        const unsigned total = __popc(b0) + 2u * __popc(b1) + 4u * __popc(b2) + 8u * __popc(b3);
-        const int leader = __ffs(lanes) - 1;
-        unsigned base = 0;
-        if (lane == leader) {
-          base = atomicAdd(&sh.count, total);
-          if (base + total > (unsigned)kSelCap) sh.overflow = 1;
-        }
-        base = __shfl_sync(0xffffffffu, base, leader);
-        unsigned pos = base + excl;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if ((cand & (1u << j)) && pos < (unsigned)kSelCap)
-            sh.buf[pos++] = ((unsigned long long)value_key<DT>(elem_bits<DT>(cur[u], j)) << ib) |
-                            (unsigned long long)(V - 1 - (e0 + j));
-      }
-    }
-    // One barrier per load group: cut the buffer back once it holds more than
-    // cut_at keys (the threshold then rises), or leave for the exact path.
-    if (__syncthreads_or(any)) {
-      if (sh.overflow) break;
-      const unsigned n = sh.count;
-      if (n > cut_at) {
-        sel_radix(sh, n, k, top, [&](long long i, unsigned long long& key) {
-          key = sh.buf[i];
-          return true;
-        });
-        tau = sh.tau;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      ncur[u] = nnxt[u];
-#pragma unroll
-      for (int i = 0; i < W; ++i) cur[u][i] = nxt[u][i];
+      for (int i = 0; i < W; ++i) tw.v[i] = w[i];
+      bad |= sel_slow<DT>(sh, tw, nv, e0, V, ib, thr);
     }
   }
   if (__syncthreads_or(bad)) {
