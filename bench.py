@@ -35,7 +35,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import get_workload, make_inputs  # noqa: E402
+from synthetic import get_workload, make_inputs, make_topk_inputs  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "verified draft positions/sec (and achieved HBM GB/s, % of GB300 peak)"
@@ -51,10 +51,12 @@ def parse():
     ap.add_argument("--config", default="c2", help="c1..c4 or sweep-k{K}-n{noise}")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["verify", "draft_sample", "greedy"], default="verify",
+    ap.add_argument("--op", choices=["verify", "draft_sample", "greedy", "topk"], default="verify",
                     help="verify: the verification step (default); draft_sample: the draft-side "
                          "sampler over every draft row of the workload; greedy: greedy-mode "
-                         "verification of the workload's target rows")
+                         "verification of the workload's target rows; topk: verification on "
+                         "top-k filtered distributions (--top-k)")
+    ap.add_argument("--top-k", type=int, default=50)
     return ap.parse_args()
 
 
@@ -728,6 +730,171 @@ def run_greedy(args, w, world, rank, local):
     }), flush=True)
 
 
+def run_topk_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    import oracle
+
+    kk = args.top_k
+    steps = max(1, args.steps)
+    sets = [make_topk_inputs(w, kk, step=70_000 + i) for i in range(min(2, steps))]
+    wide = [tuple(s[x].to(torch.float64).numpy() for x in ("target", "draft"))
+            + (s["tokens"].numpy(), s["uniforms"].to(torch.float64).numpy()) for s in sets]
+    for i in range(args.warmup):
+        oracle.verify_topk(*wide[i % len(wide)], w.temperature, kk)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        oracle.verify_topk(*wide[i % len(wide)], w.temperature, kk)
+    dt = time.perf_counter() - t0
+    value = steps * w.B * w.K / dt
+    print(json.dumps({
+        "impl": "reference", "op": "topk", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}-top{kk}", "detail": w.describe()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{steps} top-{kk} steps of {w.name} (fp64 numpy oracle, 1 thread)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_topk(args, w, world, rank, local):
+    """A step is one spec_verify_topk call over the B sequences of one step of
+    the workload: the row selection kernel over all 2K+1 rows, then the
+    verification kernel on the kept entries."""
+    import speculative_sampling_verification_gb300 as sv
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sv.load_library(build=True)
+    kk = args.top_k
+    B, K, V, es = w.B, w.K, w.V, w.elem_bytes
+    dt_code = sv.SV_BF16 if w.dtype == "bf16" else sv.SV_F32
+    set_bytes = B * (2 * K + 1) * V * es
+    n_sets = max(2, min(64, -(-2 * L2_BYTES // set_bytes) + 1))
+    names = ("target", "draft", "tokens", "uniforms")
+    host = []
+    for i in range(n_sets):
+        inp = make_topk_inputs(w, kk, step=80_000 + 1000 * rank + i)
+        host.append(tuple(inp[x].pin_memory() for x in names))
+    sets = [tuple(t.to(dev) for t in h) for h in host]
+    outs = [(torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+             torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
+    ws = torch.empty(max(256, sv.sv_topk_workspace_size(B, K, V, dt_code, kk)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def call(i, tensors=None, o=None):
+        t = tensors or sets[i % n_sets]
+        o = o or outs[i % n_sets]
+        rc = sv.spec_verify_topk(*t, w.temperature, kk, o[0], o[1], ws, stream=stream)
+        if rc != 0:
+            raise RuntimeError(f"spec_verify_topk failed: {sv.sv_status_string(rc)}")
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        call(0)
+    torch.cuda.synchronize()
+    steps, warmup = args.steps, max(3, args.warmup)
+    g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=stream):
+        for i in range(warmup):
+            call(i)
+    with torch.cuda.graph(g_timed, stream=stream):
+        for i in range(steps):
+            call(warmup + i)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    g_warm.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        g_timed.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = reduce_max(start.elapsed_time(end), world, dev)
+    time.sleep(0.3)
+    clocks.stop()
+    status = sv.sv_read_device_status(ws, stream)
+    nacc_all = torch.stack([n for _, n in outs]).cpu().numpy()
+    if status != 0 or (nacc_all < 0).any() or (nacc_all > K).any():
+        raise RuntimeError(f"bad device status {status} or n_accepted out of range")
+
+    e2e_steps = args.e2e_steps or min(steps, 200)
+    dev_in = tuple(torch.empty_like(t) for t in sets[0])
+    h_out = torch.empty(B, K + 1, dtype=torch.int32).pin_memory()
+    h_n = torch.empty(B, dtype=torch.int32).pin_memory()
+
+    def host_call(i):
+        h = host[i % n_sets]
+        with torch.cuda.stream(stream):
+            for d, x in zip(dev_in, h):
+                d.copy_(x, non_blocking=True)
+            call(0, dev_in, outs[0])
+            h_out.copy_(outs[0][0], non_blocking=True)
+            h_n.copy_(outs[0][1], non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        host_call(i)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        host_call(i)
+    e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
+    if rank != 0:
+        return
+    per_step_s = elapsed_ms / 1e3 / steps
+    peak, peak_kind = load_peaks()
+    achieved = set_bytes / per_step_s / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        wide = [tuple(x.to(torch.float64).numpy() for x in h[:2]) + (h[2].to(torch.int64).numpy(),
+                h[3].to(torch.float64).numpy()) for h in host[:2]]
+        t0, n = time.perf_counter(), 0
+        while time.perf_counter() - t0 < 12.0 and n < 5000:
+            oracle.verify_topk(*wide[n % len(wide)], w.temperature, kk)
+            n += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": n * B * K / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} top-{kk} steps of {w.name} in {dt:.1f} s (fp64 numpy oracle, 1 thread)"}
+    in_bytes = sum(t.numel() * t.element_size() for t in host[0])
+    print(json.dumps({
+        "op": "topk", "metric": METRIC, "value": aggregate(B * K, world, per_step_s),
+        "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": per_step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}-top{kk}", "detail": w.describe(), "top_k": kk,
+                   "l2": f"inputs rotate over {n_sets} resident sets of {set_bytes / 1e6:.1f} MB",
+                   "timing": "K calls in one CUDA graph, CUDA events on the launching stream"},
+        "roofline": {"bound": "hbm", "kernel": "topk_select_kernel + topk_verify_kernel (call time)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                     "bytes_per_launch": set_bytes, "ms_per_launch": per_step_s * 1e3,
+                     "bytes_basis": "B(2K+1) rows of V elements, once (both kernels' time)"},
+        "e2e": {"value": aggregate(B * K * e2e_steps, world, e2e_s), "unit": UNIT,
+                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 * B * (K + 2),
+                "steps": e2e_steps},
+        "gpu_launches": steps * 2,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "cpu_baseline": cpu,
+    }), flush=True)
+
+
 def main():
     args = parse()
     w = get_workload(args.config)
@@ -743,6 +910,11 @@ def main():
                 run_greedy_reference(args, w, world, rank)
             else:
                 run_greedy(args, w, world, rank, local)
+        elif args.op == "topk":
+            if args.impl == "reference":
+                run_topk_reference(args, w, world, rank)
+            else:
+                run_topk(args, w, world, rank, local)
         elif args.impl == "reference":
             run_reference(args, w, world, rank)
         else:

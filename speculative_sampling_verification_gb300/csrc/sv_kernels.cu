@@ -1634,7 +1634,7 @@ SV_DEVINL float sel_max_f(const uint32_t (&w)[SelWords<DT>::n]) {
 constexpr int kSelSampleTiles = 16;
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(Params P) {
+__global__ void __launch_bounds__(kSelThreads, DT == 0 ? 5 : 4) topk_select_kernel(Params P) {
   extern __shared__ __align__(16) unsigned char sel_smem[];
   SelShared& sh = *reinterpret_cast<SelShared*>(sel_smem);
   constexpr int W = SelWords<DT>::n;
