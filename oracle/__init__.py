@@ -8,6 +8,7 @@ from .spec_sampling import (  # noqa: F401
     OracleResult,
     SampleResult,
     GreedyResult,
+    NucleusResult,
     STATUS_EMPTY_ROW,
     STATUS_NONFINITE,
     STATUS_OK,
@@ -23,5 +24,7 @@ from .spec_sampling import (  # noqa: F401
     verify_greedy,
     verify_topk,
     topk_mask,
+    topp_mask,
+    verify_topp,
     verify_inputs,
 )

@@ -359,6 +359,65 @@ def verify_topk(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
                   temperature)
 
 
+@dataclass
+class NucleusResult:
+    result: OracleResult         # the verification on the filtered rows
+    kept: np.ndarray             # [B, 2K+1] entries kept per row (target rows 0..K, then draft rows)
+    cut_margin: np.ndarray       # [B, 2K+1] distance of top_p from the cumulative sums at the cut
+
+
+def topp_mask(logits: np.ndarray, temperature: float, top_p: float):
+    """The nucleus (top-p) decoding transform on logits (U17): per row,
+    q = softmax(l / T) in fp64 (`temperature_softmax`); entries are ordered
+    by logit, larger first, ties to the smaller token id (-0.0 equals +0.0);
+    the shortest prefix of that order whose cumulative q, summed in that
+    order, reaches top_p is kept, the rest become -inf. top_p >= 1 keeps the
+    row; if rounding leaves the total below top_p, every entry with q > 0 is
+    kept. Rows that fail (NaN, +inf, all -inf; U12) are returned unchanged.
+
+    Returns (masked logits, kept count per row, cut margin per row): the
+    margin is min(C_n - top_p, top_p - C_{n-1}) for the kept count n and the
+    cumulative sums C, inf when the row is not cut."""
+    logits = np.asarray(logits, dtype=np.float64)
+    shape, V = logits.shape, logits.shape[-1]
+    flat = logits.reshape(-1, V)
+    out = flat.copy()
+    kept = np.full(flat.shape[0], V, dtype=np.int64)
+    margin = np.full(flat.shape[0], np.inf)
+    if top_p >= 1.0:
+        return out.reshape(shape), kept.reshape(shape[:-1]), margin.reshape(shape[:-1])
+    q, _, st = temperature_softmax(flat, temperature)
+    for r in range(flat.shape[0]):
+        if st[r] != 0:
+            continue
+        order = np.argsort(-(flat[r] + 0.0), kind="stable")
+        c = np.cumsum(q[r, order])
+        reach = np.nonzero(c >= top_p)[0]
+        n = int(reach[0]) + 1 if len(reach) else int((q[r] > 0).sum())
+        kept[r] = n
+        margin[r] = min(c[n - 1] - top_p if len(reach) else np.inf,
+                        top_p - c[n - 2] if n >= 2 else np.inf)
+        out[r, order[n:]] = -np.inf
+    return out.reshape(shape), kept.reshape(shape[:-1]), margin.reshape(shape[:-1])
+
+
+def verify_topp(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
+                uniforms: np.ndarray, temperature: float, top_p: float) -> NucleusResult:
+    """Verification on nucleus filtered distributions: the card's §4.2
+    "Decoding transforms" (apply the transform to both p and q, then the
+    rejection scheme on the modified distributions) with the nucleus rule of
+    `topp_mask` on each of the 2K+1 rows, at the same temperature as the
+    verification."""
+    if not (top_p > 0.0):
+        raise ValueError("top_p must be > 0")
+    with np.errstate(over="ignore"):
+        T = float(np.float32(temperature))
+    tm, tk, tg = topp_mask(target, T, top_p)
+    dm, dk, dg = topp_mask(draft, T, top_p)
+    res = verify(tm, dm, tokens, uniforms, temperature)
+    return NucleusResult(res, np.concatenate([tk, dk], axis=1), np.concatenate([tg, dg], axis=1))
+
+
 def _widen(x) -> np.ndarray:
     """Exact widening of a torch tensor (bf16 / fp32 / int) or array to numpy fp64."""
     if hasattr(x, "detach"):

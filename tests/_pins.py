@@ -557,8 +557,141 @@ def pin_topk_law(O, n=200_000, V=12, k=5, seed=31):
     assert stats.chisquare(counts[keep_q], expect * counts[keep_q].sum() / expect.sum()).pvalue > 1e-4
 
 
+def pin_topp_mask_cases(O):
+    """Hand-checked nucleus masks (U17): probabilities .5/.3/.15/.05 keep 1,
+    2, 3, 4 entries at p = .4/.7/.9/.99; equal logits go to the smaller id
+    (-0 equal to +0); the order is by logit, not by id; -inf entries are
+    never needed; the temperature is applied before the cut."""
+    ni = -np.inf
+    lg = np.log([0.5, 0.3, 0.15, 0.05])
+    for p, n in ((0.4, 1), (0.7, 2), (0.9, 3), (0.99, 4), (1.0, 4)):
+        m, k, _ = O.topp_mask(lg[None], 1.0, p)
+        assert k[0] == n and np.isfinite(m[0]).sum() == n and np.isfinite(m[0, :n]).all(), (p, m)
+    m, k, _ = O.topp_mask(np.zeros((1, 4)), 1.0, 0.3)        # .25 each: two needed
+    assert list(np.isfinite(m[0])) == [True, True, False, False]
+    # .25 each is exact in fp64, so the cumulative sums hit p = .25 and .5
+    # exactly: reaching p is enough
+    assert O.topp_mask(np.zeros((1, 4)), 1.0, 0.25)[1][0] == 1
+    assert O.topp_mask(np.zeros((1, 4)), 1.0, 0.5)[1][0] == 2
+    m, _, _ = O.topp_mask(np.array([[-0.0, 0.0, -5.0]]), 1.0, 0.3)
+    assert list(np.isfinite(m[0])) == [True, False, False]
+    m, _, _ = O.topp_mask(np.array([[1.0, 3.0, 2.0]]), 1.0, 0.8)   # .665 + .245 >= .8
+    assert list(np.isfinite(m[0])) == [False, True, True]
+    m, _, _ = O.topp_mask(np.array([[ni, 0.0, 0.0, ni]]), 1.0, 0.9)
+    assert list(np.isfinite(m[0])) == [False, True, True, False]
+    lt = np.log([[0.5, 0.3, 0.2]])
+    # T = 1: .5 + .3 = .8 < .85 needs all three; T = .5: .658 + .237 >= .85
+    assert O.topp_mask(lt, 1.0, 0.85)[1][0] == 3 and O.topp_mask(lt, 0.5, 0.85)[1][0] == 2
+
+
+def pin_topp_brute_force(O):
+    """Against an enumeration of subsets on tiny rows: the kept set has the
+    smallest size among all subsets whose mass reaches p, the largest mass
+    among subsets of that size, and nothing removed outranks anything kept
+    (larger logit, or equal logit and smaller id)."""
+    import itertools
+
+    rng = np.random.default_rng(37)
+    for trial in range(120):
+        V = int(rng.integers(2, 7))
+        row = np.round(rng.normal(0, 1.2, V), 1)
+        T = float(rng.choice([0.5, 1.0, 1.7]))
+        p = float(rng.choice([0.2, 0.5, 0.75, 0.9, 0.97]))
+        q = softmax(row / T)
+        masked, kept, _ = O.topp_mask(row[None], T, p)
+        keep = np.isfinite(masked[0])
+        size = None
+        for s in range(1, V + 1):
+            best = max(q[list(c)].sum() for c in itertools.combinations(range(V), s))
+            if best >= p - 1e-12:
+                size = s
+                break
+        assert size is not None and keep.sum() == size == kept[0], (row, T, p, keep)
+        best = max(q[list(c)].sum() for c in itertools.combinations(range(V), size))
+        assert abs(q[keep].sum() - best) < 1e-12
+        for i in np.nonzero(keep)[0]:
+            for j in np.nonzero(~keep)[0]:
+                assert row[i] > row[j] or (row[i] == row[j] and i < j), (row, keep)
+
+
+def pin_topp_hand_case(O):
+    """Worked by hand: V = 3, K = 1, T = 1, p = .7. Target row 0 .5/.3/.2 keeps
+    ids 0, 1 (q = .625, .375, 0); target row 1 .2/.2/.6 keeps ids 2, 0
+    (q = .25, 0, .75); the draft .1/.3/.6 keeps ids 2, 1 (p = 0, 1/3, 2/3).
+    Sequence A drafts id 1: q/p = 1.125, accepted; the bonus at u = .3 over
+    .25, 0, .75 is id 2 (unfiltered it would be id 1). Sequence B drafts id 2:
+    q = 0, rejected; the residual .625, 1/24, 0 at u = .9 is id 0 (with an
+    unfiltered draft, .525, .075, 0 would give id 1)."""
+    tl = np.log(np.array([[[0.5, 0.3, 0.2], [0.2, 0.2, 0.6]]] * 2))
+    dl = np.log(np.array([[[0.1, 0.3, 0.6]]] * 2))
+    uni = np.array([[0.5, 0.5, 0.3], [0.5, 0.9, 0.5]])
+    n = O.verify_topp(tl, dl, np.array([[1], [2]]), uni, 1.0, 0.7)
+    r = n.result
+    assert (r.status == 0).all()
+    assert list(r.out_tokens[0]) == [1, 2] and r.n_accepted[0] == 1, r.out_tokens
+    assert list(r.out_tokens[1]) == [0, -1] and r.n_accepted[1] == 0, r.out_tokens
+    np.testing.assert_allclose(r.thresholds[:, 0], [1.0, 0.0])
+    assert n.kept.tolist() == [[2, 2, 2], [2, 2, 2]]
+
+
+def pin_topp_one_is_verify(O):
+    """top_p = 1 is no filter: verify_topp equals verify."""
+    rng = np.random.default_rng(41)
+    B, K, V = 16, 3, 30
+    tl, dl = rng.normal(0, 2, (B, K + 1, V)), rng.normal(0, 2, (B, K, V))
+    tok, uni = rng.integers(0, V, (B, K)), rng.random((B, K + 2))
+    a, b = O.verify(tl, dl, tok, uni, 0.8), O.verify_topp(tl, dl, tok, uni, 0.8, 1.0).result
+    assert (a.out_tokens == b.out_tokens).all() and (a.n_accepted == b.n_accepted).all()
+    np.testing.assert_array_equal(a.thresholds, b.thresholds)
+
+
+def pin_topp_tiny_is_top1(O):
+    """A nucleus smaller than every row's largest probability keeps one entry
+    per row, the first argmax: verify_topp equals verify_topk with k = 1."""
+    rng = np.random.default_rng(43)
+    B, K, V = 32, 3, 25
+    tl = np.round(rng.normal(0, 1.5, (B, K + 1, V)), 1)
+    dl = np.round(rng.normal(0, 1.5, (B, K, V)), 1)
+    tok, uni = rng.integers(0, V, (B, K)), rng.random((B, K + 2)) * 0.999
+    a, b = O.verify_topk(tl, dl, tok, uni, 1.1, 1), O.verify_topp(tl, dl, tok, uni, 1.1, 1e-9).result
+    assert (a.out_tokens == b.out_tokens).all() and (a.n_accepted == b.n_accepted).all()
+
+
+def pin_topp_law(O, n=200_000, V=12, p=0.8, seed=47):
+    """Theorem 1 under the nucleus transform: the first emitted token is
+    distributed as the filtered q; chi-square against the renormalised
+    top entries of q, with the draft drawn from the filtered p."""
+    from scipy import stats
+
+    rng = np.random.default_rng(seed)
+    tl = rng.normal(0, 1.0, (1, 2, V))
+    dl = rng.normal(0, 1.0, (1, 1, V))
+    T = 0.9
+
+    def nucleus(row):
+        q = softmax(row / T)
+        order = np.argsort(-q, kind="stable")
+        n_keep = int(np.searchsorted(np.cumsum(q[order]), p)) + 1
+        keep = order[:n_keep]
+        f = np.zeros(V)
+        f[keep] = q[keep] / q[keep].sum()
+        return keep, f
+
+    keep_q, fq = nucleus(tl[0, 0])
+    _, fp = nucleus(dl[0, 0])
+    toks = np.minimum(np.searchsorted(np.cumsum(fp), rng.random(n), side="right"), V - 1)
+    r = O.verify_topp(np.repeat(tl, n, 0), np.repeat(dl, n, 0), toks[:, None],
+                      rng.random((n, 3)), T, p).result
+    counts = np.bincount(r.out_tokens[:, 0], minlength=V)
+    assert counts[np.setdiff1d(np.arange(V), keep_q)].sum() == 0
+    expect = fq[keep_q] * n
+    assert stats.chisquare(counts[keep_q], expect * counts[keep_q].sum() / expect.sum()).pvalue > 1e-4
+
+
 FAST_PINS = (pin_golden, pin_theorem1, pin_sequential, pin_library_special_cases,
              pin_invariants, pin_failures, pin_draft_golden, pin_draft_failures,
              pin_draft_matches_bonus, pin_greedy_golden, pin_greedy_is_zero_temperature,
              pin_greedy_failures, pin_topk_mask_cases, pin_topk_hand_case,
-             pin_topk_full_is_verify, pin_topk_one_is_greedy)
+             pin_topk_full_is_verify, pin_topk_one_is_greedy, pin_topp_mask_cases,
+             pin_topp_brute_force, pin_topp_hand_case, pin_topp_one_is_verify,
+             pin_topp_tiny_is_top1)

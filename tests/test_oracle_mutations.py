@@ -66,6 +66,17 @@ MUTATIONS = [
     ("top-k filters the target only",
      "return verify(topk_mask(target, top_k), topk_mask(draft, top_k), tokens, uniforms,",
      "return verify(topk_mask(target, top_k), draft, tokens, uniforms,"),
+    ("nucleus cut is strict (> p)",
+     "reach = np.nonzero(c >= top_p)[0]", "reach = np.nonzero(c > top_p)[0]"),
+    ("nucleus keeps one entry too few",
+     "out[r, order[n:]] = -np.inf", "out[r, order[n - 1:]] = -np.inf"),
+    ("nucleus ties go to the larger id",
+     "order = np.argsort(-(flat[r] + 0.0), kind=\"stable\")",
+     "order = (V - 1 - np.argsort(-(flat[r][::-1] + 0.0), kind=\"stable\"))"),
+    ("nucleus cut before the temperature",
+     "q, _, st = temperature_softmax(flat, temperature)", "q, _, st = temperature_softmax(flat, 1.0)"),
+    ("nucleus filters the target only",
+     "res = verify(tm, dm, tokens, uniforms, temperature)", "res = verify(tm, draft, tokens, uniforms, temperature)"),
 ]
 
 

@@ -131,3 +131,27 @@ def test_topk_first_token_law_is_filtered_q():
 
 def test_topk_hand_case_filters_the_draft_too():
     _pins.pin_topk_hand_case(oracle)
+
+
+def test_topp_mask_hand_cases():
+    _pins.pin_topp_mask_cases(oracle)
+
+
+def test_topp_against_subset_enumeration():
+    _pins.pin_topp_brute_force(oracle)
+
+
+def test_topp_hand_case_filters_both_rows():
+    _pins.pin_topp_hand_case(oracle)
+
+
+def test_topp_one_is_verify():
+    _pins.pin_topp_one_is_verify(oracle)
+
+
+def test_topp_tiny_is_top1():
+    _pins.pin_topp_tiny_is_top1(oracle)
+
+
+def test_topp_first_token_law_is_filtered_q():
+    _pins.pin_topp_law(oracle)
