@@ -271,6 +271,38 @@ int spec_verify_topk(const void* target_logits, const void* draft_logits,
                      int dtype, float temperature, int top_k, int32_t* out_tokens,
                      int32_t* n_accepted, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- nucleus (top-p) filtered verification
+ *
+ * The card's §4.2 "Decoding transforms" with the nucleus rule on both p and
+ * q: each of the 2K+1 rows keeps the shortest prefix of its entries, ordered
+ * by logit (larger first, ties to the smaller token id, -0.0 equal to +0.0),
+ * whose probability softmax(l / T) reaches top_p; the other entries count as
+ * -inf. The filtered rows are then verified exactly as by spec_verify. */
+
+/* Bytes of device workspace spec_verify_topp needs; 0 for invalid sizes. */
+size_t sv_topp_workspace_size(int B, int K, int V, int dtype);
+
+/* Nucleus filtered verification. Arguments as for spec_verify, plus
+ *   top_p        probability mass kept per row: top_p > 0; top_p >= 1 keeps
+ *                every entry (the call is spec_verify's); NaN or top_p <= 0
+ *                returns SV_ERR_SHAPE
+ *   kept_counts  device, [B, 2K+1] int32, may be NULL: entries kept per row
+ *                (target rows 0..K, then draft rows 0..K-1); V for a row that
+ *                fails (NaN, +inf or all -inf), which is left as it is
+ * Per row, a cut is found without a sort: mass histograms over (m - l) / T at
+ * finer and finer widths locate the cut to a bin of at most 1024 entries,
+ * resolved exactly by a radix select weighted by mass (a bin that never gets
+ * that small, from heavy ties, is resolved bit by bit over the key). Weights
+ * are float-float exponentials, sums fp64. Masked copies of the rows are then
+ * written into the workspace and verified by the unfiltered kernels: four or
+ * five kernels per call. Returns SV_OK once enqueued, or a host-side error
+ * code with nothing enqueued; B == 0 returns SV_OK at once. */
+int spec_verify_topp(const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                     int dtype, float temperature, float top_p, int32_t* out_tokens,
+                     int32_t* n_accepted, int32_t* kept_counts, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* Reads the device status word of the last call that used `workspace`: waits
  * for `stream`, then stores the OR of the SV_DEV_* bits in *status. */
 int sv_read_device_status(const void* workspace, void* stream, int* status);

@@ -28,6 +28,7 @@ __all__ = [
     "sv_sample_workspace_size", "spec_draft_sample", "draft_sample",
     "sv_greedy_workspace_size", "spec_verify_greedy", "verify_greedy", "sv_force_path",
     "sv_test_withhold_plans", "sv_topk_workspace_size", "spec_verify_topk", "verify_topk",
+    "sv_topp_workspace_size", "spec_verify_topp", "verify_topp",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -43,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "spec_verify_host", "sv_read_device_status", "sv_status_string", "sv_kernels_per_call",
     "spec_verify_static", "sv_sample_workspace_size", "spec_draft_sample",
     "sv_greedy_workspace_size", "spec_verify_greedy", "sv_force_path", "sv_test_withhold_plans",
-    "sv_topk_workspace_size", "spec_verify_topk",
+    "sv_topk_workspace_size", "spec_verify_topk", "sv_topp_workspace_size", "spec_verify_topp",
 )
 
 _lib = None
@@ -100,6 +101,10 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.sv_topk_workspace_size.restype = sz
     lib.spec_verify_topk.argtypes = core[:9] + [i32] + core[9:]
     lib.spec_verify_topk.restype = i32
+    lib.sv_topp_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.sv_topp_workspace_size.restype = sz
+    lib.spec_verify_topp.argtypes = core[:9] + [f32] + core[9:11] + [vp] + core[11:]
+    lib.spec_verify_topp.restype = i32
     lib.sv_kernels_per_call.argtypes = [i32, i32, i32, i32]
     lib.sv_kernels_per_call.restype = i32
     lib.sv_force_path.argtypes = [i32]
@@ -318,6 +323,44 @@ def verify_topk(target, draft, tokens, uniforms, temperature, top_k, *, workspac
     if rc != SV_OK:
         raise StatusError(rc, "spec_verify_topk")
     return out, nacc
+
+
+def sv_topp_workspace_size(B: int, K: int, V: int, dtype: int) -> int:
+    return int(load_library().sv_topp_workspace_size(B, K, V, dtype))
+
+
+def spec_verify_topp(target, draft, tokens, uniforms, temperature, top_p, out_tokens, n_accepted,
+                     workspace, kept_counts=None, stream=None) -> int:
+    """Direct binding of nucleus filtered verification; returns the host status code."""
+    B, K, V, dt = _check(target, draft, tokens, uniforms)
+    return int(load_library().spec_verify_topp(
+        _ptr(target), _ptr(draft), _ptr(tokens), _ptr(uniforms), B, K, V, dt,
+        ctypes.c_float(temperature), ctypes.c_float(top_p), _ptr(out_tokens), _ptr(n_accepted),
+        _ptr(kept_counts), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(target.device, stream)))
+
+
+def verify_topp(target, draft, tokens, uniforms, temperature, top_p, *, workspace=None,
+                stream=None):
+    """Allocate outputs (and a workspace if none is given) and run nucleus
+    filtered verification; returns (out_tokens [B, K+1] int32, n_accepted [B]
+    int32, kept_counts [B, 2K+1] int32)."""
+    if tokens.dtype == torch.int64:
+        tokens = tokens.to(torch.int32)
+    B, K, V, dt = _check(target, draft, tokens, uniforms)
+    dev = target.device
+    out = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+    nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    kept = torch.empty(B, 2 * K + 1, dtype=torch.int32, device=dev)
+    ws = workspace
+    if ws is None:
+        n = sv_topp_workspace_size(B, K, V, dt)
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    rc = spec_verify_topp(target, draft, tokens, uniforms, temperature, top_p, out, nacc, ws,
+                          kept, stream=stream)
+    if rc != SV_OK:
+        raise StatusError(rc, "spec_verify_topp")
+    return out, nacc, kept
 
 
 def sv_sample_workspace_size(N: int, V: int, dtype: int) -> int:

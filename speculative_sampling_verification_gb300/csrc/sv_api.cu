@@ -352,6 +352,86 @@ int spec_verify_topk(const void* target_logits, const void* draft_logits,
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Nucleus path workspace: the unfiltered layout, then the masked target and
+// draft copies, then one cut key per row.
+struct ToppLayout {
+  sv::Layout L;
+  size_t off_mt, off_md, off_cut, total;
+};
+
+bool make_topp_layout(int B, int K, int V, int dtype, ToppLayout* T) {
+  if (!sv::make_layout(B, K, V, dtype, &T->L)) return false;
+  const size_t es = T->L.es;
+  size_t off = sv::align_up(T->L.total, 256);
+  T->off_mt = off;
+  off = sv::align_up(off + (size_t)B * (K + 1) * V * es, 256);
+  T->off_md = off;
+  off = sv::align_up(off + (size_t)B * K * V * es, 256);
+  T->off_cut = off;
+  off = sv::align_up(off + (size_t)B * (2 * K + 1) * 8, 256);
+  T->total = off;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sv_topp_workspace_size(int B, int K, int V, int dtype) {
+  ToppLayout T;
+  if (!make_topp_layout(B, K, V, dtype, &T)) return 0;
+  return T.total;
+}
+
+int spec_verify_topp(const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
+                     int dtype, float temperature, float top_p, int32_t* out_tokens,
+                     int32_t* n_accepted, int32_t* kept_counts, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (dtype != SV_BF16 && dtype != SV_F32) return SV_ERR_DTYPE;
+  if (!(top_p > 0.0f)) return SV_ERR_SHAPE;
+  ToppLayout TL;
+  if (!make_topp_layout(B, K, V, dtype, &TL)) return SV_ERR_SHAPE;
+  sv::Layout L;
+  int rc = validate(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype,
+                    temperature, out_tokens, n_accepted, workspace, workspace_bytes, &L);
+  if (rc != SV_OK || B == 0) return rc;
+  if (misaligned(kept_counts, 4)) return SV_ERR_ALIGN;
+  if (workspace_bytes < TL.total) return SV_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long rows = (long long)B * (2 * K + 1);
+  if (top_p >= 1.0f) {  // keeps every entry: the unfiltered call
+    rc = run(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype, temperature,
+             out_tokens, n_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
+             nullptr);
+    if (rc == SV_OK && kept_counts && sv::fill_int(kept_counts, rows, V, st) != cudaSuccess)
+      return SV_ERR_CUDA;
+    return rc;
+  }
+  sv::Params P{};
+  fill_params(P, TL.L, B, K, V, dtype, temperature, workspace);
+  P.target = target_logits;
+  P.draft = draft_logits;
+  P.tokens = draft_tokens;
+  P.uniforms = uniforms;
+  int ib = 1;
+  while (ib < 31 && ((long long)(V - 1) >> ib) != 0) ++ib;
+  P.key_ibits = ib;
+  P.top_p = top_p;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  P.topp_cut = reinterpret_cast<unsigned long long*>(ws + TL.off_cut);
+  P.topp_kept = kept_counts;
+  void* mt = ws + TL.off_mt;
+  void* md = ws + TL.off_md;
+  if (sv::launch_topp(P, mt, md, st) != cudaSuccess) return SV_ERR_CUDA;
+  return run(mt, md, draft_tokens, uniforms, B, K, V, dtype, temperature, out_tokens, n_accepted,
+             workspace, workspace_bytes, stream, nullptr, nullptr, nullptr);
+}
+
 int sv_read_device_status(const void* workspace, void* stream, int* status) {
   if (!workspace || !status) return SV_ERR_NULL;
   if (misaligned(workspace, 256)) return SV_ERR_ALIGN;

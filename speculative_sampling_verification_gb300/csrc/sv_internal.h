@@ -166,6 +166,9 @@ struct Params {
   double* topk_at;      // top-k path: [B (2K+1)] probability of the row's drafted token
   int* topk_idx;        // top-k path: [B (2K+1), k] kept ids, ascending
   double* topk_prob;    // top-k path: [B (2K+1), k] their probabilities over the kept set
+  float top_p;                   // nucleus path: the probability mass kept per row
+  unsigned long long* topp_cut;  // nucleus path: [B (2K+1)] keys >= cut are kept
+  int* topp_kept;                // nucleus path: [B (2K+1)] kept entries per row, or null
   long long nsi;   // fused kernel: streaming items (of up to 8 units) per sequence
   long long lag;   // fused kernel: sequences between a sequence's streaming and draw tickets
   double inv_t;    // 1/T in fp64 (scan)
@@ -210,6 +213,11 @@ cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t stream);
 // Top-k filtered verification: the row selection kernel, then the sparse
 // verification kernel.
 cudaError_t launch_topk(const Params& P, bool aligned, cudaStream_t stream);
+// Nucleus filtering: the per-row cut kernel, then the masked copies of the
+// target and draft rows (the verification then runs on the copies).
+cudaError_t launch_topp(const Params& P, void* masked_target, void* masked_draft,
+                        cudaStream_t stream);
+cudaError_t fill_int(int* p, long long n, int v, cudaStream_t stream);
 // Kernels one call over B sequences of rows_per_seq rows of V elements of
 // `es` bytes launches: 1 when the fused kernel is taken, else 2.
 int kernels_per_call(long long B, int rows_per_seq, long long V, int es);

@@ -24,6 +24,7 @@
 #include <cfloat>
 #include <math_constants.h>
 #include <climits>
+#include <type_traits>
 #include <cstdint>
 #include <atomic>
 #include <mutex>
@@ -1912,6 +1913,342 @@ __global__ void __launch_bounds__(kTvThreads) topk_verify_kernel(Params P) {
   }
 }
 
+// ---------------------------------------------------------------- nucleus (top-p) filtered verification
+//
+// The card's §4.2 "Decoding transforms" with the nucleus rule: each of the
+// 2K+1 rows keeps the shortest prefix of its entries, in (logit descending,
+// id ascending) order, whose probability softmax(l / T) reaches top_p. The cut
+// is found per row without a sort, as a key K* (the order-preserving value key
+// above V-1-id): an entry is kept iff its key is >= K*. One CTA per row:
+//   1. the row maximum m (and NaN / +inf);
+//   2. levels of mass histograms over d = (m - l) / T: level L bins d at width
+//      4 / 16^(L-1), so a level-L bin splits into 16 level-(L+1) bins exactly
+//      (d * 2^j is exact); each level keeps the bin in which the running mass,
+//      from the top, reaches p * S (S, the row's total, from level 1), and
+//      adds the bins above it to the mass above;
+//   3. once that bin holds at most kTpCap entries, they are gathered with
+//      their weights and K* is found among them by a radix select on the key
+//      weighted by mass; a bin that never gets that small (heavy ties) is
+//      resolved bit by bit over the key with a pass per bit.
+// Weights are exp((l - m) / T) in float-float (the same exp as the unfiltered
+// path, ~1e-12 relative); masses are summed as float-float per thread and in
+// fp64 across threads. The masked rows (-inf outside the kept set) are then
+// verified by the unfiltered kernels.
+
+constexpr int kTpThreads = 256;
+constexpr int kTpBins = 16;
+constexpr int kTpCap = 1024;
+constexpr int kTpMaxLevels = 6;
+
+struct TopPShared {
+  float2 tab[256];
+  float bhi[kTpBins][kTpThreads], blo[kTpBins][kTpThreads];  // per-thread bin masses (ff)
+  unsigned bcnt[kTpBins][kTpThreads];                       // per-thread bin counts
+  unsigned long long ckey[kTpCap];
+  double cw[kTpCap];
+  double mh[256];
+  unsigned ch[256];
+  double red[kTpThreads / 32];
+  double binmass[kTpBins];
+  unsigned bincount[kTpBins];
+  unsigned n_cand;
+  unsigned long long prefix, cutmin;
+  double above;
+  int found;
+};
+
+SV_DEVINL double tp_block_sum(TopPShared& sh, double v) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_d(v);
+  __syncthreads();
+  if (lane == 0) sh.red[warp] = v;
+  __syncthreads();
+  double r = 0.0;
+#pragma unroll
+  for (int w = 0; w < kTpThreads / 32; ++w) r += sh.red[w];
+  return r;
+}
+
+// d = (m - l) / T and the float-float weight exp(-(d)) of one element.
+struct TpElem {
+  float d;
+  ff w;
+};
+
+SV_DEVINL TpElem tp_elem(float l, float m, const Params& P, const float2* tab) {
+  const ff x = scaled_diff(l, m, P.ih, P.il, P.unit_t != 0);
+  return {-x.hi, exp_ff(x.hi, x.lo, tab)};
+}
+
+// Level-L bin of d: floor(d * 4^(2L-3)) (width 4 at L = 1, /16 per level).
+SV_DEVINL float tp_scale(int level) { return ldexpf(1.0f, 4 * level - 6); }
+
+template <int DT>
+__global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
+  extern __shared__ __align__(16) unsigned char tp_smem[];
+  TopPShared& sh = *reinterpret_cast<TopPShared*>(tp_smem);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long row = blockIdx.x;
+  const unsigned char* rb = row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
+  const int V = P.V, ib = P.key_ibits;
+  constexpr int NB = DT == 0 ? 16 : 32;
+  const int bits = NB + ib;
+  sh.tab[tid] = kSvExp2Table[tid];
+  const unsigned ntiles = (unsigned)(((long long)V + kSelTile - 1) / kSelTile);
+  auto key_of = [&](uint32_t b, unsigned i) -> unsigned long long {
+    return ((unsigned long long)value_key<DT>(b) << ib) | (unsigned long long)(V - 1 - (int)i);
+  };
+  // Visit every element of the row (8 consecutive per thread per tile).
+  auto for_each = [&](auto&& fn) {
+    for (unsigned t = 0; t < ntiles; ++t) {
+      uint32_t w[SelWords<DT>::n];
+      const unsigned e0 = t * kSelTile + tid * 8;
+      const int nv = load_sel_tile<DT, false>(rb, (long long)e0, V, w);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < nv) fn(elem_bits<DT>(w, j), e0 + j);
+    }
+  };
+  auto to_float = [](uint32_t b) { return __uint_as_float(DT == 0 ? b << 16 : b); };
+  // 1. The maximum, and NaN / +inf.
+  float m = -CUDART_INF_F;
+  bool bad = false;
+  for_each([&](uint32_t b, unsigned) {
+    bad |= nan_or_pos_inf<DT>(b);
+    m = fmaxf(m, to_float(b));
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) sh.red[warp] = m;
+  const bool any_bad = __syncthreads_or(bad);
+  m = (float)sh.red[0];
+  for (int w2 = 1; w2 < kTpThreads / 32; ++w2) m = fmaxf(m, (float)sh.red[w2]);
+  if (any_bad || m == -CUDART_INF_F) {
+    // A failing row stays as it is (the verification reports it).
+    if (tid == 0) {
+      P.topp_cut[row] = 0;
+      if (P.topp_kept) P.topp_kept[row] = V;
+    }
+    return;
+  }
+  double target = 0.0, above = 0.0;
+  unsigned long long cut = 0;
+  int level = 1;
+  long long parent = 0;  // the bin, at level - 1, that holds the cut
+  bool gathered = false;
+  for (; level <= kTpMaxLevels; ++level) {
+    const float sc = tp_scale(level), psc = tp_scale(level - 1);
+#pragma unroll
+    for (int b = 0; b < kTpBins; ++b) {
+      sh.bhi[b][tid] = 0.0f;
+      sh.blo[b][tid] = 0.0f;
+      sh.bcnt[b][tid] = 0;
+    }
+    ff total = {0.0f, 0.0f};
+    for_each([&](uint32_t b, unsigned) {
+      const float l = to_float(b);
+      const float d = -scaled_diff(l, m, P.ih, P.il, P.unit_t != 0).hi;
+      if (level > 1 && floorf(d * psc) != (float)parent) return;
+      const TpElem e = tp_elem(l, m, P, sh.tab);
+      const float r = fminf(floorf(d * sc) - (level > 1 ? 16.0f * (float)parent : 0.0f), 15.0f);
+      const int bin = (int)r;
+      ff acc = {sh.bhi[bin][tid], sh.blo[bin][tid]};
+      ff_accumulate(acc, e.w);
+      sh.bhi[bin][tid] = acc.hi;
+      sh.blo[bin][tid] = acc.lo;
+      sh.bcnt[bin][tid] += 1;
+      if (level == 1) ff_accumulate(total, e.w);
+    });
+    __syncthreads();
+    // Bin totals: warp w sums bins 2w and 2w+1 over the threads.
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int b = 2 * warp + h;
+      double s = 0.0;
+      unsigned c = 0;
+      for (int t = lane; t < kTpThreads; t += 32) {
+        s += (double)sh.bhi[b][t] + (double)sh.blo[b][t];
+        c += sh.bcnt[b][t];
+      }
+      s = warp_sum_d(s);
+      c = __reduce_add_sync(0xffffffffu, c);
+      if (lane == 0) {
+        sh.binmass[b] = s;
+        sh.bincount[b] = c;
+      }
+    }
+    if (level == 1) {
+      const double S = tp_block_sum(sh, ff_to_double(total));
+      target = (double)P.top_p * S;
+    }
+    __syncthreads();
+    // The bin where the running mass from the top reaches the target. If
+    // rounding (the bins re-sum the parent bin in another order) leaves the
+    // target just out of reach, the cut is at the end of the parent bin: its
+    // last non-empty bin.
+    int bstar = -1, last = -1;
+    double a = above;
+    for (int b = 0; b < kTpBins; ++b) {
+      if (sh.bincount[b] == 0) continue;
+      last = b;
+      if (a + sh.binmass[b] >= target) {
+        bstar = b;
+        break;
+      }
+      a += sh.binmass[b];
+    }
+    if (bstar < 0) {
+      bstar = last;
+      a -= sh.binmass[last];
+    }
+    above = a;
+    const unsigned count = sh.bincount[bstar];
+    parent = (level > 1 ? 16 * parent : 0) + bstar;
+    if (level == 1 && bstar == kTpBins - 1) {  // d >= 60: left to the per-bit path
+      level = kTpMaxLevels + 1;
+      break;
+    }
+    if (count <= (unsigned)kTpCap) {
+      gathered = true;
+      break;
+    }
+    __syncthreads();
+  }
+  if (gathered) {
+    // 3. Gather the bin's entries with their weights.
+    const float sc = tp_scale(level);
+    if (tid == 0) {
+      sh.n_cand = 0;
+      sh.cutmin = ~0ull;
+    }
+    __syncthreads();
+    for_each([&](uint32_t b, unsigned i) {
+      const float l = to_float(b);
+      const float d = -scaled_diff(l, m, P.ih, P.il, P.unit_t != 0).hi;
+      if (floorf(d * sc) != (float)parent) return;
+      const unsigned s = atomicAdd(&sh.n_cand, 1u);
+      if (s < (unsigned)kTpCap) {
+        sh.ckey[s] = key_of(b, i);
+        sh.cw[s] = ff_to_double(tp_elem(l, m, P, sh.tab).w);
+      }
+    });
+    __syncthreads();
+    const unsigned n = min(sh.n_cand, (unsigned)kTpCap);
+    // Radix select over the candidates' keys, 8-bit digits from the top,
+    // weighted by mass: the largest key K* with above + mass(key >= K*) >=
+    // target.
+    const int pad = (8 - bits % 8) % 8, top = bits + pad;
+    unsigned long long prefix = 0;
+    double abv = above;
+    int resolved = 0;
+    while (resolved < top) {
+      const int shift = top - resolved - 8;
+      sh.mh[tid] = 0.0;
+      sh.ch[tid] = 0;
+      __syncthreads();
+      for (unsigned i = tid; i < n; i += kTpThreads) {
+        const unsigned long long k = sh.ckey[i] << pad;
+        if (resolved == 0 || (k >> (shift + 8)) == (prefix >> (shift + 8))) {
+          const unsigned bin = (unsigned)((k >> shift) & 255u);
+          atomicAdd(&sh.mh[bin], sh.cw[i]);
+          atomicAdd(&sh.ch[bin], 1u);
+        }
+      }
+      __syncthreads();
+      if (tid == 0) {
+        // Bins from the top; sequential over 256 bins (one thread).
+        double a2 = abv;
+        int sel = -1, last = -1;
+        for (int b = 255; b >= 0; --b) {
+          if (sh.ch[b] == 0) continue;
+          last = b;
+          if (a2 + sh.mh[b] >= target) {
+            sel = b;
+            break;
+          }
+          a2 += sh.mh[b];
+        }
+        if (sel < 0 && last >= 0) {  // rounding: the cut is at the last key
+          sel = last;
+          a2 -= sh.mh[last];
+        }
+        sh.found = sel;
+        sh.above = a2;
+        sh.prefix = prefix | ((unsigned long long)(sel < 0 ? 0 : sel) << shift);
+        sh.n_cand = sel < 0 ? 0 : sh.ch[sel];
+      }
+      __syncthreads();
+      prefix = sh.prefix;
+      abv = sh.above;
+      resolved += 8;
+      if (sh.n_cand <= 1) break;
+      __syncthreads();
+    }
+    // The single key under the prefix (cutmin was set before the search).
+    const int lo = top - resolved;
+    for (unsigned i = tid; i < n; i += kTpThreads) {
+      const unsigned long long k = sh.ckey[i] << pad;
+      if ((k >> lo) == (prefix >> lo)) atomicMin(&sh.cutmin, sh.ckey[i]);
+    }
+    __syncthreads();
+    cut = sh.cutmin;
+  } else {
+    // Heavy ties around the cut: bit by bit over the key, one pass per bit,
+    // with the exact mass of the keys at or above the trial cut.
+    unsigned long long x = 0;
+    for (int bit = bits - 1; bit >= 0; --bit) {
+      const unsigned long long y = x | (1ull << bit);
+      ff part = {0.0f, 0.0f};
+      for_each([&](uint32_t b, unsigned i) {
+        if (key_of(b, i) >= y) ff_accumulate(part, tp_elem(to_float(b), m, P, sh.tab).w);
+      });
+      if (tp_block_sum(sh, ff_to_double(part)) >= target) x = y;
+    }
+    cut = x;
+  }
+  // The kept count, for the caller.
+  unsigned kept = 0;
+  for_each([&](uint32_t b, unsigned i) { kept += key_of(b, i) >= cut ? 1u : 0u; });
+  kept = __reduce_add_sync(0xffffffffu, kept);
+  __syncthreads();
+  if (lane == 0) sh.ch[warp] = kept;
+  __syncthreads();
+  if (tid == 0) {
+    unsigned tot = 0;
+    for (int w2 = 0; w2 < kTpThreads / 32; ++w2) tot += sh.ch[w2];
+    P.topp_cut[row] = cut;
+    if (P.topp_kept) P.topp_kept[row] = (int)tot;
+  }
+}
+
+// The masked copies: every element of the 2K+1 rows whose key is below its
+// row's cut becomes -inf; the others are copied.
+template <int DT>
+__global__ void __launch_bounds__(256) topp_mask_kernel(Params P, void* masked_target,
+                                                        void* masked_draft) {
+  using E = typename std::conditional<DT == 0, unsigned short, uint32_t>::type;
+  const long long rows = (long long)P.B * P.rows_per_seq;
+  const long long n = rows * P.V;
+  const int ib = P.key_ibits;
+  const E kNegInf = DT == 0 ? (E)0xff80u : (E)0xff800000u;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n;
+       g += (long long)gridDim.x * blockDim.x) {
+    const long long row = g / P.V;
+    const int i = (int)(g - row * P.V);
+    const long long b = row / P.rows_per_seq;
+    const int r = (int)(row % P.rows_per_seq);
+    const E* src = reinterpret_cast<const E*>(row_base(P, b, r));
+    E* dst = r <= P.K
+                 ? reinterpret_cast<E*>(masked_target) + ((size_t)b * (P.K + 1) + r) * (size_t)P.V
+                 : reinterpret_cast<E*>(masked_draft) +
+                       ((size_t)b * P.K + (r - P.K - 1)) * (size_t)P.V;
+    const E v = src[i];
+    const unsigned long long key =
+        ((unsigned long long)value_key<DT>((uint32_t)v) << ib) | (unsigned long long)(P.V - 1 - i);
+    dst[i] = key >= P.topp_cut[row] ? v : kNegInf;
+  }
+}
+
 // ---------------------------------------------------------------- host-side launch
 
 namespace {
@@ -2048,6 +2385,47 @@ cudaError_t launch_topk(const Params& P, bool aligned, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (e != cudaSuccess) return e;
   topk_verify_kernel<<<(unsigned)P.B, kTvThreads, 0, st>>>(P);
+  return cudaGetLastError();
+}
+
+template <int DT>
+static cudaError_t launch_topp_kernels(const Params& P, void* mt, void* md, cudaStream_t st) {
+  const size_t smem = sizeof(TopPShared);
+  cudaError_t e = cudaFuncSetAttribute(topp_cut_kernel<DT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const unsigned rows = (unsigned)((long long)P.B * P.rows_per_seq);
+  topp_cut_kernel<DT><<<rows, kTpThreads, smem, st>>>(P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long n = (long long)rows * P.V;
+  const long long blocks = (n + 255) / 256;
+  const unsigned grid = (unsigned)(blocks < 152LL * 8 * 4 ? blocks : 152LL * 8 * 4);
+  topp_mask_kernel<DT><<<grid, 256, 0, st>>>(P, mt, md);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topp(const Params& P, void* masked_target, void* masked_draft,
+                        cudaStream_t st) {
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  e = prepare_device(device);
+  if (e != cudaSuccess) return e;
+  return P.dtype == 0 ? launch_topp_kernels<0>(P, masked_target, masked_draft, st)
+                      : launch_topp_kernels<1>(P, masked_target, masked_draft, st);
+}
+
+__global__ void fill_int_kernel(int* p, long long n, int v) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    p[i] = v;
+}
+
+cudaError_t fill_int(int* p, long long n, int v, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const long long blocks = (n + 255) / 256;
+  fill_int_kernel<<<(unsigned)(blocks < 1024 ? blocks : 1024), 256, 0, st>>>(p, n, v);
   return cudaGetLastError();
 }
 

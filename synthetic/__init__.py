@@ -7,7 +7,8 @@ fed from here, and neither imports the other.
 """
 
 from .configs import WORKLOADS, SWEEP_K, SWEEP_NOISE, Workload, sweep_workload, get_workload
-from .generate import make_inputs, make_sequence, make_topk_inputs, topk_draft_tokens, DTYPES
+from .generate import (DTYPES, make_inputs, make_sequence, make_topk_inputs, make_topp_inputs,
+                       topk_draft_tokens, topp_draft_tokens)
 
 __all__ = [
     "WORKLOADS",
@@ -20,5 +21,7 @@ __all__ = [
     "make_sequence",
     "make_topk_inputs",
     "topk_draft_tokens",
+    "make_topp_inputs",
+    "topp_draft_tokens",
     "DTYPES",
 ]

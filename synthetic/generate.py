@@ -125,3 +125,32 @@ def make_topk_inputs(w: Workload, top_k: int, step: int = 0, seqs=None, pin_memo
         inp["tokens"][i] = topk_draft_tokens(inp["draft"][i], top_k, w.temperature,
                                              _gen(w, step, b, 3))
     return inp
+
+
+def topp_draft_tokens(draft: torch.Tensor, top_p: float, temperature: float,
+                      g: torch.Generator) -> torch.Tensor:
+    """Drafts for nucleus decoding: x_t drawn (Gumbel-max) from softmax(dl[t]/T)
+    restricted to the shortest prefix of the draft row, in descending order,
+    whose probability reaches top_p (torch's sort; any order among equal
+    logits gives a valid draft)."""
+    rows = draft.reshape(-1, draft.shape[-1]).to(torch.float64)
+    if top_p < 1.0:
+        q = torch.softmax(rows / float(temperature), dim=-1)
+        vals, order = torch.sort(q, dim=-1, descending=True)
+        csum = torch.cumsum(vals, dim=-1)
+        n_keep = (csum < top_p).sum(dim=-1, keepdim=True) + 1
+        pos = torch.arange(rows.shape[-1]).expand_as(order)
+        keep = torch.zeros_like(rows, dtype=torch.bool).scatter_(-1, order, pos < n_keep)
+        rows = torch.where(keep, rows, torch.full_like(rows, float("-inf")))
+    return gumbel_max_draw(rows, temperature, g).reshape(draft.shape[:-1])
+
+
+def make_topp_inputs(w: Workload, top_p: float, step: int = 0, seqs=None, pin_memory: bool = False):
+    """`make_inputs` with drafts drawn from the nucleus filtered draft rows (a
+    fifth per-sequence stream), as a nucleus decoding draft model would."""
+    inp = make_inputs(w, step=step, seqs=seqs, pin_memory=pin_memory)
+    idx = list(range(w.B)) if seqs is None else list(seqs)
+    for i, b in enumerate(idx):
+        inp["tokens"][i] = topp_draft_tokens(inp["draft"][i], top_p, w.temperature,
+                                             _gen(w, step, b, 4))
+    return inp

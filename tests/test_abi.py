@@ -176,3 +176,25 @@ def test_topk_workspace_and_validation(lib):
     # top_k >= V takes the unfiltered entry point, with its own checks.
     assert call(k=5000, wsb=16) == 6 and call(k=5000, T=-1.0) == 3
     assert call(B=0, t=0, d=0, tok=0, u=0) == 0
+
+
+def test_topp_workspace_and_validation(lib):
+    full = lib.sv_workspace_size(8, 4, 32000, sv.SV_BF16)
+    assert lib.sv_topp_workspace_size(8, 4, 32000, sv.SV_BF16) > full + 8 * 9 * 32000 * 2
+    for bad in ((-1, 4, 10, 0), (1, 0, 10, 0), (1, 65, 10, 0), (1, 4, 0, 0), (1, 4, 10, 7)):
+        assert lib.sv_topp_workspace_size(*bad) == 0
+    vp = ctypes.c_void_p
+
+    def call(t=1 << 20, d=1 << 20, tok=1 << 20, u=1 << 20, B=2, K=3, V=1000, dtype=sv.SV_F32,
+             T=1.0, p=0.9, out=1 << 20, nacc=1 << 20, kept=None, ws=1 << 20, wsb=1 << 30):
+        return lib.spec_verify_topp(vp(t), vp(d), vp(tok), vp(u), B, K, V, dtype, ctypes.c_float(T),
+                                    ctypes.c_float(p), vp(out), vp(nacc), vp(kept), vp(ws), wsb, None)
+
+    assert call(dtype=3) == 4
+    assert call(p=0.0) == 2 and call(p=-1.0) == 2 and call(p=float("nan")) == 2
+    assert call(K=0) == 2 and call(B=-1) == 2
+    assert call(T=0.0) == 3
+    assert call(t=0) == 1 and call(d=0) == 1 and call(ws=0) == 1
+    assert call(t=(1 << 20) + 2) == 5 and call(kept=(1 << 20) + 2) == 5
+    assert call(wsb=lib.sv_workspace_size(2, 3, 1000, sv.SV_F32)) == 6
+    assert call(B=0, t=0, d=0, tok=0, u=0) == 0
