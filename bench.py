@@ -35,7 +35,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import get_workload, make_inputs, make_topk_inputs  # noqa: E402
+from synthetic import get_workload, make_inputs, make_topk_inputs, make_topp_inputs  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "verified draft positions/sec (and achieved HBM GB/s, % of GB300 peak)"
@@ -51,12 +51,15 @@ def parse():
     ap.add_argument("--config", default="c2", help="c1..c4 or sweep-k{K}-n{noise}")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["verify", "draft_sample", "greedy", "topk"], default="verify",
+    ap.add_argument("--op", choices=["verify", "draft_sample", "greedy", "topk", "topp"],
+                    default="verify",
                     help="verify: the verification step (default); draft_sample: the draft-side "
                          "sampler over every draft row of the workload; greedy: greedy-mode "
                          "verification of the workload's target rows; topk: verification on "
-                         "top-k filtered distributions (--top-k)")
+                         "top-k filtered distributions (--top-k); topp: verification on nucleus "
+                         "filtered distributions (--top-p)")
     ap.add_argument("--top-k", type=int, default=50)
+    ap.add_argument("--top-p", type=float, default=0.9)
     return ap.parse_args()
 
 
@@ -730,45 +733,64 @@ def run_greedy(args, w, world, rank, local):
     }), flush=True)
 
 
-def run_topk_reference(args, w, world, rank):
+def _filter_mode(args, w):
+    """(label, input maker, oracle call, workload suffix) of --op topk / topp.
+    The oracle is imported only when its call runs (the CPU baseline and the
+    reference arm)."""
+
+    def ref(*a):
+        import oracle
+
+        if args.op == "topk":
+            return oracle.verify_topk(*a, w.temperature, args.top_k)
+        return oracle.verify_topp(*a, w.temperature, args.top_p)
+
+    if args.op == "topk":
+        kk = args.top_k
+        return f"top-{kk}", lambda step: make_topk_inputs(w, kk, step=step), ref, f"-top{kk}"
+    pp = args.top_p
+    return f"top-p {pp:g}", lambda step: make_topp_inputs(w, pp, step=step), ref, f"-topp{pp:g}"
+
+
+def run_filter_reference(args, w, world, rank):
     if rank != 0:
         return
-    import oracle
-
-    kk = args.top_k
+    label, make, ref, suffix = _filter_mode(args, w)
     steps = max(1, args.steps)
-    sets = [make_topk_inputs(w, kk, step=70_000 + i) for i in range(min(2, steps))]
+    sets = [make(70_000 + i) for i in range(min(2, steps))]
     wide = [tuple(s[x].to(torch.float64).numpy() for x in ("target", "draft"))
             + (s["tokens"].numpy(), s["uniforms"].to(torch.float64).numpy()) for s in sets]
     for i in range(args.warmup):
-        oracle.verify_topk(*wide[i % len(wide)], w.temperature, kk)
+        ref(*wide[i % len(wide)])
     t0 = time.perf_counter()
     for i in range(steps):
-        oracle.verify_topk(*wide[i % len(wide)], w.temperature, kk)
+        ref(*wide[i % len(wide)])
     dt = time.perf_counter() - t0
     value = steps * w.B * w.K / dt
     print(json.dumps({
-        "impl": "reference", "op": "topk", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "op": args.op, "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
         "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name}-top{kk}", "detail": w.describe()},
+        "config": {"workload": w.name + suffix, "detail": w.describe()},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{steps} top-{kk} steps of {w.name} (fp64 numpy oracle, 1 thread)"},
+                         "sample": f"{steps} {label} steps of {w.name} (fp64 numpy oracle, 1 thread)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
-def run_topk(args, w, world, rank, local):
-    """A step is one spec_verify_topk call over the B sequences of one step of
-    the workload: the row selection kernel over all 2K+1 rows, then the
-    verification kernel on the kept entries."""
+def run_filter(args, w, world, rank, local):
+    """A step is one filtered verification call over the B sequences of one
+    step of the workload. topk: the row selection kernel over all 2K+1 rows,
+    then the verification kernel on the kept entries. topp: the per-row cut
+    kernel, the masked copies, then the unfiltered verification kernels."""
     import speculative_sampling_verification_gb300 as sv
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sv.load_library(build=True)
-    kk = args.top_k
+    label, make, ref, suffix = _filter_mode(args, w)
+    kk, pp = args.top_k, args.top_p
     B, K, V, es = w.B, w.K, w.V, w.elem_bytes
     dt_code = sv.SV_BF16 if w.dtype == "bf16" else sv.SV_F32
     set_bytes = B * (2 * K + 1) * V * es
@@ -776,21 +798,31 @@ def run_topk(args, w, world, rank, local):
     names = ("target", "draft", "tokens", "uniforms")
     host = []
     for i in range(n_sets):
-        inp = make_topk_inputs(w, kk, step=80_000 + 1000 * rank + i)
+        inp = make(80_000 + 1000 * rank + i)
         host.append(tuple(inp[x].pin_memory() for x in names))
     sets = [tuple(t.to(dev) for t in h) for h in host]
     outs = [(torch.empty(B, K + 1, dtype=torch.int32, device=dev),
              torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
-    ws = torch.empty(max(256, sv.sv_topk_workspace_size(B, K, V, dt_code, kk)), dtype=torch.uint8,
-                     device=dev)
+    if args.op == "topk":
+        ws_bytes = sv.sv_topk_workspace_size(B, K, V, dt_code, kk)
+        launches = 2
+        kernel = "topk_select_kernel + topk_verify_kernel (call time)"
+    else:
+        ws_bytes = sv.sv_topp_workspace_size(B, K, V, dt_code)
+        launches = 2 + sv.sv_kernels_per_call(B, K, V, dt_code)
+        kernel = "topp_cut_kernel + topp_mask_kernel + the verification kernels (call time)"
+    ws = torch.empty(max(256, ws_bytes), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
 
     def call(i, tensors=None, o=None):
         t = tensors or sets[i % n_sets]
         o = o or outs[i % n_sets]
-        rc = sv.spec_verify_topk(*t, w.temperature, kk, o[0], o[1], ws, stream=stream)
+        if args.op == "topk":
+            rc = sv.spec_verify_topk(*t, w.temperature, kk, o[0], o[1], ws, stream=stream)
+        else:
+            rc = sv.spec_verify_topp(*t, w.temperature, pp, o[0], o[1], ws, stream=stream)
         if rc != 0:
-            raise RuntimeError(f"spec_verify_topk failed: {sv.sv_status_string(rc)}")
+            raise RuntimeError(f"{args.op} call failed: {sv.sv_status_string(rc)}")
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -867,29 +899,30 @@ def run_topk(args, w, world, rank, local):
                 h[3].to(torch.float64).numpy()) for h in host[:2]]
         t0, n = time.perf_counter(), 0
         while time.perf_counter() - t0 < 12.0 and n < 5000:
-            oracle.verify_topk(*wide[n % len(wide)], w.temperature, kk)
+            ref(*wide[n % len(wide)])
             n += 1
         dt = time.perf_counter() - t0
         cpu = {"value": n * B * K / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} top-{kk} steps of {w.name} in {dt:.1f} s (fp64 numpy oracle, 1 thread)"}
+               "sample": f"{n} {label} steps of {w.name} in {dt:.1f} s (fp64 numpy oracle, 1 thread)"}
     in_bytes = sum(t.numel() * t.element_size() for t in host[0])
     print(json.dumps({
-        "op": "topk", "metric": METRIC, "value": aggregate(B * K, world, per_step_s),
+        "op": args.op, "metric": METRIC, "value": aggregate(B * K, world, per_step_s),
         "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warmup,
         "ms_per_step": per_step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": f"{w.name}-top{kk}", "detail": w.describe(), "top_k": kk,
+        "config": {"workload": w.name + suffix, "detail": w.describe(),
+                   ("top_k" if args.op == "topk" else "top_p"): kk if args.op == "topk" else pp,
                    "l2": f"inputs rotate over {n_sets} resident sets of {set_bytes / 1e6:.1f} MB",
                    "timing": "K calls in one CUDA graph, CUDA events on the launching stream"},
-        "roofline": {"bound": "hbm", "kernel": "topk_select_kernel + topk_verify_kernel (call time)",
+        "roofline": {"bound": "hbm", "kernel": kernel,
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
                      "bytes_per_launch": set_bytes, "ms_per_launch": per_step_s * 1e3,
-                     "bytes_basis": "B(2K+1) rows of V elements, once (both kernels' time)"},
+                     "bytes_basis": "B(2K+1) rows of V elements, once (the whole call's time)"},
         "e2e": {"value": aggregate(B * K * e2e_steps, world, e2e_s), "unit": UNIT,
                 "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 * B * (K + 2),
                 "steps": e2e_steps},
-        "gpu_launches": steps * 2,
+        "gpu_launches": steps * launches,
         "clocks": clocks.summary(t_wall0, t_wall1),
         "cpu_baseline": cpu,
     }), flush=True)
@@ -910,11 +943,11 @@ def main():
                 run_greedy_reference(args, w, world, rank)
             else:
                 run_greedy(args, w, world, rank, local)
-        elif args.op == "topk":
+        elif args.op in ("topk", "topp"):
             if args.impl == "reference":
-                run_topk_reference(args, w, world, rank)
+                run_filter_reference(args, w, world, rank)
             else:
-                run_topk(args, w, world, rank, local)
+                run_filter(args, w, world, rank, local)
         elif args.impl == "reference":
             run_reference(args, w, world, rank)
         else:

@@ -427,7 +427,9 @@ int spec_verify_topp(const void* target_logits, const void* draft_logits,
   P.topp_kept = kept_counts;
   void* mt = ws + TL.off_mt;
   void* md = ws + TL.off_md;
-  if (sv::launch_topp(P, mt, md, st) != cudaSuccess) return SV_ERR_CUDA;
+  const bool aligned = !misaligned(target_logits, 16) && !misaligned(draft_logits, 16) &&
+                       ((size_t)V * TL.L.es) % 16 == 0;
+  if (sv::launch_topp(P, aligned, mt, md, st) != cudaSuccess) return SV_ERR_CUDA;
   return run(mt, md, draft_tokens, uniforms, B, K, V, dtype, temperature, out_tokens, n_accepted,
              workspace, workspace_bytes, stream, nullptr, nullptr, nullptr);
 }

@@ -215,7 +215,7 @@ cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t stream);
 cudaError_t launch_topk(const Params& P, bool aligned, cudaStream_t stream);
 // Nucleus filtering: the per-row cut kernel, then the masked copies of the
 // target and draft rows (the verification then runs on the copies).
-cudaError_t launch_topp(const Params& P, void* masked_target, void* masked_draft,
+cudaError_t launch_topp(const Params& P, bool aligned, void* masked_target, void* masked_draft,
                         cudaStream_t stream);
 cudaError_t fill_int(int* p, long long n, int v, cudaStream_t stream);
 // Kernels one call over B sequences of rows_per_seq rows of V elements of

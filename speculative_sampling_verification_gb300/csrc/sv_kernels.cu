@@ -1983,7 +1983,7 @@ SV_DEVINL TpElem tp_elem(float l, float m, const Params& P, const float2* tab) {
 // Level-L bin of d: floor(d * 4^(2L-3)) (width 4 at L = 1, /16 per level).
 SV_DEVINL float tp_scale(int level) { return ldexpf(1.0f, 4 * level - 6); }
 
-template <int DT>
+template <int DT, bool VEC>
 __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
   extern __shared__ __align__(16) unsigned char tp_smem[];
   TopPShared& sh = *reinterpret_cast<TopPShared*>(tp_smem);
@@ -2003,7 +2003,7 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
     for (unsigned t = 0; t < ntiles; ++t) {
       uint32_t w[SelWords<DT>::n];
       const unsigned e0 = t * kSelTile + tid * 8;
-      const int nv = load_sel_tile<DT, false>(rb, (long long)e0, V, w);
+      const int nv = load_sel_tile<DT, VEC>(rb, (long long)e0, V, w);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         if (j < nv) fn(elem_bits<DT>(w, j), e0 + j);
@@ -2032,6 +2032,7 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
     return;
   }
   double target = 0.0, above = 0.0;
+  unsigned count_above = 0;  // entries in the bins above the cut bin, over the levels
   unsigned long long cut = 0;
   int level = 1;
   long long parent = 0;  // the bin, at level - 1, that holds the cut
@@ -2102,6 +2103,7 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
       a -= sh.binmass[last];
     }
     above = a;
+    for (int b = 0; b < bstar; ++b) count_above += sh.bincount[b];
     const unsigned count = sh.bincount[bstar];
     parent = (level > 1 ? 16 * parent : 0) + bstar;
     if (level == 1 && bstar == kTpBins - 1) {  // d >= 60: left to the per-bit path
@@ -2192,6 +2194,19 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
     }
     __syncthreads();
     cut = sh.cutmin;
+    // Kept: the entries above the cut bin, and the candidates at or above K*.
+    unsigned c = 0;
+    for (unsigned i = tid; i < n; i += kTpThreads) c += sh.ckey[i] >= cut ? 1u : 0u;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) sh.ch[warp] = c;
+    __syncthreads();
+    if (tid == 0) {
+      unsigned tot = count_above;
+      for (int w2 = 0; w2 < kTpThreads / 32; ++w2) tot += sh.ch[w2];
+      P.topp_cut[row] = cut;
+      if (P.topp_kept) P.topp_kept[row] = (int)tot;
+    }
+    return;
   } else {
     // Heavy ties around the cut: bit by bit over the key, one pass per bit,
     // with the exact mass of the keys at or above the trial cut.
@@ -2206,7 +2221,7 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
     }
     cut = x;
   }
-  // The kept count, for the caller.
+  // The kept count, for the caller (a pass over the row on this path).
   unsigned kept = 0;
   for_each([&](uint32_t b, unsigned i) { kept += key_of(b, i) >= cut ? 1u : 0u; });
   kept = __reduce_add_sync(0xffffffffu, kept);
@@ -2222,30 +2237,51 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
 }
 
 // The masked copies: every element of the 2K+1 rows whose key is below its
-// row's cut becomes -inf; the others are copied.
-template <int DT>
+// row's cut becomes -inf; the others are copied. blockIdx.y strides over the
+// rows, blockIdx.x over chunks of 8 elements per thread; VEC moves the 8 as
+// 16-byte words (the rows and the copies 16-byte aligned).
+template <int DT, bool VEC>
 __global__ void __launch_bounds__(256) topp_mask_kernel(Params P, void* masked_target,
                                                         void* masked_draft) {
   using E = typename std::conditional<DT == 0, unsigned short, uint32_t>::type;
+  constexpr int W = SelWords<DT>::n;
   const long long rows = (long long)P.B * P.rows_per_seq;
-  const long long n = rows * P.V;
-  const int ib = P.key_ibits;
+  const int V = P.V, ib = P.key_ibits;
   const E kNegInf = DT == 0 ? (E)0xff80u : (E)0xff800000u;
-  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n;
-       g += (long long)gridDim.x * blockDim.x) {
-    const long long row = g / P.V;
-    const int i = (int)(g - row * P.V);
+  const unsigned e0 = (blockIdx.x * 256 + threadIdx.x) * 8;
+  if (e0 >= (unsigned)V) return;
+  for (long long row = blockIdx.y; row < rows; row += gridDim.y) {
     const long long b = row / P.rows_per_seq;
     const int r = (int)(row % P.rows_per_seq);
-    const E* src = reinterpret_cast<const E*>(row_base(P, b, r));
+    const unsigned char* src = row_base(P, b, r);
     E* dst = r <= P.K
-                 ? reinterpret_cast<E*>(masked_target) + ((size_t)b * (P.K + 1) + r) * (size_t)P.V
-                 : reinterpret_cast<E*>(masked_draft) +
-                       ((size_t)b * P.K + (r - P.K - 1)) * (size_t)P.V;
-    const E v = src[i];
-    const unsigned long long key =
-        ((unsigned long long)value_key<DT>((uint32_t)v) << ib) | (unsigned long long)(P.V - 1 - i);
-    dst[i] = key >= P.topp_cut[row] ? v : kNegInf;
+                 ? reinterpret_cast<E*>(masked_target) + ((size_t)b * (P.K + 1) + r) * (size_t)V
+                 : reinterpret_cast<E*>(masked_draft) + ((size_t)b * P.K + (r - P.K - 1)) * (size_t)V;
+    const unsigned long long cut = __ldg(P.topp_cut + row);
+    uint32_t w[W];
+    const int nv = load_sel_tile<DT, VEC>(src, (long long)e0, V, w);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t bits = elem_bits<DT>(w, j);
+      const unsigned long long key =
+          ((unsigned long long)value_key<DT>(bits) << ib) | (unsigned long long)(V - 1 - (int)(e0 + j));
+      const uint32_t out = key >= cut ? bits : (uint32_t)kNegInf;
+      if constexpr (DT == 0)
+        w[j >> 1] = (w[j >> 1] & ((j & 1) ? 0x0000ffffu : 0xffff0000u)) | (out << ((j & 1) * 16));
+      else
+        w[j] = out;
+    }
+    if (VEC && nv == 8) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + e0);
+      if constexpr (DT == 0) {
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    } else {
+      for (int j = 0; j < nv; ++j) dst[e0 + j] = (E)elem_bits<DT>(w, j);
+    }
   }
 }
 
@@ -2388,32 +2424,34 @@ cudaError_t launch_topk(const Params& P, bool aligned, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int DT>
+template <int DT, bool VEC>
 static cudaError_t launch_topp_kernels(const Params& P, void* mt, void* md, cudaStream_t st) {
   const size_t smem = sizeof(TopPShared);
-  cudaError_t e = cudaFuncSetAttribute(topp_cut_kernel<DT>,
+  cudaError_t e = cudaFuncSetAttribute(topp_cut_kernel<DT, VEC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned rows = (unsigned)((long long)P.B * P.rows_per_seq);
-  topp_cut_kernel<DT><<<rows, kTpThreads, smem, st>>>(P);
+  const long long rows = (long long)P.B * P.rows_per_seq;
+  topp_cut_kernel<DT, VEC><<<(unsigned)rows, kTpThreads, smem, st>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long n = (long long)rows * P.V;
-  const long long blocks = (n + 255) / 256;
-  const unsigned grid = (unsigned)(blocks < 152LL * 8 * 4 ? blocks : 152LL * 8 * 4);
-  topp_mask_kernel<DT><<<grid, 256, 0, st>>>(P, mt, md);
+  const dim3 grid((unsigned)(((long long)P.V + 2047) / 2048),
+                  (unsigned)(rows < 65535 ? rows : 65535));
+  topp_mask_kernel<DT, VEC><<<grid, 256, 0, st>>>(P, mt, md);
   return cudaGetLastError();
 }
 
-cudaError_t launch_topp(const Params& P, void* masked_target, void* masked_draft,
+cudaError_t launch_topp(const Params& P, bool aligned, void* masked_target, void* masked_draft,
                         cudaStream_t st) {
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   e = prepare_device(device);
   if (e != cudaSuccess) return e;
-  return P.dtype == 0 ? launch_topp_kernels<0>(P, masked_target, masked_draft, st)
-                      : launch_topp_kernels<1>(P, masked_target, masked_draft, st);
+  if (P.dtype == 0)
+    return aligned ? launch_topp_kernels<0, true>(P, masked_target, masked_draft, st)
+                   : launch_topp_kernels<0, false>(P, masked_target, masked_draft, st);
+  return aligned ? launch_topp_kernels<1, true>(P, masked_target, masked_draft, st)
+                 : launch_topp_kernels<1, false>(P, masked_target, masked_draft, st);
 }
 
 __global__ void fill_int_kernel(int* p, long long n, int v) {
