@@ -422,6 +422,7 @@ int spec_verify_topp(const void* target_logits, const void* draft_logits,
   while (ib < 31 && ((long long)(V - 1) >> ib) != 0) ++ib;
   P.key_ibits = ib;
   P.top_p = top_p;
+  P.temp_d = (double)temperature;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   P.topp_cut = reinterpret_cast<unsigned long long*>(ws + TL.off_cut);
   P.topp_kept = kept_counts;

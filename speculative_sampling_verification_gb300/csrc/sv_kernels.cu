@@ -1942,19 +1942,27 @@ constexpr int kTpMaxLevels = 6;
 
 struct TopPShared {
   float2 tab[256];
-  float bhi[kTpBins][kTpThreads], blo[kTpBins][kTpThreads];  // per-thread bin masses (ff)
-  unsigned bcnt[kTpBins][kTpThreads];                       // per-thread bin counts
-  unsigned long long ckey[kTpCap];
-  double cw[kTpCap];
-  double mh[256];
-  unsigned ch[256];
+  union {
+    struct {  // level histograms: per-thread float-float masses and counts
+      float bhi[kTpBins][kTpThreads], blo[kTpBins][kTpThreads];
+      unsigned bcnt[kTpBins][kTpThreads];
+    } lv;
+    struct {  // the cut bin's entries, and the mass-weighted radix select over them
+      unsigned long long ckey[kTpCap];
+      double cw[kTpCap];
+      double mh[256];
+      unsigned ch[256];
+    } rs;
+  } u;
   double red[kTpThreads / 32];
+  double wsum[kTpThreads / 32];
   double binmass[kTpBins];
   unsigned bincount[kTpBins];
-  unsigned n_cand;
-  unsigned long long prefix, cutmin;
-  double above;
-  int found;
+  unsigned n_cand, wcnt[kTpThreads / 32];
+  unsigned long long cutmin, prefix;
+  int sel;
+  double sel_above;
+  unsigned sel_count;
 };
 
 SV_DEVINL double tp_block_sum(TopPShared& sh, double v) {
@@ -1969,54 +1977,60 @@ SV_DEVINL double tp_block_sum(TopPShared& sh, double v) {
   return r;
 }
 
-// d = (m - l) / T and the float-float weight exp(-(d)) of one element.
-struct TpElem {
-  float d;
-  ff w;
-};
+// Level-L bins of d have width 16^-(L-1): index floor(d * 16^(L-1)) (exact:
+// the product is a power-of-two scaling), clamped far above any real index.
+SV_DEVINL float tp_scale(int level) { return ldexpf(1.0f, 4 * (level - 1)); }
+SV_DEVINL long long tp_index(float d, float sc) { return (long long)floorf(fminf(d * sc, 1e15f)); }
 
-SV_DEVINL TpElem tp_elem(float l, float m, const Params& P, const float2* tab) {
-  const ff x = scaled_diff(l, m, P.ih, P.il, P.unit_t != 0);
-  return {-x.hi, exp_ff(x.hi, x.lo, tab)};
+template <int DT>
+SV_DEVINL float tp_float(uint32_t b) { return __uint_as_float(DT == 0 ? b << 16 : b); }
+
+// Element j of a tile's words, selected without indexing the array at run time.
+template <int DT>
+SV_DEVINL uint32_t tp_pick(const uint32_t (&w)[SelWords<DT>::n], int j) {
+  uint32_t r = elem_bits<DT>(w, 0);
+#pragma unroll
+  for (int k = 1; k < 8; ++k) r = j == k ? elem_bits<DT>(w, k) : r;
+  return r;
 }
 
-// Level-L bin of d: floor(d * 4^(2L-3)) (width 4 at L = 1, /16 per level).
-SV_DEVINL float tp_scale(int level) { return ldexpf(1.0f, 4 * level - 6); }
-
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
+__global__ void __launch_bounds__(kTpThreads, 3) topp_cut_kernel(Params P) {
   extern __shared__ __align__(16) unsigned char tp_smem[];
   TopPShared& sh = *reinterpret_cast<TopPShared*>(tp_smem);
+  constexpr int W = SelWords<DT>::n;
+  constexpr int NB = DT == 0 ? 16 : 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long row = blockIdx.x;
   const unsigned char* rb = row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
   const int V = P.V, ib = P.key_ibits;
-  constexpr int NB = DT == 0 ? 16 : 32;
   const int bits = NB + ib;
+  const bool unit_t = P.unit_t != 0;
   sh.tab[tid] = kSvExp2Table[tid];
   const unsigned ntiles = (unsigned)(((long long)V + kSelTile - 1) / kSelTile);
   auto key_of = [&](uint32_t b, unsigned i) -> unsigned long long {
     return ((unsigned long long)value_key<DT>(b) << ib) | (unsigned long long)(V - 1 - (int)i);
   };
-  // Visit every element of the row (8 consecutive per thread per tile).
-  auto for_each = [&](auto&& fn) {
-    for (unsigned t = 0; t < ntiles; ++t) {
-      uint32_t w[SelWords<DT>::n];
-      const unsigned e0 = t * kSelTile + tid * 8;
-      const int nv = load_sel_tile<DT, VEC>(rb, (long long)e0, V, w);
+  // Visit the row 4 tiles at a time (4 loads in flight per thread); fn(w, nv,
+  // e0) gets one tile's words, its valid count and its first element.
+  auto for_tiles = [&](auto&& fn) {
+    for (unsigned t = 0; t < ntiles; t += 4) {
+      uint32_t w[4][W];
+      int nv[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < nv) fn(elem_bits<DT>(w, j), e0 + j);
+      for (int u = 0; u < 4; ++u)
+        nv[u] = load_sel_tile<DT, VEC>(rb, (long long)(t + u) * kSelTile + tid * 8, V, w[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) fn(w[u], nv[u], (t + u) * kSelTile + tid * 8);
     }
   };
-  auto to_float = [](uint32_t b) { return __uint_as_float(DT == 0 ? b << 16 : b); };
-  // 1. The maximum, and NaN / +inf.
-  float m = -CUDART_INF_F;
-  bool bad = false;
-  for_each([&](uint32_t b, unsigned) {
-    bad |= nan_or_pos_inf<DT>(b);
-    m = fmaxf(m, to_float(b));
+  // 1. The maximum, and NaN / +inf (NaN-propagating packed maxima).
+  float mf = -CUDART_INF_F;
+  for_tiles([&](const uint32_t (&w)[W], int, unsigned) {
+    mf = fmax_nan(mf, tp_float<DT>(sel_max_bits<DT>(w)));
   });
+  bool bad = isnan(mf) || mf == CUDART_INF_F;
+  float m = mf;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (lane == 0) sh.red[warp] = m;
@@ -2031,35 +2045,81 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
     }
     return;
   }
+  // Entries of the bin `parent` at scale sc: index(d) == parent (>= parent
+  // for an open bin, the last bin of a level holding everything below), with
+  // d = (m - l) / T, i.e. l in (m - T (parent+1)/sc, m - T parent/sc]. A
+  // widened value window screens elements before the exact test.
+  auto window = [&](float sc, long long parent, bool open, float& lo, float& hi) {
+    const double T = P.temp_d;
+    const double a = (double)m - T * (double)(parent + 1) / (double)sc;
+    const double b = (double)m - T * (double)parent / (double)sc;
+    const double slack = (fabs((double)m) + T * (double)(parent + 1) / (double)sc) * 1e-5 + 1e-30;
+    lo = open ? -CUDART_INF_F : (float)(a - slack);
+    hi = (float)(b + slack);
+  };
+  auto member = [&](float d, float sc, long long parent, bool open) {
+    const long long i = tp_index(d, sc);
+    return open ? i >= parent : i == parent;
+  };
   double target = 0.0, above = 0.0;
   unsigned count_above = 0;  // entries in the bins above the cut bin, over the levels
   unsigned long long cut = 0;
   int level = 1;
   long long parent = 0;  // the bin, at level - 1, that holds the cut
+  bool open = false;     // that bin is the open last bin of its level
   bool gathered = false;
   for (; level <= kTpMaxLevels; ++level) {
     const float sc = tp_scale(level), psc = tp_scale(level - 1);
 #pragma unroll
     for (int b = 0; b < kTpBins; ++b) {
-      sh.bhi[b][tid] = 0.0f;
-      sh.blo[b][tid] = 0.0f;
-      sh.bcnt[b][tid] = 0;
+      sh.u.lv.bhi[b][tid] = 0.0f;
+      sh.u.lv.blo[b][tid] = 0.0f;
+      sh.u.lv.bcnt[b][tid] = 0;
     }
-    ff total = {0.0f, 0.0f};
-    for_each([&](uint32_t b, unsigned) {
-      const float l = to_float(b);
-      const float d = -scaled_diff(l, m, P.ih, P.il, P.unit_t != 0).hi;
-      if (level > 1 && floorf(d * psc) != (float)parent) return;
-      const TpElem e = tp_elem(l, m, P, sh.tab);
-      const float r = fminf(floorf(d * sc) - (level > 1 ? 16.0f * (float)parent : 0.0f), 15.0f);
-      const int bin = (int)r;
-      ff acc = {sh.bhi[bin][tid], sh.blo[bin][tid]};
-      ff_accumulate(acc, e.w);
-      sh.bhi[bin][tid] = acc.hi;
-      sh.blo[bin][tid] = acc.lo;
-      sh.bcnt[bin][tid] += 1;
-      if (level == 1) ff_accumulate(total, e.w);
-    });
+    auto add = [&](float d, ff wt) {
+      const long long r = tp_index(d, sc) - (level > 1 ? 16 * parent : 0);
+      const int bin = (int)(r < 15 ? r : 15);
+      ff acc = {sh.u.lv.bhi[bin][tid], sh.u.lv.blo[bin][tid]};
+      ff_accumulate(acc, wt);
+      sh.u.lv.bhi[bin][tid] = acc.hi;
+      sh.u.lv.blo[bin][tid] = acc.lo;
+      sh.u.lv.bcnt[bin][tid] += 1;
+    };
+    if (level == 1) {
+      // Every entry: the weights of element pairs with the packed (f32x2)
+      // exponential, lane for lane the same operations as exp_ff.
+      const float2 nm2 = make_float2(-m, -m);
+      for_tiles([&](const uint32_t (&w)[W], int nv, unsigned) {
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          const float2 l2 = make_float2(tp_float<DT>(elem_bits<DT>(w, j)),
+                                        tp_float<DT>(elem_bits<DT>(w, j + 1)));
+          const ff2 x = scaled_diff2(l2, nm2, P.ih, P.il, unit_t);
+          const ff2 wt = exp_ff2(x.hi, x.lo, sh.tab);
+          if (j < nv) add(-x.hi.x, ff{wt.hi.x, wt.lo.x});
+          if (j + 1 < nv) add(-x.hi.y, ff{wt.hi.y, wt.lo.y});
+        }
+      });
+    } else {
+      float lo, hi;
+      window(psc, parent, open, lo, hi);
+      for_tiles([&](const uint32_t (&w)[W], int nv, unsigned) {
+        unsigned cand = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float l = tp_float<DT>(elem_bits<DT>(w, j));
+          if (j < nv && l >= lo && l <= hi) cand |= 1u << j;
+        }
+        while (cand) {
+          const int j = __ffs(cand) - 1;
+          cand &= cand - 1;
+          const ff x = scaled_diff(tp_float<DT>(tp_pick<DT>(w, j)), m, P.ih, P.il, unit_t);
+          const float d = -x.hi;
+          if (!member(d, psc, parent, open)) continue;
+          add(d, exp_ff(x.hi, x.lo, sh.tab));
+        }
+      });
+    }
     __syncthreads();
     // Bin totals: warp w sums bins 2w and 2w+1 over the threads.
 #pragma unroll
@@ -2068,8 +2128,8 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
       double s = 0.0;
       unsigned c = 0;
       for (int t = lane; t < kTpThreads; t += 32) {
-        s += (double)sh.bhi[b][t] + (double)sh.blo[b][t];
-        c += sh.bcnt[b][t];
+        s += (double)sh.u.lv.bhi[b][t] + (double)sh.u.lv.blo[b][t];
+        c += sh.u.lv.bcnt[b][t];
       }
       s = warp_sum_d(s);
       c = __reduce_add_sync(0xffffffffu, c);
@@ -2078,11 +2138,12 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
         sh.bincount[b] = c;
       }
     }
-    if (level == 1) {
-      const double S = tp_block_sum(sh, ff_to_double(total));
+    __syncthreads();
+    if (level == 1) {  // S: every entry is in one of the level-1 bins
+      double S = 0.0;
+      for (int b = 0; b < kTpBins; ++b) S += sh.binmass[b];
       target = (double)P.top_p * S;
     }
-    __syncthreads();
     // The bin where the running mass from the top reaches the target. If
     // rounding (the bins re-sum the parent bin in another order) leaves the
     // target just out of reach, the cut is at the end of the parent bin: its
@@ -2106,131 +2167,162 @@ __global__ void __launch_bounds__(kTpThreads) topp_cut_kernel(Params P) {
     for (int b = 0; b < bstar; ++b) count_above += sh.bincount[b];
     const unsigned count = sh.bincount[bstar];
     parent = (level > 1 ? 16 * parent : 0) + bstar;
-    if (level == 1 && bstar == kTpBins - 1) {  // d >= 60: left to the per-bit path
-      level = kTpMaxLevels + 1;
-      break;
-    }
+    open = bstar == kTpBins - 1 && (level == 1 || open);
+    __syncthreads();
     if (count <= (unsigned)kTpCap) {
       gathered = true;
       break;
     }
-    __syncthreads();
   }
   if (gathered) {
-    // 3. Gather the bin's entries with their weights.
+    // 3. Gather the bin's entries with their weights (the level histograms'
+    // memory is reused from here).
     const float sc = tp_scale(level);
     if (tid == 0) {
       sh.n_cand = 0;
       sh.cutmin = ~0ull;
     }
     __syncthreads();
-    for_each([&](uint32_t b, unsigned i) {
-      const float l = to_float(b);
-      const float d = -scaled_diff(l, m, P.ih, P.il, P.unit_t != 0).hi;
-      if (floorf(d * sc) != (float)parent) return;
-      const unsigned s = atomicAdd(&sh.n_cand, 1u);
-      if (s < (unsigned)kTpCap) {
-        sh.ckey[s] = key_of(b, i);
-        sh.cw[s] = ff_to_double(tp_elem(l, m, P, sh.tab).w);
+    float lo, hi;
+    window(sc, parent, open, lo, hi);
+    for_tiles([&](const uint32_t (&w)[W], int nv, unsigned e0) {
+      unsigned cand = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float l = tp_float<DT>(elem_bits<DT>(w, j));
+        if (j < nv && l >= lo && l <= hi) cand |= 1u << j;
+      }
+      while (cand) {
+        const int j = __ffs(cand) - 1;
+        cand &= cand - 1;
+        const uint32_t b = tp_pick<DT>(w, j);
+        const ff x = scaled_diff(tp_float<DT>(b), m, P.ih, P.il, unit_t);
+        if (!member(-x.hi, sc, parent, open)) continue;
+        const unsigned s = atomicAdd(&sh.n_cand, 1u);
+        if (s < (unsigned)kTpCap) {
+          sh.u.rs.ckey[s] = key_of(b, e0 + j);
+          sh.u.rs.cw[s] = ff_to_double(exp_ff(x.hi, x.lo, sh.tab));
+        }
       }
     });
     __syncthreads();
     const unsigned n = min(sh.n_cand, (unsigned)kTpCap);
     // Radix select over the candidates' keys, 8-bit digits from the top,
     // weighted by mass: the largest key K* with above + mass(key >= K*) >=
-    // target.
+    // target. Thread t holds bin 255 - t; an fp64 scan over the threads gives
+    // the mass at or above each bin.
     const int pad = (8 - bits % 8) % 8, top = bits + pad;
     unsigned long long prefix = 0;
     double abv = above;
     int resolved = 0;
     while (resolved < top) {
       const int shift = top - resolved - 8;
-      sh.mh[tid] = 0.0;
-      sh.ch[tid] = 0;
+      sh.u.rs.mh[tid] = 0.0;
+      sh.u.rs.ch[tid] = 0;
+      if (tid == 0) sh.sel = -1;
       __syncthreads();
       for (unsigned i = tid; i < n; i += kTpThreads) {
-        const unsigned long long k = sh.ckey[i] << pad;
+        const unsigned long long k = sh.u.rs.ckey[i] << pad;
         if (resolved == 0 || (k >> (shift + 8)) == (prefix >> (shift + 8))) {
           const unsigned bin = (unsigned)((k >> shift) & 255u);
-          atomicAdd(&sh.mh[bin], sh.cw[i]);
-          atomicAdd(&sh.ch[bin], 1u);
+          atomicAdd(&sh.u.rs.mh[bin], sh.u.rs.cw[i]);
+          atomicAdd(&sh.u.rs.ch[bin], 1u);
         }
       }
       __syncthreads();
-      if (tid == 0) {
-        // Bins from the top; sequential over 256 bins (one thread).
+      const double mk = sh.u.rs.mh[255 - tid];
+      const unsigned ck = sh.u.rs.ch[255 - tid];
+      double inc = mk;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) sh.wsum[warp] = inc;
+      __syncthreads();
+      for (int w2 = 0; w2 < warp; ++w2) inc += sh.wsum[w2];
+      if (ck > 0 && abv + inc >= target && abv + inc - mk < target) {
+        sh.sel = 255 - tid;
+        sh.sel_above = abv + inc - mk;
+        sh.sel_count = ck;
+      }
+      __syncthreads();
+      if (tid == 0 && sh.sel < 0) {
+        // Rounding: the target is just out of reach; the cut is the last key.
         double a2 = abv;
-        int sel = -1, last = -1;
+        int last = -1;
         for (int b = 255; b >= 0; --b) {
-          if (sh.ch[b] == 0) continue;
+          if (sh.u.rs.ch[b] == 0) continue;
           last = b;
-          if (a2 + sh.mh[b] >= target) {
-            sel = b;
-            break;
-          }
-          a2 += sh.mh[b];
+          a2 += sh.u.rs.mh[b];
         }
-        if (sel < 0 && last >= 0) {  // rounding: the cut is at the last key
-          sel = last;
-          a2 -= sh.mh[last];
+        if (last >= 0) {
+          sh.sel = last;
+          sh.sel_above = a2 - sh.u.rs.mh[last];
+          sh.sel_count = sh.u.rs.ch[last];
+        } else {
+          sh.sel_count = 0;
         }
-        sh.found = sel;
-        sh.above = a2;
-        sh.prefix = prefix | ((unsigned long long)(sel < 0 ? 0 : sel) << shift);
-        sh.n_cand = sel < 0 ? 0 : sh.ch[sel];
       }
       __syncthreads();
-      prefix = sh.prefix;
-      abv = sh.above;
+      const int sel = sh.sel;
+      prefix |= (unsigned long long)(sel < 0 ? 0 : sel) << shift;
+      abv = sh.sel_above;
       resolved += 8;
-      if (sh.n_cand <= 1) break;
+      if (sh.sel_count <= 1) break;
       __syncthreads();
     }
-    // The single key under the prefix (cutmin was set before the search).
-    const int lo = top - resolved;
+    // The single key under the prefix.
+    const int lo_bits = top - resolved;
     for (unsigned i = tid; i < n; i += kTpThreads) {
-      const unsigned long long k = sh.ckey[i] << pad;
-      if ((k >> lo) == (prefix >> lo)) atomicMin(&sh.cutmin, sh.ckey[i]);
+      const unsigned long long k = sh.u.rs.ckey[i] << pad;
+      if ((k >> lo_bits) == (prefix >> lo_bits)) atomicMin(&sh.cutmin, sh.u.rs.ckey[i]);
     }
     __syncthreads();
     cut = sh.cutmin;
     // Kept: the entries above the cut bin, and the candidates at or above K*.
     unsigned c = 0;
-    for (unsigned i = tid; i < n; i += kTpThreads) c += sh.ckey[i] >= cut ? 1u : 0u;
+    for (unsigned i = tid; i < n; i += kTpThreads) c += sh.u.rs.ckey[i] >= cut ? 1u : 0u;
     c = __reduce_add_sync(0xffffffffu, c);
-    if (lane == 0) sh.ch[warp] = c;
+    if (lane == 0) sh.wcnt[warp] = c;
     __syncthreads();
     if (tid == 0) {
       unsigned tot = count_above;
-      for (int w2 = 0; w2 < kTpThreads / 32; ++w2) tot += sh.ch[w2];
+      for (int w2 = 0; w2 < kTpThreads / 32; ++w2) tot += sh.wcnt[w2];
       P.topp_cut[row] = cut;
       if (P.topp_kept) P.topp_kept[row] = (int)tot;
     }
     return;
-  } else {
-    // Heavy ties around the cut: bit by bit over the key, one pass per bit,
-    // with the exact mass of the keys at or above the trial cut.
-    unsigned long long x = 0;
-    for (int bit = bits - 1; bit >= 0; --bit) {
-      const unsigned long long y = x | (1ull << bit);
-      ff part = {0.0f, 0.0f};
-      for_each([&](uint32_t b, unsigned i) {
-        if (key_of(b, i) >= y) ff_accumulate(part, tp_elem(to_float(b), m, P, sh.tab).w);
-      });
-      if (tp_block_sum(sh, ff_to_double(part)) >= target) x = y;
-    }
-    cut = x;
   }
+  // Heavy ties around the cut: bit by bit over the key, one pass per bit,
+  // with the exact mass of the keys at or above the trial cut.
+  unsigned long long x = 0;
+  for (int bit = bits - 1; bit >= 0; --bit) {
+    const unsigned long long y = x | (1ull << bit);
+    ff part = {0.0f, 0.0f};
+    for_tiles([&](const uint32_t (&w)[W], int nv, unsigned e0) {
+      for (int j = 0; j < nv; ++j) {
+        const uint32_t b = tp_pick<DT>(w, j);
+        if (key_of(b, e0 + j) >= y) {
+          const ff xx = scaled_diff(tp_float<DT>(b), m, P.ih, P.il, unit_t);
+          ff_accumulate(part, exp_ff(xx.hi, xx.lo, sh.tab));
+        }
+      }
+    });
+    if (tp_block_sum(sh, ff_to_double(part)) >= target) x = y;
+  }
+  cut = x;
   // The kept count, for the caller (a pass over the row on this path).
   unsigned kept = 0;
-  for_each([&](uint32_t b, unsigned i) { kept += key_of(b, i) >= cut ? 1u : 0u; });
+  for_tiles([&](const uint32_t (&w)[W], int nv, unsigned e0) {
+    for (int j = 0; j < nv; ++j) kept += key_of(tp_pick<DT>(w, j), e0 + j) >= cut ? 1u : 0u;
+  });
   kept = __reduce_add_sync(0xffffffffu, kept);
-  __syncthreads();
-  if (lane == 0) sh.ch[warp] = kept;
+  if (lane == 0) sh.wcnt[warp] = kept;
   __syncthreads();
   if (tid == 0) {
     unsigned tot = 0;
-    for (int w2 = 0; w2 < kTpThreads / 32; ++w2) tot += sh.ch[w2];
+    for (int w2 = 0; w2 < kTpThreads / 32; ++w2) tot += sh.wcnt[w2];
     P.topp_cut[row] = cut;
     if (P.topp_kept) P.topp_kept[row] = (int)tot;
   }
