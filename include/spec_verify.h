@@ -156,6 +156,22 @@ int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
                      int32_t* h_n_accepted, void* staging, size_t staging_bytes,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* spec_verify_host without the wait: the copies and the step are enqueued on
+ * `stream`, and the call returns SV_OK (or a host-side error code, with
+ * nothing enqueued) at once. h_out_tokens / h_n_accepted hold the results
+ * once `stream` has reached this point (cudaStreamSynchronize, or an event
+ * recorded after the call); the device status bits are read with
+ * sv_read_device_status(workspace, stream). The host input buffers must stay
+ * unchanged until then, and pinned host memory is needed for the copies to be
+ * asynchronous. A serving loop overlaps the copies of one step with the
+ * kernels of the previous one by giving consecutive calls different streams,
+ * staging buffers and workspaces. */
+int spec_verify_host_async(const void* h_target_logits, const void* h_draft_logits,
+                           const int32_t* h_draft_tokens, const float* h_uniforms, int B, int K,
+                           int V, int dtype, float temperature, int32_t* h_out_tokens,
+                           int32_t* h_n_accepted, void* staging, size_t staging_bytes,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* spec_verify for callers that cannot allocate device memory (the paper has no
  * counterpart to this; it is a property of this library only). Some callers
  * cannot provide a workspace: code running during stream capture in the global

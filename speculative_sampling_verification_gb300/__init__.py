@@ -28,7 +28,7 @@ __all__ = [
     "sv_sample_workspace_size", "spec_draft_sample", "draft_sample",
     "sv_greedy_workspace_size", "spec_verify_greedy", "verify_greedy", "sv_force_path",
     "sv_test_withhold_plans", "sv_topk_workspace_size", "spec_verify_topk", "verify_topk",
-    "sv_topp_workspace_size", "spec_verify_topp", "verify_topp",
+    "sv_topp_workspace_size", "spec_verify_topp", "verify_topp", "spec_verify_host_async",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -45,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "spec_verify_static", "sv_sample_workspace_size", "spec_draft_sample",
     "sv_greedy_workspace_size", "spec_verify_greedy", "sv_force_path", "sv_test_withhold_plans",
     "sv_topk_workspace_size", "spec_verify_topk", "sv_topp_workspace_size", "spec_verify_topp",
+    "spec_verify_host_async",
 )
 
 _lib = None
@@ -83,6 +84,8 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.spec_verify_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp, vp, sz, vp,
                                      sz, vp]
     lib.spec_verify_host.restype = i32
+    lib.spec_verify_host_async.argtypes = lib.spec_verify_host.argtypes
+    lib.spec_verify_host_async.restype = i32
     lib.sv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     lib.sv_read_device_status.restype = i32
     lib.sv_status_string.argtypes = [i32]
@@ -223,21 +226,37 @@ def spec_verify_profiled(target, draft, tokens, uniforms, temperature, out_token
         evp(ev_start), evp(ev_stats_done), evp(ev_end)))
 
 
-def spec_verify_host(h_target, h_draft, h_tokens, h_uniforms, temperature, h_out_tokens,
-                     h_n_accepted, staging, workspace, stream=None) -> int:
-    """Host-buffer call: copies in, verifies, copies out, synchronises. Returns
-    a host error code or the device status bits (0 = ok)."""
+def _host_args(h_target, h_draft, h_tokens, h_uniforms, temperature, h_out_tokens, h_n_accepted,
+               staging, workspace, stream):
     for t in (h_target, h_draft, h_tokens, h_uniforms, h_out_tokens, h_n_accepted):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError("host tensors must be contiguous CPU tensors")
     B, K1, V = h_target.shape
     K = K1 - 1
     dt = _dtype_code(h_target)
-    return int(load_library().spec_verify_host(
-        _ptr(h_target), _ptr(h_draft), _ptr(h_tokens), _ptr(h_uniforms), B, K, V, dt,
-        ctypes.c_float(temperature), _ptr(h_out_tokens), _ptr(h_n_accepted), _ptr(staging),
-        staging.numel() * staging.element_size(), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(staging.device, stream)))
+    return (_ptr(h_target), _ptr(h_draft), _ptr(h_tokens), _ptr(h_uniforms), B, K, V, dt,
+            ctypes.c_float(temperature), _ptr(h_out_tokens), _ptr(h_n_accepted), _ptr(staging),
+            staging.numel() * staging.element_size(), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(staging.device, stream))
+
+
+def spec_verify_host(h_target, h_draft, h_tokens, h_uniforms, temperature, h_out_tokens,
+                     h_n_accepted, staging, workspace, stream=None) -> int:
+    """Host-buffer call: copies in, verifies, copies out, synchronises. Returns
+    a host error code or the device status bits (0 = ok)."""
+    return int(load_library().spec_verify_host(*_host_args(
+        h_target, h_draft, h_tokens, h_uniforms, temperature, h_out_tokens, h_n_accepted, staging,
+        workspace, stream)))
+
+
+def spec_verify_host_async(h_target, h_draft, h_tokens, h_uniforms, temperature, h_out_tokens,
+                           h_n_accepted, staging, workspace, stream=None) -> int:
+    """spec_verify_host without the wait: returns the host error code once the
+    copies and the step are enqueued; the host outputs are valid once `stream`
+    has reached this point."""
+    return int(load_library().spec_verify_host_async(*_host_args(
+        h_target, h_draft, h_tokens, h_uniforms, temperature, h_out_tokens, h_n_accepted, staging,
+        workspace, stream)))
 
 
 def spec_verify_static(target, draft, tokens, uniforms, temperature, out_tokens, n_accepted,

@@ -195,11 +195,17 @@ size_t sv_staging_size(int B, int K, int V, int dtype) {
   return S.total;
 }
 
-int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
-                     const int32_t* h_draft_tokens, const float* h_uniforms, int B, int K, int V,
-                     int dtype, float temperature, int32_t* h_out_tokens, int32_t* h_n_accepted,
-                     void* staging, size_t staging_bytes, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The host-buffer step: inputs host -> device into `staging`, the step, the
+// outputs device -> host; nothing waits when `sync` is false.
+int host_step(const void* h_target_logits, const void* h_draft_logits,
+              const int32_t* h_draft_tokens, const float* h_uniforms, int B, int K, int V,
+              int dtype, float temperature, int32_t* h_out_tokens, int32_t* h_n_accepted,
+              void* staging, size_t staging_bytes, void* workspace, size_t workspace_bytes,
+              void* stream, bool sync) {
   sv::Layout L;
   int rc = validate(h_target_logits, h_draft_logits, h_draft_tokens, h_uniforms, B, K, V, dtype,
                     temperature, h_out_tokens, h_n_accepted, workspace, workspace_bytes, &L);
@@ -225,16 +231,42 @@ int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
                    reinterpret_cast<int32_t*>(d + S.out), reinterpret_cast<int32_t*>(d + S.nacc),
                    workspace, workspace_bytes, stream);
   if (rc != SV_OK) return rc;
-  unsigned status = 0;
   if (cudaMemcpyAsync(h_out_tokens, d + S.out, (size_t)B * (K + 1) * 4, cudaMemcpyDeviceToHost,
                       st) != cudaSuccess ||
       cudaMemcpyAsync(h_n_accepted, d + S.nacc, (size_t)B * 4, cudaMemcpyDeviceToHost, st) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(&status, static_cast<unsigned char*>(workspace) + L.off_status,
+          cudaSuccess)
+    return SV_ERR_CUDA;
+  if (!sync) return SV_OK;
+  unsigned status = 0;
+  if (cudaMemcpyAsync(&status, static_cast<unsigned char*>(workspace) + L.off_status,
                       sizeof(status), cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return SV_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
   return (int)status;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
+                     const int32_t* h_draft_tokens, const float* h_uniforms, int B, int K, int V,
+                     int dtype, float temperature, int32_t* h_out_tokens, int32_t* h_n_accepted,
+                     void* staging, size_t staging_bytes, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return host_step(h_target_logits, h_draft_logits, h_draft_tokens, h_uniforms, B, K, V, dtype,
+                   temperature, h_out_tokens, h_n_accepted, staging, staging_bytes, workspace,
+                   workspace_bytes, stream, true);
+}
+
+int spec_verify_host_async(const void* h_target_logits, const void* h_draft_logits,
+                           const int32_t* h_draft_tokens, const float* h_uniforms, int B, int K,
+                           int V, int dtype, float temperature, int32_t* h_out_tokens,
+                           int32_t* h_n_accepted, void* staging, size_t staging_bytes,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  return host_step(h_target_logits, h_draft_logits, h_draft_tokens, h_uniforms, B, K, V, dtype,
+                   temperature, h_out_tokens, h_n_accepted, staging, staging_bytes, workspace,
+                   workspace_bytes, stream, false);
 }
 
 size_t sv_sample_workspace_size(int N, int V, int dtype) {

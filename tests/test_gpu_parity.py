@@ -276,6 +276,36 @@ def test_host_entry_point_matches_device_entry_point():
     assert np.array_equal(h_out.numpy(), out_d) and np.array_equal(h_nacc.numpy(), nacc_d)
 
 
+def test_async_host_entry_point_pipelined_over_two_lanes():
+    """spec_verify_host_async on alternating (stream, staging, workspace)
+    lanes: each step's outputs, read once its lane's stream is done, equal the
+    device entry point's."""
+    w = shrink(WORKLOADS["c2"], B=8, V=32000)
+    B, K, V = w.B, w.K, w.V
+    steps = [make_inputs(w, step=20 + i, pin_memory=True) for i in range(6)]
+    want = [run_gpu(inp)[:2] for inp in steps]
+    lanes = []
+    for _ in range(2):
+        lanes.append((torch.cuda.Stream(),
+                      torch.empty(sv.sv_staging_size(B, K, V, sv.SV_BF16), dtype=torch.uint8, device=DEV),
+                      torch.empty(sv.sv_workspace_size(B, K, V, sv.SV_BF16), dtype=torch.uint8, device=DEV),
+                      torch.empty(B, K + 1, dtype=torch.int32).pin_memory(),
+                      torch.empty(B, dtype=torch.int32).pin_memory()))
+    got = [None] * len(steps)
+    for i, inp in enumerate(steps + [None, None]):
+        st, staging, ws, h_out, h_nacc = lanes[i % 2]
+        if i >= 2:  # the previous step on this lane: wait, read its results
+            st.synchronize()
+            assert sv.sv_read_device_status(ws, st) == 0
+            got[i - 2] = (h_out.numpy().copy(), h_nacc.numpy().copy())
+        if inp is not None:
+            assert sv.spec_verify_host_async(inp["target"], inp["draft"], inp["tokens"],
+                                             inp["uniforms"], inp["temperature"], h_out, h_nacc,
+                                             staging, ws, stream=st) == 0
+    for (o, n), (wo, wn) in zip(got, want):
+        assert np.array_equal(o, wo) and np.array_equal(n, wn)
+
+
 @pytest.mark.parametrize("B,V", [(16, 50000), (24, 128256)])
 def test_graph_capture_replay_and_determinism(B, V):
     # 27 MB of logits is one sequence group; 105 MB is three, whose draws run
