@@ -198,3 +198,20 @@ def test_topp_workspace_and_validation(lib):
     assert call(t=(1 << 20) + 2) == 5 and call(kept=(1 << 20) + 2) == 5
     assert call(wsb=lib.sv_workspace_size(2, 3, 1000, sv.SV_F32)) == 6
     assert call(B=0, t=0, d=0, tok=0, u=0) == 0
+
+
+@pytest.mark.parametrize("name", ["spec_verify_host", "spec_verify_host_async"])
+def test_host_buffer_entry_points_validate_before_any_copy(lib, name):
+    vp = ctypes.c_void_p
+    fn = getattr(lib, name)
+
+    def call(t=1 << 20, d=1 << 20, tok=1 << 20, u=1 << 20, B=2, K=3, V=100, dtype=sv.SV_F32,
+             T=1.0, out=1 << 20, nacc=1 << 20, st=1 << 20, stb=1 << 30, ws=1 << 20, wsb=1 << 30):
+        return fn(vp(t), vp(d), vp(tok), vp(u), B, K, V, dtype, ctypes.c_float(T), vp(out),
+                  vp(nacc), vp(st), stb, vp(ws), wsb, None)
+
+    assert call(dtype=3) == 4 and call(K=0) == 2 and call(T=0.0) == 3
+    assert call(t=0) == 1 and call(st=0) == 1 and call(ws=0) == 1
+    assert call(st=(1 << 20) + 16) == 5 and call(ws=(1 << 20) + 16) == 5
+    assert call(stb=16) == 6 and call(wsb=16) == 6
+    assert call(B=0, t=0, d=0) == 0
