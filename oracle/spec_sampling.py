@@ -412,6 +412,9 @@ def verify_topp(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
         raise ValueError("top_p must be > 0")
     with np.errstate(over="ignore"):
         T = float(np.float32(temperature))
+        # Like the temperature (U6), top_p is an fp32 argument: its fp32 value,
+        # widened exactly, is the mass the cut must reach.
+        top_p = float(np.float32(top_p))
     tm, tk, tg = topp_mask(target, T, top_p)
     dm, dk, dg = topp_mask(draft, T, top_p)
     res = verify(tm, dm, tokens, uniforms, temperature)

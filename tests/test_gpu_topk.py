@@ -224,3 +224,18 @@ def test_graph_capture_replay():
     assert torch.equal(out, first)
     ref = oracle_topk(inp, 32)
     _parity.compare(out.cpu().numpy(), nacc.cpu().numpy(), ref, inp["tokens"].numpy()).assert_ok(1e-5)
+
+
+def test_k256_on_a_256000_f32_vocabulary_sampled():
+    """The largest k on the widest rows (f32, 256000 entries, 32 sequences of
+    9 rows); the oracle checks a sample of the sequences."""
+    w = shrink(WORKLOADS["c4"], B=32)
+    top_k = 256
+    inp = make_topk_inputs(w, top_k)
+    out, nacc, status = run_gpu(inp, top_k)
+    assert status == 0
+    seqs = np.array([0, 13, 31])
+    sub = {k: (v[seqs] if torch.is_tensor(v) else v) for k, v in inp.items()}
+    _parity.compare(out[seqs], nacc[seqs], oracle_topk(sub, top_k),
+                    inp["tokens"].numpy()[seqs]).assert_ok(1e-5)
+    assert ((nacc >= 0) & (nacc <= w.K)).all()

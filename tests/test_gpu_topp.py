@@ -187,3 +187,12 @@ def test_graph_capture_replay():
         g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, first)
+
+
+@pytest.mark.parametrize("top_p", [0.01, 0.999])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_top_p_extremes(top_p, dt):
+    """A nucleus of one or two entries, and one that keeps nearly the whole
+    mass (the cut deep in the tail, through the open last bins)."""
+    w = _w(6, 3, 20011, dt, seed=int(top_p * 1000), std=1.5)
+    parity(make_topp_inputs(w, top_p), top_p)
