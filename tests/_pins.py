@@ -491,6 +491,26 @@ def pin_topk_mask_cases(O):
         assert np.array_equal(got, np.array(want)), (row, k, got)
 
 
+def pin_topk_order_property(O):
+    """Against the definition, without sorting: on random tie-heavy rows
+    (finite, -0 mixed with +0) the mask keeps exactly min(k, V) entries, and
+    no removed entry outranks a kept one (a larger logit, or an equal logit
+    and a smaller id)."""
+    rng = np.random.default_rng(53)
+    for trial in range(300):
+        V = int(rng.integers(1, 12))
+        row = rng.integers(-2, 3, V).astype(float)
+        row[(row == 0) & (rng.random(V) < 0.5)] = -0.0
+        k = int(rng.integers(1, V + 3))
+        masked = O.topk_mask(row[None], k)[0]
+        keep = np.isfinite(masked)
+        assert keep.sum() == min(k, V), (row, k, masked)
+        assert (masked[keep] == row[keep]).all()
+        for i in np.nonzero(keep)[0]:
+            for j in np.nonzero(~keep)[0]:
+                assert row[i] > row[j] or (row[i] == row[j] and i < j), (row, k, masked)
+
+
 def pin_topk_hand_case(O):
     """Worked by hand: V = 3, K = 1, k = 2, T = 1. Target probabilities
     .5, .3, .2 keep ids 0, 1 -> q = .625, .375, 0; draft .2, .3, .5 keep ids
@@ -692,6 +712,7 @@ FAST_PINS = (pin_golden, pin_theorem1, pin_sequential, pin_library_special_cases
              pin_invariants, pin_failures, pin_draft_golden, pin_draft_failures,
              pin_draft_matches_bonus, pin_greedy_golden, pin_greedy_is_zero_temperature,
              pin_greedy_failures, pin_topk_mask_cases, pin_topk_hand_case,
-             pin_topk_full_is_verify, pin_topk_one_is_greedy, pin_topp_mask_cases,
+             pin_topk_full_is_verify, pin_topk_one_is_greedy, pin_topk_order_property,
+             pin_topp_mask_cases,
              pin_topp_brute_force, pin_topp_hand_case, pin_topp_one_is_verify,
              pin_topp_tiny_is_top1)

@@ -155,3 +155,7 @@ def test_topp_tiny_is_top1():
 
 def test_topp_first_token_law_is_filtered_q():
     _pins.pin_topp_law(oracle)
+
+
+def test_topk_against_the_ranking_definition():
+    _pins.pin_topk_order_property(oracle)
