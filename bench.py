@@ -1,21 +1,27 @@
 """Benchmark of the speculative-sampling verification step on GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config c2]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config c4]
 
-A step is one verification call over one batch of the workload (default: B=8
-sequences, K=4 drafts, V=32000, bf16 logits, T=1; the workload defined over
-1000 repeated verify steps). Inputs are seeded synthetic logits resident in
-HBM before timing starts; steps rotate through a pool of input sets larger
-than twice the L2 cache, so every step streams its logits from HBM. The K
-timed steps are captured in one CUDA graph and timed with CUDA events on the
-launching stream; the streaming kernel of every step is bracketed by its own
-events for the roofline figure.
+A step is one verification call over one batch of the workload (default: the
+largest single-GPU workload, B=256 sequences, K=4 drafts, V=256000, fp32
+logits, T=1). Inputs are seeded synthetic logits, drawn on the device and
+resident in HBM before timing starts; a step streams more than twice the L2
+(smaller workloads rotate over input sets, or flush L2 between steps). The K
+steps are captured in one CUDA graph, which is replayed back to back until at
+least --min-seconds have passed, timed with CUDA events on the launching
+stream; a second graph with events between the two kernels gives each
+kernel's time for the roofline figure.
 
 Rank 0 prints one JSON line. `value` is verified draft positions per second
 over all ranks (B*K per step); `e2e` is the same metric through the
-host-buffer entry point (host->device copy of each step's inputs from pinned
+host-buffer entry points (host->device copy of each step's inputs from pinned
 memory, device->host copy of its outputs, inside the timed region).
-`--impl reference` times the fp64 CPU oracle on the same workload instead.
+`cpu_baseline` is the fp64 oracle on a bounded sample of the same step, on one
+core and on every host core, and `parity` compares the GPU's decisions with
+the oracle's on that sample. `workloads` holds sub-records (ms per step,
+GB/s, mean accepted length) for the 64x8x128256 workload and the 20 cells of
+the acceptance sweep. `--impl reference` times the fp64 CPU oracle on the
+host cores instead.
 """
 
 from __future__ import annotations
@@ -23,9 +29,12 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
+import shutil
 import statistics
 import subprocess
 import sys
+import tempfile
 import threading
 import time
 
@@ -35,7 +44,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import get_workload, make_inputs, make_topk_inputs, make_topp_inputs  # noqa: E402
+from synthetic import (SWEEP_K, SWEEP_NOISE, get_workload, make_batch, make_inputs,  # noqa: E402
+                       make_topk_inputs, make_topp_inputs)
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "verified draft positions/sec (and achieved HBM GB/s, % of GB300 peak)"
@@ -45,12 +55,17 @@ UNIT = "draft_positions/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="c2", help="c1..c4 or sweep-k{K}-n{noise}")
+    ap.add_argument("--config", default="c4", help="c1..c4 or sweep-k{K}-n{noise}")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="verify: replay the K-step graph until this much time has passed")
+    ap.add_argument("--sub", default="c3,sweep",
+                    help="verify: workloads measured after the headline, as sub-records")
+    ap.add_argument("--no-sub", action="store_true")
     ap.add_argument("--op", choices=["verify", "draft_sample", "greedy", "topk", "topp"],
                     default="verify",
                     help="verify: the verification step (default); draft_sample: the draft-side "
@@ -177,49 +192,296 @@ class ClockSampler:
                 "sm_max_mhz": num(rows[0][1]), "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_oracle_rate(w, seconds: float = 12.0, max_steps: int = 5000, warmup: int = 0):
-    """Draft positions per second of the fp64 oracle on whole steps of `w`."""
+# ---------------------------------------------------------------- the host and the oracle on its cores
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def host_info() -> dict:
+    return {"nproc": os.cpu_count(), "cores_available": host_cores(), "cpu_model": cpu_model(),
+            "arch": platform.machine()}
+
+
+def _scratch_dir() -> str:
+    """A directory for the oracle's input files: /dev/shm when it has room,
+    else the default temporary directory."""
+    try:
+        if shutil.disk_usage("/dev/shm").free > (16 << 30):
+            return "/dev/shm"
+    except Exception:
+        pass
+    return tempfile.gettempdir()
+
+
+def _to_np(t: torch.Tensor) -> np.ndarray:
+    """CPU numpy copy of a tensor; bf16 is kept as its raw 16-bit patterns."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def save_oracle_job(tmp: str, tag: str, inp: dict, seqs) -> list:
+    """Write sequences `seqs` of an input dict (CPU or GPU tensors) to .npy
+    files under `tmp`; returns their paths (target, draft, tokens, uniforms)."""
+    idx = torch.as_tensor(list(seqs), dtype=torch.long)
+    paths = []
+    for k in ("target", "draft", "tokens", "uniforms"):
+        x = inp[k]
+        x = x[idx.to(x.device)]
+        p = os.path.join(tmp, f"{tag}-{k}.npy")
+        np.save(p, _to_np(x))
+        paths.append(p)
+    return paths
+
+
+def _load_oracle_job(paths):
+    t, d, k, u = (np.load(p, mmap_mode="r") for p in paths)
+    if t.dtype == np.uint16:  # bf16 bit patterns: widen exactly to fp32
+        t = (t.astype(np.uint32) << np.uint32(16)).view(np.float32)
+        d = (d.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return (np.ascontiguousarray(t), np.ascontiguousarray(d), np.asarray(k).astype(np.int64),
+            np.asarray(u))
+
+
+def oracle_job(job):
+    """One oracle job (run in this process or in a spawned worker): the fp64
+    oracle over the sequences stored in `paths`, repeated for `seconds` (at
+    least once). Returns (sequences verified, seconds, the first result)."""
     import oracle
 
-    sets = [make_inputs(w, step=10_000 + i) for i in range(min(8, max_steps))]
-    for i in range(warmup):
-        oracle.verify_inputs(sets[i % len(sets)], chunk=w.B)
+    paths, temperature, seconds = job
+    t, d, k, u = _load_oracle_job(paths)
     t0 = time.perf_counter()
-    n = 0
-    while n < max_steps:
-        oracle.verify_inputs(sets[n % len(sets)], chunk=w.B)
-        n += 1
-        if time.perf_counter() - t0 > seconds:
+    n, first = 0, None
+    while True:
+        r = oracle.verify(t, d, k, u, temperature)
+        n += t.shape[0]
+        if first is None:
+            first = r
+        if time.perf_counter() - t0 >= seconds:
             break
-    dt = time.perf_counter() - t0
-    return n * w.B * w.K / dt, n, dt
+    return n, time.perf_counter() - t0, first
 
+
+class OracleHost:
+    """The fp64 oracle on the host's cores: a spawn pool fed through .npy files."""
+
+    def __init__(self, workers: int):
+        import multiprocessing as mp
+
+        self.workers = max(1, workers)
+        self.tmp = tempfile.mkdtemp(prefix="sv-oracle-", dir=_scratch_dir())
+        self.pool = mp.get_context("spawn").Pool(self.workers)
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+        shutil.rmtree(self.tmp, ignore_errors=True)
+
+
+def oracle_sample_plan(w, cores: int, call_s: float = 0.25):
+    """Sequences per oracle call, sized so that one call takes about `call_s`
+    on one core (about 25 ns per logit element)."""
+    per_seq = (2 * w.K + 1) * w.V * 25e-9
+    return max(1, min(w.B, int(call_s / per_seq)))
+
+
+def cpu_baselines(w, inp: dict, host: OracleHost, seconds: float = 10.0):
+    """The oracle, as it stands, on a bounded sample of one step of `w`
+    (`inp`, the GPU's own inputs): one thread in this process, then every
+    host core through the pool, each job on different sequences. Returns
+    (single, all_cores, the per-sequence oracle results with their indices)."""
+    per = oracle_sample_plan(w, host.workers)
+    jobs = []
+    for j in range(host.workers):
+        seqs = [(j * per + i) % w.B for i in range(per)]
+        jobs.append((seqs, save_oracle_job(host.tmp, f"{w.name}-{j}", inp, seqs)))
+    T = inp["temperature"]
+    n1, dt1, _ = oracle_job((jobs[0][1], T, seconds))
+    single = {"value": n1 * w.K / dt1, "unit": UNIT, "cores": 1, "kind": "oracle",
+              "sample": f"{n1 // per} oracle calls over {per} sequences of {w.name} in "
+                        f"{dt1:.1f} s (fp64 numpy oracle, 1 thread)"}
+    res = host.pool.map(oracle_job, [(p, T, seconds) for _, p in jobs])
+    rate = sum(n / dt for n, dt, _ in res) * w.K
+    calls = sum(n for n, _, _ in res) // per
+    every = {"value": rate, "unit": UNIT, "cores": host.workers, "kind": "oracle",
+             "sample": f"{calls} oracle calls over {per} sequences each of {w.name}, one process "
+                       f"per core on {host.workers} cores, {seconds:.0f} s each (fp64 numpy "
+                       f"oracle)"}
+    checked = [(seqs, r) for (seqs, _), (_, _, r) in zip(jobs, res)]
+    return single, every, checked
+
+
+def parity_sample(checked, out: np.ndarray, nacc: np.ndarray, tokens: np.ndarray) -> dict:
+    """Decisions of the GPU's step against the oracle's on the sampled sequences."""
+    from tests import _parity
+
+    rep = _parity.ParityReport()
+    seen = set()
+    for seqs, r in checked:
+        keep = [i for i, b in enumerate(seqs) if b not in seen]
+        seen.update(seqs)
+        if not keep:
+            continue
+        b = np.asarray(seqs)[keep]
+        sub = type(r)(*[getattr(r, f)[keep] for f in r.__dataclass_fields__])
+        rep.add(_parity.compare(out[b], nacc[b], sub, tokens[b]))
+    d = rep.as_dict()
+    d["margin"] = _parity.MARGIN
+    return d
+
+
+# ---------------------------------------------------------------- timing helpers
+
+def make_sets(w, n_sets: int, dev, step_base: int):
+    """`n_sets` input sets of `w`, drawn on the device by the batched generator."""
+    return [make_batch(w, step=step_base + i, device=dev) for i in range(n_sets)]
+
+
+def l2_plan(set_bytes: int, max_sets: int = 2):
+    """Input sets to rotate over, and whether L2 must be flushed between steps:
+    a step whose logits exceed twice the L2 needs neither."""
+    if set_bytes >= 2 * L2_BYTES:
+        return 1, False
+    n = min(max_sets, -(-2 * L2_BYTES // set_bytes))
+    return n, n * set_bytes < 2 * L2_BYTES
+
+
+def time_sub_workload(sv, name: str, dev, stream, reps_min_s: float = 0.25, steps: int = 20):
+    """ms per step, GB/s and mean accepted length of one workload (a
+    sub-record): `steps` calls in one CUDA graph, each bracketed by its own
+    events, L2 flushed between calls when the inputs fit in it."""
+    w = get_workload(name)
+    dt_code = sv.SV_BF16 if w.dtype == "bf16" else sv.SV_F32
+    B, K, V, es = w.B, w.K, w.V, w.elem_bytes
+    set_bytes = B * (2 * K + 1) * V * es
+    n_sets, flush = l2_plan(set_bytes)
+    sets = make_sets(w, n_sets, dev, 500)
+    outs = [(torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+             torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
+    ws = sv.new_workspace(B, K, V, dt_code, dev)
+    scrub = torch.empty(3 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    T = w.temperature
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+
+    def call(i):
+        s = sets[i % n_sets]
+        o, n = outs[i % n_sets]
+        rc = sv.spec_verify(s["target"], s["draft"], s["tokens"], s["uniforms"], T, o, n, ws)
+        if rc != 0:
+            raise RuntimeError(f"spec_verify failed: {sv.sv_status_string(rc)}")
+
+    with torch.cuda.stream(stream):
+        call(0)
+        for a, b in evs:
+            a.record(stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(steps):
+            if scrub is not None:
+                scrub.fill_(float(i))
+            evs[i][0].record(stream)
+            call(i)
+            evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    g.replay()  # warm-up
+    torch.cuda.synchronize()
+    per_rep, t0 = [], time.perf_counter()
+    while not per_rep or time.perf_counter() - t0 < reps_min_s:
+        g.replay()
+        torch.cuda.synchronize()
+        per_rep.append(float(np.mean([a.elapsed_time(b) for a, b in evs])))
+    if sv.sv_read_device_status(ws, stream) != 0:
+        raise RuntimeError(f"bad device status on {name}")
+    ms = float(np.median(per_rep))
+    nacc = torch.stack([n for _, n in outs]).cpu().numpy()
+    peak, _ = load_peaks()
+    ideal = w.ideal_bytes_per_step()
+    fused = sv.sv_kernels_per_call(B, K, V, dt_code) == 1
+    del sets, outs, ws, scrub, g
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "ms_per_step": ms, "draft_positions_per_s": B * K / (ms * 1e-3),
+            "sequences_per_s": B / (ms * 1e-3), "hbm_gbs_ideal_bytes": ideal / (ms * 1e-3) / 1e9,
+            "frac_of_peak_ideal_bytes": ideal / (ms * 1e-3) / 1e9 / peak,
+            "mean_accepted": float(nacc.mean()), "sequences_for_mean": int(nacc.size),
+            "path": "fused_kernel" if fused else "stats_kernel + draw_kernel",
+            "l2": "flushed between calls" if flush else f"inputs rotate over {n_sets} sets "
+                                                         f"(> 2x L2)",
+            "repeats": len(per_rep)}
+
+
+# ---------------------------------------------------------------- the verification step
 
 def run_reference(args, w, world, rank):
+    """The reference arm: the fp64 oracle, as it stands, on every host core.
+    A step is one oracle call per core over a bounded sample of the workload's
+    sequences (one process per core, each on its own sequences)."""
     if rank != 0:
         return
     steps = max(1, args.steps)
-    import oracle
-
-    sets = [make_inputs(w, step=20_000 + i) for i in range(min(8, steps))]
-    for i in range(args.warmup):
-        oracle.verify_inputs(sets[i % len(sets)], chunk=w.B)
-    t0 = time.perf_counter()
-    for i in range(steps):
-        oracle.verify_inputs(sets[i % len(sets)], chunk=w.B)
-    dt = time.perf_counter() - t0
-    value = steps * w.B * w.K / dt
+    cores = host_cores()
+    host = OracleHost(cores)
+    try:
+        per = oracle_sample_plan(w, cores)
+        seqs_all = sorted({(j * per + i) % w.B for j in range(cores) for i in range(per)})
+        inp = make_inputs(w, step=20_000, seqs=seqs_all)
+        pos = {b: i for i, b in enumerate(seqs_all)}
+        jobs = [save_oracle_job(host.tmp, f"ref-{j}", inp,
+                                [pos[(j * per + i) % w.B] for i in range(per)])
+                for j in range(cores)]
+        T = inp["temperature"]
+        for _ in range(max(1, args.warmup)):
+            host.pool.map(oracle_job, [(p, T, 0.0) for p in jobs])
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            host.pool.map(oracle_job, [(p, T, 0.0) for p in jobs])
+        dt = time.perf_counter() - t0
+    finally:
+        host.close()
+    value = steps * cores * per * w.K / dt
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
-        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "detail": w.describe()},
-        "cpu_baseline": {"value": value, "unit": "draft_positions/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{steps} whole steps of {w.name} (fp64 numpy oracle, 1 thread)"},
-        "e2e": {"value": value, "unit": "draft_positions/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": dt / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": bench_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {cores} processes, one per core, each running "
+                                   f"the oracle once over {per} sequences of {w.name}",
+                         "host": host_info()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def bench_config(w) -> dict:
+    """The `config` object of the verification step's line (both arms)."""
+    return {"workload": w.name, "detail": w.describe()}
 
 
 def run_ours(args, w, world, rank, local):
@@ -228,23 +490,27 @@ def run_ours(args, w, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sv.load_library(build=True)
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    host = OracleHost(host_cores()) if want_cpu else None  # spawned before any GPU work
+    try:
+        _run_ours(args, w, world, rank, local, dev, sv, host)
+    finally:
+        if host is not None:
+            host.close()
+
+
+def _run_ours(args, w, world, rank, local, dev, sv, host):
     dt_code = sv.SV_BF16 if w.dtype == "bf16" else sv.SV_F32
     B, K, V, es = w.B, w.K, w.V, w.elem_bytes
     set_bytes = B * (2 * K + 1) * V * es
-    n_sets = max(2, min(64, -(-2 * L2_BYTES // set_bytes) + 1))
-    if set_bytes * n_sets > 40e9:
-        n_sets = 1
-    step_base = 1000 * rank
-    host_sets = [make_inputs(w, step=step_base + i, pin_memory=True) for i in range(n_sets)]
-    sets = []
-    for h in host_sets:
-        sets.append({k: (v.to(dev, non_blocking=True) if torch.is_tensor(v) else v)
-                     for k, v in h.items()})
+    n_sets, flush = l2_plan(set_bytes, max_sets=64)
+    sets = make_sets(w, n_sets, dev, 1000 * rank)
     outs = [(torch.empty(B, K + 1, dtype=torch.int32, device=dev),
              torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
     ws = sv.new_workspace(B, K, V, dt_code, dev)
     T = w.temperature
     stream = torch.cuda.Stream(dev)
+    scrub = torch.empty(3 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
 
     def call(i, evs=None):
         s = sets[i % n_sets]
@@ -274,36 +540,52 @@ def run_ours(args, w, world, rank, local):
     # g_prof repeats the steps with events between the two kernels (which
     # makes the draw an ordinary launch) and gives the per-kernel times.
     g_warm, g_timed, g_prof = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_warm, stream=stream):
-        for i in range(warmup):
-            call(i)
-    with torch.cuda.graph(g_timed, stream=stream):
-        for i in range(steps):
-            call(warmup + i)
-    with torch.cuda.graph(g_prof, stream=stream):
-        for i in range(steps):
-            call(warmup + i, evs[i])
+
+    def steps_into(graph, first, n, with_evs=False):
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n):
+                if scrub is not None:
+                    scrub.fill_(float(i))
+                call(first + i, evs[i] if with_evs else None)
+
+    steps_into(g_warm, 0, warmup)
+    steps_into(g_timed, warmup, steps)
+    steps_into(g_prof, warmup, steps, with_evs=True)
     torch.cuda.synchronize()
 
+    # The timed region: the K-step graph replayed back to back until at least
+    # a second has passed, inside one barrier + synchronise bracket.
+    g_warm.replay()
+    torch.cuda.synchronize()
+    t_est = time.perf_counter()
+    g_timed.replay()
+    torch.cuda.synchronize()
+    est = max(time.perf_counter() - t_est, 1e-4)
+    reps = max(1, int(np.ceil(args.min_seconds / est)))
+    rep_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    g_warm.replay()
-    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     with torch.cuda.stream(stream):
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        g_timed.replay()
+        for a, b in rep_evs:
+            a.record(stream)
+            g_timed.replay()
+            b.record(stream)
         end.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(end)
+    rep_ms = [a.elapsed_time(b) for a, b in rep_evs]
     g_prof.replay()
     torch.cuda.synchronize()
     time.sleep(0.3)
@@ -311,22 +593,28 @@ def run_ours(args, w, world, rank, local):
 
     status = sv.sv_read_device_status(ws, stream)
     nacc_all = torch.stack([n for _, n in outs]).cpu().numpy()
-    if status != 0 or (nacc_all < 0).any() or (nacc_all > K).any():
-        raise RuntimeError(f"bad device status {status} or n_accepted out of range")
+    out_all = torch.stack([o for o, _ in outs]).cpu().numpy()
+    drawn = np.take_along_axis(out_all, np.clip(nacc_all, 0, K)[..., None], axis=-1)
+    bad_outputs = int((drawn < 0).sum())
+    if status != 0 or (nacc_all < 0).any() or (nacc_all > K).any() or bad_outputs:
+        raise RuntimeError(f"bad device status {status}, n_accepted out of range or "
+                           f"{bad_outputs} undrawn tokens")
 
     stats_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in evs]))
     draw_ms = float(np.mean([b.elapsed_time(c) for _, b, c in evs]))
-
     elapsed_ms = reduce_max(elapsed_ms, world, dev)
 
     # End to end through the host-buffer entry points: every step copies its
     # inputs from pinned host memory and reads its outputs back. `e2e` is a
     # serving loop over two lanes (stream, staging, workspace, host outputs)
     # with spec_verify_host_async, so that one step's copies overlap the
-    # previous step's kernels; each step's results are read, and its status
-    # checked, before its lane is reused. `e2e_sync` is one blocking
-    # spec_verify_host call per step.
-    e2e_steps = args.e2e_steps or min(steps, 200)
+    # previous step's kernels; each step's results are read, its status
+    # checked and its drawn tokens counted, before its lane is reused.
+    # `e2e_sync` is one blocking spec_verify_host call per step.
+    host_sets = [{k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in s.items()}
+                 for s in sets[:2]]
+    n_host = len(host_sets)
+    e2e_steps = args.e2e_steps or max(8, min(steps, int(np.ceil(0.5 / (est / steps)))))
     lanes = []
     for j in range(2):
         lanes.append({
@@ -339,29 +627,30 @@ def run_ours(args, w, world, rank, local):
     h_out, h_nacc, staging = lanes[0]["out"], lanes[0]["nacc"], lanes[0]["staging"]
 
     def host_call(i):
-        h = host_sets[i % n_sets]
+        h = host_sets[i % n_host]
         rc = sv.spec_verify_host(h["target"], h["draft"], h["tokens"], h["uniforms"], T, h_out,
                                  h_nacc, staging, ws, stream=stream)
         if rc != 0:
             raise RuntimeError(f"spec_verify_host: {rc}")
 
     def pipelined(n):
-        accepted = 0
+        undrawn = 0
         for i in range(n + 2):
             lane = lanes[i % 2]
             if i >= 2:  # step i-2 on this lane: wait, check and read its results
                 lane["stream"].synchronize()
                 if sv.sv_read_device_status(lane["ws"], lane["stream"]) != 0:
                     raise RuntimeError("bad device status in the e2e loop")
-                accepted += int(lane["nacc"].sum())
+                o, na = lane["out"].numpy(), lane["nacc"].numpy()
+                undrawn += int((o[np.arange(B), na] < 0).sum())
             if i < n:
-                h = host_sets[i % n_sets]
+                h = host_sets[i % n_host]
                 rc = sv.spec_verify_host_async(h["target"], h["draft"], h["tokens"],
                                                h["uniforms"], T, lane["out"], lane["nacc"],
                                                lane["staging"], lane["ws"], stream=lane["stream"])
                 if rc != 0:
                     raise RuntimeError(f"spec_verify_host_async: {rc}")
-        return accepted
+        return undrawn
 
     for i in range(3):
         host_call(i)
@@ -375,66 +664,126 @@ def run_ours(args, w, world, rank, local):
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
-    pipelined(e2e_steps)
+    undrawn = pipelined(e2e_steps)
     e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
+    if undrawn:
+        raise RuntimeError(f"{undrawn} undrawn tokens (-1 at position n_accepted) in the e2e loop")
+    del host_sets, lanes
 
     if rank != 0:
         return
-    per_step_s = elapsed_ms / 1e3 / steps
+    timed_steps = steps * reps
+    per_step_s = elapsed_ms / 1e3 / timed_steps
     value = aggregate(B * K, world, per_step_s)
     ideal = w.ideal_bytes_per_step()
     peak, peak_kind = load_peaks()
-    # Dominant HBM kernel: the streaming row-statistics kernel, or for small
-    # calls the fused kernel (streaming, scan and draw in one launch). Its
-    # algorithmic bytes are every one of the B(2K+1) rows once.
     fused = sv.sv_kernels_per_call(B, K, V, dt_code) == 1
-    launch_bytes = B * (2 * K + 1) * V * es
-    achieved = launch_bytes / (stats_ms * 1e-3) / 1e9
-    # The draw kernel re-reads two rows per residual draw and one per bonus draw.
+    # Rows the draw reads per step: two per residual draw, one per bonus draw.
     draw_rows = float(np.where(nacc_all < K, 2, 1).sum(axis=1).mean())
+    stream_bytes = B * (2 * K + 1) * V * es
+    draw_bytes = draw_rows * V * es
+    if fused:
+        # One launch streams the B(2K+1) rows and re-reads the draw's rows.
+        kern = {"kernel": "fused_kernel (streaming, scan and draw)", "ms": stats_ms,
+                "bytes": stream_bytes + draw_bytes,
+                "basis": "B(2K+1) rows once, plus 2 rows per residual draw and 1 per bonus "
+                         "draw"}
+        traffic = load_traffic("fused_kernel", w.name)
+        draw_rec = {"ms_per_launch": None, "note": "inside fused_kernel",
+                    "rows_reread_per_step": draw_rows}
+    else:
+        stats = {"kernel": "stats_kernel (streaming row statistics)", "ms": stats_ms,
+                 "bytes": stream_bytes, "basis": "B(2K+1) rows of V elements, once"}
+        draw = {"kernel": "draw_kernel (residual / bonus draw)", "ms": draw_ms,
+                "bytes": draw_bytes, "basis": "2 rows per residual draw, 1 per bonus draw"}
+        kern = stats if stats_ms >= draw_ms else draw
+        traffic = load_traffic("stats_kernel" if kern is stats else "draw_kernel", w.name)
+        draw_rec = {"ms_per_launch": draw_ms, "rows_reread_per_step": draw_rows,
+                    "achieved_gbs": draw_bytes / (draw_ms * 1e-3) / 1e9,
+                    "frac": draw_bytes / (draw_ms * 1e-3) / 1e9 / peak,
+                    "stats_ms_per_launch": stats_ms}
+    achieved = kern["bytes"] / (kern["ms"] * 1e-3) / 1e9
     h2d = B * (K + 1) * V * es + B * K * V * es + B * K * 4 + B * (K + 2) * 4
     d2h = B * (K + 1) * 4 + B * 4 + 4
-    cpu = None
-    if not args.no_cpu_baseline:
-        rate, n, dt = cpu_oracle_rate(w)
-        cpu = {"value": rate, "unit": "draft_positions/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} whole steps of {w.name} in {dt:.1f} s (fp64 numpy oracle, 1 thread)"}
+
+    cpu = parity = None
+    if host is not None:
+        s0 = sets[0]
+        single, every, checked = cpu_baselines(w, s0, host)
+        cpu = dict(every, single_thread=single, host=host_info())
+        parity = parity_sample(checked, out_all[0], nacc_all[0], s0["tokens"].cpu().numpy())
+        parity["sample"] = (f"the timed step's outputs on input set 0 against the oracle "
+                            f"results of the cpu_baseline leg ({parity['sequences']} sequences)")
+    subs = []
+    if world == 1 and not args.no_sub:
+        del sets, outs, ws, scrub, g_warm, g_timed, g_prof
+        torch.cuda.empty_cache()
+        for name in args.sub.split(","):
+            for cell in expand_sub(name):
+                if get_workload(cell).name != w.name:
+                    subs.append(time_sub_workload(sv, cell, dev, stream))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": per_step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "detail": w.describe(), "input_dtype": w.dtype,
-                   "l2": f"inputs rotate over {n_sets} resident sets of {set_bytes / 1e6:.1f} MB "
-                         f"(> 2x L2 per cycle)" if n_sets > 1 else "one set larger than L2",
-                   "timing": "value: K plain steps in one CUDA graph, CUDA events on the "
-                             "launching stream; kernel split (roofline): the same K steps again "
-                             "in a second graph with events between the two kernels"},
+        "config": bench_config(w),
+        "input_dtype": w.dtype,
+        "timing": {"l2": (f"inputs rotate over {n_sets} resident sets of "
+                          f"{set_bytes / 1e6:.1f} MB" if not flush else
+                          f"L2 flushed (a {3 * L2_BYTES // 4 / 1e6:.0f} MB write) between steps")
+                         if n_sets > 1 or flush else "each step streams more than twice the L2",
+                   "method": "K plain steps captured in one CUDA graph; the graph replayed "
+                             "back to back until at least min_seconds passed, CUDA events on "
+                             "the launching stream around the whole region (value) and around "
+                             "each replay (median); kernel split from a second graph with "
+                             "events between the two kernels",
+                   "repeats": reps, "timed_steps": timed_steps,
+                   "ms_per_step_median_repeat": float(np.median(rep_ms)) / steps,
+                   "min_seconds": args.min_seconds},
         "sequences_per_s": world * B / per_step_s,
         "hbm_gbs_ideal_bytes": ideal / per_step_s / 1e9 * world,
         "frac_of_peak_ideal_bytes": ideal / per_step_s / 1e9 / peak,
         "mean_accepted": float(nacc_all.mean()),
-        "roofline": {"bound": "hbm",
-                     "kernel": ("fused_kernel (streaming, scan and draw)" if fused
-                                else "stats_kernel (streaming row statistics)"),
-                     "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "traffic": load_traffic("fused_kernel" if fused else "stats_kernel", w.name),
-                     "bytes_per_launch": launch_bytes, "ms_per_launch": stats_ms,
-                     "bytes_basis": "B(2K+1) rows of V elements, once"},
-        "draw_kernel": ({"ms_per_launch": None, "note": "inside fused_kernel",
-                         "rows_reread_per_step": draw_rows * B} if fused else
-                        {"ms_per_launch": draw_ms, "rows_reread_per_step": draw_rows * B}),
-        "e2e": {"value": aggregate(B * K * e2e_steps, world, e2e_s), "unit": "draft_positions/s",
+        "roofline": {"bound": "hbm", "kernel": kern["kernel"], "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,
+                     "bytes_per_launch": kern["bytes"], "ms_per_launch": kern["ms"],
+                     "bytes_basis": kern["basis"]},
+        "draw_kernel": draw_rec,
+        "e2e": {"value": aggregate(B * K * e2e_steps, world, e2e_s), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "spec_verify_host_async, two lanes: a step's copies overlap the previous "
-                       "step's kernels; every step's outputs read back and its status checked"},
+                       "step's kernels; every step's outputs read back, its status checked and "
+                       "its drawn tokens counted (-1 at n_accepted would be an undrawn token)"},
         "e2e_sync": {"value": aggregate(B * K * e2e_steps, world, e2e_sync_s),
-                     "unit": "draft_positions/s", "api": "spec_verify_host, one blocking call per step"},
-        "gpu_launches": steps * sv.sv_kernels_per_call(B, K, V, dt_code),
+                     "unit": UNIT, "api": "spec_verify_host, one blocking call per step"},
+        "gpu_launches": timed_steps * sv.sv_kernels_per_call(B, K, V, dt_code),
         "clocks": clocks.summary(t_wall0, t_wall1),
         "cpu_baseline": cpu,
+        "parity": parity,
+        "parity_at_scale": load_parity_at_scale(),
+        "workloads": subs,
     }
     print(json.dumps(line), flush=True)
+
+
+def expand_sub(name: str):
+    """Workload keys of a --sub entry ("sweep": the 20 cells of the acceptance sweep)."""
+    if name == "sweep":
+        return [f"sweep-k{k}-n{n:g}" for k in SWEEP_K for n in SWEEP_NOISE]
+    return [name]
+
+
+def load_parity_at_scale():
+    """The committed summary of the last whole-batch parity run, if any."""
+    path = os.path.join(ROOT, "profiles", "parity_at_scale.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"file": "profiles/parity_at_scale.json", "when": d.get("when"),
+                "totals": d.get("totals")}
+    except Exception:
+        return None
 
 
 SAMPLE_METRIC = "draft tokens sampled/sec (and achieved HBM GB/s, % of GB300 peak)"

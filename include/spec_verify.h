@@ -116,17 +116,24 @@ int spec_verify(const void* target_logits, const void* draft_logits,
                 int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
                 void* workspace, size_t workspace_bytes, void* stream);
 
-/* spec_verify plus intermediate values for inspection (each pointer may be NULL):
- *   row_lse      device, [B, 2K+1] fp64: log sum_i exp(l_i / T) per row, target
- *                rows 0..K first, then draft rows 0..K-1 (from the streaming pass)
- *   thresholds   device, [B, K] fp64: min(1, q(x~_t)/p(x~_t)) for every t
- *   sample_prob  device, [B] fp64: normalised weight of the drawn token in the
- *                distribution it was drawn from (residual, fallback q, or bonus q) */
+/* spec_verify plus intermediate values for inspection (each pointer may be NULL;
+ * all are fp64 device arrays, NaN for every entry of a failed sequence):
+ *   row_lse      [B, 2K+1]: log sum_i exp(l_i / T) per row, target rows 0..K
+ *                first, then draft rows 0..K-1 (from the streaming pass)
+ *   thresholds   [B, K]: min(1, q(x~_t)/p(x~_t)) for every t, the acceptance
+ *                test's threshold (card, §4.2 "Modified rejection sampling")
+ *   sample_prob  [B]: normalised weight of the drawn token in the
+ *                distribution it was drawn from (residual, fallback q, or bonus q)
+ *   row_max      [B, 2K+1]: max_i l_i / T per row, same row order as row_lse
+ *   ratios       [B, K]: the ratio q(x~_t)/p(x~_t) itself, not clamped at 1;
+ *                +inf where p(x~_t) = 0 < q(x~_t), 0 where q(x~_t) = 0
+ * Every t < K gets a threshold and a ratio, also past the first rejection. */
 int spec_verify_debug(const void* target_logits, const void* draft_logits,
                       const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
                       int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
                       void* workspace, size_t workspace_bytes, void* stream, double* row_lse,
-                      double* thresholds, double* sample_prob);
+                      double* thresholds, double* sample_prob, double* row_max,
+                      double* ratios);
 
 /* spec_verify that also records three caller-owned CUDA events (cudaEvent_t
  * passed as void*, created with timing enabled) on `stream`: `ev_start` before
@@ -188,11 +195,14 @@ int spec_verify_host_async(const void* h_target_logits, const void* h_draft_logi
  * that device's array, which keeps the previous call's contents; each call
  * clears what must start at zero itself. Calls that overlap on the GPU (on
  * different streams, or from different threads) race on the array and must
- * be serialised by the caller. The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress, with that device current) and
- * sets kernel attributes; make it before any stream capture. Device status
- * bits are not readable for these calls (there is no workspace to read them
- * from); failed sequences still show as -1 outputs and n_accepted = -1. */
+ * be serialised by the caller. Outside stream capture every call looks up the
+ * array's device address in the current context (cudaGetSymbolAddress); a
+ * call made while `stream` is being captured reuses the address of the last
+ * call on that device, so make one call outside capture first (and again
+ * after cudaDeviceReset or a change of context). Device status bits are not
+ * readable for these calls (there is no workspace to read them from): a
+ * sequence that failed shows -1 in all its outputs and n_accepted = -1, and a
+ * draw that did not complete shows -1 at position n_accepted. */
 int spec_verify_static(const void* target_logits, const void* draft_logits,
                        const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
                        int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
@@ -201,9 +211,11 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
 /* ---------------------------------------------------------------- draft-side sampler
  *
  * Step 1 of the card's Algorithm 2: the draft model's tokens x~_t ~ p(.),
- * drawn from the transformed distribution p = softmax(l / T), which the card's
- * Pitfalls require ("Use the same transformed distributions everywhere":
- * draft tokens must be sampled from the transformed p). One token per row, by
+ * drawn from the transformed distribution p = softmax(l / T) ("Accelerating
+ * Large Language Model Decoding with Speculative Sampling", wikillm.com paper
+ * card, §4.2 "Decoding transforms", and the Pitfalls item on transformed
+ * distributions): the draws that feed the verifier use the very distribution
+ * the verifier's ratios and residual use. One token per row, by
  * the inverse-CDF convention above with the row's uniform; rows are
  * independent, so a caller samples one draft position for a batch per call
  * (or several positions at once when their logits are already known). */

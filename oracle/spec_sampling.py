@@ -13,8 +13,8 @@ variant, `verify_greedy`, and verification on top-k filtered distributions,
 
 * q(.|...) and p(.|...) are the target and draft distributions. The decoding
   transform (temperature) is applied to both before anything else
-  (card, §4.2 "Decoding transforms"; Pitfalls, "Use the same transformed
-  distributions everywhere").
+  (card, §4.2 "Decoding transforms"; the Pitfalls item on transformed
+  distributions).
 * Draft token x~_t is accepted while r_t < min(1, q(x~_t)/p(x~_t)), left to
   right, the ratio evaluated at the drafted token (card, §4.2 "Modified
   rejection sampling"; Algorithm 2 step 3; Pitfalls, "Indexing in alg. 2").
@@ -78,6 +78,8 @@ class OracleResult:
     sample_prob: np.ndarray      # [B] normalised weight of the sampled token
     residual_fallback: np.ndarray  # [B] bool, zero-residual fallback to q was used
     lse: np.ndarray              # [B, 2K+1] log-sum-exp of l/T: target rows 0..K, then draft rows 0..K-1
+    row_max: np.ndarray          # [B, 2K+1] max of l/T per row, same order as lse (NaN: bad row)
+    ratios: np.ndarray           # [B, K] q(x~)/p(x~) at the drafted tokens, not clamped
 
     def decisions(self) -> int:
         """Number of decisions taken (acceptance tests plus one draw per ok sequence)."""
@@ -116,6 +118,14 @@ def acceptance_thresholds(q_at: np.ndarray, p_at: np.ndarray) -> np.ndarray:
     with np.errstate(divide="ignore", invalid="ignore"):
         ratio = q_at / np.where(p_at > 0, p_at, 1.0)
     return np.where(p_at > 0, np.minimum(1.0, ratio), np.where(q_at > 0, 1.0, 0.0))
+
+
+def acceptance_ratios(q_at: np.ndarray, p_at: np.ndarray) -> np.ndarray:
+    """q(x~)/p(x~) at the drafted tokens, before the clamp at 1 (card, §4.2),
+    with U4's limits: +inf where p(x~) = 0 < q(x~), 0 where q(x~) = 0."""
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = q_at / np.where(p_at > 0, p_at, 1.0)
+    return np.where(p_at > 0, ratio, np.where(q_at > 0, np.inf, 0.0))
 
 
 def first_rejection(u_acc: np.ndarray, thr: np.ndarray) -> np.ndarray:
@@ -196,6 +206,7 @@ def verify(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
     q_at = np.take_along_axis(q[:, :K, :], tok[..., None], axis=-1)[..., 0]
     p_at = np.take_along_axis(p, tok[..., None], axis=-1)[..., 0]
     thr = acceptance_thresholds(q_at, p_at)
+    ratios = acceptance_ratios(q_at, p_at)
     u_acc = uniforms[:, :K]
     j = first_rejection(u_acc, thr)
     taken = np.arange(K)[None, :] <= j[:, None]
@@ -221,13 +232,18 @@ def verify(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
     out[failed] = -1
     n_acc[failed] = -1
     thr = np.where(failed[:, None], np.nan, thr)
+    ratios = np.where(failed[:, None], np.nan, ratios)
     accept_margin = np.where(failed[:, None], np.nan, accept_margin)
     sample_margin = np.where(failed, np.nan, sample_margin)
     sample_prob = np.where(failed, np.nan, sample_prob)
     fallback = residual & fallback & ~failed
     lse = np.concatenate([lse_q, lse_p], axis=1)
+    # Row maxima of l/T (the transformed logits), NaN where the row is bad.
+    with np.errstate(invalid="ignore"):
+        row_max = np.concatenate([np.max(target / T, axis=-1), np.max(draft / T, axis=-1)], axis=1)
+    row_max = np.where(np.isfinite(lse), row_max, np.nan)
     return OracleResult(out, n_acc, status, thr, accept_margin, sample_margin, sample_prob,
-                        fallback, lse)
+                        fallback, lse, row_max, ratios)
 
 
 @dataclass
@@ -243,9 +259,9 @@ def draft_sample(logits: np.ndarray, uniforms: np.ndarray, temperature: float) -
     """Draft-side sampling: one token per row, x~ ~ softmax(l / T).
 
     This is step 1 of the card's Algorithm 2 (the K sequential draft samples,
-    one row per call here), drawn from the transformed draft distribution as
-    the card's Pitfalls require ("Use the same transformed distributions
-    everywhere": draft tokens must come from the transformed p). The draw is
+    one row per call here), drawn from the transformed draft distribution
+    (card, §4.2 "Decoding transforms", and the Pitfalls item on transformed
+    distributions: the drafts come from the same p the ratios use). The draw is
     the inverse CDF of U3 with the row's uniform; rows fail as in U12 (NaN or
     +inf entries, every entry -inf, or a uniform that is NaN or outside
     [0, 1]): token -1 and a status word saying why.

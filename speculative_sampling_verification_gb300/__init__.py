@@ -77,7 +77,7 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     core = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp, vp, sz, vp]
     lib.spec_verify.argtypes = core
     lib.spec_verify.restype = i32
-    lib.spec_verify_debug.argtypes = core + [dp, dp, dp]
+    lib.spec_verify_debug.argtypes = core + [dp, dp, dp, dp, dp]
     lib.spec_verify_debug.restype = i32
     lib.spec_verify_profiled.argtypes = core + [vp, vp, vp]
     lib.spec_verify_profiled.restype = i32
@@ -201,13 +201,13 @@ def spec_verify(target, draft, tokens, uniforms, temperature, out_tokens, n_acce
 
 def spec_verify_debug(target, draft, tokens, uniforms, temperature, out_tokens, n_accepted,
                       workspace, row_lse=None, thresholds=None, sample_prob=None,
-                      stream=None) -> int:
+                      row_max=None, ratios=None, stream=None) -> int:
     B, K, V, dt = _check(target, draft, tokens, uniforms)
     return int(load_library().spec_verify_debug(
         _ptr(target), _ptr(draft), _ptr(tokens), _ptr(uniforms), B, K, V, dt,
         ctypes.c_float(temperature), _ptr(out_tokens), _ptr(n_accepted), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(target.device, stream),
-        _ptr(row_lse), _ptr(thresholds), _ptr(sample_prob)))
+        _ptr(row_lse), _ptr(thresholds), _ptr(sample_prob), _ptr(row_max), _ptr(ratios)))
 
 
 def spec_verify_profiled(target, draft, tokens, uniforms, temperature, out_tokens, n_accepted,
@@ -295,8 +295,10 @@ def verify(target, draft, tokens, uniforms, temperature, *, workspace=None, debu
         lse = torch.empty(B, 2 * K + 1, dtype=torch.float64, device=dev)
         thr = torch.empty(B, K, dtype=torch.float64, device=dev)
         prob = torch.empty(B, dtype=torch.float64, device=dev)
+        rmax = torch.empty(B, 2 * K + 1, dtype=torch.float64, device=dev)
+        ratio = torch.empty(B, K, dtype=torch.float64, device=dev)
         rc = spec_verify_debug(target, draft, tokens, uniforms, temperature, out, nacc, ws,
-                               lse, thr, prob, stream=stream)
+                               lse, thr, prob, rmax, ratio, stream=stream)
     else:
         rc = spec_verify(target, draft, tokens, uniforms, temperature, out, nacc, ws,
                          stream=stream)
@@ -304,7 +306,7 @@ def verify(target, draft, tokens, uniforms, temperature, *, workspace=None, debu
         raise StatusError(rc, "spec_verify")
     if debug:
         return out, nacc, {"row_lse": lse, "thresholds": thr, "sample_prob": prob,
-                           "workspace": ws}
+                           "row_max": rmax, "ratios": ratio, "workspace": ws}
     return out, nacc
 
 

@@ -37,7 +37,8 @@ int validate(const void* target, const void* draft, const void* tokens, const vo
 int run(const void* target, const void* draft, const int32_t* tokens, const float* uniforms,
         int B, int K, int V, int dtype, float temperature, int32_t* out, int32_t* n_acc,
         void* workspace, size_t workspace_bytes, void* stream, double* dbg_lse, double* dbg_thr,
-        double* dbg_prob, const sv::Events& ev = sv::Events()) {
+        double* dbg_prob, const sv::Events& ev = sv::Events(), double* dbg_max = nullptr,
+        double* dbg_ratio = nullptr) {
   sv::Layout L;
   int rc = validate(target, draft, tokens, uniforms, B, K, V, dtype, temperature, out, n_acc,
                     workspace, workspace_bytes, &L);
@@ -54,6 +55,8 @@ int run(const void* target, const void* draft, const int32_t* tokens, const floa
   P.dbg_lse = dbg_lse;
   P.dbg_thr = dbg_thr;
   P.dbg_prob = dbg_prob;
+  P.dbg_max = dbg_max;
+  P.dbg_ratio = dbg_ratio;
   const bool aligned = !misaligned(target, 16) && !misaligned(draft, 16) &&
                        ((size_t)V * L.es) % 16 == 0;
   cudaError_t e = sv::launch_all(P, aligned, static_cast<cudaStream_t>(stream), ev);
@@ -169,10 +172,11 @@ int spec_verify_debug(const void* target_logits, const void* draft_logits,
                       const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
                       int dtype, float temperature, int32_t* out_tokens, int32_t* n_accepted,
                       void* workspace, size_t workspace_bytes, void* stream, double* row_lse,
-                      double* thresholds, double* sample_prob) {
+                      double* thresholds, double* sample_prob, double* row_max,
+                      double* ratios) {
   return run(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype, temperature,
              out_tokens, n_accepted, workspace, workspace_bytes, stream, row_lse, thresholds,
-             sample_prob);
+             sample_prob, sv::Events(), row_max, ratios);
 }
 
 int spec_verify_profiled(const void* target_logits, const void* draft_logits,

@@ -197,6 +197,8 @@ struct Params {
   double* dbg_lse;
   double* dbg_thr;
   double* dbg_prob;
+  double* dbg_max;    // [B (2K+1)] row maximum of l / T
+  double* dbg_ratio;  // [B K] q(x~)/p(x~), not clamped
 };
 
 // Launchers (sv_kernels.cu). `aligned`: 16-byte aligned rows (vector-load path).

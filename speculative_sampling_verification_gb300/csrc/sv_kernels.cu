@@ -2,25 +2,31 @@
 // rejection sampling: §4.2 and Algorithm 2 of "Accelerating Large Language
 // Model Decoding with Speculative Sampling", wikillm.com paper card).
 //
-// Two kernels per call, neither of which ever waits on another CTA:
+// The verification step takes one of two launch shapes, chosen per call by
+// the bytes it streams:
 //
-//   stats_kernel   one CTA per row segment (at most 32 KB; sequence-major, so
-//       sequences complete one after another). 16-byte vector loads, four per
-//       thread in flight, reduce the segment to its maximum m and
-//       sum_i 2^((l_i - m) log2(e)/T), the temperature transform of §4.2
-//       "Decoding transforms". The CTA that counts the last segment of a
-//       sequence runs its scan: combine segments, gather the logits at the
-//       drafted tokens, thresholds min(1, q/p) in fp64, first rejection j
-//       (Algorithm 2 step 3), and the plan of the draw.
-//   draw_kernel    one CTA per 4096-element chunk of the row pair the draw
-//       needs (target and draft row j for the residual (q - p)_+, or target
-//       row K for the bonus token, Algorithm 2 step 4): float-float sums of
-//       exp((l - m)/T) and of the residual's positive part per 512-element
-//       sub-chunk. The CTA that counts the last chunk of a sequence runs the
-//       exact inverse-CDF search, in float-float, for the drawn token.
+//   stats_kernel + draw_kernel (small and very large calls). stats_kernel has
+//       one warp per row segment (at most 32 KB, sequence-major so that
+//       sequences complete one after another): each lane keeps eight 16-byte
+//       loads in flight per round and reduces its share to the segment's
+//       maximum m and sum_i 2^((l_i - m) log2(e)/T), the temperature transform
+//       of §4.2 "Decoding transforms", with no shared memory and no barrier.
+//       The warp that counts a row's last segment combines the row; the warp
+//       that counts a sequence's last row runs its scan (scan_warp): logits at
+//       the drafted tokens, thresholds min(1, q/p) in float-float, the first
+//       rejection j (Algorithm 2 step 3) and the plan of the draw.
+//       draw_kernel, a programmatic dependent of stats_kernel, has one CTA per
+//       chunk of the row pair the draw needs (target and draft row j for the
+//       residual (q - p)_+, or target row K for the bonus token, Algorithm 2
+//       step 4): float-float sums per sub-chunk, and in the CTA that counts a
+//       sequence's last chunk the exact inverse-CDF search for the token.
+//   fused_kernel (mid-sized calls). The same warp and chunk code in one
+//       launch: CTAs take tickets, streaming items first, then draw chunks,
+//       each of which waits (bounded) for its sequence's plan.
 //
-// Completion counting uses acquire-release atomics ("last CTA to arrive does
-// the follow-up"), so no CTA spins and no co-residency is assumed.
+// Hand-offs use acquire-release counters ("the last to arrive does the
+// follow-up"); only the fused kernel's draw CTAs ever wait, and every wait
+// gives up after a fixed time.
 #include <cfloat>
 #include <math_constants.h>
 #include <climits>
@@ -338,6 +344,9 @@ SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
     if (P.dbg_lse)  // lse = m/T + ln S, only for the debug export
       P.dbg_lse[b * R + r] = rb ? __longlong_as_double(0x7ff8000000000000LL)
                                 : (double)st.x * P.inv_t + log((double)st.y);
+    if (P.dbg_max)  // max_i l_i / T
+      P.dbg_max[b * R + r] = rb ? __longlong_as_double(0x7ff8000000000000LL)
+                                : (double)st.x * P.inv_t;
   }
   bits = __reduce_or_sync(0xffffffffu, bits);
   __syncwarp();
@@ -359,11 +368,13 @@ SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
       }
       const float mq = ws.m[t], mp = ws.m[K + 1 + t];
       const float sq = ws.s[t], sp = ws.s[K + 1 + t];
-      double thr;
+      double thr, ratio = 0.0;
       if (lq == neg_inf()) {
         thr = 0.0;  // q(x~) = 0 rejects
+        ratio = 0.0;
       } else if (lp == neg_inf()) {
         thr = 1.0;  // p(x~) = 0 < q(x~) accepts
+        ratio = __longlong_as_double(0x7ff0000000000000LL);
       } else {
         const bool unit_t = P.unit_t != 0;
         const ff xq = scaled_diff(lq, mq, P.ih, P.il, unit_t);
@@ -378,14 +389,17 @@ SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
           const ff rem = ff_sub(num, ff_mul_f(den, q1));
           const double r = ff_to_double(fast_two_sum(q1, __fdiv_rn(rem.hi, den.hi)));
           thr = r >= 1.0 ? 1.0 : r;
+          ratio = r;
         } else {
           const double lr = ((double)lq - (double)lp) * P.inv_t -
                             (((double)mq - (double)mp) * P.inv_t + log((double)sq / (double)sp));
           thr = lr >= 0.0 ? 1.0 : exp(lr);
+          if (P.dbg_ratio) ratio = exp(lr);
         }
       }
       ws.thr[t] = thr;
       if (P.dbg_thr) P.dbg_thr[b * K + t] = thr;
+      if (P.dbg_ratio) P.dbg_ratio[b * K + t] = ratio;
     }
   }
   __syncwarp();
@@ -404,6 +418,17 @@ SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
       }
     }
   }
+  // Outputs other than the drawn token. Position j also gets -1 here, before
+  // the plan is released: the draw overwrites it, so a draw that never
+  // completes (the fused kernel's bounded wait ran out) leaves -1 there
+  // rather than whatever the buffer held.
+  for (int t = lane; t <= K; t += 32) {
+    if (j < 0 || t >= j)
+      P.out_tokens[b * (K + 1) + t] = -1;
+    else
+      P.out_tokens[b * (K + 1) + t] = ws.tok[t];
+  }
+  __syncwarp();
   if (lane == 0) {
     Plan pl{};
     if (bits) {
@@ -434,16 +459,16 @@ SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
       P.n_acc[b] = j;
     }
     P.plans[b] = pl;
+    // The release is cumulative: with the warp barrier above it also orders
+    // the other lanes' output stores before the draw CTAs' acquire.
     if (P.fused && !P.withhold) st_release_u32(P.ready + b, 1u);  // for the fused kernel's draw CTAs
   }
-  for (int t = lane; t <= K; t += 32) {
-    if (j < 0 || t > j)
-      P.out_tokens[b * (K + 1) + t] = -1;
-    else if (t < j)
-      P.out_tokens[b * (K + 1) + t] = ws.tok[t];
+  if (bits) {
+    for (int t = lane; t < K; t += 32) {
+      if (P.dbg_thr) P.dbg_thr[b * K + t] = __longlong_as_double(0x7ff8000000000000LL);
+      if (P.dbg_ratio) P.dbg_ratio[b * K + t] = __longlong_as_double(0x7ff8000000000000LL);
+    }
   }
-  if (P.dbg_thr && bits)
-    for (int t = lane; t < K; t += 32) P.dbg_thr[b * K + t] = __longlong_as_double(0x7ff8000000000000LL);
 }
 
 // ---------------------------------------------------------------- draw: shared element code

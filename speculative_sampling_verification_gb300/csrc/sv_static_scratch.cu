@@ -30,16 +30,26 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 void* g_scratch_ptr[64] = {};
 std::mutex g_scratch_mu;
 
-// Device address of the scratch on `device` (which must be current); looked
-// up once per device, at that device's first call.
-cudaError_t scratch_address(int device, void** out) {
+// Device address of the scratch on `device` (which must be current). The
+// address belongs to the current context, so outside stream capture it is
+// looked up afresh on every call: a context created after cudaDeviceReset, or
+// another context made current by the driver API, gets its own address. While
+// `stream` is being captured the last address looked up on this device is
+// used instead, so that the capture makes no lookup; a call made outside
+// capture on the same device and context must come first.
+cudaError_t scratch_address(int device, cudaStream_t stream, void** out) {
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[device]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_ptr[device] = p;
+  } else if (!g_scratch_ptr[device]) {
+    return cudaErrorStreamCaptureUnsupported;
   }
   *out = g_scratch_ptr[device];
   return cudaSuccess;
@@ -61,7 +71,8 @@ extern "C" int spec_verify_static(const void* target_logits, const void* draft_l
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return SV_ERR_CUDA;
   void* scratch = nullptr;
-  if (scratch_address(device, &scratch) != cudaSuccess) return SV_ERR_CUDA;
+  if (scratch_address(device, static_cast<cudaStream_t>(stream), &scratch) != cudaSuccess)
+    return SV_ERR_CUDA;
   return spec_verify(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype,
                      temperature, out_tokens, n_accepted, scratch, kStaticScratchBytes, stream);
 }

@@ -7,8 +7,8 @@ fed from here, and neither imports the other.
 """
 
 from .configs import WORKLOADS, SWEEP_K, SWEEP_NOISE, Workload, sweep_workload, get_workload
-from .generate import (DTYPES, make_inputs, make_sequence, make_topk_inputs, make_topp_inputs,
-                       topk_draft_tokens, topp_draft_tokens)
+from .generate import (DTYPES, make_batch, make_inputs, make_sequence, make_topk_inputs,
+                       make_topp_inputs, topk_draft_tokens, topp_draft_tokens)
 
 __all__ = [
     "WORKLOADS",
@@ -18,6 +18,7 @@ __all__ = [
     "sweep_workload",
     "get_workload",
     "make_inputs",
+    "make_batch",
     "make_sequence",
     "make_topk_inputs",
     "topk_draft_tokens",

@@ -154,3 +154,60 @@ def make_topp_inputs(w: Workload, top_p: float, step: int = 0, seqs=None, pin_me
         inp["tokens"][i] = topp_draft_tokens(inp["draft"][i], top_p, w.temperature,
                                              _gen(w, step, b, 4))
     return inp
+
+
+def make_batch(w: Workload, step: int = 0, device="cpu", rows_per_chunk: int = 64):
+    """The recipe of `make_inputs`, drawn for the whole batch at once from one
+    torch generator on `device` (the device's own generator: on a GPU, torch's
+    counter-based Philox), for workloads too large to draw sequence by
+    sequence on the host. Same shapes, dtypes and distributions; the values
+    differ from `make_inputs`, and are reproducible for a given device type,
+    seed and step.
+
+    * target logits N(0, target_std^2) in fp32, plus `peak_boost` on `peaks`
+      distinct ids per target row (the ids of the row's `peaks` largest
+      uniform draws, a uniformly random subset);
+    * draft row t = target row t + N(0, noise^2), t < K;
+    * both rounded to the workload dtype (bf16: round to nearest even);
+    * drafts by the Gumbel-max trick in fp64, argmax_i(dl[t,i]/T + G_i), an
+      exact draw from softmax(dl[t]/T), `rows_per_chunk` draft rows at a time;
+    * K+2 fp32 uniforms in [0, 1) per sequence.
+    """
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(_mix(w.seed, step, 0x5EED))
+    dtype = DTYPES[w.dtype]
+    B, K, V = w.B, w.K, w.V
+    tl = torch.randn(B, K + 1, V, generator=g, device=dev)
+    tl.mul_(w.target_std)
+    if w.peaks:
+        for r in range(K + 1):
+            pick = torch.rand(B, V, generator=g, device=dev)
+            ids = torch.topk(pick, w.peaks, dim=-1).indices
+            tl[:, r].scatter_add_(-1, ids, torch.full(ids.shape, float(w.peak_boost), device=dev))
+            del pick, ids
+    noise = torch.randn(B, K, V, generator=g, device=dev)
+    noise.mul_(w.draft_noise_std)
+    noise.add_(tl[:, :K])
+    draft = noise.to(dtype)
+    del noise
+    target = tl.to(dtype)
+    del tl
+    rows = draft.view(B * K, V)
+    tokens = torch.empty(B * K, dtype=torch.int32, device=dev)
+    inv_t = 1.0 / float(w.temperature)
+    for r0 in range(0, B * K, rows_per_chunk):
+        r1 = min(B * K, r0 + rows_per_chunk)
+        u = torch.rand(r1 - r0, V, dtype=torch.float64, generator=g, device=dev)
+        gumbel = u.log_().neg_().log_().neg_()
+        gumbel.add_(rows[r0:r1].to(torch.float64) * inv_t)
+        tokens[r0:r1] = torch.argmax(gumbel, dim=-1).to(torch.int32)
+        del u, gumbel
+    uniforms = torch.rand(B, K + 2, generator=g, device=dev, dtype=torch.float32)
+    return {
+        "target": target,
+        "draft": draft,
+        "tokens": tokens.view(B, K),
+        "uniforms": uniforms,
+        "temperature": float(w.temperature),
+    }

@@ -14,6 +14,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 MARGIN = 1e-6
+RATE_MIN_DECISIONS = 100_000
 
 
 @dataclass
@@ -32,9 +33,21 @@ class ParityReport:
         self.failures += other.failures
 
     def assert_ok(self, max_excused_rate: float | None = None) -> None:
+        """No unexcused difference, and excused differences at most
+        `max_excused_rate` of the decisions. Below RATE_MIN_DECISIONS decisions
+        the rate cannot be resolved, so one excused difference is allowed;
+        from there on the plain rate applies."""
         assert not self.failures, self.failures[:10]
         if max_excused_rate is not None and self.decisions:
-            assert self.excused <= max(1, max_excused_rate * self.decisions), self
+            allowed = max_excused_rate * self.decisions
+            if self.decisions < RATE_MIN_DECISIONS:
+                allowed = max(1, allowed)
+            assert self.excused <= allowed, self
+
+    def as_dict(self) -> dict:
+        return {"sequences": self.sequences, "decisions": self.decisions,
+                "near_threshold": self.near_threshold, "excused_differences": self.excused,
+                "unexcused_differences": len(self.failures)}
 
 
 def compare(out, nacc, ref, drafts) -> ParityReport:

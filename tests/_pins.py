@@ -148,6 +148,13 @@ def pin_golden(O):
         assert bool(r.residual_fallback[0]) == c["expected_fallback"], name
         np.testing.assert_allclose(r.thresholds[0], c["expected_thresholds"], atol=1e-6,
                                    err_msg=name)
+        exp_r = np.array([float(v) for v in c["expected_ratios"]])
+        np.testing.assert_allclose(r.ratios[0], exp_r, rtol=1e-6, err_msg=name)
+        # Logits are ln(prob) at T = 1, so each row's maximum is the log of its
+        # largest probability (the probabilities of a row sum to one).
+        rows = list(c["target_probs"]) + list(c["draft_probs"])
+        np.testing.assert_allclose(r.row_max[0], [np.log(max(pr)) for pr in rows], atol=1e-6,
+                                   err_msg=name)
         exp_m = np.array([np.nan if v is None else v for v in c["expected_accept_margins"]])
         np.testing.assert_allclose(r.accept_margin[0], exp_m, atol=1e-6, err_msg=name)
         np.testing.assert_allclose(r.sample_margin[0], c["expected_sample_margin"], atol=1e-6,

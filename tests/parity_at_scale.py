@@ -1,0 +1,271 @@
+"""Parity at scale: the CUDA path against the fp64 oracle over whole batches.
+
+    python -m tests.parity_at_scale [--configs c2,c3,c4,sweep] [--min-decisions 100000]
+                                    [--min-decisions-cell 10000] [--out FILE]
+
+For every workload, steps are drawn on the GPU by the batched seeded
+generator, verified there through the C ABI (spec_verify_debug, whole batch),
+and every sequence of every step is verified again by the fp64 oracle on the
+host cores (a spawn pool, one process per core, fed through .npy files). Steps
+are added until the oracle has taken at least --min-decisions decisions (for
+each of the 20 cells of the acceptance sweep, --min-decisions-cell).
+
+Per workload the record holds the sequences and decisions checked, the
+decisions whose uniform lies within 1e-6 of the oracle's threshold
+(`near_threshold`: a property of the inputs), the differences at such
+decisions (`excused_differences`), and any other difference
+(`unexcused_differences`, which must be 0). It also holds the largest
+relative differences of the intermediate values (per-row log-sum-exp and
+maximum, thresholds, ratios q/p, drawn token's probability) and how many
+exceed their tolerance. The parity bar is the verification step's: no
+unexcused difference, and excused differences below 1e-5 of the decisions.
+"""
+
+from __future__ import annotations
+
+import argparse
+import collections
+import json
+import os
+import shutil
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from tests import _parity  # noqa: E402
+
+# Relative tolerances of the intermediate values (those of tests/test_gpu_parity.py).
+TOL = {"row_lse": 1e-5, "thresholds": 1e-5, "ratios": 1e-5, "row_max": 1e-12,
+       "sample_prob": 1e-8}
+MAX_EXCUSED_RATE = 1e-5
+
+
+# ---------------------------------------------------------------- oracle side (spawned workers)
+
+def _load(paths):
+    t, d, k, u = (np.load(p, mmap_mode="r") for p in paths)
+    if t.dtype == np.uint16:  # bf16 bit patterns: widen exactly to fp32
+        t = (t.astype(np.uint32) << np.uint32(16)).view(np.float32)
+        d = (d.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return (np.ascontiguousarray(t), np.ascontiguousarray(d), np.asarray(k).astype(np.int64),
+            np.asarray(u))
+
+
+def oracle_job(job):
+    """The fp64 oracle over the sequences stored in `paths` (a worker process)."""
+    import oracle
+
+    paths, temperature = job
+    return oracle.verify(*_load(paths), temperature)
+
+
+# ---------------------------------------------------------------- GPU side
+
+def _to_np(t):
+    import torch
+
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def _scratch_dir() -> str:
+    try:
+        if shutil.disk_usage("/dev/shm").free > (24 << 30):
+            return "/dev/shm"
+    except Exception:
+        pass
+    return tempfile.gettempdir()
+
+
+def _rel_err(got, ref):
+    """Largest relative difference over entries finite on both sides, and the
+    count of entries whose infinities or NaNs differ."""
+    got, ref = np.asarray(got, dtype=np.float64), np.asarray(ref, dtype=np.float64)
+    fin = np.isfinite(got) & np.isfinite(ref)
+    mismatch = int(np.sum(~fin & ~((got == ref) | (np.isnan(got) & np.isnan(ref)))))
+    if not fin.any():
+        return 0.0, mismatch
+    den = np.maximum(np.abs(ref[fin]), 1e-300)
+    return float(np.max(np.abs(got[fin] - ref[fin]) / den)), mismatch
+
+
+class Intermediates:
+    def __init__(self):
+        self.max_rel = {k: 0.0 for k in TOL}
+        self.over = {k: 0 for k in TOL}
+
+    def add(self, dbg, ref, seqs):
+        ok = ref.status == 0
+        pairs = {"row_lse": ref.lse, "thresholds": ref.thresholds, "ratios": ref.ratios,
+                 "row_max": ref.row_max, "sample_prob": ref.sample_prob}
+        for k, r in pairs.items():
+            g = dbg[k][seqs][ok]
+            r = r[ok]
+            # the tests' absolute floors: thresholds 1e-9, lse 1e-6, probabilities 1e-15
+            floor = {"row_lse": 1e-6, "thresholds": 1e-9, "sample_prob": 1e-15}.get(k, 0.0)
+            err, bad = _rel_err(g, r)
+            self.max_rel[k] = max(self.max_rel[k], err)
+            fin = np.isfinite(g) & np.isfinite(r)
+            over = np.abs(g[fin] - r[fin]) > TOL[k] * np.abs(r[fin]) + floor
+            self.over[k] += int(over.sum()) + bad
+
+    def as_dict(self):
+        return {"tolerance": TOL, "max_rel_diff": self.max_rel, "over_tolerance": self.over}
+
+
+def check_workload(sv, w, dev, pool, workers, tmp, min_decisions, max_steps=100_000,
+                   step_base=7000, depth=None, log=print):
+    """Whole-batch parity of workload `w`: returns its record."""
+    import torch
+
+    from synthetic import make_batch
+
+    B, K, V = w.B, w.K, w.V
+    dt = sv.SV_BF16 if w.dtype == "bf16" else sv.SV_F32
+    ws = sv.new_workspace(B, K, V, dt, dev)
+    per_seq = (2 * K + 1) * V * 25e-9
+    per = max(1, min(B, int(0.25 / per_seq)))
+    chunks = [list(range(s, min(B, s + per))) for s in range(0, B, per)]
+    depth = depth or max(2, -(-2 * workers // len(chunks)))
+    rep = _parity.ParityReport()
+    inter = Intermediates()
+    pending = collections.deque()
+    statuses = 0
+    step = 0
+    need_steps = max_steps
+    t0 = time.time()
+
+    def settle(item):
+        nonlocal need_steps
+        s, jobs, out, nacc, tokens, dbg, files = item
+        for seqs, res in jobs:
+            ref = res.get()
+            rep.add(_parity.compare(out[seqs], nacc[seqs], ref, tokens[seqs]))
+            inter.add(dbg, ref, seqs)
+        for f in files:
+            try:
+                os.remove(f)
+            except OSError:
+                pass
+        if need_steps == max_steps and rep.decisions:
+            done = s - step_base + 1
+            need_steps = min(max_steps, int(np.ceil(min_decisions * done / rep.decisions)))
+
+    while step < need_steps:
+        inp = make_batch(w, step=step_base + step, device=dev)
+        out, nacc, dbg = sv.verify(inp["target"], inp["draft"], inp["tokens"], inp["uniforms"],
+                                   inp["temperature"], workspace=ws, debug=True)
+        torch.cuda.synchronize()
+        statuses |= sv.sv_read_device_status(ws)
+        dbg_np = {k: v.cpu().numpy() for k, v in dbg.items() if k != "workspace"}
+        files, jobs = [], []
+        for ci, seqs in enumerate(chunks):
+            idx = torch.as_tensor(seqs, device=dev)
+            paths = []
+            for k in ("target", "draft", "tokens", "uniforms"):
+                p = os.path.join(tmp, f"{w.name}-{step}-{ci}-{k}.npy")
+                np.save(p, _to_np(inp[k].index_select(0, idx)))
+                paths.append(p)
+            files += paths
+            jobs.append((seqs, pool.apply_async(oracle_job, ((paths, inp["temperature"]),))))
+        pending.append((step_base + step, jobs, out.cpu().numpy(), nacc.cpu().numpy(),
+                        inp["tokens"].cpu().numpy(), dbg_np, files))
+        del inp, out, nacc, dbg
+        step += 1
+        while pending and (len(pending) > depth or all(r.ready() for _, r in pending[0][1])):
+            settle(pending.popleft())
+    while pending:
+        settle(pending.popleft())
+    dt = time.time() - t0
+    d = rep.as_dict()
+    d.update({"workload": w.name, "steps": step, "device_status": statuses,
+              "excused_rate": rep.excused / max(1, rep.decisions),
+              "intermediates": inter.as_dict(), "seconds": round(dt, 1),
+              "failures": [str(f)[:300] for f in rep.failures[:5]]})
+    d["pass"] = (not rep.failures and statuses == 0 and rep.excused <= MAX_EXCUSED_RATE
+                 * rep.decisions and not any(inter.over.values()))
+    log(json.dumps({k: d[k] for k in ("workload", "steps", "sequences", "decisions",
+                                      "near_threshold", "excused_differences",
+                                      "unexcused_differences", "seconds", "pass")}))
+    del ws
+    torch.cuda.empty_cache()
+    return d
+
+
+def workload_list(configs: str):
+    from synthetic import SWEEP_K, SWEEP_NOISE, get_workload
+
+    out = []
+    for name in configs.split(","):
+        if name == "sweep":
+            out += [(get_workload(f"sweep-k{k}-n{n:g}"), True) for k in SWEEP_K
+                    for n in SWEEP_NOISE]
+        else:
+            out.append((get_workload(name), False))
+    return out
+
+
+def run(configs="c2,c3,c4,sweep", min_decisions=100_000, min_decisions_cell=10_000,
+        workers=None, out=None, log=print):
+    import multiprocessing as mp
+
+    workers = workers or max(1, len(os.sched_getaffinity(0)) - 1)
+    pool = mp.get_context("spawn").Pool(workers)  # before any CUDA work
+    tmp = tempfile.mkdtemp(prefix="sv-parity-", dir=_scratch_dir())
+    try:
+        import torch
+
+        import speculative_sampling_verification_gb300 as sv
+
+        sv.load_library(build=True)
+        dev = torch.device("cuda:0")
+        records = []
+        for w, cell in workload_list(configs):
+            records.append(check_workload(sv, w, dev, pool, workers, tmp,
+                                          min_decisions_cell if cell else min_decisions,
+                                          log=log))
+    finally:
+        pool.terminate()
+        pool.join()
+        shutil.rmtree(tmp, ignore_errors=True)
+    tot = _parity.ParityReport()
+    for r in records:
+        tot.add(_parity.ParityReport(r["sequences"], r["decisions"], r["excused_differences"],
+                                     r["near_threshold"]))
+    totals = tot.as_dict()
+    totals["unexcused_differences"] = sum(r["unexcused_differences"] for r in records)
+    totals["excused_rate"] = tot.excused / max(1, tot.decisions)
+    summary = {"when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()),
+               "command": "python -m tests.parity_at_scale " + " ".join(sys.argv[1:]),
+               "margin": _parity.MARGIN, "max_excused_rate": MAX_EXCUSED_RATE,
+               "oracle_workers": workers, "totals": totals,
+               "pass": all(r["pass"] for r in records), "workloads": records}
+    if out:
+        with open(out, "w") as f:
+            json.dump(summary, f, indent=1)
+    return summary
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--configs", default="c2,c3,c4,sweep")
+    ap.add_argument("--min-decisions", type=int, default=100_000)
+    ap.add_argument("--min-decisions-cell", type=int, default=10_000)
+    ap.add_argument("--workers", type=int, default=None)
+    ap.add_argument("--out", default=None)
+    a = ap.parse_args()
+    s = run(a.configs, a.min_decisions, a.min_decisions_cell, a.workers, a.out)
+    print(json.dumps({"pass": s["pass"], "totals": s["totals"]}))
+    sys.exit(0 if s["pass"] else 1)
+
+
+if __name__ == "__main__":
+    main()

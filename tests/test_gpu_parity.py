@@ -55,10 +55,17 @@ def run_gpu(inp: dict, misalign: bool = False):
 def check_intermediates(dbg, ref, seqs=None):
     ok = ref.status == 0
     lse, thr, prob = dbg["row_lse"], dbg["thresholds"], dbg["sample_prob"]
+    rmax, ratio = dbg["row_max"], dbg["ratios"]
     if seqs is not None:
-        lse, thr, prob = lse[seqs], thr[seqs], prob[seqs]
+        lse, thr, prob, rmax, ratio = lse[seqs], thr[seqs], prob[seqs], rmax[seqs], ratio[seqs]
     np.testing.assert_allclose(lse[ok], ref.lse[ok], rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(thr[ok], ref.thresholds[ok], rtol=1e-5, atol=1e-9)
+    # the row maximum is one of the row's logits over T: equal up to fp64 rounding
+    np.testing.assert_allclose(rmax[ok], ref.row_max[ok], rtol=1e-12, atol=0)
+    # the ratio q/p itself, also where it exceeds 1 (the threshold is clamped there);
+    # +inf (p = 0 < q) and 0 (q = 0) must match exactly
+    np.testing.assert_allclose(ratio[ok], ref.ratios[ok], rtol=1e-5, atol=1e-300)
+    assert np.array_equal(np.isinf(ratio[ok]), np.isinf(ref.ratios[ok]))
     # the drawn token's normalised weight comes from the float-float pass
     np.testing.assert_allclose(prob[ok], ref.sample_prob[ok], rtol=1e-8, atol=1e-15)
 
@@ -105,6 +112,8 @@ def test_golden_hand_cases_on_gpu():
         assert out[0].tolist() == c["expected_out"], (c["name"], out[0])
         assert int(nacc[0]) == c["expected_n_accepted"], c["name"]
         np.testing.assert_allclose(dbg["thresholds"][0], c["expected_thresholds"], atol=1e-6)
+        np.testing.assert_allclose(dbg["ratios"][0], [float(v) for v in c["expected_ratios"]],
+                                   rtol=1e-6)
         np.testing.assert_allclose(dbg["sample_prob"][0], c["expected_sample_prob"], atol=1e-6)
 
 

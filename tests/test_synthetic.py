@@ -63,3 +63,50 @@ def test_sweep_cells():
             w = get_workload(f"sweep-k{k}-n{n:g}")
             assert w.B == 32 and w.V == 151936 and w.K == k and w.draft_noise_std == n
     assert WORKLOADS["c3"].ideal_bytes_per_step() == 64 * 19 * 128256 * 2
+
+
+def test_make_batch_follows_the_recipe():
+    """The batched generator: shapes, dtypes, value distributions, peaks,
+    drafts inside the vocabulary, uniforms in [0, 1), reproducible by step."""
+    from synthetic import make_batch
+
+    w = shrink(WORKLOADS["c3"], B=3, V=20000)
+    a = make_batch(w, step=5)
+    b = make_batch(w, step=5)
+    for k in ("target", "draft", "tokens", "uniforms"):
+        assert torch.equal(a[k], b[k])
+    assert not torch.equal(a["target"], make_batch(w, step=6)["target"])
+    assert a["target"].shape == (3, w.K + 1, w.V) and a["target"].dtype == torch.bfloat16
+    assert a["draft"].shape == (3, w.K, w.V) and a["draft"].dtype == torch.bfloat16
+    assert a["tokens"].dtype == torch.int32 and ((a["tokens"] >= 0) & (a["tokens"] < w.V)).all()
+    u = a["uniforms"]
+    assert u.shape == (3, w.K + 2) and u.dtype == torch.float32 and ((u >= 0) & (u < 1)).all()
+    t = a["target"].float()
+    top = torch.topk(t, w.peaks + 1, dim=-1).values
+    assert (top[..., w.peaks - 1] > 3.0).all()          # 32 boosted ids per row
+    body = t[t < 6.0]
+    assert abs(body.std().item() - w.target_std) < 0.2
+    gap = (a["draft"].float() - t[:, : w.K]).std().item()
+    assert abs(gap - w.draft_noise_std) < 0.05          # noise, plus bf16 rounding
+    # the drafted token is typically among the draft row's largest logits
+    d = a["draft"].float()
+    at = torch.gather(d, -1, a["tokens"].long()[..., None])[..., 0]
+    assert (at > torch.quantile(d[0, 0], 0.99)).float().mean() > 0.9
+
+
+def test_make_batch_drafts_follow_draft_softmax():
+    """Gumbel-max drafts of the batched generator follow softmax(dl/T): every
+    sequence has its own row, so the law is checked through the drafted
+    token's probability, whose mean under x~ ~ p is E[sum_i p_i^2]."""
+    from synthetic import make_batch
+
+    w = shrink(WORKLOADS["c1"], B=40000, K=1, V=5, target_std=1.0, draft_noise_std=0.5,
+               temperature=0.8)
+    a = make_batch(w, step=0)
+    d = a["draft"][:, 0].double()
+    p = torch.softmax(d / 0.8, dim=-1)
+    chosen = torch.gather(p, -1, a["tokens"].long())[:, 0]
+    # E[p(x~)] under x~ ~ p equals sum_i p_i^2 per row
+    expect = (p * p).sum(-1).mean().item()
+    got = chosen.mean().item()
+    assert abs(got - expect) < 4 * (p * p).sum(-1).std().item() / 200 + 0.005
