@@ -66,6 +66,11 @@ def parse():
     ap.add_argument("--sub", default="c3,sweep",
                     help="verify: workloads measured after the headline, as sub-records")
     ap.add_argument("--no-sub", action="store_true")
+    ap.add_argument("--ncu-case", type=int, default=0,
+                    help="verify: run --steps calls on the workload cut to this many sequences "
+                         "and exit (a small case for ncu captures)")
+    ap.add_argument("--path", choices=["auto", "pair", "fused"], default="auto",
+                    help="verify, --ncu-case: force the kernel pair or the fused kernel")
     ap.add_argument("--op", choices=["verify", "draft_sample", "greedy", "topk", "topp"],
                     default="verify",
                     help="verify: the verification step (default); draft_sample: the draft-side "
@@ -385,8 +390,9 @@ def time_sub_workload(sv, name: str, dev, stream, reps_min_s: float = 0.25, step
     ws = sv.new_workspace(B, K, V, dt_code, dev)
     scrub = torch.empty(3 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     T = w.temperature
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
+    # external: recorded inside the graph as timing nodes
+    evs = [(torch.cuda.Event(enable_timing=True, external=True),
+            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(steps)]
 
     def call(i):
         s = sets[i % n_sets]
@@ -484,12 +490,38 @@ def bench_config(w) -> dict:
     return {"workload": w.name, "detail": w.describe()}
 
 
+def run_ncu_case(args, w, dev, sv):
+    """A small case of the workload for ncu: its first `--ncu-case` sequences,
+    `--steps` verification calls on one input set, on the chosen kernel path."""
+    from synthetic.configs import shrink
+
+    w = shrink(w, B=min(w.B, args.ncu_case))
+    sv.sv_force_path({"auto": 0, "pair": 1, "fused": 2}[args.path])
+    inp = make_batch(w, step=1, device=dev)
+    dt_code = sv.SV_BF16 if w.dtype == "bf16" else sv.SV_F32
+    ws = sv.new_workspace(w.B, w.K, w.V, dt_code, dev)
+    out = torch.empty(w.B, w.K + 1, dtype=torch.int32, device=dev)
+    nacc = torch.empty(w.B, dtype=torch.int32, device=dev)
+    for _ in range(max(1, args.steps)):
+        rc = sv.spec_verify(inp["target"], inp["draft"], inp["tokens"], inp["uniforms"],
+                            w.temperature, out, nacc, ws)
+        if rc != 0:
+            raise RuntimeError(sv.sv_status_string(rc))
+    torch.cuda.synchronize()
+    if sv.sv_read_device_status(ws) != 0:
+        raise RuntimeError("bad device status")
+    print(json.dumps({"ncu_case": w.name, "B": w.B, "path": args.path, "calls": args.steps,
+                      "mean_accepted": float(nacc.float().mean())}))
+
+
 def run_ours(args, w, world, rank, local):
     import speculative_sampling_verification_gb300 as sv
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sv.load_library(build=True)
+    if args.ncu_case:
+        return run_ncu_case(args, w, dev, sv)
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     host = OracleHost(host_cores()) if want_cpu else None  # spawned before any GPU work
     try:

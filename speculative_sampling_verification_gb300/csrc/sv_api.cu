@@ -98,6 +98,12 @@ static void fill_params(sv::Params& P, const sv::Layout& L, int B, int K, int V,
   P.il = (float)(inv - (double)P.ih);
   P.unit_t = temperature == 1.0f ? 1 : 0;
   P.inv_t = inv;
+  {
+    const double C = T * 0.69314718055994530942 / 1024.0;
+    P.d_ch = (float)C;
+    P.d_cli = (float)((C - (double)P.d_ch) * inv);
+    P.d_inv = (float)(1.0 / C);
+  }
   P.rows_per_seq = L.rows_per_seq;
   P.nseg = L.nseg;
   P.seg_elems = L.seg_elems;

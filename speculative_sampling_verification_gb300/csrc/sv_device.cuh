@@ -310,4 +310,87 @@ SV_DEVINL ff2 scaled_diff2(float2 l, float2 nm, float ih, float il, bool unit_t)
   return {ph, lo};
 }
 
+// ---------------------------------------------------------------- the draw's exponentials
+//
+// The draw needs w = exp(l/T) 2^-q0 for every element l of the one or two
+// rows it reads, with q0 a per-row integer (above the row maximum's
+// log2(e) m/T, so that every w is below 2). Elements scale by a power of two
+// at most 2^0; a binary exponent field q + 127 <= 0 (the element more than
+// 2^126 below the row maximum, or -inf) gives exactly 0. `qb` is 127 - q0.
+
+// Constants of the fast reduction, per call: with C = T ln2/1024,
+// ch = fp32(C), cli = fp32((C - ch)/T), inv = fp32(1024/(T ln2)), ih = fp32(1/T).
+struct DrawConst {
+  float inv, ch, cli, ih;
+};
+
+// The fast exponential of one element, used by the chunk pass (packed below,
+// scalar here; both give the same bits). k = rint(l inv); r = l - k ch is
+// exact (|r| < ch and the exact value spans at most 23 bits); s = r/T - k
+// cli = (l - k C)/T, |s| <= ln2/2048 + 1e-5, rounded once (2.4e-11 of the
+// value). exp(l/T) = 2^(k >> 10) (Th + Tl)(1 + u), 2^((k & 1023)/1024) = Th + Tl
+// from the table, u = e^s - 1 = s + s^2/2 + s^3/6 (the next term is below 6e-16).
+// The result is the unnormalised float-float (Th, fl(Th u + Tl)) scaled by
+// 2^(q - q0): its low part is at most 3.6e-4 of its head and is rounded once,
+// so the value carries a relative error of about 5e-11, of either sign.
+// Valid for |l/T| <= 2048 (|k| < 2^22); callers clamp below and take the
+// shifted path for rows whose maximum is beyond that.
+SV_DEVINL ff exp_draw(float l, int qb, const DrawConst& dc, const float2* tab) {
+  const float ym = __fmaf_rn(l, -dc.inv, kRoundMagic);   // 1.5 2^23 - k
+  const float nkf = __fsub_rn(ym, kRoundMagic);           // -k
+  const float r = __fmaf_rn(nkf, dc.ch, l);               // l - k ch, exact
+  const float sv = __fmaf_rn(r, dc.ih, __fmul_rn(nkf, dc.cli));
+  const float h = __fmul_rn(__fmaf_rn(sv, 1.0f / 6.0f, 0.5f), sv);
+  const float u = __fmaf_rn(sv, h, sv);
+  const int k = __float_as_int(kRoundMagic) - __float_as_int(ym);
+  const float2 T = tab[k & 1023];
+  const float lo = __fmaf_rn(T.x, u, T.y);
+  const float scale = __int_as_float(max((k >> 10) + qb, 0) << 23);
+  return {__fmul_rn(T.x, scale), __fmul_rn(lo, scale)};
+}
+
+// exp_draw on each lane of a pair (lane x with qb.x, lane y with qb.y).
+SV_DEVINL ff2 exp_draw2(float2 l, int2 qb, const DrawConst& dc, const float2* tab) {
+  const float2 ym = f2_fma(l, f2(-dc.inv), f2(kRoundMagic));
+  const float2 nkf = f2_sub(ym, f2(kRoundMagic));
+  const float2 r = f2_fma(nkf, f2(dc.ch), l);
+  const float2 sv = f2_fma(r, f2(dc.ih), f2_mul(nkf, f2(dc.cli)));
+  const float2 h = f2_mul(f2_fma(sv, f2(1.0f / 6.0f), f2(0.5f)), sv);
+  const float2 u = f2_fma(sv, h, sv);
+  const int kx = __float_as_int(kRoundMagic) - __float_as_int(ym.x);
+  const int ky = __float_as_int(kRoundMagic) - __float_as_int(ym.y);
+  const float2 Tx = tab[kx & 1023], Ty = tab[ky & 1023];
+  const float2 Th = make_float2(Tx.x, Ty.x);
+  const float2 lo = f2_fma(Th, u, make_float2(Tx.y, Ty.y));
+  const float2 scale = make_float2(__int_as_float(max((kx >> 10) + qb.x, 0) << 23),
+                                   __int_as_float(max((ky >> 10) + qb.y, 0) << 23));
+  return {f2_mul(Th, scale), f2_mul(lo, scale)};
+}
+
+// The same quantity, exp(l/T) 2^-q0, to about 1e-12 (the finish's weights of
+// its one sub-chunk): x = l/T as the float-float l (ih + il), then exp_ff's
+// steps (Tang's method on the 256-entry table `tab`) with the result's binary
+// exponent shifted by -q0. |x| <= 2048 keeps k within the rounding range
+// and the reduction exact.
+SV_DEVINL ff exp_precise(float l, int qb, float ih, float il, const float2* tab) {
+  const float xh = __fmul_rn(l, ih);
+  const float xl = __fmaf_rn(l, il, __fmaf_rn(l, ih, -xh));
+  const float ym = __fadd_rn(__fmul_rn(xh, SV_EXP_INV_LN2_256), kRoundMagic);
+  const float kf = __fsub_rn(ym, kRoundMagic);
+  const float t = __fmaf_rn(-kf, SV_EXP_LN2_256_HI, xh);     // exact
+  const float c = __fmaf_rn(-kf, SV_EXP_LN2_256_LO, xl);
+  const float t2 = __fmul_rn(t, t);
+  const float poly = __fmaf_rn(__fmaf_rn(t, 1.0f / 24.0f, 1.0f / 6.0f), t, 0.5f);
+  const float cc = __fmaf_rn(__fmul_rn(0.5f, c), c, c);
+  const float rest = __fmaf_rn(t2, poly, __fmaf_rn(cc, t, cc));
+  const int k = __float_as_int(ym) - __float_as_int(kRoundMagic);
+  const float2 T = tab[k & 255];
+  const ff pr = two_prod(T.x, t);
+  const ff s = fast_two_sum(T.x, pr.hi);
+  const float lo =
+      __fadd_rn(__fmaf_rn(T.x, rest, __fmaf_rn(T.y, t, T.y)), __fadd_rn(s.lo, pr.lo));
+  const float scale = __int_as_float(max((k >> 8) + qb, 0) << 23);
+  return {__fmul_rn(s.hi, scale), __fmul_rn(lo, scale)};
+}
+
 }  // namespace sv

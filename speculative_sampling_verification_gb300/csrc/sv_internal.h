@@ -155,6 +155,8 @@ struct Params {
   int B, K, V, dtype, es;
   float c2;        // log2(e) / T in fp32 (streaming pass)
   float ih, il;    // 1/T as a float-float (sampling pass)
+  float d_inv, d_ch, d_cli;  // the draw's fast reduction: 1024/(T ln2), fp32(T ln2/1024),
+                             // the rest of T ln2/1024 over T
   int unit_t;      // T == 1 exactly
   int sampler;     // 1: draft-side sampler (one row per sequence, K = 0, no scan)
   int fused;       // 1: the fused kernel runs (plans are published with a release flag)

@@ -72,6 +72,7 @@ SV_DEVINL float load_elem(const unsigned char* row, long long i) {
 
 struct CtaShared {
   float2 tab[256];  // 2^(j/256), head + tail
+  float2 tab1k[1024];  // 2^(j/1024), head + tail (the fast exponential)
   ff red4[kWarps][4];
   ff s_pref;
   Plan plan;
@@ -483,7 +484,19 @@ struct DrawRow {
   float mq, mp, sq, sp;
   float ih, il;
   bool unit_t;
+  // The fast form (rows whose maximum has |m/T| below about 1386): weights
+  // exp(l/T) 2^-q0 per row, qb = 127 - q0; alpha / beta put the streaming
+  // pass's test e_q S_p > e_p S_q (e = exp((l - m)/T)) on these weights, and
+  // lmin is the clamp that keeps every argument inside the reduction's range.
+  bool fast;
+  int2 qb;
+  float alpha, beta, lmin;
+  DrawConst dc;
 };
+
+// Exponent shift of one row in the fast form, and its factor 2^(q0 - m c2)
+// (the ratio of exp((l - m)/T) to the row's weight exp(l/T) 2^-q0).
+SV_DEVINL int row_q0(float m, float c2) { return (int)floorf(m * c2) + 1; }
 
 SV_DEVINL DrawRow draw_row(const Params& P, const Plan& pl) {
   DrawRow d;
@@ -498,6 +511,15 @@ SV_DEVINL DrawRow draw_row(const Params& P, const Plan& pl) {
   d.ih = P.ih;
   d.il = P.il;
   d.unit_t = P.unit_t != 0;
+  const bool resid = pl.mode == kModeResidual;
+  const float cq = pl.m_q * P.c2, cp = resid ? pl.m_p * P.c2 : 0.0f;
+  d.fast = fabsf(cq) <= 2000.0f && fabsf(cp) <= 2000.0f;
+  const int q0q = row_q0(pl.m_q, P.c2), q0p = resid ? row_q0(pl.m_p, P.c2) : q0q;
+  d.qb = make_int2(127 - q0q, 127 - q0p);
+  d.alpha = pl.s_p * exp2f((float)q0q - cq);
+  d.beta = resid ? pl.s_q * exp2f((float)q0p - cp) : 0.0f;
+  d.lmin = -2048.0f * __fdividef(1.0f, P.ih);
+  d.dc = DrawConst{P.d_inv, P.d_ch, P.d_cli, P.ih};
   return d;
 }
 
@@ -542,15 +564,57 @@ SV_DEVINL void load_run(const unsigned char* row, long long e, int V, bool vec_o
 // ---------------------------------------------------------------- draw: one chunk
 
 template <int DT, bool RESID, int SUB>
-SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab, bool aligned,
-                            long long b, int c) {
+SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab,
+                            const float2* tab1k, bool aligned, long long b, int c) {
   constexpr int kVec = 16 / (DT == 0 ? 2 : 4);
   constexpr int kRuns = SUB / (32 * kVec);
   static_assert(kRuns >= 1 && kRuns * 32 * kVec == SUB, "sub-chunk must be whole runs");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long e0 = ((long long)c * kSubPerChunk + w) * SUB;
   ff Sq = ff_bias_start(), Sp = ff_bias_start(), A = ff_bias_start(), Bs = ff_bias_start();
-  if (e0 < P.V) {
+  if (e0 < P.V && d.fast) {
+    // The fast form: weights exp(l/T) 2^-q0 from exp_draw2 (~5e-11).
+    const float2 lmin = f2(d.lmin);
+    if constexpr (RESID) {
+      ff2 S = {f2(1.0f), f2(0.0f)}, AB = {f2(1.0f), f2(0.0f)};
+      const float2 ab = make_float2(d.alpha, d.beta);
+#pragma unroll
+      for (int r = 0; r < kRuns; ++r) {
+        const long long e = e0 + (long long)r * 32 * kVec + lane * kVec;
+        float xq[kVec], xp[kVec];
+        load_run<DT>(d.rq, e, P.V, aligned, xq);
+        load_run<DT>(d.rp, e, P.V, aligned, xp);
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) {
+          const float2 l = make_float2(fmaxf(xq[k], lmin.x), fmaxf(xp[k], lmin.y));
+          const ff2 ex = exp_draw2(l, d.qb, d.dc, tab1k);
+          ff_accumulate_biased2(S, ex);
+          const float2 v = f2_mul(f2_add(ex.hi, ex.lo), ab);
+          if (v.x > v.y) ff_accumulate_biased2(AB, ex);
+        }
+      }
+      Sq = {S.hi.x, S.lo.x};
+      Sp = {S.hi.y, S.lo.y};
+      A = {AB.hi.x, AB.lo.x};
+      Bs = {AB.hi.y, AB.lo.y};
+    } else {
+      const int2 qb = make_int2(d.qb.x, d.qb.x);
+#pragma unroll
+      for (int r = 0; r < kRuns; ++r) {
+        const long long e = e0 + (long long)r * 32 * kVec + lane * kVec;
+        float xq[kVec];
+        load_run<DT>(d.rq, e, P.V, aligned, xq);
+#pragma unroll
+        for (int k = 0; k < kVec; k += 2) {
+          const float2 l = make_float2(fmaxf(xq[k], lmin.x), fmaxf(xq[k + 1], lmin.x));
+          const ff2 ex = exp_draw2(l, qb, d.dc, tab1k);
+          ff_accumulate_biased(Sq, {ex.hi.x, ex.lo.x});
+          ff_accumulate_biased(Sq, {ex.hi.y, ex.lo.y});
+        }
+      }
+    }
+  } else if (e0 < P.V) {
+    // The shifted form (rows with an extreme maximum): weights exp((l - m)/T).
     if constexpr (RESID) {
       // The target and draft elements side by side in the two lanes of
       // packed fp32 pairs: (S_q, S_p) and (A, B) accumulate together.
@@ -799,7 +863,25 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
       const float lq = load_elem<DT>(d.rq, e);
       ff eq, ep;
       bool pos;
-      if (use_res) {
+      if (d.fast) {
+        // The chunk pass's positive-set test (the fast weights, bit for bit),
+        // then the weights to ~1e-12 in the same scaling.
+        const float lqc = fmaxf(lq, d.lmin);
+        if (use_res) {
+          const float lpc = fmaxf(load_elem<DT>(d.rp, e), d.lmin);
+          const ff fq = exp_draw(lqc, d.qb.x, d.dc, sh.tab1k);
+          const ff fp = exp_draw(lpc, d.qb.y, d.dc, sh.tab1k);
+          pos = __fmul_rn(__fadd_rn(fq.hi, fq.lo), d.alpha) >
+                __fmul_rn(__fadd_rn(fp.hi, fp.lo), d.beta);
+          if (pos) {
+            eq = exp_precise(lqc, d.qb.x, d.ih, d.il, sh.tab);
+            ep = exp_precise(lpc, d.qb.y, d.ih, d.il, sh.tab);
+            w[k] = ff_sub(ff_mul(ff_normalize(eq), Sp), ff_mul(ff_normalize(ep), Sq));
+          }
+        } else {
+          w[k] = ff_normalize(exp_precise(lqc, d.qb.x, d.ih, d.il, sh.tab));
+        }
+      } else if (use_res) {
         const float lp = load_elem<DT>(d.rp, e);
         element_exps<true>(d, lq, lp, sh.tab, eq, ep, pos);
         if (pos) w[k] = ff_sub(ff_mul(ff_normalize(eq), Sp), ff_mul(ff_normalize(ep), Sq));
@@ -954,9 +1036,9 @@ SV_DEVINL void draw_chunk(const Params& P, long long b, int c, CtaShared& sh) {
   if (pl.mode == kModeFailed) return;  // outputs already written by the scan
   const DrawRow d = draw_row(P, pl);
   if (pl.mode == kModeResidual)
-    partial_body<DT, true, SUB>(P, d, sh.tab, VEC, b, c);
+    partial_body<DT, true, SUB>(P, d, sh.tab, sh.tab1k, VEC, b, c);
   else
-    partial_body<DT, false, SUB>(P, d, sh.tab, VEC, b, c);
+    partial_body<DT, false, SUB>(P, d, sh.tab, sh.tab1k, VEC, b, c);
   __syncthreads();  // all sub-chunk writes of this CTA precede the release below
   if (tid == 0) sh.flag = atomic_add_acq_rel(P.done_p + b, 1u) == (unsigned)(P.np - 1);
   __syncthreads();
@@ -970,6 +1052,8 @@ template <int DT, bool VEC, int SUB>
 __global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
   __shared__ CtaShared sh;
   sh.tab[threadIdx.x] = kSvExp2Table[threadIdx.x];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sh.tab1k[threadIdx.x + i * kThreads] = kSvExp2Table1024[threadIdx.x + i * kThreads];
   // Wait until the streaming grid has completed and its writes are visible
   // (immediate when this kernel was launched as an ordinary dependent).
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1061,6 +1145,8 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(Params P) {
   }
   const long long b = it.b;
   sh.draw.tab[tid] = kSvExp2Table[tid];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sh.draw.tab1k[tid + i * kThreads] = kSvExp2Table1024[tid + i * kThreads];
   if (tid == 0) sh.draw.flag = wait_ready(P, b) ? 1 : 0;
   __syncthreads();
   if (!sh.draw.flag) return;

@@ -157,9 +157,17 @@ def check_workload(sv, w, dev, pool, workers, tmp, min_decisions, max_steps=100_
                 pass
         if need_steps == max_steps and rep.decisions:
             done = s - step_base + 1
-            need_steps = min(max_steps, int(np.ceil(min_decisions * done / rep.decisions)))
+            need_steps = min(max_steps,
+                             int(np.ceil(1.08 * min_decisions * done / rep.decisions)))
 
-    while step < need_steps:
+    while True:
+        if step >= need_steps:
+            while pending:
+                settle(pending.popleft())
+            if rep.decisions >= min_decisions or step >= max_steps:
+                break
+            need_steps = min(max_steps, step + int(np.ceil(
+                1.1 * (min_decisions - rep.decisions) * step / max(1, rep.decisions))) + 1)
         inp = make_batch(w, step=step_base + step, device=dev)
         out, nacc, dbg = sv.verify(inp["target"], inp["draft"], inp["tokens"], inp["uniforms"],
                                    inp["temperature"], workspace=ws, debug=True)
@@ -182,8 +190,6 @@ def check_workload(sv, w, dev, pool, workers, tmp, min_decisions, max_steps=100_
         step += 1
         while pending and (len(pending) > depth or all(r.ready() for _, r in pending[0][1])):
             settle(pending.popleft())
-    while pending:
-        settle(pending.popleft())
     dt = time.time() - t0
     d = rep.as_dict()
     d.update({"workload": w.name, "steps": step, "device_status": statuses,
