@@ -27,4 +27,6 @@ from .spec_sampling import (  # noqa: F401
     topp_mask,
     verify_topp,
     verify_inputs,
+    LMHeadStats,
+    lm_head_stats,
 )

@@ -437,6 +437,47 @@ def verify_topp(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
     return NucleusResult(res, np.concatenate([tk, dk], axis=1), np.concatenate([tg, dg], axis=1))
 
 
+@dataclass
+class LMHeadStats:
+    logits: np.ndarray           # [N, V] fp64 logits l = h W^T
+    row_max: np.ndarray          # [N] max_i l_i / T
+    lse: np.ndarray              # [N] log sum_i exp(l_i / T)
+    at: np.ndarray               # [N] l at the row's token (NaN where none is given)
+
+
+def lm_head_stats(hidden, weight, temperature, tokens=None) -> LMHeadStats:
+    """The model's final projection and the statistics of its temperature
+    transform, per row: the logits l = h W^T (hidden [N, D] times the
+    transposed projection weight [V, D], in fp64 from exactly widened inputs),
+    max_i l_i/T, log sum_i exp(l_i/T), and l at the row's token.
+
+    This is the scoring step of Algorithm 2 step 2 (one target call scores
+    the K+1 prefixes; card, §4.1 "Why it works (conditional scoring)") fused
+    with the row statistics the verification needs (§4.2 "Decoding
+    transforms"; the ratio at the drafted token, §4.2 "Modified rejection
+    sampling"). `tokens` [N] holds a token id per row, or -1 for none; the
+    temperature is an fp32 argument, widened exactly (U6)."""
+    h = np.asarray(hidden, dtype=np.float64)
+    w = np.asarray(weight, dtype=np.float64)
+    if h.ndim != 2 or w.ndim != 2 or h.shape[1] != w.shape[1]:
+        raise ValueError("hidden [N, D] and weight [V, D] must share D")
+    with np.errstate(over="ignore"):
+        T = float(np.float32(temperature))
+    if not (np.isfinite(T) and T > 0):
+        raise ValueError("temperature must be finite and > 0")
+    logits = np.matmul(h, w.T)
+    z = logits / T
+    m = np.max(z, axis=-1)
+    lse = m + np.log(np.sum(np.exp(z - m[:, None]), axis=-1))
+    N, V = logits.shape
+    at = np.full(N, np.nan)
+    if tokens is not None:
+        tok = np.asarray(tokens).astype(np.int64)
+        ok = (tok >= 0) & (tok < V)
+        at[ok] = logits[np.arange(N)[ok], tok[ok]]
+    return LMHeadStats(logits, m, lse, at)
+
+
 def _widen(x) -> np.ndarray:
     """Exact widening of a torch tensor (bf16 / fp32 / int) or array to numpy fp64."""
     if hasattr(x, "detach"):

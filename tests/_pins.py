@@ -715,6 +715,73 @@ def pin_topp_law(O, n=200_000, V=12, p=0.8, seed=47):
     assert stats.chisquare(counts[keep_q], expect * counts[keep_q].sum() / expect.sum()).pvalue > 1e-4
 
 
+# ---------------------------------------------------------------- the scoring step (LM head)
+
+def pin_lm_head_golden(O):
+    """Hand-worked logits, row maxima, log-sum-exps and gathered logits
+    (tests/golden/lm_head_cases.json)."""
+    with open(os.path.join(GOLDEN_DIR, "lm_head_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        r = O.lm_head_stats(np.array(c["hidden"], dtype=np.float64),
+                            np.array(c["weight"], dtype=np.float64), c["temperature"],
+                            np.array(c["tokens"]))
+        name = c["name"]
+        assert np.array_equal(r.logits, np.array(c["expected_logits"], dtype=np.float64)), name
+        np.testing.assert_allclose(r.row_max, c["expected_row_max"], rtol=0, atol=0, err_msg=name)
+        np.testing.assert_allclose(r.lse, c["expected_lse"], rtol=1e-14, err_msg=name)
+        exp_at = np.array([np.nan if v is None else v for v in c["expected_at"]])
+        np.testing.assert_array_equal(r.at, exp_at, err_msg=name)
+
+
+def pin_lm_head_brute_force(O, seed=61):
+    """Integer-valued inputs: the logits against explicit loops over (n, v, d)
+    (exact), the statistics against scipy's logsumexp of those logits, the
+    gather against direct indexing; shapes chosen so that no two of N, D, V
+    are equal."""
+    rng = np.random.default_rng(seed)
+    N, D, V = 3, 5, 7
+    h = rng.integers(-3, 4, (N, D)).astype(np.float64)
+    w = rng.integers(-3, 4, (V, D)).astype(np.float64)
+    tok = np.array([6, 0, -1])
+    ref = np.zeros((N, V))
+    for n in range(N):
+        for v in range(V):
+            acc = 0.0
+            for d in range(D):
+                acc += h[n, d] * w[v, d]
+            ref[n, v] = acc
+    for T in (1.0, 0.75, 3.0):
+        r = O.lm_head_stats(h, w, T, tok)
+        assert np.array_equal(r.logits, ref)
+        np.testing.assert_allclose(r.row_max, ref.max(axis=1) / T, rtol=0, atol=0)
+        np.testing.assert_allclose(r.lse, logsumexp(ref / T, axis=1), rtol=1e-13)
+        assert r.at[0] == ref[0, 6] and r.at[1] == ref[1, 0] and np.isnan(r.at[2])
+
+
+def pin_lm_head_invariances(O, seed=67):
+    """Exact invariances: (2h, 2T) gives the same z = l/T, so the same maxima
+    and log-sum-exps, and twice the gathered logits; permuting the rows of W
+    permutes the logits and leaves the statistics unchanged."""
+    rng = np.random.default_rng(seed)
+    N, D, V = 4, 16, 40
+    h = np.round(rng.normal(0, 1, (N, D)) * 64) / 64
+    w = np.round(rng.normal(0, 0.3, (V, D)) * 64) / 64
+    tok = rng.integers(0, V, N)
+    a = O.lm_head_stats(h, w, 0.75, tok)
+    b = O.lm_head_stats(2 * h, w, 1.5, tok)
+    np.testing.assert_array_equal(a.row_max, b.row_max)
+    np.testing.assert_allclose(a.lse, b.lse, rtol=1e-15)
+    np.testing.assert_array_equal(2 * a.at, b.at)
+    perm = rng.permutation(V)
+    inv = np.argsort(perm)
+    c = O.lm_head_stats(h, w[perm], 0.75, inv[tok])
+    np.testing.assert_array_equal(c.logits, a.logits[:, perm])
+    np.testing.assert_array_equal(c.row_max, a.row_max)
+    np.testing.assert_allclose(c.lse, a.lse, rtol=1e-14)
+    np.testing.assert_array_equal(c.at, a.at)
+
+
 FAST_PINS = (pin_golden, pin_theorem1, pin_sequential, pin_library_special_cases,
              pin_invariants, pin_failures, pin_draft_golden, pin_draft_failures,
              pin_draft_matches_bonus, pin_greedy_golden, pin_greedy_is_zero_temperature,
@@ -722,4 +789,5 @@ FAST_PINS = (pin_golden, pin_theorem1, pin_sequential, pin_library_special_cases
              pin_topk_full_is_verify, pin_topk_one_is_greedy, pin_topk_order_property,
              pin_topp_mask_cases,
              pin_topp_brute_force, pin_topp_hand_case, pin_topp_one_is_verify,
-             pin_topp_tiny_is_top1)
+             pin_topp_tiny_is_top1, pin_lm_head_golden, pin_lm_head_brute_force,
+             pin_lm_head_invariances)

@@ -75,6 +75,16 @@ MUTATIONS = [
      "order = (V - 1 - np.argsort(-(flat[r][::-1] + 0.0), kind=\"stable\"))"),
     ("nucleus cut before the temperature",
      "q, _, st = temperature_softmax(flat, temperature)", "q, _, st = temperature_softmax(flat, 1.0)"),
+    ("lm-head gathers a neighbouring column",
+     "at[ok] = logits[np.arange(N)[ok], tok[ok]]", "at[ok] = logits[np.arange(N)[ok], tok[ok] - 1]"),
+    ("lm-head statistics ignore the temperature",
+     "    z = logits / T\n    m = np.max(z, axis=-1)", "    z = logits\n    m = np.max(z, axis=-1)"),
+    ("lm-head maximum over the whole batch",
+     "    m = np.max(z, axis=-1)\n    lse", "    m = np.max(z) + 0 * z[:, 0]\n    lse"),
+    ("lm-head gathers z instead of l",
+     "at[ok] = logits[np.arange(N)[ok], tok[ok]]", "at[ok] = z[np.arange(N)[ok], tok[ok]]"),
+    ("lm-head weight used untransposed (square shapes hide it)",
+     "logits = np.matmul(h, w.T)", "logits = np.matmul(h, w.reshape(w.shape[1], w.shape[0]))"),
     ("nucleus filters the target only",
      "res = verify(tm, dm, tokens, uniforms, temperature)", "res = verify(tm, draft, tokens, uniforms, temperature)"),
 ]

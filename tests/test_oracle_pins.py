@@ -159,3 +159,15 @@ def test_topp_first_token_law_is_filtered_q():
 
 def test_topk_against_the_ranking_definition():
     _pins.pin_topk_order_property(oracle)
+
+
+def test_lm_head_hand_cases():
+    _pins.pin_lm_head_golden(oracle)
+
+
+def test_lm_head_against_loops_and_scipy():
+    _pins.pin_lm_head_brute_force(oracle)
+
+
+def test_lm_head_invariances():
+    _pins.pin_lm_head_invariances(oracle)
