@@ -71,13 +71,15 @@ def parse():
                          "and exit (a small case for ncu captures)")
     ap.add_argument("--path", choices=["auto", "pair", "fused"], default="auto",
                     help="verify, --ncu-case: force the kernel pair or the fused kernel")
-    ap.add_argument("--op", choices=["verify", "draft_sample", "greedy", "topk", "topp"],
+    ap.add_argument("--op", choices=["verify", "draft_sample", "greedy", "topk", "topp",
+                                     "lmhead"],
                     default="verify",
                     help="verify: the verification step (default); draft_sample: the draft-side "
                          "sampler over every draft row of the workload; greedy: greedy-mode "
                          "verification of the workload's target rows; topk: verification on "
                          "top-k filtered distributions (--top-k); topp: verification on nucleus "
-                         "filtered distributions (--top-p)")
+                         "filtered distributions (--top-p); lmhead: the scoring step's "
+                         "projection fused with the row statistics (tensor cores)")
     ap.add_argument("--top-k", type=int, default=50)
     ap.add_argument("--top-p", type=float, default=0.9)
     return ap.parse_args()
@@ -1350,12 +1352,204 @@ def run_filter(args, w, world, rank, local):
     }), flush=True)
 
 
+LMH_METRIC = ("scored rows/sec of the fused projection + row statistics (and tensor "
+              "TFLOP/s, % of GB300 bf16 peak)")
+LMH_UNIT = "rows/s"
+
+
+def lmh_oracle_sample(w, inp, rows):
+    """The oracle's statistics of `rows` (a bounded sample) and its time."""
+    import oracle
+
+    h = inp["hidden"][rows].cpu().to(torch.float64).numpy()
+    wt = inp["weight"].cpu().to(torch.float64).numpy()
+    tok = inp["tokens"][rows].cpu().numpy()
+    t0 = time.perf_counter()
+    ref = oracle.lm_head_stats(h, wt, w.temperature, tok)
+    dt = time.perf_counter() - t0
+    return ref, dt, h, wt, tok
+
+
+def run_lmhead_reference(args, world, rank):
+    if rank != 0:
+        return
+    from synthetic import LMHEAD_WORKLOADS, make_lmhead_inputs
+
+    w = LMHEAD_WORKLOADS["lmhead-c3"]
+    inp = make_lmhead_inputs(w.N, w.D, w.V, w.logit_std, w.seed, device="cpu")
+    rows = list(range(4))
+    steps = max(1, args.steps)
+    for _ in range(max(1, args.warmup)):
+        lmh_oracle_sample(w, inp, rows)
+    dt = 0.0
+    for _ in range(steps):
+        dt += lmh_oracle_sample(w, inp, rows)[1]
+    value = steps * len(rows) / dt
+    print(json.dumps({
+        "impl": "reference", "op": "lmhead", "metric": LMH_METRIC, "value": value,
+        "unit": LMH_UNIT, "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "D": w.D, "V": w.V},
+        "cpu_baseline": {"value": value, "unit": LMH_UNIT, "cores": host_cores(),
+                         "kind": "oracle",
+                         "sample": f"each step: the oracle (numpy fp64 matmul, its BLAS on the "
+                                   f"host cores) over {len(rows)} rows of {w.name}",
+                         "host": host_info()},
+        "e2e": {"value": value, "unit": LMH_UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_lmhead(args, world, rank, local):
+    """A step is one sv_lmhead_stats call over the N scored rows: the logits of
+    the N x D hidden states against the V x D projection on the tensor cores,
+    reduced to row statistics on chip."""
+    import speculative_sampling_verification_gb300 as sv
+    from synthetic import LMHEAD_WORKLOADS, make_lmhead_inputs
+
+    w = LMHEAD_WORKLOADS["lmhead-c3"]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sv.load_library(build=True)
+    inp = make_lmhead_inputs(w.N, w.D, w.V, w.logit_std, w.seed + rank, device=dev)
+    ws = torch.empty(sv.sv_lmhead_workspace_size(w.N, w.D, w.V), dtype=torch.uint8, device=dev)
+    rm = torch.empty(w.N, dtype=torch.float64, device=dev)
+    lse = torch.empty(w.N, dtype=torch.float64, device=dev)
+    at = torch.empty(w.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def call():
+        rc = sv.sv_lmhead_stats(inp["hidden"], inp["weight"], inp["tokens"], w.temperature, rm,
+                                lse, at, ws, stream=stream)
+        if rc != 0:
+            raise RuntimeError(f"sv_lmhead_stats: {sv.sv_status_string(rc)}")
+
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    steps, warmup = max(1, args.steps), max(3, args.warmup)
+    g_warm, g = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=stream):
+        for _ in range(warmup):
+            call()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(steps):
+            call()
+    g_warm.replay()
+    torch.cuda.synchronize()
+    t_est = time.perf_counter()
+    g.replay()
+    torch.cuda.synchronize()
+    est = max(time.perf_counter() - t_est, 1e-4)
+    reps = max(1, int(np.ceil(args.min_seconds / est)))
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    time.sleep(0.3)
+    clocks.stop()
+    if sv.sv_read_device_status(ws, stream) != 0:
+        raise RuntimeError("bad device status")
+    elapsed_ms = reduce_max(start.elapsed_time(end), world, dev)
+    per_s = elapsed_ms / 1e3 / (steps * reps)
+
+    # End to end: the hidden states (the model's activations) copied from
+    # pinned host memory every step and the three outputs read back; the
+    # projection weights are model parameters, resident in HBM.
+    h_host = inp["hidden"].cpu().pin_memory()
+    h_dev = torch.empty_like(inp["hidden"])
+    o_host = [torch.empty(w.N, dtype=t.dtype).pin_memory() for t in (rm, lse, at)]
+    e2e_steps = max(8, min(100, int(0.5 / per_s)))
+
+    def host_step():
+        with torch.cuda.stream(stream):
+            h_dev.copy_(h_host, non_blocking=True)
+            rc = sv.sv_lmhead_stats(h_dev, inp["weight"], inp["tokens"], w.temperature, rm, lse,
+                                    at, ws, stream=stream)
+            if rc != 0:
+                raise RuntimeError(sv.sv_status_string(rc))
+            for o, d in zip(o_host, (rm, lse, at)):
+                o.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        host_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        host_step()
+    e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
+    if rank != 0:
+        return
+    tflops = w.flops() / per_s / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        peak, kind = 1900.0, "fallback"
+    cpu = parity = None
+    if world == 1 and not args.no_cpu_baseline:
+        rows = [0, 1, 2, 3]
+        ref, dt, h, wt, tok = lmh_oracle_sample(w, inp, rows)
+        cpu = {"value": len(rows) / dt, "unit": LMH_UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": f"{len(rows)} rows of {w.name} in {dt:.2f} s (numpy fp64 matmul, its "
+                         f"BLAS on the host cores)", "host": host_info()}
+        bound = (np.abs(h) @ np.abs(wt).T * 2.0 ** -20).max(axis=1) / np.float32(w.temperature)
+        g_rm, g_lse = rm[rows].cpu().numpy(), lse[rows].cpu().numpy()
+        parity = {"rows": len(rows),
+                  "row_max_within_bound": bool(np.all(np.abs(g_rm - ref.row_max) <= bound)),
+                  "lse_within_bound": bool(np.all(np.abs(g_lse - ref.lse)
+                                                  <= bound + 1e-6 * np.abs(ref.lse))),
+                  "max_abs_diff_lse": float(np.max(np.abs(g_lse - ref.lse))),
+                  "bound": "2^-20 sum_d |h_d w_vd| / T per row (fp32 accumulation)"}
+    print(json.dumps({
+        "op": "lmhead", "metric": LMH_METRIC, "value": aggregate(w.N, world, per_s),
+        "unit": LMH_UNIT, "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": per_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "D": w.D, "V": w.V},
+        "timing": {"repeats": reps, "timed_steps": steps * reps,
+                   "l2": f"the {w.weight_bytes() / 1e9:.2f} GB projection is read once per "
+                         f"step, more than L2"},
+        "tflops": tflops,
+        "roofline": {"bound": "tensor", "kernel": "lmhead_kernel (tcgen05 bf16 GEMM + on-chip "
+                     "row statistics) with its combine kernel", "achieved": tflops, "peak": peak,
+                     "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_kind": f"{kind} cuBLAS bf16 (burst)", "traffic": None,
+                     "flops_per_launch": w.flops(), "ms_per_launch": per_s * 1e3},
+        "e2e": {"value": aggregate(w.N * e2e_steps, world, e2e_s), "unit": LMH_UNIT,
+                "h2d_bytes_per_step": w.N * w.D * 2, "d2h_bytes_per_step": w.N * 20,
+                "steps": e2e_steps, "api": "sv_lmhead_stats with the hidden states copied "
+                "from pinned host memory every step; weights resident"},
+        "gpu_launches": steps * reps * 2,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "cpu_baseline": cpu,
+        "parity": parity,
+    }), flush=True)
+
+
 def main():
     args = parse()
     w = get_workload(args.config)
     world, rank, local = dist_setup(args)
     try:
-        if args.op == "draft_sample":
+        if args.op == "lmhead":
+            if args.impl == "reference":
+                run_lmhead_reference(args, world, rank)
+            else:
+                run_lmhead(args, world, rank, local)
+        elif args.op == "draft_sample":
             if args.impl == "reference":
                 run_sampler_reference(args, w, world, rank)
             else:

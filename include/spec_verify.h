@@ -355,6 +355,42 @@ void sv_force_path(int path);
  * and the context stays usable. Process-wide; 0 restores normal calls. */
 void sv_test_withhold_plans(int on);
 
+/* ---------------------------------------------------------------- the scoring step's projection
+ *
+ * Algorithm 2 step 2 of the card: one target call scores the K+1 prefixes
+ * (§4.1 "Why it works (conditional scoring)"); the verification then needs,
+ * per scored row, only the statistics of the temperature transform (§4.2
+ * "Decoding transforms") and the logit at the drafted token (§4.2 "Modified
+ * rejection sampling"). This call fuses the model's final projection with
+ * those statistics: the logits l = h W^T are formed on the tensor cores
+ * (bf16 operands, fp32 accumulation) and reduced on chip, never stored.
+ *
+ * Bytes of device workspace sv_lmhead_stats needs; 0 for invalid sizes
+ * (N < 0, V < 1, D < 8 or not a multiple of 8). Pure host function. */
+size_t sv_lmhead_workspace_size(int N, int D, int V);
+
+/* For every row n of the hidden states:
+ *   hidden       device, [N, D] bf16, row-major, 16-byte aligned
+ *   weight       device, [V, D] bf16, row-major, 16-byte aligned: the
+ *                projection's weight, one row per token (l = h W^T)
+ *   tokens       device, [N] int32: a token per row, or -1 for none
+ *   temperature  T > 0, finite (fp32)
+ *   row_max      device, [N] fp64 (written): max_i l_i / T
+ *   lse          device, [N] fp64 (written): log sum_i exp(l_i / T)
+ *   at           device, [N] fp32 (written): l at tokens[n], NaN where tokens[n]
+ *                is outside [0, V)
+ *   workspace    device, sv_lmhead_workspace_size() bytes, 256-byte aligned;
+ *                its first 4 bytes are the device status word (read with
+ *                sv_read_device_status): 32 = a row with a non-finite logit
+ *                (its row_max and lse are NaN), 256 = a bounded wait ran out
+ * The logits carry fp32 accumulation error: against exact arithmetic, a
+ * logit differs by about 2^-24 sqrt(D) times the magnitude of the partial
+ * sums. Returns SV_OK once the two kernels are enqueued on `stream`, or a
+ * host-side error code with nothing enqueued; N == 0 returns SV_OK at once. */
+int sv_lmhead_stats(const void* hidden, const void* weight, const int32_t* tokens, int N, int D,
+                    int V, float temperature, double* row_max, double* lse, float* at,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

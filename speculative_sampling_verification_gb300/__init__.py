@@ -29,7 +29,7 @@ __all__ = [
     "sv_greedy_workspace_size", "spec_verify_greedy", "verify_greedy", "sv_force_path",
     "sv_test_withhold_plans", "sv_topk_workspace_size", "spec_verify_topk", "verify_topk",
     "sv_topp_workspace_size", "spec_verify_topp", "verify_topp", "spec_verify_host_async",
-    "EXPORTED_SYMBOLS",
+    "sv_lmhead_workspace_size", "sv_lmhead_stats", "lmhead_stats", "EXPORTED_SYMBOLS",
 ]
 
 SV_BF16 = 0
@@ -45,7 +45,7 @@ EXPORTED_SYMBOLS = (
     "spec_verify_static", "sv_sample_workspace_size", "spec_draft_sample",
     "sv_greedy_workspace_size", "spec_verify_greedy", "sv_force_path", "sv_test_withhold_plans",
     "sv_topk_workspace_size", "spec_verify_topk", "sv_topp_workspace_size", "spec_verify_topp",
-    "spec_verify_host_async",
+    "spec_verify_host_async", "sv_lmhead_workspace_size", "sv_lmhead_stats",
 )
 
 _lib = None
@@ -114,6 +114,10 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.sv_force_path.restype = None
     lib.sv_test_withhold_plans.argtypes = [i32]
     lib.sv_test_withhold_plans.restype = None
+    lib.sv_lmhead_workspace_size.argtypes = [i32, i32, i32]
+    lib.sv_lmhead_workspace_size.restype = sz
+    lib.sv_lmhead_stats.argtypes = [vp, vp, vp, i32, i32, i32, f32, dp, dp, vp, vp, sz, vp]
+    lib.sv_lmhead_stats.restype = i32
     if path is None:
         _lib = lib
     return lib
@@ -466,3 +470,51 @@ def verify_greedy(target, tokens, *, workspace=None, stream=None):
     if rc != SV_OK:
         raise StatusError(rc, "spec_verify_greedy")
     return out, nacc
+
+
+# ---------------------------------------------------------------- the scoring step's projection
+
+def sv_lmhead_workspace_size(N: int, D: int, V: int) -> int:
+    return int(load_library().sv_lmhead_workspace_size(N, D, V))
+
+
+def sv_lmhead_stats(hidden, weight, tokens, temperature, row_max, lse, at, workspace,
+                    stream=None) -> int:
+    """Direct binding of the fused projection + row statistics: hidden [N, D]
+    and weight [V, D] bf16 CUDA tensors, tokens [N] int32; row_max and lse
+    [N] fp64 and at [N] fp32 are written. Returns the host status code."""
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("hidden and weight must be bfloat16")
+    if hidden.dim() != 2 or weight.dim() != 2 or hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden [N, D] and weight [V, D] must share D")
+    if not (hidden.is_contiguous() and weight.is_contiguous() and tokens.is_contiguous()):
+        raise ValueError("inputs must be contiguous")
+    if tokens.dtype != torch.int32 or tokens.shape != (hidden.shape[0],):
+        raise TypeError("tokens must be int32 [N]")
+    N, D = hidden.shape
+    V = weight.shape[0]
+    return int(load_library().sv_lmhead_stats(
+        _ptr(hidden), _ptr(weight), _ptr(tokens), N, D, V, ctypes.c_float(temperature),
+        _ptr(row_max), _ptr(lse), _ptr(at), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(hidden.device, stream)))
+
+
+def lmhead_stats(hidden, weight, tokens, temperature, *, workspace=None, stream=None):
+    """Allocate the outputs (and a workspace if none is given) with torch and
+    run the fused projection + statistics; returns (row_max, lse, at)."""
+    if tokens.dtype == torch.int64:
+        tokens = tokens.to(torch.int32)
+    N, D = hidden.shape
+    V = weight.shape[0]
+    dev = hidden.device
+    n = sv_lmhead_workspace_size(N, D, V)
+    if n == 0:
+        raise StatusError(2, "sv_lmhead_workspace_size")
+    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
+    row_max = torch.empty(N, dtype=torch.float64, device=dev)
+    lse = torch.empty(N, dtype=torch.float64, device=dev)
+    at = torch.empty(N, dtype=torch.float32, device=dev)
+    rc = sv_lmhead_stats(hidden, weight, tokens, temperature, row_max, lse, at, ws, stream=stream)
+    if rc != SV_OK:
+        raise StatusError(rc, "sv_lmhead_stats")
+    return row_max, lse, at

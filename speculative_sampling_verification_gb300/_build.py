@@ -1,6 +1,6 @@
 """In-tree build of libspecverify.so for sm_103a (nvcc, no cmake).
 
-The two CUDA translation units compile in parallel, then link into one shared
+The CUDA translation units compile in parallel, then link into one shared
 library next to this file (lib/libspecverify.so). A rebuild happens when any
 source is newer than the library.
 """
@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libspecverify.so")
-SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_static_scratch.cu"]
+SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_static_scratch.cu", "sv_lmhead.cu"]
 HEADERS = ["sv_device.cuh", "sv_internal.h", "sv_exp_table.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

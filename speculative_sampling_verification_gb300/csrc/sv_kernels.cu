@@ -787,137 +787,169 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
                         : block_scan2(tq, ff{0.f, 0.f}, ff{0.f, 0.f}, ff{0.f, 0.f}, sh);
   const ff Sq = resid ? bs.sum1 : bs.tot1;
   const ff Sp = bs.sum2;
-  // Residual mass sum max(0, q - p), scaled by S_q S_p; zero -> fall back to q.
-  const ff R = ff_sub(ff_mul(Sp, bs.tot1), ff_mul(Sq, bs.tot2));
-  const bool use_res = resid && R.hi > 0.f;
-  if (resid && !use_res) bs = block_scan2(tq, ff{0.f, 0.f}, ff{0.f, 0.f}, ff{0.f, 0.f}, sh);
-  const ff total = use_res ? R : Sq;
-  const ff tau = ff_mul_f(total, pl.u);
-  auto weight_before = [&](ff pa, ff pb) {
-    return use_res ? ff_sub(ff_mul(Sp, pa), ff_mul(Sq, pb)) : pa;
-  };
-  auto sub_sums = [&](int g, ff& a, ff& bb) {
-    float4 x, y;
-    load_sub(g, x, y);
-    if (use_res) {
-      a = ff_of(y.x, y.y);
-      bb = ff_of(y.z, y.w);
-    } else {
-      a = ff_of(x.x, x.y);
-      bb = {0.f, 0.f};
-    }
-  };
-
-  // The first sub-chunk with positive weight whose cumulative weight passes
-  // tau, and the last sub-chunk with positive weight.
-  if (tid == 0) {
-    sh.g = INT_MAX;
-    sh.j = -1;
-  }
-  __syncthreads();
-  {
-    ff pa = bs.pre1, pb = bs.pre2;
-    ff cur = weight_before(pa, pb);
-    int found = -1, lastpos = -1;
-    for (int g = g0; g < g1; ++g) {
-      ff a, bb;
-      sub_sums(g, a, bb);
-      pa = ff_add(pa, a);
-      pb = ff_add(pb, bb);
-      const ff next = weight_before(pa, pb);
-      const bool positive = use_res ? ff_sub(ff_mul(Sp, a), ff_mul(Sq, bb)).hi > 0.f : a.hi > 0.f;
-      if (positive) {
-        lastpos = g;
-        if (found < 0 && ff_gt(next, tau)) found = g;
-      }
-      cur = next;
-    }
-    if (found >= 0) atomicMin(&sh.g, found);
-    if (lastpos >= 0) atomicMax(&sh.j, lastpos);
-  }
-  __syncthreads();
-  const bool last_mode = sh.g == INT_MAX;
-  const int gs = last_mode ? sh.j : sh.g;
-  if (gs < 0) return;  // uniform across the CTA: no positive weight at all
-  // The weight before sub-chunk gs, from the thread that holds it.
-  if (!last_mode && gs >= g0 && gs < g1) {
-    ff pa = bs.pre1, pb = bs.pre2;
-    for (int g = g0; g < gs; ++g) {
-      ff a, bb;
-      sub_sums(g, a, bb);
-      pa = ff_add(pa, a);
-      pb = ff_add(pb, bb);
-    }
-    sh.s_pref = weight_before(pa, pb);
-  }
-  // Exact search inside sub-chunk gs: kPer consecutive elements per thread.
+  // Residual mass sum max(0, q - p), scaled by S_q S_p; zero -> fall back to
+  // q. R is the difference of two float-float products; when the positive
+  // set's q and p agree exactly (e.g. one-hot rows on the same token), their
+  // rounding leaves a residue near 2^-48 of the terms, so a residual below
+  // 2^-40 of them counts as zero.
+  const ff SA = ff_mul(Sp, bs.tot1), SB = ff_mul(Sq, bs.tot2);
+  const ff R = ff_sub(SA, SB);
+  const bool res_first = resid && R.hi > 0x1p-40f * (SA.hi + SB.hi);
+  const BlockScan2 bs_res = bs;
   const DrawRow d = draw_row(P, pl);
-  const long long e0 = (long long)gs * SUB + kPer * tid;
-  ff w[kPer];
-  ff wsum{0.f, 0.f};
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const long long e = e0 + k;
-    w[k] = {0.f, 0.f};
-    if (e < P.V) {
-      const float lq = load_elem<DT>(d.rq, e);
-      ff eq, ep;
-      bool pos;
-      if (d.fast) {
-        // The chunk pass's positive-set test (the fast weights, bit for bit),
-        // then the weights to ~1e-12 in the same scaling.
-        const float lqc = fmaxf(lq, d.lmin);
-        if (use_res) {
-          const float lpc = fmaxf(load_elem<DT>(d.rp, e), d.lmin);
-          const ff fq = exp_draw(lqc, d.qb.x, d.dc, sh.tab1k);
-          const ff fp = exp_draw(lpc, d.qb.y, d.dc, sh.tab1k);
-          pos = __fmul_rn(__fadd_rn(fq.hi, fq.lo), d.alpha) >
-                __fmul_rn(__fadd_rn(fp.hi, fp.lo), d.beta);
-          if (pos) {
-            eq = exp_precise(lqc, d.qb.x, d.ih, d.il, sh.tab);
-            ep = exp_precise(lpc, d.qb.y, d.ih, d.il, sh.tab);
-            w[k] = ff_sub(ff_mul(ff_normalize(eq), Sp), ff_mul(ff_normalize(ep), Sq));
-          }
-        } else {
-          w[k] = ff_normalize(exp_precise(lqc, d.qb.x, d.ih, d.il, sh.tab));
-        }
-      } else if (use_res) {
-        const float lp = load_elem<DT>(d.rp, e);
-        element_exps<true>(d, lq, lp, sh.tab, eq, ep, pos);
-        if (pos) w[k] = ff_sub(ff_mul(ff_normalize(eq), Sp), ff_mul(ff_normalize(ep), Sq));
+
+  // One search: the sub-chunk holding u * total, then the element within it.
+  // Returns whether a token was written (uniform across the CTA).
+  auto search = [&](bool use_res) -> bool {
+    const BlockScan2 bsx = use_res ? bs_res
+                                   : (resid ? block_scan2(tq, ff{0.f, 0.f}, ff{0.f, 0.f},
+                                                          ff{0.f, 0.f}, sh)
+                                            : bs_res);
+    const ff total = use_res ? R : Sq;
+    const ff tau = ff_mul_f(total, pl.u);
+    auto weight_before = [&](ff pa, ff pb) {
+      return use_res ? ff_sub(ff_mul(Sp, pa), ff_mul(Sq, pb)) : pa;
+    };
+    auto sub_sums = [&](int g, ff& a, ff& bb) {
+      float4 x, y;
+      load_sub(g, x, y);
+      if (use_res) {
+        a = ff_of(y.x, y.y);
+        bb = ff_of(y.z, y.w);
       } else {
-        element_exps<false>(d, lq, 0.f, sh.tab, eq, ep, pos);
-        w[k] = ff_normalize(eq);
+        a = ff_of(x.x, x.y);
+        bb = {0.f, 0.f};
+      }
+    };
+
+    // The first sub-chunk with positive weight whose cumulative weight passes
+    // tau, and the last sub-chunk with positive weight.
+    __syncthreads();  // sh.g / sh.j may still be read by an earlier search
+    if (tid == 0) {
+      sh.g = INT_MAX;
+      sh.j = -1;
+    }
+    __syncthreads();
+    {
+      ff pa = bsx.pre1, pb = bsx.pre2;
+      int found = -1, lastpos = -1;
+      for (int g = g0; g < g1; ++g) {
+        ff a, bb;
+        sub_sums(g, a, bb);
+        pa = ff_add(pa, a);
+        pb = ff_add(pb, bb);
+        const ff next = weight_before(pa, pb);
+        const bool positive =
+            use_res ? ff_sub(ff_mul(Sp, a), ff_mul(Sq, bb)).hi > 0.f : a.hi > 0.f;
+        if (positive) {
+          lastpos = g;
+          if (found < 0 && ff_gt(next, tau)) found = g;
+        }
+      }
+      if (found >= 0) atomicMin(&sh.g, found);
+      if (lastpos >= 0) atomicMax(&sh.j, lastpos);
+    }
+    __syncthreads();
+    const bool last_mode = sh.g == INT_MAX;
+    const int gs = last_mode ? sh.j : sh.g;
+    if (gs < 0) return false;  // uniform across the CTA: no positive weight at all
+    // The weight before sub-chunk gs, from the thread that holds it.
+    if (!last_mode && gs >= g0 && gs < g1) {
+      ff pa = bsx.pre1, pb = bsx.pre2;
+      for (int g = g0; g < gs; ++g) {
+        ff a, bb;
+        sub_sums(g, a, bb);
+        pa = ff_add(pa, a);
+        pb = ff_add(pb, bb);
+      }
+      sh.s_pref = weight_before(pa, pb);
+    }
+    // Exact search inside sub-chunk gs: kPer consecutive elements per thread,
+    // with the chunk pass's own element weights (so that the search agrees
+    // with the sub-chunk sums it starts from).
+    const long long e0 = (long long)gs * SUB + kPer * tid;
+    ff w[kPer];
+    ff wsum{0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const long long e = e0 + k;
+      w[k] = {0.f, 0.f};
+      if (e < P.V) {
+        const float lq = load_elem<DT>(d.rq, e);
+        ff eq, ep;
+        bool pos;
+        if (d.fast) {
+          const float lqc = fmaxf(lq, d.lmin);
+          const ff fq = exp_draw(lqc, d.qb.x, d.dc, sh.tab1k);
+          if (use_res) {
+            const float lpc = fmaxf(load_elem<DT>(d.rp, e), d.lmin);
+            const ff fp = exp_draw(lpc, d.qb.y, d.dc, sh.tab1k);
+            pos = __fmul_rn(__fadd_rn(fq.hi, fq.lo), d.alpha) >
+                  __fmul_rn(__fadd_rn(fp.hi, fp.lo), d.beta);
+            if (pos) w[k] = ff_sub(ff_mul(ff_normalize(fq), Sp), ff_mul(ff_normalize(fp), Sq));
+          } else {
+            w[k] = ff_normalize(fq);
+          }
+        } else if (use_res) {
+          const float lp = load_elem<DT>(d.rp, e);
+          element_exps<true>(d, lq, lp, sh.tab, eq, ep, pos);
+          if (pos) w[k] = ff_sub(ff_mul(ff_normalize(eq), Sp), ff_mul(ff_normalize(ep), Sq));
+        } else {
+          element_exps<false>(d, lq, 0.f, sh.tab, eq, ep, pos);
+          w[k] = ff_normalize(eq);
+        }
+      }
+      wsum = ff_add(wsum, w[k]);
+    }
+    // block_exclusive_ff's barriers also publish s_pref.
+    const ff tpre = block_exclusive_ff(wsum, sh);
+    if (tid == 0) {
+      sh.g = INT_MAX;
+      sh.j = -1;
+    }
+    __syncthreads();
+    ff cum = ff_add(sh.s_pref, tpre);
+    int found = -1, lastk = -1;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      cum = ff_add(cum, w[k]);
+      if (!last_mode && found < 0 && w[k].hi > 0.f && ff_gt(cum, tau)) found = k;
+      if (w[k].hi > 0.f) lastk = k;
+    }
+    if (found >= 0) atomicMin(&sh.g, kPer * tid + found);
+    if (lastk >= 0) atomicMax(&sh.j, kPer * tid + lastk);
+    __syncthreads();
+    // The first element whose cumulative weight passes tau; else (u = 1, or
+    // rounding at the sub-chunk's end) the last positive element.
+    const int pick = sh.g != INT_MAX ? sh.g : sh.j;
+    if (pick < 0) return false;
+    if (pick / kPer == tid) {
+      const long long e = (long long)gs * SUB + pick;
+      P.out_tokens[b * (P.K + 1) + pl.j] = (int)e;
+      if (P.dbg_prob) {
+        // The drawn token's probability for the debug export, its weight
+        // taken with the precise exponential in the same scaling.
+        ff wt = w[pick % kPer];
+        if (d.fast) {
+          const float lqc = fmaxf(load_elem<DT>(d.rq, e), d.lmin);
+          const ff pq = ff_normalize(exp_precise(lqc, d.qb.x, d.ih, d.il, sh.tab));
+          if (use_res) {
+            const float lpc = fmaxf(load_elem<DT>(d.rp, e), d.lmin);
+            const ff pp = ff_normalize(exp_precise(lpc, d.qb.y, d.ih, d.il, sh.tab));
+            wt = ff_sub(ff_mul(pq, Sp), ff_mul(pp, Sq));
+          } else {
+            wt = pq;
+          }
+        }
+        P.dbg_prob[b] = ff_to_double(wt) / ff_to_double(total);
       }
     }
-    wsum = ff_add(wsum, w[k]);
-  }
-  // block_exclusive_ff's barriers also publish s_pref.
-  const ff tpre = block_exclusive_ff(wsum, sh);
-  if (tid == 0) {
-    sh.g = INT_MAX;
-    sh.j = -1;
-  }
-  __syncthreads();
-  ff cum = ff_add(sh.s_pref, tpre);
-  int found = -1, lastk = -1;
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    cum = ff_add(cum, w[k]);
-    if (!last_mode && found < 0 && w[k].hi > 0.f && ff_gt(cum, tau)) found = k;
-    if (w[k].hi > 0.f) lastk = k;
-  }
-  if (found >= 0) atomicMin(&sh.g, kPer * tid + found);
-  if (lastk >= 0) atomicMax(&sh.j, kPer * tid + lastk);
-  __syncthreads();
-  // The first element whose cumulative weight passes tau; else (u = 1, or
-  // rounding at the sub-chunk's end) the last positive element.
-  const int pick = sh.g != INT_MAX ? sh.g : sh.j;
-  if (pick >= 0 && pick / kPer == tid) {
-    const ff wt = w[pick % kPer];
-    P.out_tokens[b * (P.K + 1) + pl.j] = (int)((long long)gs * SUB + pick);
-    if (P.dbg_prob) P.dbg_prob[b] = ff_to_double(wt) / ff_to_double(total);
-  }
+    return true;
+  };
+  // The residual first (when it is not zero); if its search finds no positive
+  // weight, the zero-residual fallback to q.
+  if (search(res_first)) return;
+  if (res_first) search(false);
 }
 
 // ---------------------------------------------------------------- the two kernels

@@ -82,3 +82,30 @@ def get_workload(name: str) -> Workload:
 def shrink(w: Workload, **kw) -> Workload:
     """A copy with some fields replaced (used for small parity cases of a workload)."""
     return replace(w, **kw)
+
+
+@dataclass(frozen=True)
+class LMHeadWorkload:
+    """Inputs of the scoring step's final projection: N hidden states of width
+    D against a V-token projection, logits of standard deviation `logit_std`."""
+    name: str
+    N: int
+    D: int
+    V: int
+    temperature: float
+    logit_std: float
+    seed: int
+
+    def flops(self) -> int:
+        return 2 * self.N * self.D * self.V
+
+    def weight_bytes(self) -> int:
+        return self.V * self.D * 2
+
+
+# The target call of the 64x8x128256 workload: 64 sequences x 9 scored
+# prefixes, a model width of 8192 and the workload's vocabulary and temperature.
+LMHEAD_WORKLOADS = {
+    "lmhead-c3": LMHeadWorkload("lmhead-n576-d8192-v128256-bf16", N=576, D=8192, V=128256,
+                                temperature=0.8, logit_std=3.0, seed=3003),
+}

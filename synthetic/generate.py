@@ -211,3 +211,21 @@ def make_batch(w: Workload, step: int = 0, device="cpu", rows_per_chunk: int = 6
         "uniforms": uniforms,
         "temperature": float(w.temperature),
     }
+
+
+def make_lmhead_inputs(N: int, D: int, V: int, logit_std: float = 3.0, seed: int = 0,
+                       device="cpu", none_every: int = 7):
+    """Hidden states h [N, D] ~ N(0, 1) and projection weights W [V, D] ~
+    N(0, logit_std^2 / D), both rounded to bf16, so that the logits h W^T have
+    about `logit_std` spread; one token per row, uniform over [0, V), with
+    every `none_every`-th row given -1 (no token). One torch generator on
+    `device`."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(_mix(seed, N, D, V))
+    h = torch.randn(N, D, generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn(V, D, generator=g, device=dev) * (logit_std / D ** 0.5)).to(torch.bfloat16)
+    tok = torch.randint(0, V, (N,), generator=g, device=dev, dtype=torch.int64).to(torch.int32)
+    if none_every:
+        tok[::none_every] = -1
+    return {"hidden": h, "weight": w, "tokens": tok}

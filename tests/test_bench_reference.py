@@ -13,7 +13,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-@pytest.mark.parametrize("op", ["verify", "draft_sample", "greedy", "topk", "topp"])
+@pytest.mark.parametrize("op", ["verify", "draft_sample", "greedy", "topk", "topp", "lmhead"])
 def test_reference_arm_prints_the_contract_line(op):
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--op", op,
                         "--config", "c1", "--steps", "2", "--warmup", "1"],
