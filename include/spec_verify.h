@@ -340,8 +340,9 @@ const char* sv_status_string(int status);
 
 /* Kernels one spec_verify call over these sizes launches (for launch
  * accounting): 1 (the fused kernel) for calls streaming between 16 MiB and
- * 1 GiB, else 2 (the streaming and the draw kernel); 0 for invalid sizes or
- * B == 0. */
+ * 1 GiB; else 2 for calls whose draw needs few chunks (the streaming kernel and
+ * a one-launch draw) or 3 (the streaming kernel, the draw's sum kernel and its
+ * finish kernel); 0 for invalid sizes or B == 0. */
 int sv_kernels_per_call(int B, int K, int V, int dtype);
 
 /* Test hook: 0 (the default) chooses the kernels by size, 1 forces the kernel

@@ -5,7 +5,7 @@
 // The verification step takes one of two launch shapes, chosen per call by
 // the bytes it streams:
 //
-//   stats_kernel + draw_kernel (small and very large calls). stats_kernel has
+//   stats_kernel, then the draw (small and very large calls). stats_kernel has
 //       one warp per row segment (at most 32 KB, sequence-major so that
 //       sequences complete one after another): each lane keeps eight 16-byte
 //       loads in flight per round and reduces its share to the segment's
@@ -15,11 +15,12 @@
 //       that counts a sequence's last row runs its scan (scan_warp): logits at
 //       the drafted tokens, thresholds min(1, q/p) in float-float, the first
 //       rejection j (Algorithm 2 step 3) and the plan of the draw.
-//       draw_kernel, a programmatic dependent of stats_kernel, has one CTA per
-//       chunk of the row pair the draw needs (target and draft row j for the
-//       residual (q - p)_+, or target row K for the bonus token, Algorithm 2
-//       step 4): float-float sums per sub-chunk, and in the CTA that counts a
-//       sequence's last chunk the exact inverse-CDF search for the token.
+//       draw_sum_kernel, a programmatic dependent of stats_kernel, has one
+//       CTA per chunk of the row pair the draw needs (target and draft row j
+//       for the residual (q - p)_+, or target row K for the bonus token,
+//       Algorithm 2 step 4): each warp sums one sub-chunk in float-float and
+//       leaves. draw_finish_kernel, one CTA per sequence, then runs the
+//       inverse-CDF search for the token.
 //   fused_kernel (mid-sized calls). The same warp and chunk code in one
 //       launch: CTAs take tickets, streaming items first, then draw chunks,
 //       each of which waits (bounded) for its sequence's plan.
@@ -1077,9 +1078,11 @@ SV_DEVINL void draw_chunk(const Params& P, long long b, int c, CtaShared& sh) {
   if (sh.flag) finish_seq<DT, SUB>(P, b, pl, sh, VEC);  // the barrier above orders its reads
 }
 
-// One CTA per draw chunk c of sequence b (the plans are complete once the
-// streaming grid is); the CTA that counts the last chunk of a sequence runs
-// its inverse-CDF search.
+
+// The kernel pair's draw for small calls (2048-element chunks): one launch,
+// one CTA per draw chunk; the CTA that counts the last chunk of a sequence
+// runs its inverse-CDF search. For such calls the finish kernel's launch
+// would cost more than the CTA barrier it saves.
 template <int DT, bool VEC, int SUB>
 __global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
   __shared__ CtaShared sh;
@@ -1092,11 +1095,73 @@ __global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
   draw_chunk<DT, VEC, SUB>(P, blockIdx.x / P.np, (int)(blockIdx.x % P.np), sh);
 }
 
+// ---------------------------------------------------------------- the kernel pair's draw
+//
+// After stats_kernel, the draw of the kernel pair takes two launches. In
+// draw_sum_kernel (one CTA per draw chunk) each warp sums its sub-chunk and
+// leaves, without waiting for the CTA's other warps; draw_finish_kernel (one
+// CTA per sequence) then runs each sequence's inverse-CDF search once every
+// chunk's sums are in memory. Both are programmatic dependents of the launch
+// before them: they become resident while it ends, load their tables, and
+// wait on the device for it to complete.
+
+template <int DT, bool VEC, int SUB>
+__global__ void __launch_bounds__(kThreads, 5) draw_sum_kernel(Params P) {
+  __shared__ float2 tab[256];
+  __shared__ float2 tab1k[1024];
+  __shared__ Plan plan;
+  const int tid = threadIdx.x;
+  tab[tid] = kSvExp2Table[tid];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tab1k[tid + i * kThreads] = kSvExp2Table1024[tid + i * kThreads];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long b = blockIdx.x / P.np;
+  const int c = (int)(blockIdx.x % P.np);
+  if (tid == 0) {
+    const Plan* src = P.plans + b;
+    Plan pl;
+    pl.j = __ldcg(&src->j);
+    pl.mode = __ldcg(&src->mode);
+    pl.row_q = __ldcg(&src->row_q);
+    pl.row_p = __ldcg(&src->row_p);
+    pl.m_q = __ldcg(&src->m_q);
+    pl.m_p = __ldcg(&src->m_p);
+    pl.s_q = __ldcg(&src->s_q);
+    pl.s_p = __ldcg(&src->s_p);
+    pl.u = __ldcg(&src->u);
+    plan = pl;
+  }
+  __syncthreads();  // the tables and the plan
+  const Plan pl = plan;
+  if (pl.mode == kModeFailed) return;  // outputs already written by the scan
+  const DrawRow d = draw_row(P, pl);
+  if (pl.mode == kModeResidual)
+    partial_body<DT, true, SUB>(P, d, tab, tab1k, VEC, b, c);
+  else
+    partial_body<DT, false, SUB>(P, d, tab, tab1k, VEC, b, c);
+}
+
+template <int DT, bool VEC, int SUB>
+__global__ void __launch_bounds__(kThreads) draw_finish_kernel(Params P) {
+  __shared__ CtaShared sh;
+  const int tid = threadIdx.x;
+  sh.tab[tid] = kSvExp2Table[tid];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sh.tab1k[tid + i * kThreads] = kSvExp2Table1024[tid + i * kThreads];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long b = blockIdx.x;
+  if (tid == 0) sh.plan = P.plans[b];
+  __syncthreads();
+  const Plan pl = sh.plan;
+  if (pl.mode == kModeFailed) return;
+  finish_seq<DT, SUB>(P, b, pl, sh, VEC);
+}
+
 // ---------------------------------------------------------------- the fused kernel
 //
 // For mid-sized calls one launch does the whole step. Each CTA takes a ticket when it starts: tickets below
 // ceil(n_units / 8) are streaming items (eight warp-units, as stats_kernel's
-// warps), the rest draw chunks in sequence order (as draw_kernel's CTAs). A
+// warps), the rest draw chunks in sequence order (draw_chunk). A
 // draw CTA waits for its sequence's plan, which the sequence's scan releases;
 // every streaming ticket precedes every draw ticket and streaming never
 // waits, so each awaited plan is being computed by a CTA already running. The
@@ -2550,7 +2615,9 @@ long long fused_lag(long long B) { return B; }
 void withhold_plans(int on) { g_withhold.store(on ? 1 : 0); }
 
 int kernels_per_call(long long B, int rows_per_seq, long long V, int es) {
-  return take_fused(B, rows_per_seq, V, es) ? 1 : 2;
+  if (take_fused(B, rows_per_seq, V, es)) return 1;
+  // 2048-element draw chunks (small calls): the one-launch draw.
+  return B * ((V + 4095) / 4096) < kMinDrawCtas ? 2 : 3;
 }
 
 template <int DT, bool VEC, int SUB>
@@ -2587,7 +2654,12 @@ cudaError_t launch_pair(const Params& P, cudaStream_t st, const Events& ev) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = ev.stats_done ? 0 : 1;
-  return cudaLaunchKernelEx(&cfg, draw_kernel<DT, VEC, SUB>, P);
+  if constexpr (SUB == 256) return cudaLaunchKernelEx(&cfg, draw_kernel<DT, VEC, SUB>, P);
+  e = cudaLaunchKernelEx(&cfg, draw_sum_kernel<DT, VEC, SUB>, P);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((unsigned)P.B);
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, draw_finish_kernel<DT, VEC, SUB>, P);
 }
 
 cudaError_t prepare_device(int device) {

@@ -6,24 +6,30 @@
 //
 // For hidden states h [N, D] and the projection's weight W [V, D] (one row per
 // token, bf16), the logits l = h W^T are formed on the tensor cores and never
-// leave the chip: each CTA takes a 128 x 256 tile of l (128 rows of h, 256
-// tokens), accumulates it in tensor memory over D with tcgen05.mma (bf16
-// operands staged in shared memory by TMA, fp32 accumulator in TMEM), and its
-// epilogue reduces the tile to one (max, sum) pair per row, sum of
-// 2^((l - max) log2(e)/T), and picks up the logit at the row's token when that
-// token falls in the tile. A second kernel combines the pairs of a row into
-// max_i l_i/T and log sum_i exp(l_i/T).
+// leave the chip. The output is cut into 128 x 256 tiles of l (128 rows of h,
+// 256 tokens); one persistent CTA per SM takes tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... (the 128-row tiles that share 256 tokens are
+// consecutive, so a slice of W is read from HBM about once). A tile is
+// accumulated in tensor memory over D with tcgen05.mma (bf16 operands staged
+// in shared memory by TMA, fp32 accumulator in TMEM); its epilogue reduces it
+// to one (max, sum) pair per row, sum of 2^((l - max) log2(e)/T), and picks up
+// the logit at the row's token when that token falls in the tile. A second
+// kernel combines the pairs of a row into max_i l_i/T and log sum_i exp(l_i/T).
 //
 // Warp roles in a CTA of 192 threads: warps 0-3 read the accumulator (warp w
 // owns TMEM lanes 32w .. 32w+31, i.e. rows 32w .. 32w+31 of the tile); warp 4
 // issues the TMA loads; warp 5 allocates the tensor memory and issues the
-// MMAs. Four pipeline stages of 48 KB (a 128 x 64 tile of h and a 256 x 64
-// tile of W) with full/empty mbarriers; every wait is bounded and a wait that
-// runs out sets a status bit and ends the CTA's work, after which the tensor
-// memory is still released.
+// MMAs. Four shared-memory stages of 48 KB (a 128 x 64 tile of h and a
+// 256 x 64 tile of W), refilled across tile boundaries, with full/empty
+// mbarriers; two accumulators of 256 TMEM columns, so that the epilogue of one
+// tile runs while the MMAs of the next fill the other (full/empty mbarriers
+// between the MMA warp and the epilogue warps). Every wait is bounded: one
+// that runs out sets a status bit and ends the CTA's work, after which the
+// tensor memory is still released.
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <mutex>
 
 #include <cuda.h>
@@ -40,11 +46,13 @@ constexpr int kBM = 128;             // rows of h per tile (MMA M)
 constexpr int kBN = 256;             // tokens per tile (MMA N)
 constexpr int kBK = 64;              // D per stage: 128 bytes of bf16, one swizzle atom
 constexpr int kStages = 4;
+constexpr int kPrefetch = 8;         // k-blocks requested into L2 ahead of the ring
 constexpr int kThreads = 192;
 constexpr int kTileA = kBM * kBK * 2;   // 16 KB
 constexpr int kTileB = kBN * kBK * 2;   // 32 KB
 constexpr int kStageBytes = kTileA + kTileB;
-constexpr int kTmemCols = 256;          // the 128 x 256 fp32 accumulator
+constexpr int kAccs = 2;                // accumulators (TMEM buffers)
+constexpr int kTmemCols = 256 * kAccs;  // each 128 x 256 fp32
 constexpr unsigned kDevTimeout = 256;
 
 // Dynamic shared memory: the stages (1024-byte aligned for the 128-byte
@@ -52,7 +60,8 @@ constexpr unsigned kDevTimeout = 256;
 struct Tail {
   unsigned long long full[kStages];
   unsigned long long empty[kStages];
-  unsigned long long done;
+  unsigned long long acc_full[kAccs];   // an accumulator's MMAs are complete
+  unsigned long long acc_empty[kAccs];  // the epilogue has read an accumulator
   unsigned tmem_base;
   unsigned abort;
 };
@@ -60,7 +69,7 @@ constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* alignment slack */ + 
 
 struct Args {
   const int32_t* tokens;
-  int N, D, V, n_mt, n_nt, nk;
+  int N, D, V, n_mt, n_nt, nk, n_tiles;
   float c2;          // log2(e)/T
   float2* part;      // [N, n_nt] (max l, sum 2^((l - max) c2)) per row and tile
   float* at;         // [N] l at the row's token
@@ -80,6 +89,10 @@ SV_DEVINL void mbar_init(unsigned bar, unsigned count) {
 SV_DEVINL void mbar_expect_tx(unsigned bar, unsigned bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
+}
+
+SV_DEVINL void mbar_arrive(unsigned bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 SV_DEVINL bool mbar_try_wait(unsigned bar, unsigned parity) {
@@ -120,6 +133,14 @@ SV_DEVINL void tma_load_2d(unsigned dst, const CUtensorMap* map, int x, int y, u
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// L2 prefetch of the same box (no shared memory, no completion to wait for).
+SV_DEVINL void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // Shared-memory descriptor of a K-major bf16 tile whose rows are 128 bytes
@@ -185,15 +206,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Tail* tail = reinterpret_cast<Tail*>(smem + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x % a.n_mt, nt = blockIdx.x / a.n_mt;
-  const int m0 = mt * kBM, n0 = nt * kBN;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(&tail->full[s]), 1);
       mbar_init(smem_addr(&tail->empty[s]), 1);
     }
-    mbar_init(smem_addr(&tail->done), 1);
+    for (int i = 0; i < kAccs; ++i) {
+      mbar_init(smem_addr(&tail->acc_full[i]), 1);   // one tcgen05.commit
+      mbar_init(smem_addr(&tail->acc_empty[i]), 4);  // one arrival per epilogue warp
+    }
     tail->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -201,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_h)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
   }
-  if (warp == 5) {  // the whole warp allocates the accumulator's columns
+  if (warp == 5) {  // the whole warp allocates the accumulators' columns
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&tail->tmem_base)),
                  "r"(kTmemCols)
@@ -213,57 +235,96 @@ __global__ void __launch_bounds__(kThreads, 1)
   tmem_fence_after();
   const unsigned tmem = tail->tmem_base;
   volatile unsigned* abort = &tail->abort;
+  const int first = blockIdx.x, step = gridDim.x;
 
   if (warp == 4) {
-    // TMA producer.
+    // TMA producer: the k-blocks of this CTA's tiles, one ring across tiles.
+    // Each step also asks L2 for the k-block kPrefetch steps ahead (in this
+    // tile or the CTA's next one), so that the ring's loads find it there.
     if (lane == 0) {
-      for (int kb = 0; kb < a.nk; ++kb) {
-        const int s = kb % kStages;
-        const unsigned ph = (unsigned)(kb / kStages) & 1u;
-        if (kb >= kStages && !mbar_wait(smem_addr(&tail->empty[s]), ph ^ 1u, abort, a.status))
-          break;
-        const unsigned full = smem_addr(&tail->full[s]);
-        mbar_expect_tx(full, kStageBytes);
-        const unsigned dst = smem_addr(smem + s * kStageBytes);
-        tma_load_2d(dst, &map_h, kb * kBK, m0, full);
-        tma_load_2d(dst + kTileA, &map_w, kb * kBK, n0, full);
+      unsigned it = 0;
+      bool ok = true;
+      int pt = first, pkb = 0;  // the k-block being prefetched
+      auto prefetch_next = [&]() {
+        if (pt >= a.n_tiles) return;
+        tma_prefetch_2d(&map_w, pkb * kBK, (pt / a.n_mt) * kBN);
+        tma_prefetch_2d(&map_h, pkb * kBK, (pt % a.n_mt) * kBM);
+        if (++pkb == a.nk) {
+          pkb = 0;
+          pt += step;
+        }
+      };
+      for (int i = 0; i < kPrefetch; ++i) prefetch_next();
+      for (int t = first; t < a.n_tiles && ok; t += step) {
+        const int m0 = (t % a.n_mt) * kBM, n0 = (t / a.n_mt) * kBN;
+        for (int kb = 0; kb < a.nk; ++kb, ++it) {
+          prefetch_next();
+          const int s = (int)(it % kStages);
+          const unsigned ph = (it / kStages) & 1u;
+          if (it >= kStages && !mbar_wait(smem_addr(&tail->empty[s]), ph ^ 1u, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          const unsigned full = smem_addr(&tail->full[s]);
+          mbar_expect_tx(full, kStageBytes);
+          const unsigned dst = smem_addr(smem + s * kStageBytes);
+          tma_load_2d(dst, &map_h, kb * kBK, m0, full);
+          tma_load_2d(dst + kTileA, &map_w, kb * kBK, n0, full);
+        }
       }
     }
   } else if (warp == 5) {
-    // MMA issuer: four K = 16 steps per stage; the stage is released to the
-    // producer when its MMAs complete, and `done` when the last one does.
+    // MMA issuer: per tile, an accumulator the epilogue has released, four
+    // K = 16 steps per stage; a stage goes back to the producer when its MMAs
+    // complete, and the accumulator to the epilogue when the tile's last does.
     if (lane == 0) {
+      unsigned it = 0, ti = 0;
       bool ok = true;
-      for (int kb = 0; kb < a.nk && ok; ++kb) {
-        const int s = kb % kStages;
-        const unsigned ph = (unsigned)(kb / kStages) & 1u;
-        ok = mbar_wait(smem_addr(&tail->full[s]), ph, abort, a.status);
-        if (!ok) break;
+      for (int t = first; t < a.n_tiles && ok; t += step, ++ti) {
+        const unsigned acc = ti % kAccs, aph = (ti / kAccs) & 1u;
+        if (ti >= kAccs && !mbar_wait(smem_addr(&tail->acc_empty[acc]), aph ^ 1u, abort, a.status))
+          break;
         tmem_fence_after();
-        const unsigned sa = smem_addr(smem + s * kStageBytes);
+        const unsigned d = tmem + acc * 256;
+        for (int kb = 0; kb < a.nk; ++kb, ++it) {
+          const int s = (int)(it % kStages);
+          const unsigned ph = (it / kStages) & 1u;
+          if (!mbar_wait(smem_addr(&tail->full[s]), ph, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tmem_fence_after();
+          const unsigned sa = smem_addr(smem + s * kStageBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t da = smem_desc_sw128(sa + kk * 32);
-          const uint64_t db = smem_desc_sw128(sa + kTileA + kk * 32);
-          mma_bf16(tmem, da, db, kb > 0 || kk > 0);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t da = smem_desc_sw128(sa + kk * 32);
+            const uint64_t db = smem_desc_sw128(sa + kTileA + kk * 32);
+            mma_bf16(d, da, db, kb > 0 || kk > 0);
+          }
+          mma_commit(smem_addr(&tail->empty[s]));
         }
-        mma_commit(smem_addr(&tail->empty[s]));
+        if (ok) mma_commit(smem_addr(&tail->acc_full[acc]));
       }
-      if (ok) mma_commit(smem_addr(&tail->done));
     }
   } else {
-    // Epilogue: thread (warp, lane) owns row m0 + 32 warp + lane of the tile.
-    const int row = m0 + warp * 32 + lane;
-    // tcgen05.ld is warp-wide: the warp reads the accumulator only if every
-    // lane saw it complete.
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&tail->done), 0u, abort, a.status));
-    if (ok) {
+    // Epilogue: thread (warp, lane) owns row 32 warp + lane of each tile.
+    unsigned ti = 0;
+    for (int t = first; t < a.n_tiles; t += step, ++ti) {
+      const unsigned acc = ti % kAccs, aph = (ti / kAccs) & 1u;
+      const int mt = t % a.n_mt, nt = t / a.n_mt;
+      const int m0 = mt * kBM, n0 = nt * kBN;
+      const int row = m0 + warp * 32 + lane;
+      // tcgen05.ld is warp-wide: the warp reads the accumulator only if every
+      // lane saw it complete.
+      const bool ok =
+          __all_sync(0xffffffffu, mbar_wait(smem_addr(&tail->acc_full[acc]), aph, abort, a.status));
+      if (!ok) break;
       tmem_fence_after();
       const int tok = row < a.N ? __ldg(a.tokens + row) : -1;
       const int tcol = tok - n0;  // the token's column in this tile, if in [0, 256)
       float mx = -INFINITY, hmx = -INFINITY, sum = 0.0f, at = 0.0f;
       bool have_at = false;
-      const unsigned tbase = tmem + ((unsigned)(warp * 32) << 16);
+      const unsigned tbase = tmem + acc * 256 + ((unsigned)(warp * 32) << 16);
 #pragma unroll 1
       for (int c = 0; c < kBN / 32; ++c) {
         float v[32];
@@ -292,6 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) sum += ex2_fast(__fmaf_rn(v[j], a.c2, -hmx));
         }
       }
+      // The accumulator is read: hand it back to the MMA warp.
+      tmem_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&tail->acc_empty[acc]));
       // 2^(hmx - mx c2) folds the rounding of hmx back in (to first order).
       if (mx != -INFINITY) sum *= __fmaf_rn(__fmaf_rn(-mx, a.c2, hmx), 0.69314718f, 1.0f);
       if (row < a.N) {
@@ -417,13 +482,16 @@ extern "C" int sv_lmhead_stats(const void* hidden, const void* weight, const int
   // of the function in the device's context).
   static std::mutex attr_mu;
   static bool attr_set[64] = {};
+  static int sm_count[64] = {};
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= 64) return SV_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lock(attr_mu);
     if (!attr_set[device]) {
       if (cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes) != cudaSuccess)
+                               kSmemBytes) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sm_count[device], cudaDevAttrMultiProcessorCount, device) !=
+              cudaSuccess || sm_count[device] < 1)
         return SV_ERR_CUDA;
       attr_set[device] = true;
     }
@@ -438,13 +506,15 @@ extern "C" int sv_lmhead_stats(const void* hidden, const void* weight, const int
   a.n_mt = n_mt;
   a.n_nt = n_nt;
   a.nk = (D + kBK - 1) / kBK;
+  a.n_tiles = n_mt * n_nt;
   const double T = (double)temperature;
   a.c2 = (float)(1.4426950408889634074 / T);
   a.part = reinterpret_cast<float2*>(ws + 256);
   a.at = at;
   a.status = reinterpret_cast<unsigned*>(ws);
   if (cudaMemsetAsync(ws, 0, 4, st) != cudaSuccess) return SV_ERR_CUDA;
-  lmhead_kernel<<<(unsigned)(n_mt * n_nt), kThreads, kSmemBytes, st>>>(mh, mw, a);
+  lmhead_kernel<<<(unsigned)std::min(a.n_tiles, sm_count[device]), kThreads, kSmemBytes, st>>>(
+      mh, mw, a);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   const int rows_per_cta = 8;
   lmhead_combine_kernel<<<(unsigned)((N + rows_per_cta - 1) / rows_per_cta), 32 * rows_per_cta,

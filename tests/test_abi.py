@@ -92,7 +92,7 @@ def test_kernels_per_call(lib):
     # nothing for invalid sizes or B == 0.
     assert sv.sv_kernels_per_call(8, 4, 32000, sv.SV_BF16) == 2      # 4.6 MB
     assert sv.sv_kernels_per_call(64, 8, 128256, sv.SV_BF16) == 1    # 279 MB
-    assert sv.sv_kernels_per_call(256, 4, 256000, sv.SV_F32) == 2    # 2.36 GB
+    assert sv.sv_kernels_per_call(256, 4, 256000, sv.SV_F32) == 3    # 2.36 GB
     assert sv.sv_kernels_per_call(0, 4, 1000, sv.SV_F32) == 0
     assert sv.sv_kernels_per_call(1, 0, 1000, sv.SV_F32) == 0
 
