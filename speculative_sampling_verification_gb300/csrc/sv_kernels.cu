@@ -114,11 +114,11 @@ constexpr int kStatsWarps = kStatsThreads / 32;
 constexpr int kStatsCtasPerSm = 8;
 constexpr int kStatsVec = 8;  // 16-byte vectors per lane per round
 
-template <int DT>
-SV_DEVINL bool any_nan(const uint4 (&v)[kStatsVec]) {
+template <int DT, int N>
+SV_DEVINL bool any_nan(const uint4 (&v)[N]) {
   bool bad = false;
 #pragma unroll
-  for (int i = 0; i < kStatsVec; ++i) {
+  for (int i = 0; i < N; ++i) {
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -132,20 +132,20 @@ SV_DEVINL bool any_nan(const uint4 (&v)[kStatsVec]) {
   return bad;
 }
 
-template <int DT>
-SV_DEVINL void stats_consume(const uint4 (&v)[kStatsVec], float& m_run, float& H,
+template <int DT, int N>
+SV_DEVINL void stats_consume(const uint4 (&v)[N], float& m_run, float& H,
                              float2 (&acc)[2], bool& nan_seen, float c2) {
   float lm;
   if constexpr (DT == 0) {
     uint32_t mx = bf16x2_max(bf16x2_max(v[0].x, v[0].y), bf16x2_max(v[0].z, v[0].w));
 #pragma unroll
-    for (int i = 1; i < kStatsVec; ++i)
+    for (int i = 1; i < N; ++i)
       mx = bf16x2_max(mx, bf16x2_max(bf16x2_max(v[i].x, v[i].y), bf16x2_max(v[i].z, v[i].w)));
     lm = fmaxf(bf16_lo(mx), bf16_hi(mx));
   } else {
     lm = neg_inf();
 #pragma unroll
-    for (int i = 0; i < kStatsVec; ++i)
+    for (int i = 0; i < N; ++i)
       lm = fmaxf(lm, fmaxf(fmaxf(__uint_as_float(v[i].x), __uint_as_float(v[i].y)),
                            fmaxf(__uint_as_float(v[i].z), __uint_as_float(v[i].w))));
   }
@@ -158,12 +158,12 @@ SV_DEVINL void stats_consume(const uint4 (&v)[kStatsVec], float& m_run, float& H
     H = Hn;
   }
   if (m_run == neg_inf()) {  // only -inf (or NaN) entries so far
-    nan_seen |= any_nan<DT>(v);
+    nan_seen |= any_nan<DT, N>(v);
     return;
   }
   const float2 c2p = f2(c2), nH = f2(-H);
 #pragma unroll
-  for (int i = 0; i < kStatsVec; ++i) {
+  for (int i = 0; i < N; ++i) {
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     if constexpr (DT == 0) {
 #pragma unroll
@@ -224,13 +224,52 @@ SV_DEVINL float2 stats_warp_vec(const Params& P, long long u, int lane) {
   float m_run = neg_inf(), H = neg_inf();
   float2 acc[2] = {f2(0.0f), f2(0.0f)};
   bool nan_seen = false;
+  if constexpr (DT == 0) {
+    // bf16 carries twice the elements per byte of fp32, so a round's arithmetic
+    // takes twice as long: two half-rounds of four vectors alternate, the next
+    // one's loads issued before the current one's arithmetic, so that the
+    // lane's loads stay in flight through it.
+    constexpr int kHalf = kStatsVec / 2;
+    constexpr int kH = kHalf * 32;
+    const int nh = nvec / kH;  // whole half-rounds
+    uint4 va[kHalf], vb[kHalf];
+    if (nh > 0) {
+#pragma unroll
+      for (int k = 0; k < kHalf; ++k) va[k] = ld_global_nc_v4(base + (size_t)(k * 32 + lane) * 16);
+    }
+    int h = 0;
+    for (; h + 1 < nh; h += 2) {
+#pragma unroll
+      for (int k = 0; k < kHalf; ++k)
+        vb[k] = ld_global_nc_v4(base + (size_t)((h + 1) * kH + k * 32 + lane) * 16);
+      stats_consume<DT, kHalf>(va, m_run, H, acc, nan_seen, c2);
+      if (h + 2 < nh) {
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k)
+          va[k] = ld_global_nc_v4(base + (size_t)((h + 2) * kH + k * 32 + lane) * 16);
+      }
+      stats_consume<DT, kHalf>(vb, m_run, H, acc, nan_seen, c2);
+    }
+    if (h < nh) stats_consume<DT, kHalf>(va, m_run, H, acc, nan_seen, c2);
+    const int done = nh * kH;
+    if (done < nvec) {  // the last, partial half-round, padded with -inf
+      uint4 v[kHalf];
+#pragma unroll
+      for (int k = 0; k < kHalf; ++k) {
+        const int idx = done + k * 32 + lane;
+        v[k] = idx < nvec ? ld_global_nc_v4(base + (size_t)idx * 16) : make_uint4(fill, fill, fill, fill);
+      }
+      stats_consume<DT, kHalf>(v, m_run, H, acc, nan_seen, c2);
+    }
+    return warp_stats(m_run, H, acc, nan_seen, c2);
+  }
   constexpr int kRound = kStatsVec * 32;
   const int nfull = nvec / kRound * kRound;
   for (int i0 = 0; i0 < nfull; i0 += kRound) {  // whole rounds: no bounds tests
     uint4 v[kStatsVec];
 #pragma unroll
     for (int k = 0; k < kStatsVec; ++k) v[k] = ld_global_nc_v4(base + (size_t)(i0 + k * 32 + lane) * 16);
-    stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
+    stats_consume<DT, kStatsVec>(v, m_run, H, acc, nan_seen, c2);
   }
   if (nfull < nvec) {  // the last, partial round, padded with -inf
     uint4 v[kStatsVec];
@@ -239,7 +278,7 @@ SV_DEVINL float2 stats_warp_vec(const Params& P, long long u, int lane) {
       const int idx = nfull + k * 32 + lane;
       v[k] = idx < nvec ? ld_global_nc_v4(base + (size_t)idx * 16) : make_uint4(fill, fill, fill, fill);
     }
-    stats_consume<DT>(v, m_run, H, acc, nan_seen, c2);
+    stats_consume<DT, kStatsVec>(v, m_run, H, acc, nan_seen, c2);
   }
   return warp_stats(m_run, H, acc, nan_seen, c2);
 }

@@ -46,7 +46,6 @@ constexpr int kBM = 128;             // rows of h per tile (MMA M)
 constexpr int kBN = 256;             // tokens per tile (MMA N)
 constexpr int kBK = 64;              // D per stage: 128 bytes of bf16, one swizzle atom
 constexpr int kStages = 4;
-constexpr int kPrefetch = 8;         // k-blocks requested into L2 ahead of the ring
 constexpr int kThreads = 192;
 constexpr int kTileA = kBM * kBK * 2;   // 16 KB
 constexpr int kTileB = kBN * kBK * 2;   // 32 KB
@@ -133,14 +132,6 @@ SV_DEVINL void tma_load_2d(unsigned dst, const CUtensorMap* map, int x, int y, u
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
-}
-
-// L2 prefetch of the same box (no shared memory, no completion to wait for).
-SV_DEVINL void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
 }
 
 // Shared-memory descriptor of a K-major bf16 tile whose rows are 128 bytes
@@ -239,26 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 4) {
     // TMA producer: the k-blocks of this CTA's tiles, one ring across tiles.
-    // Each step also asks L2 for the k-block kPrefetch steps ahead (in this
-    // tile or the CTA's next one), so that the ring's loads find it there.
     if (lane == 0) {
       unsigned it = 0;
       bool ok = true;
-      int pt = first, pkb = 0;  // the k-block being prefetched
-      auto prefetch_next = [&]() {
-        if (pt >= a.n_tiles) return;
-        tma_prefetch_2d(&map_w, pkb * kBK, (pt / a.n_mt) * kBN);
-        tma_prefetch_2d(&map_h, pkb * kBK, (pt % a.n_mt) * kBM);
-        if (++pkb == a.nk) {
-          pkb = 0;
-          pt += step;
-        }
-      };
-      for (int i = 0; i < kPrefetch; ++i) prefetch_next();
       for (int t = first; t < a.n_tiles && ok; t += step) {
         const int m0 = (t % a.n_mt) * kBM, n0 = (t / a.n_mt) * kBN;
         for (int kb = 0; kb < a.nk; ++kb, ++it) {
-          prefetch_next();
           const int s = (int)(it % kStages);
           const unsigned ph = (it / kStages) & 1u;
           if (it >= kStages && !mbar_wait(smem_addr(&tail->empty[s]), ph ^ 1u, abort, a.status)) {
