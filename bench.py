@@ -838,10 +838,9 @@ def sample_sets(w, n_sets: int, base: int, pin: bool):
 
 
 def sampler_launches(n: int, V: int) -> int:
-    """Kernels of one sampler call: the streaming kernel, then the one-launch
-    draw for calls of fewer than 304 draw chunks of 4096 elements, else the
-    draw's sum and finish kernels (the library's rule)."""
-    return 2 if n * ((V + 4095) // 4096) < 2 * 152 else 3
+    """Kernels of one sampler call: the single-pass sum kernel and the finish
+    kernel."""
+    return 2
 
 
 def run_sampler_reference(args, w, world, rank):
@@ -990,7 +989,7 @@ def run_sampler(args, w, world, rank, local):
         "config": {"workload": w.name + "-draft-rows", "rows": n, "V": V, "input_dtype": w.dtype,
                    "l2": f"inputs rotate over {n_sets} resident sets of {set_bytes / 1e6:.1f} MB",
                    "timing": "K calls in one CUDA graph, CUDA events on the launching stream"},
-        "roofline": {"bound": "hbm", "kernel": "stats_kernel, draw_sum_kernel and draw_finish_kernel (one sampler call)",
+        "roofline": {"bound": "hbm", "kernel": "sample_sum_kernel and sample_finish_kernel (one sampler call)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
                      "bytes_per_launch": set_bytes, "ms_per_launch": per_step_s * 1e3,
@@ -1215,7 +1214,8 @@ def run_filter(args, w, world, rank, local):
     """A step is one filtered verification call over the B sequences of one
     step of the workload. topk: the row selection kernel over all 2K+1 rows,
     then the verification kernel on the kept entries. topp: the per-row cut
-    kernel, the masked copies, then the unfiltered verification kernels."""
+    kernel (which also leaves each row's kept mass), the scan, then the draw
+    with the kept sets applied on load."""
     import speculative_sampling_verification_gb300 as sv
 
     dev = torch.device("cuda", local)
@@ -1241,8 +1241,8 @@ def run_filter(args, w, world, rank, local):
         kernel = "topk_select_kernel + topk_verify_kernel (call time)"
     else:
         ws_bytes = sv.sv_topp_workspace_size(B, K, V, dt_code)
-        launches = 2 + sv.sv_kernels_per_call(B, K, V, dt_code)
-        kernel = "topp_cut_kernel + topp_mask_kernel + the verification kernels (call time)"
+        launches = sv.sv_topp_kernels_per_call(B, K, V, dt_code)
+        kernel = "topp_cluster_kernel + scan_kernel + the masked draw (call time)"
     ws = torch.empty(max(256, ws_bytes), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
 

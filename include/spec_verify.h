@@ -307,7 +307,8 @@ int spec_verify_topk(const void* target_logits, const void* draft_logits,
  * whose probability softmax(l / T) reaches top_p; the other entries count as
  * -inf. The filtered rows are then verified exactly as by spec_verify. */
 
-/* Bytes of device workspace spec_verify_topp needs; 0 for invalid sizes. */
+/* Bytes of device workspace spec_verify_topp needs (spec_verify's, and one
+ * 8-byte cut key per row); 0 for invalid sizes. */
 size_t sv_topp_workspace_size(int B, int K, int V, int dtype);
 
 /* Nucleus filtered verification. Arguments as for spec_verify, plus
@@ -317,14 +318,18 @@ size_t sv_topp_workspace_size(int B, int K, int V, int dtype);
  *   kept_counts  device, [B, 2K+1] int32, may be NULL: entries kept per row
  *                (target rows 0..K, then draft rows 0..K-1); V for a row that
  *                fails (NaN, +inf or all -inf), which is left as it is
- * Per row, a cut is found without a sort: mass histograms over (m - l) / T at
- * finer and finer widths locate the cut to a bin of at most 1024 entries,
- * resolved exactly by a radix select weighted by mass (a bin that never gets
- * that small, from heavy ties, is resolved bit by bit over the key). Weights
- * are float-float exponentials, sums fp64. Masked copies of the rows are then
- * written into the workspace and verified by the unfiltered kernels: four or
- * five kernels per call. Returns SV_OK once enqueued, or a host-side error
- * code with nothing enqueued; B == 0 returns SV_OK at once. */
+ * Per row, a cut is found without a sort: mass histograms over the scaled
+ * distance (m - l) / T of each entry from the row maximum, at finer and finer
+ * widths, locate the cut to a bin of at most 1024 entries, resolved exactly by
+ * a radix select weighted by mass (a bin that never gets that small, from
+ * heavy ties, is resolved bit by bit over the key). Rows up to 1.5 MB are held
+ * in the shared memory of a thread-block cluster (up to 16 CTAs per row), so
+ * each row is read from memory once; longer rows are re-read per pass. Weights
+ * are float-float exponentials. The cut also yields each row's kept mass, so
+ * the verification (a scan kernel, then the draw) reads the rows unchanged
+ * and applies each row's kept set as it loads them: sv_topp_kernels_per_call
+ * kernels per call. Returns SV_OK once enqueued, or a host-side error code
+ * with nothing enqueued; B == 0 returns SV_OK at once. */
 int spec_verify_topp(const void* target_logits, const void* draft_logits,
                      const int32_t* draft_tokens, const float* uniforms, int B, int K, int V,
                      int dtype, float temperature, float top_p, int32_t* out_tokens,
@@ -344,6 +349,11 @@ const char* sv_status_string(int status);
  * a one-launch draw) or 3 (the streaming kernel, the draw's sum kernel and its
  * finish kernel); 0 for invalid sizes or B == 0. */
 int sv_kernels_per_call(int B, int K, int V, int dtype);
+
+/* Kernels one spec_verify_topp call with top_p < 1 over these sizes launches:
+ * the cut kernel, the scan kernel and the draw (one kernel when the draw
+ * needs few chunks, else two), so 3 or 4; 0 for invalid sizes or B == 0. */
+int sv_topp_kernels_per_call(int B, int K, int V, int dtype);
 
 /* Test hook: 0 (the default) chooses the kernels by size, 1 forces the kernel
  * pair, 2 forces the fused kernel. Process-wide; for tests that compare the

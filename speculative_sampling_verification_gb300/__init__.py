@@ -24,7 +24,8 @@ __all__ = [
     "SV_BF16", "SV_F32", "StatusError", "load_library", "sv_workspace_size", "sv_staging_size",
     "spec_verify", "spec_verify_debug", "spec_verify_profiled", "spec_verify_host",
     "sv_read_device_status",
-    "sv_status_string", "sv_kernels_per_call", "spec_verify_static", "verify",
+    "sv_status_string", "sv_kernels_per_call", "sv_topp_kernels_per_call", "spec_verify_static",
+    "verify",
     "sv_sample_workspace_size", "spec_draft_sample", "draft_sample",
     "sv_greedy_workspace_size", "spec_verify_greedy", "verify_greedy", "sv_force_path",
     "sv_test_withhold_plans", "sv_topk_workspace_size", "spec_verify_topk", "verify_topk",
@@ -46,6 +47,7 @@ EXPORTED_SYMBOLS = (
     "sv_greedy_workspace_size", "spec_verify_greedy", "sv_force_path", "sv_test_withhold_plans",
     "sv_topk_workspace_size", "spec_verify_topk", "sv_topp_workspace_size", "spec_verify_topp",
     "spec_verify_host_async", "sv_lmhead_workspace_size", "sv_lmhead_stats",
+    "sv_topp_kernels_per_call",
 )
 
 _lib = None
@@ -110,6 +112,8 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.spec_verify_topp.restype = i32
     lib.sv_kernels_per_call.argtypes = [i32, i32, i32, i32]
     lib.sv_kernels_per_call.restype = i32
+    lib.sv_topp_kernels_per_call.argtypes = [i32, i32, i32, i32]
+    lib.sv_topp_kernels_per_call.restype = i32
     lib.sv_force_path.argtypes = [i32]
     lib.sv_force_path.restype = None
     lib.sv_test_withhold_plans.argtypes = [i32]
@@ -154,6 +158,10 @@ def sv_status_string(code: int) -> str:
 
 def sv_kernels_per_call(B: int, K: int, V: int, dtype: int) -> int:
     return int(load_library().sv_kernels_per_call(B, K, V, dtype))
+
+
+def sv_topp_kernels_per_call(B: int, K: int, V: int, dtype: int) -> int:
+    return int(load_library().sv_topp_kernels_per_call(B, K, V, dtype))
 
 
 def sv_test_withhold_plans(on: bool) -> None:

@@ -17,9 +17,17 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libspecverify.so")
 SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_static_scratch.cu", "sv_lmhead.cu"]
+# Translation units: (source, extra nvcc flags, object). sv_kernels.cu is
+# compiled three times, each unit holding one group of its kernels (SV_TU).
+UNITS = [("sv_kernels.cu", ["-DSV_TU=1"], "sv_kernels_verify.o"),
+         ("sv_kernels.cu", ["-DSV_TU=2"], "sv_kernels_filters.o"),
+         ("sv_kernels.cu", ["-DSV_TU=3"], "sv_kernels_topp.o"),
+         ("sv_api.cu", [], "sv_api.o"),
+         ("sv_static_scratch.cu", [], "sv_static_scratch.o"),
+         ("sv_lmhead.cu", [], "sv_lmhead.o")]
 HEADERS = ["sv_device.cuh", "sv_internal.h", "sv_exp_table.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-diag-suppress=177",
          "--expt-relaxed-constexpr"]
 
 
@@ -50,9 +58,9 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(LIBDIR, exist_ok=True)
     cc = nvcc()
     objs, procs = [], []
-    for src in SOURCES:
-        obj = os.path.join(LIBDIR, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+    for src, extra, name in UNITS:
+        obj = os.path.join(LIBDIR, name)
+        cmd = [cc, *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd))
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))

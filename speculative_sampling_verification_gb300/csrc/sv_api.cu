@@ -398,21 +398,15 @@ int spec_verify_topk(const void* target_logits, const void* draft_logits,
 
 namespace {
 
-// Nucleus path workspace: the unfiltered layout, then the masked target and
-// draft copies, then one cut key per row.
+// Nucleus path workspace: the unfiltered layout, then one cut key per row.
 struct ToppLayout {
   sv::Layout L;
-  size_t off_mt, off_md, off_cut, total;
+  size_t off_cut, total;
 };
 
 bool make_topp_layout(int B, int K, int V, int dtype, ToppLayout* T) {
   if (!sv::make_layout(B, K, V, dtype, &T->L)) return false;
-  const size_t es = T->L.es;
   size_t off = sv::align_up(T->L.total, 256);
-  T->off_mt = off;
-  off = sv::align_up(off + (size_t)B * (K + 1) * V * es, 256);
-  T->off_md = off;
-  off = sv::align_up(off + (size_t)B * K * V * es, 256);
   T->off_cut = off;
   off = sv::align_up(off + (size_t)B * (2 * K + 1) * 8, 256);
   T->total = off;
@@ -468,13 +462,11 @@ int spec_verify_topp(const void* target_logits, const void* draft_logits,
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   P.topp_cut = reinterpret_cast<unsigned long long*>(ws + TL.off_cut);
   P.topp_kept = kept_counts;
-  void* mt = ws + TL.off_mt;
-  void* md = ws + TL.off_md;
+  P.out_tokens = out_tokens;
+  P.n_acc = n_accepted;
   const bool aligned = !misaligned(target_logits, 16) && !misaligned(draft_logits, 16) &&
                        ((size_t)V * TL.L.es) % 16 == 0;
-  if (sv::launch_topp(P, aligned, mt, md, st) != cudaSuccess) return SV_ERR_CUDA;
-  return run(mt, md, draft_tokens, uniforms, B, K, V, dtype, temperature, out_tokens, n_accepted,
-             workspace, workspace_bytes, stream, nullptr, nullptr, nullptr);
+  return sv::launch_topp(P, aligned, st) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 int sv_read_device_status(const void* workspace, void* stream, int* status) {
@@ -514,6 +506,12 @@ int sv_kernels_per_call(int B, int K, int V, int dtype) {
   sv::Layout L;
   if (!sv::make_layout(B, K, V, dtype, &L) || B == 0) return 0;
   return sv::kernels_per_call(B, L.rows_per_seq, V, L.es);
+}
+
+int sv_topp_kernels_per_call(int B, int K, int V, int dtype) {
+  sv::Layout L;
+  if (!sv::make_layout(B, K, V, dtype, &L) || B == 0) return 0;
+  return L.sub_elems == 512 ? 4 : 3;
 }
 
 void sv_force_path(int path) { sv::force_path(path); }

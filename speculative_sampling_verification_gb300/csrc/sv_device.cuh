@@ -89,6 +89,60 @@ SV_DEVINL void bulk_copy_g2s(unsigned dst, const void* src, unsigned bytes, unsi
       : "memory");
 }
 
+// ---------------------------------------------------------------- thread-block clusters
+
+SV_DEVINL unsigned cluster_ctarank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster: shared-memory writes before it
+// are visible to the cluster's loads after it.
+SV_DEVINL void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// The two halves of cluster_sync, for a barrier whose wait comes later (the
+// arrival orders nothing).
+SV_DEVINL void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+SV_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// The shared::cluster address of this CTA's shared variable at `addr` in the
+// CTA of rank `rank`.
+SV_DEVINL unsigned dsmem_map(unsigned addr, unsigned rank) {
+  unsigned r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+SV_DEVINL float dsmem_ld_f32(unsigned a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+SV_DEVINL unsigned dsmem_ld_u32(unsigned a) {
+  unsigned v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+SV_DEVINL void dsmem_st_u64(unsigned a, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+SV_DEVINL void dsmem_st_f32(unsigned a, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+SV_DEVINL void dsmem_st_f32x2(unsigned a, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+}
+SV_DEVINL unsigned dsmem_atomic_add_u32(unsigned a, unsigned v) {
+  unsigned old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- bf16 and fast fp32 helpers
 
 SV_DEVINL float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

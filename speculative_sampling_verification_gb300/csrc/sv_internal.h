@@ -217,10 +217,9 @@ cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t stream);
 // Top-k filtered verification: the row selection kernel, then the sparse
 // verification kernel.
 cudaError_t launch_topk(const Params& P, bool aligned, cudaStream_t stream);
-// Nucleus filtering: the per-row cut kernel, then the masked copies of the
-// target and draft rows (the verification then runs on the copies).
-cudaError_t launch_topp(const Params& P, bool aligned, void* masked_target, void* masked_draft,
-                        cudaStream_t stream);
+// Nucleus-filtered verification: the per-row cut (with each row's kept-set
+// statistics), the scan, then the draw with the kept sets applied on load.
+cudaError_t launch_topp(Params P, bool aligned, cudaStream_t stream);
 cudaError_t fill_int(int* p, long long n, int v, cudaStream_t stream);
 // Kernels one call over B sequences of rows_per_seq rows of V elements of
 // `es` bytes launches: 1 when the fused kernel is taken, else 2.

@@ -34,10 +34,20 @@
 #include <type_traits>
 #include <cstdint>
 #include <atomic>
+#include <map>
 #include <mutex>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
+
+// This file is compiled as several translation units, in parallel: SV_TU
+// selects which host launchers (and so which kernel instantiations) a unit
+// holds: 1 the verification and the sampler, 2 greedy mode and top-k, 3 the
+// nucleus path; 0 (the default) all of them.
+#ifndef SV_TU
+#define SV_TU 0
+#endif
+#define SV_TU_HAS(n) (SV_TU == 0 || SV_TU == (n))
 
 namespace sv {
 
@@ -347,6 +357,68 @@ SV_DEVINL float2 row_combine(const Params& P, long long row, int lane) {
   return warp_combine_pairs(m, s, P.c2);
 }
 
+// ---------------------------------------------------------------- keys and kept sets of nucleus-filtered rows
+
+// Order-preserving map of a bf16 (16-bit) or f32 bit pattern to an unsigned
+// key: unsigned order is numeric order, -0 folded into +0.
+template <int DT>
+SV_DEVINL uint32_t value_key(uint32_t bits) {
+  if constexpr (DT == 0) {
+    if (bits == 0x8000u) bits = 0;
+    return (bits & 0x8000u) ? (~bits & 0xffffu) : (bits | 0x8000u);
+  } else {
+    if (bits == 0x80000000u) bits = 0;
+    return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+  }
+}
+
+// The logit back from a key (value_key above the low `ib` id bits).
+template <int DT>
+SV_DEVINL float key_value(unsigned long long key, int ib) {
+  const uint32_t vk = (uint32_t)(key >> ib);
+  if constexpr (DT == 0) {
+    const uint32_t h = (vk & 0x8000u) ? (vk & 0x7fffu) : (~vk & 0xffffu);
+    return __uint_as_float(h << 16);
+  } else {
+    return __uint_as_float((vk & 0x80000000u) ? (vk & 0x7fffffffu) : ~vk);
+  }
+}
+
+// The kept set of a nucleus-filtered row as a test on the loaded value: the
+// entry (x, id) is kept iff its key (value, then smaller id first) is at or
+// above the row's cut, i.e. x > xc, or x == xc and id <= imax (xc the cut
+// entry's value; -0.0 equals +0.0 in both orders). A row without a cut keeps
+// everything (xc = -inf, imax the largest id).
+struct RowMask {
+  float xc;
+  long long imax;
+};
+
+SV_DEVINL float masked(float x, long long id, const RowMask& k) {
+  return (x > k.xc || (x == k.xc && id <= k.imax)) ? x : neg_inf();
+}
+
+// Row r (0..K target, K+1..2K draft) of sequence b: its cut as a RowMask.
+SV_DEVINL RowMask row_mask(const Params& P, long long b, int r) {
+  RowMask k{neg_inf(), 0x7fffffffffffffffLL};
+  if (!P.topp_cut) return k;
+  const unsigned long long cut = __ldcg(P.topp_cut + b * P.rows_per_seq + r);
+  if (cut == 0) return k;
+  k.xc = P.dtype == 0 ? key_value<0>(cut, P.key_ibits) : key_value<1>(cut, P.key_ibits);
+  k.imax = (long long)P.V - 1 - (long long)(cut & ((1ull << P.key_ibits) - 1));
+  return k;
+}
+
+// Whether the entry (x, id) of a row with cut `cut` is kept (cut 0: every
+// entry), by the key itself.
+template <int DT>
+SV_DEVINL bool kept_by_key(float x, int id, unsigned long long cut, int ib, int V) {
+  const uint32_t bits = DT == 0 ? (__float_as_uint(x) >> 16) : __float_as_uint(x);
+  const unsigned long long key =
+      ((unsigned long long)value_key<DT>(bits) << ib) | (unsigned long long)(V - 1 - id);
+  return key >= cut;
+}
+
 // ---------------------------------------------------------------- scan of one sequence, one warp
 
 struct WarpScan {
@@ -406,6 +478,16 @@ SV_DEVINL void scan_warp(const Params& P, long long b, int lane, WarpScan& ws) {
       } else {
         lq = load_elem<1>(row_base(P, b, t), x);
         lp = load_elem<1>(row_base(P, b, K + 1 + t), x);
+      }
+      if (P.topp_cut) {  // nucleus-filtered rows: an entry outside the kept set is -inf
+        const unsigned long long cq = __ldcg(P.topp_cut + b * R + t);
+        const unsigned long long cp = __ldcg(P.topp_cut + b * R + K + 1 + t);
+        const bool kq = P.dtype == 0 ? kept_by_key<0>(lq, x, cq, P.key_ibits, P.V)
+                                     : kept_by_key<1>(lq, x, cq, P.key_ibits, P.V);
+        const bool kp = P.dtype == 0 ? kept_by_key<0>(lp, x, cp, P.key_ibits, P.V)
+                                     : kept_by_key<1>(lp, x, cp, P.key_ibits, P.V);
+        if (!kq) lq = neg_inf();
+        if (!kp) lp = neg_inf();
       }
       const float mq = ws.m[t], mp = ws.m[K + 1 + t];
       const float sq = ws.s[t], sp = ws.s[K + 1 + t];
@@ -532,6 +614,9 @@ struct DrawRow {
   int2 qb;
   float alpha, beta, lmin;
   DrawConst dc;
+  // Nucleus-filtered rows: the kept set of each row (RowMask), applied to
+  // every element as it is loaded.
+  RowMask kq, kp;
 };
 
 // Exponent shift of one row in the fast form, and its factor 2^(q0 - m c2)
@@ -560,6 +645,8 @@ SV_DEVINL DrawRow draw_row(const Params& P, const Plan& pl) {
   d.beta = resid ? pl.s_q * exp2f((float)q0p - cp) : 0.0f;
   d.lmin = -2048.0f * __fdividef(1.0f, P.ih);
   d.dc = DrawConst{P.d_inv, P.d_ch, P.d_cli, P.ih};
+  d.kq = row_mask(P, pl.row_q / (P.K + 1), (int)(pl.row_q % (P.K + 1)));
+  d.kp = resid ? row_mask(P, pl.row_p / P.K, P.K + 1 + (int)(pl.row_p % P.K)) : d.kq;
   return d;
 }
 
@@ -603,7 +690,7 @@ SV_DEVINL void load_run(const unsigned char* row, long long e, int V, bool vec_o
 
 // ---------------------------------------------------------------- draw: one chunk
 
-template <int DT, bool RESID, int SUB>
+template <int DT, bool RESID, int SUB, bool MASK = false>
 SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab,
                             const float2* tab1k, bool aligned, long long b, int c) {
   constexpr int kVec = 16 / (DT == 0 ? 2 : 4);
@@ -624,6 +711,13 @@ SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab
         float xq[kVec], xp[kVec];
         load_run<DT>(d.rq, e, P.V, aligned, xq);
         load_run<DT>(d.rp, e, P.V, aligned, xp);
+        if constexpr (MASK) {
+#pragma unroll
+          for (int k = 0; k < kVec; ++k) {
+            xq[k] = masked(xq[k], e + k, d.kq);
+            xp[k] = masked(xp[k], e + k, d.kp);
+          }
+        }
 #pragma unroll
         for (int k = 0; k < kVec; ++k) {
           const float2 l = make_float2(fmaxf(xq[k], lmin.x), fmaxf(xp[k], lmin.y));
@@ -644,6 +738,10 @@ SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab
         const long long e = e0 + (long long)r * 32 * kVec + lane * kVec;
         float xq[kVec];
         load_run<DT>(d.rq, e, P.V, aligned, xq);
+        if constexpr (MASK) {
+#pragma unroll
+          for (int k = 0; k < kVec; ++k) xq[k] = masked(xq[k], e + k, d.kq);
+        }
 #pragma unroll
         for (int k = 0; k < kVec; k += 2) {
           const float2 l = make_float2(fmaxf(xq[k], lmin.x), fmaxf(xq[k + 1], lmin.x));
@@ -666,6 +764,13 @@ SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab
         float xq[kVec], xp[kVec];
         load_run<DT>(d.rq, e, P.V, aligned, xq);
         load_run<DT>(d.rp, e, P.V, aligned, xp);
+        if constexpr (MASK) {
+#pragma unroll
+          for (int k = 0; k < kVec; ++k) {
+            xq[k] = masked(xq[k], e + k, d.kq);
+            xp[k] = masked(xp[k], e + k, d.kp);
+          }
+        }
 #pragma unroll
         for (int k = 0; k < kVec; ++k) {
           const ff2 x = scaled_diff2(make_float2(xq[k], xp[k]), nm, d.ih, d.il, d.unit_t);
@@ -686,6 +791,10 @@ SV_DEVINL void partial_body(const Params& P, const DrawRow& d, const float2* tab
         const long long e = e0 + (long long)r * 32 * kVec + lane * kVec;
         float xq[kVec];
         load_run<DT>(d.rq, e, P.V, aligned, xq);
+        if constexpr (MASK) {
+#pragma unroll
+          for (int k = 0; k < kVec; ++k) xq[k] = masked(xq[k], e + k, d.kq);
+        }
 #pragma unroll
         for (int k = 0; k < kVec; k += 2) {
           const ff2 x = scaled_diff2(make_float2(xq[k], xq[k + 1]), nm, d.ih, d.il, d.unit_t);
@@ -775,7 +884,7 @@ SV_DEVINL ff block_exclusive_ff(ff x, CtaShared& sh) {
 // weight before sub-chunk g is S_p * (A[0] + .. + A[g-1]) - S_q * (B[0] + ..
 // + B[g-1]) with S_p, S_q the row totals (at the end: R = S_p A - S_q B), for
 // the bonus draw (or the zero-residual fallback) it is S_q[0] + .. + S_q[g-1].
-template <int DT, int SUB>
+template <int DT, int SUB, bool MASK = false>
 SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShared& sh,
                           bool aligned) {
   constexpr int kPer = SUB / kThreads;  // elements per thread in the exact search
@@ -837,6 +946,17 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
   const bool res_first = resid && R.hi > 0x1p-40f * (SA.hi + SB.hi);
   const BlockScan2 bs_res = bs;
   const DrawRow d = draw_row(P, pl);
+  // Element loads of the two rows (the kept set applied, for filtered rows).
+  auto ld_q = [&](long long e) {
+    const float x = load_elem<DT>(d.rq, e);
+    if constexpr (MASK) return masked(x, e, d.kq);
+    return x;
+  };
+  auto ld_p = [&](long long e) {
+    const float x = load_elem<DT>(d.rp, e);
+    if constexpr (MASK) return masked(x, e, d.kp);
+    return x;
+  };
 
   // One search: the sub-chunk holding u * total, then the element within it.
   // Returns whether a token was written (uniform across the CTA).
@@ -915,14 +1035,14 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
       const long long e = e0 + k;
       w[k] = {0.f, 0.f};
       if (e < P.V) {
-        const float lq = load_elem<DT>(d.rq, e);
+        const float lq = ld_q(e);
         ff eq, ep;
         bool pos;
         if (d.fast) {
           const float lqc = fmaxf(lq, d.lmin);
           const ff fq = exp_draw(lqc, d.qb.x, d.dc, sh.tab1k);
           if (use_res) {
-            const float lpc = fmaxf(load_elem<DT>(d.rp, e), d.lmin);
+            const float lpc = fmaxf(ld_p(e), d.lmin);
             const ff fp = exp_draw(lpc, d.qb.y, d.dc, sh.tab1k);
             pos = __fmul_rn(__fadd_rn(fq.hi, fq.lo), d.alpha) >
                   __fmul_rn(__fadd_rn(fp.hi, fp.lo), d.beta);
@@ -931,7 +1051,7 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
             w[k] = ff_normalize(fq);
           }
         } else if (use_res) {
-          const float lp = load_elem<DT>(d.rp, e);
+          const float lp = ld_p(e);
           element_exps<true>(d, lq, lp, sh.tab, eq, ep, pos);
           if (pos) w[k] = ff_sub(ff_mul(ff_normalize(eq), Sp), ff_mul(ff_normalize(ep), Sq));
         } else {
@@ -971,10 +1091,10 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
         // taken with the precise exponential in the same scaling.
         ff wt = w[pick % kPer];
         if (d.fast) {
-          const float lqc = fmaxf(load_elem<DT>(d.rq, e), d.lmin);
+          const float lqc = fmaxf(ld_q(e), d.lmin);
           const ff pq = ff_normalize(exp_precise(lqc, d.qb.x, d.ih, d.il, sh.tab));
           if (use_res) {
-            const float lpc = fmaxf(load_elem<DT>(d.rp, e), d.lmin);
+            const float lpc = fmaxf(ld_p(e), d.lmin);
             const ff pp = ff_normalize(exp_precise(lpc, d.qb.y, d.ih, d.il, sh.tab));
             wt = ff_sub(ff_mul(pq, Sp), ff_mul(pp, Sq));
           } else {
@@ -1086,7 +1206,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) stats_kernel(P
 // Chunk c of sequence b's draw, by one CTA whose table is loaded and whose
 // view of the plan is current: the sub-chunk sums, and the finish in the CTA
 // that counts the sequence's last chunk.
-template <int DT, bool VEC, int SUB>
+template <int DT, bool VEC, int SUB, bool MASK = false>
 SV_DEVINL void draw_chunk(const Params& P, long long b, int c, CtaShared& sh) {
   const int tid = threadIdx.x;
   if (tid == 0) {
@@ -1108,13 +1228,13 @@ SV_DEVINL void draw_chunk(const Params& P, long long b, int c, CtaShared& sh) {
   if (pl.mode == kModeFailed) return;  // outputs already written by the scan
   const DrawRow d = draw_row(P, pl);
   if (pl.mode == kModeResidual)
-    partial_body<DT, true, SUB>(P, d, sh.tab, sh.tab1k, VEC, b, c);
+    partial_body<DT, true, SUB, MASK>(P, d, sh.tab, sh.tab1k, VEC, b, c);
   else
-    partial_body<DT, false, SUB>(P, d, sh.tab, sh.tab1k, VEC, b, c);
+    partial_body<DT, false, SUB, MASK>(P, d, sh.tab, sh.tab1k, VEC, b, c);
   __syncthreads();  // all sub-chunk writes of this CTA precede the release below
   if (tid == 0) sh.flag = atomic_add_acq_rel(P.done_p + b, 1u) == (unsigned)(P.np - 1);
   __syncthreads();
-  if (sh.flag) finish_seq<DT, SUB>(P, b, pl, sh, VEC);  // the barrier above orders its reads
+  if (sh.flag) finish_seq<DT, SUB, MASK>(P, b, pl, sh, VEC);  // the barrier above orders its reads
 }
 
 
@@ -1122,7 +1242,7 @@ SV_DEVINL void draw_chunk(const Params& P, long long b, int c, CtaShared& sh) {
 // one CTA per draw chunk; the CTA that counts the last chunk of a sequence
 // runs its inverse-CDF search. For such calls the finish kernel's launch
 // would cost more than the CTA barrier it saves.
-template <int DT, bool VEC, int SUB>
+template <int DT, bool VEC, int SUB, bool MASK = false>
 __global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
   __shared__ CtaShared sh;
   sh.tab[threadIdx.x] = kSvExp2Table[threadIdx.x];
@@ -1131,7 +1251,7 @@ __global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
   // Wait until the streaming grid has completed and its writes are visible
   // (immediate when this kernel was launched as an ordinary dependent).
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  draw_chunk<DT, VEC, SUB>(P, blockIdx.x / P.np, (int)(blockIdx.x % P.np), sh);
+  draw_chunk<DT, VEC, SUB, MASK>(P, blockIdx.x / P.np, (int)(blockIdx.x % P.np), sh);
 }
 
 // ---------------------------------------------------------------- the kernel pair's draw
@@ -1144,7 +1264,7 @@ __global__ void __launch_bounds__(kThreads, 5) draw_kernel(Params P) {
 // before them: they become resident while it ends, load their tables, and
 // wait on the device for it to complete.
 
-template <int DT, bool VEC, int SUB>
+template <int DT, bool VEC, int SUB, bool MASK = false>
 __global__ void __launch_bounds__(kThreads, 5) draw_sum_kernel(Params P) {
   __shared__ float2 tab[256];
   __shared__ float2 tab1k[1024];
@@ -1175,12 +1295,12 @@ __global__ void __launch_bounds__(kThreads, 5) draw_sum_kernel(Params P) {
   if (pl.mode == kModeFailed) return;  // outputs already written by the scan
   const DrawRow d = draw_row(P, pl);
   if (pl.mode == kModeResidual)
-    partial_body<DT, true, SUB>(P, d, tab, tab1k, VEC, b, c);
+    partial_body<DT, true, SUB, MASK>(P, d, tab, tab1k, VEC, b, c);
   else
-    partial_body<DT, false, SUB>(P, d, tab, tab1k, VEC, b, c);
+    partial_body<DT, false, SUB, MASK>(P, d, tab, tab1k, VEC, b, c);
 }
 
-template <int DT, bool VEC, int SUB>
+template <int DT, bool VEC, int SUB, bool MASK = false>
 __global__ void __launch_bounds__(kThreads) draw_finish_kernel(Params P) {
   __shared__ CtaShared sh;
   const int tid = threadIdx.x;
@@ -1193,7 +1313,194 @@ __global__ void __launch_bounds__(kThreads) draw_finish_kernel(Params P) {
   __syncthreads();
   const Plan pl = sh.plan;
   if (pl.mode == kModeFailed) return;
-  finish_seq<DT, SUB>(P, b, pl, sh, VEC);
+  finish_seq<DT, SUB, MASK>(P, b, pl, sh, VEC);
+}
+
+// ---------------------------------------------------------------- the draft-side sampler
+//
+// One token per row drawn from softmax(l/T) in a single read of the row.
+// sample_sum_kernel: each warp loads its sub-chunk into registers, takes the
+// sub-chunk's own maximum m_g, and sums its weights exp(l/T) 2^-q0_g in
+// float-float with the fast exponential, q0_g = floor(m_g log2(e)/T) + 1; it
+// records (sum, m_g, flags). sample_finish_kernel (one CTA per row): the row
+// maximum is the largest m_g; each sub-chunk sum times 2^(q0_g - q0_row) is an
+// exact power-of-two rescaling to the row's own shift, after which the
+// verifier's finish draws the token as its bonus draw does. A row whose
+// maximum lies beyond the fast form's range has its sums recomputed by the
+// finish CTA in the shifted form.
+
+constexpr unsigned kSubNonfinite = 1u, kSubExtreme = 2u;
+
+template <int DT, bool VEC, int SUB>
+__global__ void __launch_bounds__(kThreads, 5) sample_sum_kernel(Params P) {
+  constexpr int kVec = 16 / (DT == 0 ? 2 : 4);
+  constexpr int kRuns = SUB / (32 * kVec);
+  __shared__ float2 tab1k[1024];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tab1k[tid + i * kThreads] = kSvExp2Table1024[tid + i * kThreads];
+  __syncthreads();
+  const long long r = blockIdx.x / P.np;
+  const int c = (int)(blockIdx.x % P.np);
+  const long long e0 = ((long long)c * kSubPerChunk + w) * SUB;
+  const unsigned char* row = static_cast<const unsigned char*>(P.target) + (size_t)r * P.V * P.es;
+  float x[kRuns][kVec];
+  float mx = neg_inf();
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < kRuns; ++k) {
+    const long long e = e0 + (long long)k * 32 * kVec + lane * kVec;
+    if (e0 < P.V) {
+      load_run<DT>(row, e, P.V, VEC, x[k]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) x[k][j] = neg_inf();
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      bad |= x[k][j] != x[k][j] || x[k][j] == -neg_inf();
+      mx = fmaxf(mx, x[k][j]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  bad = __any_sync(0xffffffffu, bad);
+  unsigned flags = bad ? kSubNonfinite : 0u;
+  ff S = ff_bias_start();
+  if (!bad && mx != neg_inf()) {
+    const float cm = mx * P.c2;
+    if (fabsf(cm) <= 2000.0f) {
+      const int q0 = row_q0(mx, P.c2);
+      const int2 qb = make_int2(127 - q0, 127 - q0);
+      const DrawConst dc{P.d_inv, P.d_ch, P.d_cli, P.ih};
+      const float lmin = -2048.0f * __fdividef(1.0f, P.ih);
+#pragma unroll
+      for (int k = 0; k < kRuns; ++k) {
+#pragma unroll
+        for (int j = 0; j < kVec; j += 2) {
+          const float2 l = make_float2(fmaxf(x[k][j], lmin), fmaxf(x[k][j + 1], lmin));
+          const ff2 ex = exp_draw2(l, qb, dc, tab1k);
+          ff_accumulate_biased(S, {ex.hi.x, ex.lo.x});
+          ff_accumulate_biased(S, {ex.hi.y, ex.lo.y});
+        }
+      }
+    } else {
+      flags |= kSubExtreme;
+    }
+  }
+  S = ff_warp_sum(ff_bias_end(S));
+  if (lane == 0) {
+    float4* out = reinterpret_cast<float4*>(
+        P.sub_part + (((size_t)r * P.nchunk + c) * kSubPerChunk + w) * 4);
+    out[0] = make_float4(S.hi, S.lo, mx, __uint_as_float(flags));
+    out[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+template <int DT, bool VEC, int SUB>
+__global__ void __launch_bounds__(kThreads) sample_finish_kernel(Params P) {
+  __shared__ CtaShared sh;
+  __shared__ float s_m[kWarps];
+  __shared__ unsigned s_f[kWarps];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  sh.tab[tid] = kSvExp2Table[tid];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sh.tab1k[tid + i * kThreads] = kSvExp2Table1024[tid + i * kThreads];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long r = blockIdx.x;
+  const int nsub = P.nchunk * kSubPerChunk;
+  float4* part = reinterpret_cast<float4*>(P.sub_part + (size_t)r * nsub * 4);
+  // The row's maximum and flags.
+  float m = neg_inf();
+  unsigned flags = 0;
+  for (int g = tid; g < nsub; g += kThreads) {
+    const float4 rec = __ldcg(part + 2 * g);
+    m = fmaxf(m, rec.z);
+    flags |= __float_as_uint(rec.w);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    flags |= __shfl_xor_sync(0xffffffffu, flags, o);
+  }
+  if (lane == 0) {
+    s_m[w] = m;
+    s_f[w] = flags;
+  }
+  __syncthreads();
+  m = s_m[0];
+  flags = s_f[0];
+  for (int i = 1; i < kWarps; ++i) {
+    m = fmaxf(m, s_m[i]);
+    flags |= s_f[i];
+  }
+  unsigned bits = 0;
+  if (flags & kSubNonfinite) {
+    bits = kDevNonfinite;
+  } else if (m == neg_inf()) {
+    bits = kDevEmptyRow;
+  }
+  const float u = P.uniforms[r];
+  if (!(u >= 0.0f && u <= 1.0f)) bits |= kDevUniformRange;
+  if (bits) {
+    if (tid == 0) {
+      atomicOr(P.status, bits);
+      P.out_tokens[r] = -1;
+      if (P.dbg_prob) P.dbg_prob[r] = __longlong_as_double(0x7ff8000000000000LL);
+      if (P.dbg_lse) P.dbg_lse[r] = __longlong_as_double(0x7ff8000000000000LL);
+    }
+    return;
+  }
+  Plan pl{};
+  pl.j = 0;
+  pl.mode = kModeBonus;
+  pl.row_q = r;
+  pl.row_p = -1;
+  pl.m_q = m;
+  pl.s_q = 1.0f;
+  pl.u = u;
+  const float cm = m * P.c2;
+  double lse_scale;  // log of the factor the row's weights carry: exp(l/T) = w * e^lse_scale
+  if ((flags & kSubExtreme) || fabsf(cm) > 2000.0f) {
+    // Beyond the fast form's range: the row's sums again, in the shifted form
+    // (weights exp((l - m)/T)), one sub-chunk per warp.
+    __syncthreads();
+    const DrawRow d = draw_row(P, pl);
+    for (int c = 0; c < P.nchunk; ++c) partial_body<DT, false, SUB>(P, d, sh.tab, sh.tab1k, VEC, r, c);
+    lse_scale = (double)m * P.inv_t;
+  } else {
+    // Exact rescaling of every sub-chunk sum to the row's shift.
+    const int q0r = row_q0(m, P.c2);
+    for (int g = tid; g < nsub; g += kThreads) {
+      const float4 rec = __ldcg(part + 2 * g);
+      float f = 0.0f;
+      if (rec.z != neg_inf()) {
+        const int e = row_q0(rec.z, P.c2) - q0r;  // <= 0
+        f = e < -126 ? 0.0f : __int_as_float((e + 127) << 23);
+      }
+      part[2 * g] = make_float4(rec.x * f, rec.y * f, 0.f, 0.f);
+    }
+    lse_scale = (double)q0r * 0.69314718055994530942;
+  }
+  __threadfence_block();
+  __syncthreads();
+  if (P.dbg_lse) {  // log sum_i exp(l_i / T), from the row's float-float total
+    ff t{0.f, 0.f};
+    for (int g = tid; g < nsub; g += kThreads) {
+      const float4 rec = __ldcg(part + 2 * g);
+      t = ff_add(t, ff{rec.x, rec.y});
+    }
+    t = ff_warp_sum(t);
+    __syncthreads();
+    if (lane == 0) sh.red4[w][0] = t;
+    __syncthreads();
+    if (tid == 0) {
+      ff tot{0.f, 0.f};
+      for (int i = 0; i < kWarps; ++i) tot = ff_add(tot, sh.red4[i][0]);
+      P.dbg_lse[r] = lse_scale + log(ff_to_double(tot));
+    }
+  }
+  finish_seq<DT, SUB>(P, r, pl, sh, VEC);
 }
 
 // ---------------------------------------------------------------- the fused kernel
@@ -1536,31 +1843,6 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelTile = kSelThreads * 8;  // elements per tile: 8 consecutive per thread
 constexpr int kSelCap = 5120;              // candidate buffer entries
 static_assert(kTopKMax == kSelThreads, "the final stage gives one kept entry per thread");
-
-// Order-preserving map of a bf16 (16-bit) or f32 bit pattern to an unsigned
-// key: unsigned order is numeric order, -0 folded into +0.
-template <int DT>
-SV_DEVINL uint32_t value_key(uint32_t bits) {
-  if constexpr (DT == 0) {
-    if (bits == 0x8000u) bits = 0;
-    return (bits & 0x8000u) ? (~bits & 0xffffu) : (bits | 0x8000u);
-  } else {
-    if (bits == 0x80000000u) bits = 0;
-    return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
-  }
-}
-
-// The logit back from a key (value_key above the low `ib` id bits).
-template <int DT>
-SV_DEVINL float key_value(unsigned long long key, int ib) {
-  const uint32_t vk = (uint32_t)(key >> ib);
-  if constexpr (DT == 0) {
-    const uint32_t h = (vk & 0x8000u) ? (vk & 0x7fffu) : (~vk & 0xffffu);
-    return __uint_as_float(h << 16);
-  } else {
-    return __uint_as_float((vk & 0x80000000u) ? (vk & 0x7fffffffu) : ~vk);
-  }
-}
 
 template <int DT>
 SV_DEVINL bool nan_or_pos_inf(uint32_t bits) {
@@ -2060,6 +2342,7 @@ struct TopKVerifyShared {
 // The thresholds use the per-row probabilities of the drafted tokens; the
 // draw walks the k kept entries of the drawn row in ascending id, one per
 // thread, with the draft row's kept list in shared memory for the residual.
+#if SV_TU_HAS(2)
 __global__ void __launch_bounds__(kTvThreads) topk_verify_kernel(Params P) {
   __shared__ TopKVerifyShared sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -2159,6 +2442,7 @@ __global__ void __launch_bounds__(kTvThreads) topk_verify_kernel(Params P) {
     if (t > j) P.out_tokens[b * (K + 1) + t] = -1;
   }
 }
+#endif  // SV_TU_HAS(2)
 
 // ---------------------------------------------------------------- nucleus (top-p) filtered verification
 //
@@ -2179,8 +2463,10 @@ __global__ void __launch_bounds__(kTvThreads) topk_verify_kernel(Params P) {
 //      resolved bit by bit over the key with a pass per bit.
 // Weights are exp((l - m) / T) in float-float (the same exp as the unfiltered
 // path, ~1e-12 relative); masses are summed as float-float per thread and in
-// fp64 across threads. The masked rows (-inf outside the kept set) are then
-// verified by the unfiltered kernels.
+// fp64 across threads. This kernel re-reads the row from global memory for
+// every pass; it serves rows too long for a cluster's shared memory (the
+// cluster kernel below takes the others). Like that kernel it leaves the row's
+// statistics (m, S_kept) for the verification.
 
 constexpr int kTpThreads = 256;
 constexpr int kTpBins = 16;
@@ -2285,10 +2571,12 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_cut_kernel(Params P) {
   m = (float)sh.red[0];
   for (int w2 = 1; w2 < kTpThreads / 32; ++w2) m = fmaxf(m, (float)sh.red[w2]);
   if (any_bad || m == -CUDART_INF_F) {
-    // A failing row stays as it is (the verification reports it).
+    // A failing row: the verification reports it from the statistics.
     if (tid == 0) {
       P.topp_cut[row] = 0;
       if (P.topp_kept) P.topp_kept[row] = V;
+      P.row_stat[row] = any_bad ? make_float2(0.0f, __int_as_float(0x7fc00000))
+                                : make_float2(-CUDART_INF_F, 0.0f);
     }
     return;
   }
@@ -2527,17 +2815,24 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_cut_kernel(Params P) {
     }
     __syncthreads();
     cut = sh.cutmin;
-    // Kept: the entries above the cut bin, and the candidates at or above K*.
+    // Kept: the entries above the cut bin, and the candidates at or above K*;
+    // their mass is the row's kept total S_kept.
     unsigned c = 0;
-    for (unsigned i = tid; i < n; i += kTpThreads) c += sh.u.rs.ckey[i] >= cut ? 1u : 0u;
+    double kmass = 0.0;
+    for (unsigned i = tid; i < n; i += kTpThreads)
+      if (sh.u.rs.ckey[i] >= cut) {
+        ++c;
+        kmass += sh.u.rs.cw[i];
+      }
     c = __reduce_add_sync(0xffffffffu, c);
     if (lane == 0) sh.wcnt[warp] = c;
-    __syncthreads();
+    kmass = tp_block_sum(sh, kmass);
     if (tid == 0) {
       unsigned tot = count_above;
       for (int w2 = 0; w2 < kTpThreads / 32; ++w2) tot += sh.wcnt[w2];
       P.topp_cut[row] = cut;
       if (P.topp_kept) P.topp_kept[row] = (int)tot;
+      P.row_stat[row] = make_float2(m, (float)(above + kmass));
     }
     return;
   }
@@ -2559,73 +2854,800 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_cut_kernel(Params P) {
     if (tp_block_sum(sh, ff_to_double(part)) >= target) x = y;
   }
   cut = x;
-  // The kept count, for the caller (a pass over the row on this path).
+  // The kept count and mass, for the caller (a pass over the row on this path).
   unsigned kept = 0;
+  ff kpart = {0.0f, 0.0f};
   for_tiles([&](const uint32_t (&w)[W], int nv, unsigned e0) {
-    for (int j = 0; j < nv; ++j) kept += key_of(tp_pick<DT>(w, j), e0 + j) >= cut ? 1u : 0u;
+    for (int j = 0; j < nv; ++j) {
+      const uint32_t b = tp_pick<DT>(w, j);
+      if (key_of(b, e0 + j) >= cut) {
+        ++kept;
+        const ff xx = scaled_diff(tp_float<DT>(b), m, P.ih, P.il, unit_t);
+        ff_accumulate(kpart, exp_ff(xx.hi, xx.lo, sh.tab));
+      }
+    }
   });
   kept = __reduce_add_sync(0xffffffffu, kept);
   if (lane == 0) sh.wcnt[warp] = kept;
-  __syncthreads();
+  const double kmass = tp_block_sum(sh, ff_to_double(kpart));
   if (tid == 0) {
     unsigned tot = 0;
     for (int w2 = 0; w2 < kTpThreads / 32; ++w2) tot += sh.wcnt[w2];
     P.topp_cut[row] = cut;
     if (P.topp_kept) P.topp_kept[row] = (int)tot;
+    P.row_stat[row] = make_float2(m, (float)kmass);
   }
 }
 
-// The masked copies: every element of the 2K+1 rows whose key is below its
-// row's cut becomes -inf; the others are copied. blockIdx.y strides over the
-// rows, blockIdx.x over chunks of 8 elements per thread; VEC moves the 8 as
-// 16-byte words (the rows and the copies 16-byte aligned).
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(256) topp_mask_kernel(Params P, void* masked_target,
-                                                        void* masked_draft) {
-  using E = typename std::conditional<DT == 0, unsigned short, uint32_t>::type;
-  constexpr int W = SelWords<DT>::n;
-  const long long rows = (long long)P.B * P.rows_per_seq;
-  const int V = P.V, ib = P.key_ibits;
-  const E kNegInf = DT == 0 ? (E)0xff80u : (E)0xff800000u;
-  const unsigned e0 = (blockIdx.x * 256 + threadIdx.x) * 8;
-  if (e0 >= (unsigned)V) return;
-  for (long long row = blockIdx.y; row < rows; row += gridDim.y) {
-    const long long b = row / P.rows_per_seq;
-    const int r = (int)(row % P.rows_per_seq);
-    const unsigned char* src = row_base(P, b, r);
-    E* dst = r <= P.K
-                 ? reinterpret_cast<E*>(masked_target) + ((size_t)b * (P.K + 1) + r) * (size_t)V
-                 : reinterpret_cast<E*>(masked_draft) + ((size_t)b * P.K + (r - P.K - 1)) * (size_t)V;
-    const unsigned long long cut = __ldg(P.topp_cut + row);
-    uint32_t w[W];
-    const int nv = load_sel_tile<DT, VEC>(src, (long long)e0, V, w);
+// ---------------------------------------------------------------- nucleus: the cut on a thread-block cluster
+//
+// The cut of topp_cut_kernel with the row held on chip. A cluster of NC CTAs
+// takes one row; each CTA copies its slice of the row (at most one slice
+// budget of bytes) into its shared memory once, so the row crosses HBM once
+// and every later pass reads shared memory. After each pass the CTAs publish
+// per-bin totals in their own shared memory; after a cluster barrier every
+// CTA sums all CTAs' totals in rank order, so all of them take the same
+// decision. Passes:
+//   0. the row maximum m (a NaN or +inf entry fails the row);
+//   1. float-float masses of 16 bins of D = fl(fl(m - l) log2(e) / (4T)),
+//      bin floor(D), the last one open; S, the row's total, is their sum;
+//   2.. the cut bin split 16 ways (bin floor(D 16^(L-1)), an exact scaling),
+//      over the entries whose value lies in its window, counting them;
+//   once the bin just split held at most kTcCap entries (so its cut sub-bin
+//   does too), a last pass gathers the cut bin's keys and weights into the
+//   first CTA and counts the entries above it; the first CTA then finds the
+//   cut key bit by bit below the candidates' common key prefix, with one
+//   block-wide float-float sum per bit and no atomics. A cut bin that never
+//   gets that small (heavy ties) is resolved the same way over the row.
+// D is a monotone function of the logit, so bins above the cut bin hold only
+// larger keys. Weights are the draw's: exp(l/T) 2^-q0 from the fast
+// exponential (~5e-11) for rows whose maximum has |m/T| below ~1386, else
+// exp((l - m)/T) (exp_ff, ~1e-12). The kernel leaves the row's statistics
+// (m, S_kept) for the verification, which reads the unfiltered rows and
+// applies each row's kept set as it loads them.
+
+constexpr int kTcThreads = 256;
+constexpr int kTcWarps = kTcThreads / 32;
+constexpr int kTcCap = 1024;
+constexpr int kTcMaxLevels = 7;
+constexpr int kTcMaxCluster = 16;
+
+struct TcShared {
+  union {
+    float2 bin[kTpBins][kTcThreads];  // per-thread float-float bin masses, each biased by 1
+    struct {  // the first CTA's gathered candidates: keys and float-float weights
+      unsigned long long ckey[kTcCap];
+      float2 cw[kTcCap];
+    } rs;
+  } u;
+  float2 tab1k[1024];
+  float2 tab[256];
+  // Each CTA's totals of a pass, written by every CTA of the cluster into
+  // every CTA's inbox (by pass parity): 16 bin masses, then a count.
+  float2 inbox[2][kTcMaxCluster][kTpBins + 1];
+  float inmax[kTcMaxCluster];
+  float wmax[kTcWarps];
+  ff wff[kTcWarps];
+  ff wff2[2][kTcWarps];
+  unsigned long long wkey[2][kTcWarps];
+  unsigned wcnt[kTcWarps], wcnt2[kTcWarps];
+  double binmass[kTpBins];
+  unsigned members;  // entries of the bin just split, over the cluster
+  float queue[kTcWarps][64];  // per warp: window entries waiting to be weighed
+  unsigned off_cand, tot_cand, tot_above;
+  // the decision after each pass (the same in every CTA of the cluster)
+  double above, target;
+  long long parent;
+  int open, state;
+  float m;
+  unsigned n_cand, n_above;  // the first CTA's counters of the gather pass
+  unsigned long long bar;
+};
+
+constexpr size_t kTcSliceOffset = (sizeof(TcShared) + 127) / 128 * 128;
+
+template <int DT>
+SV_DEVINL void tc_unpack(const uint4& q, float (&x)[DT == 0 ? 8 : 4]) {
+  if constexpr (DT == 0) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t bits = elem_bits<DT>(w, j);
-      const unsigned long long key =
-          ((unsigned long long)value_key<DT>(bits) << ib) | (unsigned long long)(V - 1 - (int)(e0 + j));
-      const uint32_t out = key >= cut ? bits : (uint32_t)kNegInf;
-      if constexpr (DT == 0)
-        w[j >> 1] = (w[j >> 1] & ((j & 1) ? 0x0000ffffu : 0xffff0000u)) | (out << ((j & 1) * 16));
-      else
-        w[j] = out;
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = bf16_lo(w[k]);
+      x[2 * k + 1] = bf16_hi(w[k]);
     }
-    if (VEC && nv == 8) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + e0);
-      if constexpr (DT == 0) {
-        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      } else {
-        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else {
+    x[0] = __uint_as_float(q.x);
+    x[1] = __uint_as_float(q.y);
+    x[2] = __uint_as_float(q.z);
+    x[3] = __uint_as_float(q.w);
+  }
+}
+
+// Float-float add of a weight into this thread's bin b (biased accumulator:
+// every weight is at most 1).
+SV_DEVINL void tc_bin_add(TcShared& sh, int b, float hi, float lo) {
+  float2 a = sh.u.bin[b][threadIdx.x];
+  const float s = __fadd_rn(a.x, hi);
+  const float e = __fsub_rn(hi, __fsub_rn(s, a.x));
+  a.y = __fadd_rn(a.y, __fadd_rn(e, lo));
+  a.x = s;
+  sh.u.bin[b][threadIdx.x] = a;
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kTcThreads, 2) topp_cluster_kernel(Params P, int nc,
+                                                                      int slice_elems) {
+  extern __shared__ __align__(128) unsigned char tc_smem[];
+  TcShared& sh = *reinterpret_cast<TcShared*>(tc_smem);
+  constexpr int kEs = DT == 0 ? 2 : 4;
+  constexpr int kEpv = 16 / kEs;  // elements per 16-byte vector
+  uint4* sl4 = reinterpret_cast<uint4*>(tc_smem + kTcSliceOffset);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned rank = cluster_ctarank();
+  const long long row = blockIdx.x / nc;
+  const unsigned char* rb = row_base(P, row / P.rows_per_seq, (int)(row % P.rows_per_seq));
+  const int V = P.V, ib = P.key_ibits;
+  const long long e_begin = (long long)rank * slice_elems;
+  const int n = (int)max(0LL, min((long long)slice_elems, (long long)V - e_begin));
+  const int nvec = (n + kEpv - 1) / kEpv;
+  const unsigned bar = smem_u32(&sh.bar);
+  // Every CTA of the cluster must have started before another writes into
+  // its shared memory: the arrival here, the wait before the first write.
+  cluster_arrive_relaxed();
+
+  // ---- the slice into shared memory
+  if constexpr (VEC) {
+    if (tid == 0) {
+      mbar_init(bar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0) {
+      // n * kEs is a multiple of 16 (the row and V * kEs are 16-byte aligned,
+      // and slices start at multiples of 8 elements).
+      const unsigned bytes = (unsigned)n * kEs;
+      mbar_arrive_expect_tx(bar, bytes);
+      for (unsigned off = 0; off < bytes; off += 16384u)
+        bulk_copy_g2s(smem_u32(sl4) + off, rb + e_begin * kEs + off, min(16384u, bytes - off), bar);
+    }
+  } else {
+    using E = typename std::conditional<DT == 0, unsigned short, uint32_t>::type;
+    E* se = reinterpret_cast<E*>(sl4);
+    const E kNegInf = DT == 0 ? (E)0xff80u : (E)0xff800000u;
+    const E* src = reinterpret_cast<const E*>(rb) + e_begin;
+    for (int i = tid; i < nvec * kEpv; i += kTcThreads) se[i] = i < n ? src[i] : kNegInf;
+  }
+  sh.tab[tid] = kSvExp2Table[tid];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sh.tab1k[tid + i * kTcThreads] = kSvExp2Table1024[tid + i * kTcThreads];
+  bool copied = true;
+  if constexpr (VEC) {
+    if (!mbar_test_parity(bar, 0)) {
+      const uint64_t t0 = global_ns();
+      for (unsigned i = 1;; ++i) {
+        if (mbar_test_parity(bar, 0)) break;
+        if ((i & 255) == 0 && global_ns() - t0 > kWaitLimitNs) {
+          copied = false;
+          break;
+        }
       }
-    } else {
-      for (int j = 0; j < nv; ++j) dst[e0 + j] = (E)elem_bits<DT>(w, j);
     }
+  }
+  __syncthreads();
+
+  // ---- pass 0: the maximum (NaN-propagating; +inf is caught as well)
+  float mx = neg_inf();
+  if constexpr (DT == 0) {
+    uint32_t mm = 0xff80ff80u;
+    for (int v = tid; v < nvec; v += kTcThreads) {
+      const uint4 q = sl4[v];
+      mm = bf16x2_max_nan(mm, bf16x2_max_nan(bf16x2_max_nan(q.x, q.y), bf16x2_max_nan(q.z, q.w)));
+    }
+    mx = fmax_nan(bf16_lo(mm), bf16_hi(mm));
+  } else {
+    for (int v = tid; v < nvec; v += kTcThreads) {
+      const uint4 q = sl4[v];
+      mx = fmax_nan(mx, fmax_nan(fmax_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
+                                 fmax_nan(__uint_as_float(q.z), __uint_as_float(q.w))));
+    }
+  }
+  if (!copied) mx = __int_as_float(0x7fc00000);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) sh.wmax[warp] = mx;
+  __syncthreads();
+  cluster_wait();
+  if (tid < nc) {  // this CTA's maximum into every CTA's inbox
+    float c = sh.wmax[0];
+    for (int w2 = 1; w2 < kTcWarps; ++w2) c = fmax_nan(c, sh.wmax[w2]);
+    dsmem_st_f32(dsmem_map(smem_u32(&sh.inmax[rank]), tid), c);
+  }
+  cluster_sync();
+  if (warp == 0) {
+    float c = lane < nc ? sh.inmax[lane] : neg_inf();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c = fmax_nan(c, __shfl_xor_sync(0xffffffffu, c, o));
+    if (lane == 0) sh.m = c;
+  }
+  __syncthreads();
+  const float m = sh.m;
+  if (!copied && tid == 0) atomicOr(P.status, kDevTimeout);
+  if (isnan(m) || m == CUDART_INF_F || m == neg_inf()) {
+    // A failing row: the verification reports it from the statistics.
+    if (rank == 0 && tid == 0) {
+      P.topp_cut[row] = 0;
+      if (P.topp_kept) P.topp_kept[row] = V;
+      P.row_stat[row] = m == neg_inf() ? make_float2(neg_inf(), 0.0f)
+                                       : make_float2(0.0f, __int_as_float(0x7fc00000));
+    }
+    return;
+  }
+
+  // ---- row constants: D's scale, the weights' form
+  const float c2q = P.c2 * 0.25f;
+  const bool unit_t = P.unit_t != 0;
+  const float mc = m * P.c2;
+  const bool fast = fabsf(mc) <= 2000.0f;
+  const int q0 = row_q0(m, P.c2);
+  const int qb = 127 - q0;
+  const float lmin = -2048.0f * __fdividef(1.0f, P.ih);
+  const DrawConst dc{P.d_inv, P.d_ch, P.d_cli, P.ih};
+  auto weight = [&](float l) -> ff {
+    if (fast) return exp_draw(fmaxf(l, lmin), qb, dc, sh.tab1k);
+    const ff x = scaled_diff(l, m, P.ih, P.il, unit_t);
+    return exp_ff(x.hi, x.lo, sh.tab);
+  };
+  auto dval = [&](float l) { return __fmul_rn(__fsub_rn(m, l), c2q); };
+  // The value window of bin `parent` at scale sc (open: everything below too),
+  // widened by far more than D's rounding.
+  // (fp32: its rounding, ~1e-7 of |m| + D, is far inside the slack.)
+  auto window = [&](float sc, long long parent, bool open, float& lo, float& hi) {
+    const float w = 1.0f / (sc * c2q);
+    const float s0 = (float)parent * w, s1 = (float)(parent + 1) * w;
+    const float slack = (fabsf(m) + s1) * 1e-5f + 1e-30f;
+    lo = open ? neg_inf() : m - s1 - slack;
+    hi = m - s0 + slack;
+  };
+  // floor(D sc) (D >= 0; the product is exact; an infinite or huge D
+  // saturates). Indices stay below 2^28 for D < 16 and scales up to 16^6.
+  auto bin_index = [&](float d, float sc) -> long long {
+    return (long long)__float2int_rz(__fmul_rn(d, sc));
+  };
+
+  // Per-pass reduction: this CTA's 16 bin totals (float-float, each thread's
+  // bias removed) and the entries it split (`members`, one count per
+  // thread), published at parity `par`; after the cluster barrier, warp 0
+  // sums the CTAs' totals in rank order into binmass and members.
+  auto reduce_and_share = [&](int par, unsigned members) {
+    members = __reduce_add_sync(0xffffffffu, members);
+    if (lane == 0) sh.wcnt[warp] = members;
+    __syncthreads();
+    {
+      // Thread (b, part) sums bin b over 16 threads' columns; after the
+      // butterfly all 16 hold the total, and thread (b, r) writes it into
+      // CTA r's inbox.
+      const int b = tid >> 4, part = tid & 15;
+      ff acc{0.0f, 0.0f};
+      for (int t = part; t < kTcThreads; t += 16) {
+        const float2 a = sh.u.bin[b][t];
+        acc = ff_add(acc, fast_two_sum(__fsub_rn(a.x, 1.0f), a.y));
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) acc = ff_add(acc, ff_shfl_xor(acc, o));
+      if (part < nc)
+        dsmem_st_f32x2(dsmem_map(smem_u32(&sh.inbox[par][rank][b]), part), acc.hi, acc.lo);
+      if (tid < nc) {
+        unsigned c = 0;
+        for (int w2 = 0; w2 < kTcWarps; ++w2) c += sh.wcnt[w2];
+        dsmem_st_f32x2(dsmem_map(smem_u32(&sh.inbox[par][rank][kTpBins]), tid),
+                       __uint_as_float(c), 0.0f);
+      }
+    }
+    cluster_sync();
+    if (warp == 0) {
+      ff tot{0.0f, 0.0f};
+      unsigned c = 0;
+      if (lane < kTpBins) {
+        for (int r = 0; r < nc; ++r) {
+          const float2 v = sh.inbox[par][r][lane];
+          tot = ff_add(tot, ff{v.x, v.y});
+        }
+        sh.binmass[lane] = ff_to_double(tot);
+      } else if (lane == kTpBins) {
+        for (int r = 0; r < nc; ++r) c += __float_as_uint(sh.inbox[par][r][kTpBins].x);
+        sh.members = c;
+      }
+    }
+    __syncthreads();
+  };
+  // (Each thread writes only its own column; the last pass's reads of
+  // other columns ended before the barriers that closed it.)
+  auto zero_bins = [&]() {
+#pragma unroll
+    for (int b = 0; b < kTpBins; ++b) sh.u.bin[b][tid] = make_float2(1.0f, 0.0f);
+  };
+  // The bin where the running mass from the top reaches the target; if
+  // rounding leaves the target just out of reach, the last bin with mass.
+  // Warp 0 decides (a scan over the 16 bins, lane b holding bin b); the
+  // caller synchronises.
+  auto decide = [&](int level) {
+    if (warp != 0) return;
+    const double M = lane < kTpBins ? sh.binmass[lane] : 0.0;
+    if (level == 1) {
+      double S = M;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+      if (lane == 0) {
+        sh.target = (double)P.top_p * S;
+        sh.above = 0.0;
+        sh.parent = 0;
+        sh.open = 0;
+      }
+      __syncwarp();
+    }
+    const double above0 = sh.above, target = sh.target;
+    double Pb = M;  // inclusive prefix over the bins
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, Pb, o);
+      if (lane >= o) Pb += y;
+    }
+    const unsigned nonempty = __ballot_sync(0xffffffffu, lane < kTpBins && M > 0.0);
+    const unsigned reach = __ballot_sync(0xffffffffu, lane < kTpBins && M > 0.0 && above0 + Pb >= target);
+    const int bstar = reach ? __ffs(reach) - 1 : (nonempty ? 31 - __clz(nonempty) : 0);
+    const double before = __shfl_sync(0xffffffffu, Pb - M, bstar);  // mass of the bins above bstar
+    if (lane == 0) {
+      sh.above = above0 + before;
+      const long long parent = (level > 1 ? 16 * sh.parent : 0) + bstar;
+      sh.open = (bstar == kTpBins - 1 && (level == 1 || sh.open)) ? 1 : 0;
+      sh.parent = parent;
+      // state: 0 split the new cut bin, 1 gather it (it holds at most as many
+      // entries as the bin just split), 2 heavy ties
+      if (sh.members <= (unsigned)kTcCap)
+        sh.state = 1;
+      else
+        sh.state = level >= kTcMaxLevels ? 2 : 0;
+    }
+  };
+
+  // ---- pass 1: every entry, float-float masses of the 16 level-1 bins
+  zero_bins();
+  {
+    const float2 mm2 = f2(m), cq2 = f2(c2q);
+    const int2 qb2 = make_int2(qb, qb);
+    const float2 nm2 = f2(-m);
+    for (int v = tid; v < nvec; v += kTcThreads) {
+      float x[kEpv];
+      tc_unpack<DT>(sl4[v], x);
+#pragma unroll
+      for (int j = 0; j < kEpv; j += 2) {
+        const float2 l = make_float2(x[j], x[j + 1]);
+        ff2 w;
+        if (fast) {
+          w = exp_draw2(make_float2(fmaxf(l.x, lmin), fmaxf(l.y, lmin)), qb2, dc, sh.tab1k);
+        } else {
+          const ff2 xs = scaled_diff2(l, nm2, P.ih, P.il, unit_t);
+          w = exp_ff2(xs.hi, xs.lo, sh.tab);
+        }
+        const float2 D = f2_mul(f2_sub(mm2, l), cq2);
+        const int b0 = min(kTpBins - 1, __float2int_rz(D.x));
+        const int b1 = min(kTpBins - 1, __float2int_rz(D.y));
+        tc_bin_add(sh, b0, w.hi.x, w.lo.x);
+        tc_bin_add(sh, b1, w.hi.y, w.lo.y);
+      }
+    }
+  }
+  reduce_and_share(1, tid == 0 ? (unsigned)n : 0u);  // level 1 splits the whole slice
+  decide(1);
+  __syncthreads();
+
+  // ---- passes 2..: the cut bin at 16 times the resolution
+  int level = 1;
+  while (sh.state == 0) {
+    ++level;
+    const float psc = ldexpf(1.0f, 4 * (level - 2)), sc = ldexpf(1.0f, 4 * (level - 1));
+    const long long parent = sh.parent;
+    const bool open = sh.open != 0;
+    float lo, hi;
+    window(psc, parent, open, lo, hi);
+    zero_bins();
+    unsigned members = 0;
+    // The entries inside the window go through a per-warp queue and are
+    // weighed 32 at a time, one per lane, so that the exponentials do not
+    // diverge with the lanes' candidate counts.
+    float* wq = sh.queue[warp];
+    int qn = 0;  // queued entries (the same in every lane)
+    auto weigh = [&](int cnt) {
+      if (lane < cnt) {
+        const float l = wq[lane];
+        const float d = dval(l);
+        const long long ip = bin_index(d, psc);
+        if (open ? ip >= parent : ip == parent) {
+          const long long r = bin_index(d, sc) - 16 * parent;
+          const int b = (int)(r < kTpBins - 1 ? r : kTpBins - 1);
+          const ff w = weight(l);
+          tc_bin_add(sh, b, w.hi, w.lo);
+          ++members;
+        }
+      }
+    };
+    for (int v0 = 0; v0 < nvec; v0 += kTcThreads) {  // the same trip count in every lane
+      const int v = v0 + tid;
+      float x[kEpv];
+      unsigned cand = 0;
+      if (v < nvec) {
+        tc_unpack<DT>(sl4[v], x);
+#pragma unroll
+        for (int j = 0; j < kEpv; ++j)
+          if (x[j] >= lo && x[j] <= hi && v * kEpv + j < n) cand |= 1u << j;
+      }
+      while (__any_sync(0xffffffffu, cand != 0)) {
+        const bool has = cand != 0;
+        float l = 0.0f;
+        if (has) {
+          const int j = __ffs(cand) - 1;
+          cand &= cand - 1;
+          l = x[0];
+#pragma unroll
+          for (int k = 1; k < kEpv; ++k) l = j == k ? x[k] : l;
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, has);
+        if (has) wq[qn + __popc(bal & ((1u << lane) - 1u))] = l;
+        qn += __popc(bal);
+        if (qn >= 32) {  // at most 63 queued
+          __syncwarp();
+          weigh(32);
+          __syncwarp();
+          if (lane < qn - 32) wq[lane] = wq[32 + lane];
+          __syncwarp();
+          qn -= 32;
+        }
+      }
+    }
+    __syncwarp();
+    weigh(qn);
+    reduce_and_share(level & 1, members);
+    decide(level);
+    __syncthreads();
+  }
+
+  const float sc = ldexpf(1.0f, 4 * (level - 1));
+  const long long parent = sh.parent;
+  const bool open = sh.open != 0;
+  float lo, hi;
+  window(sc, parent, open, lo, hi);
+  // Class of an entry against the cut bin: 1 above it, 0 in it, -1 below.
+  auto classify = [&](float l, float& d) -> int {
+    if (l > hi) return 1;
+    if (l < lo) return -1;
+    d = dval(l);
+    const long long i = bin_index(d, sc);
+    if (i < parent) return 1;
+    return (open || i == parent) ? 0 : -1;
+  };
+
+  if (sh.state == 1) {
+    // ---- the gather pass: this CTA's entries of the cut bin (keys and
+    // weights) into its own shared memory, the entries above the bin counted;
+    // then each CTA copies its entries into the first CTA after those of the
+    // lower ranks.
+    if (tid == 0) {
+      sh.n_cand = 0;
+      sh.n_above = 0;
+    }
+    __syncthreads();  // the bins (whose memory the candidates reuse) are no longer read
+    unsigned n_ab = 0;
+    for (int v0 = 0; v0 < nvec; v0 += kTcThreads) {  // the same trip count in every lane
+      const int v = v0 + tid;
+      float x[kEpv];
+      if (v < nvec) {
+        tc_unpack<DT>(sl4[v], x);
+      } else {
+#pragma unroll
+        for (int k = 0; k < kEpv; ++k) x[k] = neg_inf();
+      }
+#pragma unroll
+      for (int j = 0; j < kEpv; ++j) {
+        const int e = v * kEpv + j;
+        float d;
+        const int cls = (v < nvec && e < n) ? classify(x[j], d) : -1;
+        n_ab += cls > 0 ? 1u : 0u;
+        const unsigned bal = __ballot_sync(0xffffffffu, cls == 0);
+        if (bal) {
+          const int first = __ffs(bal) - 1;
+          unsigned base = 0;
+          if (lane == first) base = atomicAdd(&sh.n_cand, (unsigned)__popc(bal));
+          base = __shfl_sync(0xffffffffu, base, first);
+          const unsigned s = base + (unsigned)__popc(bal & ((1u << lane) - 1u));
+          if (cls == 0 && s < (unsigned)kTcCap) {
+            const uint32_t bits = DT == 0 ? (__float_as_uint(x[j]) >> 16) : __float_as_uint(x[j]);
+            sh.u.rs.ckey[s] = ((unsigned long long)value_key<DT>(bits) << ib) |
+                              (unsigned long long)(V - 1 - (int)(e_begin + e));
+            const ff w = ff_normalize(weight(x[j]));
+            sh.u.rs.cw[s] = make_float2(w.hi, w.lo);
+          }
+        }
+      }
+    }
+    n_ab = __reduce_add_sync(0xffffffffu, n_ab);
+    if (lane == 0 && n_ab) atomicAdd(&sh.n_above, n_ab);
+    __syncthreads();
+    // (The other parity than the last level's, whose inboxes may still be
+    // read.)
+    const int gpar = (level + 1) & 1;
+    if (tid < nc)  // this CTA's counts into every CTA's inbox
+      dsmem_st_f32x2(dsmem_map(smem_u32(&sh.inbox[gpar][rank][0]), tid),
+                     __uint_as_float(sh.n_cand), __uint_as_float(sh.n_above));
+    cluster_sync();  // every CTA's counts and entries are final
+    if (warp == 0) {
+      unsigned off = 0, tot = 0, tab = 0;
+      if (lane < nc) {
+        const float2 c = sh.inbox[gpar][lane][0];
+        off = lane < (int)rank ? __float_as_uint(c.x) : 0u;
+        tot = __float_as_uint(c.x);
+        tab = __float_as_uint(c.y);
+      }
+      off = __reduce_add_sync(0xffffffffu, off);
+      tot = __reduce_add_sync(0xffffffffu, tot);
+      tab = __reduce_add_sync(0xffffffffu, tab);
+      if (lane == 0) {
+        sh.off_cand = off;
+        sh.tot_cand = tot;
+        sh.tot_above = tab;
+      }
+    }
+    __syncthreads();
+    if (rank != 0) {
+      const unsigned off = sh.off_cand, mine = min(sh.n_cand, (unsigned)kTcCap);
+      const unsigned ckey_a = dsmem_map(smem_u32(&sh.u.rs.ckey[0]), 0);
+      const unsigned cw_a = dsmem_map(smem_u32(&sh.u.rs.cw[0]), 0);
+      for (unsigned i = tid; i < mine && off + i < (unsigned)kTcCap; i += kTcThreads) {
+        dsmem_st_u64(ckey_a + 8u * (off + i), sh.u.rs.ckey[i]);
+        const float2 w = sh.u.rs.cw[i];
+        dsmem_st_f32x2(cw_a + 8u * (off + i), w.x, w.y);
+      }
+    }
+    cluster_sync();  // every entry is in the first CTA
+    if (rank != 0) return;
+
+    // ---- the first CTA: the cut key K*, the largest candidate key with
+    // above + mass(keys >= K*) >= target, found bit by bit below the
+    // candidates' common prefix with one block reduction (float-float) per
+    // bit; no atomics.
+    const unsigned ncand = min(sh.tot_cand, (unsigned)kTcCap);
+    auto to_ff = [](double d) -> ff {
+      const float h = (float)d;
+      return {h, (float)(d - (double)h)};
+    };
+    const ff above_ff = to_ff(sh.above), target_ff = to_ff(sh.target);
+    auto reaches = [&](ff part) {  // above + part >= target
+      const ff a = ff_add(above_ff, part);
+      return a.hi > target_ff.hi || (a.hi == target_ff.hi && a.lo >= target_ff.lo);
+    };
+    // Block sums alternate between two slot arrays, so one barrier per sum
+    // suffices: a slot is rewritten only after every thread has passed the
+    // barrier of the sum in between.
+    int fpar = 0;
+    auto block_ff = [&](ff v) -> ff {
+      const int par = fpar;
+      fpar ^= 1;
+      v = ff_warp_sum(v);
+      if (lane == 0) sh.wff2[par][warp] = v;
+      __syncthreads();
+      ff t{0.0f, 0.0f};
+#pragma unroll
+      for (int w2 = 0; w2 < kTcWarps; ++w2) t = ff_add(t, sh.wff2[par][w2]);
+      return t;
+    };
+    // max (mode 0) or min (mode 1) of the keys over the block
+    auto block_key = [&](unsigned long long k, int mode, int par) -> unsigned long long {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, k, o);
+        k = mode == 0 ? (y > k ? y : k) : (y < k ? y : k);
+      }
+      if (lane == 0) sh.wkey[par][warp] = k;
+      __syncthreads();
+      unsigned long long r = sh.wkey[par][0];
+#pragma unroll
+      for (int w2 = 1; w2 < kTcWarps; ++w2) {
+        const unsigned long long y = sh.wkey[par][w2];
+        r = mode == 0 ? (y > r ? y : r) : (y < r ? y : r);
+      }
+      return r;
+    };
+    auto write_out = [&](unsigned long long cut, unsigned kept_c, ff kept_mass) {
+      const double S_kept = sh.above + ff_to_double(kept_mass);
+      P.topp_cut[row] = cut;
+      if (P.topp_kept) P.topp_kept[row] = (int)(sh.tot_above + kept_c);
+      const double f = fast ? exp((double)q0 * 0.69314718055994530942 - (double)m * P.inv_t) : 1.0;
+      P.row_stat[row] = make_float2(m, (float)(S_kept * f));
+    };
+    if (ncand <= (unsigned)kTcThreads) {
+      // Few candidates (the usual case): each thread takes one, with the
+      // mass and count of the candidates at or above its key; K* is the
+      // largest key whose mass reaches the target.
+      const bool has = tid < ncand;
+      unsigned long long ki = 0;
+      ff mi{0.0f, 0.0f};
+      unsigned ci = 0;
+      float wi = 0.0f;
+      if (has) {
+        ki = sh.u.rs.ckey[tid];
+        wi = sh.u.rs.cw[tid].x;
+        for (unsigned j = 0; j < ncand; ++j)
+          if (sh.u.rs.ckey[j] >= ki) {
+            const float2 w = sh.u.rs.cw[j];
+            mi = ff_add(mi, ff{w.x, w.y});
+            ++ci;
+          }
+      }
+      const bool q = has && reaches(mi);
+      unsigned long long cut;
+      if (__syncthreads_or(q)) {
+        cut = block_key(q ? ki : 0ull, 0, 0);
+      } else {
+        // Rounding leaves the target just out of reach: every entry with
+        // mass is kept, so the cut is the smallest candidate key with mass.
+        cut = block_key((has && wi > 0.0f) ? ki : ~0ull, 1, 0);
+        if (cut == ~0ull) cut = block_key(has ? ki : 0ull, 0, 1);
+      }
+      if (has && ki == cut) write_out(cut, ci, mi);
+      return;
+    }
+    unsigned long long kmax = 0, kmin = ~0ull, kpos = ~0ull;
+    ff total{0.0f, 0.0f};
+    for (unsigned i = tid; i < ncand; i += kTcThreads) {
+      const unsigned long long k = sh.u.rs.ckey[i];
+      const float2 w = sh.u.rs.cw[i];
+      kmax = k > kmax ? k : kmax;
+      kmin = k < kmin ? k : kmin;
+      if (w.x > 0.0f) kpos = k < kpos ? k : kpos;
+      total = ff_add(total, ff{w.x, w.y});
+    }
+    kmax = block_key(kmax, 0, 0);
+    kmin = block_key(kmin, 1, 1);
+    kpos = block_key(kpos, 1, 0);
+    total = block_ff(total);
+    unsigned long long cut;
+    if (!reaches(total)) {
+      // Rounding leaves the target just out of reach: every entry with mass
+      // is kept, so the cut is the smallest candidate key with mass.
+      cut = kpos != ~0ull ? kpos : kmax;
+    } else {
+      const unsigned long long diff = kmin ^ kmax;
+      const int hb = diff ? 63 - __clzll((long long)diff) : -1;
+      unsigned long long x = hb < 0 ? kmax : (hb == 63 ? 0ull : (kmax >> (hb + 1)) << (hb + 1));
+      for (int bit = hb; bit >= 0; --bit) {
+        const unsigned long long y = x | (1ull << bit);
+        ff part{0.0f, 0.0f};
+        for (unsigned i = tid; i < ncand; i += kTcThreads)
+          if (sh.u.rs.ckey[i] >= y) {
+            const float2 w = sh.u.rs.cw[i];
+            part = ff_add(part, ff{w.x, w.y});
+          }
+        part = block_ff(part);
+        if (reaches(part)) x = y;
+      }
+      cut = x;
+    }
+    // Kept: the entries above the cut bin, and the candidates at or above the
+    // cut; their mass is the row's kept total S_kept.
+    unsigned c = 0;
+    ff kmass{0.0f, 0.0f};
+    for (unsigned i = tid; i < ncand; i += kTcThreads)
+      if (sh.u.rs.ckey[i] >= cut) {
+        ++c;
+        const float2 w = sh.u.rs.cw[i];
+        kmass = ff_add(kmass, ff{w.x, w.y});
+      }
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) sh.wcnt[warp] = c;
+    const ff km = block_ff(kmass);  // its barrier also publishes wcnt
+    if (tid == 0) {
+      unsigned tot = 0;
+      for (int w2 = 0; w2 < kTcWarps; ++w2) tot += sh.wcnt[w2];
+      write_out(cut, tot, km);
+    }
+    return;
+  }
+
+  // ---- heavy ties: the cut key bit by bit, with the exact mass of the cut
+  // bin's keys at or above the trial key (the bins above it are all kept)
+  const int bits = (DT == 0 ? 16 : 32) + ib;
+  unsigned long long x = 0;
+  auto mass_at_or_above = [&](unsigned long long y, int par, double& mass, unsigned& n_ge,
+                              unsigned& n_ab) {
+    ff part{0.0f, 0.0f};
+    unsigned cge = 0, cab = 0;
+    for (int v = tid; v < nvec; v += kTcThreads) {
+      float xv[kEpv];
+      tc_unpack<DT>(sl4[v], xv);
+#pragma unroll
+      for (int j = 0; j < kEpv; ++j) {
+        const int e = v * kEpv + j;
+        if (e >= n) continue;
+        float d;
+        const int cls = classify(xv[j], d);
+        if (cls > 0) {
+          ++cab;
+          continue;
+        }
+        if (cls < 0) continue;
+        const uint32_t bb = DT == 0 ? (__float_as_uint(xv[j]) >> 16) : __float_as_uint(xv[j]);
+        const unsigned long long key = ((unsigned long long)value_key<DT>(bb) << ib) |
+                                       (unsigned long long)(V - 1 - (int)(e_begin + e));
+        if (key >= y) {
+          ff_accumulate(part, weight(xv[j]));
+          ++cge;
+        }
+      }
+    }
+    part = ff_warp_sum(part);
+    cge = __reduce_add_sync(0xffffffffu, cge);
+    cab = __reduce_add_sync(0xffffffffu, cab);
+    if (lane == 0) {
+      sh.wff[warp] = part;
+      sh.wcnt[warp] = cge;
+      sh.wcnt2[warp] = cab;
+    }
+    __syncthreads();
+    if (tid < nc) {  // this CTA's totals into every CTA's inbox
+      ff t{0.0f, 0.0f};
+      unsigned a1 = 0, a2 = 0;
+      for (int w2 = 0; w2 < kTcWarps; ++w2) {
+        t = ff_add(t, sh.wff[w2]);
+        a1 += sh.wcnt[w2];
+        a2 += sh.wcnt2[w2];
+      }
+      dsmem_st_f32x2(dsmem_map(smem_u32(&sh.inbox[par][rank][0]), tid), t.hi, t.lo);
+      dsmem_st_f32x2(dsmem_map(smem_u32(&sh.inbox[par][rank][1]), tid), __uint_as_float(a1),
+                     __uint_as_float(a2));
+    }
+    cluster_sync();
+    if (tid == 0) {
+      ff t{0.0f, 0.0f};
+      unsigned a1 = 0, a2 = 0;
+      for (int r = 0; r < nc; ++r) {
+        const float2 v = sh.inbox[par][r][0], c = sh.inbox[par][r][1];
+        t = ff_add(t, ff{v.x, v.y});
+        a1 += __float_as_uint(c.x);
+        a2 += __float_as_uint(c.y);
+      }
+      sh.binmass[0] = ff_to_double(t);
+      sh.wcnt[0] = a1;
+      sh.wcnt2[0] = a2;
+    }
+    __syncthreads();
+    mass = sh.above + sh.binmass[0];
+    n_ge = sh.wcnt[0];
+    n_ab = sh.wcnt2[0];
+    __syncthreads();
+  };
+  int par = (level + 1) & 1;
+  for (int bit = bits - 1; bit >= 0; --bit) {
+    const unsigned long long y = x | (1ull << bit);
+    double mass;
+    unsigned n_ge, n_ab;
+    mass_at_or_above(y, par, mass, n_ge, n_ab);
+    par ^= 1;
+    if (mass >= sh.target) x = y;
+  }
+  double S_kept;
+  unsigned n_ge, n_ab;
+  mass_at_or_above(x, par, S_kept, n_ge, n_ab);
+  cluster_sync();  // no CTA leaves while another may still read its totals
+  if (rank == 0 && tid == 0) {
+    P.topp_cut[row] = x;
+    if (P.topp_kept) P.topp_kept[row] = (int)(n_ge + n_ab);
+    const double f = fast ? exp((double)q0 * 0.69314718055994530942 - (double)m * P.inv_t) : 1.0;
+    P.row_stat[row] = make_float2(m, (float)(S_kept * f));
   }
 }
 
 // ---------------------------------------------------------------- host-side launch
 
+#if SV_TU_HAS(1)
 namespace {
 struct DeviceInfo {
   bool ready = false;
@@ -2668,6 +3690,23 @@ cudaError_t launch_fused(Params P, cudaStream_t st, const Events& ev) {
   if (e == cudaSuccess && ev.stats_done)
     e = cudaEventRecordWithFlags(ev.stats_done, st, cudaEventRecordExternal);
   return e;
+}
+
+template <int DT, bool VEC, int SUB>
+cudaError_t launch_sampler(const Params& P, cudaStream_t st) {
+  sample_sum_kernel<DT, VEC, SUB><<<(unsigned)((long long)P.B * P.np), kThreads, 0, st>>>(P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)P.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sample_finish_kernel<DT, VEC, SUB>, P);
 }
 
 template <int DT, bool VEC, int SUB>
@@ -2725,7 +3764,14 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
   const bool big = P.sub_elems == 512;
   P.fused = take_fused(P.B, P.rows_per_seq, P.V, P.es, P.sampler != 0) ? 1 : 0;
   P.withhold = g_withhold.load();
-  if (P.fused) {
+  if (P.sampler) {
+    if (P.dtype == 0)
+      e = aligned ? (big ? launch_sampler<0, true, 512>(P, st) : launch_sampler<0, true, 256>(P, st))
+                  : (big ? launch_sampler<0, false, 512>(P, st) : launch_sampler<0, false, 256>(P, st));
+    else
+      e = aligned ? (big ? launch_sampler<1, true, 512>(P, st) : launch_sampler<1, true, 256>(P, st))
+                  : (big ? launch_sampler<1, false, 512>(P, st) : launch_sampler<1, false, 256>(P, st));
+  } else if (P.fused) {
     if (P.dtype == 0)
       e = aligned ? (big ? launch_fused<0, true, 512>(P, st, ev) : launch_fused<0, true, 256>(P, st, ev))
                   : (big ? launch_fused<0, false, 512>(P, st, ev) : launch_fused<0, false, 256>(P, st, ev));
@@ -2744,6 +3790,9 @@ cudaError_t launch_all(Params P, bool aligned, cudaStream_t st, const Events& ev
   return e;
 }
 
+#endif  // SV_TU_HAS(1)
+
+#if SV_TU_HAS(2)
 template <int DT, bool VEC>
 cudaError_t launch_select(const Params& P, unsigned rows, size_t smem, cudaStream_t st) {
   topk_select_kernel<DT, VEC><<<rows, kSelThreads, smem, st>>>(P);
@@ -2770,36 +3819,134 @@ cudaError_t launch_topk(const Params& P, bool aligned, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+#endif  // SV_TU_HAS(2)
+
+#if SV_TU_HAS(3)
+// The nucleus cut's cluster shape for rows of `row_bytes`: CTAs per row and
+// elements per CTA, with a slice budget of 64 KB (two CTAs per SM) or, for
+// longer rows, 96 KB; nc = 0 when even that needs more than kTcMaxCluster.
+static void topp_cluster_shape(long long V, int es, int* nc, int* slice_elems, size_t* smem) {
+  *nc = 0;
+  for (long long budget : {64ll << 10, 96ll << 10}) {
+    const long long c = (V * es + budget - 1) / budget;
+    if (c > kTcMaxCluster) continue;
+    const long long se = ((V + c - 1) / c + 7) / 8 * 8;
+    *nc = (int)c;
+    *slice_elems = (int)se;
+    *smem = kTcSliceOffset + (size_t)((se * es + 127) / 128 * 128);
+    return;
+  }
+}
+
+// Whether clusters of `nc` CTAs with `smem` bytes each can be resident (the
+// answer cached per kernel and shape).
 template <int DT, bool VEC>
-static cudaError_t launch_topp_kernels(const Params& P, void* mt, void* md, cudaStream_t st) {
-  const size_t smem = sizeof(TopPShared);
-  cudaError_t e = cudaFuncSetAttribute(topp_cut_kernel<DT, VEC>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+static bool topp_cluster_ok(int nc, size_t smem, cudaLaunchConfig_t cfg) {
+  static std::mutex mu;
+  static std::map<std::pair<int, size_t>, bool> known;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(nc, smem);
+  const auto it = known.find(key);
+  if (it != known.end()) return it->second;
+  bool ok = cudaFuncSetAttribute(topp_cluster_kernel<DT, VEC>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess;
+  if (ok && nc > 8)
+    ok = cudaFuncSetAttribute(topp_cluster_kernel<DT, VEC>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  int clusters = 0;
+  if (ok) ok = cudaOccupancyMaxActiveClusters(&clusters, topp_cluster_kernel<DT, VEC>, &cfg) ==
+               cudaSuccess && clusters > 0;
+  (void)cudaGetLastError();  // a refused shape leaves no sticky error behind
+  known[key] = ok;
+  return ok;
+}
+
+template <int DT, bool VEC>
+static cudaError_t launch_topp_cut(const Params& P, cudaStream_t st) {
   const long long rows = (long long)P.B * P.rows_per_seq;
-  topp_cut_kernel<DT, VEC><<<(unsigned)rows, kTpThreads, smem, st>>>(P);
-  e = cudaGetLastError();
+  int nc = 0, slice_elems = 0;
+  size_t smem = 0;
+  topp_cluster_shape(P.V, P.es, &nc, &slice_elems, &smem);
+  if (nc > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * nc));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nc;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (topp_cluster_ok<DT, VEC>(nc, smem, cfg)) {
+      cudaError_t e = cudaFuncSetAttribute(topp_cluster_kernel<DT, VEC>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      return cudaLaunchKernelEx(&cfg, topp_cluster_kernel<DT, VEC>, P, nc, slice_elems);
+    }
+  }
+  const size_t tsmem = sizeof(TopPShared);
+  cudaError_t e = cudaFuncSetAttribute(topp_cut_kernel<DT, VEC>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsmem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)(((long long)P.V + 2047) / 2048),
-                  (unsigned)(rows < 65535 ? rows : 65535));
-  topp_mask_kernel<DT, VEC><<<grid, 256, 0, st>>>(P, mt, md);
+  topp_cut_kernel<DT, VEC><<<(unsigned)rows, kTpThreads, tsmem, st>>>(P);
   return cudaGetLastError();
 }
 
-cudaError_t launch_topp(const Params& P, bool aligned, void* masked_target, void* masked_draft,
-                        cudaStream_t st) {
+// The verification after the cut: one warp per sequence scans the kept-set
+// statistics, then the draw (with the kept sets applied on load).
+__global__ void __launch_bounds__(kStatsThreads) scan_kernel(Params P) {
+  __shared__ WarpScan ws[kStatsWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long b = (long long)blockIdx.x * kStatsWarps + warp;
+  if (b < P.B) scan_warp(P, b, lane, ws[warp]);
+}
+
+template <int DT, bool VEC, int SUB>
+static cudaError_t launch_masked_verify(const Params& P, cudaStream_t st) {
+  scan_kernel<<<(unsigned)((P.B + kStatsWarps - 1) / kStatsWarps), kStatsThreads, 0, st>>>(P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)((long long)P.B * P.np);
+  if constexpr (SUB == 256) {
+    draw_kernel<DT, VEC, SUB, true><<<grid, kThreads, 0, st>>>(P);
+    return cudaGetLastError();
+  }
+  draw_sum_kernel<DT, VEC, SUB, true><<<grid, kThreads, 0, st>>>(P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  draw_finish_kernel<DT, VEC, SUB, true><<<(unsigned)P.B, kThreads, 0, st>>>(P);
+  return cudaGetLastError();
+}
+
+template <int DT, bool VEC>
+static cudaError_t launch_topp_all(const Params& P, cudaStream_t st) {
+  cudaError_t e = launch_topp_cut<DT, VEC>(P, st);
+  if (e != cudaSuccess) return e;
+  return P.sub_elems == 512 ? launch_masked_verify<DT, VEC, 512>(P, st)
+                            : launch_masked_verify<DT, VEC, 256>(P, st);
+}
+
+cudaError_t launch_topp(Params P, bool aligned, cudaStream_t st) {
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   e = prepare_device(device);
   if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(P.ctrl, 0, P.ctrl_bytes, st);
+  if (e != cudaSuccess) return e;
+  P.fused = 0;
+  P.withhold = 0;
   if (P.dtype == 0)
-    return aligned ? launch_topp_kernels<0, true>(P, masked_target, masked_draft, st)
-                   : launch_topp_kernels<0, false>(P, masked_target, masked_draft, st);
-  return aligned ? launch_topp_kernels<1, true>(P, masked_target, masked_draft, st)
-                 : launch_topp_kernels<1, false>(P, masked_target, masked_draft, st);
+    return aligned ? launch_topp_all<0, true>(P, st) : launch_topp_all<0, false>(P, st);
+  return aligned ? launch_topp_all<1, true>(P, st) : launch_topp_all<1, false>(P, st);
 }
 
+#endif  // SV_TU_HAS(3)
+
+#if SV_TU_HAS(2)
 __global__ void fill_int_kernel(int* p, long long n, int v) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
@@ -2835,5 +3982,7 @@ cudaError_t launch_greedy(const Params& P, bool aligned, cudaStream_t st) {
   }
   return cudaGetLastError();
 }
+
+#endif  // SV_TU_HAS(2)
 
 }  // namespace sv

@@ -180,7 +180,10 @@ def test_topk_workspace_and_validation(lib):
 
 def test_topp_workspace_and_validation(lib):
     full = lib.sv_workspace_size(8, 4, 32000, sv.SV_BF16)
-    assert lib.sv_topp_workspace_size(8, 4, 32000, sv.SV_BF16) > full + 8 * 9 * 32000 * 2
+    assert lib.sv_topp_workspace_size(8, 4, 32000, sv.SV_BF16) >= full + 8 * 9 * 8
+    assert sv.sv_topp_kernels_per_call(8, 4, 32000, sv.SV_BF16) == 3
+    assert sv.sv_topp_kernels_per_call(256, 4, 256000, sv.SV_F32) == 4
+    assert sv.sv_topp_kernels_per_call(0, 4, 1000, sv.SV_F32) == 0
     for bad in ((-1, 4, 10, 0), (1, 0, 10, 0), (1, 65, 10, 0), (1, 4, 0, 0), (1, 4, 10, 7)):
         assert lib.sv_topp_workspace_size(*bad) == 0
     vp = ctypes.c_void_p

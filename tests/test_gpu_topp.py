@@ -196,3 +196,26 @@ def test_top_p_extremes(top_p, dt):
     mass (the cut deep in the tail, through the open last bins)."""
     w = _w(6, 3, 20011, dt, seed=int(top_p * 1000), std=1.5)
     parity(make_topp_inputs(w, top_p), top_p)
+
+
+@pytest.mark.parametrize("dt,V", [("bf16", 4099), ("f32", 4099), ("f32", 40000)])
+@pytest.mark.parametrize("top_p", [0.3, 0.7])
+def test_heavy_ties(dt, V, top_p):
+    """Two-valued rows: more than 1024 entries share the cut's value, so the
+    cut is resolved bit by bit over the key (across a cluster for the long
+    f32 rows)."""
+    g = torch.Generator().manual_seed(V + int(top_p * 10))
+    B, K = 3, 2
+    inp = make_inputs(_w(B, K, V, dt, seed=9))
+    inp["target"] = torch.randint(0, 2, (B, K + 1, V), generator=g).to(inp["target"].dtype)
+    inp["draft"] = torch.randint(0, 2, (B, K, V), generator=g).to(inp["draft"].dtype)
+    inp["tokens"] = torch.randint(0, V, (B, K), generator=g).to(torch.int32)
+    parity(inp, top_p)
+
+
+@pytest.mark.parametrize("dt,V", [("f32", 400_003), ("bf16", 800_000)])
+def test_rows_too_long_for_a_cluster(dt, V):
+    """Rows beyond sixteen CTAs' shared memory take the kernel that re-reads
+    the row from memory; the results are the same."""
+    w = _w(2, 1, V, dt, seed=V % 1000, std=1.5)
+    parity(make_topp_inputs(w, 0.9), 0.9)
