@@ -320,10 +320,10 @@ size_t sv_topp_workspace_size(int B, int K, int V, int dtype);
  *                fails (NaN, +inf or all -inf), which is left as it is
  * Per row, a cut is found without a sort: mass histograms over the scaled
  * distance (m - l) / T of each entry from the row maximum, at finer and finer
- * widths, locate the cut to a bin of at most 1024 entries, resolved exactly by
- * a radix select weighted by mass (a bin that never gets that small, from
- * heavy ties, is resolved bit by bit over the key). Rows up to 1.5 MB are held
- * in the shared memory of a thread-block cluster (up to 16 CTAs per row), so
+ * widths, locate the cut to a bin of at most 1024 entries, whose keys are then
+ * searched exactly with their masses (a bin that never gets that small, from
+ * heavy ties, is resolved bit by bit over the key). Rows up to 512 KB are held
+ * in the shared memory of a thread-block cluster (up to 8 CTAs per row), so
  * each row is read from memory once; longer rows are re-read per pass. Weights
  * are float-float exponentials. The cut also yields each row's kept mass, so
  * the verification (a scan kernel, then the draw) reads the rows unchanged

@@ -2910,7 +2910,7 @@ constexpr int kTcThreads = 256;
 constexpr int kTcWarps = kTcThreads / 32;
 constexpr int kTcCap = 1024;
 constexpr int kTcMaxLevels = 7;
-constexpr int kTcMaxCluster = 16;
+constexpr int kTcMaxCluster = 8;  // portable cluster sizes; longer rows take topp_cut_kernel
 
 struct TcShared {
   union {
@@ -2941,10 +2941,15 @@ struct TcShared {
   int open, state;
   float m;
   unsigned n_cand, n_above;  // the first CTA's counters of the gather pass
+  unsigned copied;
   unsigned long long bar;
 };
 
 constexpr size_t kTcSliceOffset = (sizeof(TcShared) + 127) / 128 * 128;
+// Two CTAs per SM (the 64 KB slice budget) need both CTAs' shared memory, with
+// the 1 KB each the driver reserves, within the SM's 228 KB.
+static_assert(2 * (kTcSliceOffset + (64u << 10) + 1024) <= 228u * 1024u,
+              "the nucleus cut kernel must fit two CTAs per SM");
 
 template <int DT>
 SV_DEVINL void tc_unpack(const uint4& q, float (&x)[DT == 0 ? 8 : 4]) {
@@ -3020,20 +3025,29 @@ __global__ void __launch_bounds__(kTcThreads, 2) topp_cluster_kernel(Params P, i
   sh.tab[tid] = kSvExp2Table[tid];
 #pragma unroll
   for (int i = 0; i < 4; ++i) sh.tab1k[tid + i * kTcThreads] = kSvExp2Table1024[tid + i * kTcThreads];
-  bool copied = true;
+  // One thread waits for the copy (with a backoff, so that the CTA sharing
+  // the SM keeps its issue slots); the barrier passes the completion on.
   if constexpr (VEC) {
-    if (!mbar_test_parity(bar, 0)) {
-      const uint64_t t0 = global_ns();
-      for (unsigned i = 1;; ++i) {
-        if (mbar_test_parity(bar, 0)) break;
-        if ((i & 255) == 0 && global_ns() - t0 > kWaitLimitNs) {
-          copied = false;
-          break;
+    if (tid == 0) {
+      unsigned ok = 1;
+      if (!mbar_test_parity(bar, 0)) {
+        const uint64_t t0 = global_ns();
+        unsigned ns = 32;
+        for (;;) {
+          __nanosleep(ns);
+          if (ns < 256) ns <<= 1;
+          if (mbar_test_parity(bar, 0)) break;
+          if (global_ns() - t0 > kWaitLimitNs) {
+            ok = 0;
+            break;
+          }
         }
       }
+      sh.copied = ok;
     }
   }
   __syncthreads();
+  const bool copied = VEC ? sh.copied != 0 : true;
 
   // ---- pass 0: the maximum (NaN-propagating; +inf is caught as well)
   float mx = neg_inf();
@@ -3230,8 +3244,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) topp_cluster_kernel(Params P, i
           w = exp_ff2(xs.hi, xs.lo, sh.tab);
         }
         const float2 D = f2_mul(f2_sub(mm2, l), cq2);
-        const int b0 = min(kTpBins - 1, __float2int_rz(D.x));
-        const int b1 = min(kTpBins - 1, __float2int_rz(D.y));
+        // floor(D) (D >= 0) as the low bits of D + 2^23 rounded toward zero:
+        // exact below 2^23, and at least 2^23 (clamped to the last bin) above.
+        const float2 Dz = f2_add_rz(D, f2(8388608.0f));
+        const int b0 = min(kTpBins - 1, __float_as_int(Dz.x) - 0x4b000000);
+        const int b1 = min(kTpBins - 1, __float_as_int(Dz.y) - 0x4b000000);
         tc_bin_add(sh, b0, w.hi.x, w.lo.x);
         tc_bin_add(sh, b1, w.hi.y, w.lo.y);
       }
@@ -3279,7 +3296,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) topp_cluster_kernel(Params P, i
         tc_unpack<DT>(sl4[v], x);
 #pragma unroll
         for (int j = 0; j < kEpv; ++j)
-          if (x[j] >= lo && x[j] <= hi && v * kEpv + j < n) cand |= 1u << j;
+          if (x[j] >= lo && x[j] <= hi && (VEC || v * kEpv + j < n)) cand |= 1u << j;
       }
       while (__any_sync(0xffffffffu, cand != 0)) {
         const bool has = cand != 0;
@@ -3346,11 +3363,23 @@ __global__ void __launch_bounds__(kTcThreads, 2) topp_cluster_kernel(Params P, i
 #pragma unroll
         for (int k = 0; k < kEpv; ++k) x[k] = neg_inf();
       }
+      // Entries above the window are counted at once; those inside it (rare)
+      // take the exact test, slot by slot, only when some lane has one.
+      unsigned win = 0;
+#pragma unroll
+      for (int j = 0; j < kEpv; ++j) {
+        const bool valid = v < nvec && (VEC || v * kEpv + j < n);
+        if (valid && x[j] > hi)
+          ++n_ab;
+        else if (valid && x[j] >= lo)
+          win |= 1u << j;
+      }
+      if (!__any_sync(0xffffffffu, win != 0)) continue;
 #pragma unroll
       for (int j = 0; j < kEpv; ++j) {
         const int e = v * kEpv + j;
         float d;
-        const int cls = (v < nvec && e < n) ? classify(x[j], d) : -1;
+        const int cls = ((win >> j) & 1u) ? classify(x[j], d) : -1;
         n_ab += cls > 0 ? 1u : 0u;
         const unsigned bal = __ballot_sync(0xffffffffu, cls == 0);
         if (bal) {
@@ -3822,20 +3851,21 @@ cudaError_t launch_topk(const Params& P, bool aligned, cudaStream_t st) {
 #endif  // SV_TU_HAS(2)
 
 #if SV_TU_HAS(3)
-// The nucleus cut's cluster shape for rows of `row_bytes`: CTAs per row and
-// elements per CTA, with a slice budget of 64 KB (two CTAs per SM) or, for
-// longer rows, 96 KB; nc = 0 when even that needs more than kTcMaxCluster.
+// The nucleus cut's cluster shape for rows of V elements of `es` bytes: CTAs
+// per row and elements per CTA, with a slice budget of 64 KB (two CTAs per
+// SM); nc = 0 for rows that would need more than kTcMaxCluster CTAs. (Longer
+// rows measured faster on the one-CTA-per-row kernel, which re-reads them
+// from L2 and memory: 4.06 ms against 7.16 ms with 16-CTA clusters for 2304
+// rows of 256000 f32.)
 static void topp_cluster_shape(long long V, int es, int* nc, int* slice_elems, size_t* smem) {
+  constexpr long long kBudget = 64ll << 10;
   *nc = 0;
-  for (long long budget : {64ll << 10, 96ll << 10}) {
-    const long long c = (V * es + budget - 1) / budget;
-    if (c > kTcMaxCluster) continue;
-    const long long se = ((V + c - 1) / c + 7) / 8 * 8;
-    *nc = (int)c;
-    *slice_elems = (int)se;
-    *smem = kTcSliceOffset + (size_t)((se * es + 127) / 128 * 128);
-    return;
-  }
+  const long long c = (V * es + kBudget - 1) / kBudget;
+  if (c > kTcMaxCluster) return;
+  const long long se = ((V + c - 1) / c + 7) / 8 * 8;
+  *nc = (int)c;
+  *slice_elems = (int)se;
+  *smem = kTcSliceOffset + (size_t)((se * es + 127) / 128 * 128);
 }
 
 // Whether clusters of `nc` CTAs with `smem` bytes each can be resident (the
@@ -3850,9 +3880,6 @@ static bool topp_cluster_ok(int nc, size_t smem, cudaLaunchConfig_t cfg) {
   if (it != known.end()) return it->second;
   bool ok = cudaFuncSetAttribute(topp_cluster_kernel<DT, VEC>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess;
-  if (ok && nc > 8)
-    ok = cudaFuncSetAttribute(topp_cluster_kernel<DT, VEC>,
-                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   int clusters = 0;
   if (ok) ok = cudaOccupancyMaxActiveClusters(&clusters, topp_cluster_kernel<DT, VEC>, &cfg) ==
                cudaSuccess && clusters > 0;

@@ -219,3 +219,11 @@ def test_rows_too_long_for_a_cluster(dt, V):
     the row from memory; the results are the same."""
     w = _w(2, 1, V, dt, seed=V % 1000, std=1.5)
     parity(make_topp_inputs(w, 0.9), 0.9)
+
+
+@pytest.mark.parametrize("dt,V", [("bf16", 262_000), ("f32", 131_000)])
+def test_eight_ctas_per_row(dt, V):
+    """Rows of 512 KB: the largest cluster, eight CTAs, each holding 64 KB."""
+    w = _w(2, 1, V, dt, seed=V % 997, std=1.5)
+    for top_p in (0.3, 0.95):
+        parity(make_topp_inputs(w, top_p), top_p)
