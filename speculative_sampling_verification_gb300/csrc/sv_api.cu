@@ -94,7 +94,6 @@ static void fill_params(sv::Params& P, const sv::Layout& L, int B, int K, int V,
   const double T = (double)temperature;
   const double inv = 1.0 / T;
   P.c2 = (float)(1.4426950408889634074 / T);
-  P.c2l = (float)(1.4426950408889634074 / T - (double)P.c2);
   P.ih = (float)inv;
   P.il = (float)(inv - (double)P.ih);
   P.unit_t = temperature == 1.0f ? 1 : 0;

@@ -165,16 +165,6 @@ SV_DEVINL float ex2_fast(float x) {
   return y;
 }
 
-// The draft-side sampler's weight exp(l/T) 2^-q0 without a table: the
-// exponent l log2(e)/T - q0, with log2(e)/T as the float-float (c2, c2l) and
-// rounded once, then ex2.approx (relative error below 2^-22). The exponent's
-// rounding adds 2^-24 |l log2(e)/T - q0| ln 2, below 1e-7 of the weight for the
-// entries within 2^-4 of the maximum and below 6e-7 for those within 2^-24.
-// Callers clamp l to at least -2048 T, where the result is 0.
-SV_DEVINL float exp_samp(float l, float q0f, float c2, float c2l) {
-  return ex2_fast(__fmaf_rn(l, c2l, __fmaf_rn(l, c2, -q0f)));
-}
-
 // ---------------------------------------------------------------- float-float arithmetic
 // A float-float value is hi + lo with |lo| small against |hi|. The error-free
 // transformations below use the _rn intrinsics so that the compiler neither

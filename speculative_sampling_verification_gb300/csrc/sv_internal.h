@@ -154,7 +154,6 @@ struct Params {
   const float* uniforms;
   int B, K, V, dtype, es;
   float c2;        // log2(e) / T in fp32 (streaming pass)
-  float c2l;       // log2(e) / T - c2 (the sampler's weights)
   float ih, il;    // 1/T as a float-float (sampling pass)
   float d_inv, d_ch, d_cli;  // the draw's fast reduction: 1024/(T ln2), fp32(T ln2/1024),
                              // the rest of T ln2/1024 over T

@@ -884,13 +884,9 @@ SV_DEVINL ff block_exclusive_ff(ff x, CtaShared& sh) {
 // weight before sub-chunk g is S_p * (A[0] + .. + A[g-1]) - S_q * (B[0] + ..
 // + B[g-1]) with S_p, S_q the row totals (at the end: R = S_p A - S_q B), for
 // the bonus draw (or the zero-residual fallback) it is S_q[0] + .. + S_q[g-1].
-// SAMP: the draft-side sampler's finish (a bonus draw whose sub-chunk sums
-// were taken with exp_samp against each sub-chunk's own shift, then rescaled
-// to the row's); `dbg_total`, if given, is the row's total with the precise
-// exponential, for the drawn token's exported probability.
-template <int DT, int SUB, bool MASK = false, bool SAMP = false>
+template <int DT, int SUB, bool MASK = false>
 SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShared& sh,
-                          bool aligned, const ff* dbg_total = nullptr) {
+                          bool aligned) {
   constexpr int kPer = SUB / kThreads;  // elements per thread in the exact search
   static_assert(kPer * kThreads == SUB, "sub-chunk must split evenly over the CTA");
   const int tid = threadIdx.x;
@@ -1032,15 +1028,6 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
     // with the chunk pass's own element weights (so that the search agrees
     // with the sub-chunk sums it starts from).
     const long long e0 = (long long)gs * SUB + kPer * tid;
-    float q0g = 0.0f, fscale = 0.0f;  // SAMP: the sub-chunk's shift, and 2^(q0_g - q0_row)
-    if constexpr (SAMP) {
-      const float mg = __ldcg(part + 2 * gs).z;
-      if (mg != neg_inf()) {
-        const int qg = row_q0(mg, P.c2), e = qg - row_q0(pl.m_q, P.c2);
-        q0g = (float)qg;
-        fscale = e < -126 ? 0.0f : __int_as_float((e + 127) << 23);
-      }
-    }
     ff w[kPer];
     ff wsum{0.f, 0.f};
 #pragma unroll
@@ -1051,9 +1038,7 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
         const float lq = ld_q(e);
         ff eq, ep;
         bool pos;
-        if (SAMP && d.fast) {
-          w[k] = {__fmul_rn(exp_samp(fmaxf(lq, d.lmin), q0g, P.c2, P.c2l), fscale), 0.f};
-        } else if (d.fast) {
+        if (d.fast) {
           const float lqc = fmaxf(lq, d.lmin);
           const ff fq = exp_draw(lqc, d.qb.x, d.dc, sh.tab1k);
           if (use_res) {
@@ -1116,7 +1101,7 @@ SV_DEVINL void finish_seq(const Params& P, long long b, const Plan& pl, CtaShare
             wt = pq;
           }
         }
-        P.dbg_prob[b] = ff_to_double(wt) / ff_to_double(dbg_total ? *dbg_total : total);
+        P.dbg_prob[b] = ff_to_double(wt) / ff_to_double(total);
       }
     }
     return true;
@@ -1336,13 +1321,8 @@ __global__ void __launch_bounds__(kThreads) draw_finish_kernel(Params P) {
 // One token per row drawn from softmax(l/T) in a single read of the row.
 // sample_sum_kernel: each warp loads its sub-chunk into registers, takes the
 // sub-chunk's own maximum m_g, and sums its weights exp(l/T) 2^-q0_g in
-// float-float, q0_g = floor(m_g log2(e)/T) + 1; it records (sum, m_g, flags).
-// The weights are exp_samp's (ex2.approx on an exponent rounded once, ~3e-7):
-// a draw from the normalised weights moves by at most about that much in
-// probability, inside the draw's parity margin, and the sampler has no
-// residual (a difference of nearly equal masses) that would magnify it. The
-// finish's search weighs its one sub-chunk with the same function and shift,
-// so it agrees with the sums exactly. sample_finish_kernel (one CTA per row): the row
+// float-float with the fast exponential, q0_g = floor(m_g log2(e)/T) + 1; it
+// records (sum, m_g, flags). sample_finish_kernel (one CTA per row): the row
 // maximum is the largest m_g; each sub-chunk sum times 2^(q0_g - q0_row) is an
 // exact power-of-two rescaling to the row's own shift, after which the
 // verifier's finish draws the token as its bonus draw does. A row whose
@@ -1355,7 +1335,11 @@ template <int DT, bool VEC, int SUB>
 __global__ void __launch_bounds__(kThreads, 5) sample_sum_kernel(Params P) {
   constexpr int kVec = 16 / (DT == 0 ? 2 : 4);
   constexpr int kRuns = SUB / (32 * kVec);
+  __shared__ float2 tab1k[1024];
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tab1k[tid + i * kThreads] = kSvExp2Table1024[tid + i * kThreads];
+  __syncthreads();
   const long long r = blockIdx.x / P.np;
   const int c = (int)(blockIdx.x % P.np);
   const long long e0 = ((long long)c * kSubPerChunk + w) * SUB;
@@ -1386,13 +1370,19 @@ __global__ void __launch_bounds__(kThreads, 5) sample_sum_kernel(Params P) {
   if (!bad && mx != neg_inf()) {
     const float cm = mx * P.c2;
     if (fabsf(cm) <= 2000.0f) {
-      const float q0f = (float)row_q0(mx, P.c2);
+      const int q0 = row_q0(mx, P.c2);
+      const int2 qb = make_int2(127 - q0, 127 - q0);
+      const DrawConst dc{P.d_inv, P.d_ch, P.d_cli, P.ih};
       const float lmin = -2048.0f * __fdividef(1.0f, P.ih);
 #pragma unroll
       for (int k = 0; k < kRuns; ++k) {
 #pragma unroll
-        for (int j = 0; j < kVec; ++j)
-          ff_accumulate_biased(S, {exp_samp(fmaxf(x[k][j], lmin), q0f, P.c2, P.c2l), 0.0f});
+        for (int j = 0; j < kVec; j += 2) {
+          const float2 l = make_float2(fmaxf(x[k][j], lmin), fmaxf(x[k][j + 1], lmin));
+          const ff2 ex = exp_draw2(l, qb, dc, tab1k);
+          ff_accumulate_biased(S, {ex.hi.x, ex.lo.x});
+          ff_accumulate_biased(S, {ex.hi.y, ex.lo.y});
+        }
       }
     } else {
       flags |= kSubExtreme;
@@ -1488,7 +1478,7 @@ __global__ void __launch_bounds__(kThreads) sample_finish_kernel(Params P) {
         const int e = row_q0(rec.z, P.c2) - q0r;  // <= 0
         f = e < -126 ? 0.0f : __int_as_float((e + 127) << 23);
       }
-      part[2 * g] = make_float4(rec.x * f, rec.y * f, rec.z, 0.f);  // m_g kept for the search
+      part[2 * g] = make_float4(rec.x * f, rec.y * f, 0.f, 0.f);
     }
     lse_scale = (double)q0r * 0.69314718055994530942;
   }
@@ -1510,31 +1500,7 @@ __global__ void __launch_bounds__(kThreads) sample_finish_kernel(Params P) {
       P.dbg_lse[r] = lse_scale + log(ff_to_double(tot));
     }
   }
-  // The row's total with the precise exponential, for the drawn token's
-  // exported probability (debug calls only; the draw itself uses the sums).
-  __shared__ ff s_ptot;
-  const bool extreme = (flags & kSubExtreme) || fabsf(cm) > 2000.0f;
-  if (P.dbg_prob && !extreme) {
-    const unsigned char* rowp = static_cast<const unsigned char*>(P.target) + (size_t)r * P.V * P.es;
-    const int qb = 127 - row_q0(m, P.c2);
-    const float lmin = -2048.0f * __fdividef(1.0f, P.ih);
-    ff t{0.f, 0.f};
-    for (long long e = tid; e < P.V; e += kThreads)
-      t = ff_add(t, ff_normalize(exp_precise(fmaxf(load_elem<DT>(rowp, e), lmin), qb, P.ih, P.il,
-                                             sh.tab)));
-    t = ff_warp_sum(t);
-    __syncthreads();
-    if (lane == 0) sh.red4[w][0] = t;
-    __syncthreads();
-    if (tid == 0) {
-      ff tot{0.f, 0.f};
-      for (int i = 0; i < kWarps; ++i) tot = ff_add(tot, sh.red4[i][0]);
-      s_ptot = tot;
-    }
-    __syncthreads();
-  }
-  finish_seq<DT, SUB, false, true>(P, r, pl, sh, VEC,
-                                   (P.dbg_prob && !extreme) ? &s_ptot : nullptr);
+  finish_seq<DT, SUB>(P, r, pl, sh, VEC);
 }
 
 // ---------------------------------------------------------------- the fused kernel
