@@ -63,10 +63,6 @@ SV_DEVINL void mbar_arrive_expect_tx(unsigned bar, unsigned bytes) {
                : "memory");
 }
 
-SV_DEVINL void mbar_arrive(unsigned bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 SV_DEVINL bool mbar_test_parity(unsigned bar, unsigned parity) {
   unsigned ok;
   asm volatile(
@@ -118,32 +114,14 @@ SV_DEVINL unsigned dsmem_map(unsigned addr, unsigned rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-SV_DEVINL float dsmem_ld_f32(unsigned a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-SV_DEVINL unsigned dsmem_ld_u32(unsigned a) {
-  unsigned v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
 SV_DEVINL void dsmem_st_u64(unsigned a, unsigned long long v) {
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
-}
-SV_DEVINL void dsmem_st_u32(unsigned a, unsigned v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 SV_DEVINL void dsmem_st_f32(unsigned a, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
 }
 SV_DEVINL void dsmem_st_f32x2(unsigned a, float x, float y) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
-}
-SV_DEVINL unsigned dsmem_atomic_add_u32(unsigned a, unsigned v) {
-  unsigned old;
-  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
-  return old;
 }
 
 // ---------------------------------------------------------------- bf16 and fast fp32 helpers
