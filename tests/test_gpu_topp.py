@@ -227,3 +227,12 @@ def test_eight_ctas_per_row(dt, V):
     w = _w(2, 1, V, dt, seed=V % 997, std=1.5)
     for top_p in (0.3, 0.95):
         parity(make_topp_inputs(w, top_p), top_p)
+
+
+@pytest.mark.parametrize("dt,V", [("f32", 40000), ("bf16", 100003)])
+def test_misaligned_rows_on_a_cluster(dt, V):
+    """Rows that are not 16-byte aligned take element loads into the cluster's
+    shared memory (padded with -inf), here over two CTAs or more."""
+    w = _w(3, 2, V, dt, seed=V % 991, std=2.0)
+    for top_p in (0.5, 0.97):
+        parity(make_topp_inputs(w, top_p), top_p, misalign=True)
