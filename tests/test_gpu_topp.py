@@ -198,19 +198,21 @@ def test_top_p_extremes(top_p, dt):
     parity(make_topp_inputs(w, top_p), top_p)
 
 
-@pytest.mark.parametrize("dt,V", [("bf16", 4099), ("f32", 4099), ("f32", 40000)])
+@pytest.mark.parametrize("dt,V,misalign", [("bf16", 4099, False), ("f32", 4099, False),
+                                           ("f32", 40000, False), ("bf16", 140000, False),
+                                           ("f32", 40000, True)])
 @pytest.mark.parametrize("top_p", [0.3, 0.7])
-def test_heavy_ties(dt, V, top_p):
+def test_heavy_ties(dt, V, misalign, top_p):
     """Two-valued rows: more than 1024 entries share the cut's value, so the
     cut is resolved bit by bit over the key (across a cluster for the long
-    f32 rows)."""
+    rows, and with element loads for misaligned ones)."""
     g = torch.Generator().manual_seed(V + int(top_p * 10))
     B, K = 3, 2
     inp = make_inputs(_w(B, K, V, dt, seed=9))
     inp["target"] = torch.randint(0, 2, (B, K + 1, V), generator=g).to(inp["target"].dtype)
     inp["draft"] = torch.randint(0, 2, (B, K, V), generator=g).to(inp["draft"].dtype)
     inp["tokens"] = torch.randint(0, V, (B, K), generator=g).to(torch.int32)
-    parity(inp, top_p)
+    parity(inp, top_p, misalign=misalign)
 
 
 @pytest.mark.parametrize("dt,V", [("f32", 400_003), ("bf16", 800_000)])
