@@ -2,6 +2,7 @@
 
     python -m tests.parity_at_scale [--configs c2,c3,c4,sweep] [--min-decisions 100000]
                                     [--min-decisions-cell 10000] [--out FILE]
+                                    [--op verify|topk|topp] [--top-k 50] [--top-p 0.9]
 
 For every workload, steps are drawn on the GPU by the batched seeded
 generator, verified there through the C ABI (spec_verify_debug, whole batch),
@@ -9,6 +10,13 @@ and every sequence of every step is verified again by the fp64 oracle on the
 host cores (a spawn pool, one process per core, fed through .npy files). Steps
 are added until the oracle has taken at least --min-decisions decisions (for
 each of the 20 cells of the acceptance sweep, --min-decisions-cell).
+
+With --op topk or topp the filtered verification (spec_verify_topk /
+spec_verify_topp) is checked against verify_topk / verify_topp the same way;
+for the nucleus, a row whose kept count differs from the oracle's is allowed
+only where top_p lies within 1e-9 of the oracle's cumulative sums at its cut
+(`cut_excused_rows`; their sequences' decisions are not compared), as in the
+GPU tests. These paths export no intermediates.
 
 Per workload the record holds the sequences and decisions checked, the
 decisions whose uniform lies within 1e-6 of the oracle's threshold
@@ -57,12 +65,25 @@ def _load(paths):
             np.asarray(u))
 
 
+CUT_MARGIN = 1e-9
+
+
 def oracle_job(job):
     """The fp64 oracle over the sequences stored in `paths` (a worker process)."""
     import oracle
 
-    paths, temperature = job
+    paths, temperature, op, param = job
+    if op == "topk":
+        return oracle.verify_topk(*_load(paths), temperature, param)
+    if op == "topp":
+        return oracle.verify_topp(*_load(paths), temperature, param)
     return oracle.verify(*_load(paths), temperature)
+
+
+def _subset(res, rows):
+    import dataclasses
+
+    return type(res)(*[getattr(res, f.name)[rows] for f in dataclasses.fields(res)])
 
 
 # ---------------------------------------------------------------- GPU side
@@ -122,15 +143,16 @@ class Intermediates:
 
 
 def check_workload(sv, w, dev, pool, workers, tmp, min_decisions, max_steps=100_000,
-                   step_base=7000, depth=None, log=print):
-    """Whole-batch parity of workload `w`: returns its record."""
+                   step_base=7000, depth=None, log=print, op="verify", param=None):
+    """Whole-batch parity of workload `w` (for `op`): returns its record."""
     import torch
 
     from synthetic import make_batch
 
     B, K, V = w.B, w.K, w.V
     dt = sv.SV_BF16 if w.dtype == "bf16" else sv.SV_F32
-    ws = sv.new_workspace(B, K, V, dt, dev)
+    ws = sv.new_workspace(B, K, V, dt, dev) if op == "verify" else None
+    cut_rows = cut_bad = 0
     per_seq = (2 * K + 1) * V * 25e-9
     per = max(1, min(B, int(0.25 / per_seq)))
     chunks = [list(range(s, min(B, s + per))) for s in range(0, B, per)]
@@ -144,12 +166,23 @@ def check_workload(sv, w, dev, pool, workers, tmp, min_decisions, max_steps=100_
     t0 = time.time()
 
     def settle(item):
-        nonlocal need_steps
+        nonlocal need_steps, cut_rows, cut_bad
         s, jobs, out, nacc, tokens, dbg, files = item
         for seqs, res in jobs:
             ref = res.get()
-            rep.add(_parity.compare(out[seqs], nacc[seqs], ref, tokens[seqs]))
-            inter.add(dbg, ref, seqs)
+            if op == "topp":
+                kept = dbg["kept"][seqs]
+                mism = kept != ref.kept
+                cut_rows += int(mism.sum())
+                cut_bad += int(np.sum(mism & ~(ref.cut_margin < CUT_MARGIN)))
+                ok = ~mism.any(axis=1)
+                sub = np.asarray(seqs)[ok]
+                rep.add(_parity.compare(out[sub], nacc[sub], _subset(ref.result, ok), tokens[sub]))
+            elif op == "topk":
+                rep.add(_parity.compare(out[seqs], nacc[seqs], ref, tokens[seqs]))
+            else:
+                rep.add(_parity.compare(out[seqs], nacc[seqs], ref, tokens[seqs]))
+                inter.add(dbg, ref, seqs)
         for f in files:
             try:
                 os.remove(f)
@@ -169,11 +202,20 @@ def check_workload(sv, w, dev, pool, workers, tmp, min_decisions, max_steps=100_
             need_steps = min(max_steps, step + int(np.ceil(
                 1.1 * (min_decisions - rep.decisions) * step / max(1, rep.decisions))) + 1)
         inp = make_batch(w, step=step_base + step, device=dev)
-        out, nacc, dbg = sv.verify(inp["target"], inp["draft"], inp["tokens"], inp["uniforms"],
-                                   inp["temperature"], workspace=ws, debug=True)
+        args = (inp["target"], inp["draft"], inp["tokens"], inp["uniforms"], inp["temperature"])
+        if op == "topk":
+            out, nacc = sv.verify_topk(*args, param)
+            dbg_np = {}
+        elif op == "topp":
+            out, nacc, kept = sv.verify_topp(*args, param)
+            dbg_np = {"kept": kept.cpu().numpy()}
+        else:
+            out, nacc, dbg = sv.verify(*args, workspace=ws, debug=True)
+            dbg_np = {k: v.cpu().numpy() for k, v in dbg.items() if k != "workspace"}
+            del dbg
         torch.cuda.synchronize()
-        statuses |= sv.sv_read_device_status(ws)
-        dbg_np = {k: v.cpu().numpy() for k, v in dbg.items() if k != "workspace"}
+        if ws is not None:
+            statuses |= sv.sv_read_device_status(ws)
         files, jobs = [], []
         for ci, seqs in enumerate(chunks):
             idx = torch.as_tensor(seqs, device=dev)
@@ -183,21 +225,27 @@ def check_workload(sv, w, dev, pool, workers, tmp, min_decisions, max_steps=100_
                 np.save(p, _to_np(inp[k].index_select(0, idx)))
                 paths.append(p)
             files += paths
-            jobs.append((seqs, pool.apply_async(oracle_job, ((paths, inp["temperature"]),))))
+            jobs.append((seqs, pool.apply_async(oracle_job,
+                                                ((paths, inp["temperature"], op, param),))))
         pending.append((step_base + step, jobs, out.cpu().numpy(), nacc.cpu().numpy(),
                         inp["tokens"].cpu().numpy(), dbg_np, files))
-        del inp, out, nacc, dbg
+        del inp, out, nacc
         step += 1
         while pending and (len(pending) > depth or all(r.ready() for _, r in pending[0][1])):
             settle(pending.popleft())
     dt = time.time() - t0
     d = rep.as_dict()
-    d.update({"workload": w.name, "steps": step, "device_status": statuses,
+    d.update({"workload": w.name, "op": op, "steps": step, "device_status": statuses,
               "excused_rate": rep.excused / max(1, rep.decisions),
-              "intermediates": inter.as_dict(), "seconds": round(dt, 1),
-              "failures": [str(f)[:300] for f in rep.failures[:5]]})
+              "intermediates": inter.as_dict() if op == "verify" else None,
+              "seconds": round(dt, 1), "failures": [str(f)[:300] for f in rep.failures[:5]]})
+    if op == "topk":
+        d["top_k"] = param
+    if op == "topp":
+        d.update({"top_p": param, "cut_excused_rows": cut_rows - cut_bad,
+                  "cut_unexcused_rows": cut_bad})
     d["pass"] = (not rep.failures and statuses == 0 and rep.excused <= MAX_EXCUSED_RATE
-                 * rep.decisions and not any(inter.over.values()))
+                 * rep.decisions and not any(inter.over.values()) and cut_bad == 0)
     log(json.dumps({k: d[k] for k in ("workload", "steps", "sequences", "decisions",
                                       "near_threshold", "excused_differences",
                                       "unexcused_differences", "seconds", "pass")}))
@@ -220,7 +268,7 @@ def workload_list(configs: str):
 
 
 def run(configs="c2,c3,c4,sweep", min_decisions=100_000, min_decisions_cell=10_000,
-        workers=None, out=None, log=print):
+        workers=None, out=None, log=print, op="verify", top_k=50, top_p=0.9):
     import multiprocessing as mp
 
     workers = workers or max(1, len(os.sched_getaffinity(0)) - 1)
@@ -237,7 +285,8 @@ def run(configs="c2,c3,c4,sweep", min_decisions=100_000, min_decisions_cell=10_0
         for w, cell in workload_list(configs):
             records.append(check_workload(sv, w, dev, pool, workers, tmp,
                                           min_decisions_cell if cell else min_decisions,
-                                          log=log))
+                                          log=log, op=op,
+                                          param={"topk": top_k, "topp": top_p}.get(op)))
     finally:
         pool.terminate()
         pool.join()
@@ -249,7 +298,7 @@ def run(configs="c2,c3,c4,sweep", min_decisions=100_000, min_decisions_cell=10_0
     totals = tot.as_dict()
     totals["unexcused_differences"] = sum(r["unexcused_differences"] for r in records)
     totals["excused_rate"] = tot.excused / max(1, tot.decisions)
-    summary = {"when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()),
+    summary = {"when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()), "op": op,
                "command": "python -m tests.parity_at_scale " + " ".join(sys.argv[1:]),
                "margin": _parity.MARGIN, "max_excused_rate": MAX_EXCUSED_RATE,
                "oracle_workers": workers, "totals": totals,
@@ -267,8 +316,12 @@ def main():
     ap.add_argument("--min-decisions-cell", type=int, default=10_000)
     ap.add_argument("--workers", type=int, default=None)
     ap.add_argument("--out", default=None)
+    ap.add_argument("--op", choices=["verify", "topk", "topp"], default="verify")
+    ap.add_argument("--top-k", type=int, default=50)
+    ap.add_argument("--top-p", type=float, default=0.9)
     a = ap.parse_args()
-    s = run(a.configs, a.min_decisions, a.min_decisions_cell, a.workers, a.out)
+    s = run(a.configs, a.min_decisions, a.min_decisions_cell, a.workers, a.out, op=a.op,
+            top_k=a.top_k, top_p=a.top_p)
     print(json.dumps({"pass": s["pass"], "totals": s["totals"]}))
     sys.exit(0 if s["pass"] else 1)
 

@@ -24,3 +24,17 @@ def test_whole_batches_match_the_oracle():
     # the excused-difference bar over all decisions (one allowed below 1e5 decisions)
     assert t["excused_differences"] <= max(1, parity_at_scale.MAX_EXCUSED_RATE
                                            * t["decisions"]), t
+
+
+@pytest.mark.parametrize("op", ["topk", "topp"])
+def test_filtered_whole_batches_match_the_oracle(op):
+    """The filtered verifications over whole batches of the 8x4x32000 workload."""
+    s = parity_at_scale.run("c2", min_decisions=2000, op=op)
+    for r in s["workloads"]:
+        assert r["unexcused_differences"] == 0, r
+        assert r["decisions"] >= 2000, r
+        if op == "topp":
+            assert r["cut_unexcused_rows"] == 0, r
+    t = s["totals"]
+    assert t["excused_differences"] <= max(1, parity_at_scale.MAX_EXCUSED_RATE
+                                           * t["decisions"]), t
