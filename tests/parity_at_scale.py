@@ -2,7 +2,8 @@
 
     python -m tests.parity_at_scale [--configs c2,c3,c4,sweep] [--min-decisions 100000]
                                     [--min-decisions-cell 10000] [--out FILE]
-                                    [--op verify|topk|topp] [--top-k 50] [--top-p 0.9]
+                                    [--op verify|topk|topp|greedy|sample] [--top-k 50]
+                                    [--top-p 0.9]
 
 For every workload, steps are drawn on the GPU by the batched seeded
 generator, verified there through the C ABI (spec_verify_debug, whole batch),
@@ -16,7 +17,11 @@ spec_verify_topp) is checked against verify_topk / verify_topp the same way;
 for the nucleus, a row whose kept count differs from the oracle's is allowed
 only where top_p lies within 1e-9 of the oracle's cumulative sums at its cut
 (`cut_excused_rows`; their sequences' decisions are not compared), as in the
-GPU tests. These paths export no intermediates.
+GPU tests. With --op greedy, greedy verification must match verify_greedy
+exactly (its decisions are integer comparisons). With --op sample, the draft
+sampler draws one token per draft row (the uniforms of the first K draws of
+each sequence) and is held to the verification draw's margin rule against
+draft_sample. These paths export no intermediates.
 
 Per workload the record holds the sequences and decisions checked, the
 decisions whose uniform lies within 1e-6 of the oracle's threshold
@@ -77,7 +82,44 @@ def oracle_job(job):
         return oracle.verify_topk(*_load(paths), temperature, param)
     if op == "topp":
         return oracle.verify_topp(*_load(paths), temperature, param)
+    if op == "greedy":
+        t, _, k, _ = _load(paths)
+        return oracle.verify_greedy(t, k)
+    if op == "sample":
+        _, d, _, u = _load(paths)
+        n, K, V = d.shape
+        return oracle.draft_sample(d.reshape(n * K, V), np.ascontiguousarray(u[:, :K]).reshape(-1),
+                                   temperature)
     return oracle.verify(*_load(paths), temperature)
+
+
+def compare_greedy(out, nacc, ref) -> _parity.ParityReport:
+    """Greedy verification: the outputs must be identical (each decision is an
+    exact comparison of integer argmaxes)."""
+    out, nacc = np.asarray(out).astype(np.int64), np.asarray(nacc).astype(np.int64)
+    ok = ref.status == 0
+    rep = _parity.ParityReport(sequences=len(nacc),
+                               decisions=int(np.sum(ref.n_accepted[ok] + 1)))
+    for b in np.nonzero((out != ref.out_tokens).any(axis=1) | (nacc != ref.n_accepted))[0]:
+        rep.failures.append((int(b), "greedy", out[b].tolist(), ref.out_tokens[b].tolist()))
+    return rep
+
+
+def compare_sample(tokens, ref) -> _parity.ParityReport:
+    """Draft sampling: one draw per row, the margin rule of the verification's
+    draw (a differing token is tolerated only within MARGIN of its CDF ends)."""
+    tokens = np.asarray(tokens).astype(np.int64).reshape(-1)
+    ok = ref.status == 0
+    rep = _parity.ParityReport(sequences=len(tokens), decisions=int(ok.sum()))
+    rep.near_threshold = int(np.sum(ref.sample_margin[ok] < _parity.MARGIN))
+    bad = (~ok) & (tokens != -1)
+    diff = ok & (tokens != ref.tokens)
+    excused = diff & (ref.sample_margin < _parity.MARGIN)
+    rep.excused = int(excused.sum())
+    for i in np.nonzero(bad | (diff & ~excused))[0][:50]:
+        rep.failures.append((int(i), "draw", int(tokens[i]), int(ref.tokens[i]),
+                             float(ref.sample_margin[i])))
+    return rep
 
 
 def _subset(res, rows):
@@ -180,6 +222,10 @@ def check_workload(sv, w, dev, pool, workers, tmp, min_decisions, max_steps=100_
                 rep.add(_parity.compare(out[sub], nacc[sub], _subset(ref.result, ok), tokens[sub]))
             elif op == "topk":
                 rep.add(_parity.compare(out[seqs], nacc[seqs], ref, tokens[seqs]))
+            elif op == "greedy":
+                rep.add(compare_greedy(out[seqs], nacc[seqs], ref))
+            elif op == "sample":
+                rep.add(compare_sample(out[seqs], ref))
             else:
                 rep.add(_parity.compare(out[seqs], nacc[seqs], ref, tokens[seqs]))
                 inter.add(dbg, ref, seqs)
@@ -209,6 +255,14 @@ def check_workload(sv, w, dev, pool, workers, tmp, min_decisions, max_steps=100_
         elif op == "topp":
             out, nacc, kept = sv.verify_topp(*args, param)
             dbg_np = {"kept": kept.cpu().numpy()}
+        elif op == "greedy":
+            out, nacc = sv.verify_greedy(inp["target"], inp["tokens"])
+            dbg_np = {}
+        elif op == "sample":
+            u = inp["uniforms"][:, :K].contiguous().reshape(-1)
+            tok = sv.draft_sample(inp["draft"].reshape(B * K, V), u, inp["temperature"])
+            out, nacc = tok.reshape(B, K), torch.zeros(B, dtype=torch.int32, device=dev)
+            dbg_np = {}
         else:
             out, nacc, dbg = sv.verify(*args, workspace=ws, debug=True)
             dbg_np = {k: v.cpu().numpy() for k, v in dbg.items() if k != "workspace"}
@@ -316,7 +370,8 @@ def main():
     ap.add_argument("--min-decisions-cell", type=int, default=10_000)
     ap.add_argument("--workers", type=int, default=None)
     ap.add_argument("--out", default=None)
-    ap.add_argument("--op", choices=["verify", "topk", "topp"], default="verify")
+    ap.add_argument("--op", choices=["verify", "topk", "topp", "greedy", "sample"],
+                    default="verify")
     ap.add_argument("--top-k", type=int, default=50)
     ap.add_argument("--top-p", type=float, default=0.9)
     a = ap.parse_args()
