@@ -26,9 +26,10 @@ def test_whole_batches_match_the_oracle():
                                            * t["decisions"]), t
 
 
-@pytest.mark.parametrize("op", ["topk", "topp"])
-def test_filtered_whole_batches_match_the_oracle(op):
-    """The filtered verifications over whole batches of the 8x4x32000 workload."""
+@pytest.mark.parametrize("op", ["topk", "topp", "greedy", "sample"])
+def test_other_paths_over_whole_batches_match_the_oracle(op):
+    """The filtered verifications, greedy mode and the draft sampler over whole
+    batches of the 8x4x32000 workload."""
     s = parity_at_scale.run("c2", min_decisions=2000, op=op)
     for r in s["workloads"]:
         assert r["unexcused_differences"] == 0, r
